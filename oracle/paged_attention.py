@@ -1,0 +1,160 @@
+"""CPU oracle for batched paged-KV decode attention and slot-mapped KV append.
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the product path may import or call
+this module: only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline
+leg of ``bench.py`` use it.  It shares no code with the CUDA library and it
+imports nothing from the package; it receives plain numpy arrays.
+
+It is the plain definition written out, in float64, with no blocking, fusion
+or reordering (split-K and online softmax are ways to reach the same result,
+so they do not appear here):
+
+* Gather.  For sequence ``s`` and KV head ``g`` the context is the rows
+  ``K_s[i] = k_cache[block_tables[s, i // bs], g, i % bs, :]`` for
+  ``0 <= i < context_lens[s]``; the same for V.  (ferrum-kernels
+  ``src/backend/cuda/paged.rs``, ``paged_decode_attention``: a sequence's
+  tokens live in blocks of ``block_size`` reached through its row of the block
+  table, ``max_kv_len = block_size * max_num_blocks_per_seq``; kapsl-backends
+  ``src/gguf_native.rs``, ``forward_batch_decode_greedy``: ``context_lens[b]``
+  is the length *after* this step's token.)
+* GQA.  Query head ``h`` reads KV head ``h // (H / Hkv)`` (cortiq-engine
+  ``src/gpu_cuda.rs``, plan construction ``hpk = nh / nkv`` and the parity test
+  that hands query rows ``g*hpk .. (g+1)*hpk`` to KV head ``g``).
+* Scores ``z_i = scale * q . K_s[i]``; ``scale`` is an argument (kapsl
+  ``one_token_compute`` passes ``scale = 1/sqrt(head_dim)``).
+* Softmax ``p_i = exp(z_i - max z) / sum_j exp(z_j - max z)`` and output
+  ``sum_i p_i V_s[i]``.
+* ``context_len == 0`` gives zeros (an empty softmax has no value; zeros are
+  the plainest total definition).
+* Append.  Token ``t`` with ``slot = slot_mapping[t] >= 0`` is written to
+  block ``slot // bs``, row ``slot % bs`` of both pools, for every KV head;
+  negative slots are skipped (kapsl ``launch_batch_kv_write`` with a
+  physical block and position-in-block per token, as one integer).
+
+Parity pins (in ``tests/test_oracle_pins.py``): contiguous equivalence against
+``torch.nn.functional.scaled_dot_product_attention`` in float64, invariance
+under a permutation of physical blocks, ``context_len == 1`` returning that V
+row exactly, identical keys (or ``scale == 0``) returning the mean of V, GQA
+equal to MHA with repeated KV heads, a hand-derived worked example under
+``tests/golden/``, and planted mistakes that each of those must catch.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+
+class OracleInputError(ValueError):
+    """The inputs break a precondition the definition needs."""
+
+
+def kv_head_of(h: int, group: int) -> int:
+    """KV head read by query head ``h``: consecutive query heads share one."""
+    return h // group
+
+
+def gather_rows(cache: np.ndarray, table_row: np.ndarray, context_len: int,
+                kv_head: int) -> np.ndarray:
+    """Rows ``0 .. context_len-1`` of one sequence and KV head, as float64."""
+    bs = cache.shape[2]
+    i = np.arange(context_len)
+    blocks = table_row[i // bs]
+    return cache[blocks, kv_head, i % bs, :].astype(np.float64)
+
+
+def softmax(z: np.ndarray) -> np.ndarray:
+    """Softmax along the last axis, shifted by its max before ``exp``."""
+    e = np.exp(z - z.max(axis=-1, keepdims=True))
+    return e / e.sum(axis=-1, keepdims=True)
+
+
+def _check_tables(block_tables, context_lens, num_blocks, block_size):
+    B, mbps = block_tables.shape
+    for s in range(B):
+        L = int(context_lens[s])
+        if L < 0 or L > mbps * block_size:
+            raise OracleInputError(f"context_lens[{s}]={L} outside [0, {mbps * block_size}]")
+        n = -(-L // block_size)
+        ids = block_tables[s, :n]
+        if n and (ids.min() < 0 or ids.max() >= num_blocks):
+            raise OracleInputError(f"block id out of range in sequence {s}")
+
+
+def decode(q, k_cache, v_cache, block_tables, context_lens, scale, seqs=None):
+    """Attention of one query token per sequence over its paged context.
+
+    Arguments are numpy arrays: ``q`` f16 ``[B][H][D]``, caches f16
+    ``[NB][Hkv][bs][D]``, ``block_tables`` int ``[B][MBPS]``, ``context_lens``
+    int ``[B]``.  Returns float64 ``[B][H][D]``; with ``seqs`` only those
+    sequences are computed (the other rows stay zero).
+    """
+    q = np.asarray(q)
+    B, H, D = q.shape
+    NB, Hkv, bs, Dk = k_cache.shape
+    if Dk != D or v_cache.shape != k_cache.shape:
+        raise OracleInputError("cache shape does not match q")
+    if H % Hkv:
+        raise OracleInputError("num_heads must be a multiple of num_kv_heads")
+    group = H // Hkv
+    _check_tables(block_tables, context_lens, NB, bs)
+    out = np.zeros((B, H, D), np.float64)
+    for s in (range(B) if seqs is None else seqs):
+        L = int(context_lens[s])
+        if L == 0:
+            continue
+        row = block_tables[s]
+        for h in range(H):
+            g = kv_head_of(h, group)
+            K = gather_rows(k_cache, row, L, g)
+            V = gather_rows(v_cache, row, L, g)
+            z = scale * (K @ q[s, h].astype(np.float64))
+            p = softmax(z)
+            out[s, h] = p @ V
+    return out
+
+
+def decode_fast(q, k_cache, v_cache, block_tables, context_lens, scale, seqs=None):
+    """Same definition as :func:`decode`, gathering each (sequence, KV head)
+    once and scoring its whole query group with one matrix product.
+
+    Used where the contexts are long (the gather dominates); the arithmetic
+    per output element is the same sums in float64.
+    """
+    q = np.asarray(q)
+    B, H, D = q.shape
+    NB, Hkv, bs, _ = k_cache.shape
+    if H % Hkv:
+        raise OracleInputError("num_heads must be a multiple of num_kv_heads")
+    group = H // Hkv
+    _check_tables(block_tables, context_lens, NB, bs)
+    out = np.zeros((B, H, D), np.float64)
+    for s in (range(B) if seqs is None else seqs):
+        L = int(context_lens[s])
+        if L == 0:
+            continue
+        row = block_tables[s]
+        for g in range(Hkv):
+            heads = [h for h in range(H) if kv_head_of(h, group) == g]
+            K = gather_rows(k_cache, row, L, g)
+            V = gather_rows(v_cache, row, L, g)
+            Z = scale * (q[s, heads].astype(np.float64) @ K.T)  # [G][L]
+            P = softmax(Z)
+            out[s, heads] = P @ V
+    return out
+
+
+def append(k, v, slot_mapping, k_cache, v_cache):
+    """Scatter new K/V rows into the pools in place; returns the skipped
+    out-of-range token indices (slots ``>= num_blocks * block_size``)."""
+    NB, Hkv, bs, D = k_cache.shape
+    bad = []
+    for t, slot in enumerate(np.asarray(slot_mapping).tolist()):
+        if slot < 0:
+            continue
+        if slot >= NB * bs:
+            bad.append(t)
+            continue
+        blk, off = divmod(slot, bs)
+        k_cache[blk, :, off, :] = k[t]
+        v_cache[blk, :, off, :] = v[t]
+    return bad

@@ -1,0 +1,85 @@
+"""The seeded input generator: determinism and the structure of each workload."""
+
+import numpy as np
+import pytest
+
+from paged_kv_decode_08_gb300 import workloads as W
+
+
+def _digest(w):
+    import hashlib
+
+    h = hashlib.sha256()
+    for a in [w.context_lens, w.block_tables, w.q] + w.seq_k + w.seq_v:
+        h.update(np.ascontiguousarray(a).tobytes())
+    return h.hexdigest()
+
+
+def test_same_seed_same_bytes():
+    assert _digest(W.tiny()) == _digest(W.tiny())
+    a = W.small_random(3, 2, 4, 2, 64, 16, [5, 40])
+    b = W.small_random(3, 2, 4, 2, 64, 16, [5, 40])
+    assert _digest(a) == _digest(b)
+
+
+def _check_structure(w):
+    B, mbps = w.block_tables.shape
+    assert B == w.num_seqs and mbps == w.max_blocks_per_seq
+    used = np.concatenate([w.blocks_of(s) for s in range(B)])
+    assert len(np.unique(used)) == len(used), "a block is shared between positions"
+    assert used.min() >= 0 and used.max() < w.num_blocks
+    assert w.poison_block not in set(used.tolist())
+    for s in range(B):
+        n = len(w.blocks_of(s))
+        assert np.all(w.block_tables[s, n:] == w.poison_block)
+        assert w.seq_k[s].shape == (int(w.context_lens[s]), w.num_kv_heads, w.head_dim)
+    assert w.q.shape == (w.num_seqs, w.num_heads, w.head_dim)
+    assert w.num_heads % w.num_kv_heads == 0
+
+
+def test_tiny_matches_its_description():
+    w = W.tiny()
+    _check_structure(w)
+    assert list(w.context_lens) == [17, 40]
+    assert (w.num_heads, w.num_kv_heads, w.head_dim, w.block_size, w.num_blocks) == (4, 2, 64, 16, 8)
+    assert w.scale == 1 / 8
+    k_new, v_new, slots = w.last_token_append()
+    # positions 16 and 39
+    assert slots[0] == w.block_tables[0, 1] * 16 + 0
+    assert slots[1] == w.block_tables[1, 2] * 16 + 7
+
+
+def test_llama8b_structure():
+    w = W.llama8b()
+    _check_structure(w)
+    assert w.context_lens.min() >= 512 and w.context_lens.max() <= 2048
+    assert (w.num_seqs, w.num_heads, w.num_kv_heads, w.head_dim, w.block_size) == (32, 32, 8, 128, 16)
+
+
+def test_ragged_lengths():
+    rng = W._rng(W.BASE_SEED + 3)
+    lens = W.ragged_lens(rng)
+    assert lens.min() == 1 and lens.max() <= 16384
+    assert (lens == 1).sum() >= 8
+    assert 600 < np.median(lens) < 1700
+
+
+def test_loop_schedule_is_consistent():
+    loop = W.AppendDecodeLoop(steps=6, num_seqs=8, max_len=40, min_len=1, num_blocks=64,
+                              max_blocks_per_seq=4, num_pad=2)
+    seen = set()
+    for t in range(loop.steps):
+        st = loop.step(t)
+        real = st.slot_mapping >= 0
+        assert real.sum() == loop.num_seqs and (~real).sum() == loop.num_pad
+        assert np.all(np.isnan(st.k_new[~real].astype(np.float32)))
+        for s, slot in enumerate(st.slot_mapping[real]):
+            pos = int(st.context_lens[s]) - 1
+            assert slot == st.block_tables[s, pos // 16] * 16 + pos % 16
+            assert slot not in seen
+            seen.add(int(slot))
+    # no block is owned by two sequences
+    last = loop.tables[-1]
+    owned = np.concatenate([last[s, : -(-int(loop.end_lens[s]) // 16)] for s in range(loop.num_seqs)])
+    assert len(np.unique(owned)) == len(owned)
+    assert loop.poison_block not in set(owned.tolist())

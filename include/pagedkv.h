@@ -1,0 +1,192 @@
+/*
+ * libpagedkv — batched paged-KV decode attention for one GB300 (sm_103a).
+ *
+ * One new query token per sequence attends over f16 K/V stored in fixed-size
+ * physical blocks, reached through a per-sequence block table and context
+ * length, with grouped-query heads.  The operations follow the paged-decode
+ * backends of the Rust LLM-serving crates:
+ *   - ferrum-kernels src/backend/cuda/paged.rs — paged_decode_attention,
+ *     paged_batched_decode_attention, paged_batched_flash_dispatch (split-K
+ *     phase 1 + reduce, split-count heuristic), paged_batched_decode_single_pass;
+ *   - kapsl-backends src/gguf_native.rs — forward_batch_decode_greedy and
+ *     one_token_compute (kv write at (physical block, position in block),
+ *     paged attention with block tables and context_lens, scale argument);
+ *   - cortiq-engine src/gpu_cuda.rs — GQA grouping hpk = nh / nkv.
+ *
+ * Conventions for every call
+ *   - Pointers named "device" are CUDA device pointers (or managed memory).
+ *     The caller owns every buffer.  The library allocates nothing per call;
+ *     its only memory is one 32-bit device status word per GPU (see
+ *     pkv_read_device_status).
+ *   - f16 is IEEE binary16 (2 bytes).  All arrays are dense, row-major,
+ *     with no padding between rows.
+ *   - KV cache layout: k_cache and v_cache are each
+ *       f16 [num_blocks][num_kv_heads][block_size][head_dim],
+ *     so the (block, kv_head) tile of block_size x head_dim is contiguous.
+ *     Both must be 16-byte aligned.
+ *   - Supported: head_dim in {64, 128}; block_size in {16, 32};
+ *     num_heads / num_kv_heads (the group) in 1..8.
+ *   - stream is a cudaStream_t (NULL = the legacy default stream).  Every
+ *     call is asynchronous on it, reads no device memory on the host and
+ *     never synchronizes, so a sequence of calls can be captured into a CUDA
+ *     graph (pkv_read_device_status is the one exception).
+ *   - Errors: a call returns a pkv_status.  Arguments are validated on the
+ *     host before any CUDA call; a rejected call launches nothing.
+ *     PKV_ERR_CUDA means a launch failed; pkv_last_error() has the message.
+ *   - Bad data inside device arrays (a block id outside [0, num_blocks), a
+ *     context length above max_blocks_per_seq * block_size, a slot past the
+ *     pool) is never dereferenced: the kernel skips it and sets a bit of the
+ *     device status word.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t pkv_status;
+
+#define PKV_OK 0
+#define PKV_ERR_INVALID_ARG (-1)       /* bad size, null pointer, misalignment */
+#define PKV_ERR_UNSUPPORTED (-2)       /* valid but not built: head_dim, block_size, group */
+#define PKV_ERR_SCRATCH_TOO_SMALL (-3) /* split-K scratch missing or too small */
+#define PKV_ERR_CUDA (-4)              /* a CUDA call failed; see pkv_last_error */
+
+/* Bits of the device status word (OR-ed by kernels, read by
+ * pkv_read_device_status). */
+#define PKV_DEV_BAD_SLOT 0x1u        /* append: slot >= num_blocks*block_size; token skipped */
+#define PKV_DEV_BAD_BLOCK_ID 0x2u    /* decode: table entry outside [0,num_blocks); block skipped */
+#define PKV_DEV_BAD_CONTEXT_LEN 0x4u /* decode: context_len < 0 (taken as 0) or above
+                                        max_blocks_per_seq*block_size (clamped) */
+#define PKV_DEV_WAIT_TIMEOUT 0x8u    /* decode: a tile copy did not land within ~2 s;
+                                        the affected outputs were not written */
+
+/* Largest num_splits pkv_decode_splitk accepts. */
+#define PKV_MAX_SPLITS 128
+
+/*
+ * pkv_append — slot-mapped KV write (kapsl-backends src/gguf_native.rs,
+ * forward_batch_decode_greedy / one_token_compute: launch_batch_kv_write and
+ * launch_kv_write store a token's K and V at (physical block, position in
+ * block); here the pair is one integer slot = block * block_size + offset).
+ *
+ *   k, v          device f16 [num_tokens][num_kv_heads][head_dim], 16-byte aligned
+ *   slot_mapping  device int32 [num_tokens]; slot < 0 skips the token
+ *   k_cache, v_cache  device f16 pools (layout above), written in place
+ *
+ * For token t with s = slot_mapping[t] >= 0 and every kv head h:
+ *   k_cache[s / block_size][h][s % block_size][:] = k[t][h][:]  (same for v),
+ * bit for bit.  Two tokens with the same non-negative slot race (undefined).
+ * num_tokens == 0 returns PKV_OK without a launch.
+ */
+pkv_status pkv_append(const void* k, const void* v, const int32_t* slot_mapping,
+                      int32_t num_tokens, void* k_cache, void* v_cache,
+                      int32_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                      int32_t head_dim, void* stream);
+
+/*
+ * pkv_decode — single-pass batched paged decode attention (ferrum-kernels
+ * src/backend/cuda/paged.rs, paged_batched_decode_single_pass and
+ * paged_decode_attention with q_len == 1; kapsl-backends
+ * launch_paged_attention parameters).
+ *
+ *   q             device f16 [num_seqs][num_heads][head_dim], 4-byte aligned
+ *   k_cache, v_cache  device f16 pools (layout above), read only
+ *   block_tables  device int32 [num_seqs][max_blocks_per_seq]: physical block
+ *                 of logical block j of sequence s; entries at or past
+ *                 ceil(context_lens[s] / block_size) are never read
+ *   context_lens  device int32 [num_seqs]: tokens to attend to, including the
+ *                 one appended this step (positions 0 .. L-1)
+ *   scale         softmax scale applied to q.k (usually 1/sqrt(head_dim))
+ *   out           device f16 [num_seqs][num_heads][head_dim], 4-byte aligned
+ *
+ * For sequence s, query head h, kv head g = h / (num_heads / num_kv_heads):
+ *   out[s][h] = sum_i softmax_i(scale * q[s][h] . K_s[i]) V_s[i],
+ *   K_s[i] = k_cache[block_tables[s][i / block_size]][g][i % block_size].
+ * Accumulation is f32; out is rounded to nearest-even f16.  L == 0 gives
+ * zeros.  num_seqs == 0 returns PKV_OK without a launch.
+ */
+pkv_status pkv_decode(const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* block_tables, const int32_t* context_lens,
+                      int32_t num_seqs, int32_t max_blocks_per_seq, int32_t num_blocks,
+                      float scale, int32_t num_heads, int32_t num_kv_heads,
+                      int32_t head_dim, int32_t block_size, void* out, void* stream);
+
+/*
+ * pkv_decode_splitk — the same result as pkv_decode, with each sequence's
+ * context split into chunks processed by separate CTAs and merged by a
+ * log-sum-exp combine (ferrum-kernels src/backend/cuda/paged.rs,
+ * paged_batched_flash_dispatch: phase 1 writes f32 partial out / max / sum,
+ * phase 2 reduces them per (sequence, head)).
+ *
+ *   num_splits    0 = pick with pkv_pick_num_splits for the current GPU; 1 =
+ *                 run the single-pass kernel (no scratch needed);
+ *                 2..PKV_MAX_SPLITS = forced.  A chunk is
+ *                 ceil(max_blocks_per_seq / num_splits) blocks.
+ *   scratch       device memory of at least
+ *                 pkv_splitk_scratch_bytes(num_seqs, num_heads, head_dim, S)
+ *                 bytes, 16-byte aligned, caller-owned; its contents need no
+ *                 initialisation and are overwritten.  Calls that overlap on
+ *                 the GPU must not share scratch.
+ *   other arguments as pkv_decode.
+ *
+ * Returns PKV_ERR_SCRATCH_TOO_SMALL when S > 1 and the scratch is null or
+ * smaller than required.
+ */
+pkv_status pkv_decode_splitk(const void* q, const void* k_cache, const void* v_cache,
+                             const int32_t* block_tables, const int32_t* context_lens,
+                             int32_t num_seqs, int32_t max_blocks_per_seq,
+                             int32_t num_blocks, float scale, int32_t num_heads,
+                             int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                             void* out, int32_t num_splits, void* scratch,
+                             size_t scratch_bytes, void* stream);
+
+/*
+ * pkv_splitk_scratch_bytes — bytes of scratch pkv_decode_splitk needs for S
+ * splits: f32 partial outputs [num_seqs][num_heads][S][head_dim] followed by
+ * f32 running max and running sum [num_seqs][num_heads][S] each (every part
+ * 256-byte aligned).  0 when S <= 1 or for invalid sizes.
+ * (ferrum-kernels paged.rs keeps these three buffers process-global and grows
+ * them on demand; here the caller owns them.)
+ */
+size_t pkv_splitk_scratch_bytes(int32_t num_seqs, int32_t num_heads, int32_t head_dim,
+                                int32_t num_splits);
+
+/*
+ * pkv_pick_num_splits — the split count pkv_decode_splitk uses when given 0
+ * (ferrum-kernels paged.rs, paged_batched_flash_dispatch: the grid wants
+ * enough CTAs to fill the SMs; once the base grid saturates them, splitting
+ * pays only for long contexts).  Here the base grid is num_seqs *
+ * num_kv_heads (one CTA per sequence and KV head covers the whole group),
+ * measured against num_sms.  max_context_len is the longest context the call
+ * may see (pkv_decode_splitk passes max_blocks_per_seq * block_size).
+ * Returns a value in 1..64; 1 for invalid sizes.
+ */
+int32_t pkv_pick_num_splits(int32_t num_seqs, int32_t num_kv_heads,
+                            int32_t max_context_len, int32_t block_size,
+                            int32_t num_sms);
+
+/* Static text for a status code (never NULL). */
+const char* pkv_status_string(pkv_status status);
+
+/* The message of the last failed call on this host thread ("" if none).
+ * Valid until the next failing call on the thread. */
+const char* pkv_last_error(void);
+
+/*
+ * pkv_read_device_status — copy the current GPU's status word (PKV_DEV_* bits
+ * OR-ed by kernels since the last read) into *flags and clear it.  Enqueued
+ * on stream and then synchronizes that stream: for tests and diagnostics,
+ * not for the decode loop.
+ */
+pkv_status pkv_read_device_status(int32_t* flags, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

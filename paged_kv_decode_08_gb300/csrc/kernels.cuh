@@ -1,0 +1,457 @@
+// Kernels of libpagedkv: slot-mapped KV append, paged decode attention
+// (single pass, and split-K phase 1), and the log-sum-exp combine of split-K.
+//
+// Decode design (GB300, sm_103a):
+//  * One CTA per (sequence, KV head[, split]).  It covers the whole GQA group
+//    of that KV head, so every K/V byte is read from HBM once.
+//  * Each of the CTA's W warps owns a private ring of P shared-memory stages.
+//    A stage holds the K and V tiles of one physical block for this KV head
+//    (block_size x head_dim f16 each, contiguous in the pool).  Lane 0 of the
+//    warp fetches them with TMA tensor copies (128-byte swizzle) that complete
+//    on the stage's mbarrier.  Warp w takes the chunk's blocks w, w+W, ...
+//  * Scores use tensor cores with tokens on M and the group on N:
+//      S^T[16 tok x 8 heads] = K[16 x D] . Q^T[D x 8]      (mma m16n8k16)
+//      O^T[D x 8 heads]     += V^T[D x 16 tok] . P^T[16 x 8]
+//    K/V fragments come from ldmatrix (V transposed), Q^T fragments stay in
+//    registers, and P^T is P transposed in registers with movmatrix.  Groups
+//    smaller than 8 leave unused columns (computed, never stored).
+//  * Online softmax in f32 (base-2 exponent with scale*log2(e) folded in);
+//    the running max is shared by the 8 lanes holding one head's column, the
+//    running sum stays per lane until the end.
+//  * At the end the W warp states are merged through shared memory; the
+//    single-pass kernel writes f16 output, the split-K kernel writes the
+//    unnormalised f32 partial output, max and sum for the combine kernel.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <math_constants.h>
+#include <stdint.h>
+
+#include "ptx.cuh"
+
+namespace pkv {
+
+// Per-GPU status word; kernels OR PKV_DEV_* bits into it.  (This header is
+// compiled into exactly one translation unit.)
+__device__ unsigned int g_device_status = 0;
+
+constexpr unsigned int kDevBadSlot = 0x1u;
+constexpr unsigned int kDevBadBlockId = 0x2u;
+constexpr unsigned int kDevBadContextLen = 0x4u;
+constexpr unsigned int kDevWaitTimeout = 0x8u;
+
+// A tile copy that has not landed after this long is reported, not awaited.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+// ---------------------------------------------------------------------------
+// append
+// ---------------------------------------------------------------------------
+
+// One thread per 16-byte chunk of a (token, kv head) row; K and V together.
+__global__ void __launch_bounds__(256)
+append_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
+              const int32_t* __restrict__ slot_mapping, long long total_chunks,
+              int chunks_per_row, int num_kv_heads, int block_size, long long num_slots,
+              uint4* __restrict__ k_cache, uint4* __restrict__ v_cache) {
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total_chunks;
+       i += stride) {
+    const int ch = (int)(i % chunks_per_row);
+    const long long row = i / chunks_per_row;  // token * num_kv_heads + head
+    const int h = (int)(row % num_kv_heads);
+    const long long t = row / num_kv_heads;
+    const int slot = __ldg(slot_mapping + t);
+    if (slot < 0) continue;
+    if ((long long)slot >= num_slots) {
+      if (h == 0 && ch == 0) atomicOr(&g_device_status, kDevBadSlot);
+      continue;
+    }
+    const int blk = slot / block_size;
+    const int off = slot - blk * block_size;
+    const size_t dst = (((size_t)blk * num_kv_heads + h) * block_size + off) * chunks_per_row + ch;
+    k_cache[dst] = __ldg(k + i);
+    v_cache[dst] = __ldg(v + i);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// decode
+// ---------------------------------------------------------------------------
+
+struct DecodeParams {
+  const __half* q;              // [B][H][D]
+  const int32_t* block_tables;  // [B][MBPS]
+  const int32_t* context_lens;  // [B]
+  __half* out;                  // [B][H][D]             (single pass)
+  float* part_out;              // [B][H][S][D]          (split-K)
+  float* part_m;                // [B][H][S]  base-2 running max
+  float* part_l;                // [B][H][S]  running sum
+  int num_heads;
+  int num_kv_heads;
+  int group;
+  int max_blocks_per_seq;
+  int num_blocks;
+  int num_splits;    // S (1 for single pass)
+  int chunk_blocks;  // blocks per split
+  float scale_log2;  // scale * log2(e)
+};
+
+template <int D, int BS, int W, int P>
+struct DecodeShape {
+  static constexpr int kTileBytes = BS * D * 2;  // one K (or V) tile
+  static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kRingBytes = W * P * kStageBytes;
+  static constexpr int kBarrierBytes = W * P * 8;
+  static constexpr int kSmemBytes = 1024 + kRingBytes + kBarrierBytes;  // +1024: alignment slack
+  static constexpr int kMT = BS / 16;     // 16-token slices per tile
+  static constexpr int kKS = D / 16;      // 16-wide slices of head_dim
+  static constexpr int kHalves = D / 64;  // 128-byte lines per row
+  static constexpr int kRedFloats = 16 + 8 * D;  // per warp: m[8], l[8], o[8][D]
+  static_assert(kTileBytes % 1024 == 0, "tiles must keep 1024-byte alignment for the swizzle");
+  static_assert(W * kRedFloats * 4 <= kRingBytes, "the merge area reuses the ring");
+};
+
+// Byte offset of element (row, d) inside a tile stored as [D/64][BS][64] f16
+// with the TMA 128-byte swizzle (16-byte chunk index XOR row % 8).
+template <int BS>
+__device__ __forceinline__ uint32_t swz(int row, int d) {
+  const int line = (d >> 6) * BS + row;
+  const int chunk = ((d & 63) >> 3) ^ (row & 7);
+  return (uint32_t)(line * 128 + chunk * 16 + (d & 7) * 2);
+}
+
+template <int D, int BS, int W, int P, bool SPLIT>
+__global__ void __launch_bounds__(W * 32)
+paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
+                    const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
+  using Shape = DecodeShape<D, BS, W, P>;
+  constexpr int MT = Shape::kMT;
+  constexpr int KS = Shape::kKS;
+  constexpr int TB = Shape::kTileBytes;
+
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ int s_failed;
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t ring = smem_addr(smem);
+  const uint32_t bars = ring + Shape::kRingBytes;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int r = lane >> 2;  // mma group id
+  const int c = lane & 3;   // thread in group
+
+  int item = blockIdx.x;
+  const int split = SPLIT ? item % p.num_splits : 0;
+  if (SPLIT) item /= p.num_splits;
+  const int g = item % p.num_kv_heads;
+  const int s = item / p.num_kv_heads;
+
+  const int cap = p.max_blocks_per_seq * BS;
+  int L = __ldg(p.context_lens + s);
+  if (L < 0 || L > cap) {
+    if (threadIdx.x == 0) atomicOr(&g_device_status, kDevBadContextLen);
+    L = L < 0 ? 0 : cap;
+  }
+  int tok_begin = 0;
+  int tok_end = L;
+  if (SPLIT) {
+    tok_begin = split * p.chunk_blocks * BS;
+    if (tok_begin >= L) return;  // empty split: the combine never reads it
+    tok_end = min(L, tok_begin + p.chunk_blocks * BS);
+  }
+  const int blk_begin = tok_begin / BS;
+  const int n_tiles = (tok_end - tok_begin + BS - 1) / BS;
+  const int32_t* table = p.block_tables + (size_t)s * p.max_blocks_per_seq;
+  const int my_tiles = n_tiles > warp ? (n_tiles - warp + W - 1) / W : 0;
+
+  if (threadIdx.x == 0) s_failed = 0;
+  const uint32_t my_bars = bars + warp * P * 8;
+  if (lane == 0) {
+#pragma unroll
+    for (int i = 0; i < P; ++i) mbar_init(my_bars + 8 * i, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  auto k_stage = [&](int stage) { return ring + (warp * P + stage) * Shape::kStageBytes; };
+
+  // Lane 0: start the copies of this warp's local tile `li` into its stage.
+  auto issue = [&](int li) {
+    const int stage = li % P;
+    const int j = blk_begin + warp + li * W;
+    const int phys = __ldg(table + j);
+    const uint32_t bar = my_bars + 8 * stage;
+    if (phys >= 0 && phys < p.num_blocks) {
+      mbar_arrive_expect_tx(bar, 2 * TB);
+      const int tile = phys * p.num_kv_heads + g;
+      const uint32_t kdst = k_stage(stage);
+#pragma unroll
+      for (int h2 = 0; h2 < Shape::kHalves; ++h2) {
+        tma_load_4d(kdst + h2 * BS * 128, &kmap, bar, 0, h2, 0, tile);
+        tma_load_4d(kdst + TB + h2 * BS * 128, &vmap, bar, 0, h2, 0, tile);
+      }
+    } else {
+      atomicOr(&g_device_status, kDevBadBlockId);
+      mbar_arrive(bar);
+    }
+  };
+
+  if (lane == 0) {
+    const int n0 = my_tiles < P ? my_tiles : P;
+    for (int li = 0; li < n0; ++li) issue(li);
+  }
+
+  // Q^T fragments (B operand): column n = lane/4 is query head g*G + n.
+  uint32_t qf[KS][2];
+  {
+    const bool live = r < p.group;
+    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+        p.q + ((size_t)s * p.num_heads + (size_t)g * p.group + (live ? r : 0)) * D);
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      qf[ks][0] = live ? __ldg(qrow + ks * 8 + c) : 0u;
+      qf[ks][1] = live ? __ldg(qrow + ks * 8 + 4 + c) : 0u;
+    }
+  }
+
+  float acc[KS][4];  // O^T fragments: rows d = 16*i + r (+8), columns heads 2c, 2c+1
+#pragma unroll
+  for (int i = 0; i < KS; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+  float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F;  // running max of heads 2c, 2c+1
+  float l0 = 0.f, l1 = 0.f;                      // this lane's share of the running sums
+  bool failed = false;
+  int li = 0;
+
+  for (; li < my_tiles; ++li) {
+    const int stage = li % P;
+    const uint32_t bar = my_bars + 8 * stage;
+    if (!mbar_wait_bounded(bar, (li / P) & 1, kWaitLimitNs)) {
+      failed = true;
+      break;
+    }
+    const int j = blk_begin + warp + li * W;
+    const int phys = __ldg(table + j);
+    if (phys >= 0 && phys < p.num_blocks) {
+      const int t0 = j * BS;
+      const int n_valid = min(BS, tok_end - t0);
+      const uint32_t kb = k_stage(stage);
+      const uint32_t vb = kb + TB;
+      if (n_valid < BS) {
+        // Rows past the context may hold anything (even NaN); P is 0 there,
+        // but 0 * NaN is NaN, so clear those V rows before P.V.
+        const int n_chunks = (BS - n_valid) * Shape::kHalves * 8;
+        for (int x = lane; x < n_chunks; x += 32) {
+          const int row = n_valid + x / (Shape::kHalves * 8);
+          const int rest = x % (Shape::kHalves * 8);
+          const int line = (rest >> 3) * BS + row;
+          const uint32_t a = vb + line * 128 + (rest & 7) * 16;
+          asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0) : "memory");
+        }
+        __syncwarp();
+      }
+
+      // S^T = K . Q^T for every 16-token slice of the tile.
+      float sc[MT][4];
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        sc[mt][0] = sc[mt][1] = sc[mt][2] = sc[mt][3] = 0.f;
+        const int row = mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          uint32_t a[4];
+          ldsm_x4(kb + swz<BS>(row, ks * 16 + (lane >> 4) * 8), a);
+          mma_16816(sc[mt], a, qf[ks][0], qf[ks][1]);
+        }
+      }
+
+      // scale, mask rows past the chunk, tile max per head
+      float x0 = -CUDART_INF_F, x1 = -CUDART_INF_F;
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int tok = t0 + mt * 16 + r + (e >> 1) * 8;
+          const float v = sc[mt][e] * p.scale_log2;
+          sc[mt][e] = tok < tok_end ? v : -CUDART_INF_F;
+        }
+        x0 = fmaxf(x0, fmaxf(sc[mt][0], sc[mt][2]));
+        x1 = fmaxf(x1, fmaxf(sc[mt][1], sc[mt][3]));
+      }
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, o));
+        x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, o));
+      }
+      const float mn0 = fmaxf(m0, x0);
+      const float mn1 = fmaxf(m1, x1);
+      const float al0 = exp2f(m0 - mn0);  // 0 on the first tile (m = -inf)
+      const float al1 = exp2f(m1 - mn1);
+      m0 = mn0;
+      m1 = mn1;
+
+      // P = exp2(S - m), rounded to f16 for the tensor cores; the running sum
+      // adds the same rounded values so numerator and denominator agree.
+      uint32_t pb[MT][2];
+      float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        const __half2 h01 = __floats2half2_rn(exp2f(sc[mt][0] - m0), exp2f(sc[mt][1] - m1));
+        const __half2 h23 = __floats2half2_rn(exp2f(sc[mt][2] - m0), exp2f(sc[mt][3] - m1));
+        const float2 f01 = __half22float2(h01);
+        const float2 f23 = __half22float2(h23);
+        ps0 += f01.x + f23.x;
+        ps1 += f01.y + f23.y;
+        pb[mt][0] = movmatrix_trans(pack_half2(h01));
+        pb[mt][1] = movmatrix_trans(pack_half2(h23));
+      }
+      l0 = l0 * al0 + ps0;
+      l1 = l1 * al1 + ps1;
+#pragma unroll
+      for (int i = 0; i < KS; ++i) {
+        acc[i][0] *= al0;
+        acc[i][1] *= al1;
+        acc[i][2] *= al0;
+        acc[i][3] *= al1;
+      }
+
+      // O^T += V^T . P^T
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        const int row = mt * 16 + (lane & 7) + (lane >> 4) * 8;
+#pragma unroll
+        for (int i = 0; i < KS; ++i) {
+          uint32_t a[4];
+          ldsm_x4_trans(vb + swz<BS>(row, i * 16 + ((lane >> 3) & 1) * 8), a);
+          mma_16816(acc[i], a, pb[mt][0], pb[mt][1]);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0 && li + P < my_tiles) {
+      fence_proxy_async_smem();
+      issue(li + P);
+    }
+  }
+
+  if (failed) {
+    // Let the copies this warp still has in flight land before the CTA may
+    // exit (bounded as well), then report.
+    if (lane == 0) atomicOr(&g_device_status, kDevWaitTimeout);
+    const int last = min(li + P, my_tiles);
+    for (int lj = li; lj < last; ++lj)
+      (void)mbar_wait_bounded(my_bars + 8 * (lj % P), (lj / P) & 1, kWaitLimitNs);
+    if (lane == 0) atomicOr(&s_failed, 1);
+  }
+
+  // complete the per-lane sums across the 8 lanes of each head column
+#pragma unroll
+  for (int o = 4; o < 32; o <<= 1) {
+    l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+  }
+
+  __syncthreads();  // every warp is done with its ring
+  if (s_failed) return;
+
+  // merge the W warp states through shared memory (reusing the ring)
+  float* red = reinterpret_cast<float*>(smem);
+  {
+    float* mine = red + warp * Shape::kRedFloats;
+    if (r == 0) {
+      mine[2 * c] = m0;
+      mine[2 * c + 1] = m1;
+      mine[8 + 2 * c] = l0;
+      mine[8 + 2 * c + 1] = l1;
+    }
+    float* o = mine + 16;
+#pragma unroll
+    for (int i = 0; i < KS; ++i) {
+      const int d = i * 16 + r;
+      o[(2 * c) * D + d] = acc[i][0];
+      o[(2 * c + 1) * D + d] = acc[i][1];
+      o[(2 * c) * D + d + 8] = acc[i][2];
+      o[(2 * c + 1) * D + d + 8] = acc[i][3];
+    }
+  }
+  __syncthreads();
+
+  const int G = p.group;
+  for (int idx = threadIdx.x; idx < G * D; idx += W * 32) {
+    const int h = idx / D;
+    const int d = idx - h * D;
+    float M = -CUDART_INF_F;
+#pragma unroll
+    for (int w = 0; w < W; ++w) M = fmaxf(M, red[w * Shape::kRedFloats + h]);
+    float num = 0.f, den = 0.f;
+#pragma unroll
+    for (int w = 0; w < W; ++w) {
+      const float mw = red[w * Shape::kRedFloats + h];
+      const float f = (mw == -CUDART_INF_F) ? 0.f : exp2f(mw - M);
+      num += f * red[w * Shape::kRedFloats + 16 + h * D + d];
+      den += f * red[w * Shape::kRedFloats + 8 + h];
+    }
+    const size_t qh = (size_t)s * p.num_heads + (size_t)g * G + h;
+    if (SPLIT) {
+      const size_t slot = qh * p.num_splits + split;
+      p.part_out[slot * D + d] = num;
+      if (d == 0) {
+        p.part_m[slot] = M;
+        p.part_l[slot] = den;
+      }
+    } else {
+      p.out[qh * D + d] = __float2half_rn(den > 0.f ? num / den : 0.f);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// split-K combine
+// ---------------------------------------------------------------------------
+
+struct CombineParams {
+  const float* part_out;
+  const float* part_m;
+  const float* part_l;
+  const int32_t* context_lens;
+  __half* out;
+  int num_heads;
+  int head_dim;
+  int num_splits;
+  int chunk_tokens;
+  int cap_tokens;  // max_blocks_per_seq * block_size
+};
+
+// One CTA per (sequence, query head); threads over head_dim.  Splits whose
+// first token is at or past the context length were never written and are
+// not read.
+__global__ void __launch_bounds__(128) splitk_combine_kernel(const CombineParams p) {
+  const int sh = blockIdx.x;
+  const int s = sh / p.num_heads;
+  int L = __ldg(p.context_lens + s);
+  L = L < 0 ? 0 : (L > p.cap_tokens ? p.cap_tokens : L);
+  const int n_valid = min(p.num_splits, (L + p.chunk_tokens - 1) / p.chunk_tokens);
+  const float* pm = p.part_m + (size_t)sh * p.num_splits;
+  const float* pl = p.part_l + (size_t)sh * p.num_splits;
+  const float* po = p.part_out + (size_t)sh * p.num_splits * p.head_dim;
+
+  float M = -CUDART_INF_F;
+  for (int k = 0; k < n_valid; ++k) M = fmaxf(M, __ldg(pm + k));
+  float den = 0.f;
+  for (int k = 0; k < n_valid; ++k) {
+    const float mk = __ldg(pm + k);
+    den += (mk == -CUDART_INF_F) ? 0.f : exp2f(mk - M) * __ldg(pl + k);
+  }
+  for (int d = threadIdx.x; d < p.head_dim; d += blockDim.x) {
+    float num = 0.f;
+    for (int k = 0; k < n_valid; ++k) {
+      const float mk = __ldg(pm + k);
+      if (mk == -CUDART_INF_F) continue;
+      num += exp2f(mk - M) * __ldg(po + (size_t)k * p.head_dim + d);
+    }
+    p.out[(size_t)sh * p.head_dim + d] = __float2half_rn(den > 0.f ? num / den : 0.f);
+  }
+}
+
+}  // namespace pkv

@@ -1,0 +1,398 @@
+// libpagedkv: the C-ABI entry points declared in include/pagedkv.h.
+//
+// Host side of every call: validate the arguments (before any CUDA call),
+// build the TMA tensor maps of the two cache pools, pick the kernel
+// instantiation for (head_dim, block_size) and launch on the caller's stream.
+// Nothing here allocates device memory or reads device memory on the host
+// (pkv_read_device_status excepted).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "kernels.cuh"
+#include "pagedkv.h"
+
+namespace pkv {
+namespace {
+
+// Resident decode CTAs per SM the kernels are sized for (64 KB ring each).
+constexpr int kCtasPerSm = 3;
+// With the base grid already filling the GPU, a CTA keeps at most this many
+// tokens, so one long context does not leave a long serial tail.
+constexpr int kSaturatedChunkTokens = 2048;
+// Below this a split's fixed costs outweigh its work.
+constexpr int kMinSplitTokens = 256;
+constexpr int kMaxAutoSplits = 64;
+
+thread_local char t_last_error[512] = "";
+
+pkv_status fail(pkv_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_last_error, sizeof(t_last_error), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+pkv_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(PKV_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+int current_device_sms(int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  static std::atomic<int> cache[64];
+  if (dev >= 0 && dev < 64) {
+    const int v = cache[dev].load(std::memory_order_relaxed);
+    if (v > 0) {
+      *sms = v;
+      return 0;
+    }
+  }
+  int v = 0;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+    return -1;
+  if (dev >= 0 && dev < 64) cache[dev].store(v, std::memory_order_relaxed);
+  *sms = v;
+  return 0;
+}
+
+// The pool as a 4-D tensor {64 elements, head_dim/64 halves, block_size rows,
+// num_blocks*num_kv_heads tiles} (innermost first); a box is one half of one
+// tile: 64 x 1 x block_size x 1, landing as block_size 128-byte lines with the
+// 128-byte swizzle.  The strides are those of the dense pool.
+pkv_status make_cache_map(CUtensorMap* map, const void* base, int num_blocks, int num_kv_heads,
+                          int block_size, int head_dim) {
+  auto encode = tensor_map_encoder();
+  if (!encode) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t dims[4] = {64, (cuuint64_t)(head_dim / 64), (cuuint64_t)block_size,
+                              (cuuint64_t)num_blocks * (cuuint64_t)num_kv_heads};
+  const cuuint64_t strides[3] = {128, (cuuint64_t)head_dim * 2,
+                                 (cuuint64_t)block_size * head_dim * 2};
+  const cuuint32_t box[4] = {64, 1, (cuuint32_t)block_size, 1};
+  const cuuint32_t estride[4] = {1, 1, 1, 1};
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void*>(base), dims,
+                            strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+  return PKV_OK;
+}
+
+struct DecodeArgs {
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  int num_seqs, max_blocks_per_seq, num_blocks;
+  float scale;
+  int num_heads, num_kv_heads, head_dim, block_size;
+  void* out;
+};
+
+pkv_status validate_decode(const DecodeArgs& a) {
+  if (a.num_seqs < 0) return fail(PKV_ERR_INVALID_ARG, "num_seqs < 0");
+  if (!a.q || !a.k_cache || !a.v_cache || !a.block_tables || !a.context_lens || !a.out)
+    return fail(PKV_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (a.num_heads <= 0 || a.num_kv_heads <= 0 || a.num_heads % a.num_kv_heads != 0)
+    return fail(PKV_ERR_INVALID_ARG, "num_heads (%d) must be a positive multiple of num_kv_heads (%d)",
+                a.num_heads, a.num_kv_heads);
+  if (a.max_blocks_per_seq <= 0 || a.num_blocks <= 0 || a.head_dim <= 0 || a.block_size <= 0)
+    return fail(PKV_ERR_INVALID_ARG, "sizes must be positive");
+  if (!std::isfinite(a.scale)) return fail(PKV_ERR_INVALID_ARG, "scale is not finite");
+  if (a.head_dim != 64 && a.head_dim != 128)
+    return fail(PKV_ERR_UNSUPPORTED, "head_dim %d (built: 64, 128)", a.head_dim);
+  if (a.block_size != 16 && a.block_size != 32)
+    return fail(PKV_ERR_UNSUPPORTED, "block_size %d (built: 16, 32)", a.block_size);
+  if (a.num_heads / a.num_kv_heads > 8)
+    return fail(PKV_ERR_UNSUPPORTED, "group %d (built: 1..8)", a.num_heads / a.num_kv_heads);
+  if ((long long)a.num_blocks * a.block_size >= (1ll << 31) ||
+      (long long)a.num_blocks * a.num_kv_heads >= (1ll << 31))
+    return fail(PKV_ERR_INVALID_ARG, "num_blocks too large for 32-bit slots");
+  if ((long long)a.max_blocks_per_seq * a.block_size >= (1ll << 31))
+    return fail(PKV_ERR_INVALID_ARG, "max_blocks_per_seq * block_size overflows");
+  if ((long long)a.num_seqs * a.num_heads >= (1ll << 31))
+    return fail(PKV_ERR_INVALID_ARG, "num_seqs * num_heads too large");
+  if (!aligned(a.k_cache, 16) || !aligned(a.v_cache, 16))
+    return fail(PKV_ERR_INVALID_ARG, "k_cache and v_cache must be 16-byte aligned");
+  if (!aligned(a.q, 4) || !aligned(a.out, 4))
+    return fail(PKV_ERR_INVALID_ARG, "q and out must be 4-byte aligned");
+  if (!aligned(a.block_tables, 4) || !aligned(a.context_lens, 4))
+    return fail(PKV_ERR_INVALID_ARG, "block_tables and context_lens must be 4-byte aligned");
+  return PKV_OK;
+}
+
+template <int D, int BS>
+struct Tuning {
+  static constexpr int W = 4;
+  static constexpr int kStage = 2 * BS * D * 2;
+  static constexpr int P = (64 * 1024) / (W * kStage) > 0 ? (64 * 1024) / (W * kStage) : 1;
+};
+
+template <int D, int BS, bool SPLIT>
+pkv_status launch_decode(const DecodeArgs& a, const DecodeParams& prm, cudaStream_t stream,
+                         int grid) {
+  constexpr int W = Tuning<D, BS>::W;
+  constexpr int P = Tuning<D, BS>::P;
+  using Shape = DecodeShape<D, BS, W, P>;
+  auto kernel = paged_decode_kernel<D, BS, W, P, SPLIT>;
+
+  static std::atomic<unsigned long long> attr_set{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (!(attr_set.load(std::memory_order_relaxed) & bit)) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Shape::kSmemBytes);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(decode)");
+    attr_set.fetch_or(bit, std::memory_order_relaxed);
+  }
+
+  CUtensorMap kmap, vmap;
+  pkv_status st = make_cache_map(&kmap, a.k_cache, a.num_blocks, a.num_kv_heads, BS, D);
+  if (st != PKV_OK) return st;
+  st = make_cache_map(&vmap, a.v_cache, a.num_blocks, a.num_kv_heads, BS, D);
+  if (st != PKV_OK) return st;
+
+  kernel<<<grid, W * 32, Shape::kSmemBytes, stream>>>(kmap, vmap, prm);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, SPLIT ? "split-K phase 1 launch" : "decode launch");
+  return PKV_OK;
+}
+
+template <bool SPLIT>
+pkv_status dispatch_decode(const DecodeArgs& a, const DecodeParams& prm, cudaStream_t stream,
+                           int grid) {
+  if (a.head_dim == 128 && a.block_size == 16) return launch_decode<128, 16, SPLIT>(a, prm, stream, grid);
+  if (a.head_dim == 128 && a.block_size == 32) return launch_decode<128, 32, SPLIT>(a, prm, stream, grid);
+  if (a.head_dim == 64 && a.block_size == 16) return launch_decode<64, 16, SPLIT>(a, prm, stream, grid);
+  if (a.head_dim == 64 && a.block_size == 32) return launch_decode<64, 32, SPLIT>(a, prm, stream, grid);
+  return fail(PKV_ERR_UNSUPPORTED, "head_dim %d / block_size %d", a.head_dim, a.block_size);
+}
+
+DecodeParams base_params(const DecodeArgs& a) {
+  DecodeParams p{};
+  p.q = static_cast<const __half*>(a.q);
+  p.block_tables = a.block_tables;
+  p.context_lens = a.context_lens;
+  p.out = static_cast<__half*>(a.out);
+  p.num_heads = a.num_heads;
+  p.num_kv_heads = a.num_kv_heads;
+  p.group = a.num_heads / a.num_kv_heads;
+  p.max_blocks_per_seq = a.max_blocks_per_seq;
+  p.num_blocks = a.num_blocks;
+  p.num_splits = 1;
+  p.chunk_blocks = a.max_blocks_per_seq;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  return p;
+}
+
+pkv_status single_pass(const DecodeArgs& a, cudaStream_t stream) {
+  const long long grid = (long long)a.num_seqs * a.num_kv_heads;
+  if (grid >= (1ll << 31)) return fail(PKV_ERR_INVALID_ARG, "grid too large");
+  return dispatch_decode<false>(a, base_params(a), stream, (int)grid);
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+const char* pkv_status_string(pkv_status status) {
+  switch (status) {
+    case PKV_OK: return "ok";
+    case PKV_ERR_INVALID_ARG: return "invalid argument";
+    case PKV_ERR_UNSUPPORTED: return "unsupported configuration";
+    case PKV_ERR_SCRATCH_TOO_SMALL: return "split-K scratch missing or too small";
+    case PKV_ERR_CUDA: return "CUDA error";
+    default: return "unknown status";
+  }
+}
+
+const char* pkv_last_error(void) { return t_last_error; }
+
+size_t pkv_splitk_scratch_bytes(int32_t num_seqs, int32_t num_heads, int32_t head_dim,
+                                int32_t num_splits) {
+  if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || num_splits <= 1) return 0;
+  const size_t rows = (size_t)num_seqs * num_heads * num_splits;
+  return align256(rows * head_dim * sizeof(float)) + 2 * align256(rows * sizeof(float));
+}
+
+int32_t pkv_pick_num_splits(int32_t num_seqs, int32_t num_kv_heads, int32_t max_context_len,
+                            int32_t block_size, int32_t num_sms) {
+  if (num_seqs <= 0 || num_kv_heads <= 0 || max_context_len <= 0 || block_size <= 0 ||
+      num_sms <= 0)
+    return 1;
+  const long long base = (long long)num_seqs * num_kv_heads;
+  const long long slots = (long long)num_sms * kCtasPerSm;
+  long long s;
+  if (base >= slots) {
+    s = (max_context_len + kSaturatedChunkTokens - 1) / kSaturatedChunkTokens;
+  } else {
+    s = slots / base;  // every split CTA resident in one wave
+  }
+  const long long by_len = max_context_len / kMinSplitTokens;
+  const long long max_blocks = (max_context_len + block_size - 1) / block_size;
+  if (s > by_len) s = by_len;
+  if (s > max_blocks) s = max_blocks;
+  if (s > kMaxAutoSplits) s = kMaxAutoSplits;
+  if (s < 1) s = 1;
+  return (int32_t)s;
+}
+
+pkv_status pkv_append(const void* k, const void* v, const int32_t* slot_mapping,
+                      int32_t num_tokens, void* k_cache, void* v_cache, int32_t num_blocks,
+                      int32_t block_size, int32_t num_kv_heads, int32_t head_dim, void* stream) {
+  if (num_tokens < 0) return fail(PKV_ERR_INVALID_ARG, "num_tokens < 0");
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache)
+    return fail(PKV_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0)
+    return fail(PKV_ERR_INVALID_ARG, "sizes must be positive");
+  if (head_dim != 64 && head_dim != 128)
+    return fail(PKV_ERR_UNSUPPORTED, "head_dim %d (built: 64, 128)", head_dim);
+  if (block_size != 16 && block_size != 32)
+    return fail(PKV_ERR_UNSUPPORTED, "block_size %d (built: 16, 32)", block_size);
+  if ((long long)num_blocks * block_size >= (1ll << 31))
+    return fail(PKV_ERR_INVALID_ARG, "num_blocks too large for 32-bit slots");
+  if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+    return fail(PKV_ERR_INVALID_ARG, "k, v, k_cache and v_cache must be 16-byte aligned");
+  if (!aligned(slot_mapping, 4)) return fail(PKV_ERR_INVALID_ARG, "slot_mapping must be 4-byte aligned");
+  if (num_tokens == 0) return PKV_OK;
+
+  const int chunks_per_row = head_dim / 8;
+  const long long total = (long long)num_tokens * num_kv_heads * chunks_per_row;
+  long long blocks = (total + 255) / 256;
+  if (blocks > 65536) blocks = 65536;  // grid-stride beyond this
+  append_kernel<<<(int)blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint4*>(k), static_cast<const uint4*>(v), slot_mapping, total,
+      chunks_per_row, num_kv_heads, block_size, (long long)num_blocks * block_size,
+      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache));
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "append launch");
+  return PKV_OK;
+}
+
+pkv_status pkv_decode(const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* block_tables, const int32_t* context_lens, int32_t num_seqs,
+                      int32_t max_blocks_per_seq, int32_t num_blocks, float scale,
+                      int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                      int32_t block_size, void* out, void* stream) {
+  const DecodeArgs a{q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                     max_blocks_per_seq, num_blocks, scale, num_heads, num_kv_heads,
+                     head_dim, block_size, out};
+  pkv_status st = validate_decode(a);
+  if (st != PKV_OK) return st;
+  if (num_seqs == 0) return PKV_OK;
+  return single_pass(a, static_cast<cudaStream_t>(stream));
+}
+
+pkv_status pkv_decode_splitk(const void* q, const void* k_cache, const void* v_cache,
+                             const int32_t* block_tables, const int32_t* context_lens,
+                             int32_t num_seqs, int32_t max_blocks_per_seq, int32_t num_blocks,
+                             float scale, int32_t num_heads, int32_t num_kv_heads,
+                             int32_t head_dim, int32_t block_size, void* out, int32_t num_splits,
+                             void* scratch, size_t scratch_bytes, void* stream) {
+  const DecodeArgs a{q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                     max_blocks_per_seq, num_blocks, scale, num_heads, num_kv_heads,
+                     head_dim, block_size, out};
+  pkv_status st = validate_decode(a);
+  if (st != PKV_OK) return st;
+  if (num_splits < 0 || num_splits > PKV_MAX_SPLITS)
+    return fail(PKV_ERR_INVALID_ARG, "num_splits %d outside 0..%d", num_splits, PKV_MAX_SPLITS);
+  if (num_seqs == 0) return PKV_OK;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+
+  int S = num_splits;
+  if (S == 0) {
+    int sms = 0;
+    if (current_device_sms(&sms) != 0) return fail(PKV_ERR_CUDA, "cannot query the SM count");
+    S = pkv_pick_num_splits(num_seqs, num_kv_heads, max_blocks_per_seq * block_size, block_size, sms);
+  }
+  const int chunk_blocks = (max_blocks_per_seq + S - 1) / S;
+  const int S_eff = (max_blocks_per_seq + chunk_blocks - 1) / chunk_blocks;
+  if (S_eff <= 1) return single_pass(a, cs);
+
+  const size_t need = pkv_splitk_scratch_bytes(num_seqs, num_heads, head_dim, S_eff);
+  if (!scratch || scratch_bytes < need)
+    return fail(PKV_ERR_SCRATCH_TOO_SMALL, "split-K with %d splits needs %zu scratch bytes, got %zu",
+                S_eff, need, scratch ? scratch_bytes : (size_t)0);
+  if (!aligned(scratch, 16)) return fail(PKV_ERR_INVALID_ARG, "scratch must be 16-byte aligned");
+  const long long grid1 = (long long)num_seqs * num_kv_heads * S_eff;
+  if (grid1 >= (1ll << 31)) return fail(PKV_ERR_INVALID_ARG, "grid too large");
+
+  const size_t rows = (size_t)num_seqs * num_heads * S_eff;
+  uint8_t* base = static_cast<uint8_t*>(scratch);
+  DecodeParams prm = base_params(a);
+  prm.num_splits = S_eff;
+  prm.chunk_blocks = chunk_blocks;
+  prm.part_out = reinterpret_cast<float*>(base);
+  prm.part_m = reinterpret_cast<float*>(base + align256(rows * head_dim * sizeof(float)));
+  prm.part_l = reinterpret_cast<float*>(base + align256(rows * head_dim * sizeof(float)) +
+                                        align256(rows * sizeof(float)));
+  st = dispatch_decode<true>(a, prm, cs, (int)grid1);
+  if (st != PKV_OK) return st;
+
+  CombineParams cp{};
+  cp.part_out = prm.part_out;
+  cp.part_m = prm.part_m;
+  cp.part_l = prm.part_l;
+  cp.context_lens = context_lens;
+  cp.out = static_cast<__half*>(out);
+  cp.num_heads = num_heads;
+  cp.head_dim = head_dim;
+  cp.num_splits = S_eff;
+  cp.chunk_tokens = chunk_blocks * block_size;
+  cp.cap_tokens = max_blocks_per_seq * block_size;
+  splitk_combine_kernel<<<num_seqs * num_heads, 128, 0, cs>>>(cp);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "split-K combine launch");
+  return PKV_OK;
+}
+
+pkv_status pkv_read_device_status(int32_t* flags, void* stream) {
+  if (!flags) return fail(PKV_ERR_INVALID_ARG, "flags is NULL");
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  unsigned int host = 0;
+  cudaError_t e = cudaMemcpyFromSymbolAsync(&host, g_device_status, sizeof(host), 0,
+                                            cudaMemcpyDeviceToHost, cs);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device status word");
+  void* addr = nullptr;
+  e = cudaGetSymbolAddress(&addr, g_device_status);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)");
+  e = cudaMemsetAsync(addr, 0, sizeof(unsigned int), cs);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the device status word");
+  e = cudaStreamSynchronize(cs);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  *flags = (int32_t)host;
+  return PKV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,213 @@
+"""Python binding of libpagedkv: the C-ABI calls under the same names.
+
+Argument marshalling only: every step of the path runs in the CUDA library.
+There is no fallback; if ``libpagedkv.so`` is missing or does not load, the
+import fails with an error that says how to build it.
+
+The tensor-level wrappers take torch CUDA tensors, check dtype, shape,
+device and contiguity, and pass ``data_ptr()`` plus the current torch stream
+(or the one given).  :data:`lib` exposes the raw ``ctypes`` functions for
+callers that manage their own pointers.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpagedkv.so")
+
+PKV_OK = 0
+PKV_ERR_INVALID_ARG = -1
+PKV_ERR_UNSUPPORTED = -2
+PKV_ERR_SCRATCH_TOO_SMALL = -3
+PKV_ERR_CUDA = -4
+
+PKV_DEV_BAD_SLOT = 0x1
+PKV_DEV_BAD_BLOCK_ID = 0x2
+PKV_DEV_BAD_CONTEXT_LEN = 0x4
+PKV_DEV_WAIT_TIMEOUT = 0x8
+
+PKV_MAX_SPLITS = 128
+
+
+class PagedKVError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{message} (status {status})")
+        self.status = status
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is not built; run `python -c 'import __graft_entry__ as g; g.build()'` "
+            "or `python paged_kv_decode_08_gb300/build.py`")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i32, sz, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t, ctypes.c_float
+    lib.pkv_append.argtypes = [vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, vp]
+    lib.pkv_append.restype = i32
+    lib.pkv_decode.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, f32, i32, i32, i32, i32, vp, vp]
+    lib.pkv_decode.restype = i32
+    lib.pkv_decode_splitk.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, f32, i32, i32, i32, i32,
+                                      vp, i32, vp, sz, vp]
+    lib.pkv_decode_splitk.restype = i32
+    lib.pkv_splitk_scratch_bytes.argtypes = [i32, i32, i32, i32]
+    lib.pkv_splitk_scratch_bytes.restype = sz
+    lib.pkv_pick_num_splits.argtypes = [i32, i32, i32, i32, i32]
+    lib.pkv_pick_num_splits.restype = i32
+    lib.pkv_status_string.argtypes = [i32]
+    lib.pkv_status_string.restype = ctypes.c_char_p
+    lib.pkv_last_error.argtypes = []
+    lib.pkv_last_error.restype = ctypes.c_char_p
+    lib.pkv_read_device_status.argtypes = [ctypes.POINTER(ctypes.c_int32), vp]
+    lib.pkv_read_device_status.restype = i32
+    return lib
+
+
+lib = _load()
+
+
+def _check(status: int, what: str):
+    if status != PKV_OK:
+        msg = lib.pkv_last_error().decode(errors="replace")
+        raise PagedKVError(status, f"{what}: {lib.pkv_status_string(status).decode()}: {msg}")
+
+
+def status_string(status: int) -> str:
+    return lib.pkv_status_string(status).decode()
+
+
+def last_error() -> str:
+    return lib.pkv_last_error().decode(errors="replace")
+
+
+def _stream_ptr(stream):
+    import torch
+
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _want(t, name, dtype, ndim=None, shape=None):
+    import torch
+
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def pkv_append(k, v, slot_mapping, k_cache, v_cache, stream=None):
+    """Write ``k``/``v`` rows ``[T][Hkv][D]`` into the pools at ``slot_mapping``."""
+    import torch
+
+    _want(k_cache, "k_cache", torch.float16, 4)
+    NB, Hkv, bs, D = k_cache.shape
+    _want(v_cache, "v_cache", torch.float16, 4, k_cache.shape)
+    _want(k, "k", torch.float16, 3)
+    T = k.shape[0]
+    _want(k, "k", torch.float16, 3, (T, Hkv, D))
+    _want(v, "v", torch.float16, 3, (T, Hkv, D))
+    _want(slot_mapping, "slot_mapping", torch.int32, 1, (T,))
+    _check(lib.pkv_append(k.data_ptr(), v.data_ptr(), slot_mapping.data_ptr(), T,
+                          k_cache.data_ptr(), v_cache.data_ptr(), NB, bs, Hkv, D,
+                          _stream_ptr(stream)), "pkv_append")
+
+
+def _decode_shapes(q, k_cache, v_cache, block_tables, context_lens, out):
+    import torch
+
+    _want(q, "q", torch.float16, 3)
+    B, H, D = q.shape
+    _want(k_cache, "k_cache", torch.float16, 4)
+    NB, Hkv, bs, Dk = k_cache.shape
+    if Dk != D:
+        raise ValueError("k_cache head_dim differs from q")
+    _want(v_cache, "v_cache", torch.float16, 4, k_cache.shape)
+    _want(block_tables, "block_tables", torch.int32, 2)
+    if block_tables.shape[0] != B:
+        raise ValueError("block_tables must have num_seqs rows")
+    _want(context_lens, "context_lens", torch.int32, 1, (B,))
+    if out is None:
+        out = torch.empty_like(q)
+    _want(out, "out", torch.float16, 3, (B, H, D))
+    return B, H, D, NB, Hkv, bs, block_tables.shape[1], out
+
+
+def pkv_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out=None, stream=None):
+    """Single-pass paged decode; returns ``out`` ``[B][H][D]`` f16."""
+    B, H, D, NB, Hkv, bs, mbps, out = _decode_shapes(q, k_cache, v_cache, block_tables,
+                                                     context_lens, out)
+    _check(lib.pkv_decode(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                          block_tables.data_ptr(), context_lens.data_ptr(), B, mbps, NB,
+                          float(scale), H, Hkv, D, bs, out.data_ptr(), _stream_ptr(stream)),
+           "pkv_decode")
+    return out
+
+
+def pkv_splitk_scratch_bytes(num_seqs, num_heads, head_dim, num_splits) -> int:
+    return int(lib.pkv_splitk_scratch_bytes(num_seqs, num_heads, head_dim, num_splits))
+
+
+def pkv_pick_num_splits(num_seqs, num_kv_heads, max_context_len, block_size, num_sms) -> int:
+    return int(lib.pkv_pick_num_splits(num_seqs, num_kv_heads, max_context_len, block_size,
+                                       num_sms))
+
+
+def splits_for(q, k_cache, block_tables, num_splits=0, device=None) -> int:
+    """The split count :func:`pkv_decode_splitk` will use for these tensors."""
+    import torch
+
+    if num_splits:
+        return int(num_splits)
+    sms = torch.cuda.get_device_properties(device or q.device).multi_processor_count
+    bs = k_cache.shape[2]
+    return pkv_pick_num_splits(q.shape[0], k_cache.shape[1], block_tables.shape[1] * bs, bs, sms)
+
+
+def alloc_scratch(q, k_cache, block_tables, num_splits=0):
+    """A scratch tensor (uint8, on q's device) big enough for the split count
+    :func:`pkv_decode_splitk` will pick (or ``num_splits`` if given)."""
+    import torch
+
+    S = splits_for(q, k_cache, block_tables, num_splits)
+    n = pkv_splitk_scratch_bytes(q.shape[0], q.shape[1], q.shape[2], S)
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=q.device)
+
+
+def pkv_decode_splitk(q, k_cache, v_cache, block_tables, context_lens, scale, num_splits=0,
+                      scratch=None, out=None, stream=None):
+    """Split-K paged decode (``num_splits`` 0 = heuristic); returns ``out``."""
+    import torch
+
+    B, H, D, NB, Hkv, bs, mbps, out = _decode_shapes(q, k_cache, v_cache, block_tables,
+                                                     context_lens, out)
+    if scratch is None:
+        scratch = alloc_scratch(q, k_cache, block_tables, num_splits)
+    _want(scratch, "scratch", torch.uint8, 1)
+    _check(lib.pkv_decode_splitk(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                 block_tables.data_ptr(), context_lens.data_ptr(), B, mbps, NB,
+                                 float(scale), H, Hkv, D, bs, out.data_ptr(), int(num_splits),
+                                 scratch.data_ptr(), scratch.numel(), _stream_ptr(stream)),
+           "pkv_decode_splitk")
+    return out
+
+
+def pkv_read_device_status(stream=None) -> int:
+    """Read and clear the device status word (synchronizes ``stream``)."""
+    flags = ctypes.c_int32(0)
+    _check(lib.pkv_read_device_status(ctypes.byref(flags), _stream_ptr(stream)),
+           "pkv_read_device_status")
+    return int(flags.value)

@@ -1,0 +1,145 @@
+"""The C-ABI library on the host: it loads, exports every declared symbol,
+rejects bad arguments before any CUDA call, and its host-side helpers (split
+heuristic, scratch size, status strings) behave as documented.  No GPU."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pagedkv.h")
+
+
+@pytest.fixture(scope="module")
+def pk():
+    from paged_kv_decode_08_gb300 import build
+
+    build.build_library()
+    from paged_kv_decode_08_gb300 import pagedkv
+
+    return pagedkv
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkv_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_expected_calls():
+    names = declared_functions()
+    for n in ["pkv_append", "pkv_decode", "pkv_decode_splitk", "pkv_splitk_scratch_bytes",
+              "pkv_pick_num_splits", "pkv_status_string", "pkv_last_error",
+              "pkv_read_device_status"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(pk):
+    lib = ctypes.CDLL(pk.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings(pk):
+    for code in (0, -1, -2, -3, -4, 99):
+        s = pk.status_string(code)
+        assert isinstance(s, str) and s
+    assert pk.status_string(-3).startswith("split-K scratch")
+
+
+def test_scratch_bytes(pk):
+    assert pk.pkv_splitk_scratch_bytes(4, 32, 128, 1) == 0
+    assert pk.pkv_splitk_scratch_bytes(0, 32, 128, 4) == 0
+    n = pk.pkv_splitk_scratch_bytes(4, 32, 128, 64)
+    rows = 4 * 32 * 64
+    a = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    assert n == a(rows * 128 * 4) + 2 * a(rows * 4)
+
+
+@pytest.mark.parametrize("args,expect", [
+    # (num_seqs, num_kv_heads, max_context_len, block_size, num_sms) -> splits
+    ((2, 2, 48, 16, 152), 1),          # tiny: too short to split
+    ((32, 8, 2048, 16, 152), 1),       # Llama-3-8B shape: 256 CTAs fit one wave
+    ((4, 8, 131072, 16, 152), 14),     # long context: fill 3 CTAs x 152 SMs
+    ((256, 4, 16384, 32, 152), 8),     # ragged batch: saturated, cap 2048 tokens per CTA
+    ((128, 16, 4352, 16, 152), 3),     # append+decode loop
+    ((1, 1, 1 << 20, 16, 152), 64),    # capped at 64
+    ((0, 8, 2048, 16, 152), 1),        # invalid -> 1
+    ((1, 1, 100, 16, 152), 1),         # shorter than one split's minimum
+])
+def test_pick_num_splits_table(pk, args, expect):
+    assert pk.pkv_pick_num_splits(*args) == expect
+
+
+def test_pick_num_splits_never_leaves_a_split_empty_by_length(pk):
+    for L in (256, 300, 512, 777, 4096, 65536):
+        for base in (1, 4, 32, 300, 2000):
+            s = pk.pkv_pick_num_splits(base, 1, L, 16, 152)
+            assert 1 <= s <= 64
+            assert s <= max(1, L // 256)
+
+
+NULL = None
+F16 = 0x10000  # a fake, 16-byte aligned address; validation rejects before any use
+
+
+def _decode_args(**over):
+    a = dict(q=F16, k=F16, v=F16, bt=F16, cl=F16, B=2, mbps=3, nb=8, scale=0.125, H=4, Hkv=2,
+             D=64, bs=16, out=F16)
+    a.update(over)
+    return a
+
+
+def _call_decode(pk, a):
+    return pk.lib.pkv_decode(a["q"], a["k"], a["v"], a["bt"], a["cl"], a["B"], a["mbps"],
+                             a["nb"], a["scale"], a["H"], a["Hkv"], a["D"], a["bs"], a["out"],
+                             None)
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(q=None), -1),
+    (dict(out=None), -1),
+    (dict(H=6, Hkv=4), -1),          # not a multiple
+    (dict(Hkv=0), -1),
+    (dict(D=96), -2),
+    (dict(bs=8), -2),
+    (dict(H=18, Hkv=2), -2),         # group 9
+    (dict(B=-1), -1),
+    (dict(nb=1 << 28), -1),          # nb * bs overflows int32 slots
+    (dict(k=F16 + 8), -1),           # misaligned cache
+    (dict(q=F16 + 2), -1),           # misaligned q
+    (dict(scale=float("inf")), -1),
+    (dict(mbps=0), -1),
+])
+def test_decode_rejects_bad_arguments_before_cuda(pk, over, status):
+    assert _call_decode(pk, _decode_args(**over)) == status
+    assert pk.last_error()
+
+
+def test_decode_with_no_sequences_is_a_no_op(pk):
+    assert _call_decode(pk, _decode_args(B=0)) == 0
+
+
+def test_splitk_rejects_bad_splits_and_small_scratch(pk):
+    a = _decode_args(B=4, mbps=8192, nb=24576, H=32, Hkv=8, D=128, bs=16)
+    f = pk.lib.pkv_decode_splitk
+    args = [a["q"], a["k"], a["v"], a["bt"], a["cl"], a["B"], a["mbps"], a["nb"], a["scale"],
+            a["H"], a["Hkv"], a["D"], a["bs"], a["out"]]
+    assert f(*args, -1, F16, 1 << 30, None) == -1
+    assert f(*args, 129, F16, 1 << 30, None) == -1
+    assert f(*args, 16, None, 0, None) == -3
+    need = pk.pkv_splitk_scratch_bytes(4, 32, 128, 16)
+    assert f(*args, 16, F16, need - 1, None) == -3
+    assert "needs" in pk.last_error()
+
+
+def test_append_rejects_bad_arguments(pk):
+    f = pk.lib.pkv_append
+    assert f(F16, F16, F16, -1, F16, F16, 8, 16, 2, 64, None) == -1
+    assert f(None, F16, F16, 2, F16, F16, 8, 16, 2, 64, None) == -1
+    assert f(F16, F16, F16, 2, F16, F16, 8, 16, 2, 80, None) == -2
+    assert f(F16, F16, F16, 2, F16, F16, 8, 24, 2, 64, None) == -2
+    assert f(F16 + 4, F16, F16, 2, F16, F16, 8, 16, 2, 64, None) == -1
+    assert f(F16, F16, F16, 0, F16, F16, 8, 16, 2, 64, None) == 0

@@ -1,0 +1,403 @@
+"""Benchmark of the paged-KV decode step on GB300.
+
+One step = one pass of the whole hot path over one batch: ``pkv_append`` of
+each sequence's newest token through its slot, then ``pkv_decode_splitk``
+with the split count from the heuristic (which falls back to the single-pass
+kernel when one wave of CTAs already fills the GPU), on the Llama-3-8B-shaped
+workload (B=32, H=32, Hkv=8, D=128, bs=16, L~U[512,2048], 16384-block pool).
+
+The metric is KV bytes read per second (each token's K and V once, f16),
+with decode tokens/s and microseconds per call alongside.  Four independent
+pool sets (4.3 GB together, far above the 129 MB L2) rotate between steps so
+no step is served from L2.
+
+``--impl reference`` times the CPU oracle (a bounded sample of the same
+workload per step) on the host cores and prints the same JSON line with
+``"impl": "reference"``.
+
+Under ``torchrun`` (N>1) every rank runs its own replica on its own GPU (the
+path has no exchange step); time is the max over ranks and ``value`` counts
+the bytes all ranks processed.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attn: KV HBM GB/s (% of ~8 TB/s), decode tokens/s, \u00b5s/call"
+UNIT = "GB/s"
+NOMINAL_HBM_GBS = 8000.0
+WORKLOAD_DESC = ("Llama-3-8B-shaped decode step: B=32, H=32, Hkv=8, D=128, bs=16, "
+                 "context_lens~U[512,2048], block tables drawn without replacement from a "
+                 "16384-block pool, f16 q/k/v ~N(0,1)")
+N_SETS = 4
+
+# DRAM bytes (read + write) of one decode launch on this workload, from the
+# ncu capture summarised in profiles/ (kernel source hash at capture time).
+# Reported as null when the kernels have changed since.
+NCU_TRAFFIC = {}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("kernels.cuh", "ptx.cuh", "pagedkv.cu"):
+        with open(os.path.join(ROOT, "paged_kv_decode_08_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def cpu_oracle_sample(w, seqs, kc, vc):
+    import oracle
+
+    t0 = time.perf_counter()
+    oracle.decode_fast(w.q, kc, vc, w.block_tables, w.context_lens, w.scale, seqs=seqs)
+    dt = time.perf_counter() - t0
+    per_tok = 2 * w.num_kv_heads * w.head_dim * 2
+    nbytes = sum(int(w.context_lens[s]) for s in seqs) * per_tok
+    return nbytes, dt
+
+
+def cpu_baseline_subprocess(budget_s=12.0):
+    """Time the oracle in a child process pinned to one BLAS/OpenMP thread."""
+    code = (
+        "import sys, json, time; sys.path.insert(0, %r)\n"
+        "import bench\n"
+        "from paged_kv_decode_08_gb300 import workloads as W\n"
+        "w = W.llama8b(); kc, vc = W.host_pool(w)\n"
+        "tot_b = 0; tot_t = 0.0; calls = 0\n"
+        "while tot_t < %f:\n"
+        "    b, t = bench.cpu_oracle_sample(w, list(range(w.num_seqs)), kc, vc)\n"
+        "    tot_b += b; tot_t += t; calls += 1\n"
+        "print(json.dumps({'bytes': tot_b, 'seconds': tot_t, 'calls': calls}))\n"
+    ) % (ROOT, budget_s)
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[k] = "1"
+    res = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
+                         timeout=600)
+    if res.returncode != 0:
+        return None
+    d = json.loads(res.stdout.strip().splitlines()[-1])
+    return {"value": d["bytes"] / d["seconds"] / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{d['calls']} full decode call(s) of the workload (32 sequences, "
+                      f"{d['bytes'] / d['calls'] / 1e6:.0f} MB of K/V each) in float64, "
+                      f"{d['seconds']:.1f} s on one host thread"}
+
+
+def run_reference(args):
+    """The oracle on the host cores, a bounded sample per step."""
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    from paged_kv_decode_08_gb300 import workloads as W
+
+    w = W.llama8b()
+    kc, vc = W.host_pool(w)
+    seqs = list(range(4))
+    for _ in range(args.warmup):
+        cpu_oracle_sample(w, seqs, kc, vc)
+    tot_b, tot_t = 0, 0.0
+    for _ in range(args.steps):
+        b, t = cpu_oracle_sample(w, seqs, kc, vc)
+        tot_b += b
+        tot_t += t
+    value = tot_b / tot_t / 1e9
+    cores = 1  # main() pins BLAS/OpenMP to one thread for this arm
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_t / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD_DESC, "sample_per_step": "4 of the 32 sequences"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": "4 of the 32 sequences per step, float64 numpy oracle, "
+                                   "one host thread"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def build_sets(w, dev, n_sets):
+    """Device pools for the workload: set 0 holds the generator's values, the
+    others the same tables with fresh N(0,1) pools (distinct HBM bytes)."""
+    import torch
+
+    from paged_kv_decode_08_gb300 import workloads as W
+
+    sets = []
+    base = W.to_device(w, dev, upto_last=True)
+    sets.append(base)
+    g = torch.Generator(device=dev)
+    for r in range(1, n_sets):
+        g.manual_seed(1000 + r)
+        kc = torch.randn(base["k_cache"].shape, generator=g, device=dev).to(torch.float16)
+        vc = torch.randn(base["v_cache"].shape, generator=g, device=dev).to(torch.float16)
+        sets.append({**base, "k_cache": kc, "v_cache": vc})
+    return sets
+
+
+def run_ours(args):
+    import torch
+
+    from paged_kv_decode_08_gb300 import pagedkv as pk
+    from paged_kv_decode_08_gb300 import workloads as W
+
+    world, rank, local = dist_setup()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+
+    w = W.llama8b()
+    sets = build_sets(w, dev, N_SETS)
+    k_new, v_new, slots = w.last_token_append()
+    k_new_d = torch.from_numpy(k_new).to(dev)
+    v_new_d = torch.from_numpy(v_new).to(dev)
+    slots_d = torch.from_numpy(slots).to(dev)
+    q, bt, cl = sets[0]["q"], sets[0]["block_tables"], sets[0]["context_lens"]
+    S = pk.splits_for(q, sets[0]["k_cache"], bt, args.splits)
+    scratch = pk.alloc_scratch(q, sets[0]["k_cache"], bt, args.splits)
+    out = torch.empty_like(q)
+    stream = torch.cuda.current_stream()
+    kv_bytes = w.kv_bytes
+    launches_per_step = 1 + (2 if S > 1 else 1)
+
+    def step(i, ev=None):
+        st = sets[i % N_SETS]
+        pk.pkv_append(k_new_d, v_new_d, slots_d, st["k_cache"], st["v_cache"], stream=stream)
+        if ev is not None:
+            ev[0].record(stream)
+        pk.pkv_decode_splitk(q, st["k_cache"], st["v_cache"], bt, cl, w.scale,
+                             num_splits=args.splits, scratch=scratch, out=out, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    flags = pk.pkv_read_device_status()
+    if flags:
+        raise RuntimeError(f"device status flags {flags:#x} after warm-up")
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        t_start.record(stream)
+        for i in range(args.steps):
+            step(i, evs[i])
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    decode_ms = [a.elapsed_time(b) for a, b in evs]
+    if dist is not None:
+        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    # end to end through the public API: pinned host inputs in, result out
+    e2e = None
+    if not args.no_e2e:
+        import numpy as np
+
+        pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+        h_q, h_k, h_v, h_s = pin(w.q), pin(k_new), pin(v_new), pin(slots)
+        h_bt, h_cl = pin(w.block_tables), pin(w.context_lens)
+        h_out = torch.empty(tuple(q.shape), dtype=torch.float16).pin_memory()
+        d_q, d_bt, d_cl = torch.empty_like(q), torch.empty_like(bt), torch.empty_like(cl)
+        h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_s, h_bt, h_cl))
+        d2h = h_out.numel() * h_out.element_size()
+
+        def e2e_step(i):
+            st = sets[i % N_SETS]
+            d_q.copy_(h_q, non_blocking=True)
+            k_new_d.copy_(h_k, non_blocking=True)
+            v_new_d.copy_(h_v, non_blocking=True)
+            slots_d.copy_(h_s, non_blocking=True)
+            d_bt.copy_(h_bt, non_blocking=True)
+            d_cl.copy_(h_cl, non_blocking=True)
+            pk.pkv_append(k_new_d, v_new_d, slots_d, st["k_cache"], st["v_cache"], stream=stream)
+            pk.pkv_decode_splitk(d_q, st["k_cache"], st["v_cache"], d_bt, d_cl, w.scale,
+                                 num_splits=args.splits, scratch=scratch, out=out, stream=stream)
+            h_out.copy_(out, non_blocking=True)
+
+        for i in range(args.warmup):
+            e2e_step(i)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(args.steps):
+            e2e_step(i)
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = a.elapsed_time(b)
+        if dist is not None:
+            t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": world * kv_bytes * args.steps / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e2e_ms / args.steps}
+
+    flags = pk.pkv_read_device_status()
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+    ms_per_step = total_ms / args.steps
+    value = world * kv_bytes / (ms_per_step * 1e-3) / 1e9
+    dec_avg_ms = statistics.fmean(decode_ms)
+    achieved = kv_bytes / (dec_avg_ms * 1e-3) / 1e9
+    peak, peak_kind = measured_peaks()
+    traffic = None
+    tr = NCU_TRAFFIC.get("llama8b")
+    if tr and tr.get("kernel_hash") == kernel_source_hash():
+        traffic = tr["bytes_per_launch"]
+    cpu = None if args.no_cpu_baseline else cpu_baseline_subprocess()
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": {"workload": WORKLOAD_DESC, "step": "pkv_append (32 tokens) + "
+                   "pkv_decode_splitk (heuristic)", "num_splits": S,
+                   "l2": f"{N_SETS} rotating pool sets ({N_SETS * 2 * sets[0]['k_cache'].numel() * 2 / 1e9:.1f} GB) "
+                         "> 129 MB L2",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "kv_bytes_per_step": kv_bytes,
+        "decode_tokens_per_s": world * w.num_seqs / (ms_per_step * 1e-3),
+        "us_per_step": ms_per_step * 1e3,
+        "decode_us_per_call": {"mean": dec_avg_ms * 1e3, "median": statistics.median(decode_ms) * 1e3,
+                               "min": min(decode_ms) * 1e3},
+        "pct_of_8TBs": 100.0 * achieved / NOMINAL_HBM_GBS,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": peak_kind,
+                     "kernel": "decode call (phase 1 + combine when split)",
+                     "traffic": traffic},
+        "clocks": clocks.summary(),
+        "gpu_launches": launches_per_step * args.steps,
+        "device_status_flags": flags,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--splits", type=int, default=0, help="0 = heuristic")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+            os.environ[k] = "1"  # before numpy is first imported
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -62,8 +62,10 @@ typedef int32_t pkv_status;
 #define PKV_DEV_BAD_BLOCK_ID 0x2u    /* decode: table entry outside [0,num_blocks); block skipped */
 #define PKV_DEV_BAD_CONTEXT_LEN 0x4u /* decode: context_len < 0 (taken as 0) or above
                                         max_blocks_per_seq*block_size (clamped) */
-#define PKV_DEV_WAIT_TIMEOUT 0x8u    /* decode: a tile copy did not land within ~2 s;
-                                        the affected outputs were not written */
+#define PKV_DEV_WAIT_TIMEOUT 0x8u    /* decode: a tile copy did not land within 100 ms;
+                                        the affected outputs were not written, and
+                                        decode calls write nothing until the word
+                                        is cleared by pkv_read_device_status */
 
 /* Largest num_splits pkv_decode_splitk accepts. */
 #define PKV_MAX_SPLITS 128

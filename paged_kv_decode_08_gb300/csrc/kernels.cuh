@@ -41,8 +41,9 @@ constexpr unsigned int kDevBadBlockId = 0x2u;
 constexpr unsigned int kDevBadContextLen = 0x4u;
 constexpr unsigned int kDevWaitTimeout = 0x8u;
 
-// A tile copy that has not landed after this long is reported, not awaited.
-constexpr uint64_t kWaitLimitNs = 2000000000ull;
+// A tile copy that has not landed after this long is reported, not awaited
+// (a real copy takes microseconds).
+constexpr uint64_t kWaitLimitNs = 100000000ull;
 
 // ---------------------------------------------------------------------------
 // append
@@ -147,6 +148,10 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   if (SPLIT) item /= p.num_splits;
   const int g = item % p.num_kv_heads;
   const int s = item / p.num_kv_heads;
+
+  // After a lost copy has been flagged, later CTAs do no work (and write
+  // nothing) until the host reads and clears the status word.
+  if (*reinterpret_cast<volatile unsigned int*>(&g_device_status) & kDevWaitTimeout) return;
 
   const int cap = p.max_blocks_per_seq * BS;
   int L = __ldg(p.context_lens + s);

@@ -1,0 +1,303 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Append is compared bit for bit; attention within |gpu-ref| <= 2e-3 + 1e-2|ref|
+(see tests/tolerance.py).  Inputs come from the seeded generator; unused pool
+blocks, rows past a sequence's length and table entries past its blocks all
+hold or point at NaN, so a stray read shows up as NaN.
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+from paged_kv_decode_08_gb300 import workloads as W
+from tests.tolerance import assert_attention_close, assert_bits_equal
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def pk(cuda_device):
+    from paged_kv_decode_08_gb300 import pagedkv
+
+    pagedkv.pkv_read_device_status()  # start from a clean status word
+    return pagedkv
+
+
+_CACHE = {}
+
+
+def workload(name):
+    if name not in _CACHE:
+        w = W.make(name)
+        kc, vc = W.host_pool(w)
+        ref = oracle.decode_fast(w.q, kc, vc, w.block_tables, w.context_lens, w.scale)
+        del kc, vc
+        _CACHE[name] = (w, ref)
+    return _CACHE[name]
+
+
+def to_np(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def appended_device(pk, w, dev):
+    """Device pools without each sequence's newest token, then pkv_append it."""
+    d = W.to_device(w, dev, upto_last=True)
+    k_new, v_new, slots = w.last_token_append()
+    pk.pkv_append(torch.from_numpy(k_new).to(dev), torch.from_numpy(v_new).to(dev),
+                  torch.from_numpy(slots).to(dev), d["k_cache"], d["v_cache"])
+    return d
+
+
+def decode_all(pk, w, d, splits):
+    """{label: output} for single pass and the requested split counts."""
+    outs = {"single": pk.pkv_decode(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                                    d["context_lens"], w.scale)}
+    for S in splits:
+        outs[f"splitk{S}"] = pk.pkv_decode_splitk(d["q"], d["k_cache"], d["v_cache"],
+                                                  d["block_tables"], d["context_lens"], w.scale,
+                                                  num_splits=S)
+    torch.cuda.synchronize()
+    return {k: to_np(v) for k, v in outs.items()}
+
+
+# ---------------------------------------------------------------------------
+# append
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["tiny", "llama8b"])
+def test_append_is_bit_exact(pk, cuda_device, name):
+    w, _ = workload(name)
+    d = appended_device(pk, w, cuda_device)
+    ids, kb, vb = W.compact_blocks(w, upto_last=False)
+    idx = torch.from_numpy(ids).to(cuda_device)
+    got_k = d["k_cache"].index_select(0, idx).cpu().numpy()
+    got_v = d["v_cache"].index_select(0, idx).cpu().numpy()
+    # expected: the oracle's scatter applied to the host pool without the token
+    hk, hv = W.host_pool(w, upto_last=True)
+    k_new, v_new, slots = w.last_token_append()
+    assert oracle.append(k_new, v_new, slots, hk, hv) == []
+    assert_bits_equal(got_k, hk[ids], f"{name} K")
+    assert_bits_equal(got_v, hv[ids], f"{name} V")
+    assert pk.pkv_read_device_status() == 0
+
+
+def test_append_skips_padding_and_flags_bad_slots(pk, cuda_device):
+    w, _ = workload("tiny")
+    d = W.to_device(w, cuda_device)
+    before_k = d["k_cache"].clone()
+    before_v = d["v_cache"].clone()
+    T = 3
+    k = torch.ones((T, w.num_kv_heads, w.head_dim), dtype=torch.float16, device=cuda_device)
+    slots = torch.tensor([-1, -5, w.num_blocks * w.block_size], dtype=torch.int32,
+                         device=cuda_device)
+    pk.pkv_append(k, k, slots, d["k_cache"], d["v_cache"])
+    flags = pk.pkv_read_device_status()
+    assert flags & pk.PKV_DEV_BAD_SLOT
+    assert torch.equal(d["k_cache"].view(torch.int16), before_k.view(torch.int16))
+    assert torch.equal(d["v_cache"].view(torch.int16), before_v.view(torch.int16))
+
+
+# ---------------------------------------------------------------------------
+# decode parity on the workloads
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name,splits", [
+    ("tiny", [0, 2, 3]),
+    ("llama8b", [0, 2, 4, 16]),
+    ("long", [0, 4, 16, 64]),
+    ("ragged", [0, 3, 8]),
+])
+def test_decode_matches_oracle(pk, cuda_device, name, splits):
+    w, ref = workload(name)
+    d = appended_device(pk, w, cuda_device)
+    outs = decode_all(pk, w, d, splits)
+    for label, got in outs.items():
+        assert_attention_close(got, ref, f"{name}/{label}")
+    assert pk.pkv_read_device_status() == 0
+
+
+def test_heuristic_split_counts(pk, cuda_device):
+    sms = torch.cuda.get_device_properties(cuda_device).multi_processor_count
+    for name in ["tiny", "llama8b", "long", "ragged"]:
+        w, _ = workload(name)
+        S = pk.pkv_pick_num_splits(w.num_seqs, w.num_kv_heads,
+                                   w.max_blocks_per_seq * w.block_size, w.block_size, sms)
+        assert 1 <= S <= 64
+    w, _ = workload("long")
+    assert pk.pkv_pick_num_splits(4, 8, 131072, 16, sms) > 1
+
+
+def test_context_len_one_is_exact(pk, cuda_device):
+    """One token: its softmax weight is exactly 1, so the f16 output is that V
+    row bit for bit, in the single-pass and split-K kernels alike."""
+    w = W.small_random(41, num_seqs=6, num_heads=14, num_kv_heads=2, head_dim=128,
+                       block_size=32, lens=[1, 1, 33, 1, 64, 1])
+    d = appended_device(pk, w, cuda_device)
+    for S in (1, 2):
+        out = pk.pkv_decode_splitk(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                                   d["context_lens"], w.scale, num_splits=S).cpu().numpy()
+        for s in range(w.num_seqs):
+            if int(w.context_lens[s]) != 1:
+                continue
+            for h in range(w.num_heads):
+                exp = w.seq_v[s][0, h // w.group]
+                assert np.array_equal(out[s, h].view(np.uint16), exp.view(np.uint16)), (S, s, h)
+
+
+@pytest.mark.parametrize("D,bs,G", [(64, 16, 1), (64, 32, 3), (128, 16, 5), (128, 32, 8),
+                                    (64, 16, 8), (128, 16, 2)])
+def test_ragged_small_shapes(pk, cuda_device, D, bs, G):
+    lens = [1, bs - 1, bs, bs + 1, 5 * bs + 3, 37, 300]
+    w = W.small_random(1000 + D + bs + G, num_seqs=len(lens), num_heads=2 * G, num_kv_heads=2,
+                       head_dim=D, block_size=bs, lens=lens)
+    kc, vc = W.host_pool(w)
+    ref = oracle.decode(w.q, kc, vc, w.block_tables, w.context_lens, w.scale)
+    d = appended_device(pk, w, cuda_device)
+    for label, got in decode_all(pk, w, d, [0, 2, 5, 128]).items():
+        assert_attention_close(got, ref, f"D{D} bs{bs} G{G} {label}")
+
+
+def test_empty_context_gives_zeros(pk, cuda_device):
+    w = W.small_random(51, num_seqs=3, num_heads=4, num_kv_heads=2, head_dim=64, block_size=16,
+                       lens=[20, 1, 40])
+    kc, vc = W.host_pool(w)
+    d = W.to_device(w, cuda_device)
+    lens = w.context_lens.copy()
+    lens[1] = 0
+    d["context_lens"] = torch.from_numpy(lens).to(cuda_device)
+    ref = oracle.decode(w.q, kc, vc, w.block_tables, lens, w.scale)
+    for label, got in decode_all(pk, w, d, [2]).items():
+        assert np.all(got[1] == 0.0), label
+        assert_attention_close(got, ref, label)
+
+
+def test_scale_zero_gives_mean_of_v(pk, cuda_device):
+    w = W.small_random(61, num_seqs=2, num_heads=8, num_kv_heads=2, head_dim=128, block_size=16,
+                       lens=[100, 17])
+    d = W.to_device(w, cuda_device)
+    got = to_np(pk.pkv_decode(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                              d["context_lens"], 0.0))
+    for s in range(2):
+        mean = w.seq_v[s].astype(np.float64).mean(axis=0)
+        for h in range(8):
+            assert_attention_close(got[s, h], mean[h // 4], f"seq {s} head {h}")
+
+
+# ---------------------------------------------------------------------------
+# bad device data is skipped and flagged, never dereferenced
+# ---------------------------------------------------------------------------
+
+def test_bad_block_id_is_skipped_and_flagged(pk, cuda_device):
+    w = W.small_random(71, num_seqs=2, num_heads=4, num_kv_heads=2, head_dim=64, block_size=16,
+                       lens=[48, 40])
+    kc, vc = W.host_pool(w)
+    ref = oracle.decode(w.q, kc, vc, w.block_tables, w.context_lens, w.scale)
+    d = W.to_device(w, cuda_device)
+    tables = w.block_tables.copy()
+    tables[0, 1] = w.num_blocks + 5  # out of range: tokens 16..31 of sequence 0 are skipped
+    d["block_tables"] = torch.from_numpy(tables).to(cuda_device)
+    for S in (1, 3):
+        out = to_np(pk.pkv_decode_splitk(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                                         d["context_lens"], w.scale, num_splits=S))
+        assert pk.pkv_read_device_status() & pk.PKV_DEV_BAD_BLOCK_ID
+        assert np.all(np.isfinite(out))
+        assert_attention_close(out[1], ref[1], "untouched sequence")
+        # sequence 0 equals attention over its remaining 32 tokens
+        keep = [i for i in range(48) if not 16 <= i < 32]
+        K = w.seq_k[0][keep].astype(np.float64)
+        V = w.seq_v[0][keep].astype(np.float64)
+        for h in range(4):
+            z = w.scale * K[:, h // 2] @ w.q[0, h].astype(np.float64)
+            p = np.exp(z - z.max())
+            p /= p.sum()
+            assert_attention_close(out[0, h], p @ V[:, h // 2], f"S={S} head {h}")
+
+
+def test_context_len_above_capacity_is_clamped_and_flagged(pk, cuda_device):
+    w = W.small_random(81, num_seqs=2, num_heads=2, num_kv_heads=1, head_dim=64, block_size=16,
+                       lens=[32, 10])
+    kc, vc = W.host_pool(w)
+    ref = oracle.decode(w.q, kc, vc, w.block_tables, w.context_lens, w.scale)
+    d = W.to_device(w, cuda_device)
+    lens = w.context_lens.copy()
+    lens[0] = 10 ** 6  # capacity is 2 blocks * 16 = 32 tokens, the real length
+    d["context_lens"] = torch.from_numpy(lens).to(cuda_device)
+    out = to_np(pk.pkv_decode(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                              d["context_lens"], w.scale))
+    assert pk.pkv_read_device_status() & pk.PKV_DEV_BAD_CONTEXT_LEN
+    assert_attention_close(out, ref, "clamped")
+
+
+# ---------------------------------------------------------------------------
+# the append+decode loop (128 steps on one stream)
+# ---------------------------------------------------------------------------
+
+def test_append_decode_loop(pk, cuda_device):
+    loop = W.AppendDecodeLoop()
+    w0 = loop.initial_workload()
+    d = W.to_device(w0, cuda_device)
+    kc, vc = d["k_cache"], d["v_cache"]
+    hk, hv = W.host_pool(w0)
+    sample = {0, 63, 127} | set(int(x) for x in np.random.default_rng(5).choice(128, 3, False))
+    stream = torch.cuda.current_stream()
+    outs = {}
+    for t in range(loop.steps):
+        st = loop.step(t)
+        k_new = torch.from_numpy(st.k_new).to(cuda_device)
+        v_new = torch.from_numpy(st.v_new).to(cuda_device)
+        slots = torch.from_numpy(st.slot_mapping).to(cuda_device)
+        q = torch.from_numpy(st.q).to(cuda_device)
+        bt = torch.from_numpy(st.block_tables).to(cuda_device)
+        cl = torch.from_numpy(st.context_lens).to(cuda_device)
+        pk.pkv_append(k_new, v_new, slots, kc, vc, stream=stream)
+        out = pk.pkv_decode_splitk(q, kc, vc, bt, cl, loop.scale, stream=stream)
+        assert oracle.append(st.k_new, st.v_new, st.slot_mapping, hk, hv) == []
+        if t in sample:
+            single = pk.pkv_decode(q, kc, vc, bt, cl, loop.scale, stream=stream)
+            ref = oracle.decode_fast(st.q, hk, hv, st.block_tables, st.context_lens, loop.scale)
+            outs[t] = (to_np(out), to_np(single), ref)
+    for t, (split, single, ref) in sorted(outs.items()):
+        assert_attention_close(split, ref, f"step {t} split-K")
+        assert_attention_close(single, ref, f"step {t} single pass")
+    owned = np.unique(loop.tables[-1][loop.tables[-1] != loop.poison_block])
+    idx = torch.from_numpy(owned.astype(np.int64)).to(cuda_device)
+    assert_bits_equal(kc.index_select(0, idx).cpu().numpy(), hk[owned], "K pool after 128 steps")
+    assert_bits_equal(vc.index_select(0, idx).cpu().numpy(), hv[owned], "V pool after 128 steps")
+    assert pk.pkv_read_device_status() == 0
+
+
+# ---------------------------------------------------------------------------
+# graphs and streams
+# ---------------------------------------------------------------------------
+
+def test_append_and_decode_replay_from_a_cuda_graph(pk, cuda_device):
+    w, ref = workload("llama8b")
+    d = W.to_device(w, cuda_device, upto_last=True)
+    k_new, v_new, slots = w.last_token_append()
+    k_new = torch.from_numpy(k_new).to(cuda_device)
+    v_new = torch.from_numpy(v_new).to(cuda_device)
+    slots = torch.from_numpy(slots).to(cuda_device)
+    out = torch.empty_like(d["q"])
+    scratch = pk.alloc_scratch(d["q"], d["k_cache"], d["block_tables"], 4)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):  # warm-up outside capture
+        pk.pkv_append(k_new, v_new, slots, d["k_cache"], d["v_cache"])
+        pk.pkv_decode_splitk(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                             d["context_lens"], w.scale, num_splits=4, scratch=scratch, out=out)
+    torch.cuda.current_stream().wait_stream(s)
+    out.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        pk.pkv_append(k_new, v_new, slots, d["k_cache"], d["v_cache"])
+        pk.pkv_decode_splitk(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                             d["context_lens"], w.scale, num_splits=4, scratch=scratch, out=out)
+    for _ in range(3):
+        out.zero_()
+        g.replay()
+    torch.cuda.synchronize()
+    assert_attention_close(to_np(out), ref, "graph replay")

@@ -241,7 +241,7 @@ def test_append_decode_loop(pk, cuda_device):
     w0 = loop.initial_workload()
     d = W.to_device(w0, cuda_device)
     kc, vc = d["k_cache"], d["v_cache"]
-    hk, hv = W.host_pool(w0)
+    hk, hv = W.host_pool(w0, fill=np.nan)  # unused blocks are NaN on the device too
     sample = {0, 63, 127} | set(int(x) for x in np.random.default_rng(5).choice(128, 3, False))
     stream = torch.cuda.current_stream()
     outs = {}

@@ -42,7 +42,7 @@ NOMINAL_HBM_GBS = 8000.0
 WORKLOAD_DESC = ("Llama-3-8B-shaped decode step: B=32, H=32, Hkv=8, D=128, bs=16, "
                  "context_lens~U[512,2048], block tables drawn without replacement from a "
                  "16384-block pool, f16 q/k/v ~N(0,1)")
-N_SETS = 4
+N_SETS = 4  # default number of rotating pool sets (--sets)
 
 # DRAM bytes (read + write) of one decode launch on this workload, from the
 # ncu capture summarised in profiles/ (kernel source hash at capture time).
@@ -238,7 +238,8 @@ def run_ours(args):
     torch.cuda.set_device(dev)
 
     w = W.llama8b()
-    sets = build_sets(w, dev, N_SETS)
+    n_sets = args.sets
+    sets = build_sets(w, dev, n_sets)
     k_new, v_new, slots = w.last_token_append()
     k_new_d = torch.from_numpy(k_new).to(dev)
     v_new_d = torch.from_numpy(v_new).to(dev)
@@ -252,7 +253,7 @@ def run_ours(args):
     launches_per_step = 1 + (2 if S > 1 else 1)
 
     def step(i, ev=None):
-        st = sets[i % N_SETS]
+        st = sets[i % n_sets]
         pk.pkv_append(k_new_d, v_new_d, slots_d, st["k_cache"], st["v_cache"], stream=stream)
         if ev is not None:
             ev[0].record(stream)
@@ -304,7 +305,7 @@ def run_ours(args):
         d2h = h_out.numel() * h_out.element_size()
 
         def e2e_step(i):
-            st = sets[i % N_SETS]
+            st = sets[i % n_sets]
             d_q.copy_(h_q, non_blocking=True)
             k_new_d.copy_(h_k, non_blocking=True)
             v_new_d.copy_(h_v, non_blocking=True)
@@ -355,8 +356,8 @@ def run_ours(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
         "config": {"workload": WORKLOAD_DESC, "step": "pkv_append (32 tokens) + "
                    "pkv_decode_splitk (heuristic)", "num_splits": S,
-                   "l2": f"{N_SETS} rotating pool sets ({N_SETS * 2 * sets[0]['k_cache'].numel() * 2 / 1e9:.1f} GB) "
-                         "> 129 MB L2",
+                   "l2": f"{n_sets} rotating pool set(s) ({n_sets * 2 * sets[0]['k_cache'].numel() * 2 / 1e9:.1f} GB; "
+                         f"{kv_bytes / 1e6:.0f} MB of K/V read per step) vs 129 MB L2",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "kv_bytes_per_step": kv_bytes,
         "decode_tokens_per_s": world * w.num_seqs / (ms_per_step * 1e-3),
@@ -386,6 +387,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--splits", type=int, default=0, help="0 = heuristic")
+    ap.add_argument("--sets", type=int, default=N_SETS, help="rotating pool sets")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

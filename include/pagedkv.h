@@ -172,6 +172,39 @@ int32_t pkv_pick_num_splits(int32_t num_seqs, int32_t num_kv_heads,
                             int32_t max_context_len, int32_t block_size,
                             int32_t num_sms);
 
+/*
+ * pkv_decode_splitk_noalloc — pkv_decode_splitk without caller scratch and
+ * without any allocation, for callers that cannot allocate device memory: a
+ * plugin or extension whose host hands it only the input and output buffers
+ * and owns every allocation itself, or a decode loop under a latency budget
+ * where cudaMalloc (which can block and synchronize the device) is not
+ * allowed.  The pages have no counterpart; it is an addition of this library.
+ *
+ * The split-K partials live in one static device buffer of
+ * PKV_NOALLOC_SCRATCH_BYTES that the library declares; every GPU that loads
+ * the library holds it until the process exits.  The first call on a device
+ * looks up that buffer's device address (cudaGetSymbolAddress, with the
+ * device current) and caches it; make that first call before any stream
+ * capture.  Nothing in the buffer needs to start at zero: phase 1 writes
+ * every partial the combine reads.  All calls share the one buffer, which
+ * keeps the last call's contents, so calls that may overlap on the GPU (on
+ * different streams, or from different host threads) race and must not be
+ * issued; calls on one stream are ordered and safe.
+ *
+ * Arguments and result are those of pkv_decode_splitk (num_splits 0 = the
+ * heuristic, 1 = single pass).  Returns PKV_ERR_SCRATCH_TOO_SMALL, before any
+ * launch, when the partials for the chosen split count need more than
+ * PKV_NOALLOC_SCRATCH_BYTES (pkv_splitk_scratch_bytes gives the need); call
+ * pkv_decode_splitk with caller-owned scratch, or fewer splits, instead.
+ */
+#define PKV_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
+pkv_status pkv_decode_splitk_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                     const int32_t* block_tables, const int32_t* context_lens,
+                                     int32_t num_seqs, int32_t max_blocks_per_seq,
+                                     int32_t num_blocks, float scale, int32_t num_heads,
+                                     int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                     void* out, int32_t num_splits, void* stream);
+
 /* Static text for a status code (never NULL). */
 const char* pkv_status_string(pkv_status status);
 

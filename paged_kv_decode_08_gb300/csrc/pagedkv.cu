@@ -396,3 +396,78 @@ pkv_status pkv_read_device_status(int32_t* flags, void* stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// pkv_decode_splitk_noalloc: split-K with a built-in static scratch buffer,
+// for callers that cannot allocate device memory (see include/pagedkv.h).
+// ---------------------------------------------------------------------------
+
+namespace pkv {
+namespace {
+
+// The built-in split-K scratch.  In host code this name is only a stand-in
+// for the device array: its device address comes from cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[PKV_NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[64] = {};  // per device ordinal, filled on first use
+
+// Device address of g_noalloc_scratch on the current device.
+pkv_status noalloc_scratch(void** ptr) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (dev >= 0 && dev < 64 && g_noalloc_ptr[dev]) {
+    *ptr = g_noalloc_ptr[dev];
+    return PKV_OK;
+  }
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  if (e != cudaSuccess || !p) return cuda_fail(e, "cudaGetSymbolAddress(built-in scratch)");
+  if (dev >= 0 && dev < 64) g_noalloc_ptr[dev] = p;
+  *ptr = p;
+  return PKV_OK;
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" pkv_status pkv_decode_splitk_noalloc(
+    const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+    const int32_t* context_lens, int32_t num_seqs, int32_t max_blocks_per_seq, int32_t num_blocks,
+    float scale, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+    void* out, int32_t num_splits, void* stream) {
+  const DecodeArgs a{q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                     max_blocks_per_seq, num_blocks, scale, num_heads, num_kv_heads,
+                     head_dim, block_size, out};
+  pkv_status st = validate_decode(a);
+  if (st != PKV_OK) return st;
+  if (num_splits < 0 || num_splits > PKV_MAX_SPLITS)
+    return fail(PKV_ERR_INVALID_ARG, "num_splits %d outside 0..%d", num_splits, PKV_MAX_SPLITS);
+  if (num_seqs == 0) return PKV_OK;
+
+  // The split count pkv_decode_splitk will use, and the scratch it needs.
+  int S = num_splits;
+  if (S == 0) {
+    int sms = 0;
+    if (current_device_sms(&sms) != 0) return fail(PKV_ERR_CUDA, "cannot query the SM count");
+    S = pkv_pick_num_splits(num_seqs, num_kv_heads, max_blocks_per_seq * block_size, block_size, sms);
+  }
+  const int chunk_blocks = (max_blocks_per_seq + S - 1) / S;
+  const int S_eff = (max_blocks_per_seq + chunk_blocks - 1) / chunk_blocks;
+  const size_t need = pkv_splitk_scratch_bytes(num_seqs, num_heads, head_dim, S_eff);
+  if (need > (size_t)PKV_NOALLOC_SCRATCH_BYTES)
+    return fail(PKV_ERR_SCRATCH_TOO_SMALL,
+                "%d splits need %zu bytes of scratch but the built-in buffer holds %zu; use "
+                "pkv_decode_splitk with caller scratch or fewer splits",
+                S_eff, need, (size_t)PKV_NOALLOC_SCRATCH_BYTES);
+
+  void* scratch = nullptr;
+  st = noalloc_scratch(&scratch);
+  if (st != PKV_OK) return st;
+  return pkv_decode_splitk(q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                           max_blocks_per_seq, num_blocks, scale, num_heads, num_kv_heads,
+                           head_dim, block_size, out, S, scratch,
+                           (size_t)PKV_NOALLOC_SCRATCH_BYTES, stream);
+}

@@ -30,6 +30,7 @@ PKV_DEV_BAD_CONTEXT_LEN = 0x4
 PKV_DEV_WAIT_TIMEOUT = 0x8
 
 PKV_MAX_SPLITS = 128
+PKV_NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
 
 
 class PagedKVError(RuntimeError):
@@ -52,6 +53,9 @@ def _load():
     lib.pkv_decode_splitk.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, f32, i32, i32, i32, i32,
                                       vp, i32, vp, sz, vp]
     lib.pkv_decode_splitk.restype = i32
+    lib.pkv_decode_splitk_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, f32, i32, i32,
+                                              i32, i32, vp, i32, vp]
+    lib.pkv_decode_splitk_noalloc.restype = i32
     lib.pkv_splitk_scratch_bytes.argtypes = [i32, i32, i32, i32]
     lib.pkv_splitk_scratch_bytes.restype = sz
     lib.pkv_pick_num_splits.argtypes = [i32, i32, i32, i32, i32]
@@ -202,6 +206,25 @@ def pkv_decode_splitk(q, k_cache, v_cache, block_tables, context_lens, scale, nu
                                  float(scale), H, Hkv, D, bs, out.data_ptr(), int(num_splits),
                                  scratch.data_ptr(), scratch.numel(), _stream_ptr(stream)),
            "pkv_decode_splitk")
+    return out
+
+
+def pkv_decode_splitk_noalloc(q, k_cache, v_cache, block_tables, context_lens, scale, out,
+                              num_splits=0, stream=None):
+    """Split-K decode that allocates nothing: the partials go to the library's
+    built-in static device buffer (PKV_NOALLOC_SCRATCH_BYTES) instead of caller
+    scratch, and ``out`` must be given.  For callers that may not allocate
+    device memory; calls that can overlap on the GPU share that buffer and
+    must not be issued."""
+    if out is None:
+        raise ValueError("pkv_decode_splitk_noalloc needs a caller-provided out")
+    B, H, D, NB, Hkv, bs, mbps, out = _decode_shapes(q, k_cache, v_cache, block_tables,
+                                                     context_lens, out)
+    _check(lib.pkv_decode_splitk_noalloc(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                         block_tables.data_ptr(), context_lens.data_ptr(), B,
+                                         mbps, NB, float(scale), H, Hkv, D, bs, out.data_ptr(),
+                                         int(num_splits), _stream_ptr(stream)),
+           "pkv_decode_splitk_noalloc")
     return out
 
 

@@ -143,3 +143,13 @@ def test_append_rejects_bad_arguments(pk):
     assert f(F16, F16, F16, 2, F16, F16, 8, 24, 2, 64, None) == -2
     assert f(F16 + 4, F16, F16, 2, F16, F16, 8, 16, 2, 64, None) == -1
     assert f(F16, F16, F16, 0, F16, F16, 8, 16, 2, 64, None) == 0
+
+
+def test_noalloc_rejects_oversized_requests_before_any_cuda_call(pk):
+    # 256 sequences x 32 heads x 64 splits x 128 dims of f32 partials: 268 MB,
+    # far beyond the built-in buffer; rejected on the host, nothing launched.
+    f = pk.lib.pkv_decode_splitk_noalloc
+    st = f(F16, F16, F16, F16, F16, 256, 8192, 24576, 0.1, 32, 8, 128, 16, F16, 64, None)
+    assert st == pk.PKV_ERR_SCRATCH_TOO_SMALL
+    assert "built-in buffer" in pk.last_error()
+    assert f(F16, F16, F16, F16, F16, 2, 3, 8, 0.1, 4, 2, 64, 16, F16, -1, None) == -1

@@ -39,9 +39,18 @@ if ROOT not in sys.path:
 METRIC = "paged decode attn: KV HBM GB/s (% of ~8 TB/s), decode tokens/s, \u00b5s/call"
 UNIT = "GB/s"
 NOMINAL_HBM_GBS = 8000.0
-WORKLOAD_DESC = ("Llama-3-8B-shaped decode step: B=32, H=32, Hkv=8, D=128, bs=16, "
-                 "context_lens~U[512,2048], block tables drawn without replacement from a "
-                 "16384-block pool, f16 q/k/v ~N(0,1)")
+WORKLOAD_DESC = {
+    "llama8b": ("Llama-3-8B-shaped decode step: B=32, H=32, Hkv=8, D=128, bs=16, "
+                "context_lens~U[512,2048], block tables drawn without replacement from a "
+                "16384-block pool, f16 q/k/v ~N(0,1)"),
+    "long": ("long-context split-K decode: B=4, H=32, Hkv=8, D=128, bs=16, context_lens "
+             "{32768,65536,98304,131072}, one key per sequence x8, 24576-block pool"),
+    "ragged": ("large ragged batch: B=256, H=28, Hkv=4, D=128, bs=32, lognormal context_lens "
+               "(median 1024, sigma 1, clipped to [1,16384], 8 of length 1), 200000-block pool, "
+               "f16 q/k/v ~N(0,0.5)"),
+    "tiny": ("tiny paged decode: B=2, H=4, Hkv=2, D=64, bs=16, context_lens {17,40}, "
+             "8-block pool"),
+}
 N_SETS = 4  # default number of rotating pool sets (--sets)
 
 # DRAM bytes (read + write) of one decode launch on this workload, from the
@@ -194,7 +203,7 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_t / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD_DESC, "sample_per_step": "4 of the 32 sequences"},
+        "config": {"workload": WORKLOAD_DESC["llama8b"], "sample_per_step": "4 of the 32 sequences"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": "4 of the 32 sequences per step, float64 numpy oracle, "
                                    "one host thread"},
@@ -237,7 +246,7 @@ def run_ours(args):
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
 
-    w = W.llama8b()
+    w = W.make(args.workload)
     n_sets = args.sets
     sets = build_sets(w, dev, n_sets)
     k_new, v_new, slots = w.last_token_append()
@@ -354,8 +363,10 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
-        "config": {"workload": WORKLOAD_DESC, "step": "pkv_append (32 tokens) + "
-                   "pkv_decode_splitk (heuristic)", "num_splits": S,
+        "config": {"workload": WORKLOAD_DESC[args.workload],
+                   "step": f"pkv_append ({w.num_seqs} tokens) + pkv_decode_splitk "
+                           f"({'heuristic' if args.splits == 0 else 'forced'})",
+                   "num_splits": S,
                    "l2": f"{n_sets} rotating pool set(s) ({n_sets * 2 * sets[0]['k_cache'].numel() * 2 / 1e9:.1f} GB; "
                          f"{kv_bytes / 1e6:.0f} MB of K/V read per step) vs 129 MB L2",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
@@ -388,6 +399,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--splits", type=int, default=0, help="0 = heuristic")
     ap.add_argument("--sets", type=int, default=N_SETS, help="rotating pool sets")
+    ap.add_argument("--workload", choices=sorted(WORKLOAD_DESC), default="llama8b")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -55,6 +55,8 @@ def build_library(force=False, verbose=False, extra=()):
 
 
 if __name__ == "__main__":
-    build_library(force="--force" in sys.argv, verbose=True,
-                  extra=["-Xptxas", "-v"] if "--ptxas-v" in sys.argv else [])
+    extra = [a for a in sys.argv[1:] if a.startswith("-D")]
+    if "--ptxas-v" in sys.argv:
+        extra += ["-Xptxas", "-v"]
+    build_library(force="--force" in sys.argv, verbose=True, extra=extra)
     print(LIB)

@@ -19,11 +19,24 @@
 #include "kernels.cuh"
 #include "pagedkv.h"
 
+// Warps per decode CTA and the shared-memory ring they split (KB); the
+// defaults give three resident CTAs per SM.  Overridable at build time.
+#ifndef PKV_DECODE_WARPS
+#define PKV_DECODE_WARPS 4
+#endif
+#ifndef PKV_DECODE_RING_KB
+#define PKV_DECODE_RING_KB 64
+#endif
+#ifndef PKV_CTAS_PER_SM
+#define PKV_CTAS_PER_SM 3
+#endif
+
+
 namespace pkv {
 namespace {
 
-// Resident decode CTAs per SM the kernels are sized for (64 KB ring each).
-constexpr int kCtasPerSm = 3;
+// Resident decode CTAs per SM the kernels are sized for.
+constexpr int kCtasPerSm = PKV_CTAS_PER_SM;
 // With the base grid already filling the GPU, a CTA keeps at most this many
 // tokens, so one long context does not leave a long serial tail.
 constexpr int kSaturatedChunkTokens = 2048;
@@ -148,9 +161,11 @@ pkv_status validate_decode(const DecodeArgs& a) {
 
 template <int D, int BS>
 struct Tuning {
-  static constexpr int W = 4;
+  static constexpr int W = PKV_DECODE_WARPS;
   static constexpr int kStage = 2 * BS * D * 2;
-  static constexpr int P = (64 * 1024) / (W * kStage) > 0 ? (64 * 1024) / (W * kStage) : 1;
+  static constexpr int P = (PKV_DECODE_RING_KB * 1024) / (W * kStage) > 0
+                               ? (PKV_DECODE_RING_KB * 1024) / (W * kStage)
+                               : 1;
 };
 
 template <int D, int BS, bool SPLIT>

@@ -69,6 +69,10 @@ typedef int32_t pkv_status;
 
 /* Largest num_splits pkv_decode_splitk accepts. */
 #define PKV_MAX_SPLITS 128
+/* num_splits value selecting the balanced schedule of pkv_decode_splitk. */
+#define PKV_SPLITS_BALANCED (-1)
+/* Most CTAs the balanced schedule launches (sizes its scratch). */
+#define PKV_BALANCED_MAX_CTAS 768
 
 /*
  * pkv_append — slot-mapped KV write (kapsl-backends src/gguf_native.rs,
@@ -127,8 +131,15 @@ pkv_status pkv_decode(const void* q, const void* k_cache, const void* v_cache,
  *
  *   num_splits    0 = pick with pkv_pick_num_splits for the current GPU; 1 =
  *                 run the single-pass kernel (no scratch needed);
- *                 2..PKV_MAX_SPLITS = forced.  A chunk is
- *                 ceil(max_blocks_per_seq / num_splits) blocks.
+ *                 2..PKV_MAX_SPLITS = forced fixed chunks of
+ *                 ceil(max_blocks_per_seq / num_splits) blocks;
+ *                 PKV_SPLITS_BALANCED = the balanced schedule: the list of
+ *                 all (sequence, kv head, block) tiles is cut into equal
+ *                 contiguous ranges, one per resident CTA (at most
+ *                 PKV_BALANCED_MAX_CTAS), planned on the GPU from
+ *                 context_lens, so every CTA reads the same number of bytes
+ *                 whatever the mix of lengths; (sequence, head) runs cut by a
+ *                 range boundary are merged by a second kernel.
  *   scratch       device memory of at least
  *                 pkv_splitk_scratch_bytes(num_seqs, num_heads, head_dim, S)
  *                 bytes, 16-byte aligned, caller-owned; its contents need no
@@ -151,7 +162,9 @@ pkv_status pkv_decode_splitk(const void* q, const void* k_cache, const void* v_c
  * pkv_splitk_scratch_bytes — bytes of scratch pkv_decode_splitk needs for S
  * splits: f32 partial outputs [num_seqs][num_heads][S][head_dim] followed by
  * f32 running max and running sum [num_seqs][num_heads][S] each (every part
- * 256-byte aligned).  0 when S <= 1 or for invalid sizes.
+ * 256-byte aligned).  For S = PKV_SPLITS_BALANCED: f32 records
+ * [PKV_BALANCED_MAX_CTAS][2][8][2 + head_dim] (independent of num_seqs and
+ * num_heads).  0 when S is 0 or 1 or for invalid sizes.
  * (ferrum-kernels paged.rs keeps these three buffers process-global and grows
  * them on demand; here the caller owns them.)
  */
@@ -166,7 +179,8 @@ size_t pkv_splitk_scratch_bytes(int32_t num_seqs, int32_t num_heads, int32_t hea
  * num_kv_heads (one CTA per sequence and KV head covers the whole group),
  * measured against num_sms.  max_context_len is the longest context the call
  * may see (pkv_decode_splitk passes max_blocks_per_seq * block_size).
- * Returns a value in 1..64; 1 for invalid sizes.
+ * Returns 1 (single pass), a split count in 2..64, or PKV_SPLITS_BALANCED;
+ * 1 for invalid sizes.
  */
 int32_t pkv_pick_num_splits(int32_t num_seqs, int32_t num_kv_heads,
                             int32_t max_context_len, int32_t block_size,

@@ -122,12 +122,212 @@ __device__ __forceinline__ uint32_t swz(int row, int d) {
   return (uint32_t)(line * 128 + chunk * 16 + (d & 7) * 2);
 }
 
+// One warp's online-softmax state.  Lane (r = lane/4, c = lane%4) holds the
+// O^T fragments of rows d = 16*i + r (+8) for query heads 2c and 2c+1, the
+// running max of those two heads (shared by the 8 lanes of a column) and its
+// own share of their running sums.
+template <int D>
+struct WarpState {
+  float acc[D / 16][4];
+  float m0, m1, l0, l1;
+
+  __device__ __forceinline__ void reset() {
+#pragma unroll
+    for (int i = 0; i < D / 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    m0 = m1 = -CUDART_INF_F;
+    l0 = l1 = 0.f;
+  }
+
+  // Completes the running sums across the 8 lanes of each head column.
+  __device__ __forceinline__ void finish_sums() {
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+    }
+  }
+
+  // Writes m[8], l[8] and o[heads][D] (heads 0..heads-1 of the group) at `dst`.
+  __device__ __forceinline__ void store(float* dst, int lane, int heads) const {
+    const int r = lane >> 2, c = lane & 3;
+    if (r == 0) {
+      dst[2 * c] = m0;
+      dst[2 * c + 1] = m1;
+      dst[8 + 2 * c] = l0;
+      dst[8 + 2 * c + 1] = l1;
+    }
+    float* o = dst + 16;
+#pragma unroll
+    for (int i = 0; i < D / 16; ++i) {
+      const int d = i * 16 + r;
+      if (2 * c < heads) {
+        o[(2 * c) * D + d] = acc[i][0];
+        o[(2 * c) * D + d + 8] = acc[i][2];
+      }
+      if (2 * c + 1 < heads) {
+        o[(2 * c + 1) * D + d] = acc[i][1];
+        o[(2 * c + 1) * D + d + 8] = acc[i][3];
+      }
+    }
+  }
+};
+
+// Q^T fragments (B operand): column n = lane/4 is query head `head0 + n`;
+// columns at or past `group` are zero.
+template <int D>
+__device__ __forceinline__ void load_q_frags(uint32_t (&qf)[D / 16][2], const __half* q,
+                                             size_t head0, int group, int lane) {
+  const int r = lane >> 2, c = lane & 3;
+  const bool live = r < group;
+  const uint32_t* qrow = reinterpret_cast<const uint32_t*>(q + (head0 + (live ? r : 0)) * D);
+#pragma unroll
+  for (int ks = 0; ks < D / 16; ++ks) {
+    qf[ks][0] = live ? __ldg(qrow + ks * 8 + c) : 0u;
+    qf[ks][1] = live ? __ldg(qrow + ks * 8 + 4 + c) : 0u;
+  }
+}
+
+// Folds one K/V tile (already in shared memory at kb / vb) into the warp
+// state.  Token t0 is the tile's first position; positions at or past
+// tok_end are masked.
+template <int D, int BS>
+__device__ __forceinline__ void consume_tile(uint32_t kb, uint32_t vb, int t0, int tok_end,
+                                             const uint32_t (&qf)[D / 16][2], float scale_log2,
+                                             WarpState<D>& st, int lane) {
+  constexpr int MT = BS / 16;
+  constexpr int KS = D / 16;
+  constexpr int HALVES = D / 64;
+  const int r = lane >> 2;
+  const int n_valid = min(BS, tok_end - t0);
+  if (n_valid < BS) {
+    // Rows past the context may hold anything (even NaN); P is 0 there, but
+    // 0 * NaN is NaN, so clear those V rows before P.V.
+    const int n_chunks = (BS - n_valid) * HALVES * 8;
+    for (int x = lane; x < n_chunks; x += 32) {
+      const int row = n_valid + x / (HALVES * 8);
+      const int rest = x % (HALVES * 8);
+      const int line = (rest >> 3) * BS + row;
+      const uint32_t a = vb + line * 128 + (rest & 7) * 16;
+      asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0) : "memory");
+    }
+    __syncwarp();
+  }
+
+  // S^T = K . Q^T for every 16-token slice of the tile.
+  float sc[MT][4];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) {
+    sc[mt][0] = sc[mt][1] = sc[mt][2] = sc[mt][3] = 0.f;
+    const int row = mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      uint32_t a[4];
+      ldsm_x4(kb + swz<BS>(row, ks * 16 + (lane >> 4) * 8), a);
+      mma_16816(sc[mt], a, qf[ks][0], qf[ks][1]);
+    }
+  }
+
+  // scale, mask rows past the context, tile max per head
+  float x0 = -CUDART_INF_F, x1 = -CUDART_INF_F;
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int tok = t0 + mt * 16 + r + (e >> 1) * 8;
+      const float v = sc[mt][e] * scale_log2;
+      sc[mt][e] = tok < tok_end ? v : -CUDART_INF_F;
+    }
+    x0 = fmaxf(x0, fmaxf(sc[mt][0], sc[mt][2]));
+    x1 = fmaxf(x1, fmaxf(sc[mt][1], sc[mt][3]));
+  }
+#pragma unroll
+  for (int o = 4; o < 32; o <<= 1) {
+    x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, o));
+    x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, o));
+  }
+  const float mn0 = fmaxf(st.m0, x0);
+  const float mn1 = fmaxf(st.m1, x1);
+  const float al0 = exp2f(st.m0 - mn0);  // 0 on the first tile (m = -inf)
+  const float al1 = exp2f(st.m1 - mn1);
+  st.m0 = mn0;
+  st.m1 = mn1;
+
+  // P = exp2(S - m), rounded to f16 for the tensor cores; the running sum
+  // adds the same rounded values so numerator and denominator agree.
+  uint32_t pb[MT][2];
+  float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) {
+    const __half2 h01 = __floats2half2_rn(exp2f(sc[mt][0] - mn0), exp2f(sc[mt][1] - mn1));
+    const __half2 h23 = __floats2half2_rn(exp2f(sc[mt][2] - mn0), exp2f(sc[mt][3] - mn1));
+    const float2 f01 = __half22float2(h01);
+    const float2 f23 = __half22float2(h23);
+    ps0 += f01.x + f23.x;
+    ps1 += f01.y + f23.y;
+    pb[mt][0] = movmatrix_trans(pack_half2(h01));
+    pb[mt][1] = movmatrix_trans(pack_half2(h23));
+  }
+  st.l0 = st.l0 * al0 + ps0;
+  st.l1 = st.l1 * al1 + ps1;
+#pragma unroll
+  for (int i = 0; i < KS; ++i) {
+    st.acc[i][0] *= al0;
+    st.acc[i][1] *= al1;
+    st.acc[i][2] *= al0;
+    st.acc[i][3] *= al1;
+  }
+
+  // O^T += V^T . P^T
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) {
+    const int row = mt * 16 + (lane & 7) + (lane >> 4) * 8;
+#pragma unroll
+    for (int i = 0; i < KS; ++i) {
+      uint32_t a[4];
+      ldsm_x4_trans(vb + swz<BS>(row, i * 16 + ((lane >> 3) & 1) * 8), a);
+      mma_16816(st.acc[i], a, pb[mt][0], pb[mt][1]);
+    }
+  }
+}
+
+// Log-sum-exp merge of W warp states stored with WarpState::store (stride
+// `stride` floats per warp) for head h, element d.
+template <int W, int D>
+__device__ __forceinline__ void merge_warps(const float* red, int stride, int h, int d, float& M,
+                                            float& num, float& den) {
+  M = -CUDART_INF_F;
+#pragma unroll
+  for (int w = 0; w < W; ++w) M = fmaxf(M, red[w * stride + h]);
+  num = 0.f;
+  den = 0.f;
+#pragma unroll
+  for (int w = 0; w < W; ++w) {
+    const float mw = red[w * stride + h];
+    const float f = (mw == -CUDART_INF_F) ? 0.f : exp2f(mw - M);
+    num += f * red[w * stride + 16 + h * D + d];
+    den += f * red[w * stride + 8 + h];
+  }
+}
+
+// Starts the TMA copies of the K and V tiles of (physical block, kv head)
+// into the stage at `kdst` (V follows K), completing on `bar`.
+template <int D, int BS>
+__device__ __forceinline__ void issue_tile_copy(uint32_t kdst, uint32_t bar, int tile,
+                                                const CUtensorMap* kmap, const CUtensorMap* vmap) {
+  constexpr int TB = BS * D * 2;
+  mbar_arrive_expect_tx(bar, 2 * TB);
+#pragma unroll
+  for (int h2 = 0; h2 < D / 64; ++h2) {
+    tma_load_4d(kdst + h2 * BS * 128, kmap, bar, 0, h2, 0, tile);
+    tma_load_4d(kdst + TB + h2 * BS * 128, vmap, bar, 0, h2, 0, tile);
+  }
+}
+
 template <int D, int BS, int W, int P, bool SPLIT>
 __global__ void __launch_bounds__(W * 32)
 paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
   using Shape = DecodeShape<D, BS, W, P>;
-  constexpr int MT = Shape::kMT;
   constexpr int KS = Shape::kKS;
   constexpr int TB = Shape::kTileBytes;
 
@@ -140,8 +340,6 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int r = lane >> 2;  // mma group id
-  const int c = lane & 3;   // thread in group
 
   int item = blockIdx.x;
   const int split = SPLIT ? item % p.num_splits : 0;
@@ -189,14 +387,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     const int phys = __ldg(table + j);
     const uint32_t bar = my_bars + 8 * stage;
     if (phys >= 0 && phys < p.num_blocks) {
-      mbar_arrive_expect_tx(bar, 2 * TB);
-      const int tile = phys * p.num_kv_heads + g;
-      const uint32_t kdst = k_stage(stage);
-#pragma unroll
-      for (int h2 = 0; h2 < Shape::kHalves; ++h2) {
-        tma_load_4d(kdst + h2 * BS * 128, &kmap, bar, 0, h2, 0, tile);
-        tma_load_4d(kdst + TB + h2 * BS * 128, &vmap, bar, 0, h2, 0, tile);
-      }
+      issue_tile_copy<D, BS>(k_stage(stage), bar, phys * p.num_kv_heads + g, &kmap, &vmap);
     } else {
       atomicOr(&g_device_status, kDevBadBlockId);
       mbar_arrive(bar);
@@ -208,24 +399,11 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     for (int li = 0; li < n0; ++li) issue(li);
   }
 
-  // Q^T fragments (B operand): column n = lane/4 is query head g*G + n.
   uint32_t qf[KS][2];
-  {
-    const bool live = r < p.group;
-    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
-        p.q + ((size_t)s * p.num_heads + (size_t)g * p.group + (live ? r : 0)) * D);
-#pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      qf[ks][0] = live ? __ldg(qrow + ks * 8 + c) : 0u;
-      qf[ks][1] = live ? __ldg(qrow + ks * 8 + 4 + c) : 0u;
-    }
-  }
+  load_q_frags<D>(qf, p.q, (size_t)s * p.num_heads + (size_t)g * p.group, p.group, lane);
 
-  float acc[KS][4];  // O^T fragments: rows d = 16*i + r (+8), columns heads 2c, 2c+1
-#pragma unroll
-  for (int i = 0; i < KS; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-  float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F;  // running max of heads 2c, 2c+1
-  float l0 = 0.f, l1 = 0.f;                      // this lane's share of the running sums
+  WarpState<D> st;
+  st.reset();
   bool failed = false;
   int li = 0;
 
@@ -239,99 +417,8 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     const int j = blk_begin + warp + li * W;
     const int phys = __ldg(table + j);
     if (phys >= 0 && phys < p.num_blocks) {
-      const int t0 = j * BS;
-      const int n_valid = min(BS, tok_end - t0);
       const uint32_t kb = k_stage(stage);
-      const uint32_t vb = kb + TB;
-      if (n_valid < BS) {
-        // Rows past the context may hold anything (even NaN); P is 0 there,
-        // but 0 * NaN is NaN, so clear those V rows before P.V.
-        const int n_chunks = (BS - n_valid) * Shape::kHalves * 8;
-        for (int x = lane; x < n_chunks; x += 32) {
-          const int row = n_valid + x / (Shape::kHalves * 8);
-          const int rest = x % (Shape::kHalves * 8);
-          const int line = (rest >> 3) * BS + row;
-          const uint32_t a = vb + line * 128 + (rest & 7) * 16;
-          asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0) : "memory");
-        }
-        __syncwarp();
-      }
-
-      // S^T = K . Q^T for every 16-token slice of the tile.
-      float sc[MT][4];
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
-        sc[mt][0] = sc[mt][1] = sc[mt][2] = sc[mt][3] = 0.f;
-        const int row = mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-#pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-          uint32_t a[4];
-          ldsm_x4(kb + swz<BS>(row, ks * 16 + (lane >> 4) * 8), a);
-          mma_16816(sc[mt], a, qf[ks][0], qf[ks][1]);
-        }
-      }
-
-      // scale, mask rows past the chunk, tile max per head
-      float x0 = -CUDART_INF_F, x1 = -CUDART_INF_F;
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int tok = t0 + mt * 16 + r + (e >> 1) * 8;
-          const float v = sc[mt][e] * p.scale_log2;
-          sc[mt][e] = tok < tok_end ? v : -CUDART_INF_F;
-        }
-        x0 = fmaxf(x0, fmaxf(sc[mt][0], sc[mt][2]));
-        x1 = fmaxf(x1, fmaxf(sc[mt][1], sc[mt][3]));
-      }
-#pragma unroll
-      for (int o = 4; o < 32; o <<= 1) {
-        x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, o));
-        x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, o));
-      }
-      const float mn0 = fmaxf(m0, x0);
-      const float mn1 = fmaxf(m1, x1);
-      const float al0 = exp2f(m0 - mn0);  // 0 on the first tile (m = -inf)
-      const float al1 = exp2f(m1 - mn1);
-      m0 = mn0;
-      m1 = mn1;
-
-      // P = exp2(S - m), rounded to f16 for the tensor cores; the running sum
-      // adds the same rounded values so numerator and denominator agree.
-      uint32_t pb[MT][2];
-      float ps0 = 0.f, ps1 = 0.f;
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
-        const __half2 h01 = __floats2half2_rn(exp2f(sc[mt][0] - m0), exp2f(sc[mt][1] - m1));
-        const __half2 h23 = __floats2half2_rn(exp2f(sc[mt][2] - m0), exp2f(sc[mt][3] - m1));
-        const float2 f01 = __half22float2(h01);
-        const float2 f23 = __half22float2(h23);
-        ps0 += f01.x + f23.x;
-        ps1 += f01.y + f23.y;
-        pb[mt][0] = movmatrix_trans(pack_half2(h01));
-        pb[mt][1] = movmatrix_trans(pack_half2(h23));
-      }
-      l0 = l0 * al0 + ps0;
-      l1 = l1 * al1 + ps1;
-#pragma unroll
-      for (int i = 0; i < KS; ++i) {
-        acc[i][0] *= al0;
-        acc[i][1] *= al1;
-        acc[i][2] *= al0;
-        acc[i][3] *= al1;
-      }
-
-      // O^T += V^T . P^T
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
-        const int row = mt * 16 + (lane & 7) + (lane >> 4) * 8;
-#pragma unroll
-        for (int i = 0; i < KS; ++i) {
-          uint32_t a[4];
-          ldsm_x4_trans(vb + swz<BS>(row, i * 16 + ((lane >> 3) & 1) * 8), a);
-          mma_16816(acc[i], a, pb[mt][0], pb[mt][1]);
-        }
-      }
+      consume_tile<D, BS>(kb, kb + TB, j * BS, tok_end, qf, p.scale_log2, st, lane);
     }
     __syncwarp();
     if (lane == 0 && li + P < my_tiles) {
@@ -350,53 +437,21 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     if (lane == 0) atomicOr(&s_failed, 1);
   }
 
-  // complete the per-lane sums across the 8 lanes of each head column
-#pragma unroll
-  for (int o = 4; o < 32; o <<= 1) {
-    l0 += __shfl_xor_sync(0xffffffffu, l0, o);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, o);
-  }
-
+  st.finish_sums();
   __syncthreads();  // every warp is done with its ring
   if (s_failed) return;
 
   // merge the W warp states through shared memory (reusing the ring)
   float* red = reinterpret_cast<float*>(smem);
-  {
-    float* mine = red + warp * Shape::kRedFloats;
-    if (r == 0) {
-      mine[2 * c] = m0;
-      mine[2 * c + 1] = m1;
-      mine[8 + 2 * c] = l0;
-      mine[8 + 2 * c + 1] = l1;
-    }
-    float* o = mine + 16;
-#pragma unroll
-    for (int i = 0; i < KS; ++i) {
-      const int d = i * 16 + r;
-      o[(2 * c) * D + d] = acc[i][0];
-      o[(2 * c + 1) * D + d] = acc[i][1];
-      o[(2 * c) * D + d + 8] = acc[i][2];
-      o[(2 * c + 1) * D + d + 8] = acc[i][3];
-    }
-  }
+  st.store(red + warp * Shape::kRedFloats, lane, 8);
   __syncthreads();
 
   const int G = p.group;
   for (int idx = threadIdx.x; idx < G * D; idx += W * 32) {
     const int h = idx / D;
     const int d = idx - h * D;
-    float M = -CUDART_INF_F;
-#pragma unroll
-    for (int w = 0; w < W; ++w) M = fmaxf(M, red[w * Shape::kRedFloats + h]);
-    float num = 0.f, den = 0.f;
-#pragma unroll
-    for (int w = 0; w < W; ++w) {
-      const float mw = red[w * Shape::kRedFloats + h];
-      const float f = (mw == -CUDART_INF_F) ? 0.f : exp2f(mw - M);
-      num += f * red[w * Shape::kRedFloats + 16 + h * D + d];
-      den += f * red[w * Shape::kRedFloats + 8 + h];
-    }
+    float M, num, den;
+    merge_warps<W, D>(red, Shape::kRedFloats, h, d, M, num, den);
     const size_t qh = (size_t)s * p.num_heads + (size_t)g * G + h;
     if (SPLIT) {
       const size_t slot = qh * p.num_splits + split;
@@ -408,6 +463,354 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     } else {
       p.out[qh * D + d] = __float2half_rn(den > 0.f ? num / den : 0.f);
     }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// balanced schedule
+// ---------------------------------------------------------------------------
+//
+// The work is the list of all tiles (sequence s, KV head g, logical block j)
+// in (s, g, j) order; a (s, g) run is a "segment".  CTA c of N takes the
+// contiguous range [c*T/N, (c+1)*T/N) of the T tiles, so every CTA moves the
+// same number of K/V bytes whatever the mix of context lengths.  Each CTA
+// plans its range on the device from context_lens (no host read).  Segments
+// that lie wholly inside one CTA's range are finished there (f16 output);
+// a segment cut by a range boundary leaves one partial record (m, l, acc)
+// per CTA piece, merged by balanced_combine_kernel.  A CTA has at most two
+// cut pieces (its first and last), so records are [N][2][8 heads][2 + D] f32.
+
+struct BalancedParams {
+  const __half* q;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  __half* out;
+  float* records;
+  int num_seqs;
+  int num_heads;
+  int num_kv_heads;
+  int group;
+  int max_blocks_per_seq;
+  int num_blocks;
+  int num_ctas;  // N
+  float scale_log2;
+};
+
+constexpr int kRecHeads = 8;
+
+template <int BS>
+__device__ __forceinline__ int clamped_len(const int32_t* lens, int s, int cap) {
+  int L = __ldg(lens + s);
+  return L < 0 ? 0 : (L > cap ? cap : L);
+}
+
+// Sum over the CTA (every thread passes its value; all get the total).
+template <int NT>
+__device__ __forceinline__ long long block_sum(long long v, long long* sm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  if (lane == 0) sm[warp] = v;
+  __syncthreads();
+  long long t = 0;
+#pragma unroll
+  for (int w = 0; w < NT / 32; ++w) t += sm[w];
+  __syncthreads();
+  return t;
+}
+
+// Inclusive prefix sum over the CTA in thread order; *total gets the sum.
+template <int NT>
+__device__ __forceinline__ long long block_incl_scan(long long v, long long* sm, long long* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long y = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += y;
+  }
+  if (lane == 31) sm[warp] = v;
+  __syncthreads();
+  long long before = 0, t = 0;
+#pragma unroll
+  for (int w = 0; w < NT / 32; ++w) {
+    const long long x = sm[w];
+    if (w < warp) before += x;
+    t += x;
+  }
+  __syncthreads();
+  *total = t;
+  return v + before;
+}
+
+// Position in the tile list: the segment (s, g) holding a tile and where it
+// starts.  n is the tile count of sequence s, P the tiles of sequences < s.
+struct SegCursor {
+  int s, g, n;
+  long long P, start;
+};
+
+template <int BS>
+__device__ __forceinline__ void cursor_next(SegCursor& cu, const int32_t* lens, int B, int Hkv,
+                                            int cap) {
+  if (++cu.g == Hkv) {
+    cu.g = 0;
+    cu.P += cu.n;
+    do {
+      ++cu.s;
+      cu.n = cu.s < B ? (clamped_len<BS>(lens, cu.s, cap) + BS - 1) / BS : 1;
+    } while (cu.n == 0);
+  }
+  cu.start = cu.P * Hkv + (long long)cu.g * cu.n;
+}
+
+template <int BS>
+__device__ __forceinline__ void cursor_seek(SegCursor& cu, long long u, const int32_t* lens, int B,
+                                            int Hkv, int cap) {
+  while (u >= cu.start + cu.n) cursor_next<BS>(cu, lens, B, Hkv, cap);
+}
+
+// Plans this CTA's range: T, [u_begin, u_end) and the segment holding
+// u_begin.  Returns false (uniformly) when the range is empty.
+template <int BS, int NT>
+__device__ __forceinline__ bool plan_range(const BalancedParams& p, int c, long long* T_out,
+                                           long long* ub, long long* ue, SegCursor* cu,
+                                           long long* sm_scan, int* sm_s, long long* sm_P) {
+  const int cap = p.max_blocks_per_seq * BS;
+  const int B = p.num_seqs, Hkv = p.num_kv_heads;
+  long long mine = 0;
+  for (int s = threadIdx.x; s < B; s += NT) {
+    const int L = __ldg(p.context_lens + s);
+    if ((L < 0 || L > cap) && c == 0) atomicOr(&g_device_status, kDevBadContextLen);
+    mine += (clamped_len<BS>(p.context_lens, s, cap) + BS - 1) / BS;
+  }
+  const long long T = block_sum<NT>(mine, sm_scan) * Hkv;
+  *T_out = T;
+  if (T == 0) return false;
+  const long long N = p.num_ctas;
+  const long long u_begin = T * c / N, u_end = T * (c + 1) / N;
+  *ub = u_begin;
+  *ue = u_end;
+  if (u_begin >= u_end) return false;
+
+  if (threadIdx.x == 0) *sm_s = -1;
+  __syncthreads();
+  long long carry = 0;
+  for (int base = 0; base < B; base += NT) {
+    const int s = base + threadIdx.x;
+    const long long n = s < B ? (clamped_len<BS>(p.context_lens, s, cap) + BS - 1) / BS : 0;
+    long long chunk_total;
+    const long long incl = block_incl_scan<NT>(n, sm_scan, &chunk_total);
+    const long long first = carry + incl - n;  // tiles of sequences before s
+    if (n > 0 && first * Hkv <= u_begin && u_begin < (first + n) * Hkv) {
+      *sm_s = s;
+      *sm_P = first;
+    }
+    carry += chunk_total;
+    __syncthreads();
+    if (*sm_s >= 0) break;
+  }
+  cu->s = *sm_s;
+  cu->P = *sm_P;
+  cu->n = (clamped_len<BS>(p.context_lens, cu->s, cap) + BS - 1) / BS;
+  cu->g = (int)((u_begin - cu->P * Hkv) / cu->n);
+  cu->start = cu->P * Hkv + (long long)cu->g * cu->n;
+  return true;
+}
+
+template <int D, int BS, int W, int P>
+__global__ void __launch_bounds__(W * 32)
+paged_decode_balanced_kernel(const __grid_constant__ CUtensorMap kmap,
+                             const __grid_constant__ CUtensorMap vmap, const BalancedParams p) {
+  using Shape = DecodeShape<D, BS, W, P>;
+  constexpr int KS = Shape::kKS;
+  constexpr int TB = Shape::kTileBytes;
+  constexpr int NT = W * 32;
+
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ int s_failed;
+  __shared__ long long sm_scan[NT / 32];
+  __shared__ int sm_s;
+  __shared__ long long sm_P;
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t ring = smem_addr(smem);
+  const uint32_t bars = ring + Shape::kRingBytes;
+  const int G = p.group;
+  const int red_stride = 16 + G * D;
+  float* red = reinterpret_cast<float*>(smem + Shape::kRingBytes + Shape::kBarrierBytes);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int c = blockIdx.x;
+
+  if (*reinterpret_cast<volatile unsigned int*>(&g_device_status) & kDevWaitTimeout) return;
+
+  long long T, u_begin, u_end;
+  SegCursor cc;
+  if (!plan_range<BS, NT>(p, c, &T, &u_begin, &u_end, &cc, sm_scan, &sm_s, &sm_P)) return;
+
+  const int cap = p.max_blocks_per_seq * BS;
+  const int B = p.num_seqs, Hkv = p.num_kv_heads;
+  const long long span = u_end - u_begin;
+  const int my_tiles = span > warp ? (int)((span - warp + W - 1) / W) : 0;
+
+  if (threadIdx.x == 0) s_failed = 0;
+  const uint32_t my_bars = bars + warp * P * 8;
+  if (lane == 0) {
+#pragma unroll
+    for (int i = 0; i < P; ++i) mbar_init(my_bars + 8 * i, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  auto k_stage = [&](int stage) { return ring + (warp * P + stage) * Shape::kStageBytes; };
+
+  // Producer (lane 0): the warp's k-th tile is u_begin + warp + k*W.
+  SegCursor pc = cc;
+  auto issue = [&](int k) {
+    const long long u = u_begin + warp + (long long)k * W;
+    cursor_seek<BS>(pc, u, p.context_lens, B, Hkv, cap);
+    const int j = (int)(u - pc.start);
+    const int phys = __ldg(p.block_tables + (size_t)pc.s * p.max_blocks_per_seq + j);
+    const uint32_t bar = my_bars + 8 * (k % P);
+    if (phys >= 0 && phys < p.num_blocks) {
+      issue_tile_copy<D, BS>(k_stage(k % P), bar, phys * Hkv + pc.g, &kmap, &vmap);
+    } else {
+      atomicOr(&g_device_status, kDevBadBlockId);
+      mbar_arrive(bar);
+    }
+  };
+  if (lane == 0) {
+    const int n0 = my_tiles < P ? my_tiles : P;
+    for (int k = 0; k < n0; ++k) issue(k);
+  }
+
+  bool failed = false;
+  int k_done = 0;  // tiles this warp has consumed
+  long long u = u_begin;
+  while (u < u_end) {
+    const long long seg_end = cc.start + cc.n;
+    const long long a = u, b = seg_end < u_end ? seg_end : u_end;
+    const int L = clamped_len<BS>(p.context_lens, cc.s, cap);
+
+    uint32_t qf[KS][2];
+    load_q_frags<D>(qf, p.q, (size_t)cc.s * p.num_heads + (size_t)cc.g * G, G, lane);
+    WarpState<D> st;
+    st.reset();
+
+    // this warp's tiles in [a, b)
+    const int off = (int)((a - u_begin) % W);
+    for (long long t = a + ((warp - off + W) % W); t < b && !failed; t += W) {
+      const int k = (int)((t - u_begin - warp) / W);
+      if (!mbar_wait_bounded(my_bars + 8 * (k % P), (k / P) & 1, kWaitLimitNs)) {
+        failed = true;
+        break;
+      }
+      const int j = (int)(t - cc.start);
+      const int phys = __ldg(p.block_tables + (size_t)cc.s * p.max_blocks_per_seq + j);
+      if (phys >= 0 && phys < p.num_blocks) {
+        const uint32_t kb = k_stage(k % P);
+        consume_tile<D, BS>(kb, kb + TB, j * BS, L, qf, p.scale_log2, st, lane);
+      }
+      k_done = k + 1;
+      __syncwarp();
+      if (lane == 0 && k + P < my_tiles) {
+        fence_proxy_async_smem();
+        issue(k + P);
+      }
+    }
+    if (failed && lane == 0) atomicOr(&s_failed, 1);
+
+    st.finish_sums();
+    st.store(red + warp * red_stride, lane, G);
+    __syncthreads();
+    if (!s_failed) {
+      const bool whole = (a == cc.start) && (b == seg_end);
+      const int slot = (a == u_begin) ? 0 : 1;
+      for (int idx = threadIdx.x; idx < G * D; idx += NT) {
+        const int h = idx / D;
+        const int d = idx - h * D;
+        float M, num, den;
+        merge_warps<W, D>(red, red_stride, h, d, M, num, den);
+        if (whole) {
+          const size_t qh = (size_t)cc.s * p.num_heads + (size_t)cc.g * G + h;
+          p.out[qh * D + d] = __float2half_rn(den > 0.f ? num / den : 0.f);
+        } else {
+          float* rec = p.records + (((size_t)c * 2 + slot) * kRecHeads + h) * (D + 2);
+          rec[2 + d] = num;
+          if (d == 0) {
+            rec[0] = M;
+            rec[1] = den;
+          }
+        }
+      }
+    }
+    __syncthreads();
+    u = b;
+    if (u < u_end) cursor_next<BS>(cc, p.context_lens, B, Hkv, cap);
+  }
+
+  if (failed) {
+    if (lane == 0) atomicOr(&g_device_status, kDevWaitTimeout);
+    const int last = min(k_done + P, my_tiles);
+    for (int k = k_done; k < last; ++k)
+      (void)mbar_wait_bounded(my_bars + 8 * (k % P), (k / P) & 1, kWaitLimitNs);
+  }
+}
+
+// Merges the records of every segment that a CTA range boundary cut, and
+// writes zeros for empty segments.  One CTA per (sequence, KV head).
+template <int D, int BS>
+__global__ void __launch_bounds__(128) balanced_combine_kernel(const BalancedParams p) {
+  constexpr int NT = 128;
+  __shared__ long long sm_scan[NT / 32];
+  const int s = blockIdx.x / p.num_kv_heads;
+  const int g = blockIdx.x % p.num_kv_heads;
+  const int cap = p.max_blocks_per_seq * BS;
+  const int B = p.num_seqs, Hkv = p.num_kv_heads, G = p.group;
+
+  long long all = 0, before = 0;
+  for (int s2 = threadIdx.x; s2 < B; s2 += NT) {
+    const long long n = (clamped_len<BS>(p.context_lens, s2, cap) + BS - 1) / BS;
+    all += n;
+    if (s2 < s) before += n;
+  }
+  const long long tiles = block_sum<NT>(all, sm_scan);
+  const long long Ps = block_sum<NT>(before, sm_scan);
+  const long long n = (clamped_len<BS>(p.context_lens, s, cap) + BS - 1) / BS;
+  const size_t qh0 = (size_t)s * p.num_heads + (size_t)g * G;
+  if (n == 0) {
+    for (int idx = threadIdx.x; idx < G * D; idx += NT) p.out[qh0 * D + idx] = __float2half_rn(0.f);
+    return;
+  }
+  const long long T = tiles * Hkv, N = p.num_ctas;
+  const long long seg_start = Ps * Hkv + (long long)g * n, seg_end = seg_start + n;
+  const long long c_lo = ((seg_start + 1) * N - 1) / T;  // owner of the first tile
+  const long long c_hi = (seg_end * N - 1) / T;          // owner of the last tile
+  if (c_lo == c_hi) return;  // finished by its CTA
+  const long long ub_lo = c_lo * T / N;
+
+  for (int idx = threadIdx.x; idx < G * D; idx += NT) {
+    const int h = idx / D;
+    const int d = idx - h * D;
+    float M = -CUDART_INF_F;
+    for (long long c = c_lo; c <= c_hi; ++c) {
+      if (c * T / N >= (c + 1) * T / N) continue;  // empty range, no record
+      const int slot = (c == c_lo && seg_start > ub_lo) ? 1 : 0;
+      M = fmaxf(M, __ldg(p.records + ((c * 2 + slot) * kRecHeads + h) * (D + 2)));
+    }
+    float num = 0.f, den = 0.f;
+    for (long long c = c_lo; c <= c_hi; ++c) {
+      if (c * T / N >= (c + 1) * T / N) continue;
+      const int slot = (c == c_lo && seg_start > ub_lo) ? 1 : 0;
+      const float* rec = p.records + ((c * 2 + slot) * kRecHeads + h) * (D + 2);
+      const float m = __ldg(rec);
+      if (m == -CUDART_INF_F) continue;
+      const float f = exp2f(m - M);
+      num += f * __ldg(rec + 2 + d);
+      den += f * __ldg(rec + 1);
+    }
+    p.out[(qh0 + h) * D + d] = __float2half_rn(den > 0.f ? num / den : 0.f);
   }
 }
 

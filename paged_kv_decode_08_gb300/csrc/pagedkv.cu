@@ -209,6 +209,83 @@ pkv_status dispatch_decode(const DecodeArgs& a, const DecodeParams& prm, cudaStr
   return fail(PKV_ERR_UNSUPPORTED, "head_dim %d / block_size %d", a.head_dim, a.block_size);
 }
 
+size_t balanced_scratch_bytes(int head_dim) {
+  return ((size_t)PKV_BALANCED_MAX_CTAS * 2 * kRecHeads * (head_dim + 2) * sizeof(float) + 255) &
+         ~size_t(255);
+}
+
+template <int D, int BS>
+pkv_status launch_balanced(const DecodeArgs& a, float* records, cudaStream_t stream) {
+  constexpr int W = Tuning<D, BS>::W;
+  constexpr int P = Tuning<D, BS>::P;
+  using Shape = DecodeShape<D, BS, W, P>;
+  auto kernel = paged_decode_balanced_kernel<D, BS, W, P>;
+  const int G = a.num_heads / a.num_kv_heads;
+  const int smem = Shape::kSmemBytes + W * (16 + G * D) * (int)sizeof(float);
+  const int smem_max = Shape::kSmemBytes + W * (16 + 8 * D) * (int)sizeof(float);
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  // per device: attribute set once; occupancy per group size
+  static std::atomic<int> occ_cache[64][9];
+  static std::atomic<unsigned long long> attr_set{0};
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (!(attr_set.load(std::memory_order_relaxed) & bit)) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(balanced)");
+    attr_set.fetch_or(bit, std::memory_order_relaxed);
+  }
+  int occ = (dev >= 0 && dev < 64) ? occ_cache[dev][G].load(std::memory_order_relaxed) : 0;
+  if (occ <= 0) {
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, W * 32, smem);
+    if (e != cudaSuccess || occ <= 0) return cuda_fail(e, "occupancy of the balanced kernel");
+    if (dev >= 0 && dev < 64) occ_cache[dev][G].store(occ, std::memory_order_relaxed);
+  }
+  int sms = 0;
+  if (current_device_sms(&sms) != 0) return fail(PKV_ERR_CUDA, "cannot query the SM count");
+  int N = sms * occ;
+  if (N > PKV_BALANCED_MAX_CTAS) N = PKV_BALANCED_MAX_CTAS;
+
+  CUtensorMap kmap, vmap;
+  pkv_status st = make_cache_map(&kmap, a.k_cache, a.num_blocks, a.num_kv_heads, BS, D);
+  if (st != PKV_OK) return st;
+  st = make_cache_map(&vmap, a.v_cache, a.num_blocks, a.num_kv_heads, BS, D);
+  if (st != PKV_OK) return st;
+
+  BalancedParams bp{};
+  bp.q = static_cast<const __half*>(a.q);
+  bp.block_tables = a.block_tables;
+  bp.context_lens = a.context_lens;
+  bp.out = static_cast<__half*>(a.out);
+  bp.records = records;
+  bp.num_seqs = a.num_seqs;
+  bp.num_heads = a.num_heads;
+  bp.num_kv_heads = a.num_kv_heads;
+  bp.group = G;
+  bp.max_blocks_per_seq = a.max_blocks_per_seq;
+  bp.num_blocks = a.num_blocks;
+  bp.num_ctas = N;
+  bp.scale_log2 = a.scale * 1.4426950408889634f;
+  kernel<<<N, W * 32, smem, stream>>>(kmap, vmap, bp);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "balanced decode launch");
+  const long long grid2 = (long long)a.num_seqs * a.num_kv_heads;
+  if (grid2 >= (1ll << 31)) return fail(PKV_ERR_INVALID_ARG, "grid too large");
+  balanced_combine_kernel<D, BS><<<(int)grid2, 128, 0, stream>>>(bp);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "balanced combine launch");
+  return PKV_OK;
+}
+
+pkv_status dispatch_balanced(const DecodeArgs& a, float* records, cudaStream_t stream) {
+  if (a.head_dim == 128 && a.block_size == 16) return launch_balanced<128, 16>(a, records, stream);
+  if (a.head_dim == 128 && a.block_size == 32) return launch_balanced<128, 32>(a, records, stream);
+  if (a.head_dim == 64 && a.block_size == 16) return launch_balanced<64, 16>(a, records, stream);
+  if (a.head_dim == 64 && a.block_size == 32) return launch_balanced<64, 32>(a, records, stream);
+  return fail(PKV_ERR_UNSUPPORTED, "head_dim %d / block_size %d", a.head_dim, a.block_size);
+}
+
 DecodeParams base_params(const DecodeArgs& a) {
   DecodeParams p{};
   p.q = static_cast<const __half*>(a.q);
@@ -256,6 +333,7 @@ const char* pkv_last_error(void) { return t_last_error; }
 
 size_t pkv_splitk_scratch_bytes(int32_t num_seqs, int32_t num_heads, int32_t head_dim,
                                 int32_t num_splits) {
+  if (num_splits == PKV_SPLITS_BALANCED) return head_dim > 0 ? balanced_scratch_bytes(head_dim) : 0;
   if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || num_splits <= 1) return 0;
   const size_t rows = (size_t)num_seqs * num_heads * num_splits;
   return align256(rows * head_dim * sizeof(float)) + 2 * align256(rows * sizeof(float));
@@ -340,8 +418,8 @@ pkv_status pkv_decode_splitk(const void* q, const void* k_cache, const void* v_c
                      head_dim, block_size, out};
   pkv_status st = validate_decode(a);
   if (st != PKV_OK) return st;
-  if (num_splits < 0 || num_splits > PKV_MAX_SPLITS)
-    return fail(PKV_ERR_INVALID_ARG, "num_splits %d outside 0..%d", num_splits, PKV_MAX_SPLITS);
+  if (num_splits < PKV_SPLITS_BALANCED || num_splits > PKV_MAX_SPLITS)
+    return fail(PKV_ERR_INVALID_ARG, "num_splits %d outside -1..%d", num_splits, PKV_MAX_SPLITS);
   if (num_seqs == 0) return PKV_OK;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
 
@@ -350,6 +428,14 @@ pkv_status pkv_decode_splitk(const void* q, const void* k_cache, const void* v_c
     int sms = 0;
     if (current_device_sms(&sms) != 0) return fail(PKV_ERR_CUDA, "cannot query the SM count");
     S = pkv_pick_num_splits(num_seqs, num_kv_heads, max_blocks_per_seq * block_size, block_size, sms);
+  }
+  if (S == PKV_SPLITS_BALANCED) {
+    const size_t need_b = balanced_scratch_bytes(head_dim);
+    if (!scratch || scratch_bytes < need_b)
+      return fail(PKV_ERR_SCRATCH_TOO_SMALL, "the balanced schedule needs %zu scratch bytes, got %zu",
+                  need_b, scratch ? scratch_bytes : (size_t)0);
+    if (!aligned(scratch, 16)) return fail(PKV_ERR_INVALID_ARG, "scratch must be 16-byte aligned");
+    return dispatch_balanced(a, static_cast<float*>(scratch), cs);
   }
   const int chunk_blocks = (max_blocks_per_seq + S - 1) / S;
   const int S_eff = (max_blocks_per_seq + chunk_blocks - 1) / chunk_blocks;
@@ -458,8 +544,8 @@ extern "C" pkv_status pkv_decode_splitk_noalloc(
                      head_dim, block_size, out};
   pkv_status st = validate_decode(a);
   if (st != PKV_OK) return st;
-  if (num_splits < 0 || num_splits > PKV_MAX_SPLITS)
-    return fail(PKV_ERR_INVALID_ARG, "num_splits %d outside 0..%d", num_splits, PKV_MAX_SPLITS);
+  if (num_splits < PKV_SPLITS_BALANCED || num_splits > PKV_MAX_SPLITS)
+    return fail(PKV_ERR_INVALID_ARG, "num_splits %d outside -1..%d", num_splits, PKV_MAX_SPLITS);
   if (num_seqs == 0) return PKV_OK;
 
   // The split count pkv_decode_splitk will use, and the scratch it needs.
@@ -469,8 +555,11 @@ extern "C" pkv_status pkv_decode_splitk_noalloc(
     if (current_device_sms(&sms) != 0) return fail(PKV_ERR_CUDA, "cannot query the SM count");
     S = pkv_pick_num_splits(num_seqs, num_kv_heads, max_blocks_per_seq * block_size, block_size, sms);
   }
-  const int chunk_blocks = (max_blocks_per_seq + S - 1) / S;
-  const int S_eff = (max_blocks_per_seq + chunk_blocks - 1) / chunk_blocks;
+  int S_eff = S;
+  if (S > 1) {
+    const int chunk_blocks = (max_blocks_per_seq + S - 1) / S;
+    S_eff = (max_blocks_per_seq + chunk_blocks - 1) / chunk_blocks;
+  }
   const size_t need = pkv_splitk_scratch_bytes(num_seqs, num_heads, head_dim, S_eff);
   if (need > (size_t)PKV_NOALLOC_SCRATCH_BYTES)
     return fail(PKV_ERR_SCRATCH_TOO_SMALL,

@@ -30,6 +30,8 @@ PKV_DEV_BAD_CONTEXT_LEN = 0x4
 PKV_DEV_WAIT_TIMEOUT = 0x8
 
 PKV_MAX_SPLITS = 128
+PKV_SPLITS_BALANCED = -1
+PKV_BALANCED_MAX_CTAS = 768
 PKV_NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
 
 
@@ -187,6 +189,9 @@ def alloc_scratch(q, k_cache, block_tables, num_splits=0):
     import torch
 
     S = splits_for(q, k_cache, block_tables, num_splits)
+    if S > 1:  # the kernel uses ceil(MBPS / ceil(MBPS / S)) <= S splits
+        mbps = block_tables.shape[1]
+        S = -(-mbps // -(-mbps // S))
     n = pkv_splitk_scratch_bytes(q.shape[0], q.shape[1], q.shape[2], S)
     return torch.empty(max(n, 16), dtype=torch.uint8, device=q.device)
 

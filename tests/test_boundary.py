@@ -49,6 +49,14 @@ def test_status_strings(pk):
     assert pk.status_string(-3).startswith("split-K scratch")
 
 
+def test_balanced_scratch_bytes(pk):
+    for D in (64, 128):
+        n = pk.pkv_splitk_scratch_bytes(4, 32, D, -1)
+        assert n >= pk.PKV_BALANCED_MAX_CTAS * 2 * 8 * (D + 2) * 4
+        assert n == pk.pkv_splitk_scratch_bytes(256, 28, D, -1)  # independent of B and H
+    assert pk.pkv_splitk_scratch_bytes(4, 32, 128, -1) <= pk.PKV_NOALLOC_SCRATCH_BYTES
+
+
 def test_scratch_bytes(pk):
     assert pk.pkv_splitk_scratch_bytes(4, 32, 128, 1) == 0
     assert pk.pkv_splitk_scratch_bytes(0, 32, 128, 4) == 0
@@ -127,8 +135,9 @@ def test_splitk_rejects_bad_splits_and_small_scratch(pk):
     f = pk.lib.pkv_decode_splitk
     args = [a["q"], a["k"], a["v"], a["bt"], a["cl"], a["B"], a["mbps"], a["nb"], a["scale"],
             a["H"], a["Hkv"], a["D"], a["bs"], a["out"]]
-    assert f(*args, -1, F16, 1 << 30, None) == -1
+    assert f(*args, -2, F16, 1 << 30, None) == -1
     assert f(*args, 129, F16, 1 << 30, None) == -1
+    assert f(*args, -1, F16, pk.pkv_splitk_scratch_bytes(4, 32, 128, -1) - 1, None) == -3
     assert f(*args, 16, None, 0, None) == -3
     need = pk.pkv_splitk_scratch_bytes(4, 32, 128, 16)
     assert f(*args, 16, F16, need - 1, None) == -3
@@ -152,4 +161,4 @@ def test_noalloc_rejects_oversized_requests_before_any_cuda_call(pk):
     st = f(F16, F16, F16, F16, F16, 256, 8192, 24576, 0.1, 32, 8, 128, 16, F16, 64, None)
     assert st == pk.PKV_ERR_SCRATCH_TOO_SMALL
     assert "built-in buffer" in pk.last_error()
-    assert f(F16, F16, F16, F16, F16, 2, 3, 8, 0.1, 4, 2, 64, 16, F16, -1, None) == -1
+    assert f(F16, F16, F16, F16, F16, 2, 3, 8, 0.1, 4, 2, 64, 16, F16, -2, None) == -1

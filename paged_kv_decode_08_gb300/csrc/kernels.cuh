@@ -28,6 +28,7 @@
 #include <math_constants.h>
 #include <stdint.h>
 
+#include "pagedkv.h"
 #include "ptx.cuh"
 
 namespace pkv {
@@ -55,6 +56,8 @@ append_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
               const int32_t* __restrict__ slot_mapping, long long total_chunks,
               int chunks_per_row, int num_kv_heads, int block_size, long long num_slots,
               uint4* __restrict__ k_cache, uint4* __restrict__ v_cache) {
+  pdl_launch_dependents();
+  pdl_wait();
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total_chunks;
        i += stride) {
@@ -347,6 +350,8 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   const int g = item % p.num_kv_heads;
   const int s = item / p.num_kv_heads;
 
+  pdl_launch_dependents();
+  pdl_wait();
   // After a lost copy has been flagged, later CTAs do no work (and write
   // nothing) until the host reads and clears the status word.
   if (*reinterpret_cast<volatile unsigned int*>(&g_device_status) & kDevWaitTimeout) return;
@@ -643,6 +648,8 @@ paged_decode_balanced_kernel(const __grid_constant__ CUtensorMap kmap,
   const int lane = threadIdx.x & 31;
   const int c = blockIdx.x;
 
+  pdl_launch_dependents();
+  pdl_wait();
   if (*reinterpret_cast<volatile unsigned int*>(&g_device_status) & kDevWaitTimeout) return;
 
   long long T, u_begin, u_end;
@@ -759,15 +766,23 @@ paged_decode_balanced_kernel(const __grid_constant__ CUtensorMap kmap,
 }
 
 // Merges the records of every segment that a CTA range boundary cut, and
-// writes zeros for empty segments.  One CTA per (sequence, KV head).
+// writes zeros for empty segments.  One CTA per (sequence, KV head).  The
+// record list and each head's weights are worked out once into shared
+// memory; the threads then sum over records per output element.
 template <int D, int BS>
 __global__ void __launch_bounds__(128) balanced_combine_kernel(const BalancedParams p) {
   constexpr int NT = 128;
   __shared__ long long sm_scan[NT / 32];
+  __shared__ int s_rec[PKV_BALANCED_MAX_CTAS];             // record index, -1 = none
+  __shared__ float s_w[PKV_BALANCED_MAX_CTAS][kRecHeads];  // 2^(m - M) per record and head
+  __shared__ float s_den[kRecHeads];
+  pdl_launch_dependents();
+  pdl_wait();
   const int s = blockIdx.x / p.num_kv_heads;
   const int g = blockIdx.x % p.num_kv_heads;
   const int cap = p.max_blocks_per_seq * BS;
   const int B = p.num_seqs, Hkv = p.num_kv_heads, G = p.group;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
   long long all = 0, before = 0;
   for (int s2 = threadIdx.x; s2 < B; s2 += NT) {
@@ -789,27 +804,48 @@ __global__ void __launch_bounds__(128) balanced_combine_kernel(const BalancedPar
   const long long c_hi = (seg_end * N - 1) / T;          // owner of the last tile
   if (c_lo == c_hi) return;  // finished by its CTA
   const long long ub_lo = c_lo * T / N;
+  const int R = (int)(c_hi - c_lo + 1);
 
+  for (int r = threadIdx.x; r < R; r += NT) {
+    const long long c = c_lo + r;
+    const bool has = c * T / N < (c + 1) * T / N;  // a CTA with an empty range wrote nothing
+    const int slot = (c == c_lo && seg_start > ub_lo) ? 1 : 0;
+    s_rec[r] = has ? (int)(c * 2 + slot) : -1;
+  }
+  __syncthreads();
+  for (int h = warp; h < G; h += NT / 32) {
+    float M = -CUDART_INF_F;
+    for (int r = lane; r < R; r += 32)
+      if (s_rec[r] >= 0) M = fmaxf(M, __ldg(p.records + ((size_t)s_rec[r] * kRecHeads + h) * (D + 2)));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float den = 0.f;
+    for (int r = lane; r < R; r += 32) {
+      float f = 0.f;
+      if (s_rec[r] >= 0) {
+        const float* rec = p.records + ((size_t)s_rec[r] * kRecHeads + h) * (D + 2);
+        const float m = __ldg(rec);
+        if (m != -CUDART_INF_F) {
+          f = exp2f(m - M);
+          den += f * __ldg(rec + 1);
+        }
+      }
+      s_w[r][h] = f;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+    if (lane == 0) s_den[h] = den;
+  }
+  __syncthreads();
   for (int idx = threadIdx.x; idx < G * D; idx += NT) {
     const int h = idx / D;
     const int d = idx - h * D;
-    float M = -CUDART_INF_F;
-    for (long long c = c_lo; c <= c_hi; ++c) {
-      if (c * T / N >= (c + 1) * T / N) continue;  // empty range, no record
-      const int slot = (c == c_lo && seg_start > ub_lo) ? 1 : 0;
-      M = fmaxf(M, __ldg(p.records + ((c * 2 + slot) * kRecHeads + h) * (D + 2)));
+    float num = 0.f;
+    for (int r = 0; r < R; ++r) {
+      const float f = s_w[r][h];
+      if (f != 0.f) num += f * __ldg(p.records + ((size_t)s_rec[r] * kRecHeads + h) * (D + 2) + 2 + d);
     }
-    float num = 0.f, den = 0.f;
-    for (long long c = c_lo; c <= c_hi; ++c) {
-      if (c * T / N >= (c + 1) * T / N) continue;
-      const int slot = (c == c_lo && seg_start > ub_lo) ? 1 : 0;
-      const float* rec = p.records + ((c * 2 + slot) * kRecHeads + h) * (D + 2);
-      const float m = __ldg(rec);
-      if (m == -CUDART_INF_F) continue;
-      const float f = exp2f(m - M);
-      num += f * __ldg(rec + 2 + d);
-      den += f * __ldg(rec + 1);
-    }
+    const float den = s_den[h];
     p.out[(qh0 + h) * D + d] = __float2half_rn(den > 0.f ? num / den : 0.f);
   }
 }
@@ -835,6 +871,8 @@ struct CombineParams {
 // first token is at or past the context length were never written and are
 // not read.
 __global__ void __launch_bounds__(128) splitk_combine_kernel(const CombineParams p) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int sh = blockIdx.x;
   const int s = sh / p.num_heads;
   int L = __ldg(p.context_lens + s);

@@ -15,6 +15,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <utility>
 
 #include "kernels.cuh"
 #include "pagedkv.h"
@@ -59,6 +60,25 @@ pkv_status cuda_fail(cudaError_t e, const char* what) {
 }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Launches with programmatic stream serialization: the kernel's CTAs may
+// start while the previous kernel in the stream finishes; every kernel here
+// waits for it (griddepcontrol.wait) before touching global memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), int grid, int block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3((unsigned)block, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -193,8 +213,7 @@ pkv_status launch_decode(const DecodeArgs& a, const DecodeParams& prm, cudaStrea
   st = make_cache_map(&vmap, a.v_cache, a.num_blocks, a.num_kv_heads, BS, D);
   if (st != PKV_OK) return st;
 
-  kernel<<<grid, W * 32, Shape::kSmemBytes, stream>>>(kmap, vmap, prm);
-  e = cudaGetLastError();
+  e = launch_pdl(kernel, grid, W * 32, Shape::kSmemBytes, stream, kmap, vmap, prm);
   if (e != cudaSuccess) return cuda_fail(e, SPLIT ? "split-K phase 1 launch" : "decode launch");
   return PKV_OK;
 }
@@ -267,13 +286,11 @@ pkv_status launch_balanced(const DecodeArgs& a, float* records, cudaStream_t str
   bp.num_blocks = a.num_blocks;
   bp.num_ctas = N;
   bp.scale_log2 = a.scale * 1.4426950408889634f;
-  kernel<<<N, W * 32, smem, stream>>>(kmap, vmap, bp);
-  e = cudaGetLastError();
+  e = launch_pdl(kernel, N, W * 32, smem, stream, kmap, vmap, bp);
   if (e != cudaSuccess) return cuda_fail(e, "balanced decode launch");
   const long long grid2 = (long long)a.num_seqs * a.num_kv_heads;
   if (grid2 >= (1ll << 31)) return fail(PKV_ERR_INVALID_ARG, "grid too large");
-  balanced_combine_kernel<D, BS><<<(int)grid2, 128, 0, stream>>>(bp);
-  e = cudaGetLastError();
+  e = launch_pdl(balanced_combine_kernel<D, BS>, (int)grid2, 128, 0, stream, bp);
   if (e != cudaSuccess) return cuda_fail(e, "balanced combine launch");
   return PKV_OK;
 }
@@ -384,11 +401,11 @@ pkv_status pkv_append(const void* k, const void* v, const int32_t* slot_mapping,
   const long long total = (long long)num_tokens * num_kv_heads * chunks_per_row;
   long long blocks = (total + 255) / 256;
   if (blocks > 65536) blocks = 65536;  // grid-stride beyond this
-  append_kernel<<<(int)blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+  const cudaError_t e = launch_pdl(
+      append_kernel, (int)blocks, 256, 0, static_cast<cudaStream_t>(stream),
       static_cast<const uint4*>(k), static_cast<const uint4*>(v), slot_mapping, total,
       chunks_per_row, num_kv_heads, block_size, (long long)num_blocks * block_size,
       static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache));
-  const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "append launch");
   return PKV_OK;
 }
@@ -472,8 +489,7 @@ pkv_status pkv_decode_splitk(const void* q, const void* k_cache, const void* v_c
   cp.num_splits = S_eff;
   cp.chunk_tokens = chunk_blocks * block_size;
   cp.cap_tokens = max_blocks_per_seq * block_size;
-  splitk_combine_kernel<<<num_seqs * num_heads, 128, 0, cs>>>(cp);
-  const cudaError_t e = cudaGetLastError();
+  const cudaError_t e = launch_pdl(splitk_combine_kernel, num_seqs * num_heads, 128, 0, cs, cp);
   if (e != cudaSuccess) return cuda_fail(e, "split-K combine launch");
   return PKV_OK;
 }

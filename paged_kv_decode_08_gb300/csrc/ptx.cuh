@@ -74,6 +74,19 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
   }
 }
 
+// ---- programmatic dependent launch ---------------------------------------------
+
+// Lets the next kernel in the stream (launched with programmatic stream
+// serialization) start its CTAs; they still wait in pdl_wait for this grid.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Waits until the grids this one depends on have completed and their memory
+// is visible (returns at once when there is no such dependency).  Every
+// kernel calls it before its first global-memory access.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---- TMA ----------------------------------------------------------------------
 
 // 4-D tiled bulk tensor copy global -> shared, completing on `bar`.

@@ -813,6 +813,8 @@ __global__ void __launch_bounds__(128) balanced_combine_kernel(const BalancedPar
     s_rec[r] = has ? (int)(c * 2 + slot) : -1;
   }
   __syncthreads();
+  // per head: max over records, then weights and the weighted sum of sums;
+  // warp h handles head h, lanes take records (independent loads)
   for (int h = warp; h < G; h += NT / 32) {
     float M = -CUDART_INF_F;
     for (int r = lane; r < R; r += 32)
@@ -825,9 +827,10 @@ __global__ void __launch_bounds__(128) balanced_combine_kernel(const BalancedPar
       if (s_rec[r] >= 0) {
         const float* rec = p.records + ((size_t)s_rec[r] * kRecHeads + h) * (D + 2);
         const float m = __ldg(rec);
+        const float l = __ldg(rec + 1);
         if (m != -CUDART_INF_F) {
           f = exp2f(m - M);
-          den += f * __ldg(rec + 1);
+          den += f * l;
         }
       }
       s_w[r][h] = f;
@@ -841,9 +844,20 @@ __global__ void __launch_bounds__(128) balanced_combine_kernel(const BalancedPar
     const int h = idx / D;
     const int d = idx - h * D;
     float num = 0.f;
-    for (int r = 0; r < R; ++r) {
-      const float f = s_w[r][h];
-      if (f != 0.f) num += f * __ldg(p.records + ((size_t)s_rec[r] * kRecHeads + h) * (D + 2) + 2 + d);
+    int r = 0;
+    for (; r + 4 <= R; r += 4) {
+      float a[4];
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        const int ri = s_rec[r + x];
+        a[x] = ri >= 0 ? __ldg(p.records + ((size_t)ri * kRecHeads + h) * (D + 2) + 2 + d) : 0.f;
+      }
+#pragma unroll
+      for (int x = 0; x < 4; ++x) num += s_w[r + x][h] * a[x];
+    }
+    for (; r < R; ++r) {
+      const int ri = s_rec[r];
+      if (ri >= 0) num += s_w[r][h] * __ldg(p.records + ((size_t)ri * kRecHeads + h) * (D + 2) + 2 + d);
     }
     const float den = s_den[h];
     p.out[(qh0 + h) * D + d] = __float2half_rn(den > 0.f ? num / den : 0.f);
@@ -867,14 +881,21 @@ struct CombineParams {
   int cap_tokens;  // max_blocks_per_seq * block_size
 };
 
-// One CTA per (sequence, query head); threads over head_dim.  Splits whose
-// first token is at or past the context length were never written and are
-// not read.
+// One CTA per (sequence, query head), 128 threads.  Splits whose first token
+// is at or past the context length were never written and are not read.
+// Thread k loads split k's max and sum (all splits at once), the CTA reduces
+// them, and thread d then sums the splits' partial outputs with independent
+// loads.
 __global__ void __launch_bounds__(128) splitk_combine_kernel(const CombineParams p) {
+  constexpr int NT = 128;
+  static_assert(PKV_MAX_SPLITS <= NT, "one thread per split");
+  __shared__ float s_w[PKV_MAX_SPLITS];
+  __shared__ float s_red[NT / 32];
   pdl_launch_dependents();
   pdl_wait();
   const int sh = blockIdx.x;
   const int s = sh / p.num_heads;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int L = __ldg(p.context_lens + s);
   L = L < 0 ? 0 : (L > p.cap_tokens ? p.cap_tokens : L);
   const int n_valid = min(p.num_splits, (L + p.chunk_tokens - 1) / p.chunk_tokens);
@@ -882,20 +903,36 @@ __global__ void __launch_bounds__(128) splitk_combine_kernel(const CombineParams
   const float* pl = p.part_l + (size_t)sh * p.num_splits;
   const float* po = p.part_out + (size_t)sh * p.num_splits * p.head_dim;
 
-  float M = -CUDART_INF_F;
-  for (int k = 0; k < n_valid; ++k) M = fmaxf(M, __ldg(pm + k));
-  float den = 0.f;
-  for (int k = 0; k < n_valid; ++k) {
-    const float mk = __ldg(pm + k);
-    den += (mk == -CUDART_INF_F) ? 0.f : exp2f(mk - M) * __ldg(pl + k);
-  }
-  for (int d = threadIdx.x; d < p.head_dim; d += blockDim.x) {
+  const int k = threadIdx.x;  // num_splits <= PKV_MAX_SPLITS = NT
+  const float mk = k < n_valid ? __ldg(pm + k) : -CUDART_INF_F;
+  const float lk = k < n_valid ? __ldg(pl + k) : 0.f;
+  float M = mk;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  if (lane == 0) s_red[warp] = M;
+  __syncthreads();
+  M = fmaxf(fmaxf(s_red[0], s_red[1]), fmaxf(s_red[2], s_red[3]));
+  __syncthreads();
+  const float w = (mk == -CUDART_INF_F) ? 0.f : exp2f(mk - M);
+  if (k < PKV_MAX_SPLITS) s_w[k] = w;
+  float den = w * lk;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+  if (lane == 0) s_red[warp] = den;
+  __syncthreads();
+  den = s_red[0] + s_red[1] + s_red[2] + s_red[3];
+
+  for (int d = threadIdx.x; d < p.head_dim; d += NT) {
     float num = 0.f;
-    for (int k = 0; k < n_valid; ++k) {
-      const float mk = __ldg(pm + k);
-      if (mk == -CUDART_INF_F) continue;
-      num += exp2f(mk - M) * __ldg(po + (size_t)k * p.head_dim + d);
+    int kk = 0;
+    for (; kk + 4 <= n_valid; kk += 4) {
+      const float a0 = __ldg(po + (size_t)kk * p.head_dim + d);
+      const float a1 = __ldg(po + (size_t)(kk + 1) * p.head_dim + d);
+      const float a2 = __ldg(po + (size_t)(kk + 2) * p.head_dim + d);
+      const float a3 = __ldg(po + (size_t)(kk + 3) * p.head_dim + d);
+      num += s_w[kk] * a0 + s_w[kk + 1] * a1 + s_w[kk + 2] * a2 + s_w[kk + 3] * a3;
     }
+    for (; kk < n_valid; ++kk) num += s_w[kk] * __ldg(po + (size_t)kk * p.head_dim + d);
     p.out[(size_t)sh * p.head_dim + d] = __float2half_rn(den > 0.f ? num / den : 0.f);
   }
 }

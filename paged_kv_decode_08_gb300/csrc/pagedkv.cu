@@ -367,7 +367,7 @@ int32_t pkv_pick_num_splits(int32_t num_seqs, int32_t num_kv_heads, int32_t max_
   if (base >= slots) {
     s = (max_context_len + kSaturatedChunkTokens - 1) / kSaturatedChunkTokens;
   } else {
-    s = slots / base;  // every split CTA resident in one wave
+    s = (2 * slots + base) / (2 * base);  // nearest to one wave of split CTAs
   }
   const long long by_len = max_context_len / kMinSplitTokens;
   const long long max_blocks = (max_context_len + block_size - 1) / block_size;

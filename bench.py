@@ -56,7 +56,11 @@ N_SETS = 4  # default number of rotating pool sets (--sets)
 # DRAM bytes (read + write) of one decode launch on this workload, from the
 # ncu capture summarised in profiles/ (kernel source hash at capture time).
 # Reported as null when the kernels have changed since.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # profiles/decode_llama8b.md: split-K phase-1 launch, dram read 175.086 MB + write 3.590 MB
+    "llama8b": {"kernel_hash": "1e959f1a9bff6398", "bytes_per_launch": 178675712,
+                "kernel": "paged_decode_kernel<128,16,4,2,split> (phase 1)"},
+}
 
 
 def kernel_source_hash():
@@ -376,8 +380,8 @@ def run_ours(args):
     achieved = kv_bytes / (dec_avg_ms * 1e-3) / 1e9
     peak, peak_kind = measured_peaks()
     traffic = None
-    tr = NCU_TRAFFIC.get("llama8b")
-    if tr and tr.get("kernel_hash") == kernel_source_hash():
+    tr = NCU_TRAFFIC.get(args.workload)
+    if tr and tr.get("kernel_hash") == kernel_source_hash() and S == 2:
         traffic = tr["bytes_per_launch"]
     cpu = None if args.no_cpu_baseline else cpu_baseline_subprocess()
     line = {
@@ -401,7 +405,8 @@ def run_ours(args):
                      "frac": achieved / peak, "peak_source": peak_kind,
                      "kernel": "decode call (phase 1 + combine when split), timed as a graph "
                                "of back-to-back decode calls",
-                     "traffic": traffic},
+                     "traffic": traffic,
+                     "traffic_kernel": tr["kernel"] if traffic is not None else None},
         "clocks": clocks.summary(),
         "gpu_launches": launches_per_step * steps,
         "device_status_flags": flags,

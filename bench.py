@@ -61,7 +61,7 @@ N_SETS = 4  # default number of rotating pool sets (--sets)
 # Reported as null when the kernels have changed since.
 NCU_TRAFFIC = {
     # profiles/decode_llama8b.md: split-K phase-1 launch, dram read 175.086 MB + write 3.590 MB
-    "llama8b": {"kernel_hash": "1e959f1a9bff6398", "bytes_per_launch": 178675712,
+    "llama8b": {"kernel_hash": "1e959f1a9bff6398", "bytes_per_launch": 178675712, "num_splits": 2,
                 "kernel": "paged_decode_kernel<128,16,4,2,split> (phase 1)"},
 }
 
@@ -498,7 +498,7 @@ def run_ours(args):
     peak, peak_kind = measured_peaks()
     traffic = None
     tr = NCU_TRAFFIC.get(args.workload)
-    if tr and tr.get("kernel_hash") == kernel_source_hash() and S == 2:
+    if tr and tr.get("kernel_hash") == kernel_source_hash() and S == tr.get("num_splits"):
         traffic = tr["bytes_per_launch"]
     cpu = None if args.no_cpu_baseline else cpu_baseline_subprocess()
     line = {

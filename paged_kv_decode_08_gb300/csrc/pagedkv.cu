@@ -21,15 +21,16 @@
 #include "pagedkv.h"
 
 // Warps per decode CTA and the shared-memory ring they split (KB); the
-// defaults give three resident CTAs per SM.  Overridable at build time.
+// defaults (6 warps, 96 KB: two resident CTAs per SM) won a sweep of warps x
+// ring x CTAs per SM on all five workloads.  Overridable at build time.
 #ifndef PKV_DECODE_WARPS
-#define PKV_DECODE_WARPS 4
+#define PKV_DECODE_WARPS 6
 #endif
 #ifndef PKV_DECODE_RING_KB
-#define PKV_DECODE_RING_KB 64
+#define PKV_DECODE_RING_KB 96
 #endif
 #ifndef PKV_CTAS_PER_SM
-#define PKV_CTAS_PER_SM 3
+#define PKV_CTAS_PER_SM 2
 #endif
 
 

@@ -69,8 +69,8 @@ def test_scratch_bytes(pk):
 @pytest.mark.parametrize("args,expect", [
     # (num_seqs, num_kv_heads, max_context_len, block_size, num_sms) -> splits
     ((2, 2, 48, 16, 152), 1),          # tiny: too short to split
-    ((32, 8, 2048, 16, 152), 2),       # Llama-3-8B shape: 2 x 256 CTAs is nearest one wave of 456
-    ((4, 8, 131072, 16, 152), 14),     # long context: fill 3 CTAs x 152 SMs
+    ((32, 8, 2048, 16, 152), 1),       # Llama-3-8B shape: 256 CTAs are nearest one wave of 304
+    ((4, 8, 131072, 16, 152), 10),     # long context: fill 2 CTAs x 152 SMs
     ((256, 4, 16384, 32, 152), 8),     # ragged batch: saturated, cap 2048 tokens per CTA
     ((128, 16, 4352, 16, 152), 3),     # append+decode loop
     ((1, 1, 1 << 20, 16, 152), 64),    # capped at 64

@@ -60,9 +60,9 @@ N_SETS = 4  # default number of rotating pool sets (--sets)
 # ncu capture summarised in profiles/ (kernel source hash at capture time).
 # Reported as null when the kernels have changed since.
 NCU_TRAFFIC = {
-    # profiles/decode_llama8b.md: split-K phase-1 launch, dram read 175.086 MB + write 3.590 MB
-    "llama8b": {"kernel_hash": "1e959f1a9bff6398", "bytes_per_launch": 178675712, "num_splits": 2,
-                "kernel": "paged_decode_kernel<128,16,4,2,split> (phase 1)"},
+    # profiles/decode_llama8b.md: single-pass launch, dram read 175.087 MB + write 3.740 MB
+    "llama8b": {"kernel_hash": "4579a7c45e3e37a7", "bytes_per_launch": 178826752, "num_splits": 1,
+                "kernel": "paged_decode_kernel<128,16,6,2,single>"},
 }
 
 
@@ -520,8 +520,8 @@ def run_ours(args):
         "pct_of_8TBs": 100.0 * achieved / NOMINAL_HBM_GBS,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_kind,
-                     "kernel": "decode call (phase 1 + combine when split), timed as a graph "
-                               "of back-to-back decode calls",
+                     "kernel": "decode call (single-pass kernel, or phase 1 + combine when "
+                               "split), timed as a graph of back-to-back decode calls",
                      "traffic": traffic,
                      "traffic_kernel": tr["kernel"] if traffic is not None else None},
         "clocks": clocks.summary(),

@@ -575,50 +575,84 @@ __device__ __forceinline__ void cursor_seek(SegCursor& cu, long long u, const in
 }
 
 // Plans this CTA's range: T, [u_begin, u_end) and the segment holding
-// u_begin.  Returns false (uniformly) when the range is empty.
+// u_begin.  Returns false (uniformly) when the range is empty.  With at most
+// NT sequences one block-wide scan gives everything; otherwise the totals
+// come first and a chunked scan then finds the segment.
 template <int BS, int NT>
 __device__ __forceinline__ bool plan_range(const BalancedParams& p, int c, long long* T_out,
                                            long long* ub, long long* ue, SegCursor* cu,
                                            long long* sm_scan, int* sm_s, long long* sm_P) {
   const int cap = p.max_blocks_per_seq * BS;
   const int B = p.num_seqs, Hkv = p.num_kv_heads;
-  long long mine = 0;
-  for (int s = threadIdx.x; s < B; s += NT) {
-    const int L = __ldg(p.context_lens + s);
-    if ((L < 0 || L > cap) && c == 0) atomicOr(&g_device_status, kDevBadContextLen);
-    mine += (clamped_len<BS>(p.context_lens, s, cap) + BS - 1) / BS;
-  }
-  const long long T = block_sum<NT>(mine, sm_scan) * Hkv;
-  *T_out = T;
-  if (T == 0) return false;
   const long long N = p.num_ctas;
-  const long long u_begin = T * c / N, u_end = T * (c + 1) / N;
-  *ub = u_begin;
-  *ue = u_end;
-  if (u_begin >= u_end) return false;
-
-  if (threadIdx.x == 0) *sm_s = -1;
-  __syncthreads();
-  long long carry = 0;
-  for (int base = 0; base < B; base += NT) {
-    const int s = base + threadIdx.x;
+  if (threadIdx.x == 0) *sm_s = -1;  // ordered before its use by the scan's barriers
+  long long T, u_begin, u_end;
+  if (B <= NT) {
+    const int s = threadIdx.x;
+    const int L = s < B ? __ldg(p.context_lens + s) : 0;
+    if ((L < 0 || L > cap) && c == 0) atomicOr(&g_device_status, kDevBadContextLen);
     const long long n = s < B ? (clamped_len<BS>(p.context_lens, s, cap) + BS - 1) / BS : 0;
-    long long chunk_total;
-    const long long incl = block_incl_scan<NT>(n, sm_scan, &chunk_total);
-    const long long first = carry + incl - n;  // tiles of sequences before s
+    long long total;
+    const long long incl = block_incl_scan<NT>(n, sm_scan, &total);
+    T = total * Hkv;
+    *T_out = T;
+    if (T == 0) return false;
+    u_begin = T * c / N;
+    u_end = T * (c + 1) / N;
+    if (u_begin >= u_end) return false;
+    const long long first = incl - n;
     if (n > 0 && first * Hkv <= u_begin && u_begin < (first + n) * Hkv) {
       *sm_s = s;
       *sm_P = first;
     }
-    carry += chunk_total;
     __syncthreads();
-    if (*sm_s >= 0) break;
+  } else {
+    long long mine = 0;
+    for (int s = threadIdx.x; s < B; s += NT) {
+      const int L = __ldg(p.context_lens + s);
+      if ((L < 0 || L > cap) && c == 0) atomicOr(&g_device_status, kDevBadContextLen);
+      mine += (clamped_len<BS>(p.context_lens, s, cap) + BS - 1) / BS;
+    }
+    T = block_sum<NT>(mine, sm_scan) * Hkv;
+    *T_out = T;
+    if (T == 0) return false;
+    u_begin = T * c / N;
+    u_end = T * (c + 1) / N;
+    if (u_begin >= u_end) return false;
+    long long carry = 0;
+    for (int base = 0; base < B; base += NT) {
+      const int s = base + threadIdx.x;
+      const long long n = s < B ? (clamped_len<BS>(p.context_lens, s, cap) + BS - 1) / BS : 0;
+      long long chunk_total;
+      const long long incl = block_incl_scan<NT>(n, sm_scan, &chunk_total);
+      const long long first = carry + incl - n;  // tiles of sequences before s
+      if (n > 0 && first * Hkv <= u_begin && u_begin < (first + n) * Hkv) {
+        *sm_s = s;
+        *sm_P = first;
+      }
+      carry += chunk_total;
+      __syncthreads();
+      if (*sm_s >= 0) break;
+    }
   }
+  *ub = u_begin;
+  *ue = u_end;
   cu->s = *sm_s;
   cu->P = *sm_P;
   cu->n = (clamped_len<BS>(p.context_lens, cu->s, cap) + BS - 1) / BS;
   cu->g = (int)((u_begin - cu->P * Hkv) / cu->n);
   cu->start = cu->P * Hkv + (long long)cu->g * cu->n;
+  return true;
+}
+
+// Bounded wait for a shared-memory counter to reach `want`.
+__device__ __forceinline__ bool smem_wait_eq(volatile int* x, int want, uint64_t limit_ns) {
+  if (*x == want) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (*x != want) {
+    __nanosleep(64);
+    if (global_timer_ns() - t0 > limit_ns) return false;
+  }
   return true;
 }
 
@@ -633,6 +667,8 @@ paged_decode_balanced_kernel(const __grid_constant__ CUtensorMap kmap,
 
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_failed;
+  __shared__ int s_arrive;  // warps that deposited the current piece
+  __shared__ int s_done;    // pieces merged so far
   __shared__ long long sm_scan[NT / 32];
   __shared__ int sm_s;
   __shared__ long long sm_P;
@@ -661,7 +697,11 @@ paged_decode_balanced_kernel(const __grid_constant__ CUtensorMap kmap,
   const long long span = u_end - u_begin;
   const int my_tiles = span > warp ? (int)((span - warp + W - 1) / W) : 0;
 
-  if (threadIdx.x == 0) s_failed = 0;
+  if (threadIdx.x == 0) {
+    s_failed = 0;
+    s_arrive = 0;
+    s_done = 0;
+  }
   const uint32_t my_bars = bars + warp * P * 8;
   if (lane == 0) {
 #pragma unroll
@@ -692,20 +732,27 @@ paged_decode_balanced_kernel(const __grid_constant__ CUtensorMap kmap,
     for (int k = 0; k < n0; ++k) issue(k);
   }
 
+  // q of the current piece, and of the next one loaded a piece ahead
+  uint32_t qf[KS][2], qn[KS][2];
+  load_q_frags<D>(qf, p.q, (size_t)cc.s * p.num_heads + (size_t)cc.g * G, G, lane);
+  SegCursor nc = cc;
+  bool has_next = cc.start + cc.n < u_end;
+  if (has_next) {
+    cursor_next<BS>(nc, p.context_lens, B, Hkv, cap);
+    load_q_frags<D>(qn, p.q, (size_t)nc.s * p.num_heads + (size_t)nc.g * G, G, lane);
+  }
+
   bool failed = false;
   int k_done = 0;  // tiles this warp has consumed
+  int piece = 0;
   long long u = u_begin;
   while (u < u_end) {
     const long long seg_end = cc.start + cc.n;
     const long long a = u, b = seg_end < u_end ? seg_end : u_end;
     const int L = clamped_len<BS>(p.context_lens, cc.s, cap);
 
-    uint32_t qf[KS][2];
-    load_q_frags<D>(qf, p.q, (size_t)cc.s * p.num_heads + (size_t)cc.g * G, G, lane);
     WarpState<D> st;
     st.reset();
-
-    // this warp's tiles in [a, b)
     const int off = (int)((a - u_begin) % W);
     for (long long t = a + ((warp - off + W) % W); t < b && !failed; t += W) {
       const int k = (int)((t - u_begin - warp) / W);
@@ -726,63 +773,100 @@ paged_decode_balanced_kernel(const __grid_constant__ CUtensorMap kmap,
         issue(k + P);
       }
     }
-    if (failed && lane == 0) atomicOr(&s_failed, 1);
-
     st.finish_sums();
+
+    // Deposit this warp's state for the piece; the last warp to arrive
+    // merges the W states and writes the piece's output or record while the
+    // others go on.  The buffer is free once the previous piece is merged.
+    if (!smem_wait_eq(&s_done, piece, kWaitLimitNs)) failed = true;
+    if (failed && lane == 0) atomicOr(&s_failed, 1);
+    __threadfence_block();
     st.store(red + warp * red_stride, lane, G);
-    __syncthreads();
-    if (!s_failed) {
-      const bool whole = (a == cc.start) && (b == seg_end);
-      const int slot = (a == u_begin) ? 0 : 1;
-      for (int idx = threadIdx.x; idx < G * D; idx += NT) {
-        const int h = idx / D;
-        const int d = idx - h * D;
-        float M, num, den;
-        merge_warps<W, D>(red, red_stride, h, d, M, num, den);
-        if (whole) {
-          const size_t qh = (size_t)cc.s * p.num_heads + (size_t)cc.g * G + h;
-          p.out[qh * D + d] = __float2half_rn(den > 0.f ? num / den : 0.f);
-        } else {
-          float* rec = p.records + (((size_t)c * 2 + slot) * kRecHeads + h) * (D + 2);
-          rec[2 + d] = num;
-          if (d == 0) {
-            rec[0] = M;
-            rec[1] = den;
+    __threadfence_block();
+    __syncwarp();
+    int last = 0;
+    if (lane == 0) {
+      __threadfence_block();
+      last = atomicAdd(&s_arrive, 1) == W - 1;
+    }
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (last) {
+      __threadfence_block();
+      if (!*reinterpret_cast<volatile int*>(&s_failed)) {
+        const bool whole = (a == cc.start) && (b == seg_end);
+        const int slot = (a == u_begin) ? 0 : 1;
+        for (int idx = lane; idx < G * D; idx += 32) {
+          const int h = idx / D;
+          const int d = idx - h * D;
+          float M, num, den;
+          merge_warps<W, D>(red, red_stride, h, d, M, num, den);
+          if (whole) {
+            const size_t qh = (size_t)cc.s * p.num_heads + (size_t)cc.g * G + h;
+            p.out[qh * D + d] = __float2half_rn(den > 0.f ? num / den : 0.f);
+          } else {
+            float* rec = p.records + (((size_t)c * 2 + slot) * kRecHeads + h) * (D + 2);
+            rec[2 + d] = num;
+            if (d == 0) {
+              rec[0] = M;
+              rec[1] = den;
+            }
           }
         }
       }
+      __syncwarp();
+      if (lane == 0) {
+        s_arrive = 0;
+        __threadfence_block();
+        atomicAdd(&s_done, 1);
+      }
     }
-    __syncthreads();
+
+    ++piece;
     u = b;
-    if (u < u_end) cursor_next<BS>(cc, p.context_lens, B, Hkv, cap);
+    if (u < u_end) {
+      cc = nc;
+#pragma unroll
+      for (int i = 0; i < KS; ++i) {
+        qf[i][0] = qn[i][0];
+        qf[i][1] = qn[i][1];
+      }
+      has_next = cc.start + cc.n < u_end;
+      if (has_next) {
+        cursor_next<BS>(nc, p.context_lens, B, Hkv, cap);
+        load_q_frags<D>(qn, p.q, (size_t)nc.s * p.num_heads + (size_t)nc.g * G, G, lane);
+      }
+    }
   }
 
   if (failed) {
     if (lane == 0) atomicOr(&g_device_status, kDevWaitTimeout);
-    const int last = min(k_done + P, my_tiles);
-    for (int k = k_done; k < last; ++k)
+    const int last_k = min(k_done + P, my_tiles);
+    for (int k = k_done; k < last_k; ++k)
       (void)mbar_wait_bounded(my_bars + 8 * (k % P), (k / P) & 1, kWaitLimitNs);
   }
 }
 
-// Merges the records of every segment that a CTA range boundary cut, and
-// writes zeros for empty segments.  One CTA per (sequence, KV head).  The
-// record list and each head's weights are worked out once into shared
-// memory; the threads then sum over records per output element.
+// Merges the records of segments that CTA range boundaries cut, and writes
+// zeros for empty sequences.  One CTA per (sequence, query head), threads
+// over head_dim; each thread sums the records with batches of independent
+// loads.
 template <int D, int BS>
 __global__ void __launch_bounds__(128) balanced_combine_kernel(const BalancedParams p) {
   constexpr int NT = 128;
   __shared__ long long sm_scan[NT / 32];
-  __shared__ int s_rec[PKV_BALANCED_MAX_CTAS];             // record index, -1 = none
-  __shared__ float s_w[PKV_BALANCED_MAX_CTAS][kRecHeads];  // 2^(m - M) per record and head
-  __shared__ float s_den[kRecHeads];
+  __shared__ int s_rec[PKV_BALANCED_MAX_CTAS];   // record index, -1 = none
+  __shared__ float s_w[PKV_BALANCED_MAX_CTAS];   // 2^(m - M) per record
+  __shared__ float s_red[NT / 32];
   pdl_launch_dependents();
   pdl_wait();
-  const int s = blockIdx.x / p.num_kv_heads;
-  const int g = blockIdx.x % p.num_kv_heads;
+  const int s = blockIdx.x / p.num_heads;
+  const int hq = blockIdx.x % p.num_heads;  // query head
+  const int G = p.group;
+  const int g = hq / G, h = hq % G;
   const int cap = p.max_blocks_per_seq * BS;
-  const int B = p.num_seqs, Hkv = p.num_kv_heads, G = p.group;
+  const int B = p.num_seqs, Hkv = p.num_kv_heads;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const size_t orow = ((size_t)s * p.num_heads + hq) * D;
 
   long long all = 0, before = 0;
   for (int s2 = threadIdx.x; s2 < B; s2 += NT) {
@@ -793,9 +877,8 @@ __global__ void __launch_bounds__(128) balanced_combine_kernel(const BalancedPar
   const long long tiles = block_sum<NT>(all, sm_scan);
   const long long Ps = block_sum<NT>(before, sm_scan);
   const long long n = (clamped_len<BS>(p.context_lens, s, cap) + BS - 1) / BS;
-  const size_t qh0 = (size_t)s * p.num_heads + (size_t)g * G;
   if (n == 0) {
-    for (int idx = threadIdx.x; idx < G * D; idx += NT) p.out[qh0 * D + idx] = __float2half_rn(0.f);
+    for (int d = threadIdx.x; d < D; d += NT) p.out[orow + d] = __float2half_rn(0.f);
     return;
   }
   const long long T = tiles * Hkv, N = p.num_ctas;
@@ -807,60 +890,63 @@ __global__ void __launch_bounds__(128) balanced_combine_kernel(const BalancedPar
   const int R = (int)(c_hi - c_lo + 1);
 
   for (int r = threadIdx.x; r < R; r += NT) {
-    const long long c = c_lo + r;
-    const bool has = c * T / N < (c + 1) * T / N;  // a CTA with an empty range wrote nothing
-    const int slot = (c == c_lo && seg_start > ub_lo) ? 1 : 0;
-    s_rec[r] = has ? (int)(c * 2 + slot) : -1;
+    const long long cr = c_lo + r;
+    const bool has = cr * T / N < (cr + 1) * T / N;  // an empty range wrote nothing
+    const int slot = (cr == c_lo && seg_start > ub_lo) ? 1 : 0;
+    const int ri = has ? (int)(cr * 2 + slot) : -1;
+    s_rec[r] = ri;
   }
   __syncthreads();
-  // per head: max over records, then weights and the weighted sum of sums;
-  // warp h handles head h, lanes take records (independent loads)
-  for (int h = warp; h < G; h += NT / 32) {
-    float M = -CUDART_INF_F;
-    for (int r = lane; r < R; r += 32)
-      if (s_rec[r] >= 0) M = fmaxf(M, __ldg(p.records + ((size_t)s_rec[r] * kRecHeads + h) * (D + 2)));
+  float M = -CUDART_INF_F;
+  for (int r = threadIdx.x; r < R; r += NT) {
+    const int ri = s_rec[r];
+    if (ri >= 0) M = fmaxf(M, __ldg(p.records + ((size_t)ri * kRecHeads + h) * (D + 2)));
+  }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float den = 0.f;
-    for (int r = lane; r < R; r += 32) {
-      float f = 0.f;
-      if (s_rec[r] >= 0) {
-        const float* rec = p.records + ((size_t)s_rec[r] * kRecHeads + h) * (D + 2);
-        const float m = __ldg(rec);
-        const float l = __ldg(rec + 1);
-        if (m != -CUDART_INF_F) {
-          f = exp2f(m - M);
-          den += f * l;
-        }
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  if (lane == 0) s_red[warp] = M;
+  __syncthreads();
+  M = fmaxf(fmaxf(s_red[0], s_red[1]), fmaxf(s_red[2], s_red[3]));
+  __syncthreads();
+  float den = 0.f;
+  for (int r = threadIdx.x; r < R; r += NT) {
+    const int ri = s_rec[r];
+    float f = 0.f;
+    if (ri >= 0) {
+      const float* rec = p.records + ((size_t)ri * kRecHeads + h) * (D + 2);
+      const float mr = __ldg(rec);
+      const float lr = __ldg(rec + 1);
+      if (mr != -CUDART_INF_F) {
+        f = exp2f(mr - M);
+        den += f * lr;
       }
-      s_w[r][h] = f;
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-    if (lane == 0) s_den[h] = den;
+    s_w[r] = f;
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+  if (lane == 0) s_red[warp] = den;
   __syncthreads();
-  for (int idx = threadIdx.x; idx < G * D; idx += NT) {
-    const int h = idx / D;
-    const int d = idx - h * D;
+  den = s_red[0] + s_red[1] + s_red[2] + s_red[3];
+
+  for (int d = threadIdx.x; d < D; d += NT) {
     float num = 0.f;
     int r = 0;
-    for (; r + 4 <= R; r += 4) {
-      float a[4];
+    for (; r + 8 <= R; r += 8) {
+      float a[8];
 #pragma unroll
-      for (int x = 0; x < 4; ++x) {
+      for (int x = 0; x < 8; ++x) {
         const int ri = s_rec[r + x];
         a[x] = ri >= 0 ? __ldg(p.records + ((size_t)ri * kRecHeads + h) * (D + 2) + 2 + d) : 0.f;
       }
 #pragma unroll
-      for (int x = 0; x < 4; ++x) num += s_w[r + x][h] * a[x];
+      for (int x = 0; x < 8; ++x) num += s_w[r + x] * a[x];
     }
     for (; r < R; ++r) {
       const int ri = s_rec[r];
-      if (ri >= 0) num += s_w[r][h] * __ldg(p.records + ((size_t)ri * kRecHeads + h) * (D + 2) + 2 + d);
+      if (ri >= 0) num += s_w[r] * __ldg(p.records + ((size_t)ri * kRecHeads + h) * (D + 2) + 2 + d);
     }
-    const float den = s_den[h];
-    p.out[(qh0 + h) * D + d] = __float2half_rn(den > 0.f ? num / den : 0.f);
+    p.out[orow + d] = __float2half_rn(den > 0.f ? num / den : 0.f);
   }
 }
 

@@ -289,7 +289,7 @@ pkv_status launch_balanced(const DecodeArgs& a, float* records, cudaStream_t str
   bp.scale_log2 = a.scale * 1.4426950408889634f;
   e = launch_pdl(kernel, N, W * 32, smem, stream, kmap, vmap, bp);
   if (e != cudaSuccess) return cuda_fail(e, "balanced decode launch");
-  const long long grid2 = (long long)a.num_seqs * a.num_kv_heads;
+  const long long grid2 = (long long)a.num_seqs * a.num_heads;
   if (grid2 >= (1ll << 31)) return fail(PKV_ERR_INVALID_ARG, "grid too large");
   e = launch_pdl(balanced_combine_kernel<D, BS>, (int)grid2, 128, 0, stream, bp);
   if (e != cudaSuccess) return cuda_fail(e, "balanced combine launch");

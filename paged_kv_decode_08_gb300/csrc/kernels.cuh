@@ -475,15 +475,17 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
 // balanced schedule
 // ---------------------------------------------------------------------------
 //
-// The work is the list of all tiles (sequence s, KV head g, logical block j)
-// in (s, g, j) order; a (s, g) run is a "segment".  CTA c of N takes the
-// contiguous range [c*T/N, (c+1)*T/N) of the T tiles, so every CTA moves the
-// same number of K/V bytes whatever the mix of context lengths.  Each CTA
-// plans its range on the device from context_lens (no host read).  Segments
-// that lie wholly inside one CTA's range are finished there (f16 output);
-// a segment cut by a range boundary leaves one partial record (m, l, acc)
-// per CTA piece, merged by balanced_combine_kernel.  A CTA has at most two
-// cut pieces (its first and last), so records are [N][2][8 heads][2 + D] f32.
+// The work is the list of all (sequence s, logical block j) units in (s, j)
+// order, T = the total.  CTA c = m * Hkv + g of N = M * Hkv takes KV head g
+// of the contiguous unit range [m*T/M, (m+1)*T/M), so every CTA moves the
+// same number of K/V bytes whatever the mix of context lengths, and the Hkv
+// CTAs of a range read the Hkv tiles of each physical block (contiguous in
+// the pool) at about the same time.  Each CTA plans its range on the device
+// from context_lens (no host read).  A sequence wholly inside one range is
+// finished there (f16 output); a sequence cut by range boundaries leaves one
+// partial record (m, l, acc) per CTA piece, merged by
+// balanced_combine_kernel.  A CTA has at most two cut pieces (its first and
+// last), so records are [N][2][8 heads][2 + D] f32.
 
 struct BalancedParams {
   const __half* q;
@@ -547,61 +549,58 @@ __device__ __forceinline__ long long block_incl_scan(long long v, long long* sm,
   return v + before;
 }
 
-// Position in the tile list: the segment (s, g) holding a tile and where it
-// starts.  n is the tile count of sequence s, P the tiles of sequences < s.
+// Position in the unit list: the sequence s holding a unit and where its
+// blocks start.  n is the block count of sequence s, start the units of
+// sequences < s.  (The KV head is the CTA's own.)
 struct SegCursor {
-  int s, g, n;
-  long long P, start;
+  int s, n;
+  long long start;
 };
 
 template <int BS>
-__device__ __forceinline__ void cursor_next(SegCursor& cu, const int32_t* lens, int B, int Hkv,
-                                            int cap) {
-  if (++cu.g == Hkv) {
-    cu.g = 0;
-    cu.P += cu.n;
-    do {
-      ++cu.s;
-      cu.n = cu.s < B ? (clamped_len<BS>(lens, cu.s, cap) + BS - 1) / BS : 1;
-    } while (cu.n == 0);
-  }
-  cu.start = cu.P * Hkv + (long long)cu.g * cu.n;
+__device__ __forceinline__ void cursor_next(SegCursor& cu, const int32_t* lens, int B, int cap) {
+  cu.start += cu.n;
+  do {
+    ++cu.s;
+    cu.n = cu.s < B ? (clamped_len<BS>(lens, cu.s, cap) + BS - 1) / BS : 1;
+  } while (cu.n == 0);
 }
 
 template <int BS>
 __device__ __forceinline__ void cursor_seek(SegCursor& cu, long long u, const int32_t* lens, int B,
-                                            int Hkv, int cap) {
-  while (u >= cu.start + cu.n) cursor_next<BS>(cu, lens, B, Hkv, cap);
+                                            int cap) {
+  while (u >= cu.start + cu.n) cursor_next<BS>(cu, lens, B, cap);
 }
 
-// Plans this CTA's range: T, [u_begin, u_end) and the segment holding
-// u_begin.  Returns false (uniformly) when the range is empty.  With at most
-// NT sequences one block-wide scan gives everything; otherwise the totals
-// come first and a chunked scan then finds the segment.
+// Plans this CTA's range: T (units), [u_begin, u_end) and the sequence
+// holding u_begin.  Returns false (uniformly) when the range is empty.  With
+// at most NT sequences one block-wide scan gives everything; otherwise the
+// total comes first and a chunked scan then finds the sequence.
 template <int BS, int NT>
-__device__ __forceinline__ bool plan_range(const BalancedParams& p, int c, long long* T_out,
+__device__ __forceinline__ bool plan_range(const BalancedParams& p, int m, long long* T_out,
                                            long long* ub, long long* ue, SegCursor* cu,
                                            long long* sm_scan, int* sm_s, long long* sm_P) {
   const int cap = p.max_blocks_per_seq * BS;
-  const int B = p.num_seqs, Hkv = p.num_kv_heads;
-  const long long N = p.num_ctas;
+  const int B = p.num_seqs;
+  const long long M = p.num_ctas / p.num_kv_heads;
+  const bool flag = blockIdx.x == 0;
   if (threadIdx.x == 0) *sm_s = -1;  // ordered before its use by the scan's barriers
   long long T, u_begin, u_end;
   if (B <= NT) {
     const int s = threadIdx.x;
     const int L = s < B ? __ldg(p.context_lens + s) : 0;
-    if ((L < 0 || L > cap) && c == 0) atomicOr(&g_device_status, kDevBadContextLen);
+    if ((L < 0 || L > cap) && flag) atomicOr(&g_device_status, kDevBadContextLen);
     const long long n = s < B ? (clamped_len<BS>(p.context_lens, s, cap) + BS - 1) / BS : 0;
     long long total;
     const long long incl = block_incl_scan<NT>(n, sm_scan, &total);
-    T = total * Hkv;
+    T = total;
     *T_out = T;
     if (T == 0) return false;
-    u_begin = T * c / N;
-    u_end = T * (c + 1) / N;
+    u_begin = T * m / M;
+    u_end = T * (m + 1) / M;
     if (u_begin >= u_end) return false;
     const long long first = incl - n;
-    if (n > 0 && first * Hkv <= u_begin && u_begin < (first + n) * Hkv) {
+    if (n > 0 && first <= u_begin && u_begin < first + n) {
       *sm_s = s;
       *sm_P = first;
     }
@@ -610,14 +609,14 @@ __device__ __forceinline__ bool plan_range(const BalancedParams& p, int c, long 
     long long mine = 0;
     for (int s = threadIdx.x; s < B; s += NT) {
       const int L = __ldg(p.context_lens + s);
-      if ((L < 0 || L > cap) && c == 0) atomicOr(&g_device_status, kDevBadContextLen);
+      if ((L < 0 || L > cap) && flag) atomicOr(&g_device_status, kDevBadContextLen);
       mine += (clamped_len<BS>(p.context_lens, s, cap) + BS - 1) / BS;
     }
-    T = block_sum<NT>(mine, sm_scan) * Hkv;
+    T = block_sum<NT>(mine, sm_scan);
     *T_out = T;
     if (T == 0) return false;
-    u_begin = T * c / N;
-    u_end = T * (c + 1) / N;
+    u_begin = T * m / M;
+    u_end = T * (m + 1) / M;
     if (u_begin >= u_end) return false;
     long long carry = 0;
     for (int base = 0; base < B; base += NT) {
@@ -625,8 +624,8 @@ __device__ __forceinline__ bool plan_range(const BalancedParams& p, int c, long 
       const long long n = s < B ? (clamped_len<BS>(p.context_lens, s, cap) + BS - 1) / BS : 0;
       long long chunk_total;
       const long long incl = block_incl_scan<NT>(n, sm_scan, &chunk_total);
-      const long long first = carry + incl - n;  // tiles of sequences before s
-      if (n > 0 && first * Hkv <= u_begin && u_begin < (first + n) * Hkv) {
+      const long long first = carry + incl - n;  // blocks of sequences before s
+      if (n > 0 && first <= u_begin && u_begin < first + n) {
         *sm_s = s;
         *sm_P = first;
       }
@@ -638,10 +637,8 @@ __device__ __forceinline__ bool plan_range(const BalancedParams& p, int c, long 
   *ub = u_begin;
   *ue = u_end;
   cu->s = *sm_s;
-  cu->P = *sm_P;
+  cu->start = *sm_P;
   cu->n = (clamped_len<BS>(p.context_lens, cu->s, cap) + BS - 1) / BS;
-  cu->g = (int)((u_begin - cu->P * Hkv) / cu->n);
-  cu->start = cu->P * Hkv + (long long)cu->g * cu->n;
   return true;
 }
 
@@ -683,6 +680,9 @@ paged_decode_balanced_kernel(const __grid_constant__ CUtensorMap kmap,
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int c = blockIdx.x;
+  const int Hkv = p.num_kv_heads;
+  const int g = c % Hkv;  // this CTA's KV head
+  const int m = c / Hkv;  // and its unit range
 
   pdl_launch_dependents();
   pdl_wait();
@@ -690,10 +690,10 @@ paged_decode_balanced_kernel(const __grid_constant__ CUtensorMap kmap,
 
   long long T, u_begin, u_end;
   SegCursor cc;
-  if (!plan_range<BS, NT>(p, c, &T, &u_begin, &u_end, &cc, sm_scan, &sm_s, &sm_P)) return;
+  if (!plan_range<BS, NT>(p, m, &T, &u_begin, &u_end, &cc, sm_scan, &sm_s, &sm_P)) return;
 
   const int cap = p.max_blocks_per_seq * BS;
-  const int B = p.num_seqs, Hkv = p.num_kv_heads;
+  const int B = p.num_seqs;
   const long long span = u_end - u_begin;
   const int my_tiles = span > warp ? (int)((span - warp + W - 1) / W) : 0;
 
@@ -716,12 +716,12 @@ paged_decode_balanced_kernel(const __grid_constant__ CUtensorMap kmap,
   SegCursor pc = cc;
   auto issue = [&](int k) {
     const long long u = u_begin + warp + (long long)k * W;
-    cursor_seek<BS>(pc, u, p.context_lens, B, Hkv, cap);
+    cursor_seek<BS>(pc, u, p.context_lens, B, cap);
     const int j = (int)(u - pc.start);
     const int phys = __ldg(p.block_tables + (size_t)pc.s * p.max_blocks_per_seq + j);
     const uint32_t bar = my_bars + 8 * (k % P);
     if (phys >= 0 && phys < p.num_blocks) {
-      issue_tile_copy<D, BS>(k_stage(k % P), bar, phys * Hkv + pc.g, &kmap, &vmap);
+      issue_tile_copy<D, BS>(k_stage(k % P), bar, phys * Hkv + g, &kmap, &vmap);
     } else {
       atomicOr(&g_device_status, kDevBadBlockId);
       mbar_arrive(bar);
@@ -734,12 +734,12 @@ paged_decode_balanced_kernel(const __grid_constant__ CUtensorMap kmap,
 
   // q of the current piece, and of the next one loaded a piece ahead
   uint32_t qf[KS][2], qn[KS][2];
-  load_q_frags<D>(qf, p.q, (size_t)cc.s * p.num_heads + (size_t)cc.g * G, G, lane);
+  load_q_frags<D>(qf, p.q, (size_t)cc.s * p.num_heads + (size_t)g * G, G, lane);
   SegCursor nc = cc;
   bool has_next = cc.start + cc.n < u_end;
   if (has_next) {
-    cursor_next<BS>(nc, p.context_lens, B, Hkv, cap);
-    load_q_frags<D>(qn, p.q, (size_t)nc.s * p.num_heads + (size_t)nc.g * G, G, lane);
+    cursor_next<BS>(nc, p.context_lens, B, cap);
+    load_q_frags<D>(qn, p.q, (size_t)nc.s * p.num_heads + (size_t)g * G, G, lane);
   }
 
   bool failed = false;
@@ -801,7 +801,7 @@ paged_decode_balanced_kernel(const __grid_constant__ CUtensorMap kmap,
           float M, num, den;
           merge_warps<W, D>(red, red_stride, h, d, M, num, den);
           if (whole) {
-            const size_t qh = (size_t)cc.s * p.num_heads + (size_t)cc.g * G + h;
+            const size_t qh = (size_t)cc.s * p.num_heads + (size_t)g * G + h;
             p.out[qh * D + d] = __float2half_rn(den > 0.f ? num / den : 0.f);
           } else {
             float* rec = p.records + (((size_t)c * 2 + slot) * kRecHeads + h) * (D + 2);
@@ -832,8 +832,8 @@ paged_decode_balanced_kernel(const __grid_constant__ CUtensorMap kmap,
       }
       has_next = cc.start + cc.n < u_end;
       if (has_next) {
-        cursor_next<BS>(nc, p.context_lens, B, Hkv, cap);
-        load_q_frags<D>(qn, p.q, (size_t)nc.s * p.num_heads + (size_t)nc.g * G, G, lane);
+        cursor_next<BS>(nc, p.context_lens, B, cap);
+        load_q_frags<D>(qn, p.q, (size_t)nc.s * p.num_heads + (size_t)g * G, G, lane);
       }
     }
   }
@@ -881,19 +881,19 @@ __global__ void __launch_bounds__(128) balanced_combine_kernel(const BalancedPar
     for (int d = threadIdx.x; d < D; d += NT) p.out[orow + d] = __float2half_rn(0.f);
     return;
   }
-  const long long T = tiles * Hkv, N = p.num_ctas;
-  const long long seg_start = Ps * Hkv + (long long)g * n, seg_end = seg_start + n;
-  const long long c_lo = ((seg_start + 1) * N - 1) / T;  // owner of the first tile
-  const long long c_hi = (seg_end * N - 1) / T;          // owner of the last tile
-  if (c_lo == c_hi) return;  // finished by its CTA
-  const long long ub_lo = c_lo * T / N;
-  const int R = (int)(c_hi - c_lo + 1);
+  const long long T = tiles, Mp = p.num_ctas / Hkv;
+  const long long seg_start = Ps, seg_end = seg_start + n;
+  const long long m_lo = ((seg_start + 1) * Mp - 1) / T;  // range holding the first block
+  const long long m_hi = (seg_end * Mp - 1) / T;          // range holding the last block
+  if (m_lo == m_hi) return;  // finished by its CTA
+  const long long ub_lo = m_lo * T / Mp;
+  const int R = (int)(m_hi - m_lo + 1);
 
   for (int r = threadIdx.x; r < R; r += NT) {
-    const long long cr = c_lo + r;
-    const bool has = cr * T / N < (cr + 1) * T / N;  // an empty range wrote nothing
-    const int slot = (cr == c_lo && seg_start > ub_lo) ? 1 : 0;
-    const int ri = has ? (int)(cr * 2 + slot) : -1;
+    const long long mr = m_lo + r;
+    const bool has = mr * T / Mp < (mr + 1) * T / Mp;  // an empty range wrote nothing
+    const int slot = (mr == m_lo && seg_start > ub_lo) ? 1 : 0;
+    const int ri = has ? (int)((mr * Hkv + g) * 2 + slot) : -1;
     s_rec[r] = ri;
   }
   __syncthreads();

@@ -264,8 +264,14 @@ pkv_status launch_balanced(const DecodeArgs& a, float* records, cudaStream_t str
   }
   int sms = 0;
   if (current_device_sms(&sms) != 0) return fail(PKV_ERR_CUDA, "cannot query the SM count");
+  // N = M * Hkv: each unit range is taken by one CTA per KV head
   int N = sms * occ;
   if (N > PKV_BALANCED_MAX_CTAS) N = PKV_BALANCED_MAX_CTAS;
+  N = (N / a.num_kv_heads) * a.num_kv_heads;
+  if (N < a.num_kv_heads) N = a.num_kv_heads;
+  if (N > PKV_BALANCED_MAX_CTAS)
+    return fail(PKV_ERR_UNSUPPORTED, "the balanced schedule supports at most %d kv heads",
+                PKV_BALANCED_MAX_CTAS);
 
   CUtensorMap kmap, vmap;
   pkv_status st = make_cache_map(&kmap, a.k_cache, a.num_blocks, a.num_kv_heads, BS, D);

@@ -83,6 +83,13 @@ append_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
 // decode
 // ---------------------------------------------------------------------------
 
+// Fair-share depth: a CTA keeps copies in flight in proportion to its share
+// of the longest chunk in the call (HBM serves outstanding requests about
+// evenly, so every CTA then progresses at the same fraction of its work).
+#ifndef PKV_SHAPE_DEPTH
+#define PKV_SHAPE_DEPTH 0
+#endif
+
 struct DecodeParams {
   const __half* q;              // [B][H][D]
   const int32_t* block_tables;  // [B][MBPS]
@@ -91,6 +98,7 @@ struct DecodeParams {
   float* part_out;              // [B][H][S][D]          (split-K)
   float* part_m;                // [B][H][S]  base-2 running max
   float* part_l;                // [B][H][S]  running sum
+  int num_seqs;
   int num_heads;
   int num_kv_heads;
   int group;
@@ -372,7 +380,30 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   const int blk_begin = tok_begin / BS;
   const int n_tiles = (tok_end - tok_begin + BS - 1) / BS;
   const int32_t* table = p.block_tables + (size_t)s * p.max_blocks_per_seq;
-  const int my_tiles = n_tiles > warp ? (n_tiles - warp + W - 1) / W : 0;
+
+  // Warps that take tiles: all W, or (fair share) W scaled by this chunk's
+  // tiles over the longest chunk of the call.
+  int WE = W;
+  if (PKV_SHAPE_DEPTH) {
+    __shared__ int s_max[W];
+    int mx = 0;
+    for (int i = threadIdx.x; i < p.num_seqs; i += W * 32) {
+      int Li = __ldg(p.context_lens + i);
+      Li = Li < 0 ? 0 : (Li > cap ? cap : Li);
+      int ni = (Li + BS - 1) / BS;
+      if (SPLIT && ni > p.chunk_blocks) ni = p.chunk_blocks;
+      mx = max(mx, ni);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) s_max[warp] = mx;
+    __syncthreads();
+    mx = 0;
+#pragma unroll
+    for (int w = 0; w < W; ++w) mx = max(mx, s_max[w]);
+    if (mx > 0) WE = max(1, min(W, (W * n_tiles + mx - 1) / mx));
+  }
+  const int my_tiles = (warp < WE && n_tiles > warp) ? (n_tiles - warp + WE - 1) / WE : 0;
 
   if (threadIdx.x == 0) s_failed = 0;
   const uint32_t my_bars = bars + warp * P * 8;
@@ -388,7 +419,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   // Lane 0: start the copies of this warp's local tile `li` into its stage.
   auto issue = [&](int li) {
     const int stage = li % P;
-    const int j = blk_begin + warp + li * W;
+    const int j = blk_begin + warp + li * WE;
     const int phys = __ldg(table + j);
     const uint32_t bar = my_bars + 8 * stage;
     if (phys >= 0 && phys < p.num_blocks) {
@@ -419,7 +450,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
       failed = true;
       break;
     }
-    const int j = blk_begin + warp + li * W;
+    const int j = blk_begin + warp + li * WE;
     const int phys = __ldg(table + j);
     if (phys >= 0 && phys < p.num_blocks) {
       const uint32_t kb = k_stage(stage);

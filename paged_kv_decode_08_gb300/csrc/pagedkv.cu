@@ -316,6 +316,7 @@ DecodeParams base_params(const DecodeArgs& a) {
   p.block_tables = a.block_tables;
   p.context_lens = a.context_lens;
   p.out = static_cast<__half*>(a.out);
+  p.num_seqs = a.num_seqs;
   p.num_heads = a.num_heads;
   p.num_kv_heads = a.num_kv_heads;
   p.group = a.num_heads / a.num_kv_heads;

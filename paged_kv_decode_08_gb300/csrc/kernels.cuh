@@ -83,13 +83,6 @@ append_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
 // decode
 // ---------------------------------------------------------------------------
 
-// Fair-share depth: a CTA keeps copies in flight in proportion to its share
-// of the longest chunk in the call (HBM serves outstanding requests about
-// evenly, so every CTA then progresses at the same fraction of its work).
-#ifndef PKV_SHAPE_DEPTH
-#define PKV_SHAPE_DEPTH 0
-#endif
-
 struct DecodeParams {
   const __half* q;              // [B][H][D]
   const int32_t* block_tables;  // [B][MBPS]
@@ -107,6 +100,11 @@ struct DecodeParams {
   int num_splits;    // S (1 for single pass)
   int chunk_blocks;  // blocks per split
   float scale_log2;  // scale * log2(e)
+  // Fair-share depth (set when the whole grid is resident at once): a CTA
+  // keeps copies in flight in proportion to its share of the longest chunk
+  // in the call.  HBM serves outstanding requests about evenly, so every CTA
+  // then progresses at the same fraction of its work and they end together.
+  int fair_depth;
 };
 
 template <int D, int BS, int W, int P>
@@ -384,7 +382,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   // Warps that take tiles: all W, or (fair share) W scaled by this chunk's
   // tiles over the longest chunk of the call.
   int WE = W;
-  if (PKV_SHAPE_DEPTH) {
+  if (p.fair_depth) {
     __shared__ int s_max[W];
     int mx = 0;
     for (int i = threadIdx.x; i < p.num_seqs; i += W * 32) {

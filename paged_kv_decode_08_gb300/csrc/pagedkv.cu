@@ -214,7 +214,11 @@ pkv_status launch_decode(const DecodeArgs& a, const DecodeParams& prm, cudaStrea
   st = make_cache_map(&vmap, a.v_cache, a.num_blocks, a.num_kv_heads, BS, D);
   if (st != PKV_OK) return st;
 
-  e = launch_pdl(kernel, grid, W * 32, Shape::kSmemBytes, stream, kmap, vmap, prm);
+  // fair-share depth only pays when every CTA of the grid is resident at once
+  DecodeParams prm2 = prm;
+  int sms = 0;
+  prm2.fair_depth = (current_device_sms(&sms) == 0 && grid <= sms * kCtasPerSm) ? 1 : 0;
+  e = launch_pdl(kernel, grid, W * 32, Shape::kSmemBytes, stream, kmap, vmap, prm2);
   if (e != cudaSuccess) return cuda_fail(e, SPLIT ? "split-K phase 1 launch" : "decode launch");
   return PKV_OK;
 }

@@ -60,8 +60,8 @@ N_SETS = 4  # default number of rotating pool sets (--sets)
 # ncu capture summarised in profiles/ (kernel source hash at capture time).
 # Reported as null when the kernels have changed since.
 NCU_TRAFFIC = {
-    # profiles/decode_llama8b.md: single-pass launch, dram read 175.087 MB + write 3.740 MB
-    "llama8b": {"kernel_hash": "4579a7c45e3e37a7", "bytes_per_launch": 178826752, "num_splits": 1,
+    # profiles/decode_llama8b.md: single-pass launch, dram read 175.096 MB + write 3.659 MB
+    "llama8b": {"kernel_hash": "ce46e6f1c86ce018", "bytes_per_launch": 178754560, "num_splits": 1,
                 "kernel": "paged_decode_kernel<128,16,6,2,single>"},
 }
 

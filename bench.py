@@ -385,13 +385,17 @@ def run_ours(args):
     out = torch.empty_like(q)
     stream = torch.cuda.current_stream()
     kv_bytes = w.kv_bytes
-    launches_per_step = 1 + (2 if S > 1 else 1)
+    launches_per_step = (1 if args.separate else 0) + (2 if S > 1 else 1)
 
     def step(i):
         st = sets[i % n_sets]
-        pk.pkv_append(k_new_d, v_new_d, slots_d, st["k_cache"], st["v_cache"])
-        pk.pkv_decode_splitk(q, st["k_cache"], st["v_cache"], bt, cl, w.scale,
-                             num_splits=args.splits, scratch=scratch, out=out)
+        if args.separate:
+            pk.pkv_append(k_new_d, v_new_d, slots_d, st["k_cache"], st["v_cache"])
+            pk.pkv_decode_splitk(q, st["k_cache"], st["v_cache"], bt, cl, w.scale,
+                                 num_splits=args.splits, scratch=scratch, out=out)
+        else:
+            pk.pkv_append_decode(k_new_d, v_new_d, slots_d, st["k_cache"], st["v_cache"], q, bt,
+                                 cl, w.scale, num_splits=args.splits, scratch=scratch, out=out)
 
     def decode_only(i):
         st = sets[i % n_sets]
@@ -467,9 +471,16 @@ def run_ours(args):
             slots_d.copy_(h_s, non_blocking=True)
             d_bt.copy_(h_bt, non_blocking=True)
             d_cl.copy_(h_cl, non_blocking=True)
-            pk.pkv_append(k_new_d, v_new_d, slots_d, st["k_cache"], st["v_cache"], stream=stream)
-            pk.pkv_decode_splitk(d_q, st["k_cache"], st["v_cache"], d_bt, d_cl, w.scale,
-                                 num_splits=args.splits, scratch=scratch, out=out, stream=stream)
+            if args.separate:
+                pk.pkv_append(k_new_d, v_new_d, slots_d, st["k_cache"], st["v_cache"],
+                              stream=stream)
+                pk.pkv_decode_splitk(d_q, st["k_cache"], st["v_cache"], d_bt, d_cl, w.scale,
+                                     num_splits=args.splits, scratch=scratch, out=out,
+                                     stream=stream)
+            else:
+                pk.pkv_append_decode(k_new_d, v_new_d, slots_d, st["k_cache"], st["v_cache"],
+                                     d_q, d_bt, d_cl, w.scale, num_splits=args.splits,
+                                     scratch=scratch, out=out, stream=stream)
             h_out.copy_(out, non_blocking=True)
 
         for i in range(args.warmup):
@@ -506,8 +517,11 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
         "config": {"workload": WORKLOAD_DESC[args.workload],
-                   "step": f"pkv_append ({w.num_seqs} tokens) + pkv_decode_splitk "
-                           f"({'heuristic' if args.splits == 0 else 'forced'})",
+                   "step": (f"pkv_append ({w.num_seqs} tokens) + pkv_decode_splitk"
+                            if args.separate else
+                            f"pkv_append_decode (slot-mapped append of the {w.num_seqs} "
+                            "newest tokens fused with the decode)")
+                           + f", split count {'heuristic' if args.splits == 0 else 'forced'}",
                    "num_splits": S,
                    "launch": f"CUDA graph of {n_sets} steps (one per pool set), replayed",
                    "l2": f"{n_sets} rotating pool set(s) ({n_sets * 2 * sets[0]['k_cache'].numel() * 2 / 1e9:.1f} GB; "
@@ -544,6 +558,9 @@ def main():
     ap.add_argument("--splits", type=int, default=0, help="0 = heuristic")
     ap.add_argument("--sets", type=int, default=N_SETS, help="rotating pool sets")
     ap.add_argument("--workload", choices=sorted(WORKLOAD_DESC), default="llama8b")
+    ap.add_argument("--separate", action="store_true",
+                    help="step = pkv_append then pkv_decode_splitk (two calls) instead of "
+                         "the fused pkv_append_decode")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -159,6 +159,39 @@ pkv_status pkv_decode_splitk(const void* q, const void* k_cache, const void* v_c
                              size_t scratch_bytes, void* stream);
 
 /*
+ * pkv_append_decode — one decode step in one launch: the slot-mapped append
+ * of each sequence's newest token followed by the decode of
+ * pkv_decode_splitk (the per-layer kv write then paged attention of
+ * kapsl-backends src/gguf_native.rs, forward_batch_decode_greedy).
+ *
+ *   k_new, v_new  device f16 [num_seqs][num_kv_heads][head_dim], 16-byte
+ *                 aligned: row s is sequence s's newest token, at position
+ *                 context_lens[s] - 1
+ *   slot_mapping  device int32 [num_seqs]: the slot of that position
+ *                 (block_tables[s][p / block_size] * block_size +
+ *                 p % block_size, p = context_lens[s] - 1), or < 0 to
+ *                 append nothing for sequence s
+ *   other arguments as pkv_decode_splitk
+ *
+ * The result equals pkv_append(k_new, v_new, slot_mapping, num_seqs, ...)
+ * then pkv_decode_splitk(...): the cache ends with the new rows written and
+ * out holds the attention over every context including them.  The decode CTA
+ * that reads position context_lens[s] - 1 writes the row and uses it
+ * directly.  A non-negative slot that is not that position's slot is not
+ * written (PKV_DEV_BAD_SLOT is set) and the decode reads the cache as it is.
+ * With num_splits = PKV_SPLITS_BALANCED the append runs as its own kernel
+ * first.
+ */
+pkv_status pkv_append_decode(const void* k_new, const void* v_new, const int32_t* slot_mapping,
+                             void* k_cache, void* v_cache, const void* q,
+                             const int32_t* block_tables, const int32_t* context_lens,
+                             int32_t num_seqs, int32_t max_blocks_per_seq, int32_t num_blocks,
+                             float scale, int32_t num_heads, int32_t num_kv_heads,
+                             int32_t head_dim, int32_t block_size, void* out,
+                             int32_t num_splits, void* scratch, size_t scratch_bytes,
+                             void* stream);
+
+/*
  * pkv_splitk_scratch_bytes — bytes of scratch pkv_decode_splitk needs for S
  * splits: f32 partial outputs [num_seqs][num_heads][S][head_dim] followed by
  * f32 running max and running sum [num_seqs][num_heads][S] each (every part

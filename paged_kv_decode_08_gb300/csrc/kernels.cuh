@@ -105,6 +105,13 @@ struct DecodeParams {
   // in the call.  HBM serves outstanding requests about evenly, so every CTA
   // then progresses at the same fraction of its work and they end together.
   int fair_depth;
+  // Fused append (pkv_append_decode; null when off): token s is sequence s's
+  // newest position context_lens[s] - 1, written at new_slots[s] (< 0: none).
+  const __half* k_new;  // [B][Hkv][D]
+  const __half* v_new;
+  const int32_t* new_slots;  // [B]
+  __half* k_cache;           // the pools, for the row writes
+  __half* v_cache;
 };
 
 template <int D, int BS, int W, int P>
@@ -403,6 +410,42 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   }
   const int my_tiles = (warp < WE && n_tiles > warp) ? (n_tiles - warp + WE - 1) / WE : 0;
 
+  // Fused append: the CTA whose chunk holds position L-1 writes this KV
+  // head's new row into the pools and, for its own attention, patches the
+  // row into that tile in shared memory once the tile's copy has landed (so
+  // it never depends on the global write being visible to its TMA reads).
+  // A slot other than that position's is neither written nor used: flagged.
+  constexpr int HPL = D / 32;  // halves per lane of one row
+  int fuse_li = -1;            // local tile index of the new row, in its owner warp
+  int fuse_row = 0;
+  uint32_t kn[HPL / 2], vn[HPL / 2];
+  if (p.new_slots != nullptr && L > 0 && L - 1 >= tok_begin && L - 1 < tok_end) {
+    const int pos = L - 1;
+    const int slot = __ldg(p.new_slots + s);
+    if (slot >= 0) {
+      const int phys = __ldg(table + pos / BS);
+      const bool ok = phys >= 0 && phys < p.num_blocks && slot == phys * BS + pos % BS;
+      if (!ok) {
+        if (threadIdx.x == 0) atomicOr(&g_device_status, kDevBadSlot);
+      } else {
+        const int idx = pos / BS - blk_begin;  // tile within the chunk
+        if (warp == idx % WE) {
+          fuse_li = idx / WE;
+          fuse_row = pos % BS;
+          const size_t src = ((size_t)s * p.num_kv_heads + g) * D + lane * HPL;
+          const size_t dst = (((size_t)phys * p.num_kv_heads + g) * BS + fuse_row) * D + lane * HPL;
+#pragma unroll
+          for (int x = 0; x < HPL / 2; ++x) {
+            kn[x] = __ldg(reinterpret_cast<const uint32_t*>(p.k_new + src) + x);
+            vn[x] = __ldg(reinterpret_cast<const uint32_t*>(p.v_new + src) + x);
+            reinterpret_cast<uint32_t*>(p.k_cache + dst)[x] = kn[x];
+            reinterpret_cast<uint32_t*>(p.v_cache + dst)[x] = vn[x];
+          }
+        }
+      }
+    }
+  }
+
   if (threadIdx.x == 0) s_failed = 0;
   const uint32_t my_bars = bars + warp * P * 8;
   if (lane == 0) {
@@ -452,6 +495,16 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     const int phys = __ldg(table + j);
     if (phys >= 0 && phys < p.num_blocks) {
       const uint32_t kb = k_stage(stage);
+      if (li == fuse_li) {
+        // the new row of this tile comes from the step's k/v, not the copy
+#pragma unroll
+        for (int x = 0; x < HPL / 2; ++x) {
+          const int d = lane * HPL + 2 * x;
+          asm volatile("st.shared.u32 [%0], %1;" ::"r"(kb + swz<BS>(fuse_row, d)), "r"(kn[x]) : "memory");
+          asm volatile("st.shared.u32 [%0], %1;" ::"r"(kb + TB + swz<BS>(fuse_row, d)), "r"(vn[x]) : "memory");
+        }
+        __syncwarp();
+      }
       consume_tile<D, BS>(kb, kb + TB, j * BS, tok_end, qf, p.scale_log2, st, lane);
     }
     __syncwarp();

@@ -332,10 +332,30 @@ DecodeParams base_params(const DecodeArgs& a) {
   return p;
 }
 
-pkv_status single_pass(const DecodeArgs& a, cudaStream_t stream) {
+// The fused append of pkv_append_decode (all null: none).
+struct FuseArgs {
+  const void* k_new = nullptr;
+  const void* v_new = nullptr;
+  const int32_t* slots = nullptr;
+  void* k_cache = nullptr;
+  void* v_cache = nullptr;
+};
+
+void apply_fuse(DecodeParams& p, const FuseArgs* f) {
+  if (!f) return;
+  p.k_new = static_cast<const __half*>(f->k_new);
+  p.v_new = static_cast<const __half*>(f->v_new);
+  p.new_slots = f->slots;
+  p.k_cache = static_cast<__half*>(f->k_cache);
+  p.v_cache = static_cast<__half*>(f->v_cache);
+}
+
+pkv_status single_pass(const DecodeArgs& a, cudaStream_t stream, const FuseArgs* fuse = nullptr) {
   const long long grid = (long long)a.num_seqs * a.num_kv_heads;
   if (grid >= (1ll << 31)) return fail(PKV_ERR_INVALID_ARG, "grid too large");
-  return dispatch_decode<false>(a, base_params(a), stream, (int)grid);
+  DecodeParams prm = base_params(a);
+  apply_fuse(prm, fuse);
+  return dispatch_decode<false>(a, prm, stream, (int)grid);
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -436,21 +456,21 @@ pkv_status pkv_decode(const void* q, const void* k_cache, const void* v_cache,
   return single_pass(a, static_cast<cudaStream_t>(stream));
 }
 
-pkv_status pkv_decode_splitk(const void* q, const void* k_cache, const void* v_cache,
-                             const int32_t* block_tables, const int32_t* context_lens,
-                             int32_t num_seqs, int32_t max_blocks_per_seq, int32_t num_blocks,
-                             float scale, int32_t num_heads, int32_t num_kv_heads,
-                             int32_t head_dim, int32_t block_size, void* out, int32_t num_splits,
-                             void* scratch, size_t scratch_bytes, void* stream) {
-  const DecodeArgs a{q, k_cache, v_cache, block_tables, context_lens, num_seqs,
-                     max_blocks_per_seq, num_blocks, scale, num_heads, num_kv_heads,
-                     head_dim, block_size, out};
-  pkv_status st = validate_decode(a);
-  if (st != PKV_OK) return st;
+}  // extern "C"
+
+namespace pkv {
+namespace {
+
+// The body of pkv_decode_splitk and pkv_append_decode (arguments validated).
+pkv_status decode_impl(const DecodeArgs& a, int num_splits, void* scratch, size_t scratch_bytes,
+                       cudaStream_t cs, const FuseArgs* fuse) {
+  pkv_status st = PKV_OK;
+  const int num_seqs = a.num_seqs, num_kv_heads = a.num_kv_heads, num_heads = a.num_heads;
+  const int max_blocks_per_seq = a.max_blocks_per_seq, block_size = a.block_size;
+  const int head_dim = a.head_dim;
   if (num_splits < PKV_SPLITS_BALANCED || num_splits > PKV_MAX_SPLITS)
     return fail(PKV_ERR_INVALID_ARG, "num_splits %d outside -1..%d", num_splits, PKV_MAX_SPLITS);
   if (num_seqs == 0) return PKV_OK;
-  cudaStream_t cs = static_cast<cudaStream_t>(stream);
 
   int S = num_splits;
   if (S == 0) {
@@ -464,11 +484,16 @@ pkv_status pkv_decode_splitk(const void* q, const void* k_cache, const void* v_c
       return fail(PKV_ERR_SCRATCH_TOO_SMALL, "the balanced schedule needs %zu scratch bytes, got %zu",
                   need_b, scratch ? scratch_bytes : (size_t)0);
     if (!aligned(scratch, 16)) return fail(PKV_ERR_INVALID_ARG, "scratch must be 16-byte aligned");
+    if (fuse) {  // the balanced kernel does not fuse: append first, in stream order
+      st = pkv_append(fuse->k_new, fuse->v_new, fuse->slots, num_seqs, fuse->k_cache,
+                      fuse->v_cache, a.num_blocks, block_size, num_kv_heads, head_dim, cs);
+      if (st != PKV_OK) return st;
+    }
     return dispatch_balanced(a, static_cast<float*>(scratch), cs);
   }
   const int chunk_blocks = (max_blocks_per_seq + S - 1) / S;
   const int S_eff = (max_blocks_per_seq + chunk_blocks - 1) / chunk_blocks;
-  if (S_eff <= 1) return single_pass(a, cs);
+  if (S_eff <= 1) return single_pass(a, cs, fuse);
 
   const size_t need = pkv_splitk_scratch_bytes(num_seqs, num_heads, head_dim, S_eff);
   if (!scratch || scratch_bytes < need)
@@ -481,6 +506,7 @@ pkv_status pkv_decode_splitk(const void* q, const void* k_cache, const void* v_c
   const size_t rows = (size_t)num_seqs * num_heads * S_eff;
   uint8_t* base = static_cast<uint8_t*>(scratch);
   DecodeParams prm = base_params(a);
+  apply_fuse(prm, fuse);
   prm.num_splits = S_eff;
   prm.chunk_blocks = chunk_blocks;
   prm.part_out = reinterpret_cast<float*>(base);
@@ -494,8 +520,8 @@ pkv_status pkv_decode_splitk(const void* q, const void* k_cache, const void* v_c
   cp.part_out = prm.part_out;
   cp.part_m = prm.part_m;
   cp.part_l = prm.part_l;
-  cp.context_lens = context_lens;
-  cp.out = static_cast<__half*>(out);
+  cp.context_lens = a.context_lens;
+  cp.out = static_cast<__half*>(a.out);
   cp.num_heads = num_heads;
   cp.head_dim = head_dim;
   cp.num_splits = S_eff;
@@ -504,6 +530,52 @@ pkv_status pkv_decode_splitk(const void* q, const void* k_cache, const void* v_c
   const cudaError_t e = launch_pdl(splitk_combine_kernel, num_seqs * num_heads, 128, 0, cs, cp);
   if (e != cudaSuccess) return cuda_fail(e, "split-K combine launch");
   return PKV_OK;
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" {
+
+pkv_status pkv_decode_splitk(const void* q, const void* k_cache, const void* v_cache,
+                             const int32_t* block_tables, const int32_t* context_lens,
+                             int32_t num_seqs, int32_t max_blocks_per_seq, int32_t num_blocks,
+                             float scale, int32_t num_heads, int32_t num_kv_heads,
+                             int32_t head_dim, int32_t block_size, void* out, int32_t num_splits,
+                             void* scratch, size_t scratch_bytes, void* stream) {
+  const DecodeArgs a{q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                     max_blocks_per_seq, num_blocks, scale, num_heads, num_kv_heads,
+                     head_dim, block_size, out};
+  pkv_status st = validate_decode(a);
+  if (st != PKV_OK) return st;
+  return decode_impl(a, num_splits, scratch, scratch_bytes, static_cast<cudaStream_t>(stream),
+                     nullptr);
+}
+
+pkv_status pkv_append_decode(const void* k_new, const void* v_new, const int32_t* slot_mapping,
+                             void* k_cache, void* v_cache, const void* q,
+                             const int32_t* block_tables, const int32_t* context_lens,
+                             int32_t num_seqs, int32_t max_blocks_per_seq, int32_t num_blocks,
+                             float scale, int32_t num_heads, int32_t num_kv_heads,
+                             int32_t head_dim, int32_t block_size, void* out, int32_t num_splits,
+                             void* scratch, size_t scratch_bytes, void* stream) {
+  const DecodeArgs a{q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                     max_blocks_per_seq, num_blocks, scale, num_heads, num_kv_heads,
+                     head_dim, block_size, out};
+  pkv_status st = validate_decode(a);
+  if (st != PKV_OK) return st;
+  if (!k_new || !v_new || !slot_mapping)
+    return fail(PKV_ERR_INVALID_ARG, "k_new, v_new and slot_mapping must not be NULL");
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(slot_mapping, 4))
+    return fail(PKV_ERR_INVALID_ARG,
+                "k_new and v_new must be 16-byte aligned, slot_mapping 4-byte aligned");
+  FuseArgs f;
+  f.k_new = k_new;
+  f.v_new = v_new;
+  f.slots = slot_mapping;
+  f.k_cache = k_cache;
+  f.v_cache = v_cache;
+  return decode_impl(a, num_splits, scratch, scratch_bytes, static_cast<cudaStream_t>(stream), &f);
 }
 
 pkv_status pkv_read_device_status(int32_t* flags, void* stream) {

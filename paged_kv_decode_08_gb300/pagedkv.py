@@ -55,6 +55,9 @@ def _load():
     lib.pkv_decode_splitk.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, f32, i32, i32, i32, i32,
                                       vp, i32, vp, sz, vp]
     lib.pkv_decode_splitk.restype = i32
+    lib.pkv_append_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, f32, i32,
+                                      i32, i32, i32, vp, i32, vp, sz, vp]
+    lib.pkv_append_decode.restype = i32
     lib.pkv_decode_splitk_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, f32, i32, i32,
                                               i32, i32, vp, i32, vp]
     lib.pkv_decode_splitk_noalloc.restype = i32
@@ -211,6 +214,29 @@ def pkv_decode_splitk(q, k_cache, v_cache, block_tables, context_lens, scale, nu
                                  float(scale), H, Hkv, D, bs, out.data_ptr(), int(num_splits),
                                  scratch.data_ptr(), scratch.numel(), _stream_ptr(stream)),
            "pkv_decode_splitk")
+    return out
+
+
+def pkv_append_decode(k_new, v_new, slot_mapping, k_cache, v_cache, q, block_tables,
+                      context_lens, scale, num_splits=0, scratch=None, out=None, stream=None):
+    """One decode step: append row s of ``k_new``/``v_new`` (sequence s's newest
+    token) at ``slot_mapping[s]`` and decode; returns ``out``."""
+    import torch
+
+    B, H, D, NB, Hkv, bs, mbps, out = _decode_shapes(q, k_cache, v_cache, block_tables,
+                                                     context_lens, out)
+    _want(k_new, "k_new", torch.float16, 3, (B, Hkv, D))
+    _want(v_new, "v_new", torch.float16, 3, (B, Hkv, D))
+    _want(slot_mapping, "slot_mapping", torch.int32, 1, (B,))
+    if scratch is None:
+        scratch = alloc_scratch(q, k_cache, block_tables, num_splits)
+    _want(scratch, "scratch", torch.uint8, 1)
+    _check(lib.pkv_append_decode(k_new.data_ptr(), v_new.data_ptr(), slot_mapping.data_ptr(),
+                                 k_cache.data_ptr(), v_cache.data_ptr(), q.data_ptr(),
+                                 block_tables.data_ptr(), context_lens.data_ptr(), B, mbps, NB,
+                                 float(scale), H, Hkv, D, bs, out.data_ptr(), int(num_splits),
+                                 scratch.data_ptr(), scratch.numel(), _stream_ptr(stream)),
+           "pkv_append_decode")
     return out
 
 

@@ -30,7 +30,8 @@ def declared_functions():
 
 def test_header_declares_the_expected_calls():
     names = declared_functions()
-    for n in ["pkv_append", "pkv_decode", "pkv_decode_splitk", "pkv_splitk_scratch_bytes",
+    for n in ["pkv_append", "pkv_decode", "pkv_decode_splitk", "pkv_append_decode",
+              "pkv_splitk_scratch_bytes",
               "pkv_pick_num_splits", "pkv_status_string", "pkv_last_error",
               "pkv_read_device_status"]:
         assert n in names
@@ -162,3 +163,19 @@ def test_noalloc_rejects_oversized_requests_before_any_cuda_call(pk):
     assert st == pk.PKV_ERR_SCRATCH_TOO_SMALL
     assert "built-in buffer" in pk.last_error()
     assert f(F16, F16, F16, F16, F16, 2, 3, 8, 0.1, 4, 2, 64, 16, F16, -2, None) == -1
+
+
+def test_append_decode_rejects_bad_arguments(pk):
+    f = pk.lib.pkv_append_decode
+    ok = [F16, F16, F16, F16, F16, F16, F16, F16, 2, 3, 8, 0.125, 4, 2, 64, 16, F16, 0, None, 0,
+          None]
+    bad_k = list(ok)
+    bad_k[0] = None
+    assert f(*bad_k) == -1
+    misaligned = list(ok)
+    misaligned[1] = F16 + 4
+    assert f(*misaligned) == -1
+    bad_group = list(ok)
+    bad_group[12] = 5  # 5 heads over 2 kv heads
+    assert f(*bad_group) == -1
+    assert f(*(ok[:8] + [0] + ok[9:])) == 0  # no sequences: nothing to do

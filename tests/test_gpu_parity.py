@@ -332,3 +332,55 @@ def test_balanced_schedule_with_every_length_zero(pk, cuda_device):
     pk.pkv_decode_splitk(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
                          d["context_lens"], w.scale, num_splits=-1, out=out)
     assert torch.count_nonzero(out).item() == 0
+
+
+# ---------------------------------------------------------------------------
+# fused append + decode
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name,splits", [
+    ("tiny", [0, 2, -1]),
+    ("llama8b", [0, 1, 3, -1]),
+    ("ragged", [0, 8]),
+    ("long", [0, 1]),
+])
+def test_append_decode_matches_oracle(pk, cuda_device, name, splits):
+    """One launch appends each sequence's newest token and decodes: the cache
+    ends bit-exact and the output matches the oracle over the full context."""
+    w, ref = workload(name)
+    k_new, v_new, slots = w.last_token_append()
+    kd = torch.from_numpy(k_new).to(cuda_device)
+    vd = torch.from_numpy(v_new).to(cuda_device)
+    sd = torch.from_numpy(slots).to(cuda_device)
+    ids, _, _ = W.compact_blocks(w, upto_last=False)
+    idx = torch.from_numpy(ids).to(cuda_device)
+    hk, hv = W.host_pool(w, upto_last=True)
+    assert oracle.append(k_new, v_new, slots, hk, hv) == []
+    for S in splits:
+        d = W.to_device(w, cuda_device, upto_last=True)
+        out = pk.pkv_append_decode(kd, vd, sd, d["k_cache"], d["v_cache"], d["q"],
+                                   d["block_tables"], d["context_lens"], w.scale, num_splits=S)
+        torch.cuda.synchronize()
+        assert_attention_close(to_np(out), ref, f"{name} fused S={S}")
+        assert_bits_equal(d["k_cache"].index_select(0, idx).cpu().numpy(), hk[ids], f"{name} K S={S}")
+        assert_bits_equal(d["v_cache"].index_select(0, idx).cpu().numpy(), hv[ids], f"{name} V S={S}")
+        assert pk.pkv_read_device_status() == 0
+
+
+def test_append_decode_skips_negative_and_flags_wrong_slots(pk, cuda_device):
+    w = W.small_random(1111, num_seqs=3, num_heads=4, num_kv_heads=2, head_dim=128,
+                       block_size=16, lens=[40, 17, 5])
+    kc, vc = W.host_pool(w)
+    ref = oracle.decode(w.q, kc, vc, w.block_tables, w.context_lens, w.scale)
+    d = W.to_device(w, cuda_device)  # the pool already holds every row
+    before_k = d["k_cache"].clone()
+    before_v = d["v_cache"].clone()
+    junk = torch.full((3, 2, 128), 7.0, dtype=torch.float16, device=cuda_device)
+    wrong = int(w.block_tables[1, 0]) * 16 + 3  # a slot of sequence 1, not its newest position
+    slots = torch.tensor([-1, wrong, -5], dtype=torch.int32, device=cuda_device)
+    out = pk.pkv_append_decode(junk, junk, slots, d["k_cache"], d["v_cache"], d["q"],
+                               d["block_tables"], d["context_lens"], w.scale, num_splits=1)
+    assert pk.pkv_read_device_status() & pk.PKV_DEV_BAD_SLOT
+    assert torch.equal(d["k_cache"].view(torch.int16), before_k.view(torch.int16))
+    assert torch.equal(d["v_cache"].view(torch.int16), before_v.view(torch.int16))
+    assert_attention_close(to_np(out), ref, "nothing appended")

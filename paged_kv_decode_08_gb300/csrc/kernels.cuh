@@ -105,6 +105,12 @@ struct DecodeParams {
   // in the call.  HBM serves outstanding requests about evenly, so every CTA
   // then progresses at the same fraction of its work and they end together.
   int fair_depth;
+  // L2 prefetch: when a warp starts the copy of its local tile li, it also
+  // prefetches tile li + prefetch_ahead into L2 (0 = off), so the copy that
+  // refills the stage later hits L2.
+  int prefetch_ahead;
+  const __half* k_base;  // the pools as global addresses, for the prefetch
+  const __half* v_base;
   // Fused append (pkv_append_decode; null when off): token s is sequence s's
   // newest position context_lens[s] - 1, written at new_slots[s] (< 0: none).
   const __half* k_new;  // [B][Hkv][D]
@@ -229,18 +235,25 @@ __device__ __forceinline__ void consume_tile(uint32_t kb, uint32_t vb, int t0, i
     __syncwarp();
   }
 
-  // S^T = K . Q^T for every 16-token slice of the tile.
+  // S^T = K . Q^T for every 16-token slice of the tile (two accumulators
+  // per slice halve the dependent mma chain).
   float sc[MT][4];
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt) {
+    float s2[4] = {0.f, 0.f, 0.f, 0.f};
     sc[mt][0] = sc[mt][1] = sc[mt][2] = sc[mt][3] = 0.f;
     const int row = mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
       uint32_t a[4];
       ldsm_x4(kb + swz<BS>(row, ks * 16 + (lane >> 4) * 8), a);
-      mma_16816(sc[mt], a, qf[ks][0], qf[ks][1]);
+      if (ks & 1)
+        mma_16816(s2, a, qf[ks][0], qf[ks][1]);
+      else
+        mma_16816(sc[mt], a, qf[ks][0], qf[ks][1]);
     }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) sc[mt][e] += s2[e];
   }
 
   // scale, mask rows past the context, tile max per head
@@ -457,7 +470,8 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
 
   auto k_stage = [&](int stage) { return ring + (warp * P + stage) * Shape::kStageBytes; };
 
-  // Lane 0: start the copies of this warp's local tile `li` into its stage.
+  // Lane 0: start the copies of this warp's local tile `li` into its stage
+  // (and the L2 prefetch of a later tile).
   auto issue = [&](int li) {
     const int stage = li % P;
     const int j = blk_begin + warp + li * WE;
@@ -468,6 +482,15 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     } else {
       atomicOr(&g_device_status, kDevBadBlockId);
       mbar_arrive(bar);
+    }
+    const int lp = li + p.prefetch_ahead;
+    if (p.prefetch_ahead > 0 && lp < my_tiles) {
+      const int pp = __ldg(table + blk_begin + warp + lp * WE);
+      if (pp >= 0 && pp < p.num_blocks) {
+        const size_t off = ((size_t)pp * p.num_kv_heads + g) * (size_t)(BS * D);
+        prefetch_l2(p.k_base + off, TB);
+        prefetch_l2(p.v_base + off, TB);
+      }
     }
   };
 

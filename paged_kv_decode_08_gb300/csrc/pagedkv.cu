@@ -32,6 +32,10 @@
 #ifndef PKV_CTAS_PER_SM
 #define PKV_CTAS_PER_SM 2
 #endif
+// L2 prefetch distance of the decode kernels, in a warp's tiles (0 = off).
+#ifndef PKV_PREFETCH_AHEAD
+#define PKV_PREFETCH_AHEAD 0
+#endif
 
 
 namespace pkv {
@@ -329,6 +333,9 @@ DecodeParams base_params(const DecodeArgs& a) {
   p.num_splits = 1;
   p.chunk_blocks = a.max_blocks_per_seq;
   p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.prefetch_ahead = PKV_PREFETCH_AHEAD;
+  p.k_base = static_cast<const __half*>(a.k_cache);
+  p.v_base = static_cast<const __half*>(a.v_cache);
   return p;
 }
 

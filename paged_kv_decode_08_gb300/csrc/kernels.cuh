@@ -42,6 +42,11 @@ constexpr unsigned int kDevBadBlockId = 0x2u;
 constexpr unsigned int kDevBadContextLen = 0x4u;
 constexpr unsigned int kDevWaitTimeout = 0x8u;
 
+// Split the q.K mma chain of a tile over two accumulators (build flag).
+#ifndef PKV_QK_SPLIT
+#define PKV_QK_SPLIT 1
+#endif
+
 // A tile copy that has not landed after this long is reported, not awaited
 // (a real copy takes microseconds).
 constexpr uint64_t kWaitLimitNs = 100000000ull;
@@ -247,7 +252,7 @@ __device__ __forceinline__ void consume_tile(uint32_t kb, uint32_t vb, int t0, i
     for (int ks = 0; ks < KS; ++ks) {
       uint32_t a[4];
       ldsm_x4(kb + swz<BS>(row, ks * 16 + (lane >> 4) * 8), a);
-      if (ks & 1)
+      if (PKV_QK_SPLIT && (ks & 1))
         mma_16816(s2, a, qf[ks][0], qf[ks][1]);
       else
         mma_16816(sc[mt], a, qf[ks][0], qf[ks][1]);

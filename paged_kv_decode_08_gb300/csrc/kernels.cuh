@@ -110,13 +110,7 @@ struct DecodeParams {
   // in the call.  HBM serves outstanding requests about evenly, so every CTA
   // then progresses at the same fraction of its work and they end together.
   int fair_depth;
-  // L2 prefetch: when a warp starts the copy of its local tile li, it also
-  // prefetches tile li + prefetch_ahead into L2 (0 = off), so the copy that
-  // refills the stage later hits L2.
-  int prefetch_ahead;
-  const __half* k_base;  // the pools as global addresses, for the prefetch
-  const __half* v_base;
-  // Fused append (pkv_append_decode; null when off): token s is sequence s's
+  // Fused append (pkv_append_decode; FUSE kernels only): token s is sequence s's
   // newest position context_lens[s] - 1, written at new_slots[s] (< 0: none).
   const __half* k_new;  // [B][Hkv][D]
   const __half* v_new;
@@ -357,7 +351,7 @@ __device__ __forceinline__ void issue_tile_copy(uint32_t kdst, uint32_t bar, int
   }
 }
 
-template <int D, int BS, int W, int P, bool SPLIT>
+template <int D, int BS, int W, int P, bool SPLIT, bool FUSE>
 __global__ void __launch_bounds__(W * 32)
 paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
@@ -437,7 +431,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   int fuse_li = -1;            // local tile index of the new row, in its owner warp
   int fuse_row = 0;
   uint32_t kn[HPL / 2], vn[HPL / 2];
-  if (p.new_slots != nullptr && L > 0 && L - 1 >= tok_begin && L - 1 < tok_end) {
+  if (FUSE && L > 0 && L - 1 >= tok_begin && L - 1 < tok_end) {
     const int pos = L - 1;
     const int slot = __ldg(p.new_slots + s);
     if (slot >= 0) {
@@ -475,8 +469,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
 
   auto k_stage = [&](int stage) { return ring + (warp * P + stage) * Shape::kStageBytes; };
 
-  // Lane 0: start the copies of this warp's local tile `li` into its stage
-  // (and the L2 prefetch of a later tile).
+  // Lane 0: start the copies of this warp's local tile `li` into its stage.
   auto issue = [&](int li) {
     const int stage = li % P;
     const int j = blk_begin + warp + li * WE;
@@ -487,15 +480,6 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     } else {
       atomicOr(&g_device_status, kDevBadBlockId);
       mbar_arrive(bar);
-    }
-    const int lp = li + p.prefetch_ahead;
-    if (p.prefetch_ahead > 0 && lp < my_tiles) {
-      const int pp = __ldg(table + blk_begin + warp + lp * WE);
-      if (pp >= 0 && pp < p.num_blocks) {
-        const size_t off = ((size_t)pp * p.num_kv_heads + g) * (size_t)(BS * D);
-        prefetch_l2(p.k_base + off, TB);
-        prefetch_l2(p.v_base + off, TB);
-      }
     }
   };
 
@@ -523,7 +507,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     const int phys = __ldg(table + j);
     if (phys >= 0 && phys < p.num_blocks) {
       const uint32_t kb = k_stage(stage);
-      if (li == fuse_li) {
+      if (FUSE && li == fuse_li) {
         // the new row of this tile comes from the step's k/v, not the copy
 #pragma unroll
         for (int x = 0; x < HPL / 2; ++x) {

@@ -32,10 +32,7 @@
 #ifndef PKV_CTAS_PER_SM
 #define PKV_CTAS_PER_SM 2
 #endif
-// L2 prefetch distance of the decode kernels, in a warp's tiles (0 = off).
-#ifndef PKV_PREFETCH_AHEAD
-#define PKV_PREFETCH_AHEAD 0
-#endif
+
 
 
 namespace pkv {
@@ -193,13 +190,13 @@ struct Tuning {
                                : 1;
 };
 
-template <int D, int BS, bool SPLIT>
+template <int D, int BS, bool SPLIT, bool FUSE>
 pkv_status launch_decode(const DecodeArgs& a, const DecodeParams& prm, cudaStream_t stream,
                          int grid) {
   constexpr int W = Tuning<D, BS>::W;
   constexpr int P = Tuning<D, BS>::P;
   using Shape = DecodeShape<D, BS, W, P>;
-  auto kernel = paged_decode_kernel<D, BS, W, P, SPLIT>;
+  auto kernel = paged_decode_kernel<D, BS, W, P, SPLIT, FUSE>;
 
   static std::atomic<unsigned long long> attr_set{0};
   int dev = 0;
@@ -227,14 +224,27 @@ pkv_status launch_decode(const DecodeArgs& a, const DecodeParams& prm, cudaStrea
   return PKV_OK;
 }
 
+template <bool SPLIT, bool FUSE>
+pkv_status dispatch_decode_f(const DecodeArgs& a, const DecodeParams& prm, cudaStream_t stream,
+                             int grid) {
+  if (a.head_dim == 128 && a.block_size == 16)
+    return launch_decode<128, 16, SPLIT, FUSE>(a, prm, stream, grid);
+  if (a.head_dim == 128 && a.block_size == 32)
+    return launch_decode<128, 32, SPLIT, FUSE>(a, prm, stream, grid);
+  if (a.head_dim == 64 && a.block_size == 16)
+    return launch_decode<64, 16, SPLIT, FUSE>(a, prm, stream, grid);
+  if (a.head_dim == 64 && a.block_size == 32)
+    return launch_decode<64, 32, SPLIT, FUSE>(a, prm, stream, grid);
+  return fail(PKV_ERR_UNSUPPORTED, "head_dim %d / block_size %d", a.head_dim, a.block_size);
+}
+
+// Kernels with the fused append only where a call asks for it, so plain
+// decode kernels carry none of its code.
 template <bool SPLIT>
 pkv_status dispatch_decode(const DecodeArgs& a, const DecodeParams& prm, cudaStream_t stream,
                            int grid) {
-  if (a.head_dim == 128 && a.block_size == 16) return launch_decode<128, 16, SPLIT>(a, prm, stream, grid);
-  if (a.head_dim == 128 && a.block_size == 32) return launch_decode<128, 32, SPLIT>(a, prm, stream, grid);
-  if (a.head_dim == 64 && a.block_size == 16) return launch_decode<64, 16, SPLIT>(a, prm, stream, grid);
-  if (a.head_dim == 64 && a.block_size == 32) return launch_decode<64, 32, SPLIT>(a, prm, stream, grid);
-  return fail(PKV_ERR_UNSUPPORTED, "head_dim %d / block_size %d", a.head_dim, a.block_size);
+  return prm.new_slots ? dispatch_decode_f<SPLIT, true>(a, prm, stream, grid)
+                       : dispatch_decode_f<SPLIT, false>(a, prm, stream, grid);
 }
 
 size_t balanced_scratch_bytes(int head_dim) {
@@ -333,9 +343,6 @@ DecodeParams base_params(const DecodeArgs& a) {
   p.num_splits = 1;
   p.chunk_blocks = a.max_blocks_per_seq;
   p.scale_log2 = a.scale * 1.4426950408889634f;
-  p.prefetch_ahead = PKV_PREFETCH_AHEAD;
-  p.k_base = static_cast<const __half*>(a.k_cache);
-  p.v_base = static_cast<const __half*>(a.v_cache);
   return p;
 }
 

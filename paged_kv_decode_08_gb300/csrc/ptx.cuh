@@ -99,12 +99,6 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// Prefetches `bytes` (a multiple of 16) at a 16-byte aligned global address
-// into L2; completes on its own, nothing waits for it.
-__device__ __forceinline__ void prefetch_l2(const void* gaddr, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gaddr), "r"(bytes) : "memory");
-}
-
 // ---- warp-level matrix ops ----------------------------------------------------
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {

@@ -376,13 +376,44 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   const int s = item / p.num_kv_heads;
 
   pdl_launch_dependents();
+  // Barrier set-up touches no global memory: before the dependency wait.
+  if (threadIdx.x == 0) s_failed = 0;
+  const uint32_t my_bars = bars + warp * P * 8;
+  if (lane == 0) {
+#pragma unroll
+    for (int i = 0; i < P; ++i) mbar_init(my_bars + 8 * i, 1);
+    fence_mbar_init();
+  }
   pdl_wait();
-  // After a lost copy has been flagged, later CTAs do no work (and write
-  // nothing) until the host reads and clears the status word.
-  if (*reinterpret_cast<volatile unsigned int*>(&g_device_status) & kDevWaitTimeout) return;
 
+  // Every independent global load of the prologue goes out together: the
+  // status word, the length, the warp's first block-table entry (its first
+  // tile is the chunk's block `warp` whatever the fair share decides; the
+  // entry is in bounds and only used if the tile exists), the lengths for
+  // the fair share and the fused slot.
   const int cap = p.max_blocks_per_seq * BS;
+  const int32_t* table = p.block_tables + (size_t)s * p.max_blocks_per_seq;
+  const unsigned int status = *reinterpret_cast<volatile unsigned int*>(&g_device_status);
   int L = __ldg(p.context_lens + s);
+  const int j0 = (SPLIT ? split * p.chunk_blocks : 0) + warp;
+  const int phys0 = (lane == 0 && j0 < p.max_blocks_per_seq) ? __ldg(table + j0) : -1;
+  int mx = 0;
+  if (p.fair_depth) {
+    for (int i = threadIdx.x; i < p.num_seqs; i += W * 32) {
+      int Li = __ldg(p.context_lens + i);
+      Li = Li < 0 ? 0 : (Li > cap ? cap : Li);
+      int ni = (Li + BS - 1) / BS;
+      if (SPLIT && ni > p.chunk_blocks) ni = p.chunk_blocks;
+      mx = max(mx, ni);
+    }
+  }
+  const int slot_new = FUSE ? __ldg(p.new_slots + s) : -1;
+
+  // After a lost copy has been flagged, later CTAs do no work (and write
+  // nothing) until the host reads and clears the status word.  The decision
+  // is made for the whole CTA at once.
+  if (__syncthreads_or(status & kDevWaitTimeout)) return;
+
   if (L < 0 || L > cap) {
     if (threadIdx.x == 0) atomicOr(&g_device_status, kDevBadContextLen);
     L = L < 0 ? 0 : cap;
@@ -396,21 +427,12 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   }
   const int blk_begin = tok_begin / BS;
   const int n_tiles = (tok_end - tok_begin + BS - 1) / BS;
-  const int32_t* table = p.block_tables + (size_t)s * p.max_blocks_per_seq;
 
   // Warps that take tiles: all W, or (fair share) W scaled by this chunk's
   // tiles over the longest chunk of the call.
   int WE = W;
   if (p.fair_depth) {
     __shared__ int s_max[W];
-    int mx = 0;
-    for (int i = threadIdx.x; i < p.num_seqs; i += W * 32) {
-      int Li = __ldg(p.context_lens + i);
-      Li = Li < 0 ? 0 : (Li > cap ? cap : Li);
-      int ni = (Li + BS - 1) / BS;
-      if (SPLIT && ni > p.chunk_blocks) ni = p.chunk_blocks;
-      mx = max(mx, ni);
-    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     if (lane == 0) s_max[warp] = mx;
@@ -431,49 +453,38 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   int fuse_li = -1;            // local tile index of the new row, in its owner warp
   int fuse_row = 0;
   uint32_t kn[HPL / 2], vn[HPL / 2];
-  if (FUSE && L > 0 && L - 1 >= tok_begin && L - 1 < tok_end) {
+  if (FUSE && L > 0 && L - 1 >= tok_begin && L - 1 < tok_end && slot_new >= 0) {
     const int pos = L - 1;
-    const int slot = __ldg(p.new_slots + s);
-    if (slot >= 0) {
-      const int phys = __ldg(table + pos / BS);
-      const bool ok = phys >= 0 && phys < p.num_blocks && slot == phys * BS + pos % BS;
-      if (!ok) {
-        if (threadIdx.x == 0) atomicOr(&g_device_status, kDevBadSlot);
-      } else {
-        const int idx = pos / BS - blk_begin;  // tile within the chunk
-        if (warp == idx % WE) {
-          fuse_li = idx / WE;
-          fuse_row = pos % BS;
-          const size_t src = ((size_t)s * p.num_kv_heads + g) * D + lane * HPL;
-          const size_t dst = (((size_t)phys * p.num_kv_heads + g) * BS + fuse_row) * D + lane * HPL;
+    const int phys = __ldg(table + pos / BS);
+    const bool ok = phys >= 0 && phys < p.num_blocks && slot_new == phys * BS + pos % BS;
+    if (!ok) {
+      if (threadIdx.x == 0) atomicOr(&g_device_status, kDevBadSlot);
+    } else {
+      const int idx = pos / BS - blk_begin;  // tile within the chunk
+      if (warp == idx % WE) {
+        fuse_li = idx / WE;
+        fuse_row = pos % BS;
+        const size_t src = ((size_t)s * p.num_kv_heads + g) * D + lane * HPL;
+        const size_t dst = (((size_t)phys * p.num_kv_heads + g) * BS + fuse_row) * D + lane * HPL;
 #pragma unroll
-          for (int x = 0; x < HPL / 2; ++x) {
-            kn[x] = __ldg(reinterpret_cast<const uint32_t*>(p.k_new + src) + x);
-            vn[x] = __ldg(reinterpret_cast<const uint32_t*>(p.v_new + src) + x);
-            reinterpret_cast<uint32_t*>(p.k_cache + dst)[x] = kn[x];
-            reinterpret_cast<uint32_t*>(p.v_cache + dst)[x] = vn[x];
-          }
+        for (int x = 0; x < HPL / 2; ++x) {
+          kn[x] = __ldg(reinterpret_cast<const uint32_t*>(p.k_new + src) + x);
+          vn[x] = __ldg(reinterpret_cast<const uint32_t*>(p.v_new + src) + x);
+          reinterpret_cast<uint32_t*>(p.k_cache + dst)[x] = kn[x];
+          reinterpret_cast<uint32_t*>(p.v_cache + dst)[x] = vn[x];
         }
       }
     }
   }
 
-  if (threadIdx.x == 0) s_failed = 0;
-  const uint32_t my_bars = bars + warp * P * 8;
-  if (lane == 0) {
-#pragma unroll
-    for (int i = 0; i < P; ++i) mbar_init(my_bars + 8 * i, 1);
-    fence_mbar_init();
-  }
-  __syncthreads();
-
   auto k_stage = [&](int stage) { return ring + (warp * P + stage) * Shape::kStageBytes; };
 
-  // Lane 0: start the copies of this warp's local tile `li` into its stage.
+  // Lane 0: start the copies of this warp's local tile `li` into its stage
+  // (tile 0's block-table entry was loaded in the prologue).
   auto issue = [&](int li) {
     const int stage = li % P;
     const int j = blk_begin + warp + li * WE;
-    const int phys = __ldg(table + j);
+    const int phys = (li == 0) ? phys0 : __ldg(table + j);
     const uint32_t bar = my_bars + 8 * stage;
     if (phys >= 0 && phys < p.num_blocks) {
       issue_tile_copy<D, BS>(k_stage(stage), bar, phys * p.num_kv_heads + g, &kmap, &vmap);
@@ -780,7 +791,9 @@ paged_decode_balanced_kernel(const __grid_constant__ CUtensorMap kmap,
 
   pdl_launch_dependents();
   pdl_wait();
-  if (*reinterpret_cast<volatile unsigned int*>(&g_device_status) & kDevWaitTimeout) return;
+  if (__syncthreads_or(*reinterpret_cast<volatile unsigned int*>(&g_device_status) &
+                       kDevWaitTimeout))
+    return;
 
   long long T, u_begin, u_end;
   SegCursor cc;

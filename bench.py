@@ -60,9 +60,11 @@ N_SETS = 4  # default number of rotating pool sets (--sets)
 # ncu capture summarised in profiles/ (kernel source hash at capture time).
 # Reported as null when the kernels have changed since.
 NCU_TRAFFIC = {
-    # profiles/decode_llama8b.md: single-pass launch, dram read 175.096 MB + write 3.659 MB
-    "llama8b": {"kernel_hash": "ce46e6f1c86ce018", "bytes_per_launch": 178754560, "num_splits": 1,
-                "kernel": "paged_decode_kernel<128,16,6,2,single>"},
+    # profiles/decode_llama8b.md: the fused append + single-pass decode launch,
+    # dram read 175.218 MB + write 3.241 MB
+    "llama8b": {"kernel_hash": "3fbec2a6293e5277", "bytes_per_launch": 178459136, "num_splits": 1,
+                "fused": True,
+                "kernel": "paged_decode_kernel<128,16,6,2,single,fused>"},
 }
 
 

@@ -8,4 +8,5 @@ from .paged_attention import (  # noqa: F401
     gather_rows,
     kv_head_of,
     softmax,
+    varlen,
 )

@@ -26,6 +26,8 @@ so they do not appear here):
   ``sum_i p_i V_s[i]``.
 * ``context_len == 0`` gives zeros (an empty softmax has no value; zeros are
   the plainest total definition).
+* Multi-token queries (``varlen``): query ``t`` of a sequence sits at
+  ``pos_offset + t`` and attends causally to positions ``0 .. pos_offset + t``.
 * Append.  Token ``t`` with ``slot = slot_mapping[t] >= 0`` is written to
   block ``slot // bs``, row ``slot % bs`` of both pools, for every KV head;
   negative slots are skipped (kapsl ``launch_batch_kv_write`` with a
@@ -140,6 +142,46 @@ def decode_fast(q, k_cache, v_cache, block_tables, context_lens, scale, seqs=Non
             Z = scale * (q[s, heads].astype(np.float64) @ K.T)  # [G][L]
             P = softmax(Z)
             out[s, heads] = P @ V
+    return out
+
+
+def varlen(q, k_cache, v_cache, cu_seqlens_q, pos_offsets, block_tables, scale):
+    """Multi-token queries over the paged context, causal.
+
+    ``q`` f16 ``[total_q][H][D]`` token-major; the queries of sequence ``s``
+    are rows ``cu_seqlens_q[s] .. cu_seqlens_q[s+1]-1``; query ``t`` of ``s``
+    sits at position ``pos_offsets[s] + t`` and attends to positions
+    ``0 .. pos_offsets[s] + t`` of its sequence (ferrum-kernels
+    ``src/backend/cuda/paged.rs``, ``paged_varlen_attention`` and
+    ``paged_decode_attention``: ``pos_offset = final_kv_len - q_len``).
+    Returns float64 ``[total_q][H][D]``.
+    """
+    q = np.asarray(q)
+    total_q, H, D = q.shape
+    NB, Hkv, bs, _ = k_cache.shape
+    if H % Hkv:
+        raise OracleInputError("num_heads must be a multiple of num_kv_heads")
+    group = H // Hkv
+    cu = np.asarray(cu_seqlens_q).astype(np.int64)
+    B = len(cu) - 1
+    if cu[0] != 0 or np.any(np.diff(cu) < 0) or cu[-1] != total_q:
+        raise OracleInputError("cu_seqlens_q must rise from 0 to total_q")
+    lens = np.array([int(pos_offsets[s]) + int(cu[s + 1] - cu[s]) for s in range(B)])
+    if np.any(np.asarray(pos_offsets) < 0):
+        raise OracleInputError("negative pos_offset")
+    _check_tables(block_tables, lens, NB, bs)
+    out = np.zeros((total_q, H, D), np.float64)
+    for s in range(B):
+        row = block_tables[s]
+        for t in range(int(cu[s + 1] - cu[s])):
+            L = int(pos_offsets[s]) + t + 1
+            i = int(cu[s]) + t
+            for h in range(H):
+                g = kv_head_of(h, group)
+                K = gather_rows(k_cache, row, L, g)
+                V = gather_rows(v_cache, row, L, g)
+                z = scale * (K @ q[i, h].astype(np.float64))
+                out[i, h] = softmax(z) @ V
     return out
 
 

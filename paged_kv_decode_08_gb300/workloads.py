@@ -413,3 +413,54 @@ def to_device(w: Workload, device="cuda", upto_last: bool = False, poison_fill=T
         "context_lens": torch.from_numpy(np.ascontiguousarray(w.context_lens)).to(device),
         "q": torch.from_numpy(np.ascontiguousarray(w.q)).to(device),
     }
+
+
+@dataclasses.dataclass
+class VarlenWorkload:
+    """Multi-token queries over a paged context: sequence s has q_lens[s]
+    query tokens at positions pos_offsets[s] .. pos_offsets[s]+q_lens[s]-1,
+    and its cache holds pos_offsets[s] + q_lens[s] rows (the prefix and the
+    new tokens' K/V, already written)."""
+
+    base: Workload  # context_lens = pos_offsets + q_lens; q unused
+    q: np.ndarray  # f16 [total_q][H][D]
+    cu_seqlens_q: np.ndarray  # int32 [B+1]
+    pos_offsets: np.ndarray  # int32 [B]
+
+    @property
+    def total_q(self) -> int:
+        return int(self.cu_seqlens_q[-1])
+
+    @property
+    def max_q_len(self) -> int:
+        return int(np.diff(self.cu_seqlens_q).max()) if len(self.cu_seqlens_q) > 1 else 0
+
+
+def varlen_random(seed: int, num_heads: int, num_kv_heads: int, head_dim: int, block_size: int,
+                  q_lens, prefix_lens, std: float = 1.0, num_blocks: Optional[int] = None
+                  ) -> VarlenWorkload:
+    """A seeded case: sequence s has prefix_lens[s] earlier tokens and
+    q_lens[s] new query tokens."""
+    q_lens = [int(x) for x in q_lens]
+    prefix = [int(x) for x in prefix_lens]
+    base = small_random(seed, num_seqs=len(q_lens), num_heads=num_heads,
+                        num_kv_heads=num_kv_heads, head_dim=head_dim, block_size=block_size,
+                        lens=[p + n for p, n in zip(prefix, q_lens)], num_blocks=num_blocks,
+                        std=std)
+    rng = _rng(seed * 7919 + 13)
+    total_q = sum(q_lens)
+    q = _normal_f16(rng, (total_q, num_heads, head_dim), std)
+    cu = np.zeros(len(q_lens) + 1, np.int32)
+    cu[1:] = np.cumsum(q_lens)
+    return VarlenWorkload(base=base, q=q, cu_seqlens_q=cu,
+                          pos_offsets=np.asarray(prefix, np.int32))
+
+
+def spec_verify() -> VarlenWorkload:
+    """Speculative-decode verification on the Llama-3-8B attention shape:
+    B=32, H=32, Hkv=8, D=128, bs=16, 4 draft tokens per sequence over a
+    prefix ~U[512,2048]."""
+    rng = _rng(BASE_SEED + 5)
+    prefix = rng.integers(508, 2044, size=32, endpoint=True)
+    return varlen_random(BASE_SEED + 5, 32, 8, 128, 16, [4] * 32, prefix,
+                         num_blocks=16384)

@@ -277,7 +277,10 @@ def test_append_skips_negative_and_reports_out_of_range():
 
 MUTATIONS = {
     "dropped_scale": ("z = scale * (K @ q[s, h]", "z = (K @ q[s, h]"),
-    "wrong_gqa_mapping": ("g = kv_head_of(h, group)", "g = h % Hkv"),
+    "wrong_gqa_mapping": ("g = kv_head_of(h, group)\n            K = gather_rows(k_cache, row, L, g)\n"
+                          "            V = gather_rows(v_cache, row, L, g)\n            z = scale * (K @ q[s, h]",
+                          "g = h % Hkv\n            K = gather_rows(k_cache, row, L, g)\n"
+                          "            V = gather_rows(v_cache, row, L, g)\n            z = scale * (K @ q[s, h]"),
     "values_from_keys": ("V = gather_rows(v_cache, row, L, g)\n            z = scale",
                          "V = gather_rows(k_cache, row, L, g)\n            z = scale"),
     "row_index_off_by_one": ("cache[blocks, kv_head, i % bs, :]", "cache[blocks, kv_head, (i + 1) % bs, :]"),

@@ -192,6 +192,41 @@ pkv_status pkv_append_decode(const void* k_new, const void* v_new, const int32_t
                              void* stream);
 
 /*
+ * pkv_varlen_attention — several query tokens per sequence over its paged
+ * context, causal (ferrum-kernels src/backend/cuda/paged.rs,
+ * paged_varlen_attention, and paged_decode_attention with q_len > 1:
+ * pos_offset = final_kv_len - q_len): prefill chunks, speculative-decode
+ * verification, multi-token decode.
+ *
+ *   q             device f16 [total_q][num_heads][head_dim], token-major,
+ *                 4-byte aligned
+ *   cu_seqlens_q  device int32 [num_seqs + 1]: the queries of sequence s are
+ *                 rows cu_seqlens_q[s] .. cu_seqlens_q[s+1]-1 (rising from 0
+ *                 to total_q)
+ *   pos_offsets   device int32 [num_seqs]: position of sequence s's first
+ *                 query; query t sits at pos_offsets[s] + t and attends to
+ *                 positions 0 .. pos_offsets[s] + t, whose K/V must already
+ *                 be in the cache (so pos_offsets[s] + q_len <=
+ *                 max_blocks_per_seq * block_size)
+ *   max_q_len     a host-side bound on every sequence's query count (sizes
+ *                 the grid; queries past it are not computed and
+ *                 PKV_DEV_BAD_CONTEXT_LEN is set)
+ *   out           device f16 [total_q][num_heads][head_dim]
+ *   other arguments as pkv_decode.
+ *
+ * One CTA covers max(1, 8 / group) queries of one sequence and KV head, so
+ * each reads the context once per chunk of queries: meant for short query
+ * runs (a few tokens per sequence), not long prompts.
+ */
+pkv_status pkv_varlen_attention(const void* q, const void* k_cache, const void* v_cache,
+                                const int32_t* cu_seqlens_q, const int32_t* pos_offsets,
+                                const int32_t* block_tables, int32_t num_seqs, int32_t total_q,
+                                int32_t max_q_len, int32_t max_blocks_per_seq,
+                                int32_t num_blocks, float scale, int32_t num_heads,
+                                int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                void* out, void* stream);
+
+/*
  * pkv_splitk_scratch_bytes — bytes of scratch pkv_decode_splitk needs for S
  * splits: f32 partial outputs [num_seqs][num_heads][S][head_dim] followed by
  * f32 running max and running sum [num_seqs][num_heads][S] each (every part

@@ -211,10 +211,11 @@ __device__ __forceinline__ void load_q_frags(uint32_t (&qf)[D / 16][2], const __
 // Folds one K/V tile (already in shared memory at kb / vb) into the warp
 // state.  Token t0 is the tile's first position; positions at or past
 // tok_end are masked.
-template <int D, int BS>
+template <int D, int BS, bool COLMASK = false>
 __device__ __forceinline__ void consume_tile(uint32_t kb, uint32_t vb, int t0, int tok_end,
                                              const uint32_t (&qf)[D / 16][2], float scale_log2,
-                                             WarpState<D>& st, int lane) {
+                                             WarpState<D>& st, int lane, int lim0 = 0,
+                                             int lim1 = 0) {
   constexpr int MT = BS / 16;
   constexpr int KS = D / 16;
   constexpr int HALVES = D / 64;
@@ -263,7 +264,9 @@ __device__ __forceinline__ void consume_tile(uint32_t kb, uint32_t vb, int t0, i
     for (int e = 0; e < 4; ++e) {
       const int tok = t0 + mt * 16 + r + (e >> 1) * 8;
       const float v = sc[mt][e] * scale_log2;
-      sc[mt][e] = tok < tok_end ? v : -CUDART_INF_F;
+      // COLMASK: each column (query) has its own causal limit
+      const int lim = COLMASK ? ((e & 1) ? lim1 : lim0) : tok_end;
+      sc[mt][e] = tok < lim ? v : -CUDART_INF_F;
     }
     x0 = fmaxf(x0, fmaxf(sc[mt][0], sc[mt][2]));
     x1 = fmaxf(x1, fmaxf(sc[mt][1], sc[mt][3]));
@@ -273,12 +276,17 @@ __device__ __forceinline__ void consume_tile(uint32_t kb, uint32_t vb, int t0, i
     x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, o));
     x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, o));
   }
-  const float mn0 = fmaxf(st.m0, x0);
-  const float mn1 = fmaxf(st.m1, x1);
-  const float al0 = exp2f(st.m0 - mn0);  // 0 on the first tile (m = -inf)
-  const float al1 = exp2f(st.m1 - mn1);
+  float mn0 = fmaxf(st.m0, x0);
+  float mn1 = fmaxf(st.m1, x1);
+  float al0 = exp2f(st.m0 - mn0);  // 0 on the first tile (m = -inf)
+  float al1 = exp2f(st.m1 - mn1);
   st.m0 = mn0;
   st.m1 = mn1;
+  if (COLMASK) {
+    // a column with nothing valid so far keeps m = -inf: no rescale, P = 0
+    if (mn0 == -CUDART_INF_F) { al0 = 1.f; mn0 = 0.f; }
+    if (mn1 == -CUDART_INF_F) { al1 = 1.f; mn1 = 0.f; }
+  }
 
   // P = exp2(S - m), rounded to f16 for the tensor cores; the running sum
   // adds the same rounded values so numerator and denominator agree.
@@ -573,6 +581,179 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     } else {
       p.out[qh * D + d] = __float2half_rn(den > 0.f ? num / den : 0.f);
     }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// multi-token queries (varlen, causal)
+// ---------------------------------------------------------------------------
+//
+// One CTA per (sequence, KV head, chunk of QC queries), QC = max(1, 8 / G):
+// the mma's 8 columns are the (query, head) pairs of the chunk.  Query t of
+// sequence s sits at position pos_offsets[s] + t and sees positions up to
+// and including it: each column masks with its own limit.  The chunk reads
+// the context up to its last query's position.
+
+struct VarlenParams {
+  const __half* q;              // [total_q][H][D]
+  const int32_t* cu_seqlens_q;  // [B + 1]
+  const int32_t* pos_offsets;   // [B]
+  const int32_t* block_tables;  // [B][MBPS]
+  __half* out;                  // [total_q][H][D]
+  int total_q;
+  int num_heads;
+  int num_kv_heads;
+  int group;
+  int qc;          // queries per CTA
+  int num_chunks;  // chunks per (sequence, KV head) in the grid
+  int max_blocks_per_seq;
+  int num_blocks;
+  float scale_log2;
+};
+
+template <int D, int BS, int W, int P>
+__global__ void __launch_bounds__(W * 32)
+paged_varlen_kernel(const __grid_constant__ CUtensorMap kmap,
+                    const __grid_constant__ CUtensorMap vmap, const VarlenParams p) {
+  using Shape = DecodeShape<D, BS, W, P>;
+  constexpr int KS = Shape::kKS;
+  constexpr int TB = Shape::kTileBytes;
+
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ int s_failed;
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t ring = smem_addr(smem);
+  const uint32_t bars = ring + Shape::kRingBytes;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int r = lane >> 2, c = lane & 3;
+
+  int item = blockIdx.x;
+  const int qc_idx = item % p.num_chunks;
+  item /= p.num_chunks;
+  const int g = item % p.num_kv_heads;
+  const int s = item / p.num_kv_heads;
+  const int G = p.group;
+
+  pdl_launch_dependents();
+  if (threadIdx.x == 0) s_failed = 0;
+  const uint32_t my_bars = bars + warp * P * 8;
+  if (lane == 0) {
+#pragma unroll
+    for (int i = 0; i < P; ++i) mbar_init(my_bars + 8 * i, 1);
+    fence_mbar_init();
+  }
+  pdl_wait();
+
+  const unsigned int status = *reinterpret_cast<volatile unsigned int*>(&g_device_status);
+  const int cap = p.max_blocks_per_seq * BS;
+  const int q_begin = __ldg(p.cu_seqlens_q + s);
+  const int q_end = __ldg(p.cu_seqlens_q + s + 1);
+  int pos0 = __ldg(p.pos_offsets + s);
+  if (__syncthreads_or(status & kDevWaitTimeout)) return;
+
+  // bad query ranges or positions are flagged and skipped / clamped
+  if (q_begin < 0 || q_end < q_begin || q_end > p.total_q) {
+    if (threadIdx.x == 0) atomicOr(&g_device_status, kDevBadContextLen);
+    return;
+  }
+  const int q_len = q_end - q_begin;
+  if (qc_idx == p.num_chunks - 1 && q_len > p.num_chunks * p.qc && threadIdx.x == 0)
+    atomicOr(&g_device_status, kDevBadContextLen);  // more queries than the grid covers
+  const int t0 = qc_idx * p.qc;
+  if (t0 >= q_len) return;
+  const int nq = min(p.qc, q_len - t0);
+  if (pos0 < 0 || pos0 + q_len > cap) {
+    if (threadIdx.x == 0) atomicOr(&g_device_status, kDevBadContextLen);
+    pos0 = pos0 < 0 ? 0 : max(0, cap - q_len);
+  }
+  const int tok_end = min(cap, pos0 + t0 + nq);  // positions this chunk reads
+  const int n_tiles = (tok_end + BS - 1) / BS;
+  const int32_t* table = p.block_tables + (size_t)s * p.max_blocks_per_seq;
+  const int my_tiles = n_tiles > warp ? (n_tiles - warp + W - 1) / W : 0;
+
+  auto k_stage = [&](int stage) { return ring + (warp * P + stage) * Shape::kStageBytes; };
+  auto issue = [&](int li) {
+    const int stage = li % P;
+    const int j = warp + li * W;
+    const int phys = __ldg(table + j);
+    const uint32_t bar = my_bars + 8 * stage;
+    if (phys >= 0 && phys < p.num_blocks) {
+      issue_tile_copy<D, BS>(k_stage(stage), bar, phys * p.num_kv_heads + g, &kmap, &vmap);
+    } else {
+      atomicOr(&g_device_status, kDevBadBlockId);
+      mbar_arrive(bar);
+    }
+  };
+  if (lane == 0) {
+    const int n0 = my_tiles < P ? my_tiles : P;
+    for (int li = 0; li < n0; ++li) issue(li);
+  }
+
+  // column n = (query t0 + n / G, head n % G) while n < nq * G
+  const int ncols = nq * G;
+  uint32_t qf[KS][2];
+  {
+    const bool live = r < ncols;
+    const size_t row = (size_t)(q_begin + t0 + (live ? r / G : 0)) * p.num_heads +
+                       (size_t)g * G + (live ? r % G : 0);
+    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(p.q + row * D);
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      qf[ks][0] = live ? __ldg(qrow + ks * 8 + c) : 0u;
+      qf[ks][1] = live ? __ldg(qrow + ks * 8 + 4 + c) : 0u;
+    }
+  }
+  // this lane's columns 2c and 2c+1: their causal limits
+  const int lim0 = (2 * c < ncols) ? pos0 + t0 + (2 * c) / G + 1 : tok_end;
+  const int lim1 = (2 * c + 1 < ncols) ? pos0 + t0 + (2 * c + 1) / G + 1 : tok_end;
+
+  WarpState<D> st;
+  st.reset();
+  bool failed = false;
+  int li = 0;
+  for (; li < my_tiles; ++li) {
+    const int stage = li % P;
+    if (!mbar_wait_bounded(my_bars + 8 * stage, (li / P) & 1, kWaitLimitNs)) {
+      failed = true;
+      break;
+    }
+    const int j = warp + li * W;
+    const int phys = __ldg(table + j);
+    if (phys >= 0 && phys < p.num_blocks) {
+      const uint32_t kb = k_stage(stage);
+      consume_tile<D, BS, true>(kb, kb + TB, j * BS, tok_end, qf, p.scale_log2, st, lane, lim0,
+                                lim1);
+    }
+    __syncwarp();
+    if (lane == 0 && li + P < my_tiles) {
+      fence_proxy_async_smem();
+      issue(li + P);
+    }
+  }
+  if (failed) {
+    if (lane == 0) atomicOr(&g_device_status, kDevWaitTimeout);
+    const int last = min(li + P, my_tiles);
+    for (int lj = li; lj < last; ++lj)
+      (void)mbar_wait_bounded(my_bars + 8 * (lj % P), (lj / P) & 1, kWaitLimitNs);
+    if (lane == 0) atomicOr(&s_failed, 1);
+  }
+
+  st.finish_sums();
+  __syncthreads();  // every warp is done with its ring
+  if (s_failed) return;
+  float* red = reinterpret_cast<float*>(smem);
+  st.store(red + warp * Shape::kRedFloats, lane, 8);
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < ncols * D; idx += W * 32) {
+    const int n = idx / D;
+    const int d = idx - n * D;
+    float M, num, den;
+    merge_warps<W, D>(red, Shape::kRedFloats, n, d, M, num, den);
+    const size_t row = (size_t)(q_begin + t0 + n / G) * p.num_heads + (size_t)g * G + n % G;
+    p.out[row * D + d] = __float2half_rn(den > 0.f ? num / den : 0.f);
   }
 }
 

@@ -346,6 +346,33 @@ DecodeParams base_params(const DecodeArgs& a) {
   return p;
 }
 
+template <int D, int BS>
+pkv_status launch_varlen(const DecodeArgs& a, const VarlenParams& vp, cudaStream_t stream,
+                         int grid) {
+  constexpr int W = Tuning<D, BS>::W;
+  constexpr int P = Tuning<D, BS>::P;
+  using Shape = DecodeShape<D, BS, W, P>;
+  auto kernel = paged_varlen_kernel<D, BS, W, P>;
+  static std::atomic<unsigned long long> attr_set{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (!(attr_set.load(std::memory_order_relaxed) & bit)) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Shape::kSmemBytes);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(varlen)");
+    attr_set.fetch_or(bit, std::memory_order_relaxed);
+  }
+  CUtensorMap kmap, vmap;
+  pkv_status st = make_cache_map(&kmap, a.k_cache, a.num_blocks, a.num_kv_heads, BS, D);
+  if (st != PKV_OK) return st;
+  st = make_cache_map(&vmap, a.v_cache, a.num_blocks, a.num_kv_heads, BS, D);
+  if (st != PKV_OK) return st;
+  e = launch_pdl(kernel, grid, W * 32, Shape::kSmemBytes, stream, kmap, vmap, vp);
+  if (e != cudaSuccess) return cuda_fail(e, "varlen attention launch");
+  return PKV_OK;
+}
+
 // The fused append of pkv_append_decode (all null: none).
 struct FuseArgs {
   const void* k_new = nullptr;
@@ -590,6 +617,51 @@ pkv_status pkv_append_decode(const void* k_new, const void* v_new, const int32_t
   f.k_cache = k_cache;
   f.v_cache = v_cache;
   return decode_impl(a, num_splits, scratch, scratch_bytes, static_cast<cudaStream_t>(stream), &f);
+}
+
+pkv_status pkv_varlen_attention(const void* q, const void* k_cache, const void* v_cache,
+                                const int32_t* cu_seqlens_q, const int32_t* pos_offsets,
+                                const int32_t* block_tables, int32_t num_seqs, int32_t total_q,
+                                int32_t max_q_len, int32_t max_blocks_per_seq,
+                                int32_t num_blocks, float scale, int32_t num_heads,
+                                int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                void* out, void* stream) {
+  // pos_offsets stands in for context_lens in the shared checks
+  const DecodeArgs a{q, k_cache, v_cache, block_tables, pos_offsets, num_seqs,
+                     max_blocks_per_seq, num_blocks, scale, num_heads, num_kv_heads,
+                     head_dim, block_size, out};
+  pkv_status st = validate_decode(a);
+  if (st != PKV_OK) return st;
+  if (!cu_seqlens_q || !aligned(cu_seqlens_q, 4))
+    return fail(PKV_ERR_INVALID_ARG, "cu_seqlens_q must be a 4-byte aligned device pointer");
+  if (total_q < 0 || max_q_len < 0) return fail(PKV_ERR_INVALID_ARG, "total_q / max_q_len < 0");
+  if (num_seqs == 0 || total_q == 0 || max_q_len == 0) return PKV_OK;
+  const int G = num_heads / num_kv_heads;
+  const int qc = G >= 8 ? 1 : 8 / G;
+  const int chunks = (max_q_len + qc - 1) / qc;
+  const long long grid = (long long)num_seqs * num_kv_heads * chunks;
+  if (grid >= (1ll << 31)) return fail(PKV_ERR_INVALID_ARG, "grid too large");
+  VarlenParams vp{};
+  vp.q = static_cast<const __half*>(q);
+  vp.cu_seqlens_q = cu_seqlens_q;
+  vp.pos_offsets = pos_offsets;
+  vp.block_tables = block_tables;
+  vp.out = static_cast<__half*>(out);
+  vp.total_q = total_q;
+  vp.num_heads = num_heads;
+  vp.num_kv_heads = num_kv_heads;
+  vp.group = G;
+  vp.qc = qc;
+  vp.num_chunks = chunks;
+  vp.max_blocks_per_seq = max_blocks_per_seq;
+  vp.num_blocks = num_blocks;
+  vp.scale_log2 = scale * 1.4426950408889634f;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (head_dim == 128 && block_size == 16) return launch_varlen<128, 16>(a, vp, cs, (int)grid);
+  if (head_dim == 128 && block_size == 32) return launch_varlen<128, 32>(a, vp, cs, (int)grid);
+  if (head_dim == 64 && block_size == 16) return launch_varlen<64, 16>(a, vp, cs, (int)grid);
+  if (head_dim == 64 && block_size == 32) return launch_varlen<64, 32>(a, vp, cs, (int)grid);
+  return fail(PKV_ERR_UNSUPPORTED, "head_dim %d / block_size %d", head_dim, block_size);
 }
 
 pkv_status pkv_read_device_status(int32_t* flags, void* stream) {

@@ -31,7 +31,7 @@ def declared_functions():
 def test_header_declares_the_expected_calls():
     names = declared_functions()
     for n in ["pkv_append", "pkv_decode", "pkv_decode_splitk", "pkv_append_decode",
-              "pkv_splitk_scratch_bytes",
+              "pkv_varlen_attention", "pkv_splitk_scratch_bytes",
               "pkv_pick_num_splits", "pkv_status_string", "pkv_last_error",
               "pkv_read_device_status"]:
         assert n in names
@@ -179,3 +179,18 @@ def test_append_decode_rejects_bad_arguments(pk):
     bad_group[12] = 5  # 5 heads over 2 kv heads
     assert f(*bad_group) == -1
     assert f(*(ok[:8] + [0] + ok[9:])) == 0  # no sequences: nothing to do
+
+
+def test_varlen_rejects_bad_arguments(pk):
+    f = pk.lib.pkv_varlen_attention
+    ok = [F16, F16, F16, F16, F16, F16, 2, 5, 4, 3, 8, 0.125, 4, 2, 64, 16, F16, None]
+    cu_null = list(ok)
+    cu_null[3] = None
+    assert f(*cu_null) == -1
+    neg = list(ok)
+    neg[7] = -1
+    assert f(*neg) == -1
+    assert f(*(ok[:7] + [0] + ok[8:])) == 0  # no queries
+    bad_d = list(ok)
+    bad_d[14] = 96
+    assert f(*bad_d) == -2

@@ -384,3 +384,71 @@ def test_append_decode_skips_negative_and_flags_wrong_slots(pk, cuda_device):
     assert torch.equal(d["k_cache"].view(torch.int16), before_k.view(torch.int16))
     assert torch.equal(d["v_cache"].view(torch.int16), before_v.view(torch.int16))
     assert_attention_close(to_np(out), ref, "nothing appended")
+
+
+# ---------------------------------------------------------------------------
+# multi-token queries (varlen, causal)
+# ---------------------------------------------------------------------------
+
+def varlen_device(v, dev):
+    d = W.to_device(v.base, dev)
+    d["q"] = torch.from_numpy(v.q).to(dev)
+    d["cu"] = torch.from_numpy(v.cu_seqlens_q).to(dev)
+    d["pos"] = torch.from_numpy(v.pos_offsets).to(dev)
+    return d
+
+
+@pytest.mark.parametrize("H,Hkv,D,bs,q_lens,prefix", [
+    (8, 8, 64, 16, [1, 9, 0, 17], [0, 15, 3, 40]),       # G=1: 8 queries per CTA, 3 chunks
+    (4, 2, 64, 32, [5, 2, 1], [31, 0, 64]),              # G=2
+    (32, 8, 128, 16, [4, 4, 7, 1], [500, 16, 1, 77]),    # G=4
+    (28, 4, 128, 32, [3, 1, 6], [33, 1000, 0]),          # G=7: 1 query per CTA
+    (16, 2, 128, 16, [2, 5], [9, 130]),                  # G=8
+])
+def test_varlen_matches_oracle(pk, cuda_device, H, Hkv, D, bs, q_lens, prefix):
+    v = W.varlen_random(3000 + H + D + bs, H, Hkv, D, bs, q_lens, prefix)
+    kc, vc = W.host_pool(v.base)
+    ref = oracle.varlen(v.q, kc, vc, v.cu_seqlens_q, v.pos_offsets, v.base.block_tables,
+                        v.base.scale)
+    d = varlen_device(v, cuda_device)
+    out = pk.pkv_varlen_attention(d["q"], d["k_cache"], d["v_cache"], d["cu"], d["pos"],
+                                  d["block_tables"], v.base.scale, max_q_len=v.max_q_len)
+    torch.cuda.synchronize()
+    assert_attention_close(to_np(out), ref, f"varlen H{H} Hkv{Hkv} D{D} bs{bs}")
+    assert pk.pkv_read_device_status() == 0
+
+
+def test_varlen_speculative_verification(pk, cuda_device):
+    """Four draft tokens per sequence on the Llama-3-8B attention shape."""
+    v = W.spec_verify()
+    kc, vc = W.host_pool(v.base)
+    ref = oracle.varlen(v.q, kc, vc, v.cu_seqlens_q, v.pos_offsets, v.base.block_tables,
+                        v.base.scale)
+    d = varlen_device(v, cuda_device)
+    out = pk.pkv_varlen_attention(d["q"], d["k_cache"], d["v_cache"], d["cu"], d["pos"],
+                                  d["block_tables"], v.base.scale, max_q_len=4)
+    torch.cuda.synchronize()
+    assert_attention_close(to_np(out), ref, "spec verify")
+    assert pk.pkv_read_device_status() == 0
+
+
+def test_varlen_single_queries_match_decode(pk, cuda_device):
+    v = W.varlen_random(3100, 32, 8, 128, 16, [1] * 5, [0, 17, 300, 511, 63])
+    d = varlen_device(v, cuda_device)
+    a = pk.pkv_varlen_attention(d["q"], d["k_cache"], d["v_cache"], d["cu"], d["pos"],
+                                d["block_tables"], v.base.scale, max_q_len=1)
+    lens = (d["pos"] + 1).contiguous()
+    b = pk.pkv_decode(d["q"], d["k_cache"], d["v_cache"], d["block_tables"], lens, v.base.scale)
+    torch.cuda.synchronize()
+    assert_attention_close(to_np(a), to_np(b), "varlen q_len=1 vs decode")
+
+
+def test_varlen_flags_bad_query_ranges(pk, cuda_device):
+    v = W.varlen_random(3200, 4, 2, 64, 16, [2, 2], [5, 5])
+    d = varlen_device(v, cuda_device)
+    d["cu"] = torch.tensor([0, 2, 9], dtype=torch.int32, device=cuda_device)  # past total_q
+    out = torch.zeros_like(d["q"])
+    pk.pkv_varlen_attention(d["q"], d["k_cache"], d["v_cache"], d["cu"], d["pos"],
+                            d["block_tables"], v.base.scale, max_q_len=4, out=out)
+    assert pk.pkv_read_device_status() & pk.PKV_DEV_BAD_CONTEXT_LEN
+    assert torch.count_nonzero(out[2:]).item() == 0  # sequence 1 skipped

@@ -1,14 +1,22 @@
-// Kernels of libpagedkv: slot-mapped KV append, paged decode attention
-// (single pass, and split-K phase 1), and the log-sum-exp combine of split-K.
+// Kernels of libpagedkv (GB300, sm_103a):
+//   append_kernel                 slot-mapped KV write
+//   paged_decode_kernel           decode: single pass, or split-K phase 1;
+//                                 optionally with the step's append fused in
+//   splitk_combine_kernel         log-sum-exp merge of split-K partials
+//   paged_varlen_kernel           several causal queries per sequence
+//   paged_decode_balanced_kernel  decode over equal tile ranges per CTA
+//   balanced_combine_kernel       merge of the balanced schedule's records
 //
-// Decode design (GB300, sm_103a):
+// Decode design:
 //  * One CTA per (sequence, KV head[, split]).  It covers the whole GQA group
 //    of that KV head, so every K/V byte is read from HBM once.
 //  * Each of the CTA's W warps owns a private ring of P shared-memory stages.
 //    A stage holds the K and V tiles of one physical block for this KV head
 //    (block_size x head_dim f16 each, contiguous in the pool).  Lane 0 of the
 //    warp fetches them with TMA tensor copies (128-byte swizzle) that complete
-//    on the stage's mbarrier.  Warp w takes the chunk's blocks w, w+W, ...
+//    on the stage's mbarrier.  Warp w takes the chunk's blocks w, w+WE, ...
+//    where WE <= W warps are active (fewer for short sequences under the
+//    fair-share depth, see DecodeParams::fair_depth).
 //  * Scores use tensor cores with tokens on M and the group on N:
 //      S^T[16 tok x 8 heads] = K[16 x D] . Q^T[D x 8]      (mma m16n8k16)
 //      O^T[D x 8 heads]     += V^T[D x 16 tok] . P^T[16 x 8]
@@ -21,6 +29,9 @@
 //  * At the end the W warp states are merged through shared memory; the
 //    single-pass kernel writes f16 output, the split-K kernel writes the
 //    unnormalised f32 partial output, max and sum for the combine kernel.
+//  * Every kernel is launched with programmatic dependent launch: it lets the
+//    next kernel start on entry and waits (griddepcontrol.wait) before its
+//    first global-memory access.
 #pragma once
 
 #include <cuda.h>

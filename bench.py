@@ -240,7 +240,7 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-def build_sets(w, dev, n_sets):
+def build_sets(w, dev, n_sets, layout="blocked"):
     """Device pools for the workload: set 0 holds the generator's values, the
     others the same tables with fresh N(0,1) pools (distinct HBM bytes)."""
     import torch
@@ -248,7 +248,7 @@ def build_sets(w, dev, n_sets):
     from paged_kv_decode_08_gb300 import workloads as W
 
     sets = []
-    base = W.to_device(w, dev, upto_last=True)
+    base = (W.to_device_vllm if layout == "vllm" else W.to_device)(w, dev, upto_last=True)
     sets.append(base)
     g = torch.Generator(device=dev)
     for r in range(1, n_sets):
@@ -455,7 +455,12 @@ def run_ours(args):
 
     w = W.make(args.workload)
     n_sets = args.sets
-    sets = build_sets(w, dev, n_sets)
+    vllm = args.layout == "vllm"
+    if vllm:
+        args.separate = True  # no fused append on the vLLM layout
+    sets = build_sets(w, dev, n_sets, args.layout)
+    append_call = pk.pkv_append_vllm_layout if vllm else pk.pkv_append
+    decode_call = pk.pkv_decode_vllm_layout if vllm else pk.pkv_decode_splitk
     k_new, v_new, slots = w.last_token_append()
     k_new_d = torch.from_numpy(k_new).to(dev)
     v_new_d = torch.from_numpy(v_new).to(dev)
@@ -471,17 +476,17 @@ def run_ours(args):
     def step(i):
         st = sets[i % n_sets]
         if args.separate:
-            pk.pkv_append(k_new_d, v_new_d, slots_d, st["k_cache"], st["v_cache"])
-            pk.pkv_decode_splitk(q, st["k_cache"], st["v_cache"], bt, cl, w.scale,
-                                 num_splits=args.splits, scratch=scratch, out=out)
+            append_call(k_new_d, v_new_d, slots_d, st["k_cache"], st["v_cache"])
+            decode_call(q, st["k_cache"], st["v_cache"], bt, cl, w.scale,
+                        num_splits=args.splits, scratch=scratch, out=out)
         else:
             pk.pkv_append_decode(k_new_d, v_new_d, slots_d, st["k_cache"], st["v_cache"], q, bt,
                                  cl, w.scale, num_splits=args.splits, scratch=scratch, out=out)
 
     def decode_only(i):
         st = sets[i % n_sets]
-        pk.pkv_decode_splitk(q, st["k_cache"], st["v_cache"], bt, cl, w.scale,
-                             num_splits=args.splits, scratch=scratch, out=out)
+        decode_call(q, st["k_cache"], st["v_cache"], bt, cl, w.scale,
+                    num_splits=args.splits, scratch=scratch, out=out)
 
     def capture(fn):
         """A CUDA graph of one round: fn(i) for every pool set in turn."""
@@ -531,43 +536,58 @@ def run_ours(args):
     decode_total_ms = max_over_ranks(decode_total_ms, dist, dev)
     decode_ms = decode_total_ms / steps
 
-    # end to end through the public API: pinned host inputs in, result out
+    # end to end through the public API: each step copies its host inputs
+    # (q, the new K/V rows, slots, block tables, lengths), packed in one
+    # pinned buffer, to the device in one copy, runs the step on views of
+    # that device buffer, and copies the output back to pinned memory.
     e2e = None
     if not args.no_e2e:
         import numpy as np
 
-        pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
-        h_q, h_k, h_v, h_s = pin(w.q), pin(k_new), pin(v_new), pin(slots)
-        h_bt, h_cl = pin(w.block_tables), pin(w.context_lens)
+        parts = [("q", np.ascontiguousarray(w.q)), ("k", np.ascontiguousarray(k_new)),
+                 ("v", np.ascontiguousarray(v_new)), ("slots", np.ascontiguousarray(slots)),
+                 ("bt", np.ascontiguousarray(w.block_tables)),
+                 ("cl", np.ascontiguousarray(w.context_lens))]
+        offs, cur = {}, 0
+        for name, a in parts:
+            offs[name] = cur
+            cur += (a.nbytes + 255) // 256 * 256
+        h_buf = torch.empty(cur, dtype=torch.uint8).pin_memory()
+        for name, a in parts:
+            h_buf[offs[name]:offs[name] + a.nbytes] = torch.from_numpy(a.view(np.uint8).reshape(-1))
+        d_buf = torch.empty(cur, dtype=torch.uint8, device=dev)
+
+        def view(name, a, dtype):
+            return d_buf[offs[name]:offs[name] + a.nbytes].view(dtype).view(a.shape)
+
+        d_q = view("q", w.q, torch.float16)
+        d_k = view("k", k_new, torch.float16)
+        d_v = view("v", v_new, torch.float16)
+        d_s = view("slots", slots, torch.int32)
+        d_bt = view("bt", w.block_tables, torch.int32)
+        d_cl = view("cl", w.context_lens, torch.int32)
         h_out = torch.empty(tuple(q.shape), dtype=torch.float16).pin_memory()
-        d_q, d_bt, d_cl = torch.empty_like(q), torch.empty_like(bt), torch.empty_like(cl)
-        h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_s, h_bt, h_cl))
+        h2d = sum(a.nbytes for _, a in parts)
         d2h = h_out.numel() * h_out.element_size()
 
         def e2e_step(i):
             st = sets[i % n_sets]
-            d_q.copy_(h_q, non_blocking=True)
-            k_new_d.copy_(h_k, non_blocking=True)
-            v_new_d.copy_(h_v, non_blocking=True)
-            slots_d.copy_(h_s, non_blocking=True)
-            d_bt.copy_(h_bt, non_blocking=True)
-            d_cl.copy_(h_cl, non_blocking=True)
+            d_buf.copy_(h_buf, non_blocking=True)
             if args.separate:
-                pk.pkv_append(k_new_d, v_new_d, slots_d, st["k_cache"], st["v_cache"],
-                              stream=stream)
-                pk.pkv_decode_splitk(d_q, st["k_cache"], st["v_cache"], d_bt, d_cl, w.scale,
-                                     num_splits=args.splits, scratch=scratch, out=out,
-                                     stream=stream)
+                append_call(d_k, d_v, d_s, st["k_cache"], st["v_cache"], stream=stream)
+                decode_call(d_q, st["k_cache"], st["v_cache"], d_bt, d_cl, w.scale,
+                            num_splits=args.splits, scratch=scratch, out=out, stream=stream)
             else:
-                pk.pkv_append_decode(k_new_d, v_new_d, slots_d, st["k_cache"], st["v_cache"],
-                                     d_q, d_bt, d_cl, w.scale, num_splits=args.splits,
-                                     scratch=scratch, out=out, stream=stream)
+                pk.pkv_append_decode(d_k, d_v, d_s, st["k_cache"], st["v_cache"], d_q, d_bt,
+                                     d_cl, w.scale, num_splits=args.splits, scratch=scratch,
+                                     out=out, stream=stream)
             h_out.copy_(out, non_blocking=True)
 
         for i in range(args.warmup):
             e2e_step(i)
         torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
         for i in range(args.steps):
             e2e_step(i)
@@ -576,7 +596,9 @@ def run_ours(args):
         e2e_ms = max_over_ranks(a.elapsed_time(b), dist, dev)
         e2e = {"value": job_throughput(kv_bytes, world, e2e_ms / args.steps), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": e2e_ms / args.steps}
+               "ms_per_step": e2e_ms / args.steps,
+               "how": "direct Python calls each step: one pinned H2D copy of the packed step "
+                      "inputs, the step, one D2H copy of the output"}
 
     flags = pk.pkv_read_device_status()
     if rank != 0:
@@ -596,7 +618,7 @@ def run_ours(args):
     traffic = None
     tr = NCU_TRAFFIC.get(args.workload)
     if (tr and tr.get("kernel_hash") == kernel_source_hash() and S == tr.get("num_splits")
-            and one_launch == tr.get("fused", False)):
+            and one_launch == tr.get("fused", False) and tr.get("layout", "blocked") == args.layout):
         traffic = tr["bytes_per_launch"]
     cpu = None if args.no_cpu_baseline else cpu_baseline_subprocess()
     line = {
@@ -604,7 +626,9 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
         "config": {"workload": WORKLOAD_DESC[args.workload],
-                   "step": (f"pkv_append ({w.num_seqs} tokens) + pkv_decode_splitk"
+                   "step": (f"pkv_append_vllm_layout ({w.num_seqs} tokens) + "
+                            "pkv_decode_vllm_layout (vLLM cache layout)" if vllm else
+                            f"pkv_append ({w.num_seqs} tokens) + pkv_decode_splitk"
                             if args.separate else
                             f"pkv_append_decode (slot-mapped append of the {w.num_seqs} "
                             "newest tokens fused with the decode)")
@@ -650,6 +674,9 @@ def main():
     ap.add_argument("--separate", action="store_true",
                     help="step = pkv_append then pkv_decode_splitk (two calls) instead of "
                          "the fused pkv_append_decode")
+    ap.add_argument("--layout", choices=["blocked", "vllm"], default="blocked",
+                    help="cache layout: [NB][Hkv][bs][D], or vLLM's K [NB][Hkv][D/8][bs][8] "
+                         "with V [NB][Hkv][D][bs] (append and decode as two calls)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

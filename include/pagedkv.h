@@ -227,6 +227,52 @@ pkv_status pkv_varlen_attention(const void* q, const void* k_cache, const void* 
                                 void* out, void* stream);
 
 /*
+ * The vLLM cache layout: the pools that ferrum-kernels
+ * src/backend/cuda/paged.rs reaches through its vLLM-layout paged write
+ * (split_qkv_norm_rope_into_paged_cache_vllm) and vLLM paged attention
+ * (paged_decode_attention_v2).  The pages name this layout without
+ * spelling it out; it is read as vLLM's published paged-attention layout,
+ * with x = 16 bytes / sizeof(f16) = 8:
+ *
+ *   k_cache  f16 [num_blocks][num_kv_heads][head_dim / 8][block_size][8]:
+ *            element d of the token at offset o of block b, kv head h, is
+ *            k_cache[b][h][d / 8][o][d % 8]
+ *   v_cache  f16 [num_blocks][num_kv_heads][head_dim][block_size]:
+ *            v_cache[b][h][d][o]
+ *
+ * Each (block, kv head) tile is still one contiguous block_size * head_dim
+ * f16 run per pool, so these calls read the same bytes as the blocked ones.
+ * Slots, tables, lengths, q, out, scratch and every status, flag and
+ * size rule are those of pkv_append / pkv_decode_splitk.
+ */
+
+/*
+ * pkv_append_vllm_layout — pkv_append into vLLM-layout pools: for token t
+ * with slot_mapping[t] = b * block_size + o >= 0, k[t][h][d] goes to
+ * k_cache[b][h][d / 8][o][d % 8] and v[t][h][d] to v_cache[b][h][d][o],
+ * bit for bit.  Arguments, skips, flags and errors as pkv_append.
+ */
+pkv_status pkv_append_vllm_layout(const void* k, const void* v, const int32_t* slot_mapping,
+                                  int32_t num_tokens, void* k_cache, void* v_cache,
+                                  int32_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                                  int32_t head_dim, void* stream);
+
+/*
+ * pkv_decode_vllm_layout — pkv_decode_splitk over vLLM-layout pools (the
+ * decode of paged_decode_attention_v2 in ferrum-kernels
+ * src/backend/cuda/paged.rs): the same attention, the same outputs within
+ * rounding.  num_splits 0, 1 or 2..PKV_MAX_SPLITS as for pkv_decode_splitk
+ * (same scratch); PKV_SPLITS_BALANCED returns PKV_ERR_UNSUPPORTED.
+ */
+pkv_status pkv_decode_vllm_layout(const void* q, const void* k_cache, const void* v_cache,
+                                  const int32_t* block_tables, const int32_t* context_lens,
+                                  int32_t num_seqs, int32_t max_blocks_per_seq,
+                                  int32_t num_blocks, float scale, int32_t num_heads,
+                                  int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                  void* out, int32_t num_splits, void* scratch,
+                                  size_t scratch_bytes, void* stream);
+
+/*
  * pkv_splitk_scratch_bytes — bytes of scratch pkv_decode_splitk needs for S
  * splits: f32 partial outputs [num_seqs][num_heads][S][head_dim] followed by
  * f32 running max and running sum [num_seqs][num_heads][S] each (every part

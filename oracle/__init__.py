@@ -3,8 +3,11 @@
 from .paged_attention import (  # noqa: F401
     OracleInputError,
     append,
+    append_vllm_layout,
+    blocked_from_vllm_layout,
     decode,
     decode_fast,
+    decode_vllm_layout,
     gather_rows,
     kv_head_of,
     softmax,

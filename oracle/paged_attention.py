@@ -33,6 +33,18 @@ so they do not appear here):
   negative slots are skipped (kapsl ``launch_batch_kv_write`` with a
   physical block and position-in-block per token, as one integer).
 
+* vLLM cache layout (ferrum-kernels ``src/backend/cuda/paged.rs``, the
+  vLLM-layout paged write and ``paged_decode_attention_v2``; the pages name
+  the layout without spelling it out, so it is read as vLLM's published
+  paged-attention layout with ``x = 16 bytes / 2 = 8``): K is
+  ``[NB][Hkv][D/8][bs][8]``, element ``d`` of the token at row ``o`` of block
+  ``b`` at ``[b, h, d // 8, o, d % 8]``; V is ``[NB][Hkv][D][bs]``, at
+  ``[b, h, d, o]``.  ``append_vllm_layout`` writes element by element;
+  ``blocked_from_vllm_layout`` reads the pools back as ``[NB][Hkv][bs][D]``,
+  after which the definitions above apply unchanged.  Pinned in
+  ``tests/test_oracle_vllm_layout.py`` by a round trip through the blocked
+  append and by chunk contiguity found by search.
+
 Parity pins (in ``tests/test_oracle_pins.py``): contiguous equivalence against
 ``torch.nn.functional.scaled_dot_product_attention`` in float64, invariance
 under a permutation of physical blocks, ``context_len == 1`` returning that V
@@ -200,3 +212,60 @@ def append(k, v, slot_mapping, k_cache, v_cache):
         k_cache[blk, :, off, :] = k[t]
         v_cache[blk, :, off, :] = v[t]
     return bad
+
+
+VLLM_X = 8  # f16 elements in one 16-byte K chunk of the vLLM layout
+
+
+def append_vllm_layout(k, v, slot_mapping, k_cache, v_cache):
+    """``append`` into vLLM-layout pools (K ``[NB][Hkv][D/8][bs][8]``, V
+    ``[NB][Hkv][D][bs]``), one element at a time; returns the skipped
+    out-of-range token indices."""
+    NB, Hkv, D8, bs, x = k_cache.shape
+    bad = []
+    for t, slot in enumerate(np.asarray(slot_mapping).tolist()):
+        if slot < 0:
+            continue
+        if slot >= NB * bs:
+            bad.append(t)
+            continue
+        blk, off = divmod(slot, bs)
+        for h in range(Hkv):
+            for d in range(D8 * x):
+                k_cache[blk, h, d // x, off, d % x] = k[t, h, d]
+                v_cache[blk, h, d, off] = v[t, h, d]
+    return bad
+
+
+def blocked_from_vllm_layout(k_cache, v_cache, blocks=None):
+    """The vLLM-layout pools read as ``[n][Hkv][bs][D]`` pools (all blocks,
+    or those listed in ``blocks``, in that order)."""
+    NB, Hkv, D8, bs, x = k_cache.shape
+    D = D8 * x
+    idx = np.arange(NB) if blocks is None else np.asarray(blocks)
+    kb = np.empty((len(idx), Hkv, bs, D), dtype=k_cache.dtype)
+    vb = np.empty((len(idx), Hkv, bs, D), dtype=v_cache.dtype)
+    for d in range(D):
+        kb[:, :, :, d] = k_cache[idx, :, d // x, :, d % x]
+        vb[:, :, :, d] = v_cache[idx, :, d, :]
+    return kb, vb
+
+
+def decode_vllm_layout(q, k_cache, v_cache, block_tables, context_lens, scale, seqs=None,
+                       fast=False):
+    """``decode`` (``decode_fast`` with ``fast``) over vLLM-layout pools: the
+    blocks the chosen sequences read are read back as blocked pools (tables
+    renumbered to match), then the definition runs on those."""
+    bs = k_cache.shape[3]
+    bt = np.asarray(block_tables)
+    lens = np.asarray(context_lens)
+    _check_tables(bt, lens, k_cache.shape[0], bs)
+    chosen = range(len(lens)) if seqs is None else seqs
+    used = sorted({int(bt[s, j]) for s in chosen for j in range(-(-int(lens[s]) // bs))}) or [0]
+    where = {b: i for i, b in enumerate(used)}
+    kb, vb = blocked_from_vllm_layout(k_cache, v_cache, used)
+    bt2 = np.zeros_like(bt)
+    for s in chosen:
+        for j in range(-(-int(lens[s]) // bs)):
+            bt2[s, j] = where[int(bt[s, j])]
+    return (decode_fast if fast else decode)(q, kb, vb, bt2, lens, scale, seqs)

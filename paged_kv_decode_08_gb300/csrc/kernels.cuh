@@ -95,6 +95,42 @@ append_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
   }
 }
 
+// The same write into vLLM-layout pools: K [NB][Hkv][D/8][bs][8] (a 16-byte
+// chunk of 8 head-dim elements per token), V [NB][Hkv][D][bs] (tokens
+// innermost).  One thread per 16-byte chunk of a (token, kv head) row: its
+// K chunk lands whole, its V chunk as 8 two-byte writes, one per d.
+__global__ void __launch_bounds__(256)
+append_vllm_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
+                   const int32_t* __restrict__ slot_mapping, long long total_chunks,
+                   int chunks_per_row, int num_kv_heads, int block_size, long long num_slots,
+                   uint4* __restrict__ k_cache, __half* __restrict__ v_cache) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total_chunks;
+       i += stride) {
+    const int ch = (int)(i % chunks_per_row);
+    const long long row = i / chunks_per_row;  // token * num_kv_heads + head
+    const int h = (int)(row % num_kv_heads);
+    const long long t = row / num_kv_heads;
+    const int slot = __ldg(slot_mapping + t);
+    if (slot < 0) continue;
+    if ((long long)slot >= num_slots) {
+      if (h == 0 && ch == 0) atomicOr(&g_device_status, kDevBadSlot);
+      continue;
+    }
+    const int blk = slot / block_size;
+    const int off = slot - blk * block_size;
+    const size_t tile = (size_t)blk * num_kv_heads + h;
+    k_cache[(tile * chunks_per_row + ch) * block_size + off] = __ldg(k + i);
+    const uint4 vv = __ldg(v + i);
+    const __half* vh = reinterpret_cast<const __half*>(&vv);
+    __half* vdst = v_cache + (tile * chunks_per_row * 8 + (size_t)ch * 8) * block_size + off;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) vdst[(size_t)e * block_size] = vh[e];
+  }
+}
+
 // ---------------------------------------------------------------------------
 // decode
 // ---------------------------------------------------------------------------
@@ -152,6 +188,24 @@ __device__ __forceinline__ uint32_t swz(int row, int d) {
   const int line = (d >> 6) * BS + row;
   const int chunk = ((d & 63) >> 3) ^ (row & 7);
   return (uint32_t)(line * 128 + chunk * 16 + (d & 7) * 2);
+}
+
+// vLLM-layout tiles in shared memory.  K [D/8][BS][8] arrives unchanged
+// (16-byte chunk (d/8, row) at (d/8 * BS + row) * 16; eight consecutive rows
+// of one chunk column are 128 contiguous bytes, so ldmatrix is conflict-free
+// without a swizzle).  V^T [D][BS] arrives through TMA with the swizzle whose
+// span is one row (32 bytes for BS 16, 64 for BS 32): 16-byte chunk bits
+// XOR the 128-byte line bits above them, which spreads the 8 rows d..d+7 of
+// one ldmatrix over distinct banks.
+template <int BS>
+__device__ __forceinline__ uint32_t vllm_k_off(int row, int d) {
+  return (uint32_t)(((d >> 3) * BS + row) * 16 + (d & 7) * 2);
+}
+
+template <int BS>
+__device__ __forceinline__ uint32_t vllm_vt_off(int d, int tok) {
+  const uint32_t off = (uint32_t)(d * BS * 2 + tok * 2);
+  return off ^ (((off >> 7) & (uint32_t)(BS / 8 - 1)) << 4);
 }
 
 // One warp's online-softmax state.  Lane (r = lane/4, c = lane%4) holds the
@@ -221,8 +275,9 @@ __device__ __forceinline__ void load_q_frags(uint32_t (&qf)[D / 16][2], const __
 
 // Folds one K/V tile (already in shared memory at kb / vb) into the warp
 // state.  Token t0 is the tile's first position; positions at or past
-// tok_end are masked.
-template <int D, int BS, bool COLMASK = false>
+// tok_end are masked.  VLLM: the tiles are in the vLLM layout (see
+// vllm_k_off / vllm_vt_off) instead of the swizzled [D/64][BS][64].
+template <int D, int BS, bool COLMASK = false, bool VLLM = false>
 __device__ __forceinline__ void consume_tile(uint32_t kb, uint32_t vb, int t0, int tok_end,
                                              const uint32_t (&qf)[D / 16][2], float scale_log2,
                                              WarpState<D>& st, int lane, int lim0 = 0,
@@ -235,13 +290,37 @@ __device__ __forceinline__ void consume_tile(uint32_t kb, uint32_t vb, int t0, i
   if (n_valid < BS) {
     // Rows past the context may hold anything (even NaN); P is 0 there, but
     // 0 * NaN is NaN, so clear those V rows before P.V.
-    const int n_chunks = (BS - n_valid) * HALVES * 8;
-    for (int x = lane; x < n_chunks; x += 32) {
-      const int row = n_valid + x / (HALVES * 8);
-      const int rest = x % (HALVES * 8);
-      const int line = (rest >> 3) * BS + row;
-      const uint32_t a = vb + line * 128 + (rest & 7) * 16;
-      asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0) : "memory");
+    if (VLLM) {
+      // V^T: the tokens are columns; clear them chunk by chunk (8 tokens)
+      const int c0 = n_valid >> 3;
+      const int n_chunks = (BS / 8 - c0) * D;
+      for (int x = lane; x < n_chunks; x += 32) {
+        const int d = x % D;
+        const int ch = c0 + x / D;
+        const uint32_t a = vb + vllm_vt_off<BS>(d, ch * 8);
+        uint32_t w[4];
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                     : "r"(a));
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int tk = ch * 8 + 2 * e;  // tokens tk (low half) and tk + 1
+          if (tk >= n_valid) w[e] = 0u;
+          else if (tk + 1 >= n_valid) w[e] &= 0xffffu;
+        }
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(w[0]), "r"(w[1]),
+                     "r"(w[2]), "r"(w[3])
+                     : "memory");
+      }
+    } else {
+      const int n_chunks = (BS - n_valid) * HALVES * 8;
+      for (int x = lane; x < n_chunks; x += 32) {
+        const int row = n_valid + x / (HALVES * 8);
+        const int rest = x % (HALVES * 8);
+        const int line = (rest >> 3) * BS + row;
+        const uint32_t a = vb + line * 128 + (rest & 7) * 16;
+        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0) : "memory");
+      }
     }
     __syncwarp();
   }
@@ -257,7 +336,10 @@ __device__ __forceinline__ void consume_tile(uint32_t kb, uint32_t vb, int t0, i
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
       uint32_t a[4];
-      ldsm_x4(kb + swz<BS>(row, ks * 16 + (lane >> 4) * 8), a);
+      if (VLLM)
+        ldsm_x4(kb + vllm_k_off<BS>(row, ks * 16 + (lane >> 4) * 8), a);
+      else
+        ldsm_x4(kb + swz<BS>(row, ks * 16 + (lane >> 4) * 8), a);
       if (PKV_QK_SPLIT && (ks & 1))
         mma_16816(s2, a, qf[ks][0], qf[ks][1]);
       else
@@ -324,14 +406,20 @@ __device__ __forceinline__ void consume_tile(uint32_t kb, uint32_t vb, int t0, i
     st.acc[i][3] *= al1;
   }
 
-  // O^T += V^T . P^T
+  // O^T += V^T . P^T (V^T fragments: matrix lane/8 covers d rows +8*(bit 0),
+  // token columns +8*(bit 1))
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt) {
     const int row = mt * 16 + (lane & 7) + (lane >> 4) * 8;
 #pragma unroll
     for (int i = 0; i < KS; ++i) {
       uint32_t a[4];
-      ldsm_x4_trans(vb + swz<BS>(row, i * 16 + ((lane >> 3) & 1) * 8), a);
+      if (VLLM)
+        ldsm_x4(vb + vllm_vt_off<BS>(i * 16 + ((lane >> 3) & 1) * 8 + (lane & 7),
+                                     mt * 16 + (lane >> 4) * 8),
+                a);
+      else
+        ldsm_x4_trans(vb + swz<BS>(row, i * 16 + ((lane >> 3) & 1) * 8), a);
       mma_16816(st.acc[i], a, pb[mt][0], pb[mt][1]);
     }
   }
@@ -357,23 +445,33 @@ __device__ __forceinline__ void merge_warps(const float* red, int stride, int h,
 }
 
 // Starts the TMA copies of the K and V tiles of (physical block, kv head)
-// into the stage at `kdst` (V follows K), completing on `bar`.
-template <int D, int BS>
+// into the stage at `kdst` (V follows K), completing on `bar`.  VLLM: K is
+// one contiguous bulk copy from `kpool`, V one 3-D tensor copy.
+template <int D, int BS, bool VLLM = false>
 __device__ __forceinline__ void issue_tile_copy(uint32_t kdst, uint32_t bar, int tile,
-                                                const CUtensorMap* kmap, const CUtensorMap* vmap) {
+                                                const CUtensorMap* kmap, const CUtensorMap* vmap,
+                                                const __half* kpool = nullptr) {
   constexpr int TB = BS * D * 2;
   mbar_arrive_expect_tx(bar, 2 * TB);
+  if (VLLM) {
+    bulk_load(kdst, kpool + (size_t)tile * (BS * D), TB, bar);
+    tma_load_3d(kdst + TB, vmap, bar, 0, 0, tile);
+  } else {
 #pragma unroll
-  for (int h2 = 0; h2 < D / 64; ++h2) {
-    tma_load_4d(kdst + h2 * BS * 128, kmap, bar, 0, h2, 0, tile);
-    tma_load_4d(kdst + TB + h2 * BS * 128, vmap, bar, 0, h2, 0, tile);
+    for (int h2 = 0; h2 < D / 64; ++h2) {
+      tma_load_4d(kdst + h2 * BS * 128, kmap, bar, 0, h2, 0, tile);
+      tma_load_4d(kdst + TB + h2 * BS * 128, vmap, bar, 0, h2, 0, tile);
+    }
   }
 }
 
-template <int D, int BS, int W, int P, bool SPLIT, bool FUSE>
+// VLLM: the pools are in the vLLM layout (p.k_cache is the K pool; kmap is
+// unused); no fused append.
+template <int D, int BS, int W, int P, bool SPLIT, bool FUSE, bool VLLM = false>
 __global__ void __launch_bounds__(W * 32)
 paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
+  static_assert(!(FUSE && VLLM), "the fused append writes the blocked layout only");
   using Shape = DecodeShape<D, BS, W, P>;
   constexpr int KS = Shape::kKS;
   constexpr int TB = Shape::kTileBytes;
@@ -506,7 +604,8 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     const int phys = (li == 0) ? phys0 : __ldg(table + j);
     const uint32_t bar = my_bars + 8 * stage;
     if (phys >= 0 && phys < p.num_blocks) {
-      issue_tile_copy<D, BS>(k_stage(stage), bar, phys * p.num_kv_heads + g, &kmap, &vmap);
+      issue_tile_copy<D, BS, VLLM>(k_stage(stage), bar, phys * p.num_kv_heads + g, &kmap, &vmap,
+                                   p.k_cache);
     } else {
       atomicOr(&g_device_status, kDevBadBlockId);
       mbar_arrive(bar);
@@ -547,7 +646,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
         }
         __syncwarp();
       }
-      consume_tile<D, BS>(kb, kb + TB, j * BS, tok_end, qf, p.scale_log2, st, lane);
+      consume_tile<D, BS, false, VLLM>(kb, kb + TB, j * BS, tok_end, qf, p.scale_log2, st, lane);
     }
     __syncwarp();
     if (lane == 0 && li + P < my_tiles) {

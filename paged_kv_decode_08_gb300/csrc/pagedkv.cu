@@ -137,6 +137,27 @@ pkv_status make_cache_map(CUtensorMap* map, const void* base, int num_blocks, in
   return PKV_OK;
 }
 
+// The vLLM-layout V pool as a 3-D tensor {block_size tokens, head_dim rows,
+// num_blocks*num_kv_heads tiles}; a box is one whole V^T tile, landing with
+// the swizzle whose span is one row (block_size * 2 bytes).
+pkv_status make_vllm_v_map(CUtensorMap* map, const void* base, int num_blocks, int num_kv_heads,
+                           int block_size, int head_dim) {
+  auto encode = tensor_map_encoder();
+  if (!encode) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t dims[3] = {(cuuint64_t)block_size, (cuuint64_t)head_dim,
+                              (cuuint64_t)num_blocks * (cuuint64_t)num_kv_heads};
+  const cuuint64_t strides[2] = {(cuuint64_t)block_size * 2, (cuuint64_t)block_size * head_dim * 2};
+  const cuuint32_t box[3] = {(cuuint32_t)block_size, (cuuint32_t)head_dim, 1};
+  const cuuint32_t estride[3] = {1, 1, 1};
+  const CUtensorMapSwizzle swz =
+      block_size == 16 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B;
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims,
+                            strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+  return PKV_OK;
+}
+
 struct DecodeArgs {
   const void* q;
   const void* k_cache;
@@ -147,6 +168,7 @@ struct DecodeArgs {
   float scale;
   int num_heads, num_kv_heads, head_dim, block_size;
   void* out;
+  bool vllm = false;  // pools in the vLLM layout
 };
 
 pkv_status validate_decode(const DecodeArgs& a) {
@@ -190,13 +212,13 @@ struct Tuning {
                                : 1;
 };
 
-template <int D, int BS, bool SPLIT, bool FUSE>
+template <int D, int BS, bool SPLIT, bool FUSE, bool VLLM>
 pkv_status launch_decode(const DecodeArgs& a, const DecodeParams& prm, cudaStream_t stream,
                          int grid) {
   constexpr int W = Tuning<D, BS>::W;
   constexpr int P = Tuning<D, BS>::P;
   using Shape = DecodeShape<D, BS, W, P>;
-  auto kernel = paged_decode_kernel<D, BS, W, P, SPLIT, FUSE>;
+  auto kernel = paged_decode_kernel<D, BS, W, P, SPLIT, FUSE, VLLM>;
 
   static std::atomic<unsigned long long> attr_set{0};
   int dev = 0;
@@ -210,13 +232,22 @@ pkv_status launch_decode(const DecodeArgs& a, const DecodeParams& prm, cudaStrea
   }
 
   CUtensorMap kmap, vmap;
-  pkv_status st = make_cache_map(&kmap, a.k_cache, a.num_blocks, a.num_kv_heads, BS, D);
-  if (st != PKV_OK) return st;
-  st = make_cache_map(&vmap, a.v_cache, a.num_blocks, a.num_kv_heads, BS, D);
-  if (st != PKV_OK) return st;
+  pkv_status st;
+  DecodeParams prm2 = prm;
+  if (VLLM) {
+    // K tiles are bulk-copied from the pool pointer; kmap only fills the slot
+    st = make_vllm_v_map(&vmap, a.v_cache, a.num_blocks, a.num_kv_heads, BS, D);
+    if (st != PKV_OK) return st;
+    kmap = vmap;
+    prm2.k_cache = static_cast<__half*>(const_cast<void*>(a.k_cache));
+  } else {
+    st = make_cache_map(&kmap, a.k_cache, a.num_blocks, a.num_kv_heads, BS, D);
+    if (st != PKV_OK) return st;
+    st = make_cache_map(&vmap, a.v_cache, a.num_blocks, a.num_kv_heads, BS, D);
+    if (st != PKV_OK) return st;
+  }
 
   // fair-share depth only pays when every CTA of the grid is resident at once
-  DecodeParams prm2 = prm;
   int sms = 0;
   prm2.fair_depth = (current_device_sms(&sms) == 0 && grid <= sms * kCtasPerSm) ? 1 : 0;
   e = launch_pdl(kernel, grid, W * 32, Shape::kSmemBytes, stream, kmap, vmap, prm2);
@@ -224,27 +255,31 @@ pkv_status launch_decode(const DecodeArgs& a, const DecodeParams& prm, cudaStrea
   return PKV_OK;
 }
 
-template <bool SPLIT, bool FUSE>
+template <bool SPLIT, bool FUSE, bool VLLM>
 pkv_status dispatch_decode_f(const DecodeArgs& a, const DecodeParams& prm, cudaStream_t stream,
                              int grid) {
   if (a.head_dim == 128 && a.block_size == 16)
-    return launch_decode<128, 16, SPLIT, FUSE>(a, prm, stream, grid);
+    return launch_decode<128, 16, SPLIT, FUSE, VLLM>(a, prm, stream, grid);
   if (a.head_dim == 128 && a.block_size == 32)
-    return launch_decode<128, 32, SPLIT, FUSE>(a, prm, stream, grid);
+    return launch_decode<128, 32, SPLIT, FUSE, VLLM>(a, prm, stream, grid);
   if (a.head_dim == 64 && a.block_size == 16)
-    return launch_decode<64, 16, SPLIT, FUSE>(a, prm, stream, grid);
+    return launch_decode<64, 16, SPLIT, FUSE, VLLM>(a, prm, stream, grid);
   if (a.head_dim == 64 && a.block_size == 32)
-    return launch_decode<64, 32, SPLIT, FUSE>(a, prm, stream, grid);
+    return launch_decode<64, 32, SPLIT, FUSE, VLLM>(a, prm, stream, grid);
   return fail(PKV_ERR_UNSUPPORTED, "head_dim %d / block_size %d", a.head_dim, a.block_size);
 }
 
-// Kernels with the fused append only where a call asks for it, so plain
-// decode kernels carry none of its code.
+// Kernels with the fused append (or the vLLM layout) only where a call asks
+// for it, so plain decode kernels carry none of that code.
 template <bool SPLIT>
 pkv_status dispatch_decode(const DecodeArgs& a, const DecodeParams& prm, cudaStream_t stream,
                            int grid) {
-  return prm.new_slots ? dispatch_decode_f<SPLIT, true>(a, prm, stream, grid)
-                       : dispatch_decode_f<SPLIT, false>(a, prm, stream, grid);
+  if (a.vllm) {
+    if (prm.new_slots) return fail(PKV_ERR_UNSUPPORTED, "no fused append on the vLLM layout");
+    return dispatch_decode_f<SPLIT, false, true>(a, prm, stream, grid);
+  }
+  return prm.new_slots ? dispatch_decode_f<SPLIT, true, false>(a, prm, stream, grid)
+                       : dispatch_decode_f<SPLIT, false, false>(a, prm, stream, grid);
 }
 
 size_t balanced_scratch_bytes(int head_dim) {
@@ -399,6 +434,46 @@ pkv_status single_pass(const DecodeArgs& a, cudaStream_t stream, const FuseArgs*
   return dispatch_decode<false>(a, prm, stream, (int)grid);
 }
 
+// pkv_append and pkv_append_vllm_layout: the same checks and grid, a kernel
+// per layout.
+pkv_status append_impl(const void* k, const void* v, const int32_t* slot_mapping,
+                       int num_tokens, void* k_cache, void* v_cache, int num_blocks,
+                       int block_size, int num_kv_heads, int head_dim, cudaStream_t stream,
+                       bool vllm) {
+  if (num_tokens < 0) return fail(PKV_ERR_INVALID_ARG, "num_tokens < 0");
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache)
+    return fail(PKV_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0)
+    return fail(PKV_ERR_INVALID_ARG, "sizes must be positive");
+  if (head_dim != 64 && head_dim != 128)
+    return fail(PKV_ERR_UNSUPPORTED, "head_dim %d (built: 64, 128)", head_dim);
+  if (block_size != 16 && block_size != 32)
+    return fail(PKV_ERR_UNSUPPORTED, "block_size %d (built: 16, 32)", block_size);
+  if ((long long)num_blocks * block_size >= (1ll << 31))
+    return fail(PKV_ERR_INVALID_ARG, "num_blocks too large for 32-bit slots");
+  if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+    return fail(PKV_ERR_INVALID_ARG, "k, v, k_cache and v_cache must be 16-byte aligned");
+  if (!aligned(slot_mapping, 4)) return fail(PKV_ERR_INVALID_ARG, "slot_mapping must be 4-byte aligned");
+  if (num_tokens == 0) return PKV_OK;
+
+  const int chunks_per_row = head_dim / 8;
+  const long long total = (long long)num_tokens * num_kv_heads * chunks_per_row;
+  long long blocks = (total + 255) / 256;
+  if (blocks > 65536) blocks = 65536;  // grid-stride beyond this
+  const long long num_slots = (long long)num_blocks * block_size;
+  const cudaError_t e =
+      vllm ? launch_pdl(append_vllm_kernel, (int)blocks, 256, 0, stream,
+                        static_cast<const uint4*>(k), static_cast<const uint4*>(v), slot_mapping,
+                        total, chunks_per_row, num_kv_heads, block_size, num_slots,
+                        static_cast<uint4*>(k_cache), static_cast<__half*>(v_cache))
+           : launch_pdl(append_kernel, (int)blocks, 256, 0, stream, static_cast<const uint4*>(k),
+                        static_cast<const uint4*>(v), slot_mapping, total, chunks_per_row,
+                        num_kv_heads, block_size, num_slots, static_cast<uint4*>(k_cache),
+                        static_cast<uint4*>(v_cache));
+  if (e != cudaSuccess) return cuda_fail(e, "append launch");
+  return PKV_OK;
+}
+
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 }  // namespace
@@ -454,33 +529,16 @@ int32_t pkv_pick_num_splits(int32_t num_seqs, int32_t num_kv_heads, int32_t max_
 pkv_status pkv_append(const void* k, const void* v, const int32_t* slot_mapping,
                       int32_t num_tokens, void* k_cache, void* v_cache, int32_t num_blocks,
                       int32_t block_size, int32_t num_kv_heads, int32_t head_dim, void* stream) {
-  if (num_tokens < 0) return fail(PKV_ERR_INVALID_ARG, "num_tokens < 0");
-  if (!k || !v || !slot_mapping || !k_cache || !v_cache)
-    return fail(PKV_ERR_INVALID_ARG, "a required pointer is NULL");
-  if (num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0)
-    return fail(PKV_ERR_INVALID_ARG, "sizes must be positive");
-  if (head_dim != 64 && head_dim != 128)
-    return fail(PKV_ERR_UNSUPPORTED, "head_dim %d (built: 64, 128)", head_dim);
-  if (block_size != 16 && block_size != 32)
-    return fail(PKV_ERR_UNSUPPORTED, "block_size %d (built: 16, 32)", block_size);
-  if ((long long)num_blocks * block_size >= (1ll << 31))
-    return fail(PKV_ERR_INVALID_ARG, "num_blocks too large for 32-bit slots");
-  if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
-    return fail(PKV_ERR_INVALID_ARG, "k, v, k_cache and v_cache must be 16-byte aligned");
-  if (!aligned(slot_mapping, 4)) return fail(PKV_ERR_INVALID_ARG, "slot_mapping must be 4-byte aligned");
-  if (num_tokens == 0) return PKV_OK;
+  return append_impl(k, v, slot_mapping, num_tokens, k_cache, v_cache, num_blocks, block_size,
+                     num_kv_heads, head_dim, static_cast<cudaStream_t>(stream), false);
+}
 
-  const int chunks_per_row = head_dim / 8;
-  const long long total = (long long)num_tokens * num_kv_heads * chunks_per_row;
-  long long blocks = (total + 255) / 256;
-  if (blocks > 65536) blocks = 65536;  // grid-stride beyond this
-  const cudaError_t e = launch_pdl(
-      append_kernel, (int)blocks, 256, 0, static_cast<cudaStream_t>(stream),
-      static_cast<const uint4*>(k), static_cast<const uint4*>(v), slot_mapping, total,
-      chunks_per_row, num_kv_heads, block_size, (long long)num_blocks * block_size,
-      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache));
-  if (e != cudaSuccess) return cuda_fail(e, "append launch");
-  return PKV_OK;
+pkv_status pkv_append_vllm_layout(const void* k, const void* v, const int32_t* slot_mapping,
+                                  int32_t num_tokens, void* k_cache, void* v_cache,
+                                  int32_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                                  int32_t head_dim, void* stream) {
+  return append_impl(k, v, slot_mapping, num_tokens, k_cache, v_cache, num_blocks, block_size,
+                     num_kv_heads, head_dim, static_cast<cudaStream_t>(stream), true);
 }
 
 pkv_status pkv_decode(const void* q, const void* k_cache, const void* v_cache,
@@ -520,6 +578,7 @@ pkv_status decode_impl(const DecodeArgs& a, int num_splits, void* scratch, size_
     S = pkv_pick_num_splits(num_seqs, num_kv_heads, max_blocks_per_seq * block_size, block_size, sms);
   }
   if (S == PKV_SPLITS_BALANCED) {
+    if (a.vllm) return fail(PKV_ERR_UNSUPPORTED, "no balanced schedule on the vLLM layout");
     const size_t need_b = balanced_scratch_bytes(head_dim);
     if (!scratch || scratch_bytes < need_b)
       return fail(PKV_ERR_SCRATCH_TOO_SMALL, "the balanced schedule needs %zu scratch bytes, got %zu",
@@ -589,6 +648,25 @@ pkv_status pkv_decode_splitk(const void* q, const void* k_cache, const void* v_c
                      head_dim, block_size, out};
   pkv_status st = validate_decode(a);
   if (st != PKV_OK) return st;
+  return decode_impl(a, num_splits, scratch, scratch_bytes, static_cast<cudaStream_t>(stream),
+                     nullptr);
+}
+
+pkv_status pkv_decode_vllm_layout(const void* q, const void* k_cache, const void* v_cache,
+                                  const int32_t* block_tables, const int32_t* context_lens,
+                                  int32_t num_seqs, int32_t max_blocks_per_seq,
+                                  int32_t num_blocks, float scale, int32_t num_heads,
+                                  int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                  void* out, int32_t num_splits, void* scratch,
+                                  size_t scratch_bytes, void* stream) {
+  DecodeArgs a{q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+               max_blocks_per_seq, num_blocks, scale, num_heads, num_kv_heads,
+               head_dim, block_size, out};
+  a.vllm = true;
+  pkv_status st = validate_decode(a);
+  if (st != PKV_OK) return st;
+  if (num_splits == PKV_SPLITS_BALANCED)
+    return fail(PKV_ERR_UNSUPPORTED, "no balanced schedule on the vLLM layout");
   return decode_impl(a, num_splits, scratch, scratch_bytes, static_cast<cudaStream_t>(stream),
                      nullptr);
 }

@@ -64,6 +64,11 @@ def _load():
     lib.pkv_decode_splitk_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, f32, i32, i32,
                                               i32, i32, vp, i32, vp]
     lib.pkv_decode_splitk_noalloc.restype = i32
+    lib.pkv_append_vllm_layout.argtypes = [vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, vp]
+    lib.pkv_append_vllm_layout.restype = i32
+    lib.pkv_decode_vllm_layout.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, f32, i32, i32, i32,
+                                           i32, vp, i32, vp, sz, vp]
+    lib.pkv_decode_vllm_layout.restype = i32
     lib.pkv_splitk_scratch_bytes.argtypes = [i32, i32, i32, i32]
     lib.pkv_splitk_scratch_bytes.restype = sz
     lib.pkv_pick_num_splits.argtypes = [i32, i32, i32, i32, i32]
@@ -185,7 +190,7 @@ def splits_for(q, k_cache, block_tables, num_splits=0, device=None) -> int:
     if num_splits:
         return int(num_splits)
     sms = torch.cuda.get_device_properties(device or q.device).multi_processor_count
-    bs = k_cache.shape[2]
+    bs = k_cache.shape[3] if k_cache.dim() == 5 else k_cache.shape[2]  # vLLM K: [..][bs][8]
     return pkv_pick_num_splits(q.shape[0], k_cache.shape[1], block_tables.shape[1] * bs, bs, sms)
 
 
@@ -289,6 +294,62 @@ def pkv_decode_splitk_noalloc(q, k_cache, v_cache, block_tables, context_lens, s
                                          mbps, NB, float(scale), H, Hkv, D, bs, out.data_ptr(),
                                          int(num_splits), _stream_ptr(stream)),
            "pkv_decode_splitk_noalloc")
+    return out
+
+
+def _vllm_pools(k_cache, v_cache):
+    """(NB, Hkv, bs, D) of vLLM-layout pools: K [NB][Hkv][D/8][bs][8], V [NB][Hkv][D][bs]."""
+    import torch
+
+    _want(k_cache, "k_cache", torch.float16, 5)
+    NB, Hkv, D8, bs, x = k_cache.shape
+    if x != 8:
+        raise ValueError("vLLM-layout k_cache must end in 8 (16 bytes of f16)")
+    _want(v_cache, "v_cache", torch.float16, 4, (NB, Hkv, D8 * 8, bs))
+    return NB, Hkv, bs, D8 * 8
+
+
+def pkv_append_vllm_layout(k, v, slot_mapping, k_cache, v_cache, stream=None):
+    """:func:`pkv_append` into vLLM-layout pools."""
+    import torch
+
+    NB, Hkv, bs, D = _vllm_pools(k_cache, v_cache)
+    _want(k, "k", torch.float16, 3)
+    T = k.shape[0]
+    _want(k, "k", torch.float16, 3, (T, Hkv, D))
+    _want(v, "v", torch.float16, 3, (T, Hkv, D))
+    _want(slot_mapping, "slot_mapping", torch.int32, 1, (T,))
+    _check(lib.pkv_append_vllm_layout(k.data_ptr(), v.data_ptr(), slot_mapping.data_ptr(), T,
+                                      k_cache.data_ptr(), v_cache.data_ptr(), NB, bs, Hkv, D,
+                                      _stream_ptr(stream)), "pkv_append_vllm_layout")
+
+
+def pkv_decode_vllm_layout(q, k_cache, v_cache, block_tables, context_lens, scale, num_splits=0,
+                           scratch=None, out=None, stream=None):
+    """:func:`pkv_decode_splitk` over vLLM-layout pools; returns ``out``."""
+    import torch
+
+    NB, Hkv, bs, D = _vllm_pools(k_cache, v_cache)
+    _want(q, "q", torch.float16, 3)
+    B, H, Dq = q.shape
+    if Dq != D:
+        raise ValueError("k_cache head_dim differs from q")
+    _want(block_tables, "block_tables", torch.int32, 2)
+    if block_tables.shape[0] != B:
+        raise ValueError("block_tables must have num_seqs rows")
+    _want(context_lens, "context_lens", torch.int32, 1, (B,))
+    if out is None:
+        out = torch.empty_like(q)
+    _want(out, "out", torch.float16, 3, (B, H, D))
+    mbps = block_tables.shape[1]
+    if scratch is None:
+        scratch = alloc_scratch(q, k_cache, block_tables, num_splits)
+    _want(scratch, "scratch", torch.uint8, 1)
+    _check(lib.pkv_decode_vllm_layout(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                      block_tables.data_ptr(), context_lens.data_ptr(), B, mbps,
+                                      NB, float(scale), H, Hkv, D, bs, out.data_ptr(),
+                                      int(num_splits), scratch.data_ptr(), scratch.numel(),
+                                      _stream_ptr(stream)), "pkv_decode_vllm_layout")
     return out
 
 

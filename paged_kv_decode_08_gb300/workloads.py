@@ -406,13 +406,58 @@ def to_device(w: Workload, device="cuda", upto_last: bool = False, poison_fill=T
     idx = torch.from_numpy(ids).to(device)
     kc.index_copy_(0, idx, torch.from_numpy(kb).to(device))
     vc.index_copy_(0, idx, torch.from_numpy(vb).to(device))
+    return {"k_cache": kc, "v_cache": vc, **_device_meta(w, device)}
+
+
+def _device_meta(w: Workload, device):
+    import torch
+
     return {
-        "k_cache": kc,
-        "v_cache": vc,
         "block_tables": torch.from_numpy(np.ascontiguousarray(w.block_tables)).to(device),
         "context_lens": torch.from_numpy(np.ascontiguousarray(w.context_lens)).to(device),
         "q": torch.from_numpy(np.ascontiguousarray(w.q)).to(device),
     }
+
+
+def vllm_layout_tiles(kb: np.ndarray, vb: np.ndarray):
+    """Blocked tiles ``[n][Hkv][bs][D]`` rearranged into the vLLM layout:
+    K ``[n][Hkv][D/8][bs][8]``, V ``[n][Hkv][D][bs]`` (same values)."""
+    n, Hkv, bs, D = kb.shape
+    kv = np.ascontiguousarray(kb.reshape(n, Hkv, bs, D // 8, 8).transpose(0, 1, 3, 2, 4))
+    vv = np.ascontiguousarray(vb.transpose(0, 1, 3, 2))
+    return kv, vv
+
+
+def host_pool_vllm(w: Workload, upto_last: bool = False, fill: float = 0.0):
+    """:func:`host_pool` in the vLLM layout."""
+    NB, Hkv, bs, D = w.num_blocks, w.num_kv_heads, w.block_size, w.head_dim
+    make = np.zeros if fill == 0.0 else (lambda shp, dt: np.full(shp, fill, dt))
+    kc = make((NB, Hkv, D // 8, bs, 8), np.float16)
+    vc = make((NB, Hkv, D, bs), np.float16)
+    ids, kb, vb = compact_blocks(w, upto_last=upto_last)
+    kv, vv = vllm_layout_tiles(kb, vb)
+    kc[ids] = kv
+    vc[ids] = vv
+    return kc, vc
+
+
+def to_device_vllm(w: Workload, device="cuda", upto_last: bool = False, poison_fill=True):
+    """:func:`to_device` with the pools in the vLLM layout."""
+    import torch
+
+    d = _device_meta(w, device)
+    NB, Hkv, bs, D = w.num_blocks, w.num_kv_heads, w.block_size, w.head_dim
+    fill = float("nan") if poison_fill else 0.0
+    kc = torch.full((NB, Hkv, D // 8, bs, 8), fill, dtype=torch.float16, device=device)
+    vc = torch.full((NB, Hkv, D, bs), fill, dtype=torch.float16, device=device)
+    ids, kb, vb = compact_blocks(w, upto_last=upto_last)
+    kv, vv = vllm_layout_tiles(kb, vb)
+    idx = torch.from_numpy(ids).to(device)
+    kc.index_copy_(0, idx, torch.from_numpy(kv).to(device))
+    vc.index_copy_(0, idx, torch.from_numpy(vv).to(device))
+    d["k_cache"] = kc
+    d["v_cache"] = vc
+    return d
 
 
 @dataclasses.dataclass

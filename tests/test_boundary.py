@@ -33,7 +33,7 @@ def test_header_declares_the_expected_calls():
     for n in ["pkv_append", "pkv_decode", "pkv_decode_splitk", "pkv_append_decode",
               "pkv_varlen_attention", "pkv_splitk_scratch_bytes",
               "pkv_pick_num_splits", "pkv_status_string", "pkv_last_error",
-              "pkv_read_device_status"]:
+              "pkv_read_device_status", "pkv_append_vllm_layout", "pkv_decode_vllm_layout"]:
         assert n in names
 
 
@@ -194,3 +194,20 @@ def test_varlen_rejects_bad_arguments(pk):
     bad_d = list(ok)
     bad_d[14] = 96
     assert f(*bad_d) == -2
+
+
+def test_vllm_layout_calls_reject_bad_arguments(pk):
+    f = pk.lib.pkv_decode_vllm_layout
+    ok = [F16, F16, F16, F16, F16, 2, 3, 8, 0.125, 4, 2, 64, 16, F16]
+    assert f(*ok, -1, F16, 1 << 30, None) == -2   # no balanced schedule on this layout
+    assert f(*ok, -2, F16, 1 << 30, None) == -1
+    assert f(*ok, 4, None, 0, None) == -3
+    bad = list(ok)
+    bad[11] = 96
+    assert f(*bad, 1, None, 0, None) == -2
+    assert f(*(ok[:5] + [0] + ok[6:]), 1, None, 0, None) == 0  # no sequences
+    a = pk.lib.pkv_append_vllm_layout
+    assert a(F16, F16, F16, -1, F16, F16, 8, 16, 2, 64, None) == -1
+    assert a(F16, F16, F16, 2, F16, F16, 8, 24, 2, 64, None) == -2
+    assert a(F16, F16, F16, 2, F16 + 4, F16, 8, 16, 2, 64, None) == -1
+    assert a(F16, F16, F16, 0, F16, F16, 8, 16, 2, 64, None) == 0

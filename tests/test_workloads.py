@@ -83,3 +83,18 @@ def test_loop_schedule_is_consistent():
     owned = np.concatenate([last[s, : -(-int(loop.end_lens[s]) // 16)] for s in range(loop.num_seqs)])
     assert len(np.unique(owned)) == len(owned)
     assert loop.poison_block not in set(owned.tolist())
+
+
+def test_vllm_layout_pools_hold_the_blocked_pools_values():
+    """The generator's vLLM-layout pools, read back by the oracle's adapter,
+    are the blocked pools bit for bit (NaN poison included)."""
+    import oracle
+
+    for w in (W.make("tiny"), W.small_random(7, 3, 8, 2, 128, 32, [1, 40, 65])):
+        kb, vb = W.host_pool(w, fill=np.nan)
+        kv, vv = W.host_pool_vllm(w, fill=np.nan)
+        assert kv.shape == (w.num_blocks, w.num_kv_heads, w.head_dim // 8, w.block_size, 8)
+        assert vv.shape == (w.num_blocks, w.num_kv_heads, w.head_dim, w.block_size)
+        k2, v2 = oracle.blocked_from_vllm_layout(kv, vv)
+        assert np.array_equal(k2.view(np.uint16), kb.view(np.uint16))
+        assert np.array_equal(v2.view(np.uint16), vb.view(np.uint16))

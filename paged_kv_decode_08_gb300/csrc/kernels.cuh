@@ -193,10 +193,10 @@ __device__ __forceinline__ uint32_t swz(int row, int d) {
 // vLLM-layout tiles in shared memory.  K [D/8][BS][8] arrives unchanged
 // (16-byte chunk (d/8, row) at (d/8 * BS + row) * 16; eight consecutive rows
 // of one chunk column are 128 contiguous bytes, so ldmatrix is conflict-free
-// without a swizzle).  V^T [D][BS] arrives through TMA with the swizzle whose
-// span is one row (32 bytes for BS 16, 64 for BS 32): 16-byte chunk bits
-// XOR the 128-byte line bits above them, which spreads the 8 rows d..d+7 of
-// one ldmatrix over distinct banks.
+// without a swizzle).  V^T [D][BS] arrives through TMA as 128-byte lines
+// (128 / (2 BS) rows of d per line) with the 128-byte swizzle (16-byte chunk
+// index XOR line % 8); the 8 rows d..d+7 of one ldmatrix then fall on 8
+// distinct bank groups for BS 16 and 32 alike.
 template <int BS>
 __device__ __forceinline__ uint32_t vllm_k_off(int row, int d) {
   return (uint32_t)(((d >> 3) * BS + row) * 16 + (d & 7) * 2);
@@ -205,7 +205,7 @@ __device__ __forceinline__ uint32_t vllm_k_off(int row, int d) {
 template <int BS>
 __device__ __forceinline__ uint32_t vllm_vt_off(int d, int tok) {
   const uint32_t off = (uint32_t)(d * BS * 2 + tok * 2);
-  return off ^ (((off >> 7) & (uint32_t)(BS / 8 - 1)) << 4);
+  return off ^ (((off >> 7) & 7u) << 4);
 }
 
 // One warp's online-softmax state.  Lane (r = lane/4, c = lane%4) holds the

@@ -137,23 +137,24 @@ pkv_status make_cache_map(CUtensorMap* map, const void* base, int num_blocks, in
   return PKV_OK;
 }
 
-// The vLLM-layout V pool as a 3-D tensor {block_size tokens, head_dim rows,
-// num_blocks*num_kv_heads tiles}; a box is one whole V^T tile, landing with
-// the swizzle whose span is one row (block_size * 2 bytes).
+// The vLLM-layout V pool as a 3-D tensor {64 elements, head_dim*block_size/64
+// lines, num_blocks*num_kv_heads tiles}: each V^T tile [head_dim][block_size]
+// read as 128-byte lines.  A box is one whole tile, landing with the 128-byte
+// swizzle.
 pkv_status make_vllm_v_map(CUtensorMap* map, const void* base, int num_blocks, int num_kv_heads,
                            int block_size, int head_dim) {
   auto encode = tensor_map_encoder();
   if (!encode) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-  const cuuint64_t dims[3] = {(cuuint64_t)block_size, (cuuint64_t)head_dim,
+  const int lines = head_dim * block_size / 64;
+  const cuuint64_t dims[3] = {64, (cuuint64_t)lines,
                               (cuuint64_t)num_blocks * (cuuint64_t)num_kv_heads};
-  const cuuint64_t strides[2] = {(cuuint64_t)block_size * 2, (cuuint64_t)block_size * head_dim * 2};
-  const cuuint32_t box[3] = {(cuuint32_t)block_size, (cuuint32_t)head_dim, 1};
+  const cuuint64_t strides[2] = {128, (cuuint64_t)block_size * head_dim * 2};
+  const cuuint32_t box[3] = {64, (cuuint32_t)lines, 1};
   const cuuint32_t estride[3] = {1, 1, 1};
-  const CUtensorMapSwizzle swz =
-      block_size == 16 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B;
   const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims,
-                            strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
-                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                            strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
   return PKV_OK;
 }

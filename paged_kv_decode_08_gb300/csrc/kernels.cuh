@@ -273,15 +273,18 @@ __device__ __forceinline__ void load_q_frags(uint32_t (&qf)[D / 16][2], const __
   }
 }
 
-// Folds one K/V tile (already in shared memory at kb / vb) into the warp
-// state.  Token t0 is the tile's first position; positions at or past
-// tok_end are masked.  VLLM: the tiles are in the vLLM layout (see
-// vllm_k_off / vllm_vt_off) instead of the swizzled [D/64][BS][64].
-template <int D, int BS, bool COLMASK = false, bool VLLM = false>
-__device__ __forceinline__ void consume_tile(uint32_t kb, uint32_t vb, int t0, int tok_end,
-                                             const uint32_t (&qf)[D / 16][2], float scale_log2,
-                                             WarpState<D>& st, int lane, int lim0 = 0,
-                                             int lim1 = 0) {
+// Folds one K/V tile (already in shared memory at kb / vb) into NT warp
+// states, one per 8-column n-tile of queries (each K and V fragment read
+// from shared memory serves all NT tiles).  Token t0 is the tile's first
+// position; positions at or past tok_end are masked, and with COLMASK each
+// lane's two columns of n-tile nt also stop at lim[nt][0] / lim[nt][1].
+// VLLM: the tiles are in the vLLM layout (see vllm_k_off / vllm_vt_off)
+// instead of the swizzled [D/64][BS][64].
+template <int D, int BS, int NT, bool COLMASK, bool VLLM>
+__device__ __forceinline__ void consume_tiles(uint32_t kb, uint32_t vb, int t0, int tok_end,
+                                              const uint32_t (&qf)[NT][D / 16][2],
+                                              float scale_log2, WarpState<D> (&st)[NT], int lane,
+                                              const int (&lim)[NT][2]) {
   constexpr int MT = BS / 16;
   constexpr int KS = D / 16;
   constexpr int HALVES = D / 64;
@@ -325,13 +328,17 @@ __device__ __forceinline__ void consume_tile(uint32_t kb, uint32_t vb, int t0, i
     __syncwarp();
   }
 
-  // S^T = K . Q^T for every 16-token slice of the tile (two accumulators
-  // per slice halve the dependent mma chain).
-  float sc[MT][4];
+  // S^T = K . Q^T for every 16-token slice of the tile and every n-tile (two
+  // accumulators per slice halve the dependent mma chain).
+  float sc[MT][NT][4];
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt) {
-    float s2[4] = {0.f, 0.f, 0.f, 0.f};
-    sc[mt][0] = sc[mt][1] = sc[mt][2] = sc[mt][3] = 0.f;
+    float s2[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      s2[nt][0] = s2[nt][1] = s2[nt][2] = s2[nt][3] = 0.f;
+      sc[mt][nt][0] = sc[mt][nt][1] = sc[mt][nt][2] = sc[mt][nt][3] = 0.f;
+    }
     const int row = mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
@@ -340,70 +347,81 @@ __device__ __forceinline__ void consume_tile(uint32_t kb, uint32_t vb, int t0, i
         ldsm_x4(kb + vllm_k_off<BS>(row, ks * 16 + (lane >> 4) * 8), a);
       else
         ldsm_x4(kb + swz<BS>(row, ks * 16 + (lane >> 4) * 8), a);
-      if (PKV_QK_SPLIT && (ks & 1))
-        mma_16816(s2, a, qf[ks][0], qf[ks][1]);
-      else
-        mma_16816(sc[mt], a, qf[ks][0], qf[ks][1]);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        if (PKV_QK_SPLIT && (ks & 1))
+          mma_16816(s2[nt], a, qf[nt][ks][0], qf[nt][ks][1]);
+        else
+          mma_16816(sc[mt][nt], a, qf[nt][ks][0], qf[nt][ks][1]);
+      }
     }
 #pragma unroll
-    for (int e = 0; e < 4; ++e) sc[mt][e] += s2[e];
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sc[mt][nt][e] += s2[nt][e];
   }
 
-  // scale, mask rows past the context, tile max per head
-  float x0 = -CUDART_INF_F, x1 = -CUDART_INF_F;
 #pragma unroll
-  for (int mt = 0; mt < MT; ++mt) {
+  for (int nt = 0; nt < NT; ++nt) {
+    WarpState<D>& w = st[nt];
+    // scale, mask rows past the context, tile max per column
+    float x0 = -CUDART_INF_F, x1 = -CUDART_INF_F;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int tok = t0 + mt * 16 + r + (e >> 1) * 8;
-      const float v = sc[mt][e] * scale_log2;
-      // COLMASK: each column (query) has its own causal limit
-      const int lim = COLMASK ? ((e & 1) ? lim1 : lim0) : tok_end;
-      sc[mt][e] = tok < lim ? v : -CUDART_INF_F;
+    for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int tok = t0 + mt * 16 + r + (e >> 1) * 8;
+        const float v = sc[mt][nt][e] * scale_log2;
+        // COLMASK: each column (query) has its own causal limit
+        const int lm = COLMASK ? lim[nt][e & 1] : tok_end;
+        sc[mt][nt][e] = tok < lm ? v : -CUDART_INF_F;
+      }
+      x0 = fmaxf(x0, fmaxf(sc[mt][nt][0], sc[mt][nt][2]));
+      x1 = fmaxf(x1, fmaxf(sc[mt][nt][1], sc[mt][nt][3]));
     }
-    x0 = fmaxf(x0, fmaxf(sc[mt][0], sc[mt][2]));
-    x1 = fmaxf(x1, fmaxf(sc[mt][1], sc[mt][3]));
-  }
 #pragma unroll
-  for (int o = 4; o < 32; o <<= 1) {
-    x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, o));
-    x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, o));
-  }
-  float mn0 = fmaxf(st.m0, x0);
-  float mn1 = fmaxf(st.m1, x1);
-  float al0 = exp2f(st.m0 - mn0);  // 0 on the first tile (m = -inf)
-  float al1 = exp2f(st.m1 - mn1);
-  st.m0 = mn0;
-  st.m1 = mn1;
-  if (COLMASK) {
-    // a column with nothing valid so far keeps m = -inf: no rescale, P = 0
-    if (mn0 == -CUDART_INF_F) { al0 = 1.f; mn0 = 0.f; }
-    if (mn1 == -CUDART_INF_F) { al1 = 1.f; mn1 = 0.f; }
-  }
+    for (int o = 4; o < 32; o <<= 1) {
+      x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, o));
+      x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, o));
+    }
+    float mn0 = fmaxf(w.m0, x0);
+    float mn1 = fmaxf(w.m1, x1);
+    float al0 = exp2f(w.m0 - mn0);  // 0 on the first tile (m = -inf)
+    float al1 = exp2f(w.m1 - mn1);
+    w.m0 = mn0;
+    w.m1 = mn1;
+    if (COLMASK) {
+      // a column with nothing valid so far keeps m = -inf: no rescale, P = 0
+      if (mn0 == -CUDART_INF_F) { al0 = 1.f; mn0 = 0.f; }
+      if (mn1 == -CUDART_INF_F) { al1 = 1.f; mn1 = 0.f; }
+    }
 
-  // P = exp2(S - m), rounded to f16 for the tensor cores; the running sum
-  // adds the same rounded values so numerator and denominator agree.
-  uint32_t pb[MT][2];
-  float ps0 = 0.f, ps1 = 0.f;
+    // P = exp2(S - m), rounded to f16 for the tensor cores; the running sum
+    // adds the same rounded values so numerator and denominator agree.  P^T
+    // overwrites the scores of this n-tile (as two packed registers).
+    float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
-  for (int mt = 0; mt < MT; ++mt) {
-    const __half2 h01 = __floats2half2_rn(exp2f(sc[mt][0] - mn0), exp2f(sc[mt][1] - mn1));
-    const __half2 h23 = __floats2half2_rn(exp2f(sc[mt][2] - mn0), exp2f(sc[mt][3] - mn1));
-    const float2 f01 = __half22float2(h01);
-    const float2 f23 = __half22float2(h23);
-    ps0 += f01.x + f23.x;
-    ps1 += f01.y + f23.y;
-    pb[mt][0] = movmatrix_trans(pack_half2(h01));
-    pb[mt][1] = movmatrix_trans(pack_half2(h23));
-  }
-  st.l0 = st.l0 * al0 + ps0;
-  st.l1 = st.l1 * al1 + ps1;
+    for (int mt = 0; mt < MT; ++mt) {
+      const __half2 h01 =
+          __floats2half2_rn(exp2f(sc[mt][nt][0] - mn0), exp2f(sc[mt][nt][1] - mn1));
+      const __half2 h23 =
+          __floats2half2_rn(exp2f(sc[mt][nt][2] - mn0), exp2f(sc[mt][nt][3] - mn1));
+      const float2 f01 = __half22float2(h01);
+      const float2 f23 = __half22float2(h23);
+      ps0 += f01.x + f23.x;
+      ps1 += f01.y + f23.y;
+      sc[mt][nt][0] = __uint_as_float(movmatrix_trans(pack_half2(h01)));
+      sc[mt][nt][1] = __uint_as_float(movmatrix_trans(pack_half2(h23)));
+    }
+    w.l0 = w.l0 * al0 + ps0;
+    w.l1 = w.l1 * al1 + ps1;
 #pragma unroll
-  for (int i = 0; i < KS; ++i) {
-    st.acc[i][0] *= al0;
-    st.acc[i][1] *= al1;
-    st.acc[i][2] *= al0;
-    st.acc[i][3] *= al1;
+    for (int i = 0; i < KS; ++i) {
+      w.acc[i][0] *= al0;
+      w.acc[i][1] *= al1;
+      w.acc[i][2] *= al0;
+      w.acc[i][3] *= al1;
+    }
   }
 
   // O^T += V^T . P^T (V^T fragments: matrix lane/8 covers d rows +8*(bit 0),
@@ -420,9 +438,24 @@ __device__ __forceinline__ void consume_tile(uint32_t kb, uint32_t vb, int t0, i
                 a);
       else
         ldsm_x4_trans(vb + swz<BS>(row, i * 16 + ((lane >> 3) & 1) * 8), a);
-      mma_16816(st.acc[i], a, pb[mt][0], pb[mt][1]);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+        mma_16816(st[nt].acc[i], a, __float_as_uint(sc[mt][nt][0]),
+                  __float_as_uint(sc[mt][nt][1]));
     }
   }
+}
+
+// One n-tile (the decode kernels: the 8 columns are the GQA group).
+template <int D, int BS, bool COLMASK = false, bool VLLM = false>
+__device__ __forceinline__ void consume_tile(uint32_t kb, uint32_t vb, int t0, int tok_end,
+                                             const uint32_t (&qf)[D / 16][2], float scale_log2,
+                                             WarpState<D>& st, int lane, int lim0 = 0,
+                                             int lim1 = 0) {
+  const int lim[1][2] = {{lim0, lim1}};
+  consume_tiles<D, BS, 1, COLMASK, VLLM>(
+      kb, vb, t0, tok_end, reinterpret_cast<const uint32_t(&)[1][D / 16][2]>(qf), scale_log2,
+      reinterpret_cast<WarpState<D>(&)[1]>(st), lane, lim);
 }
 
 // Log-sum-exp merge of W warp states stored with WarpState::store (stride
@@ -698,11 +731,12 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
 // multi-token queries (varlen, causal)
 // ---------------------------------------------------------------------------
 //
-// One CTA per (sequence, KV head, chunk of QC queries), QC = max(1, 8 / G):
-// the mma's 8 columns are the (query, head) pairs of the chunk.  Query t of
-// sequence s sits at position pos_offsets[s] + t and sees positions up to
-// and including it: each column masks with its own limit.  The chunk reads
-// the context up to its last query's position.
+// One CTA per (sequence, KV head, chunk of QC queries), QC = max(1, 8 NT / G):
+// the 8 NT columns of the mma n-tiles are the (query, head) pairs of the
+// chunk, column n = (query n / G, head n % G).  Query t of sequence s sits
+// at position pos_offsets[s] + t and sees positions up to and including it:
+// each column masks with its own limit.  The chunk reads the context up to
+// its last query's position, once for all its columns.
 
 struct VarlenParams {
   const __half* q;              // [total_q][H][D]
@@ -721,11 +755,13 @@ struct VarlenParams {
   float scale_log2;
 };
 
-template <int D, int BS, int W, int P>
+template <int D, int BS, int W, int P, int NT>
 __global__ void __launch_bounds__(W * 32)
 paged_varlen_kernel(const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap, const VarlenParams p) {
   using Shape = DecodeShape<D, BS, W, P>;
+  static_assert(W * NT * Shape::kRedFloats * 4 <= Shape::kRingBytes,
+                "the merge area reuses the ring");
   constexpr int KS = Shape::kKS;
   constexpr int TB = Shape::kTileBytes;
 
@@ -802,26 +838,30 @@ paged_varlen_kernel(const __grid_constant__ CUtensorMap kmap,
     for (int li = 0; li < n0; ++li) issue(li);
   }
 
-  // column n = (query t0 + n / G, head n % G) while n < nq * G
+  // column n = (query t0 + n / G, head n % G) while n < nq * G; n-tile nt
+  // holds columns 8 nt .. 8 nt + 7 (this lane's B fragment: column 8 nt + r)
   const int ncols = nq * G;
-  uint32_t qf[KS][2];
-  {
-    const bool live = r < ncols;
-    const size_t row = (size_t)(q_begin + t0 + (live ? r / G : 0)) * p.num_heads +
-                       (size_t)g * G + (live ? r % G : 0);
+  uint32_t qf[NT][KS][2];
+  int lim[NT][2];
+  WarpState<D> st[NT];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int n = nt * 8 + r;
+    const bool live = n < ncols;
+    const size_t row = (size_t)(q_begin + t0 + (live ? n / G : 0)) * p.num_heads +
+                       (size_t)g * G + (live ? n % G : 0);
     const uint32_t* qrow = reinterpret_cast<const uint32_t*>(p.q + row * D);
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
-      qf[ks][0] = live ? __ldg(qrow + ks * 8 + c) : 0u;
-      qf[ks][1] = live ? __ldg(qrow + ks * 8 + 4 + c) : 0u;
+      qf[nt][ks][0] = live ? __ldg(qrow + ks * 8 + c) : 0u;
+      qf[nt][ks][1] = live ? __ldg(qrow + ks * 8 + 4 + c) : 0u;
     }
+    // this lane's columns 8 nt + 2c and 8 nt + 2c + 1: their causal limits
+    const int n0 = nt * 8 + 2 * c;
+    lim[nt][0] = (n0 < ncols) ? pos0 + t0 + n0 / G + 1 : tok_end;
+    lim[nt][1] = (n0 + 1 < ncols) ? pos0 + t0 + (n0 + 1) / G + 1 : tok_end;
+    st[nt].reset();
   }
-  // this lane's columns 2c and 2c+1: their causal limits
-  const int lim0 = (2 * c < ncols) ? pos0 + t0 + (2 * c) / G + 1 : tok_end;
-  const int lim1 = (2 * c + 1 < ncols) ? pos0 + t0 + (2 * c + 1) / G + 1 : tok_end;
-
-  WarpState<D> st;
-  st.reset();
   bool failed = false;
   int li = 0;
   for (; li < my_tiles; ++li) {
@@ -834,8 +874,8 @@ paged_varlen_kernel(const __grid_constant__ CUtensorMap kmap,
     const int phys = __ldg(table + j);
     if (phys >= 0 && phys < p.num_blocks) {
       const uint32_t kb = k_stage(stage);
-      consume_tile<D, BS, true>(kb, kb + TB, j * BS, tok_end, qf, p.scale_log2, st, lane, lim0,
-                                lim1);
+      consume_tiles<D, BS, NT, true, false>(kb, kb + TB, j * BS, tok_end, qf, p.scale_log2, st,
+                                            lane, lim);
     }
     __syncwarp();
     if (lane == 0 && li + P < my_tiles) {
@@ -851,17 +891,20 @@ paged_varlen_kernel(const __grid_constant__ CUtensorMap kmap,
     if (lane == 0) atomicOr(&s_failed, 1);
   }
 
-  st.finish_sums();
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) st[nt].finish_sums();
   __syncthreads();  // every warp is done with its ring
   if (s_failed) return;
   float* red = reinterpret_cast<float*>(smem);
-  st.store(red + warp * Shape::kRedFloats, lane, 8);
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) st[nt].store(red + (warp * NT + nt) * Shape::kRedFloats, lane, 8);
   __syncthreads();
   for (int idx = threadIdx.x; idx < ncols * D; idx += W * 32) {
     const int n = idx / D;
     const int d = idx - n * D;
     float M, num, den;
-    merge_warps<W, D>(red, Shape::kRedFloats, n, d, M, num, den);
+    merge_warps<W, D>(red + (n / 8) * Shape::kRedFloats, NT * Shape::kRedFloats, n % 8, d, M,
+                      num, den);
     const size_t row = (size_t)(q_begin + t0 + n / G) * p.num_heads + (size_t)g * G + n % G;
     p.out[row * D + d] = __float2half_rn(den > 0.f ? num / den : 0.f);
   }

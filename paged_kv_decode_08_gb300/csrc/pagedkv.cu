@@ -382,13 +382,13 @@ DecodeParams base_params(const DecodeArgs& a) {
   return p;
 }
 
-template <int D, int BS>
+template <int D, int BS, int NT>
 pkv_status launch_varlen(const DecodeArgs& a, const VarlenParams& vp, cudaStream_t stream,
                          int grid) {
   constexpr int W = Tuning<D, BS>::W;
   constexpr int P = Tuning<D, BS>::P;
   using Shape = DecodeShape<D, BS, W, P>;
-  auto kernel = paged_varlen_kernel<D, BS, W, P>;
+  auto kernel = paged_varlen_kernel<D, BS, W, P, NT>;
   static std::atomic<unsigned long long> attr_set{0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -716,7 +716,10 @@ pkv_status pkv_varlen_attention(const void* q, const void* k_cache, const void* 
   if (total_q < 0 || max_q_len < 0) return fail(PKV_ERR_INVALID_ARG, "total_q / max_q_len < 0");
   if (num_seqs == 0 || total_q == 0 || max_q_len == 0) return PKV_OK;
   const int G = num_heads / num_kv_heads;
-  const int qc = G >= 8 ? 1 : 8 / G;
+  // two n-tiles (16 columns) once a sequence has more than 8 (query, head)
+  // pairs: each chunk then reads its context once for twice the queries
+  const int NT = (long long)max_q_len * G > 8 ? 2 : 1;
+  const int qc = G >= 8 * NT ? 1 : 8 * NT / G;
   const int chunks = (max_q_len + qc - 1) / qc;
   const long long grid = (long long)num_seqs * num_kv_heads * chunks;
   if (grid >= (1ll << 31)) return fail(PKV_ERR_INVALID_ARG, "grid too large");
@@ -736,10 +739,17 @@ pkv_status pkv_varlen_attention(const void* q, const void* k_cache, const void* 
   vp.num_blocks = num_blocks;
   vp.scale_log2 = scale * 1.4426950408889634f;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  if (head_dim == 128 && block_size == 16) return launch_varlen<128, 16>(a, vp, cs, (int)grid);
-  if (head_dim == 128 && block_size == 32) return launch_varlen<128, 32>(a, vp, cs, (int)grid);
-  if (head_dim == 64 && block_size == 16) return launch_varlen<64, 16>(a, vp, cs, (int)grid);
-  if (head_dim == 64 && block_size == 32) return launch_varlen<64, 32>(a, vp, cs, (int)grid);
+  if (NT == 2) {
+    if (head_dim == 128 && block_size == 16) return launch_varlen<128, 16, 2>(a, vp, cs, (int)grid);
+    if (head_dim == 128 && block_size == 32) return launch_varlen<128, 32, 2>(a, vp, cs, (int)grid);
+    if (head_dim == 64 && block_size == 16) return launch_varlen<64, 16, 2>(a, vp, cs, (int)grid);
+    if (head_dim == 64 && block_size == 32) return launch_varlen<64, 32, 2>(a, vp, cs, (int)grid);
+  } else {
+    if (head_dim == 128 && block_size == 16) return launch_varlen<128, 16, 1>(a, vp, cs, (int)grid);
+    if (head_dim == 128 && block_size == 32) return launch_varlen<128, 32, 1>(a, vp, cs, (int)grid);
+    if (head_dim == 64 && block_size == 16) return launch_varlen<64, 16, 1>(a, vp, cs, (int)grid);
+    if (head_dim == 64 && block_size == 32) return launch_varlen<64, 32, 1>(a, vp, cs, (int)grid);
+  }
   return fail(PKV_ERR_UNSUPPORTED, "head_dim %d / block_size %d", head_dim, block_size);
 }
 

@@ -398,12 +398,17 @@ def varlen_device(v, dev):
     return d
 
 
+# A chunk covers 8 NT (query, head) columns: NT = 2 once a sequence has more
+# than 8, else 1.
 @pytest.mark.parametrize("H,Hkv,D,bs,q_lens,prefix", [
-    (8, 8, 64, 16, [1, 9, 0, 17], [0, 15, 3, 40]),       # G=1: 8 queries per CTA, 3 chunks
-    (4, 2, 64, 32, [5, 2, 1], [31, 0, 64]),              # G=2
-    (32, 8, 128, 16, [4, 4, 7, 1], [500, 16, 1, 77]),    # G=4
-    (28, 4, 128, 32, [3, 1, 6], [33, 1000, 0]),          # G=7: 1 query per CTA
-    (16, 2, 128, 16, [2, 5], [9, 130]),                  # G=8
+    (8, 8, 64, 16, [1, 9, 0, 17], [0, 15, 3, 40]),       # G=1, NT=2: 16 queries per CTA, 2 chunks
+    (4, 2, 64, 32, [5, 2, 1], [31, 0, 64]),              # G=2, NT=2: 1 chunk
+    (32, 8, 128, 16, [4, 4, 7, 1], [500, 16, 1, 77]),    # G=4, NT=2: 4 queries per CTA
+    (28, 4, 128, 32, [3, 1, 6], [33, 1000, 0]),          # G=7, NT=2: 2 queries, 2 unused columns
+    (16, 2, 128, 16, [2, 5], [9, 130]),                  # G=8, NT=2: 2 queries per CTA
+    (4, 4, 64, 16, [3, 8, 1, 0], [10, 0, 100, 5]),       # G=1, NT=1: 8 queries per CTA
+    (8, 4, 128, 32, [4, 1, 3], [64, 200, 1]),            # G=2, NT=1: 4 queries per CTA
+    (32, 8, 128, 16, [40, 3], [100, 0]),                 # G=4, NT=2: a 40-token prefill chunk
 ])
 def test_varlen_matches_oracle(pk, cuda_device, H, Hkv, D, bs, q_lens, prefix):
     v = W.varlen_random(3000 + H + D + bs, H, Hkv, D, bs, q_lens, prefix)

@@ -750,6 +750,8 @@ struct VarlenParams {
   int group;
   int qc;          // queries per CTA
   int num_chunks;  // chunks per (sequence, KV head) in the grid
+  int num_seqs;
+  int fair_depth;  // the grid is resident at once: scale in-flight depth
   int max_blocks_per_seq;
   int num_blocks;
   float scale_log2;
@@ -798,6 +800,17 @@ paged_varlen_kernel(const __grid_constant__ CUtensorMap kmap,
   const int q_begin = __ldg(p.cu_seqlens_q + s);
   const int q_end = __ldg(p.cu_seqlens_q + s + 1);
   int pos0 = __ldg(p.pos_offsets + s);
+  // fair share (as in the decode kernel): the longest context any chunk of
+  // the call reads, in tiles
+  int mx = 0;
+  if (p.fair_depth) {
+    for (int i = threadIdx.x; i < p.num_seqs; i += W * 32) {
+      int last = __ldg(p.pos_offsets + i) + __ldg(p.cu_seqlens_q + i + 1) -
+                 __ldg(p.cu_seqlens_q + i);
+      last = last < 0 ? 0 : (last > cap ? cap : last);
+      mx = max(mx, (last + BS - 1) / BS);
+    }
+  }
   if (__syncthreads_or(status & kDevWaitTimeout)) return;
 
   // bad query ranges or positions are flagged and skipped / clamped
@@ -818,12 +831,24 @@ paged_varlen_kernel(const __grid_constant__ CUtensorMap kmap,
   const int tok_end = min(cap, pos0 + t0 + nq);  // positions this chunk reads
   const int n_tiles = (tok_end + BS - 1) / BS;
   const int32_t* table = p.block_tables + (size_t)s * p.max_blocks_per_seq;
-  const int my_tiles = n_tiles > warp ? (n_tiles - warp + W - 1) / W : 0;
+  int WE = W;  // warps that take tiles (fewer for short chunks under the fair share)
+  if (p.fair_depth) {
+    __shared__ int s_max[W];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) s_max[warp] = mx;
+    __syncthreads();
+    mx = 0;
+#pragma unroll
+    for (int w = 0; w < W; ++w) mx = max(mx, s_max[w]);
+    if (mx > 0) WE = max(1, min(W, (W * n_tiles + mx - 1) / mx));
+  }
+  const int my_tiles = (warp < WE && n_tiles > warp) ? (n_tiles - warp + WE - 1) / WE : 0;
 
   auto k_stage = [&](int stage) { return ring + (warp * P + stage) * Shape::kStageBytes; };
   auto issue = [&](int li) {
     const int stage = li % P;
-    const int j = warp + li * W;
+    const int j = warp + li * WE;
     const int phys = __ldg(table + j);
     const uint32_t bar = my_bars + 8 * stage;
     if (phys >= 0 && phys < p.num_blocks) {
@@ -870,7 +895,7 @@ paged_varlen_kernel(const __grid_constant__ CUtensorMap kmap,
       failed = true;
       break;
     }
-    const int j = warp + li * W;
+    const int j = warp + li * WE;
     const int phys = __ldg(table + j);
     if (phys >= 0 && phys < p.num_blocks) {
       const uint32_t kb = k_stage(stage);

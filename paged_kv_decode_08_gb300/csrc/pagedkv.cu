@@ -404,7 +404,10 @@ pkv_status launch_varlen(const DecodeArgs& a, const VarlenParams& vp, cudaStream
   if (st != PKV_OK) return st;
   st = make_cache_map(&vmap, a.v_cache, a.num_blocks, a.num_kv_heads, BS, D);
   if (st != PKV_OK) return st;
-  e = launch_pdl(kernel, grid, W * 32, Shape::kSmemBytes, stream, kmap, vmap, vp);
+  VarlenParams vp2 = vp;
+  int sms = 0;
+  vp2.fair_depth = (current_device_sms(&sms) == 0 && grid <= sms * kCtasPerSm) ? 1 : 0;
+  e = launch_pdl(kernel, grid, W * 32, Shape::kSmemBytes, stream, kmap, vmap, vp2);
   if (e != cudaSuccess) return cuda_fail(e, "varlen attention launch");
   return PKV_OK;
 }
@@ -735,6 +738,7 @@ pkv_status pkv_varlen_attention(const void* q, const void* k_cache, const void* 
   vp.group = G;
   vp.qc = qc;
   vp.num_chunks = chunks;
+  vp.num_seqs = num_seqs;
   vp.max_blocks_per_seq = max_blocks_per_seq;
   vp.num_blocks = num_blocks;
   vp.scale_log2 = scale * 1.4426950408889634f;

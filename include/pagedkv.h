@@ -273,6 +273,20 @@ pkv_status pkv_decode_vllm_layout(const void* q, const void* k_cache, const void
                                   size_t scratch_bytes, void* stream);
 
 /*
+ * pkv_varlen_attention_vllm_layout — pkv_varlen_attention over vLLM-layout
+ * pools (ferrum-kernels src/backend/cuda/paged.rs,
+ * paged_varlen_attention_vllm_layout: several causal queries per sequence on
+ * the vLLM cache).  Arguments, results, flags and errors as
+ * pkv_varlen_attention; only the pool layout differs.
+ */
+pkv_status pkv_varlen_attention_vllm_layout(
+    const void* q, const void* k_cache, const void* v_cache, const int32_t* cu_seqlens_q,
+    const int32_t* pos_offsets, const int32_t* block_tables, int32_t num_seqs, int32_t total_q,
+    int32_t max_q_len, int32_t max_blocks_per_seq, int32_t num_blocks, float scale,
+    int32_t num_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size, void* out,
+    void* stream);
+
+/*
  * pkv_splitk_scratch_bytes — bytes of scratch pkv_decode_splitk needs for S
  * splits: f32 partial outputs [num_seqs][num_heads][S][head_dim] followed by
  * f32 running max and running sum [num_seqs][num_heads][S] each (every part

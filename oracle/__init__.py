@@ -12,4 +12,5 @@ from .paged_attention import (  # noqa: F401
     kv_head_of,
     softmax,
     varlen,
+    varlen_vllm_layout,
 )

@@ -41,7 +41,8 @@ so they do not appear here):
   ``b`` at ``[b, h, d // 8, o, d % 8]``; V is ``[NB][Hkv][D][bs]``, at
   ``[b, h, d, o]``.  ``append_vllm_layout`` writes element by element;
   ``blocked_from_vllm_layout`` reads the pools back as ``[NB][Hkv][bs][D]``,
-  after which the definitions above apply unchanged.  Pinned in
+  after which the definitions above apply unchanged (``decode_vllm_layout``,
+  ``varlen_vllm_layout``).  Pinned in
   ``tests/test_oracle_vllm_layout.py`` by a round trip through the blocked
   append and by chunk contiguity found by search.
 
@@ -251,11 +252,9 @@ def blocked_from_vllm_layout(k_cache, v_cache, blocks=None):
     return kb, vb
 
 
-def decode_vllm_layout(q, k_cache, v_cache, block_tables, context_lens, scale, seqs=None,
-                       fast=False):
-    """``decode`` (``decode_fast`` with ``fast``) over vLLM-layout pools: the
-    blocks the chosen sequences read are read back as blocked pools (tables
-    renumbered to match), then the definition runs on those."""
+def _blocked_view_of_used(k_cache, v_cache, block_tables, context_lens, seqs):
+    """The blocks that ``seqs`` read (positions below ``context_lens``) from
+    vLLM-layout pools, as blocked pools, with the tables renumbered to match."""
     bs = k_cache.shape[3]
     bt = np.asarray(block_tables)
     lens = np.asarray(context_lens)
@@ -268,4 +267,25 @@ def decode_vllm_layout(q, k_cache, v_cache, block_tables, context_lens, scale, s
     for s in chosen:
         for j in range(-(-int(lens[s]) // bs)):
             bt2[s, j] = where[int(bt[s, j])]
-    return (decode_fast if fast else decode)(q, kb, vb, bt2, lens, scale, seqs)
+    return kb, vb, bt2
+
+
+def decode_vllm_layout(q, k_cache, v_cache, block_tables, context_lens, scale, seqs=None,
+                       fast=False):
+    """``decode`` (``decode_fast`` with ``fast``) over vLLM-layout pools: the
+    blocks the chosen sequences read are read back as blocked pools (tables
+    renumbered to match), then the definition runs on those."""
+    kb, vb, bt2 = _blocked_view_of_used(k_cache, v_cache, block_tables, context_lens, seqs)
+    return (decode_fast if fast else decode)(q, kb, vb, bt2, np.asarray(context_lens), scale,
+                                             seqs)
+
+
+def varlen_vllm_layout(q, k_cache, v_cache, cu_seqlens_q, pos_offsets, block_tables, scale):
+    """``varlen`` over vLLM-layout pools (ferrum-kernels
+    ``src/backend/cuda/paged.rs``, ``paged_varlen_attention_vllm_layout``):
+    the blocks the sequences read, up to their last query's position, are
+    read back as blocked pools, then ``varlen`` runs on those."""
+    cu = np.asarray(cu_seqlens_q).astype(np.int64)
+    ends = np.asarray(pos_offsets).astype(np.int64) + np.diff(cu)
+    kb, vb, bt2 = _blocked_view_of_used(k_cache, v_cache, block_tables, ends, None)
+    return varlen(q, kb, vb, cu_seqlens_q, pos_offsets, bt2, scale)

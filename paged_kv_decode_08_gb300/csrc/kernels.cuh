@@ -736,7 +736,8 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
 // chunk, column n = (query n / G, head n % G).  Query t of sequence s sits
 // at position pos_offsets[s] + t and sees positions up to and including it:
 // each column masks with its own limit.  The chunk reads the context up to
-// its last query's position, once for all its columns.
+// its last query's position, once for all its columns.  VLLM: the pools are
+// in the vLLM layout (p.k_pool is the K pool; kmap is unused).
 
 struct VarlenParams {
   const __half* q;              // [total_q][H][D]
@@ -752,12 +753,13 @@ struct VarlenParams {
   int num_chunks;  // chunks per (sequence, KV head) in the grid
   int num_seqs;
   int fair_depth;  // the grid is resident at once: scale in-flight depth
+  const __half* k_pool;  // the K pool (vLLM layout: tiles are bulk-copied from it)
   int max_blocks_per_seq;
   int num_blocks;
   float scale_log2;
 };
 
-template <int D, int BS, int W, int P, int NT>
+template <int D, int BS, int W, int P, int NT, bool VLLM>
 __global__ void __launch_bounds__(W * 32)
 paged_varlen_kernel(const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap, const VarlenParams p) {
@@ -852,7 +854,8 @@ paged_varlen_kernel(const __grid_constant__ CUtensorMap kmap,
     const int phys = __ldg(table + j);
     const uint32_t bar = my_bars + 8 * stage;
     if (phys >= 0 && phys < p.num_blocks) {
-      issue_tile_copy<D, BS>(k_stage(stage), bar, phys * p.num_kv_heads + g, &kmap, &vmap);
+      issue_tile_copy<D, BS, VLLM>(k_stage(stage), bar, phys * p.num_kv_heads + g, &kmap, &vmap,
+                                   p.k_pool);
     } else {
       atomicOr(&g_device_status, kDevBadBlockId);
       mbar_arrive(bar);
@@ -899,8 +902,8 @@ paged_varlen_kernel(const __grid_constant__ CUtensorMap kmap,
     const int phys = __ldg(table + j);
     if (phys >= 0 && phys < p.num_blocks) {
       const uint32_t kb = k_stage(stage);
-      consume_tiles<D, BS, NT, true, false>(kb, kb + TB, j * BS, tok_end, qf, p.scale_log2, st,
-                                            lane, lim);
+      consume_tiles<D, BS, NT, true, VLLM>(kb, kb + TB, j * BS, tok_end, qf, p.scale_log2, st,
+                                           lane, lim);
     }
     __syncwarp();
     if (lane == 0 && li + P < my_tiles) {

@@ -382,13 +382,13 @@ DecodeParams base_params(const DecodeArgs& a) {
   return p;
 }
 
-template <int D, int BS, int NT>
+template <int D, int BS, int NT, bool VLLM>
 pkv_status launch_varlen(const DecodeArgs& a, const VarlenParams& vp, cudaStream_t stream,
                          int grid) {
   constexpr int W = Tuning<D, BS>::W;
   constexpr int P = Tuning<D, BS>::P;
   using Shape = DecodeShape<D, BS, W, P>;
-  auto kernel = paged_varlen_kernel<D, BS, W, P, NT>;
+  auto kernel = paged_varlen_kernel<D, BS, W, P, NT, VLLM>;
   static std::atomic<unsigned long long> attr_set{0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -400,11 +400,20 @@ pkv_status launch_varlen(const DecodeArgs& a, const VarlenParams& vp, cudaStream
     attr_set.fetch_or(bit, std::memory_order_relaxed);
   }
   CUtensorMap kmap, vmap;
-  pkv_status st = make_cache_map(&kmap, a.k_cache, a.num_blocks, a.num_kv_heads, BS, D);
-  if (st != PKV_OK) return st;
-  st = make_cache_map(&vmap, a.v_cache, a.num_blocks, a.num_kv_heads, BS, D);
-  if (st != PKV_OK) return st;
+  pkv_status st;
   VarlenParams vp2 = vp;
+  if (VLLM) {
+    // K tiles are bulk-copied from the pool pointer; kmap only fills the slot
+    st = make_vllm_v_map(&vmap, a.v_cache, a.num_blocks, a.num_kv_heads, BS, D);
+    if (st != PKV_OK) return st;
+    kmap = vmap;
+    vp2.k_pool = static_cast<const __half*>(a.k_cache);
+  } else {
+    st = make_cache_map(&kmap, a.k_cache, a.num_blocks, a.num_kv_heads, BS, D);
+    if (st != PKV_OK) return st;
+    st = make_cache_map(&vmap, a.v_cache, a.num_blocks, a.num_kv_heads, BS, D);
+    if (st != PKV_OK) return st;
+  }
   int sms = 0;
   vp2.fair_depth = (current_device_sms(&sms) == 0 && grid <= sms * kCtasPerSm) ? 1 : 0;
   e = launch_pdl(kernel, grid, W * 32, Shape::kSmemBytes, stream, kmap, vmap, vp2);
@@ -636,6 +645,69 @@ pkv_status decode_impl(const DecodeArgs& a, int num_splits, void* scratch, size_
   return PKV_OK;
 }
 
+// The body of pkv_varlen_attention and its vLLM-layout twin.
+pkv_status varlen_impl(const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* cu_seqlens_q, const int32_t* pos_offsets,
+                       const int32_t* block_tables, int num_seqs, int total_q, int max_q_len,
+                       int max_blocks_per_seq, int num_blocks, float scale, int num_heads,
+                       int num_kv_heads, int head_dim, int block_size, void* out,
+                       cudaStream_t cs, bool vllm) {
+  // pos_offsets stands in for context_lens in the shared checks
+  const DecodeArgs a{q, k_cache, v_cache, block_tables, pos_offsets, num_seqs,
+                     max_blocks_per_seq, num_blocks, scale, num_heads, num_kv_heads,
+                     head_dim, block_size, out};
+  pkv_status st = validate_decode(a);
+  if (st != PKV_OK) return st;
+  if (!cu_seqlens_q || !aligned(cu_seqlens_q, 4))
+    return fail(PKV_ERR_INVALID_ARG, "cu_seqlens_q must be a 4-byte aligned device pointer");
+  if (total_q < 0 || max_q_len < 0) return fail(PKV_ERR_INVALID_ARG, "total_q / max_q_len < 0");
+  if (num_seqs == 0 || total_q == 0 || max_q_len == 0) return PKV_OK;
+  const int G = num_heads / num_kv_heads;
+  // two n-tiles (16 columns) once a sequence has more than 8 (query, head)
+  // pairs: each chunk then reads its context once for twice the queries
+  const int NT = (long long)max_q_len * G > 8 ? 2 : 1;
+  const int qc = G >= 8 * NT ? 1 : 8 * NT / G;
+  const int chunks = (max_q_len + qc - 1) / qc;
+  const long long grid = (long long)num_seqs * num_kv_heads * chunks;
+  if (grid >= (1ll << 31)) return fail(PKV_ERR_INVALID_ARG, "grid too large");
+  VarlenParams vp{};
+  vp.q = static_cast<const __half*>(q);
+  vp.cu_seqlens_q = cu_seqlens_q;
+  vp.pos_offsets = pos_offsets;
+  vp.block_tables = block_tables;
+  vp.out = static_cast<__half*>(out);
+  vp.total_q = total_q;
+  vp.num_heads = num_heads;
+  vp.num_kv_heads = num_kv_heads;
+  vp.group = G;
+  vp.qc = qc;
+  vp.num_chunks = chunks;
+  vp.num_seqs = num_seqs;
+  vp.max_blocks_per_seq = max_blocks_per_seq;
+  vp.num_blocks = num_blocks;
+  vp.scale_log2 = scale * 1.4426950408889634f;
+  if (NT == 2) {
+    if (head_dim == 128 && block_size == 16) return vllm ? launch_varlen<128, 16, 2, true>(a, vp, cs, (int)grid)
+                : launch_varlen<128, 16, 2, false>(a, vp, cs, (int)grid);
+    if (head_dim == 128 && block_size == 32) return vllm ? launch_varlen<128, 32, 2, true>(a, vp, cs, (int)grid)
+                : launch_varlen<128, 32, 2, false>(a, vp, cs, (int)grid);
+    if (head_dim == 64 && block_size == 16) return vllm ? launch_varlen<64, 16, 2, true>(a, vp, cs, (int)grid)
+                : launch_varlen<64, 16, 2, false>(a, vp, cs, (int)grid);
+    if (head_dim == 64 && block_size == 32) return vllm ? launch_varlen<64, 32, 2, true>(a, vp, cs, (int)grid)
+                : launch_varlen<64, 32, 2, false>(a, vp, cs, (int)grid);
+  } else {
+    if (head_dim == 128 && block_size == 16) return vllm ? launch_varlen<128, 16, 1, true>(a, vp, cs, (int)grid)
+                : launch_varlen<128, 16, 1, false>(a, vp, cs, (int)grid);
+    if (head_dim == 128 && block_size == 32) return vllm ? launch_varlen<128, 32, 1, true>(a, vp, cs, (int)grid)
+                : launch_varlen<128, 32, 1, false>(a, vp, cs, (int)grid);
+    if (head_dim == 64 && block_size == 16) return vllm ? launch_varlen<64, 16, 1, true>(a, vp, cs, (int)grid)
+                : launch_varlen<64, 16, 1, false>(a, vp, cs, (int)grid);
+    if (head_dim == 64 && block_size == 32) return vllm ? launch_varlen<64, 32, 1, true>(a, vp, cs, (int)grid)
+                : launch_varlen<64, 32, 1, false>(a, vp, cs, (int)grid);
+  }
+  return fail(PKV_ERR_UNSUPPORTED, "head_dim %d / block_size %d", head_dim, block_size);
+}
+
 }  // namespace
 }  // namespace pkv
 
@@ -708,53 +780,22 @@ pkv_status pkv_varlen_attention(const void* q, const void* k_cache, const void* 
                                 int32_t num_blocks, float scale, int32_t num_heads,
                                 int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                                 void* out, void* stream) {
-  // pos_offsets stands in for context_lens in the shared checks
-  const DecodeArgs a{q, k_cache, v_cache, block_tables, pos_offsets, num_seqs,
-                     max_blocks_per_seq, num_blocks, scale, num_heads, num_kv_heads,
-                     head_dim, block_size, out};
-  pkv_status st = validate_decode(a);
-  if (st != PKV_OK) return st;
-  if (!cu_seqlens_q || !aligned(cu_seqlens_q, 4))
-    return fail(PKV_ERR_INVALID_ARG, "cu_seqlens_q must be a 4-byte aligned device pointer");
-  if (total_q < 0 || max_q_len < 0) return fail(PKV_ERR_INVALID_ARG, "total_q / max_q_len < 0");
-  if (num_seqs == 0 || total_q == 0 || max_q_len == 0) return PKV_OK;
-  const int G = num_heads / num_kv_heads;
-  // two n-tiles (16 columns) once a sequence has more than 8 (query, head)
-  // pairs: each chunk then reads its context once for twice the queries
-  const int NT = (long long)max_q_len * G > 8 ? 2 : 1;
-  const int qc = G >= 8 * NT ? 1 : 8 * NT / G;
-  const int chunks = (max_q_len + qc - 1) / qc;
-  const long long grid = (long long)num_seqs * num_kv_heads * chunks;
-  if (grid >= (1ll << 31)) return fail(PKV_ERR_INVALID_ARG, "grid too large");
-  VarlenParams vp{};
-  vp.q = static_cast<const __half*>(q);
-  vp.cu_seqlens_q = cu_seqlens_q;
-  vp.pos_offsets = pos_offsets;
-  vp.block_tables = block_tables;
-  vp.out = static_cast<__half*>(out);
-  vp.total_q = total_q;
-  vp.num_heads = num_heads;
-  vp.num_kv_heads = num_kv_heads;
-  vp.group = G;
-  vp.qc = qc;
-  vp.num_chunks = chunks;
-  vp.num_seqs = num_seqs;
-  vp.max_blocks_per_seq = max_blocks_per_seq;
-  vp.num_blocks = num_blocks;
-  vp.scale_log2 = scale * 1.4426950408889634f;
-  cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  if (NT == 2) {
-    if (head_dim == 128 && block_size == 16) return launch_varlen<128, 16, 2>(a, vp, cs, (int)grid);
-    if (head_dim == 128 && block_size == 32) return launch_varlen<128, 32, 2>(a, vp, cs, (int)grid);
-    if (head_dim == 64 && block_size == 16) return launch_varlen<64, 16, 2>(a, vp, cs, (int)grid);
-    if (head_dim == 64 && block_size == 32) return launch_varlen<64, 32, 2>(a, vp, cs, (int)grid);
-  } else {
-    if (head_dim == 128 && block_size == 16) return launch_varlen<128, 16, 1>(a, vp, cs, (int)grid);
-    if (head_dim == 128 && block_size == 32) return launch_varlen<128, 32, 1>(a, vp, cs, (int)grid);
-    if (head_dim == 64 && block_size == 16) return launch_varlen<64, 16, 1>(a, vp, cs, (int)grid);
-    if (head_dim == 64 && block_size == 32) return launch_varlen<64, 32, 1>(a, vp, cs, (int)grid);
-  }
-  return fail(PKV_ERR_UNSUPPORTED, "head_dim %d / block_size %d", head_dim, block_size);
+  return varlen_impl(q, k_cache, v_cache, cu_seqlens_q, pos_offsets, block_tables, num_seqs,
+                     total_q, max_q_len, max_blocks_per_seq, num_blocks, scale, num_heads,
+                     num_kv_heads, head_dim, block_size, out, static_cast<cudaStream_t>(stream),
+                     false);
+}
+
+pkv_status pkv_varlen_attention_vllm_layout(
+    const void* q, const void* k_cache, const void* v_cache, const int32_t* cu_seqlens_q,
+    const int32_t* pos_offsets, const int32_t* block_tables, int32_t num_seqs, int32_t total_q,
+    int32_t max_q_len, int32_t max_blocks_per_seq, int32_t num_blocks, float scale,
+    int32_t num_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size, void* out,
+    void* stream) {
+  return varlen_impl(q, k_cache, v_cache, cu_seqlens_q, pos_offsets, block_tables, num_seqs,
+                     total_q, max_q_len, max_blocks_per_seq, num_blocks, scale, num_heads,
+                     num_kv_heads, head_dim, block_size, out, static_cast<cudaStream_t>(stream),
+                     true);
 }
 
 pkv_status pkv_read_device_status(int32_t* flags, void* stream) {

@@ -61,6 +61,8 @@ def _load():
     lib.pkv_varlen_attention.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32,
                                          i32, i32, i32, vp, vp]
     lib.pkv_varlen_attention.restype = i32
+    lib.pkv_varlen_attention_vllm_layout.argtypes = lib.pkv_varlen_attention.argtypes
+    lib.pkv_varlen_attention_vllm_layout.restype = i32
     lib.pkv_decode_splitk_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, f32, i32, i32,
                                               i32, i32, vp, i32, vp]
     lib.pkv_decode_splitk_noalloc.restype = i32
@@ -252,15 +254,31 @@ def pkv_varlen_attention(q, k_cache, v_cache, cu_seqlens_q, pos_offsets, block_t
                          max_q_len=None, out=None, stream=None):
     """Causal attention of several query tokens per sequence (token-major
     ``q [total_q][H][D]``, ``cu_seqlens_q [B+1]``, ``pos_offsets [B]``)."""
+    return _varlen(q, k_cache, v_cache, cu_seqlens_q, pos_offsets, block_tables, scale,
+                   max_q_len, out, stream, vllm=False)
+
+
+def pkv_varlen_attention_vllm_layout(q, k_cache, v_cache, cu_seqlens_q, pos_offsets,
+                                     block_tables, scale, max_q_len=None, out=None, stream=None):
+    """:func:`pkv_varlen_attention` over vLLM-layout pools."""
+    return _varlen(q, k_cache, v_cache, cu_seqlens_q, pos_offsets, block_tables, scale,
+                   max_q_len, out, stream, vllm=True)
+
+
+def _varlen(q, k_cache, v_cache, cu_seqlens_q, pos_offsets, block_tables, scale, max_q_len, out,
+            stream, vllm):
     import torch
 
     _want(q, "q", torch.float16, 3)
     total_q, H, D = q.shape
-    _want(k_cache, "k_cache", torch.float16, 4)
-    NB, Hkv, bs, Dk = k_cache.shape
+    if vllm:
+        NB, Hkv, bs, Dk = _vllm_pools(k_cache, v_cache)
+    else:
+        _want(k_cache, "k_cache", torch.float16, 4)
+        NB, Hkv, bs, Dk = k_cache.shape
+        _want(v_cache, "v_cache", torch.float16, 4, k_cache.shape)
     if Dk != D:
         raise ValueError("k_cache head_dim differs from q")
-    _want(v_cache, "v_cache", torch.float16, 4, k_cache.shape)
     _want(block_tables, "block_tables", torch.int32, 2)
     B = block_tables.shape[0]
     _want(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1, (B + 1,))
@@ -270,11 +288,12 @@ def pkv_varlen_attention(q, k_cache, v_cache, cu_seqlens_q, pos_offsets, block_t
     _want(out, "out", torch.float16, 3, (total_q, H, D))
     if max_q_len is None:
         raise ValueError("max_q_len (a host-side bound) is required")
-    _check(lib.pkv_varlen_attention(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
-                                    cu_seqlens_q.data_ptr(), pos_offsets.data_ptr(),
-                                    block_tables.data_ptr(), B, total_q, int(max_q_len),
-                                    block_tables.shape[1], NB, float(scale), H, Hkv, D, bs,
-                                    out.data_ptr(), _stream_ptr(stream)), "pkv_varlen_attention")
+    fn = lib.pkv_varlen_attention_vllm_layout if vllm else lib.pkv_varlen_attention
+    _check(fn(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), cu_seqlens_q.data_ptr(),
+              pos_offsets.data_ptr(), block_tables.data_ptr(), B, total_q, int(max_q_len),
+              block_tables.shape[1], NB, float(scale), H, Hkv, D, bs, out.data_ptr(),
+              _stream_ptr(stream)),
+           "pkv_varlen_attention_vllm_layout" if vllm else "pkv_varlen_attention")
     return out
 
 

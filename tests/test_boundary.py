@@ -33,7 +33,8 @@ def test_header_declares_the_expected_calls():
     for n in ["pkv_append", "pkv_decode", "pkv_decode_splitk", "pkv_append_decode",
               "pkv_varlen_attention", "pkv_splitk_scratch_bytes",
               "pkv_pick_num_splits", "pkv_status_string", "pkv_last_error",
-              "pkv_read_device_status", "pkv_append_vllm_layout", "pkv_decode_vllm_layout"]:
+              "pkv_read_device_status", "pkv_append_vllm_layout", "pkv_decode_vllm_layout",
+              "pkv_varlen_attention_vllm_layout"]:
         assert n in names
 
 
@@ -211,3 +212,15 @@ def test_vllm_layout_calls_reject_bad_arguments(pk):
     assert a(F16, F16, F16, 2, F16, F16, 8, 24, 2, 64, None) == -2
     assert a(F16, F16, F16, 2, F16 + 4, F16, 8, 16, 2, 64, None) == -1
     assert a(F16, F16, F16, 0, F16, F16, 8, 16, 2, 64, None) == 0
+
+
+def test_vllm_varlen_rejects_bad_arguments(pk):
+    f = pk.lib.pkv_varlen_attention_vllm_layout
+    ok = [F16, F16, F16, F16, F16, F16, 2, 5, 4, 3, 8, 0.125, 4, 2, 64, 16, F16, None]
+    cu_null = list(ok)
+    cu_null[3] = None
+    assert f(*cu_null) == -1
+    assert f(*(ok[:7] + [0] + ok[8:])) == 0  # no queries
+    bad_bs = list(ok)
+    bad_bs[15] = 24
+    assert f(*bad_bs) == -2

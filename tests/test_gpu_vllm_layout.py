@@ -1,5 +1,6 @@
 """GPU parity of the vLLM-layout calls (pkv_append_vllm_layout,
-pkv_decode_vllm_layout) against the CPU oracle, through the C ABI.
+pkv_decode_vllm_layout, pkv_varlen_attention_vllm_layout) against the CPU
+oracle, through the C ABI.
 
 Pools are K [NB][Hkv][D/8][bs][8] and V [NB][Hkv][D][bs], built from the
 same seeded workloads as the blocked tests, with NaN in every unused block and
@@ -206,3 +207,57 @@ def test_vllm_balanced_schedule_is_unsupported(pk, cuda_device):
         pk.pkv_decode_vllm_layout(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
                                   d["context_lens"], w.scale, num_splits=-1, scratch=scratch)
     assert e.value.status == pk.PKV_ERR_UNSUPPORTED
+
+
+# ---------------------------------------------------------------------------
+# several causal queries per sequence on the vLLM layout
+# ---------------------------------------------------------------------------
+
+def varlen_device_vllm(v, dev):
+    d = W.to_device_vllm(v.base, dev)
+    d["q"] = torch.from_numpy(v.q).to(dev)
+    d["cu"] = torch.from_numpy(v.cu_seqlens_q).to(dev)
+    d["pos"] = torch.from_numpy(v.pos_offsets).to(dev)
+    return d
+
+
+@pytest.mark.parametrize("H,Hkv,D,bs,q_lens,prefix", [
+    (8, 8, 64, 16, [1, 9, 0, 17], [0, 15, 3, 40]),       # G=1, NT=2, 2 chunks
+    (32, 8, 128, 16, [4, 4, 7, 1], [500, 16, 1, 77]),    # G=4, NT=2
+    (28, 4, 128, 32, [3, 1, 6], [33, 1000, 0]),          # G=7, NT=2
+    (8, 4, 128, 32, [4, 1, 3], [64, 200, 1]),            # G=2, NT=1
+])
+def test_vllm_varlen_matches_oracle(pk, cuda_device, H, Hkv, D, bs, q_lens, prefix):
+    v = W.varlen_random(4000 + H + D + bs, H, Hkv, D, bs, q_lens, prefix)
+    kc, vc = W.host_pool_vllm(v.base)
+    ref = oracle.varlen_vllm_layout(v.q, kc, vc, v.cu_seqlens_q, v.pos_offsets,
+                                    v.base.block_tables, v.base.scale)
+    d = varlen_device_vllm(v, cuda_device)
+    out = pk.pkv_varlen_attention_vllm_layout(d["q"], d["k_cache"], d["v_cache"], d["cu"],
+                                              d["pos"], d["block_tables"], v.base.scale,
+                                              max_q_len=v.max_q_len)
+    torch.cuda.synchronize()
+    assert_attention_close(to_np(out), ref, f"vLLM varlen H{H} Hkv{Hkv} D{D} bs{bs}")
+    assert pk.pkv_read_device_status() == 0
+
+
+def test_vllm_varlen_speculative_verification_equals_blocked(pk, cuda_device):
+    """Four draft tokens per sequence on the Llama-3-8B shape: the vLLM-layout
+    call matches the oracle and the blocked call bit for bit."""
+    v = W.spec_verify()
+    kc, vc = W.host_pool_vllm(v.base)
+    ref = oracle.varlen_vllm_layout(v.q, kc, vc, v.cu_seqlens_q, v.pos_offsets,
+                                    v.base.block_tables, v.base.scale)
+    del kc, vc
+    d = varlen_device_vllm(v, cuda_device)
+    got = pk.pkv_varlen_attention_vllm_layout(d["q"], d["k_cache"], d["v_cache"], d["cu"],
+                                              d["pos"], d["block_tables"], v.base.scale,
+                                              max_q_len=4)
+    del d["k_cache"], d["v_cache"]
+    db = W.to_device(v.base, cuda_device)
+    blocked = pk.pkv_varlen_attention(d["q"], db["k_cache"], db["v_cache"], d["cu"], d["pos"],
+                                      d["block_tables"], v.base.scale, max_q_len=4)
+    torch.cuda.synchronize()
+    assert_attention_close(to_np(got), ref, "vLLM spec verify")
+    assert_bits_equal(got.cpu().numpy(), blocked.cpu().numpy(), "vLLM vs blocked varlen")
+    assert pk.pkv_read_device_status() == 0

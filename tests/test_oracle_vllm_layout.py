@@ -13,7 +13,8 @@ The layout is vLLM's published paged-attention layout: K
   is an aligned run of 8 consecutive head-dim values of one token row, and
   every V row ``[b, h, d, :]`` holds element d of the block's tokens in slot
   order;
-* ``decode_vllm_layout`` equals ``decode`` on the same logical cache.
+* ``decode_vllm_layout`` equals ``decode``, and ``varlen_vllm_layout`` equals
+  ``varlen``, on the same logical cache.
 
 Each planted mistake below must break one of them.  D = 64 makes D/8 = 8,
 so swapping the chunk and element axes keeps every shape valid.
@@ -122,9 +123,42 @@ def decode_ok(mod, seed=2):
             and not part[[0, 1, 3]].any())
 
 
+def varlen_ok(mod, seed=5):
+    """Several causal queries per sequence: the vLLM-layout varlen equals the
+    blocked varlen on the same logical cache."""
+    rng = np.random.default_rng(seed)
+    NB, Hkv, bs, D, H = 12, 2, 16, 64, 4
+    prefix = np.array([0, 15, 30], np.int32)
+    q_lens = np.array([3, 1, 5], np.int32)
+    lens = prefix + q_lens
+    perm = rng.permutation(NB).astype(np.int32)
+    bt = np.full((3, 3), 11, np.int32)
+    cur = 0
+    for s, L in enumerate(lens):
+        n = -(-int(L) // bs)
+        bt[s, :n] = perm[cur:cur + n]
+        cur += n
+    T = int(lens.sum())
+    k = rng.standard_normal((T, Hkv, D)).astype(np.float16)
+    v = rng.standard_normal((T, Hkv, D)).astype(np.float16)
+    slots = np.concatenate([bt[s, np.arange(L) // bs] * bs + np.arange(L) % bs
+                            for s, L in enumerate(lens)]).astype(np.int32)
+    kb = np.zeros((NB, Hkv, bs, D), np.float16)
+    vb = np.zeros_like(kb)
+    oracle.append(k, v, slots, kb, vb)
+    kv = np.zeros((NB, Hkv, D // 8, bs, 8), np.float16)
+    vv = np.zeros((NB, Hkv, D, bs), np.float16)
+    mod.append_vllm_layout(k, v, slots, kv, vv)
+    cu = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    q = rng.standard_normal((int(cu[-1]), H, D)).astype(np.float16)
+    ref = oracle.varlen(q, kb, vb, cu, prefix, bt, 0.125)
+    got = mod.varlen_vllm_layout(q, kv, vv, cu, prefix, bt, 0.125)
+    return np.array_equal(got, ref)
+
+
 def all_pins(mod):
     return {"round_trip": round_trip_ok(mod), "contiguity": contiguity_ok(mod),
-            "decode": decode_ok(mod)}
+            "decode": decode_ok(mod), "varlen": varlen_ok(mod)}
 
 
 def test_oracle_vllm_layout_pins():
@@ -170,6 +204,8 @@ MUTATIONS = {
     "adapter_v_from_k": ("vb[:, :, :, d] = v_cache[idx, :, d, :]",
                          "vb[:, :, :, d] = k_cache[idx, :, d // x, :, d % x]"),
     "decode_tables_not_renumbered": ("bt2[s, j] = where[int(bt[s, j])]", "bt2[s, j] = int(bt[s, j]) % len(used)"),
+    "varlen_reads_only_the_prefix": ("ends = np.asarray(pos_offsets).astype(np.int64) + np.diff(cu)",
+                                     "ends = np.asarray(pos_offsets).astype(np.int64) + 1"),
 }
 
 

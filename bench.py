@@ -63,9 +63,9 @@ N_SETS = 4  # default number of rotating pool sets (--sets)
 # Reported as null when the kernels have changed since.
 NCU_TRAFFIC = {
     # profiles/decode_llama8b.md: the fused append + single-pass decode launch,
-    # dram read 175.218 MB + write 3.241 MB
-    "llama8b": {"kernel_hash": "3fbec2a6293e5277", "bytes_per_launch": 178459136, "num_splits": 1,
-                "fused": True,
+    # dram read 175.222 MB + write 3.364 MB
+    "llama8b": {"kernel_hash": "e8e4bd0554894353", "bytes_per_launch": 178585600, "num_splits": 1,
+                "fused": True, "layout": "blocked",
                 "kernel": "paged_decode_kernel<128,16,6,2,single,fused>"},
 }
 

@@ -1,9 +1,13 @@
 // Kernels of libpagedkv (GB300, sm_103a):
 //   append_kernel                 slot-mapped KV write
+//   append_vllm_kernel            the same write into vLLM-layout pools
 //   paged_decode_kernel           decode: single pass, or split-K phase 1;
-//                                 optionally with the step's append fused in
+//                                 optionally with the step's append fused in;
+//                                 blocked or vLLM-layout pools
 //   splitk_combine_kernel         log-sum-exp merge of split-K partials
-//   paged_varlen_kernel           several causal queries per sequence
+//   paged_varlen_kernel           several causal queries per sequence (one or
+//                                 two mma n-tiles of 8 query-head columns);
+//                                 blocked or vLLM-layout pools
 //   paged_decode_balanced_kernel  decode over equal tile ranges per CTA
 //   balanced_combine_kernel       merge of the balanced schedule's records
 //
@@ -13,8 +17,9 @@
 //  * Each of the CTA's W warps owns a private ring of P shared-memory stages.
 //    A stage holds the K and V tiles of one physical block for this KV head
 //    (block_size x head_dim f16 each, contiguous in the pool).  Lane 0 of the
-//    warp fetches them with TMA tensor copies (128-byte swizzle) that complete
-//    on the stage's mbarrier.  Warp w takes the chunk's blocks w, w+WE, ...
+//    warp fetches them with TMA copies (tensor copies with the 128-byte
+//    swizzle; a bulk copy for vLLM-layout K tiles) that complete on the
+//    stage's mbarrier.  Warp w takes the chunk's blocks w, w+WE, ...
 //    where WE <= W warps are active (fewer for short sequences under the
 //    fair-share depth, see DecodeParams::fair_depth).
 //  * Scores use tensor cores with tokens on M and the group on N:

@@ -51,7 +51,10 @@ WORKLOAD_DESC = {
     "tiny": ("tiny paged decode: B=2, H=4, Hkv=2, D=64, bs=16, context_lens {17,40}, "
              "8-block pool"),
     "spec": ("speculative-decode verification: B=32, H=32, Hkv=8, D=128, bs=16, 4 draft tokens "
-             "per sequence over a prefix ~U[508,2044] (pkv_varlen_attention, causal)"),
+             "per sequence over a prefix ~U[508,2044] (pkv_varlen_attention_splitk, causal)"),
+    "spec_long": ("speculative-decode verification over long contexts: B=4, H=32, Hkv=8, D=128, "
+                  "bs=16, 4 draft tokens per sequence after prefixes {32768,65536,98304,131072}-4, "
+                  "24576-block pool (pkv_varlen_attention_splitk, causal)"),
     "loop": ("append+decode loop: MHA H=Hkv=16, D=64, bs=16, B=128, start context U[64,4096], "
              "128 steps of pkv_append (142 rows, 14 padding slots = -1, new blocks from a "
              "shuffled free list of 40000) then pkv_decode_splitk on one stream"),
@@ -368,9 +371,12 @@ def run_loop(args):
 
 def run_varlen(args):
     """Speculative verification: 4 query tokens per sequence, causal, over
-    the paged context (pkv_varlen_attention).  Algorithmic bytes count each
-    sequence's context once; a CTA covers 8 / G queries, so the kernel reads
-    a context ceil(4 / (8 / G)) times (twice at G = 4)."""
+    the paged context (pkv_varlen_attention_splitk; the split count is the
+    library's heuristic unless --splits forces one).  Algorithmic bytes count
+    each sequence's context once; a CTA covers max(1, 8 NT / G) queries (NT =
+    2 n-tiles once a sequence has more than 8 query-head pairs), so the
+    kernel reads a context ceil(q_len / that) times: once for 4 queries at
+    G = 4."""
     import torch
 
     from paged_kv_decode_08_gb300 import pagedkv as pk
@@ -379,7 +385,7 @@ def run_varlen(args):
     world, rank, local = dist_setup()
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
-    v = W.spec_verify()
+    v = W.spec_verify_long() if args.workload == "spec_long" else W.spec_verify()
     w = v.base
     sets = build_sets(w, dev, args.sets)
     q = torch.from_numpy(v.q).to(dev)
@@ -387,11 +393,16 @@ def run_varlen(args):
     pos = torch.from_numpy(v.pos_offsets).to(dev)
     out = torch.empty_like(q)
     n_sets = args.sets
+    S = pk.varlen_splits_for(q, sets[0]["k_cache"], sets[0]["block_tables"], w.num_kv_heads,
+                             v.max_q_len, args.splits)
+    n = pk.pkv_splitk_scratch_bytes(v.total_q, w.num_heads, w.head_dim, S) if S > 1 else 0
+    scratch = torch.empty(max(n, 16), dtype=torch.uint8, device=dev)
 
     def call(i):
         st = sets[i % n_sets]
-        pk.pkv_varlen_attention(q, st["k_cache"], st["v_cache"], cu, pos, st["block_tables"],
-                                w.scale, max_q_len=v.max_q_len, out=out)
+        pk.pkv_varlen_attention_splitk(q, st["k_cache"], st["v_cache"], cu, pos,
+                                       st["block_tables"], w.scale, max_q_len=v.max_q_len,
+                                       num_splits=args.splits, scratch=scratch, out=out)
 
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
@@ -420,7 +431,8 @@ def run_varlen(args):
         return
     kv_bytes = w.kv_bytes
     G = w.group
-    reads = -(-int(v.max_q_len) // max(1, 8 // G))
+    nt = 2 if v.max_q_len * G > 8 else 1
+    reads = -(-int(v.max_q_len) // max(1, 8 * nt // G))
     peak, peak_kind = measured_peaks()
     achieved = kv_bytes / (ms * 1e-3) / 1e9
     line = {
@@ -428,16 +440,18 @@ def run_varlen(args):
         "n_gpus": world, "steps": rounds * n_sets, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD_DESC["spec"], "launch": "CUDA graph, replayed",
-                   "context_reads_per_call": reads,
+        "config": {"workload": WORKLOAD_DESC[args.workload], "launch": "CUDA graph, replayed",
+                   "num_splits": S, "context_reads_per_call": reads,
                    "l2": f"{n_sets} rotating pool sets; {reads * kv_bytes / 1e6:.0f} MB read per call"},
         "kv_bytes_per_step": kv_bytes, "us_per_step": ms * 1e3,
         "query_tokens_per_s": world * v.total_q / (ms * 1e-3),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_kind,
-                     "kernel": "paged_varlen_kernel (algorithmic bytes: each context once)",
+                     "kernel": ("paged_varlen_kernel" + (" split-K phase 1 + varlen_combine_kernel"
+                                                         if S > 1 else "")
+                                + " (algorithmic bytes: each context once)"),
                      "bytes_read_frac": reads * achieved / peak, "traffic": None},
-        "clocks": clocks.summary(), "gpu_launches": rounds * n_sets,
+        "clocks": clocks.summary(), "gpu_launches": rounds * n_sets * (2 if S > 1 else 1),
         "device_status_flags": pk.pkv_read_device_status(), "e2e": None, "cpu_baseline": None,
     }
     print(json.dumps(line), flush=True)
@@ -690,7 +704,7 @@ def main():
     if args.impl == "ours" and args.workload == "loop":
         run_loop(args)
         return
-    if args.impl == "ours" and args.workload == "spec":
+    if args.impl == "ours" and args.workload in ("spec", "spec_long"):
         run_varlen(args)
         return
     if args.impl == "reference":

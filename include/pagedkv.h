@@ -287,6 +287,60 @@ pkv_status pkv_varlen_attention_vllm_layout(
     void* stream);
 
 /*
+ * pkv_varlen_attention_splitk — pkv_varlen_attention with each chunk of
+ * queries' context split over CTAs and merged by a log-sum-exp combine
+ * (ferrum-kernels src/backend/cuda/paged.rs, paged_varlen_split_k_dispatch:
+ * phase 1 per (query token, head, split) writes f32 partial out / max / sum,
+ * a reduce per (query token, head) merges them).  The same result as
+ * pkv_varlen_attention within rounding; it pays off when few sequences have
+ * long contexts.
+ *
+ *   num_splits    0 = pick: when the unsplit grid (num_seqs x num_kv_heads x
+ *                 query chunks) is under one wave of resident CTAs, the
+ *                 split count that brings it nearest one wave, capped so a
+ *                 split keeps >= 256 tokens of max_blocks_per_seq *
+ *                 block_size, at most 64; else 1.  1 = no split (no scratch
+ *                 needed); 2..PKV_MAX_SPLITS = chunks of
+ *                 ceil(max_blocks_per_seq / num_splits) blocks.
+ *   scratch       device memory of at least
+ *                 pkv_splitk_scratch_bytes(total_q, num_heads, head_dim, S)
+ *                 bytes (total_q in the num_seqs slot), 16-byte aligned,
+ *                 caller-owned, no initialisation needed; calls that overlap
+ *                 on the GPU must not share it.
+ *   other arguments, results and flags as pkv_varlen_attention.
+ *
+ * Returns PKV_ERR_SCRATCH_TOO_SMALL when S > 1 and the scratch is null or
+ * smaller than required; PKV_ERR_INVALID_ARG for num_splits outside
+ * 0..PKV_MAX_SPLITS.
+ */
+pkv_status pkv_varlen_attention_splitk(
+    const void* q, const void* k_cache, const void* v_cache, const int32_t* cu_seqlens_q,
+    const int32_t* pos_offsets, const int32_t* block_tables, int32_t num_seqs, int32_t total_q,
+    int32_t max_q_len, int32_t max_blocks_per_seq, int32_t num_blocks, float scale,
+    int32_t num_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size, void* out,
+    int32_t num_splits, void* scratch, size_t scratch_bytes, void* stream);
+
+/*
+ * pkv_varlen_pick_num_splits — the split count pkv_varlen_attention_splitk
+ * uses for num_splits = 0 (host arithmetic only; num_sms is the GPU's SM
+ * count).  Returns 1 for invalid arguments.
+ */
+int32_t pkv_varlen_pick_num_splits(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                                   int32_t max_q_len, int32_t max_blocks_per_seq,
+                                   int32_t block_size, int32_t num_sms);
+
+/*
+ * pkv_varlen_attention_splitk_vllm_layout — pkv_varlen_attention_splitk over
+ * vLLM-layout pools.
+ */
+pkv_status pkv_varlen_attention_splitk_vllm_layout(
+    const void* q, const void* k_cache, const void* v_cache, const int32_t* cu_seqlens_q,
+    const int32_t* pos_offsets, const int32_t* block_tables, int32_t num_seqs, int32_t total_q,
+    int32_t max_q_len, int32_t max_blocks_per_seq, int32_t num_blocks, float scale,
+    int32_t num_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size, void* out,
+    int32_t num_splits, void* scratch, size_t scratch_bytes, void* stream);
+
+/*
  * pkv_splitk_scratch_bytes — bytes of scratch pkv_decode_splitk needs for S
  * splits: f32 partial outputs [num_seqs][num_heads][S][head_dim] followed by
  * f32 running max and running sum [num_seqs][num_heads][S] each (every part

@@ -12,5 +12,6 @@ from .paged_attention import (  # noqa: F401
     kv_head_of,
     softmax,
     varlen,
+    varlen_fast,
     varlen_vllm_layout,
 )

@@ -198,6 +198,44 @@ def varlen(q, k_cache, v_cache, cu_seqlens_q, pos_offsets, block_tables, scale):
     return out
 
 
+def varlen_fast(q, k_cache, v_cache, cu_seqlens_q, pos_offsets, block_tables, scale):
+    """Same definition as :func:`varlen`, gathering each (sequence, KV head)
+    once up to its last query's position and scoring the group's query heads
+    together, one query at a time over its own causal prefix.  Used where the
+    contexts are long; the arithmetic per output element is the same sums in
+    float64."""
+    q = np.asarray(q)
+    total_q, H, D = q.shape
+    NB, Hkv, bs, _ = k_cache.shape
+    if H % Hkv:
+        raise OracleInputError("num_heads must be a multiple of num_kv_heads")
+    group = H // Hkv
+    cu = np.asarray(cu_seqlens_q).astype(np.int64)
+    B = len(cu) - 1
+    if cu[0] != 0 or np.any(np.diff(cu) < 0) or cu[-1] != total_q:
+        raise OracleInputError("cu_seqlens_q must rise from 0 to total_q")
+    if np.any(np.asarray(pos_offsets) < 0):
+        raise OracleInputError("negative pos_offset")
+    lens = np.array([int(pos_offsets[s]) + int(cu[s + 1] - cu[s]) for s in range(B)])
+    _check_tables(block_tables, lens, NB, bs)
+    out = np.zeros((total_q, H, D), np.float64)
+    for s in range(B):
+        n = int(cu[s + 1] - cu[s])
+        if n == 0:
+            continue
+        row = block_tables[s]
+        for g in range(Hkv):
+            K = gather_rows(k_cache, row, int(lens[s]), g)
+            V = gather_rows(v_cache, row, int(lens[s]), g)
+            heads = [h for h in range(H) if kv_head_of(h, group) == g]
+            for t in range(n):
+                L = int(pos_offsets[s]) + t + 1
+                i = int(cu[s]) + t
+                Z = scale * (q[i, heads].astype(np.float64) @ K[:L].T)
+                out[i, heads] = softmax(Z) @ V[:L]
+    return out
+
+
 def append(k, v, slot_mapping, k_cache, v_cache):
     """Scatter new K/V rows into the pools in place; returns the skipped
     out-of-range token indices (slots ``>= num_blocks * block_size``)."""

@@ -5,9 +5,11 @@
 //                                 optionally with the step's append fused in;
 //                                 blocked or vLLM-layout pools
 //   splitk_combine_kernel         log-sum-exp merge of split-K partials
+//   varlen_combine_kernel         the same for varlen split-K partials
 //   paged_varlen_kernel           several causal queries per sequence (one or
 //                                 two mma n-tiles of 8 query-head columns);
-//                                 blocked or vLLM-layout pools
+//                                 single pass or split-K phase 1; blocked or
+//                                 vLLM-layout pools
 //   paged_decode_balanced_kernel  decode over equal tile ranges per CTA
 //   balanced_combine_kernel       merge of the balanced schedule's records
 //
@@ -759,12 +761,19 @@ struct VarlenParams {
   int num_seqs;
   int fair_depth;  // the grid is resident at once: scale in-flight depth
   const __half* k_pool;  // the K pool (vLLM layout: tiles are bulk-copied from it)
+  // split-K (SPLIT kernels): chunk_blocks blocks of context per split; f32
+  // partials per (query token, head, split)
+  float* part_out;  // [total_q][H][S][D]
+  float* part_m;    // [total_q][H][S]  base-2 running max
+  float* part_l;    // [total_q][H][S]  running sum
+  int num_splits;
+  int chunk_blocks;
   int max_blocks_per_seq;
   int num_blocks;
   float scale_log2;
 };
 
-template <int D, int BS, int W, int P, int NT, bool VLLM>
+template <int D, int BS, int W, int P, int NT, bool VLLM, bool SPLIT>
 __global__ void __launch_bounds__(W * 32)
 paged_varlen_kernel(const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap, const VarlenParams p) {
@@ -786,6 +795,8 @@ paged_varlen_kernel(const __grid_constant__ CUtensorMap kmap,
   const int r = lane >> 2, c = lane & 3;
 
   int item = blockIdx.x;
+  const int split = SPLIT ? item % p.num_splits : 0;
+  if (SPLIT) item /= p.num_splits;
   const int qc_idx = item % p.num_chunks;
   item /= p.num_chunks;
   const int g = item % p.num_kv_heads;
@@ -815,7 +826,9 @@ paged_varlen_kernel(const __grid_constant__ CUtensorMap kmap,
       int last = __ldg(p.pos_offsets + i) + __ldg(p.cu_seqlens_q + i + 1) -
                  __ldg(p.cu_seqlens_q + i);
       last = last < 0 ? 0 : (last > cap ? cap : last);
-      mx = max(mx, (last + BS - 1) / BS);
+      int ni = (last + BS - 1) / BS;
+      if (SPLIT && ni > p.chunk_blocks) ni = p.chunk_blocks;
+      mx = max(mx, ni);
     }
   }
   if (__syncthreads_or(status & kDevWaitTimeout)) return;
@@ -835,8 +848,18 @@ paged_varlen_kernel(const __grid_constant__ CUtensorMap kmap,
     if (threadIdx.x == 0) atomicOr(&g_device_status, kDevBadContextLen);
     pos0 = pos0 < 0 ? 0 : max(0, cap - q_len);
   }
-  const int tok_end = min(cap, pos0 + t0 + nq);  // positions this chunk reads
-  const int n_tiles = (tok_end + BS - 1) / BS;
+  // positions this chunk of queries reads; with SPLIT, this CTA's slice of
+  // them (a split starting at or past the end is never written nor read)
+  const int chunk_end = min(cap, pos0 + t0 + nq);
+  int tok_begin = 0;
+  int tok_end = chunk_end;
+  if (SPLIT) {
+    tok_begin = split * p.chunk_blocks * BS;
+    if (tok_begin >= chunk_end) return;
+    tok_end = min(chunk_end, tok_begin + p.chunk_blocks * BS);
+  }
+  const int blk_begin = tok_begin / BS;
+  const int n_tiles = (tok_end - tok_begin + BS - 1) / BS;
   const int32_t* table = p.block_tables + (size_t)s * p.max_blocks_per_seq;
   int WE = W;  // warps that take tiles (fewer for short chunks under the fair share)
   if (p.fair_depth) {
@@ -855,7 +878,7 @@ paged_varlen_kernel(const __grid_constant__ CUtensorMap kmap,
   auto k_stage = [&](int stage) { return ring + (warp * P + stage) * Shape::kStageBytes; };
   auto issue = [&](int li) {
     const int stage = li % P;
-    const int j = warp + li * WE;
+    const int j = blk_begin + warp + li * WE;
     const int phys = __ldg(table + j);
     const uint32_t bar = my_bars + 8 * stage;
     if (phys >= 0 && phys < p.num_blocks) {
@@ -903,7 +926,7 @@ paged_varlen_kernel(const __grid_constant__ CUtensorMap kmap,
       failed = true;
       break;
     }
-    const int j = warp + li * WE;
+    const int j = blk_begin + warp + li * WE;
     const int phys = __ldg(table + j);
     if (phys >= 0 && phys < p.num_blocks) {
       const uint32_t kb = k_stage(stage);
@@ -939,7 +962,16 @@ paged_varlen_kernel(const __grid_constant__ CUtensorMap kmap,
     merge_warps<W, D>(red + (n / 8) * Shape::kRedFloats, NT * Shape::kRedFloats, n % 8, d, M,
                       num, den);
     const size_t row = (size_t)(q_begin + t0 + n / G) * p.num_heads + (size_t)g * G + n % G;
-    p.out[row * D + d] = __float2half_rn(den > 0.f ? num / den : 0.f);
+    if (SPLIT) {
+      const size_t slot = row * p.num_splits + split;
+      p.part_out[slot * D + d] = num;
+      if (d == 0) {
+        p.part_m[slot] = M;
+        p.part_l[slot] = den;
+      }
+    } else {
+      p.out[row * D + d] = __float2half_rn(den > 0.f ? num / den : 0.f);
+    }
   }
 }
 
@@ -1441,28 +1473,19 @@ struct CombineParams {
   int cap_tokens;  // max_blocks_per_seq * block_size
 };
 
-// One CTA per (sequence, query head), 128 threads.  Splits whose first token
-// is at or past the context length were never written and are not read.
-// Thread k loads split k's max and sum (all splits at once), the CTA reduces
-// them, and thread d then sums the splits' partial outputs with independent
-// loads.
-__global__ void __launch_bounds__(128) splitk_combine_kernel(const CombineParams p) {
-  constexpr int NT = 128;
-  static_assert(PKV_MAX_SPLITS <= NT, "one thread per split");
-  __shared__ float s_w[PKV_MAX_SPLITS];
-  __shared__ float s_red[NT / 32];
-  pdl_launch_dependents();
-  pdl_wait();
-  const int sh = blockIdx.x;
-  const int s = sh / p.num_heads;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int L = __ldg(p.context_lens + s);
-  L = L < 0 ? 0 : (L > p.cap_tokens ? p.cap_tokens : L);
-  const int n_valid = min(p.num_splits, (L + p.chunk_tokens - 1) / p.chunk_tokens);
-  const float* pm = p.part_m + (size_t)sh * p.num_splits;
-  const float* pl = p.part_l + (size_t)sh * p.num_splits;
-  const float* po = p.part_out + (size_t)sh * p.num_splits * p.head_dim;
+// The merge of one output row from its split partials, by a CTA of
+// kCombineThreads threads: thread k loads split k's max and sum (all splits
+// at once), the CTA reduces them, and thread d then sums the splits' partial
+// outputs with independent loads.  Only the first n_valid splits are read
+// (the others were never written).
+constexpr int kCombineThreads = 128;
 
+__device__ __forceinline__ void combine_row(const float* pm, const float* pl, const float* po,
+                                            int n_valid, int head_dim, __half* out_row,
+                                            float* s_w, float* s_red) {
+  constexpr int NT = kCombineThreads;
+  static_assert(PKV_MAX_SPLITS <= NT, "one thread per split");
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int k = threadIdx.x;  // num_splits <= PKV_MAX_SPLITS = NT
   const float mk = k < n_valid ? __ldg(pm + k) : -CUDART_INF_F;
   const float lk = k < n_valid ? __ldg(pl + k) : 0.f;
@@ -1482,19 +1505,94 @@ __global__ void __launch_bounds__(128) splitk_combine_kernel(const CombineParams
   __syncthreads();
   den = s_red[0] + s_red[1] + s_red[2] + s_red[3];
 
-  for (int d = threadIdx.x; d < p.head_dim; d += NT) {
+  for (int d = threadIdx.x; d < head_dim; d += NT) {
     float num = 0.f;
     int kk = 0;
     for (; kk + 4 <= n_valid; kk += 4) {
-      const float a0 = __ldg(po + (size_t)kk * p.head_dim + d);
-      const float a1 = __ldg(po + (size_t)(kk + 1) * p.head_dim + d);
-      const float a2 = __ldg(po + (size_t)(kk + 2) * p.head_dim + d);
-      const float a3 = __ldg(po + (size_t)(kk + 3) * p.head_dim + d);
+      const float a0 = __ldg(po + (size_t)kk * head_dim + d);
+      const float a1 = __ldg(po + (size_t)(kk + 1) * head_dim + d);
+      const float a2 = __ldg(po + (size_t)(kk + 2) * head_dim + d);
+      const float a3 = __ldg(po + (size_t)(kk + 3) * head_dim + d);
       num += s_w[kk] * a0 + s_w[kk + 1] * a1 + s_w[kk + 2] * a2 + s_w[kk + 3] * a3;
     }
-    for (; kk < n_valid; ++kk) num += s_w[kk] * __ldg(po + (size_t)kk * p.head_dim + d);
-    p.out[(size_t)sh * p.head_dim + d] = __float2half_rn(den > 0.f ? num / den : 0.f);
+    for (; kk < n_valid; ++kk) num += s_w[kk] * __ldg(po + (size_t)kk * head_dim + d);
+    out_row[d] = __float2half_rn(den > 0.f ? num / den : 0.f);
   }
+}
+
+// Decode split-K: one CTA per (sequence, query head).  A split is valid when
+// its first token is before the context length.
+__global__ void __launch_bounds__(kCombineThreads) splitk_combine_kernel(const CombineParams p) {
+  __shared__ float s_w[PKV_MAX_SPLITS];
+  __shared__ float s_red[kCombineThreads / 32];
+  pdl_launch_dependents();
+  pdl_wait();
+  const int sh = blockIdx.x;
+  const int s = sh / p.num_heads;
+  int L = __ldg(p.context_lens + s);
+  L = L < 0 ? 0 : (L > p.cap_tokens ? p.cap_tokens : L);
+  const int n_valid = min(p.num_splits, (L + p.chunk_tokens - 1) / p.chunk_tokens);
+  combine_row(p.part_m + (size_t)sh * p.num_splits, p.part_l + (size_t)sh * p.num_splits,
+              p.part_out + (size_t)sh * p.num_splits * p.head_dim, n_valid, p.head_dim,
+              p.out + (size_t)sh * p.head_dim, s_w, s_red);
+}
+
+// Varlen split-K: one CTA per (query token, head).  The token's sequence is
+// found by binary search in cu_seqlens_q; the query at position pos sees
+// positions 0..pos, so splits starting at or before pos are valid (the
+// phase-1 CTA of its chunk of queries wrote every one of them).  Positions
+// are clamped as phase 1 clamps them; rows phase 1 skipped (bad query
+// ranges, queries past the grid; both flagged there) are written as zeros.
+struct VarlenCombineParams {
+  const float* part_out;
+  const float* part_m;
+  const float* part_l;
+  const int32_t* cu_seqlens_q;
+  const int32_t* pos_offsets;
+  __half* out;
+  int num_seqs;
+  int total_q;
+  int num_heads;
+  int head_dim;
+  int num_splits;
+  int chunk_tokens;
+  int cap_tokens;
+  int covered_q;  // queries per sequence the phase-1 grid covers
+};
+
+__global__ void __launch_bounds__(kCombineThreads)
+varlen_combine_kernel(const VarlenCombineParams p) {
+  __shared__ float s_w[PKV_MAX_SPLITS];
+  __shared__ float s_red[kCombineThreads / 32];
+  pdl_launch_dependents();
+  pdl_wait();
+  const int rh = blockIdx.x;  // row * H + head
+  const int row = rh / p.num_heads;
+  int lo = 0, hi = p.num_seqs - 1;  // last sequence whose first row is <= row
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(p.cu_seqlens_q + mid) <= row)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  const int q_begin = __ldg(p.cu_seqlens_q + lo);
+  const int q_end = __ldg(p.cu_seqlens_q + lo + 1);
+  const int t = row - q_begin;
+  __half* out_row = p.out + (size_t)rh * p.head_dim;
+  if (q_begin < 0 || q_end < q_begin || q_end > p.total_q || t < 0 || t >= q_end - q_begin ||
+      t >= p.covered_q) {
+    for (int d = threadIdx.x; d < p.head_dim; d += kCombineThreads) out_row[d] = __float2half_rn(0.f);
+    return;
+  }
+  const int q_len = q_end - q_begin;
+  int pos0 = __ldg(p.pos_offsets + lo);
+  if (pos0 < 0 || pos0 + q_len > p.cap_tokens) pos0 = pos0 < 0 ? 0 : max(0, p.cap_tokens - q_len);
+  const int L = min(p.cap_tokens, pos0 + t + 1);
+  const int n_valid = min(p.num_splits, (L + p.chunk_tokens - 1) / p.chunk_tokens);
+  combine_row(p.part_m + (size_t)rh * p.num_splits, p.part_l + (size_t)rh * p.num_splits,
+              p.part_out + (size_t)rh * p.num_splits * p.head_dim, n_valid, p.head_dim, out_row,
+              s_w, s_red);
 }
 
 }  // namespace pkv

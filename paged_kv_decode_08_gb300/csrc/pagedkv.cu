@@ -382,13 +382,13 @@ DecodeParams base_params(const DecodeArgs& a) {
   return p;
 }
 
-template <int D, int BS, int NT, bool VLLM>
+template <int D, int BS, int NT, bool VLLM, bool SPLIT>
 pkv_status launch_varlen(const DecodeArgs& a, const VarlenParams& vp, cudaStream_t stream,
                          int grid) {
   constexpr int W = Tuning<D, BS>::W;
   constexpr int P = Tuning<D, BS>::P;
   using Shape = DecodeShape<D, BS, W, P>;
-  auto kernel = paged_varlen_kernel<D, BS, W, P, NT, VLLM>;
+  auto kernel = paged_varlen_kernel<D, BS, W, P, NT, VLLM, SPLIT>;
   static std::atomic<unsigned long long> attr_set{0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -419,6 +419,25 @@ pkv_status launch_varlen(const DecodeArgs& a, const VarlenParams& vp, cudaStream
   e = launch_pdl(kernel, grid, W * 32, Shape::kSmemBytes, stream, kmap, vmap, vp2);
   if (e != cudaSuccess) return cuda_fail(e, "varlen attention launch");
   return PKV_OK;
+}
+
+template <bool SPLIT>
+pkv_status dispatch_varlen(const DecodeArgs& a, const VarlenParams& vp, cudaStream_t cs, int grid,
+                           int NT, bool vllm) {
+#define PKV_VARLEN_CASE(D_, BS_)                                                              \
+  if (a.head_dim == D_ && a.block_size == BS_) {                                              \
+    if (NT == 2)                                                                              \
+      return vllm ? launch_varlen<D_, BS_, 2, true, SPLIT>(a, vp, cs, grid)                   \
+                  : launch_varlen<D_, BS_, 2, false, SPLIT>(a, vp, cs, grid);                 \
+    return vllm ? launch_varlen<D_, BS_, 1, true, SPLIT>(a, vp, cs, grid)                     \
+                : launch_varlen<D_, BS_, 1, false, SPLIT>(a, vp, cs, grid);                   \
+  }
+  PKV_VARLEN_CASE(128, 16)
+  PKV_VARLEN_CASE(128, 32)
+  PKV_VARLEN_CASE(64, 16)
+  PKV_VARLEN_CASE(64, 32)
+#undef PKV_VARLEN_CASE
+  return fail(PKV_ERR_UNSUPPORTED, "head_dim %d / block_size %d", a.head_dim, a.block_size);
 }
 
 // The fused append of pkv_append_decode (all null: none).
@@ -539,6 +558,26 @@ int32_t pkv_pick_num_splits(int32_t num_seqs, int32_t num_kv_heads, int32_t max_
   return (int32_t)s;
 }
 
+int32_t pkv_varlen_pick_num_splits(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                                   int32_t max_q_len, int32_t max_blocks_per_seq,
+                                   int32_t block_size, int32_t num_sms) {
+  if (num_seqs <= 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0 ||
+      max_q_len <= 0 || max_blocks_per_seq <= 0 || block_size <= 0 || num_sms <= 0)
+    return 1;
+  const int G = num_heads / num_kv_heads;
+  const int nt = (long long)max_q_len * G > 8 ? 2 : 1;
+  const int qc = G >= 8 * nt ? 1 : 8 * nt / G;
+  const long long grid = (long long)num_seqs * num_kv_heads * ((max_q_len + qc - 1) / qc);
+  const long long slots = (long long)num_sms * kCtasPerSm;
+  // below one wave, the split count that brings the grid nearest one wave
+  long long s = grid >= slots ? 1 : (2 * slots + grid) / (2 * grid);
+  const long long cap_tokens = (long long)max_blocks_per_seq * block_size;
+  if (s > cap_tokens / kMinSplitTokens) s = cap_tokens / kMinSplitTokens;
+  if (s > max_blocks_per_seq) s = max_blocks_per_seq;
+  if (s > kMaxAutoSplits) s = kMaxAutoSplits;
+  return s < 1 ? 1 : (int32_t)s;
+}
+
 pkv_status pkv_append(const void* k, const void* v, const int32_t* slot_mapping,
                       int32_t num_tokens, void* k_cache, void* v_cache, int32_t num_blocks,
                       int32_t block_size, int32_t num_kv_heads, int32_t head_dim, void* stream) {
@@ -651,7 +690,8 @@ pkv_status varlen_impl(const void* q, const void* k_cache, const void* v_cache,
                        const int32_t* block_tables, int num_seqs, int total_q, int max_q_len,
                        int max_blocks_per_seq, int num_blocks, float scale, int num_heads,
                        int num_kv_heads, int head_dim, int block_size, void* out,
-                       cudaStream_t cs, bool vllm) {
+                       int num_splits, void* scratch, size_t scratch_bytes, cudaStream_t cs,
+                       bool vllm) {
   // pos_offsets stands in for context_lens in the shared checks
   const DecodeArgs a{q, k_cache, v_cache, block_tables, pos_offsets, num_seqs,
                      max_blocks_per_seq, num_blocks, scale, num_heads, num_kv_heads,
@@ -661,6 +701,8 @@ pkv_status varlen_impl(const void* q, const void* k_cache, const void* v_cache,
   if (!cu_seqlens_q || !aligned(cu_seqlens_q, 4))
     return fail(PKV_ERR_INVALID_ARG, "cu_seqlens_q must be a 4-byte aligned device pointer");
   if (total_q < 0 || max_q_len < 0) return fail(PKV_ERR_INVALID_ARG, "total_q / max_q_len < 0");
+  if (num_splits < 0 || num_splits > PKV_MAX_SPLITS)
+    return fail(PKV_ERR_INVALID_ARG, "num_splits %d outside 0..%d", num_splits, PKV_MAX_SPLITS);
   if (num_seqs == 0 || total_q == 0 || max_q_len == 0) return PKV_OK;
   const int G = num_heads / num_kv_heads;
   // two n-tiles (16 columns) once a sequence has more than 8 (query, head)
@@ -686,26 +728,58 @@ pkv_status varlen_impl(const void* q, const void* k_cache, const void* v_cache,
   vp.max_blocks_per_seq = max_blocks_per_seq;
   vp.num_blocks = num_blocks;
   vp.scale_log2 = scale * 1.4426950408889634f;
-  if (NT == 2) {
-    if (head_dim == 128 && block_size == 16) return vllm ? launch_varlen<128, 16, 2, true>(a, vp, cs, (int)grid)
-                : launch_varlen<128, 16, 2, false>(a, vp, cs, (int)grid);
-    if (head_dim == 128 && block_size == 32) return vllm ? launch_varlen<128, 32, 2, true>(a, vp, cs, (int)grid)
-                : launch_varlen<128, 32, 2, false>(a, vp, cs, (int)grid);
-    if (head_dim == 64 && block_size == 16) return vllm ? launch_varlen<64, 16, 2, true>(a, vp, cs, (int)grid)
-                : launch_varlen<64, 16, 2, false>(a, vp, cs, (int)grid);
-    if (head_dim == 64 && block_size == 32) return vllm ? launch_varlen<64, 32, 2, true>(a, vp, cs, (int)grid)
-                : launch_varlen<64, 32, 2, false>(a, vp, cs, (int)grid);
-  } else {
-    if (head_dim == 128 && block_size == 16) return vllm ? launch_varlen<128, 16, 1, true>(a, vp, cs, (int)grid)
-                : launch_varlen<128, 16, 1, false>(a, vp, cs, (int)grid);
-    if (head_dim == 128 && block_size == 32) return vllm ? launch_varlen<128, 32, 1, true>(a, vp, cs, (int)grid)
-                : launch_varlen<128, 32, 1, false>(a, vp, cs, (int)grid);
-    if (head_dim == 64 && block_size == 16) return vllm ? launch_varlen<64, 16, 1, true>(a, vp, cs, (int)grid)
-                : launch_varlen<64, 16, 1, false>(a, vp, cs, (int)grid);
-    if (head_dim == 64 && block_size == 32) return vllm ? launch_varlen<64, 32, 1, true>(a, vp, cs, (int)grid)
-                : launch_varlen<64, 32, 1, false>(a, vp, cs, (int)grid);
+  vp.num_splits = 1;
+  vp.chunk_blocks = max_blocks_per_seq;
+
+  int S = num_splits;
+  if (S == 0) {
+    int sms = 0;
+    if (current_device_sms(&sms) != 0) return fail(PKV_ERR_CUDA, "cannot query the SM count");
+    S = pkv_varlen_pick_num_splits(num_seqs, num_heads, num_kv_heads, max_q_len,
+                                   max_blocks_per_seq, block_size, sms);
   }
-  return fail(PKV_ERR_UNSUPPORTED, "head_dim %d / block_size %d", head_dim, block_size);
+  const int chunk_blocks = (max_blocks_per_seq + S - 1) / S;
+  const int S_eff = (max_blocks_per_seq + chunk_blocks - 1) / chunk_blocks;
+  if (S_eff <= 1) return dispatch_varlen<false>(a, vp, cs, (int)grid, NT, vllm);
+
+  const size_t need = pkv_splitk_scratch_bytes(total_q, num_heads, head_dim, S_eff);
+  if (!scratch || scratch_bytes < need)
+    return fail(PKV_ERR_SCRATCH_TOO_SMALL, "varlen split-K with %d splits needs %zu scratch bytes, got %zu",
+                S_eff, need, scratch ? scratch_bytes : (size_t)0);
+  if (!aligned(scratch, 16)) return fail(PKV_ERR_INVALID_ARG, "scratch must be 16-byte aligned");
+  const long long grid1 = grid * S_eff;
+  const long long grid2 = (long long)total_q * num_heads;
+  if (grid1 >= (1ll << 31) || grid2 >= (1ll << 31))
+    return fail(PKV_ERR_INVALID_ARG, "grid too large");
+  const size_t rows = (size_t)total_q * num_heads * S_eff;
+  uint8_t* base = static_cast<uint8_t*>(scratch);
+  vp.num_splits = S_eff;
+  vp.chunk_blocks = chunk_blocks;
+  vp.part_out = reinterpret_cast<float*>(base);
+  vp.part_m = reinterpret_cast<float*>(base + align256(rows * head_dim * sizeof(float)));
+  vp.part_l = reinterpret_cast<float*>(base + align256(rows * head_dim * sizeof(float)) +
+                                      align256(rows * sizeof(float)));
+  st = dispatch_varlen<true>(a, vp, cs, (int)grid1, NT, vllm);
+  if (st != PKV_OK) return st;
+
+  VarlenCombineParams cp{};
+  cp.part_out = vp.part_out;
+  cp.part_m = vp.part_m;
+  cp.part_l = vp.part_l;
+  cp.cu_seqlens_q = cu_seqlens_q;
+  cp.pos_offsets = pos_offsets;
+  cp.out = static_cast<__half*>(out);
+  cp.num_seqs = num_seqs;
+  cp.total_q = total_q;
+  cp.num_heads = num_heads;
+  cp.head_dim = head_dim;
+  cp.num_splits = S_eff;
+  cp.chunk_tokens = chunk_blocks * block_size;
+  cp.cap_tokens = max_blocks_per_seq * block_size;
+  cp.covered_q = chunks * qc;
+  const cudaError_t e = launch_pdl(varlen_combine_kernel, (int)grid2, kCombineThreads, 0, cs, cp);
+  if (e != cudaSuccess) return cuda_fail(e, "varlen split-K combine launch");
+  return PKV_OK;
 }
 
 }  // namespace
@@ -782,8 +856,8 @@ pkv_status pkv_varlen_attention(const void* q, const void* k_cache, const void* 
                                 void* out, void* stream) {
   return varlen_impl(q, k_cache, v_cache, cu_seqlens_q, pos_offsets, block_tables, num_seqs,
                      total_q, max_q_len, max_blocks_per_seq, num_blocks, scale, num_heads,
-                     num_kv_heads, head_dim, block_size, out, static_cast<cudaStream_t>(stream),
-                     false);
+                     num_kv_heads, head_dim, block_size, out, 1, nullptr, 0,
+                     static_cast<cudaStream_t>(stream), false);
 }
 
 pkv_status pkv_varlen_attention_vllm_layout(
@@ -794,8 +868,32 @@ pkv_status pkv_varlen_attention_vllm_layout(
     void* stream) {
   return varlen_impl(q, k_cache, v_cache, cu_seqlens_q, pos_offsets, block_tables, num_seqs,
                      total_q, max_q_len, max_blocks_per_seq, num_blocks, scale, num_heads,
-                     num_kv_heads, head_dim, block_size, out, static_cast<cudaStream_t>(stream),
-                     true);
+                     num_kv_heads, head_dim, block_size, out, 1, nullptr, 0,
+                     static_cast<cudaStream_t>(stream), true);
+}
+
+pkv_status pkv_varlen_attention_splitk(
+    const void* q, const void* k_cache, const void* v_cache, const int32_t* cu_seqlens_q,
+    const int32_t* pos_offsets, const int32_t* block_tables, int32_t num_seqs, int32_t total_q,
+    int32_t max_q_len, int32_t max_blocks_per_seq, int32_t num_blocks, float scale,
+    int32_t num_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size, void* out,
+    int32_t num_splits, void* scratch, size_t scratch_bytes, void* stream) {
+  return varlen_impl(q, k_cache, v_cache, cu_seqlens_q, pos_offsets, block_tables, num_seqs,
+                     total_q, max_q_len, max_blocks_per_seq, num_blocks, scale, num_heads,
+                     num_kv_heads, head_dim, block_size, out, num_splits, scratch, scratch_bytes,
+                     static_cast<cudaStream_t>(stream), false);
+}
+
+pkv_status pkv_varlen_attention_splitk_vllm_layout(
+    const void* q, const void* k_cache, const void* v_cache, const int32_t* cu_seqlens_q,
+    const int32_t* pos_offsets, const int32_t* block_tables, int32_t num_seqs, int32_t total_q,
+    int32_t max_q_len, int32_t max_blocks_per_seq, int32_t num_blocks, float scale,
+    int32_t num_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size, void* out,
+    int32_t num_splits, void* scratch, size_t scratch_bytes, void* stream) {
+  return varlen_impl(q, k_cache, v_cache, cu_seqlens_q, pos_offsets, block_tables, num_seqs,
+                     total_q, max_q_len, max_blocks_per_seq, num_blocks, scale, num_heads,
+                     num_kv_heads, head_dim, block_size, out, num_splits, scratch, scratch_bytes,
+                     static_cast<cudaStream_t>(stream), true);
 }
 
 pkv_status pkv_read_device_status(int32_t* flags, void* stream) {

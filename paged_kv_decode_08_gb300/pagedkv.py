@@ -63,6 +63,11 @@ def _load():
     lib.pkv_varlen_attention.restype = i32
     lib.pkv_varlen_attention_vllm_layout.argtypes = lib.pkv_varlen_attention.argtypes
     lib.pkv_varlen_attention_vllm_layout.restype = i32
+    split_args = lib.pkv_varlen_attention.argtypes[:-1] + [i32, vp, sz, vp]
+    lib.pkv_varlen_attention_splitk.argtypes = split_args
+    lib.pkv_varlen_attention_splitk.restype = i32
+    lib.pkv_varlen_attention_splitk_vllm_layout.argtypes = split_args
+    lib.pkv_varlen_attention_splitk_vllm_layout.restype = i32
     lib.pkv_decode_splitk_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, f32, i32, i32,
                                               i32, i32, vp, i32, vp]
     lib.pkv_decode_splitk_noalloc.restype = i32
@@ -71,6 +76,8 @@ def _load():
     lib.pkv_decode_vllm_layout.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, f32, i32, i32, i32,
                                            i32, vp, i32, vp, sz, vp]
     lib.pkv_decode_vllm_layout.restype = i32
+    lib.pkv_varlen_pick_num_splits.argtypes = [i32, i32, i32, i32, i32, i32, i32]
+    lib.pkv_varlen_pick_num_splits.restype = i32
     lib.pkv_splitk_scratch_bytes.argtypes = [i32, i32, i32, i32]
     lib.pkv_splitk_scratch_bytes.restype = sz
     lib.pkv_pick_num_splits.argtypes = [i32, i32, i32, i32, i32]
@@ -265,8 +272,48 @@ def pkv_varlen_attention_vllm_layout(q, k_cache, v_cache, cu_seqlens_q, pos_offs
                    max_q_len, out, stream, vllm=True)
 
 
+def pkv_varlen_attention_splitk(q, k_cache, v_cache, cu_seqlens_q, pos_offsets, block_tables,
+                                scale, max_q_len=None, num_splits=0, scratch=None, out=None,
+                                stream=None):
+    """:func:`pkv_varlen_attention` with split-K (``num_splits`` 0 = heuristic).
+    ``scratch`` (uint8) is allocated when not given."""
+    return _varlen(q, k_cache, v_cache, cu_seqlens_q, pos_offsets, block_tables, scale,
+                   max_q_len, out, stream, vllm=False, split=(num_splits, scratch))
+
+
+def pkv_varlen_attention_splitk_vllm_layout(q, k_cache, v_cache, cu_seqlens_q, pos_offsets,
+                                            block_tables, scale, max_q_len=None, num_splits=0,
+                                            scratch=None, out=None, stream=None):
+    """:func:`pkv_varlen_attention_splitk` over vLLM-layout pools."""
+    return _varlen(q, k_cache, v_cache, cu_seqlens_q, pos_offsets, block_tables, scale,
+                   max_q_len, out, stream, vllm=True, split=(num_splits, scratch))
+
+
+def pkv_varlen_pick_num_splits(num_seqs, num_heads, num_kv_heads, max_q_len,
+                               max_blocks_per_seq, block_size, num_sms) -> int:
+    return int(lib.pkv_varlen_pick_num_splits(num_seqs, num_heads, num_kv_heads, max_q_len,
+                                              max_blocks_per_seq, block_size, num_sms))
+
+
+def varlen_splits_for(q, k_cache, block_tables, num_kv_heads, max_q_len, num_splits=0):
+    """The split count the varlen split-K call will use for these tensors."""
+    import torch
+
+    mbps = block_tables.shape[1]
+    if num_splits:
+        S = int(num_splits)
+    else:
+        sms = torch.cuda.get_device_properties(q.device).multi_processor_count
+        bs = k_cache.shape[3] if k_cache.dim() == 5 else k_cache.shape[2]
+        S = pkv_varlen_pick_num_splits(block_tables.shape[0], q.shape[1], num_kv_heads,
+                                       max_q_len, mbps, bs, sms)
+    if S > 1:  # the kernel uses ceil(MBPS / ceil(MBPS / S)) <= S splits
+        S = -(-mbps // -(-mbps // S))
+    return S
+
+
 def _varlen(q, k_cache, v_cache, cu_seqlens_q, pos_offsets, block_tables, scale, max_q_len, out,
-            stream, vllm):
+            stream, vllm, split=None):
     import torch
 
     _want(q, "q", torch.float16, 3)
@@ -288,12 +335,25 @@ def _varlen(q, k_cache, v_cache, cu_seqlens_q, pos_offsets, block_tables, scale,
     _want(out, "out", torch.float16, 3, (total_q, H, D))
     if max_q_len is None:
         raise ValueError("max_q_len (a host-side bound) is required")
-    fn = lib.pkv_varlen_attention_vllm_layout if vllm else lib.pkv_varlen_attention
-    _check(fn(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), cu_seqlens_q.data_ptr(),
-              pos_offsets.data_ptr(), block_tables.data_ptr(), B, total_q, int(max_q_len),
-              block_tables.shape[1], NB, float(scale), H, Hkv, D, bs, out.data_ptr(),
-              _stream_ptr(stream)),
-           "pkv_varlen_attention_vllm_layout" if vllm else "pkv_varlen_attention")
+    args = [q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), cu_seqlens_q.data_ptr(),
+            pos_offsets.data_ptr(), block_tables.data_ptr(), B, total_q, int(max_q_len),
+            block_tables.shape[1], NB, float(scale), H, Hkv, D, bs, out.data_ptr()]
+    if split is None:
+        fn = lib.pkv_varlen_attention_vllm_layout if vllm else lib.pkv_varlen_attention
+        name = "pkv_varlen_attention_vllm_layout" if vllm else "pkv_varlen_attention"
+    else:
+        num_splits, scratch = split
+        if scratch is None:
+            S = varlen_splits_for(q, k_cache, block_tables, Hkv, int(max_q_len), num_splits)
+            n = pkv_splitk_scratch_bytes(total_q, H, D, S) if S > 1 else 0
+            scratch = torch.empty(max(n, 16), dtype=torch.uint8, device=q.device)
+        _want(scratch, "scratch", torch.uint8, 1)
+        args += [int(num_splits), scratch.data_ptr(), scratch.numel()]
+        fn = (lib.pkv_varlen_attention_splitk_vllm_layout if vllm
+              else lib.pkv_varlen_attention_splitk)
+        name = ("pkv_varlen_attention_splitk_vllm_layout" if vllm
+                else "pkv_varlen_attention_splitk")
+    _check(fn(*args, _stream_ptr(stream)), name)
     return out
 
 

@@ -501,6 +501,14 @@ def varlen_random(seed: int, num_heads: int, num_kv_heads: int, head_dim: int, b
                           pos_offsets=np.asarray(prefix, np.int32))
 
 
+def spec_verify_long() -> VarlenWorkload:
+    """Speculative-decode verification over long contexts (the long-context
+    decode shape): B=4, H=32, Hkv=8, D=128, bs=16, 4 draft tokens per
+    sequence after prefixes of 32768/65536/98304/131072 - 4 tokens."""
+    prefix = [32768 - 4, 65536 - 4, 98304 - 4, 131072 - 4]
+    return varlen_random(BASE_SEED + 6, 32, 8, 128, 16, [4] * 4, prefix, num_blocks=24576)
+
+
 def spec_verify() -> VarlenWorkload:
     """Speculative-decode verification on the Llama-3-8B attention shape:
     B=32, H=32, Hkv=8, D=128, bs=16, 4 draft tokens per sequence over a

@@ -34,7 +34,8 @@ def test_header_declares_the_expected_calls():
               "pkv_varlen_attention", "pkv_splitk_scratch_bytes",
               "pkv_pick_num_splits", "pkv_status_string", "pkv_last_error",
               "pkv_read_device_status", "pkv_append_vllm_layout", "pkv_decode_vllm_layout",
-              "pkv_varlen_attention_vllm_layout"]:
+              "pkv_varlen_attention_vllm_layout", "pkv_varlen_attention_splitk",
+              "pkv_varlen_attention_splitk_vllm_layout", "pkv_varlen_pick_num_splits"]:
         assert n in names
 
 
@@ -224,3 +225,27 @@ def test_vllm_varlen_rejects_bad_arguments(pk):
     bad_bs = list(ok)
     bad_bs[15] = 24
     assert f(*bad_bs) == -2
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((32, 32, 8, 4, 128, 16, 152), 1),      # speculative verification: one wave already
+    ((4, 32, 8, 4, 8192, 16, 152), 10),     # long contexts: 32 CTAs -> nearest one wave
+    ((1, 8, 8, 1, 4, 16, 152), 1),          # 64 tokens of capacity: a split keeps >= 256
+    ((1, 32, 8, 4, 1 << 20, 16, 152), 38),  # 8 CTAs -> nearest one wave of 304
+    ((1, 32, 8, 4, 1 << 20, 16, 1000), 64), # capped at 64
+    ((0, 32, 8, 4, 128, 16, 152), 1),       # invalid -> 1
+    ((2, 6, 4, 4, 128, 16, 152), 1),        # heads not a multiple of kv heads -> 1
+])
+def test_varlen_pick_num_splits_table(pk, args, expect):
+    assert pk.pkv_varlen_pick_num_splits(*args) == expect
+
+
+def test_varlen_splitk_rejects_bad_arguments(pk):
+    f = pk.lib.pkv_varlen_attention_splitk
+    ok = [F16, F16, F16, F16, F16, F16, 2, 5, 4, 3, 8, 0.125, 4, 2, 64, 16, F16]
+    assert f(*ok, -1, F16, 1 << 30, None) == -1
+    assert f(*ok, 129, F16, 1 << 30, None) == -1
+    assert f(*ok, 4, None, 0, None) == -3         # 3 splits of 1 block need scratch
+    assert f(*(ok[:7] + [0] + ok[8:]), 4, None, 0, None) == 0  # no queries
+    g = pk.lib.pkv_varlen_attention_splitk_vllm_layout
+    assert g(*ok, 4, None, 0, None) == -3

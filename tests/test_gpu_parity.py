@@ -457,3 +457,68 @@ def test_varlen_flags_bad_query_ranges(pk, cuda_device):
                             d["block_tables"], v.base.scale, max_q_len=4, out=out)
     assert pk.pkv_read_device_status() & pk.PKV_DEV_BAD_CONTEXT_LEN
     assert torch.count_nonzero(out[2:]).item() == 0  # sequence 1 skipped
+
+
+# ---------------------------------------------------------------------------
+# varlen split-K (each chunk of queries' context split over CTAs, merged)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("H,Hkv,D,bs,q_lens,prefix", [
+    (8, 8, 64, 16, [1, 9, 0, 17], [0, 15, 3, 40]),
+    (28, 4, 128, 32, [3, 1, 6], [33, 1000, 0]),
+    (8, 4, 128, 32, [4, 1, 3], [64, 200, 1]),
+    (32, 8, 128, 16, [40, 3], [100, 0]),  # early queries see none of the later splits
+])
+def test_varlen_splitk_matches_oracle(pk, cuda_device, H, Hkv, D, bs, q_lens, prefix):
+    v = W.varlen_random(5000 + H + D + bs, H, Hkv, D, bs, q_lens, prefix)
+    kc, vc = W.host_pool(v.base)
+    ref = oracle.varlen(v.q, kc, vc, v.cu_seqlens_q, v.pos_offsets, v.base.block_tables,
+                        v.base.scale)
+    d = varlen_device(v, cuda_device)
+    for S in (0, 2, 3, 7, 128):
+        out = pk.pkv_varlen_attention_splitk(d["q"], d["k_cache"], d["v_cache"], d["cu"],
+                                             d["pos"], d["block_tables"], v.base.scale,
+                                             max_q_len=v.max_q_len, num_splits=S)
+        torch.cuda.synchronize()
+        assert_attention_close(to_np(out), ref, f"varlen split-K S={S} H{H} Hkv{Hkv} D{D} bs{bs}")
+    assert pk.pkv_read_device_status() == 0
+
+
+def test_varlen_splitk_long_context_speculative_verification(pk, cuda_device):
+    """Four draft tokens after 32K..128K-token prefixes: the heuristic splits
+    each context (the unsplit grid is 32 CTAs), and the result matches the
+    oracle; the vLLM-layout call equals the blocked one bit for bit."""
+    v = W.spec_verify_long()
+    kc, vc = W.host_pool(v.base)
+    ref = oracle.varlen_fast(v.q, kc, vc, v.cu_seqlens_q, v.pos_offsets, v.base.block_tables,
+                             v.base.scale)
+    del kc, vc
+    d = varlen_device(v, cuda_device)
+    S = pk.varlen_splits_for(d["q"], d["k_cache"], d["block_tables"], v.base.num_kv_heads, 4)
+    assert S > 1
+    outs = {}
+    for label, S_req in (("heuristic", 0), ("S=16", 16)):
+        outs[label] = pk.pkv_varlen_attention_splitk(d["q"], d["k_cache"], d["v_cache"], d["cu"],
+                                                     d["pos"], d["block_tables"], v.base.scale,
+                                                     max_q_len=4, num_splits=S_req)
+        torch.cuda.synchronize()
+        assert_attention_close(to_np(outs[label]), ref, f"long spec verify {label}")
+    del d["k_cache"], d["v_cache"]
+    dv = W.to_device_vllm(v.base, cuda_device)
+    got_v = pk.pkv_varlen_attention_splitk_vllm_layout(d["q"], dv["k_cache"], dv["v_cache"],
+                                                       d["cu"], d["pos"], d["block_tables"],
+                                                       v.base.scale, max_q_len=4, num_splits=0)
+    torch.cuda.synchronize()
+    assert_bits_equal(got_v.cpu().numpy(), outs["heuristic"].cpu().numpy(), "vLLM vs blocked")
+    assert pk.pkv_read_device_status() == 0
+
+
+def test_varlen_splitk_rejects_small_scratch(pk, cuda_device):
+    v = W.varlen_random(5100, 8, 2, 64, 16, [3, 2], [100, 40])
+    d = varlen_device(v, cuda_device)
+    small = torch.empty(16, dtype=torch.uint8, device=cuda_device)
+    with pytest.raises(pk.PagedKVError) as e:
+        pk.pkv_varlen_attention_splitk(d["q"], d["k_cache"], d["v_cache"], d["cu"], d["pos"],
+                                       d["block_tables"], v.base.scale, max_q_len=3,
+                                       num_splits=4, scratch=small)
+    assert e.value.status == pk.PKV_ERR_SCRATCH_TOO_SMALL

@@ -293,8 +293,8 @@ MUTATIONS = {
     # axis matters there.
     "fast:softmax_over_whole_group": ("e = np.exp(z - z.max(axis=-1, keepdims=True))\n    return e / e.sum(axis=-1, keepdims=True)",
                                       "e = np.exp(z - z.max())\n    return e / e.sum()"),
-    "fast:group_heads_from_modulo": ("heads = [h for h in range(H) if kv_head_of(h, group) == g]",
-                                     "heads = [h for h in range(H) if h % Hkv == g]"),
+    "fast:group_heads_from_modulo": ("heads = [h for h in range(H) if kv_head_of(h, group) == g]\n            K = gather_rows",
+                                     "heads = [h for h in range(H) if h % Hkv == g]\n            K = gather_rows"),
     "fast:transposed_scores": ("Z = scale * (q[s, heads].astype(np.float64) @ K.T)",
                                "Z = scale * (q[s, heads].astype(np.float64) @ K.T)[:, ::-1]"),
 }

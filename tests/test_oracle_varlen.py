@@ -75,6 +75,11 @@ def test_varlen_oracle_passes_its_pins():
     assert all(v is True for v in res.values()), res
 
 
+def test_varlen_fast_passes_the_same_pins():
+    res = pins(oracle.varlen_fast)
+    assert all(v is True for v in res.values()), res
+
+
 def test_single_token_queries_are_decode():
     v = W.varlen_random(204, 8, 2, 64, 16, [1, 1, 1], [5, 0, 47])
     kc, vc = W.host_pool(v.base)
@@ -103,19 +108,34 @@ def test_bad_inputs_are_rejected():
                       v.base.scale)
 
 
+LOOP = "for t in range(int(cu[s + 1] - cu[s])):\n            "
 MUTATIONS = {
-    "no_causal_mask": ("L = int(pos_offsets[s]) + t + 1\n", "L = int(pos_offsets[s]) + int(cu[s + 1] - cu[s])\n"),
-    "mask_off_by_one": ("L = int(pos_offsets[s]) + t + 1\n", "L = int(pos_offsets[s]) + t + (t > 0)\n"),
-    "wrong_query_row": ("i = int(cu[s]) + t\n", "i = int(cu[s + 1]) - 1 - t\n"),
+    "no_causal_mask": (LOOP + "L = int(pos_offsets[s]) + t + 1\n",
+                       LOOP + "L = int(pos_offsets[s]) + int(cu[s + 1] - cu[s])\n"),
+    "mask_off_by_one": (LOOP + "L = int(pos_offsets[s]) + t + 1\n",
+                        LOOP + "L = int(pos_offsets[s]) + t + (t > 0)\n"),
+    "wrong_query_row": ("i = int(cu[s]) + t\n            for h in range(H):",
+                        "i = int(cu[s + 1]) - 1 - t\n            for h in range(H):"),
 }
 
 
-@pytest.mark.parametrize("name", sorted(MUTATIONS))
+# varlen_fast only
+FAST_MUTATIONS = {
+    "fast:no_causal_mask": ("Z = scale * (q[i, heads].astype(np.float64) @ K[:L].T)\n                out[i, heads] = softmax(Z) @ V[:L]",
+                            "Z = scale * (q[i, heads].astype(np.float64) @ K.T)\n                out[i, heads] = softmax(Z) @ V"),
+    "fast:softmax_over_group": ("out[i, heads] = softmax(Z) @ V[:L]",
+                                "out[i, heads] = (np.exp(Z - Z.max()) / np.exp(Z - Z.max()).sum()) @ V[:L]"),
+    "fast:heads_by_modulo": ("heads = [h for h in range(H) if kv_head_of(h, group) == g]\n            for t in range(n):",
+                             "heads = [h for h in range(H) if h % Hkv == g]\n            for t in range(n):"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS) + sorted(FAST_MUTATIONS))
 def test_planted_mistake_is_caught(name):
-    old, new = MUTATIONS[name]
+    old, new = MUTATIONS[name] if name in MUTATIONS else FAST_MUTATIONS[name]
     src = inspect.getsource(OPA)
-    assert src.count(old) == 1
+    assert src.count(old) == 1, name
     mod = types.ModuleType("varlen_mutant")
     exec(compile(src.replace(old, new), "<mutant>", "exec"), mod.__dict__)
-    res = pins(mod.varlen)
+    res = pins(mod.varlen_fast if name.startswith("fast:") else mod.varlen)
     assert any(v is not True for v in res.values()), (name, res)

@@ -522,3 +522,37 @@ def test_varlen_splitk_rejects_small_scratch(pk, cuda_device):
                                        d["block_tables"], v.base.scale, max_q_len=3,
                                        num_splits=4, scratch=small)
     assert e.value.status == pk.PKV_ERR_SCRATCH_TOO_SMALL
+
+
+def test_varlen_splitk_replays_from_a_cuda_graph(pk, cuda_device):
+    """Phase 1 and the combine, captured once and replayed, reproduce the
+    eager result bit for bit (no host reads; the split count and scratch
+    are fixed at capture)."""
+    v = W.varlen_random(5200, 16, 4, 128, 16, [4, 2, 5], [3000, 1500, 4090])
+    d = varlen_device(v, cuda_device)
+    S = 6
+    n = pk.pkv_splitk_scratch_bytes(v.total_q, 16, 128, S)
+    scratch = torch.empty(n, dtype=torch.uint8, device=cuda_device)
+    eager = pk.pkv_varlen_attention_splitk(d["q"], d["k_cache"], d["v_cache"], d["cu"], d["pos"],
+                                           d["block_tables"], v.base.scale, max_q_len=5,
+                                           num_splits=S, scratch=scratch).clone()
+    out = torch.zeros_like(eager)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g):
+            pk.pkv_varlen_attention_splitk(d["q"], d["k_cache"], d["v_cache"], d["cu"],
+                                           d["pos"], d["block_tables"], v.base.scale,
+                                           max_q_len=5, num_splits=S, scratch=scratch, out=out)
+    torch.cuda.current_stream().wait_stream(side)
+    for _ in range(2):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert_bits_equal(out.cpu().numpy(), eager.cpu().numpy(), "graph replay")
+    kc, vc = W.host_pool(v.base)
+    ref = oracle.varlen(v.q, kc, vc, v.cu_seqlens_q, v.pos_offsets, v.base.block_tables,
+                        v.base.scale)
+    assert_attention_close(to_np(out), ref, "graph replay vs oracle")
+    assert pk.pkv_read_device_status() == 0

@@ -1,19 +1,21 @@
 """Benchmark of the paged-KV decode step on GB300.
 
-One step = one pass of the whole hot path over one batch: ``pkv_append`` of
-each sequence's newest token through its slot, then ``pkv_decode_splitk``
-with the split count from the heuristic (which falls back to the single-pass
-kernel when one wave of CTAs already fills the GPU), on the Llama-3-8B-shaped
-workload (B=32, H=32, Hkv=8, D=128, bs=16, L~U[512,2048], 16384-block pool).
+One step = one pass of the whole hot path over one batch: the slot-mapped
+append of each sequence's newest token fused into the decode
+(``pkv_append_decode``; ``--separate`` runs ``pkv_append`` then
+``pkv_decode_splitk``), with the split count from the heuristic, on the
+Llama-3-8B-shaped workload (B=32, H=32, Hkv=8, D=128, bs=16, L~U[512,2048],
+16384-block pool).  ``--workload`` selects the other shapes, ``--layout vllm``
+the vLLM cache layout.
 
 The metric is KV bytes read per second (each token's K and V once, f16),
 with decode tokens/s and microseconds per call alongside.  Four independent
 pool sets (4.3 GB together, far above the 129 MB L2) rotate between steps so
 no step is served from L2.
 
-``--impl reference`` times the CPU oracle (a bounded sample of the same
-workload per step) on the host cores and prints the same JSON line with
-``"impl": "reference"``.
+``--impl reference`` times the CPU oracle on the host cores (each step one
+whole decode call of the same workload, its sequences spread over one worker
+process per core) and prints the same JSON line with ``"impl": "reference"``.
 
 Under ``torchrun`` (N>1) every rank runs its own replica on its own GPU (the
 path has no exchange step); time is the max over ranks and ``value`` counts
@@ -188,61 +190,104 @@ def cpu_oracle_sample(w, seqs, kc, vc):
     return nbytes, dt
 
 
-def cpu_baseline_subprocess(budget_s=12.0):
-    """Time the oracle in a child process pinned to one BLAS/OpenMP thread."""
-    code = (
-        "import sys, json, time; sys.path.insert(0, %r)\n"
-        "import bench\n"
-        "from paged_kv_decode_08_gb300 import workloads as W\n"
-        "w = W.llama8b(); kc, vc = W.host_pool(w)\n"
-        "tot_b = 0; tot_t = 0.0; calls = 0\n"
-        "while tot_t < %f:\n"
-        "    b, t = bench.cpu_oracle_sample(w, list(range(w.num_seqs)), kc, vc)\n"
-        "    tot_b += b; tot_t += t; calls += 1\n"
-        "print(json.dumps({'bytes': tot_b, 'seconds': tot_t, 'calls': calls}))\n"
-    ) % (ROOT, budget_s)
-    env = dict(os.environ)
-    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
-        env[k] = "1"
-    res = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
-                         timeout=600)
-    if res.returncode != 0:
-        return None
-    d = json.loads(res.stdout.strip().splitlines()[-1])
-    return {"value": d["bytes"] / d["seconds"] / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{d['calls']} full decode call(s) of the workload (32 sequences, "
-                      f"{d['bytes'] / d['calls'] / 1e6:.0f} MB of K/V each) in float64, "
-                      f"{d['seconds']:.1f} s on one host thread"}
+# The oracle timed on the host: a fresh interpreter that never touches CUDA
+# builds the workload once, then forks one worker per host core (forking is
+# safe there: no GPU context exists in that process); each step is one whole
+# decode call of the workload (its 32 sequences spread over the workers).
+_ORACLE_STATE = {}
 
 
-def run_reference(args):
-    """The oracle on the host cores, a bounded sample per step."""
-    world, rank, _ = dist_setup()
-    if rank != 0:
-        return
+def _oracle_one_seq(s):
+    w, kc, vc = _ORACLE_STATE["w"], _ORACLE_STATE["kc"], _ORACLE_STATE["vc"]
+    return cpu_oracle_sample(w, [s], kc, vc)[0]
+
+
+def oracle_child_main(mode, steps, warmup, budget_s):
+    import multiprocessing as mp
+
     from paged_kv_decode_08_gb300 import workloads as W
 
     w = W.llama8b()
     kc, vc = W.host_pool(w)
-    seqs = list(range(4))
-    for _ in range(args.warmup):
-        cpu_oracle_sample(w, seqs, kc, vc)
-    tot_b, tot_t = 0, 0.0
-    for _ in range(args.steps):
-        b, t = cpu_oracle_sample(w, seqs, kc, vc)
-        tot_b += b
-        tot_t += t
-    value = tot_b / tot_t / 1e9
-    cores = 1  # main() pins BLAS/OpenMP to one thread for this arm
+    _ORACLE_STATE.update(w=w, kc=kc, vc=vc)
+    procs = os.cpu_count() or 1
+    seqs = list(range(w.num_seqs))
+    res = {"procs": procs}
+    if mode == "baseline":  # one core: whole decode calls in this process
+        tot_b, tot_t, calls = 0, 0.0, 0
+        while tot_t < budget_s / 2:
+            b, t = cpu_oracle_sample(w, seqs, kc, vc)
+            tot_b, tot_t, calls = tot_b + b, tot_t + t, calls + 1
+        res["one_core"] = {"bytes": tot_b, "seconds": tot_t, "calls": calls}
+    with mp.get_context("fork").Pool(procs) as pool:
+        def step():
+            t0 = time.perf_counter()
+            nb = sum(pool.map(_oracle_one_seq, seqs, chunksize=1))
+            return nb, time.perf_counter() - t0
+
+        for _ in range(warmup):
+            step()
+        tot_b, tot_t, calls = 0, 0.0, 0
+        while (calls < steps) if mode == "reference" else (tot_t < budget_s / 2):
+            b, t = step()
+            tot_b, tot_t, calls = tot_b + b, tot_t + t, calls + 1
+        res["all_cores"] = {"bytes": tot_b, "seconds": tot_t, "calls": calls}
+    print(json.dumps(res), flush=True)
+
+
+def run_oracle_child(mode, steps=0, warmup=1, budget_s=12.0):
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[k] = "1"
+    res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--oracle-child", mode,
+                          "--steps", str(steps), "--warmup", str(max(warmup, 3)),
+                          "--oracle-budget", str(budget_s)],
+                         capture_output=True, text=True, env=env, timeout=1200)
+    if res.returncode != 0:
+        return None
+    return json.loads(res.stdout.strip().splitlines()[-1])
+
+
+def cpu_baseline_subprocess(budget_s=12.0):
+    """The oracle on all host cores and on one (about budget_s of CPU time)."""
+    d = run_oracle_child("baseline", budget_s=budget_s)
+    if d is None:
+        return None
+    a, o = d["all_cores"], d["one_core"]
+    per_call = a["bytes"] / a["calls"] / 1e6
+    return {"value": a["bytes"] / a["seconds"] / 1e9, "unit": UNIT, "cores": d["procs"],
+            "kind": "oracle",
+            "sample": f"{a['calls']} full decode call(s) of the workload (32 sequences, "
+                      f"{per_call:.0f} MB of K/V each) in float64, sequences spread over "
+                      f"{d['procs']} worker processes, {a['seconds']:.1f} s",
+            "one_core": {"value": o["bytes"] / o["seconds"] / 1e9, "unit": UNIT, "cores": 1,
+                         "sample": f"{o['calls']} full decode call(s) on one host thread, "
+                                   f"{o['seconds']:.1f} s"}}
+
+
+def run_reference(args):
+    """The oracle on the host cores: each step one whole decode call of the
+    workload, its sequences spread over one worker process per core."""
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    d = run_oracle_child("reference", steps=args.steps, warmup=args.warmup)
+    if d is None:
+        print(json.dumps({"impl": "reference", "unavailable": "the oracle child process failed"}),
+              flush=True)
+        return
+    a = d["all_cores"]
+    value = a["bytes"] / a["seconds"] / 1e9
+    sample = (f"whole decode calls (32 sequences) per step, float64 numpy oracle, sequences "
+              f"spread over {d['procs']} worker processes")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_t / args.steps * 1e3,
+        "steps": a["calls"], "warmup": args.warmup, "ms_per_step": a["seconds"] / a["calls"] * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD_DESC["llama8b"], "sample_per_step": "4 of the 32 sequences"},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": "4 of the 32 sequences per step, float64 numpy oracle, "
-                                   "one host thread"},
+        "config": {"workload": WORKLOAD_DESC["llama8b"], "sample_per_step": "all 32 sequences"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": d["procs"], "kind": "oracle",
+                         "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -698,7 +743,13 @@ def main():
                          "with V [NB][Hkv][D][bs] (append and decode as two calls)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--oracle-child", choices=["baseline", "reference"], default=None,
+                    help=argparse.SUPPRESS)
+    ap.add_argument("--oracle-budget", type=float, default=12.0, help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.oracle_child:
+        oracle_child_main(args.oracle_child, args.steps, args.warmup, args.oracle_budget)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "ours" and args.workload == "loop":

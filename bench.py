@@ -68,10 +68,14 @@ N_SETS = 4  # default number of rotating pool sets (--sets)
 # Reported as null when the kernels have changed since.
 NCU_TRAFFIC = {
     # profiles/decode_llama8b.md: the fused append + single-pass decode launch,
-    # dram read 175.222 MB + write 3.364 MB
-    "llama8b": {"kernel_hash": "a27bab2667561d02", "bytes_per_launch": 178585600, "num_splits": 1,
+    # dram read 175.231 MB + write 3.333 MB
+    "llama8b": {"kernel_hash": "675ee69190d7ec06", "bytes_per_launch": 178563584, "num_splits": 1,
                 "fused": True, "layout": "blocked",
                 "kernel": "paged_decode_kernel<128,16,6,2,single,fused>"},
+    # profiles/varlen_spec_long.md: the varlen split-K phase 1 (10 splits),
+    # dram read 1342.525 MB + write 3.425 MB
+    "spec_long": {"kernel_hash": "675ee69190d7ec06", "bytes_per_launch": 1345949952,
+                  "num_splits": 10, "kernel": "paged_varlen_kernel<128,16,6,2,NT=2,blocked,split>"},
 }
 
 
@@ -480,6 +484,9 @@ def run_varlen(args):
     reads = -(-int(v.max_q_len) // max(1, 8 * nt // G))
     peak, peak_kind = measured_peaks()
     achieved = kv_bytes / (ms * 1e-3) / 1e9
+    tr = NCU_TRAFFIC.get(args.workload)
+    traffic = (tr["bytes_per_launch"] if tr and tr.get("kernel_hash") == kernel_source_hash()
+               and S == tr.get("num_splits") else None)
     line = {
         "metric": METRIC, "value": job_throughput(kv_bytes, world, ms), "unit": UNIT,
         "n_gpus": world, "steps": rounds * n_sets, "warmup": args.warmup, "ms_per_step": ms,
@@ -495,7 +502,8 @@ def run_varlen(args):
                      "kernel": ("paged_varlen_kernel" + (" split-K phase 1 + varlen_combine_kernel"
                                                          if S > 1 else "")
                                 + " (algorithmic bytes: each context once)"),
-                     "bytes_read_frac": reads * achieved / peak, "traffic": None},
+                     "bytes_read_frac": reads * achieved / peak, "traffic": traffic,
+                     "traffic_kernel": tr["kernel"] if traffic is not None else None},
         "clocks": clocks.summary(), "gpu_launches": rounds * n_sets * (2 if S > 1 else 1),
         "device_status_flags": pk.pkv_read_device_status(), "e2e": None, "cpu_baseline": None,
     }

@@ -1,0 +1,39 @@
+/* A plain C99 caller of libpagedkv: includes the header, links the shared
+ * library and exercises the host-only entry points (no GPU needed).  Prints
+ * one line per check and exits non-zero on the first failure. */
+#include <stdio.h>
+#include <string.h>
+
+#include "pagedkv.h"
+
+#define CHECK(cond)                                   \
+  do {                                                \
+    if (!(cond)) {                                    \
+      printf("FAIL %s (line %d)\n", #cond, __LINE__); \
+      return 1;                                       \
+    }                                                 \
+    printf("ok %s\n", #cond);                         \
+  } while (0)
+
+int main(void) {
+  /* split heuristics: host arithmetic only */
+  CHECK(pkv_pick_num_splits(32, 8, 2048, 16, 152) == 1);
+  CHECK(pkv_pick_num_splits(4, 8, 131072, 16, 152) > 1);
+  CHECK(pkv_pick_num_splits(0, 8, 2048, 16, 152) == 1);
+  CHECK(pkv_varlen_pick_num_splits(4, 32, 8, 4, 8192, 16, 152) == 10);
+  /* scratch sizes */
+  CHECK(pkv_splitk_scratch_bytes(4, 32, 128, 1) == 0);
+  CHECK(pkv_splitk_scratch_bytes(4, 32, 128, 16) >= (size_t)4 * 32 * 16 * 130 * 4);
+  CHECK(pkv_splitk_scratch_bytes(4, 32, 128, PKV_SPLITS_BALANCED) > 0);
+  /* status strings */
+  CHECK(strcmp(pkv_status_string(PKV_OK), "ok") == 0);
+  CHECK(strlen(pkv_status_string(PKV_ERR_SCRATCH_TOO_SMALL)) > 0);
+  /* argument validation returns before any CUDA call */
+  CHECK(pkv_decode(NULL, NULL, NULL, NULL, NULL, 1, 1, 1, 0.125f, 4, 2, 64, 16, NULL, NULL) ==
+        PKV_ERR_INVALID_ARG);
+  CHECK(strlen(pkv_last_error()) > 0);
+  CHECK(pkv_append((void*)0x10000, (void*)0x10000, (const int32_t*)0x10000, 0, (void*)0x10000,
+                   (void*)0x10000, 8, 16, 2, 64, NULL) == PKV_OK);
+  printf("all ok\n");
+  return 0;
+}

@@ -249,3 +249,25 @@ def test_varlen_splitk_rejects_bad_arguments(pk):
     assert f(*(ok[:7] + [0] + ok[8:]), 4, None, 0, None) == 0  # no queries
     g = pk.lib.pkv_varlen_attention_splitk_vllm_layout
     assert g(*ok, 4, None, 0, None) == -3
+
+
+def test_header_compiles_as_c99_and_links(pk, tmp_path):
+    """A plain C caller: the header is valid C99 without CUDA headers, and the
+    library's host-only entry points answer through it."""
+    import shutil
+    import subprocess
+
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    src = os.path.join(ROOT, "tests", "c_abi", "host_calls.c")
+    exe = str(tmp_path / "host_calls")
+    libdir = os.path.dirname(pk.LIB_PATH)
+    build = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic",
+                            "-I", os.path.join(ROOT, "include"), src, "-o", exe,
+                            "-L", libdir, "-lpagedkv", "-Wl,-rpath," + libdir],
+                           capture_output=True, text=True)
+    assert build.returncode == 0, build.stderr
+    run = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert run.returncode == 0, run.stdout + run.stderr
+    assert "all ok" in run.stdout

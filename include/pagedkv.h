@@ -341,6 +341,17 @@ pkv_status pkv_varlen_attention_splitk_vllm_layout(
     int32_t num_splits, void* scratch, size_t scratch_bytes, void* stream);
 
 /*
+ * pkv_selftest_wait_timeout — a diagnostic of the failure path (the pages
+ * have no counterpart): launches one warp that waits on a barrier nothing
+ * arrives on.  The bounded wait gives up after 100 ms and sets
+ * PKV_DEV_WAIT_TIMEOUT, as a decode kernel does when a tile copy is lost; the
+ * kernel then returns and the context stays usable.  Until
+ * pkv_read_device_status clears the word, decode and varlen calls write
+ * nothing.  Asynchronous on stream; no memory is touched but the status word.
+ */
+pkv_status pkv_selftest_wait_timeout(void* stream);
+
+/*
  * pkv_splitk_scratch_bytes — bytes of scratch pkv_decode_splitk needs for S
  * splits: f32 partial outputs [num_seqs][num_heads][S][head_dim] followed by
  * f32 running max and running sum [num_seqs][num_heads][S] each (every part

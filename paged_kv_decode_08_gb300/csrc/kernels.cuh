@@ -1527,6 +1527,9 @@ __global__ void __launch_bounds__(kCombineThreads) splitk_combine_kernel(const C
   __shared__ float s_red[kCombineThreads / 32];
   pdl_launch_dependents();
   pdl_wait();
+  // after a lost copy has been flagged, decode calls write nothing (the
+  // partials were not written either); uniform for the CTA
+  if (*reinterpret_cast<volatile unsigned int*>(&g_device_status) & kDevWaitTimeout) return;
   const int sh = blockIdx.x;
   const int s = sh / p.num_heads;
   int L = __ldg(p.context_lens + s);
@@ -1566,6 +1569,7 @@ varlen_combine_kernel(const VarlenCombineParams p) {
   __shared__ float s_red[kCombineThreads / 32];
   pdl_launch_dependents();
   pdl_wait();
+  if (*reinterpret_cast<volatile unsigned int*>(&g_device_status) & kDevWaitTimeout) return;
   const int rh = blockIdx.x;  // row * H + head
   const int row = rh / p.num_heads;
   int lo = 0, hi = p.num_seqs - 1;  // last sequence whose first row is <= row
@@ -1593,6 +1597,23 @@ varlen_combine_kernel(const VarlenCombineParams p) {
   combine_row(p.part_m + (size_t)rh * p.num_splits, p.part_l + (size_t)rh * p.num_splits,
               p.part_out + (size_t)rh * p.num_splits * p.head_dim, n_valid, p.head_dim, out_row,
               s_w, s_red);
+}
+
+// Diagnostic: one warp waits on an mbarrier that nothing arrives on.  The
+// bounded wait gives up after kWaitLimitNs and the kernel flags
+// kDevWaitTimeout, as a decode kernel does when a tile copy is lost; no copy,
+// no global access but the flag.
+__global__ void __launch_bounds__(32) wait_timeout_probe_kernel() {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = smem_addr(&bar);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  const bool landed = mbar_wait_bounded(b, 0, kWaitLimitNs);
+  if (!__any_sync(0xffffffffu, !landed)) return;
+  if (threadIdx.x == 0) atomicOr(&g_device_status, kDevWaitTimeout);
 }
 
 }  // namespace pkv

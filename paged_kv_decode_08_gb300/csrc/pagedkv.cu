@@ -896,6 +896,13 @@ pkv_status pkv_varlen_attention_splitk_vllm_layout(
                      static_cast<cudaStream_t>(stream), true);
 }
 
+pkv_status pkv_selftest_wait_timeout(void* stream) {
+  const cudaError_t e = launch_pdl(wait_timeout_probe_kernel, 1, 32, 0,
+                                   static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "wait-timeout probe launch");
+  return PKV_OK;
+}
+
 pkv_status pkv_read_device_status(int32_t* flags, void* stream) {
   if (!flags) return fail(PKV_ERR_INVALID_ARG, "flags is NULL");
   cudaStream_t cs = static_cast<cudaStream_t>(stream);

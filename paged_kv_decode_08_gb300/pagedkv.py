@@ -86,6 +86,8 @@ def _load():
     lib.pkv_status_string.restype = ctypes.c_char_p
     lib.pkv_last_error.argtypes = []
     lib.pkv_last_error.restype = ctypes.c_char_p
+    lib.pkv_selftest_wait_timeout.argtypes = [vp]
+    lib.pkv_selftest_wait_timeout.restype = i32
     lib.pkv_read_device_status.argtypes = [ctypes.POINTER(ctypes.c_int32), vp]
     lib.pkv_read_device_status.restype = i32
     return lib
@@ -430,6 +432,11 @@ def pkv_decode_vllm_layout(q, k_cache, v_cache, block_tables, context_lens, scal
                                       int(num_splits), scratch.data_ptr(), scratch.numel(),
                                       _stream_ptr(stream)), "pkv_decode_vllm_layout")
     return out
+
+
+def pkv_selftest_wait_timeout(stream=None):
+    """Launch the failure-path diagnostic (sets PKV_DEV_WAIT_TIMEOUT after 100 ms)."""
+    _check(lib.pkv_selftest_wait_timeout(_stream_ptr(stream)), "pkv_selftest_wait_timeout")
 
 
 def pkv_read_device_status(stream=None) -> int:

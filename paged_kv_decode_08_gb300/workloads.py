@@ -318,7 +318,11 @@ class AppendDecodeLoop:
         nalloc = np.zeros(B, np.int64)
         for s in range(B):
             n = -(-int(self.start_lens[s]) // bs)
+            if n > max_blocks_per_seq:
+                raise ValueError("start length exceeds max_blocks_per_seq")
             for j in range(n):
+                if not free:
+                    raise RuntimeError("free list exhausted")
                 tables[s, j] = free.pop()
             nalloc[s] = n
         self.start_tables = tables.copy()

@@ -98,3 +98,18 @@ def test_vllm_layout_pools_hold_the_blocked_pools_values():
         k2, v2 = oracle.blocked_from_vllm_layout(kv, vv)
         assert np.array_equal(k2.view(np.uint16), kb.view(np.uint16))
         assert np.array_equal(v2.view(np.uint16), vb.view(np.uint16))
+
+
+def test_loop_allocator_reports_exhaustion_and_overflow():
+    """The loop harness's block allocator fails loudly, never silently: a
+    pool too small for the start lengths or for a later step, and a sequence
+    growing past its table row."""
+    kw = dict(num_seqs=2, num_heads=2, head_dim=64, block_size=16, min_len=32, max_len=32)
+    with pytest.raises(RuntimeError, match="free list exhausted"):
+        W.AppendDecodeLoop(steps=1, num_blocks=4, max_blocks_per_seq=4, **kw)  # needs 4 + poison
+    with pytest.raises(RuntimeError, match="free list exhausted"):
+        W.AppendDecodeLoop(steps=1, num_blocks=5, max_blocks_per_seq=4, **kw)  # step 0 needs a 6th
+    with pytest.raises(ValueError, match="max_blocks_per_seq"):
+        W.AppendDecodeLoop(steps=1, num_blocks=50, max_blocks_per_seq=2, **kw)
+    ok = W.AppendDecodeLoop(steps=1, num_blocks=7, max_blocks_per_seq=4, **kw)  # 2 + 2 + 2 + poison
+    assert ok.end_lens.tolist() == [33, 33]

@@ -341,6 +341,50 @@ pkv_status pkv_varlen_attention_splitk_vllm_layout(
     int32_t num_splits, void* scratch, size_t scratch_bytes, void* stream);
 
 /*
+ * pkv_qkv_norm_rope_append — the step before attention in one launch: split
+ * each token's fused projection row into query, key and value heads, RMS-norm
+ * the query and key heads, turn them by the rotary angles of the token's
+ * position, write the queries token-major and append the keys and values to
+ * the paged pools (ferrum-kernels src/backend/cuda/paged.rs,
+ * split_qkv_norm_rope_into_paged_cache and its _varlen form; the pages give
+ * the launch, the arithmetic below is its plainest reading).
+ *
+ *   qkv           device f16 [total_q][(num_heads + 2 num_kv_heads) * head_dim]:
+ *                 each row holds the query heads, then the key heads, then
+ *                 the value heads
+ *   q_norm_w, k_norm_w  device f16 [head_dim], or NULL for no norm of that
+ *                 kind: y = x / sqrt(mean(x^2) + eps) * w over a head
+ *   cos_table, sin_table  device f32 [max_pos][head_dim / 2]: the rotary
+ *                 angle's cosine and sine per position and pair
+ *   q_out         device f16 [total_q][num_heads][head_dim]
+ *   k_cache, v_cache  device f16 pools (layout above), written in place
+ *   cu_seqlens_q  device int32 [num_seqs + 1], rising from 0 to total_q
+ *   pos_offsets   device int32 [num_seqs]: row t of sequence s is at
+ *                 position p = pos_offsets[s] + t, its rotary position and
+ *                 its cache row
+ *   block_tables  device int32 [num_seqs][max_blocks_per_seq]
+ *
+ * Rotation: pair (x[i], x[i + head_dim/2]) of a (normed) query or key head
+ * becomes (x[i] c - x[i + head_dim/2] s, x[i + head_dim/2] c + x[i] s) with
+ * c = cos_table[p][i], s = sin_table[p][i]; f32 arithmetic, f16 results
+ * rounded to nearest even.  Value heads are copied bit for bit.  Keys and
+ * values land at slot block_tables[s][p / block_size] * block_size +
+ * p % block_size, as pkv_append writes.  A row whose sequence range or
+ * position is invalid (p < 0, p >= max_pos or beyond the table) is skipped
+ * and sets PKV_DEV_BAD_CONTEXT_LEN; a table entry outside [0, num_blocks)
+ * skips that row's key and value writes and sets PKV_DEV_BAD_BLOCK_ID.
+ * head_dim in {64, 128}, block_size in {16, 32}; eps >= 0.
+ */
+pkv_status pkv_qkv_norm_rope_append(const void* qkv, const void* q_norm_w, const void* k_norm_w,
+                                    const float* cos_table, const float* sin_table, void* q_out,
+                                    void* k_cache, void* v_cache, const int32_t* cu_seqlens_q,
+                                    const int32_t* pos_offsets, const int32_t* block_tables,
+                                    int32_t num_seqs, int32_t total_q, int32_t max_blocks_per_seq,
+                                    int32_t num_blocks, int32_t num_heads, int32_t num_kv_heads,
+                                    int32_t head_dim, int32_t block_size, int32_t max_pos, float eps,
+                                    void* stream);
+
+/*
  * pkv_selftest_wait_timeout — a diagnostic of the failure path (the pages
  * have no counterpart): launches one warp that waits on a barrier nothing
  * arrives on.  The bounded wait gives up after 100 ms and sets

@@ -1,6 +1,8 @@
 // Kernels of libpagedkv (GB300, sm_103a):
 //   append_kernel                 slot-mapped KV write
 //   append_vllm_kernel            the same write into vLLM-layout pools
+//   qkv_norm_rope_kernel          fused QKV split + RMS norm + rotary
+//                                 embedding + paged append
 //   paged_decode_kernel           decode: single pass, or split-K phase 1;
 //                                 optionally with the step's append fused in;
 //                                 blocked or vLLM-layout pools
@@ -135,6 +137,128 @@ append_vllm_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
     __half* vdst = v_cache + (tile * chunks_per_row * 8 + (size_t)ch * 8) * block_size + off;
 #pragma unroll
     for (int e = 0; e < 8; ++e) vdst[(size_t)e * block_size] = vh[e];
+  }
+}
+
+// ---------------------------------------------------------------------------
+// fused QKV split + per-head RMS norm + rotary embedding + paged append
+// ---------------------------------------------------------------------------
+//
+// One CTA per token, one warp per head (warps loop over the H + 2 Hkv heads
+// of the token's row [q heads | k heads | v heads]).  Token row r of sequence
+// s sits at position p = pos_offsets[s] + (r - cu_seqlens_q[s]), its rotary
+// position and its cache row.  Query and key heads are RMS-normalised when a
+// weight vector is given, then turned by the rotary angles of position p
+// (rotate-half pairs (i, i + D/2), cos/sin tables [max_pos][D/2] f32); value
+// heads are copied.  Queries go to q_out token-major, keys and values to the
+// pools at slot block_tables[s][p / bs] * bs + p % bs.  A token whose
+// sequence range or position is invalid is skipped and flagged; an invalid
+// block id skips its key and value writes and is flagged.
+
+struct QkvRopeParams {
+  const __half* qkv;       // [total_q][(H + 2 Hkv) D]
+  const __half* q_norm_w;  // [D] or null: no query norm
+  const __half* k_norm_w;  // [D] or null: no key norm
+  const float* cos_t;      // [max_pos][D/2]
+  const float* sin_t;
+  __half* q_out;  // [total_q][H][D]
+  __half* k_cache;
+  __half* v_cache;
+  const int32_t* cu_seqlens_q;  // [B + 1]
+  const int32_t* pos_offsets;   // [B]
+  const int32_t* block_tables;  // [B][MBPS]
+  int num_seqs;
+  int total_q;
+  int num_heads;
+  int num_kv_heads;
+  int max_blocks_per_seq;
+  int num_blocks;
+  int block_size;
+  int max_pos;
+  float eps;
+};
+
+template <int D>
+__global__ void __launch_bounds__(256) qkv_norm_rope_kernel(const QkvRopeParams p) {
+  constexpr int PAIRS = D / 64;  // rotate-half pairs per lane
+  pdl_launch_dependents();
+  pdl_wait();
+  const int row = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int lo = 0, hi = p.num_seqs - 1;  // last sequence whose first row is <= row
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(p.cu_seqlens_q + mid) <= row)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  const int q_begin = __ldg(p.cu_seqlens_q + lo);
+  const int q_end = __ldg(p.cu_seqlens_q + lo + 1);
+  const int pos = __ldg(p.pos_offsets + lo) + (row - q_begin);
+  const int cap = p.max_blocks_per_seq * p.block_size;
+  if (q_begin < 0 || q_end > p.total_q || row < q_begin || row >= q_end || pos < 0 ||
+      pos >= p.max_pos || pos >= cap) {
+    if (threadIdx.x == 0) atomicOr(&g_device_status, kDevBadContextLen);
+    return;
+  }
+  const int blk = __ldg(p.block_tables + (size_t)lo * p.max_blocks_per_seq + pos / p.block_size);
+  const bool blk_ok = blk >= 0 && blk < p.num_blocks;
+  if (!blk_ok && threadIdx.x == 0) atomicOr(&g_device_status, kDevBadBlockId);
+  const int off = pos - (pos / p.block_size) * p.block_size;
+
+  const int H = p.num_heads, Hkv = p.num_kv_heads;
+  const __half* x_row = p.qkv + (size_t)row * (H + 2 * Hkv) * D;
+  const float* cs = p.cos_t + (size_t)pos * (D / 2);
+  const float* sn = p.sin_t + (size_t)pos * (D / 2);
+  for (int hh = warp; hh < H + 2 * Hkv; hh += 8) {
+    const __half* x = x_row + (size_t)hh * D;
+    float a[PAIRS], b[PAIRS];
+#pragma unroll
+    for (int j = 0; j < PAIRS; ++j) {
+      a[j] = __half2float(x[lane + 32 * j]);
+      b[j] = __half2float(x[lane + 32 * j + D / 2]);
+    }
+    if (hh >= H + Hkv) {  // value head: copied into the pool
+      if (blk_ok) {
+        __half* dst = p.v_cache + (((size_t)blk * Hkv + (hh - H - Hkv)) * p.block_size + off) * D;
+#pragma unroll
+        for (int j = 0; j < PAIRS; ++j) {
+          dst[lane + 32 * j] = x[lane + 32 * j];
+          dst[lane + 32 * j + D / 2] = x[lane + 32 * j + D / 2];
+        }
+      }
+      continue;
+    }
+    const bool is_q = hh < H;
+    const __half* w = is_q ? p.q_norm_w : p.k_norm_w;
+    if (w != nullptr) {
+      float ss = 0.f;
+#pragma unroll
+      for (int j = 0; j < PAIRS; ++j) ss += a[j] * a[j] + b[j] * b[j];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      const float r = rsqrtf(ss / (float)D + p.eps);
+#pragma unroll
+      for (int j = 0; j < PAIRS; ++j) {
+        a[j] = a[j] * r * __half2float(w[lane + 32 * j]);
+        b[j] = b[j] * r * __half2float(w[lane + 32 * j + D / 2]);
+      }
+    }
+    __half* dst;
+    if (is_q) {
+      dst = p.q_out + ((size_t)row * H + hh) * D;
+    } else {
+      if (!blk_ok) continue;
+      dst = p.k_cache + (((size_t)blk * Hkv + (hh - H)) * p.block_size + off) * D;
+    }
+#pragma unroll
+    for (int j = 0; j < PAIRS; ++j) {
+      const int i = lane + 32 * j;
+      const float c = __ldg(cs + i), sv = __ldg(sn + i);
+      dst[i] = __float2half_rn(a[j] * c - b[j] * sv);
+      dst[i + D / 2] = __float2half_rn(b[j] * c + a[j] * sv);
+    }
   }
 }
 

@@ -896,6 +896,67 @@ pkv_status pkv_varlen_attention_splitk_vllm_layout(
                      static_cast<cudaStream_t>(stream), true);
 }
 
+pkv_status pkv_qkv_norm_rope_append(const void* qkv, const void* q_norm_w, const void* k_norm_w,
+                                    const float* cos_table, const float* sin_table, void* q_out,
+                                    void* k_cache, void* v_cache, const int32_t* cu_seqlens_q,
+                                    const int32_t* pos_offsets, const int32_t* block_tables,
+                                    int32_t num_seqs, int32_t total_q, int32_t max_blocks_per_seq,
+                                    int32_t num_blocks, int32_t num_heads, int32_t num_kv_heads,
+                                    int32_t head_dim, int32_t block_size, int32_t max_pos, float eps,
+                                    void* stream) {
+  if (!qkv || !cos_table || !sin_table || !q_out || !k_cache || !v_cache || !cu_seqlens_q ||
+      !pos_offsets || !block_tables)
+    return fail(PKV_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (num_seqs < 0 || total_q < 0) return fail(PKV_ERR_INVALID_ARG, "num_seqs / total_q < 0");
+  if (num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0)
+    return fail(PKV_ERR_INVALID_ARG, "num_heads (%d) must be a positive multiple of num_kv_heads (%d)",
+                num_heads, num_kv_heads);
+  if (max_blocks_per_seq <= 0 || num_blocks <= 0 || max_pos <= 0 || head_dim <= 0 ||
+      block_size <= 0)
+    return fail(PKV_ERR_INVALID_ARG, "sizes must be positive");
+  if (!std::isfinite(eps) || eps < 0.f) return fail(PKV_ERR_INVALID_ARG, "eps must be finite and >= 0");
+  if (head_dim != 64 && head_dim != 128)
+    return fail(PKV_ERR_UNSUPPORTED, "head_dim %d (built: 64, 128)", head_dim);
+  if (block_size != 16 && block_size != 32)
+    return fail(PKV_ERR_UNSUPPORTED, "block_size %d (built: 16, 32)", block_size);
+  if ((long long)num_blocks * block_size >= (1ll << 31) ||
+      (long long)max_blocks_per_seq * block_size >= (1ll << 31))
+    return fail(PKV_ERR_INVALID_ARG, "pool or table too large for 32-bit positions");
+  if (!aligned(qkv, 2) || !aligned(q_out, 2) || !aligned(k_cache, 2) || !aligned(v_cache, 2) ||
+      (q_norm_w && !aligned(q_norm_w, 2)) || (k_norm_w && !aligned(k_norm_w, 2)) ||
+      !aligned(cos_table, 4) || !aligned(sin_table, 4) || !aligned(cu_seqlens_q, 4) ||
+      !aligned(pos_offsets, 4) || !aligned(block_tables, 4))
+    return fail(PKV_ERR_INVALID_ARG, "misaligned pointer");
+  if (num_seqs == 0 || total_q == 0) return PKV_OK;
+  QkvRopeParams qp{};
+  qp.qkv = static_cast<const __half*>(qkv);
+  qp.q_norm_w = static_cast<const __half*>(q_norm_w);
+  qp.k_norm_w = static_cast<const __half*>(k_norm_w);
+  qp.cos_t = cos_table;
+  qp.sin_t = sin_table;
+  qp.q_out = static_cast<__half*>(q_out);
+  qp.k_cache = static_cast<__half*>(k_cache);
+  qp.v_cache = static_cast<__half*>(v_cache);
+  qp.cu_seqlens_q = cu_seqlens_q;
+  qp.pos_offsets = pos_offsets;
+  qp.block_tables = block_tables;
+  qp.num_seqs = num_seqs;
+  qp.total_q = total_q;
+  qp.num_heads = num_heads;
+  qp.num_kv_heads = num_kv_heads;
+  qp.max_blocks_per_seq = max_blocks_per_seq;
+  qp.num_blocks = num_blocks;
+  qp.block_size = block_size;
+  qp.max_pos = max_pos;
+  qp.eps = eps;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = head_dim == 128
+                            ? launch_pdl(qkv_norm_rope_kernel<128>, total_q, 256, 0, cs, qp)
+                            : launch_pdl(qkv_norm_rope_kernel<64>, total_q, 256, 0, cs, qp);
+  if (e != cudaSuccess) return cuda_fail(e, "qkv norm/rope/append launch");
+  return PKV_OK;
+}
+
 pkv_status pkv_selftest_wait_timeout(void* stream) {
   const cudaError_t e = launch_pdl(wait_timeout_probe_kernel, 1, 32, 0,
                                    static_cast<cudaStream_t>(stream));

@@ -86,6 +86,9 @@ def _load():
     lib.pkv_status_string.restype = ctypes.c_char_p
     lib.pkv_last_error.argtypes = []
     lib.pkv_last_error.restype = ctypes.c_char_p
+    lib.pkv_qkv_norm_rope_append.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32,
+                                             i32, i32, i32, i32, i32, i32, i32, f32, vp]
+    lib.pkv_qkv_norm_rope_append.restype = i32
     lib.pkv_selftest_wait_timeout.argtypes = [vp]
     lib.pkv_selftest_wait_timeout.restype = i32
     lib.pkv_read_device_status.argtypes = [ctypes.POINTER(ctypes.c_int32), vp]
@@ -432,6 +435,44 @@ def pkv_decode_vllm_layout(q, k_cache, v_cache, block_tables, context_lens, scal
                                       int(num_splits), scratch.data_ptr(), scratch.numel(),
                                       _stream_ptr(stream)), "pkv_decode_vllm_layout")
     return out
+
+
+def pkv_qkv_norm_rope_append(qkv, q_norm_w, k_norm_w, cos_table, sin_table, k_cache, v_cache,
+                             cu_seqlens_q, pos_offsets, block_tables, num_heads, eps=1e-6,
+                             q_out=None, stream=None):
+    """Split ``qkv [total_q][(H + 2 Hkv) D]``, RMS-norm query/key heads (weights
+    may be None), rotate by the tables ``[max_pos][D/2]`` (f32), write the
+    queries (returned, ``[total_q][H][D]``) and append keys/values to the pools."""
+    import torch
+
+    _want(k_cache, "k_cache", torch.float16, 4)
+    NB, Hkv, bs, D = k_cache.shape
+    _want(v_cache, "v_cache", torch.float16, 4, k_cache.shape)
+    H = int(num_heads)
+    _want(qkv, "qkv", torch.float16, 2)
+    total_q = qkv.shape[0]
+    _want(qkv, "qkv", torch.float16, 2, (total_q, (H + 2 * Hkv) * D))
+    for name, w in (("q_norm_w", q_norm_w), ("k_norm_w", k_norm_w)):
+        if w is not None:
+            _want(w, name, torch.float16, 1, (D,))
+    _want(cos_table, "cos_table", torch.float32, 2)
+    max_pos = cos_table.shape[0]
+    _want(cos_table, "cos_table", torch.float32, 2, (max_pos, D // 2))
+    _want(sin_table, "sin_table", torch.float32, 2, (max_pos, D // 2))
+    _want(block_tables, "block_tables", torch.int32, 2)
+    B = block_tables.shape[0]
+    _want(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1, (B + 1,))
+    _want(pos_offsets, "pos_offsets", torch.int32, 1, (B,))
+    if q_out is None:
+        q_out = torch.empty((total_q, H, D), dtype=torch.float16, device=qkv.device)
+    _want(q_out, "q_out", torch.float16, 3, (total_q, H, D))
+    ptr = lambda t: None if t is None else t.data_ptr()  # noqa: E731
+    _check(lib.pkv_qkv_norm_rope_append(
+        qkv.data_ptr(), ptr(q_norm_w), ptr(k_norm_w), cos_table.data_ptr(), sin_table.data_ptr(),
+        q_out.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), cu_seqlens_q.data_ptr(),
+        pos_offsets.data_ptr(), block_tables.data_ptr(), B, total_q, block_tables.shape[1], NB,
+        H, Hkv, D, bs, max_pos, float(eps), _stream_ptr(stream)), "pkv_qkv_norm_rope_append")
+    return q_out
 
 
 def pkv_selftest_wait_timeout(stream=None):

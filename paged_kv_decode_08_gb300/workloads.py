@@ -521,3 +521,64 @@ def spec_verify() -> VarlenWorkload:
     prefix = rng.integers(508, 2044, size=32, endpoint=True)
     return varlen_random(BASE_SEED + 5, 32, 8, 128, 16, [4] * 32, prefix,
                          num_blocks=16384)
+
+
+# ---------------------------------------------------------------------------
+# Inputs of the fused QKV split + norm + rotary + append step
+# ---------------------------------------------------------------------------
+
+@dataclasses.dataclass
+class QkvCase:
+    """Seeded inputs: fused projection rows, norm weights, rotary tables and a
+    paged context for each sequence's new tokens (positions prefix .. prefix +
+    q_len - 1).  The tables hold cos/sin of the standard rotary angles
+    p * base^(-2i/D); they are inputs of the step, like the weights."""
+
+    qkv: np.ndarray        # f16 [total_q][(H + 2 Hkv) D]
+    q_norm_w: Optional[np.ndarray]  # f16 [D] or None
+    k_norm_w: Optional[np.ndarray]
+    cos: np.ndarray        # f32 [max_pos][D/2]
+    sin: np.ndarray
+    cu_seqlens_q: np.ndarray  # int32 [B+1]
+    pos_offsets: np.ndarray   # int32 [B]
+    block_tables: np.ndarray  # int32 [B][MBPS]
+    num_heads: int
+    num_kv_heads: int
+    head_dim: int
+    block_size: int
+    num_blocks: int
+    eps: float = 1e-6
+
+
+def qkv_case(seed: int, num_heads: int, num_kv_heads: int, head_dim: int, block_size: int,
+             q_lens, prefix_lens, norm: bool = True, base: float = 10000.0,
+             extra_blocks: int = 3) -> QkvCase:
+    rng = _rng(seed)
+    q_lens = [int(x) for x in q_lens]
+    prefix = [int(x) for x in prefix_lens]
+    B = len(q_lens)
+    ends = [p + n for p, n in zip(prefix, q_lens)]
+    nblk = [-(-e // block_size) for e in ends]
+    NB = sum(nblk) + extra_blocks
+    mbps = max(1, max(nblk))
+    perm = rng.permutation(NB).astype(np.int32)
+    tables = np.full((B, mbps), perm[-1], np.int32)
+    cur = 0
+    for s, n in enumerate(nblk):
+        tables[s, :n] = perm[cur:cur + n]
+        cur += n
+    total_q = sum(q_lens)
+    width = (num_heads + 2 * num_kv_heads) * head_dim
+    qkv = _normal_f16(rng, (total_q, width), 1.0)
+    qw = rng.uniform(0.5, 1.5, head_dim).astype(np.float16) if norm else None
+    kw = rng.uniform(0.5, 1.5, head_dim).astype(np.float16) if norm else None
+    max_pos = max(ends) + 1
+    inv = base ** (-np.arange(head_dim // 2) * 2.0 / head_dim)
+    ang = np.arange(max_pos)[:, None] * inv[None, :]
+    cu = np.zeros(B + 1, np.int32)
+    cu[1:] = np.cumsum(q_lens)
+    return QkvCase(qkv=qkv, q_norm_w=qw, k_norm_w=kw, cos=np.cos(ang).astype(np.float32),
+                   sin=np.sin(ang).astype(np.float32), cu_seqlens_q=cu,
+                   pos_offsets=np.asarray(prefix, np.int32), block_tables=tables,
+                   num_heads=num_heads, num_kv_heads=num_kv_heads, head_dim=head_dim,
+                   block_size=block_size, num_blocks=NB)

@@ -35,7 +35,8 @@ def test_header_declares_the_expected_calls():
               "pkv_pick_num_splits", "pkv_status_string", "pkv_last_error",
               "pkv_read_device_status", "pkv_append_vllm_layout", "pkv_decode_vllm_layout",
               "pkv_varlen_attention_vllm_layout", "pkv_varlen_attention_splitk",
-              "pkv_varlen_attention_splitk_vllm_layout", "pkv_varlen_pick_num_splits"]:
+              "pkv_varlen_attention_splitk_vllm_layout", "pkv_varlen_pick_num_splits",
+              "pkv_qkv_norm_rope_append", "pkv_selftest_wait_timeout"]:
         assert n in names
 
 
@@ -271,3 +272,32 @@ def test_header_compiles_as_c99_and_links(pk, tmp_path):
     run = subprocess.run([exe], capture_output=True, text=True, timeout=60)
     assert run.returncode == 0, run.stdout + run.stderr
     assert "all ok" in run.stdout
+
+
+def test_qkv_norm_rope_rejects_bad_arguments(pk):
+    """Every call here is rejected (or has no rows) before any CUDA call."""
+    f = pk.lib.pkv_qkv_norm_rope_append
+    # qkv, qw, kw, cos, sin, q_out, kc, vc, cu, pos, bt, B, T, MBPS, NB, H, Hkv, D, bs, max_pos, eps
+    base = [F16, None, None, F16, F16, F16, F16, F16, F16, F16, F16, 2, 4, 3, 8, 4, 2, 64, 16,
+            100, 1e-6]
+
+    def call(**over):
+        a = list(base)
+        names = ["qkv", "qw", "kw", "cos", "sin", "qo", "kc", "vc", "cu", "pos", "bt", "B", "T",
+                 "mbps", "nb", "H", "Hkv", "D", "bs", "max_pos", "eps"]
+        for k, v in over.items():
+            a[names.index(k)] = v
+        return f(*a, None)
+
+    assert call(qkv=None) == -1
+    assert call(cos=None) == -1
+    assert call(H=6, Hkv=4) == -1
+    assert call(D=96) == -2
+    assert call(bs=8) == -2
+    assert call(max_pos=0) == -1
+    assert call(eps=-1.0) == -1
+    assert call(eps=float("nan")) == -1
+    assert call(qkv=F16 + 1) == -1            # misaligned f16
+    assert call(cos=F16 + 2) == -1            # misaligned f32
+    assert call(T=0) == 0                      # no rows: nothing launched
+    assert call(B=0) == 0

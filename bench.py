@@ -57,11 +57,15 @@ WORKLOAD_DESC = {
     "spec_long": ("speculative-decode verification over long contexts: B=4, H=32, Hkv=8, D=128, "
                   "bs=16, 4 draft tokens per sequence after prefixes {32768,65536,98304,131072}-4, "
                   "24576-block pool (pkv_varlen_attention_splitk, causal)"),
+    "qkv_prefill": ("fused QKV split + per-head RMS norm + rotary + paged append on the "
+                    "Llama-3-8B attention shape: 4 sequences x 2048 new tokens (H=32, Hkv=8, "
+                    "D=128, bs=16), f16 rows ~N(0,1) (pkv_qkv_norm_rope_append)"),
     "loop": ("append+decode loop: MHA H=Hkv=16, D=64, bs=16, B=128, start context U[64,4096], "
              "128 steps of pkv_append (142 rows, 14 padding slots = -1, new blocks from a "
              "shuffled free list of 40000) then pkv_decode_splitk on one stream"),
 }
 N_SETS = 4  # default number of rotating pool sets (--sets)
+BASE_QKV_SEED = 20261210
 
 # DRAM bytes (read + write) of one decode launch on this workload, from the
 # ncu capture summarised in profiles/ (kernel source hash at capture time).
@@ -293,6 +297,95 @@ def run_reference(args):
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": d["procs"], "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_qkv(args):
+    """The fused QKV split + norm + rotary + append step on a prefill-sized
+    call.  Bytes per call: the rows read (q, k, v heads), the cos/sin rows read
+    and the queries, keys and values written; rotating input sets keep the
+    reads out of L2."""
+    import numpy as np
+    import torch
+
+    from paged_kv_decode_08_gb300 import pagedkv as pk
+    from paged_kv_decode_08_gb300 import workloads as W
+
+    world, rank, local = dist_setup()
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    H, Hkv, D, bs = 32, 8, 128, 16
+    c = W.qkv_case(BASE_QKV_SEED, H, Hkv, D, bs, [2048] * 4, [0] * 4)
+    n_sets = args.sets
+    g = torch.Generator(device=dev)
+    sets = []
+    for r in range(n_sets):
+        g.manual_seed(2000 + r)
+        qkv = (torch.from_numpy(c.qkv).to(dev) if r == 0 else
+               torch.randn(c.qkv.shape, generator=g, device=dev).to(torch.float16))
+        shape = (c.num_blocks, Hkv, bs, D)
+        sets.append({"qkv": qkv, "kc": torch.empty(shape, dtype=torch.float16, device=dev),
+                     "vc": torch.empty(shape, dtype=torch.float16, device=dev),
+                     "q_out": torch.empty((c.qkv.shape[0], H, D), dtype=torch.float16,
+                                          device=dev)})
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    qw, kw, cos, sin = t(c.q_norm_w), t(c.k_norm_w), t(c.cos), t(c.sin)
+    cu, pos, bt = t(c.cu_seqlens_q), t(c.pos_offsets), t(c.block_tables)
+
+    def call(i):
+        st = sets[i % n_sets]
+        pk.pkv_qkv_norm_rope_append(st["qkv"], qw, kw, cos, sin, st["kc"], st["vc"], cu, pos, bt,
+                                    H, eps=c.eps, q_out=st["q_out"])
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for i in range(n_sets):
+            call(i)
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for i in range(n_sets):
+            call(i)
+    rounds = max(1, args.steps // n_sets)
+    for _ in range(max(1, args.warmup // n_sets)):
+        graph.replay()
+    torch.cuda.synchronize()
+    flags = pk.pkv_read_device_status()
+    if flags:
+        raise RuntimeError(f"device status flags {flags:#x} after warm-up")
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        a.record()
+        for _ in range(rounds):
+            graph.replay()
+        b.record()
+        torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / (rounds * n_sets)
+    if rank != 0:
+        return
+    T = c.qkv.shape[0]
+    nbytes = (T * (H + 2 * Hkv) * D * 2          # rows read
+              + T * D * 4                          # cos and sin rows read (f32, D/2 each)
+              + T * (H + 2 * Hkv) * D * 2)         # queries, keys and values written
+    peak, peak_kind = measured_peaks()
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": job_throughput(nbytes, world, ms), "unit": UNIT,
+        "n_gpus": world, "steps": rounds * n_sets, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD_DESC["qkv_prefill"], "launch": "CUDA graph, replayed",
+                   "l2": f"{n_sets} rotating input sets; {nbytes / 1e6:.0f} MB moved per call"},
+        "bytes_per_step": nbytes, "us_per_step": ms * 1e3,
+        "tokens_per_s": world * T / (ms * 1e-3),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": peak_kind,
+                     "kernel": "qkv_norm_rope_kernel (bytes read + written)", "traffic": None},
+        "clocks": clocks.summary(), "gpu_launches": rounds * n_sets,
+        "device_status_flags": pk.pkv_read_device_status(), "e2e": None, "cpu_baseline": None,
     }
     print(json.dumps(line), flush=True)
 
@@ -762,6 +855,9 @@ def main():
         ap.error("--warmup must be at least 3")
     if args.impl == "ours" and args.workload == "loop":
         run_loop(args)
+        return
+    if args.impl == "ours" and args.workload == "qkv_prefill":
+        run_qkv(args)
         return
     if args.impl == "ours" and args.workload in ("spec", "spec_long"):
         run_varlen(args)

@@ -48,6 +48,8 @@
 #include <math_constants.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "pagedkv.h"
 #include "ptx.cuh"
 
@@ -144,8 +146,8 @@ append_vllm_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
 // fused QKV split + per-head RMS norm + rotary embedding + paged append
 // ---------------------------------------------------------------------------
 //
-// One CTA per token, one warp per head (warps loop over the H + 2 Hkv heads
-// of the token's row [q heads | k heads | v heads]).  Token row r of sequence
+// One CTA per (token, group of 24 heads), four warps of six heads each,
+// over the token's row [q heads | k heads | v heads].  Token row r of sequence
 // s sits at position p = pos_offsets[s] + (r - cu_seqlens_q[s]), its rotary
 // position and its cache row.  Query and key heads are RMS-normalised when a
 // weight vector is given, then turned by the rotary angles of position p
@@ -178,13 +180,41 @@ struct QkvRopeParams {
   float eps;
 };
 
+// Heads per warp and per CTA of qkv_norm_rope_kernel (4 warps): a warp
+// issues the loads of all its heads before it works on any, so a CTA keeps
+// 24 heads' rows in flight (6 per warp measured faster than 4 or 8 on a
+// prefill-sized call).
+constexpr int kQkvHeadsPerWarp = 6;
+constexpr int kQkvHeadsPerCta = 4 * kQkvHeadsPerWarp;
+
 template <int D>
-__global__ void __launch_bounds__(256) qkv_norm_rope_kernel(const QkvRopeParams p) {
-  constexpr int PAIRS = D / 64;  // rotate-half pairs per lane
+__global__ void __launch_bounds__(128) qkv_norm_rope_kernel(const QkvRopeParams p) {
+  constexpr int HPW = kQkvHeadsPerWarp;
+  constexpr int PL = D / 64;  // rotate-half pairs per lane: i = PL * lane + k
+  using Raw = typename std::conditional<PL == 2, uint32_t, uint16_t>::type;
   pdl_launch_dependents();
   pdl_wait();
-  const int row = blockIdx.x;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int H = p.num_heads, Hkv = p.num_kv_heads;
+  const int heads = H + 2 * Hkv;
+  const int groups = (heads + kQkvHeadsPerCta - 1) / kQkvHeadsPerCta;
+  const int row = blockIdx.x / groups;
+  const int h0 = (blockIdx.x - row * groups) * kQkvHeadsPerCta + (threadIdx.x >> 5) * HPW;
+  const int lane = threadIdx.x & 31;
+  const int i0 = PL * lane;
+
+  // The row's loads depend on nothing but the block index: they go out
+  // first (raw bits, so value rows are copied exactly), and the sequence
+  // lookup runs while they are in flight.
+  const __half* x_row = p.qkv + (size_t)row * heads * D;
+  Raw ra[HPW], rb[HPW];
+#pragma unroll
+  for (int k = 0; k < HPW; ++k) {
+    const int hh = min(h0 + k, heads - 1);  // duplicates past the end are never stored
+    const Raw* x = reinterpret_cast<const Raw*>(x_row + (size_t)hh * D);
+    ra[k] = __ldg(x + lane);
+    rb[k] = __ldg(x + lane + D / (2 * PL));
+  }
+
   int lo = 0, hi = p.num_seqs - 1;  // last sequence whose first row is <= row
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -202,47 +232,58 @@ __global__ void __launch_bounds__(256) qkv_norm_rope_kernel(const QkvRopeParams 
     if (threadIdx.x == 0) atomicOr(&g_device_status, kDevBadContextLen);
     return;
   }
+  if (h0 >= heads) return;
   const int blk = __ldg(p.block_tables + (size_t)lo * p.max_blocks_per_seq + pos / p.block_size);
+  float cs[PL], sn[PL], wq[2][PL], wk[2][PL];
+#pragma unroll
+  for (int j = 0; j < PL; ++j) {
+    cs[j] = __ldg(p.cos_t + (size_t)pos * (D / 2) + i0 + j);
+    sn[j] = __ldg(p.sin_t + (size_t)pos * (D / 2) + i0 + j);
+    wq[0][j] = p.q_norm_w ? __half2float(p.q_norm_w[i0 + j]) : 1.f;
+    wq[1][j] = p.q_norm_w ? __half2float(p.q_norm_w[i0 + j + D / 2]) : 1.f;
+    wk[0][j] = p.k_norm_w ? __half2float(p.k_norm_w[i0 + j]) : 1.f;
+    wk[1][j] = p.k_norm_w ? __half2float(p.k_norm_w[i0 + j + D / 2]) : 1.f;
+  }
   const bool blk_ok = blk >= 0 && blk < p.num_blocks;
   if (!blk_ok && threadIdx.x == 0) atomicOr(&g_device_status, kDevBadBlockId);
   const int off = pos - (pos / p.block_size) * p.block_size;
 
-  const int H = p.num_heads, Hkv = p.num_kv_heads;
-  const __half* x_row = p.qkv + (size_t)row * (H + 2 * Hkv) * D;
-  const float* cs = p.cos_t + (size_t)pos * (D / 2);
-  const float* sn = p.sin_t + (size_t)pos * (D / 2);
-  for (int hh = warp; hh < H + 2 * Hkv; hh += 8) {
-    const __half* x = x_row + (size_t)hh * D;
-    float a[PAIRS], b[PAIRS];
 #pragma unroll
-    for (int j = 0; j < PAIRS; ++j) {
-      a[j] = __half2float(x[lane + 32 * j]);
-      b[j] = __half2float(x[lane + 32 * j + D / 2]);
-    }
-    if (hh >= H + Hkv) {  // value head: copied into the pool
-      if (blk_ok) {
-        __half* dst = p.v_cache + (((size_t)blk * Hkv + (hh - H - Hkv)) * p.block_size + off) * D;
-#pragma unroll
-        for (int j = 0; j < PAIRS; ++j) {
-          dst[lane + 32 * j] = x[lane + 32 * j];
-          dst[lane + 32 * j + D / 2] = x[lane + 32 * j + D / 2];
-        }
-      }
+  for (int k = 0; k < HPW; ++k) {
+    const int hh = h0 + k;
+    if (hh >= heads) break;
+    if (hh >= H + Hkv) {  // value head: copied into the pool, bit for bit
+      if (!blk_ok) continue;
+      Raw* dst = reinterpret_cast<Raw*>(
+          p.v_cache + (((size_t)blk * Hkv + (hh - H - Hkv)) * p.block_size + off) * D);
+      dst[lane] = ra[k];
+      dst[lane + D / (2 * PL)] = rb[k];
       continue;
     }
+    float a[PL], b[PL];
+    if (PL == 2) {
+      const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&ra[k]));
+      const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&rb[k]));
+      a[0] = fa.x;
+      a[PL - 1] = fa.y;
+      b[0] = fb.x;
+      b[PL - 1] = fb.y;
+    } else {
+      a[0] = __half2float(*reinterpret_cast<const __half*>(&ra[k]));
+      b[0] = __half2float(*reinterpret_cast<const __half*>(&rb[k]));
+    }
     const bool is_q = hh < H;
-    const __half* w = is_q ? p.q_norm_w : p.k_norm_w;
-    if (w != nullptr) {
+    if (is_q ? p.q_norm_w != nullptr : p.k_norm_w != nullptr) {
       float ss = 0.f;
 #pragma unroll
-      for (int j = 0; j < PAIRS; ++j) ss += a[j] * a[j] + b[j] * b[j];
+      for (int j = 0; j < PL; ++j) ss += a[j] * a[j] + b[j] * b[j];
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-      const float r = rsqrtf(ss / (float)D + p.eps);
+      const float rr = rsqrtf(ss / (float)D + p.eps);
 #pragma unroll
-      for (int j = 0; j < PAIRS; ++j) {
-        a[j] = a[j] * r * __half2float(w[lane + 32 * j]);
-        b[j] = b[j] * r * __half2float(w[lane + 32 * j + D / 2]);
+      for (int j = 0; j < PL; ++j) {
+        a[j] = a[j] * rr * (is_q ? wq[0][j] : wk[0][j]);
+        b[j] = b[j] * rr * (is_q ? wq[1][j] : wk[1][j]);
       }
     }
     __half* dst;
@@ -252,12 +293,18 @@ __global__ void __launch_bounds__(256) qkv_norm_rope_kernel(const QkvRopeParams 
       if (!blk_ok) continue;
       dst = p.k_cache + (((size_t)blk * Hkv + (hh - H)) * p.block_size + off) * D;
     }
+    float oa[PL], ob[PL];
 #pragma unroll
-    for (int j = 0; j < PAIRS; ++j) {
-      const int i = lane + 32 * j;
-      const float c = __ldg(cs + i), sv = __ldg(sn + i);
-      dst[i] = __float2half_rn(a[j] * c - b[j] * sv);
-      dst[i + D / 2] = __float2half_rn(b[j] * c + a[j] * sv);
+    for (int j = 0; j < PL; ++j) {
+      oa[j] = a[j] * cs[j] - b[j] * sn[j];
+      ob[j] = b[j] * cs[j] + a[j] * sn[j];
+    }
+    if (PL == 2) {
+      *reinterpret_cast<__half2*>(dst + i0) = __floats2half2_rn(oa[0], oa[PL - 1]);
+      *reinterpret_cast<__half2*>(dst + i0 + D / 2) = __floats2half2_rn(ob[0], ob[PL - 1]);
+    } else {
+      dst[i0] = __float2half_rn(oa[0]);
+      dst[i0 + D / 2] = __float2half_rn(ob[0]);
     }
   }
 }

@@ -922,7 +922,7 @@ pkv_status pkv_qkv_norm_rope_append(const void* qkv, const void* q_norm_w, const
   if ((long long)num_blocks * block_size >= (1ll << 31) ||
       (long long)max_blocks_per_seq * block_size >= (1ll << 31))
     return fail(PKV_ERR_INVALID_ARG, "pool or table too large for 32-bit positions");
-  if (!aligned(qkv, 2) || !aligned(q_out, 2) || !aligned(k_cache, 2) || !aligned(v_cache, 2) ||
+  if (!aligned(qkv, 4) || !aligned(q_out, 4) || !aligned(k_cache, 4) || !aligned(v_cache, 4) ||
       (q_norm_w && !aligned(q_norm_w, 2)) || (k_norm_w && !aligned(k_norm_w, 2)) ||
       !aligned(cos_table, 4) || !aligned(sin_table, 4) || !aligned(cu_seqlens_q, 4) ||
       !aligned(pos_offsets, 4) || !aligned(block_tables, 4))
@@ -950,9 +950,12 @@ pkv_status pkv_qkv_norm_rope_append(const void* qkv, const void* q_norm_w, const
   qp.max_pos = max_pos;
   qp.eps = eps;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const int groups = (num_heads + 2 * num_kv_heads + kQkvHeadsPerCta - 1) / kQkvHeadsPerCta;
+  if ((long long)total_q * groups >= (1ll << 31)) return fail(PKV_ERR_INVALID_ARG, "grid too large");
+  const int grid = total_q * groups;
   const cudaError_t e = head_dim == 128
-                            ? launch_pdl(qkv_norm_rope_kernel<128>, total_q, 256, 0, cs, qp)
-                            : launch_pdl(qkv_norm_rope_kernel<64>, total_q, 256, 0, cs, qp);
+                            ? launch_pdl(qkv_norm_rope_kernel<128>, grid, 128, 0, cs, qp)
+                            : launch_pdl(qkv_norm_rope_kernel<64>, grid, 128, 0, cs, qp);
   if (e != cudaSuccess) return cuda_fail(e, "qkv norm/rope/append launch");
   return PKV_OK;
 }

@@ -297,7 +297,7 @@ def test_qkv_norm_rope_rejects_bad_arguments(pk):
     assert call(max_pos=0) == -1
     assert call(eps=-1.0) == -1
     assert call(eps=float("nan")) == -1
-    assert call(qkv=F16 + 1) == -1            # misaligned f16
+    assert call(qkv=F16 + 2) == -1            # 2-byte aligned only: half2 loads need 4
     assert call(cos=F16 + 2) == -1            # misaligned f32
     assert call(T=0) == 0                      # no rows: nothing launched
     assert call(B=0) == 0

@@ -146,7 +146,7 @@ append_vllm_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
 // fused QKV split + per-head RMS norm + rotary embedding + paged append
 // ---------------------------------------------------------------------------
 //
-// One CTA per (token, group of 24 heads), four warps of six heads each,
+// One CTA per (token, group of 24 heads) (grid x, y), four warps of six heads each,
 // over the token's row [q heads | k heads | v heads].  Token row r of sequence
 // s sits at position p = pos_offsets[s] + (r - cu_seqlens_q[s]), its rotary
 // position and its cache row.  Query and key heads are RMS-normalised when a
@@ -187,7 +187,7 @@ struct QkvRopeParams {
 constexpr int kQkvHeadsPerWarp = 6;
 constexpr int kQkvHeadsPerCta = 4 * kQkvHeadsPerWarp;
 
-template <int D>
+template <int D, int BS>
 __global__ void __launch_bounds__(128) qkv_norm_rope_kernel(const QkvRopeParams p) {
   constexpr int HPW = kQkvHeadsPerWarp;
   constexpr int PL = D / 64;  // rotate-half pairs per lane: i = PL * lane + k
@@ -196,9 +196,8 @@ __global__ void __launch_bounds__(128) qkv_norm_rope_kernel(const QkvRopeParams 
   pdl_wait();
   const int H = p.num_heads, Hkv = p.num_kv_heads;
   const int heads = H + 2 * Hkv;
-  const int groups = (heads + kQkvHeadsPerCta - 1) / kQkvHeadsPerCta;
-  const int row = blockIdx.x / groups;
-  const int h0 = (blockIdx.x - row * groups) * kQkvHeadsPerCta + (threadIdx.x >> 5) * HPW;
+  const int row = blockIdx.x;  // grid: x = token row, y = group of heads
+  const int h0 = blockIdx.y * kQkvHeadsPerCta + (threadIdx.x >> 5) * HPW;
   const int lane = threadIdx.x & 31;
   const int i0 = PL * lane;
 
@@ -226,14 +225,14 @@ __global__ void __launch_bounds__(128) qkv_norm_rope_kernel(const QkvRopeParams 
   const int q_begin = __ldg(p.cu_seqlens_q + lo);
   const int q_end = __ldg(p.cu_seqlens_q + lo + 1);
   const int pos = __ldg(p.pos_offsets + lo) + (row - q_begin);
-  const int cap = p.max_blocks_per_seq * p.block_size;
+  const int cap = p.max_blocks_per_seq * BS;
   if (q_begin < 0 || q_end > p.total_q || row < q_begin || row >= q_end || pos < 0 ||
       pos >= p.max_pos || pos >= cap) {
     if (threadIdx.x == 0) atomicOr(&g_device_status, kDevBadContextLen);
     return;
   }
   if (h0 >= heads) return;
-  const int blk = __ldg(p.block_tables + (size_t)lo * p.max_blocks_per_seq + pos / p.block_size);
+  const int blk = __ldg(p.block_tables + (size_t)lo * p.max_blocks_per_seq + pos / BS);
   float cs[PL], sn[PL], wq[2][PL], wk[2][PL];
 #pragma unroll
   for (int j = 0; j < PL; ++j) {
@@ -246,7 +245,7 @@ __global__ void __launch_bounds__(128) qkv_norm_rope_kernel(const QkvRopeParams 
   }
   const bool blk_ok = blk >= 0 && blk < p.num_blocks;
   if (!blk_ok && threadIdx.x == 0) atomicOr(&g_device_status, kDevBadBlockId);
-  const int off = pos - (pos / p.block_size) * p.block_size;
+  const int off = pos % BS;
 
 #pragma unroll
   for (int k = 0; k < HPW; ++k) {
@@ -255,7 +254,7 @@ __global__ void __launch_bounds__(128) qkv_norm_rope_kernel(const QkvRopeParams 
     if (hh >= H + Hkv) {  // value head: copied into the pool, bit for bit
       if (!blk_ok) continue;
       Raw* dst = reinterpret_cast<Raw*>(
-          p.v_cache + (((size_t)blk * Hkv + (hh - H - Hkv)) * p.block_size + off) * D);
+          p.v_cache + (((size_t)blk * Hkv + (hh - H - Hkv)) * BS + off) * D);
       dst[lane] = ra[k];
       dst[lane + D / (2 * PL)] = rb[k];
       continue;
@@ -291,7 +290,7 @@ __global__ void __launch_bounds__(128) qkv_norm_rope_kernel(const QkvRopeParams 
       dst = p.q_out + ((size_t)row * H + hh) * D;
     } else {
       if (!blk_ok) continue;
-      dst = p.k_cache + (((size_t)blk * Hkv + (hh - H)) * p.block_size + off) * D;
+      dst = p.k_cache + (((size_t)blk * Hkv + (hh - H)) * BS + off) * D;
     }
     float oa[PL], ob[PL];
 #pragma unroll

@@ -67,10 +67,10 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 // start while the previous kernel in the stream finishes; every kernel here
 // waits for it (griddepcontrol.wait) before touching global memory.
 template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kernel)(KArgs...), int grid, int block, size_t smem,
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, int block, size_t smem,
                        cudaStream_t stream, Args&&... args) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.gridDim = grid;
   cfg.blockDim = dim3((unsigned)block, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
@@ -951,11 +951,15 @@ pkv_status pkv_qkv_norm_rope_append(const void* qkv, const void* q_norm_w, const
   qp.eps = eps;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const int groups = (num_heads + 2 * num_kv_heads + kQkvHeadsPerCta - 1) / kQkvHeadsPerCta;
-  if ((long long)total_q * groups >= (1ll << 31)) return fail(PKV_ERR_INVALID_ARG, "grid too large");
-  const int grid = total_q * groups;
-  const cudaError_t e = head_dim == 128
-                            ? launch_pdl(qkv_norm_rope_kernel<128>, grid, 128, 0, cs, qp)
-                            : launch_pdl(qkv_norm_rope_kernel<64>, grid, 128, 0, cs, qp);
+  if (groups > 65535) return fail(PKV_ERR_INVALID_ARG, "too many heads");
+  const dim3 grid((unsigned)total_q, (unsigned)groups, 1);  // x: token, y: group of heads
+  cudaError_t e;
+  if (head_dim == 128)
+    e = block_size == 16 ? launch_pdl(qkv_norm_rope_kernel<128, 16>, grid, 128, 0, cs, qp)
+                         : launch_pdl(qkv_norm_rope_kernel<128, 32>, grid, 128, 0, cs, qp);
+  else
+    e = block_size == 16 ? launch_pdl(qkv_norm_rope_kernel<64, 16>, grid, 128, 0, cs, qp)
+                         : launch_pdl(qkv_norm_rope_kernel<64, 32>, grid, 128, 0, cs, qp);
   if (e != cudaSuccess) return cuda_fail(e, "qkv norm/rope/append launch");
   return PKV_OK;
 }

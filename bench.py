@@ -60,6 +60,11 @@ WORKLOAD_DESC = {
     "qkv_prefill": ("fused QKV split + per-head RMS norm + rotary + paged append on the "
                     "Llama-3-8B attention shape: 4 sequences x 2048 new tokens (H=32, Hkv=8, "
                     "D=128, bs=16), f16 rows ~N(0,1) (pkv_qkv_norm_rope_append)"),
+    "step_qkv": ("a whole attention step on the Llama-3-8B decode workload: the 32 new "
+                 "tokens' fused QKV rows (RMS-normed q/k heads, rotary at position L-1, "
+                 "keys/values appended) and the decode over the grown contexts, in one call "
+                 "(pkv_qkv_norm_rope_append_decode); the two-launch form "
+                 "(pkv_qkv_norm_rope_append then pkv_decode_splitk) timed beside it"),
     "loop": ("append+decode loop: MHA H=Hkv=16, D=64, bs=16, B=128, start context U[64,4096], "
              "128 steps of pkv_append (142 rows, 14 padding slots = -1, new blocks from a "
              "shuffled free list of 40000) then pkv_decode_splitk on one stream"),
@@ -385,6 +390,117 @@ def run_qkv(args):
                      "frac": achieved / peak, "peak_source": peak_kind,
                      "kernel": "qkv_norm_rope_kernel (bytes read + written)", "traffic": None},
         "clocks": clocks.summary(), "gpu_launches": rounds * n_sets,
+        "device_status_flags": pk.pkv_read_device_status(), "e2e": None, "cpu_baseline": None,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_step_qkv(args):
+    """A whole attention step: the fused QKV split + norm + rotary + append of
+    each sequence's new token, then the decode (two launches), timed as a
+    graph of steps over rotating pool sets; the decode alone is timed beside
+    it."""
+    import numpy as np
+    import torch
+
+    from paged_kv_decode_08_gb300 import pagedkv as pk
+    from paged_kv_decode_08_gb300 import workloads as W
+
+    world, rank, local = dist_setup()
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    w = W.make("llama8b")
+    n_sets = args.sets
+    sets = build_sets(w, dev, n_sets)
+    lens = w.context_lens.astype(np.int64)
+    c = W.qkv_case(BASE_QKV_SEED + 1, w.num_heads, w.num_kv_heads, w.head_dim, w.block_size,
+                   [1] * w.num_seqs, (lens - 1).tolist())
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    qkv, qw, kw, cos, sin = t(c.qkv), t(c.q_norm_w), t(c.k_norm_w), t(c.cos), t(c.sin)
+    cu, pos = t(c.cu_seqlens_q), t(c.pos_offsets)
+    bt, cl = sets[0]["block_tables"], sets[0]["context_lens"]
+    q = torch.empty((w.num_seqs, w.num_heads, w.head_dim), dtype=torch.float16, device=dev)
+    out = torch.empty_like(q)
+    S = pk.splits_for(q, sets[0]["k_cache"], bt, args.splits)
+    scratch = pk.alloc_scratch(q, sets[0]["k_cache"], bt, args.splits)
+
+    def step(i):
+        st = sets[i % n_sets]
+        pk.pkv_qkv_norm_rope_append(qkv, qw, kw, cos, sin, st["k_cache"], st["v_cache"], cu, pos,
+                                    bt, w.num_heads, eps=c.eps, q_out=q)
+        pk.pkv_decode_splitk(q, st["k_cache"], st["v_cache"], bt, cl, w.scale,
+                             num_splits=args.splits, scratch=scratch, out=out)
+
+    def fused(i):
+        st = sets[i % n_sets]
+        pk.pkv_qkv_norm_rope_append_decode(qkv, qw, kw, cos, sin, st["k_cache"], st["v_cache"],
+                                           bt, cl, w.num_heads, w.scale, eps=c.eps,
+                                           num_splits=args.splits, scratch=scratch, out=out)
+
+    def decode_only(i):
+        st = sets[i % n_sets]
+        pk.pkv_decode_splitk(q, st["k_cache"], st["v_cache"], bt, cl, w.scale,
+                             num_splits=args.splits, scratch=scratch, out=out)
+
+    def capture(fn):
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for i in range(n_sets):
+                fn(i)
+        torch.cuda.current_stream().wait_stream(side)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(n_sets):
+                fn(i)
+        return g
+
+    g_step, g_fused, g_dec = capture(step), capture(fused), capture(decode_only)
+    rounds = max(1, args.steps // n_sets)
+    for _ in range(max(1, args.warmup // n_sets)):
+        g_step.replay()
+        g_fused.replay()
+        g_dec.replay()
+    torch.cuda.synchronize()
+    flags = pk.pkv_read_device_status()
+    if flags:
+        raise RuntimeError(f"device status flags {flags:#x} after warm-up")
+
+    def timed(g):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(rounds):
+            g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / (rounds * n_sets)
+
+    with ClockSampler(local) as clocks:
+        two_ms = timed(g_step)
+        ms = timed(g_fused)
+        dec_ms = timed(g_dec)
+    if rank != 0:
+        return
+    kv_bytes = w.kv_bytes
+    peak, peak_kind = measured_peaks()
+    achieved = kv_bytes / (dec_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": job_throughput(kv_bytes, world, ms), "unit": UNIT,
+        "n_gpus": world, "steps": rounds * n_sets, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD_DESC["step_qkv"], "num_splits": S,
+                   "launch": f"CUDA graph of {n_sets} steps, replayed",
+                   "l2": f"{n_sets} rotating pool sets"},
+        "kv_bytes_per_step": kv_bytes, "us_per_step": ms * 1e3,
+        "two_launch_us_per_step": two_ms * 1e3, "decode_us_per_call": dec_ms * 1e3,
+        "decode_tokens_per_s": world * w.num_seqs / (ms * 1e-3),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": peak_kind,
+                     "kernel": "the decode call alone (the fused step's attention part)",
+                     "traffic": None},
+        "clocks": clocks.summary(), "gpu_launches": rounds * n_sets * (1 + (S > 1)),
         "device_status_flags": pk.pkv_read_device_status(), "e2e": None, "cpu_baseline": None,
     }
     print(json.dumps(line), flush=True)
@@ -855,6 +971,9 @@ def main():
         ap.error("--warmup must be at least 3")
     if args.impl == "ours" and args.workload == "loop":
         run_loop(args)
+        return
+    if args.impl == "ours" and args.workload == "step_qkv":
+        run_step_qkv(args)
         return
     if args.impl == "ours" and args.workload == "qkv_prefill":
         run_qkv(args)

@@ -386,6 +386,45 @@ pkv_status pkv_qkv_norm_rope_append(const void* qkv, const void* q_norm_w, const
                                     void* stream);
 
 /*
+ * pkv_qkv_norm_rope_append_decode — a whole decode attention step in one
+ * launch (two with splits): pkv_qkv_norm_rope_append of each sequence's
+ * newest token (one row per sequence, at position context_lens[s] - 1)
+ * followed by the decode of pkv_decode_splitk with the rotated queries.  The
+ * decode CTA of (sequence, KV head[, split]) computes its group's queries
+ * itself; the CTA whose chunk holds the newest position computes that KV
+ * head's key and value row, writes it to the pools and attends to it
+ * directly (ferrum-kernels src/backend/cuda/paged.rs,
+ * split_qkv_norm_rope_into_paged_cache then paged_decode_attention, the
+ * per-layer order of one decode step).
+ *
+ *   qkv           device f16 [num_seqs][(num_heads + 2 num_kv_heads) * head_dim],
+ *                 4-byte aligned: sequence s's newest token's projection row
+ *   q_norm_w, k_norm_w, cos_table, sin_table, eps  as
+ *                 pkv_qkv_norm_rope_append
+ *   max_pos       rows in the rotary tables; a sequence with
+ *                 context_lens[s] > max_pos sets PKV_DEV_BAD_CONTEXT_LEN,
+ *                 appends nothing and attends with zero queries (its output
+ *                 is written but meaningless)
+ *   k_cache, v_cache  the pools (blocked layout), read and written in place
+ *   other arguments as pkv_decode_splitk (num_splits = PKV_SPLITS_BALANCED
+ *   returns PKV_ERR_UNSUPPORTED)
+ *
+ * The cache ends as pkv_qkv_norm_rope_append would leave it (the key and
+ * value rows of position context_lens[s] - 1 written) and out holds the
+ * attention of the rotated queries over every context including the new
+ * rows.  The queries are not written out.  A table entry outside
+ * [0, num_blocks) at the newest position sets PKV_DEV_BAD_SLOT and the row
+ * is neither written nor used (the decode flags the tile as well).
+ */
+pkv_status pkv_qkv_norm_rope_append_decode(
+    const void* qkv, const void* q_norm_w, const void* k_norm_w, const float* cos_table,
+    const float* sin_table, int32_t max_pos, float eps, void* k_cache, void* v_cache,
+    const int32_t* block_tables, const int32_t* context_lens, int32_t num_seqs,
+    int32_t max_blocks_per_seq, int32_t num_blocks, float scale, int32_t num_heads,
+    int32_t num_kv_heads, int32_t head_dim, int32_t block_size, void* out, int32_t num_splits,
+    void* scratch, size_t scratch_bytes, void* stream);
+
+/*
  * pkv_selftest_wait_timeout — a diagnostic of the failure path (the pages
  * have no counterpart): launches one warp that waits on a barrier nothing
  * arrives on.  The bounded wait gives up after 100 ms and sets

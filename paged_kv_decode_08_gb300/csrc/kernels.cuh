@@ -341,6 +341,18 @@ struct DecodeParams {
   const int32_t* new_slots;  // [B]
   __half* k_cache;           // the pools, for the row writes
   __half* v_cache;
+  // Fused QKV step (pkv_qkv_rope_append_decode; QKV kernels only): sequence
+  // s's newest token (position context_lens[s] - 1) comes as its fused
+  // projection row; the kernel norms and rotates its query and key heads
+  // (as qkv_norm_rope_kernel does), attends with the queries and appends
+  // the key and value rows.
+  const __half* qkv;       // [B][(H + 2 Hkv) D]
+  const __half* q_norm_w;  // [D] or null
+  const __half* k_norm_w;  // [D] or null
+  const float* cos_t;      // [max_pos][D/2]
+  const float* sin_t;
+  int max_pos;
+  float eps;
 };
 
 template <int D, int BS, int W, int P>
@@ -434,6 +446,82 @@ struct WarpState {
     }
   }
 };
+
+// One query or key head of a fused projection row, RMS-normed over its D
+// elements when `w` is given and turned by the rotary angles of one position
+// (rotate-half pairs (i, i + D/2); f32, rounded once to f16), in the pair
+// layout of qkv_norm_rope_kernel: lane holds elements PL*lane .. +PL and the
+// same + D/2, returned packed (PL = 2: one half2 word each; PL = 1: one half
+// in the low bits).  All lanes of the warp take part.
+template <int D>
+__device__ __forceinline__ void norm_rotate_head(const __half* x, const __half* w,
+                                                 const float* cs_row, const float* sn_row,
+                                                 float eps, int lane, uint32_t& lo, uint32_t& hi) {
+  constexpr int PL = D / 64;
+  const int i0 = PL * lane;
+  float a[PL], b[PL];
+#pragma unroll
+  for (int j = 0; j < PL; ++j) {
+    a[j] = __half2float(x[i0 + j]);
+    b[j] = __half2float(x[i0 + j + D / 2]);
+  }
+  if (w != nullptr) {
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < PL; ++j) ss += a[j] * a[j] + b[j] * b[j];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float rr = rsqrtf(ss / (float)D + eps);
+#pragma unroll
+    for (int j = 0; j < PL; ++j) {
+      a[j] = a[j] * rr * __half2float(w[i0 + j]);
+      b[j] = b[j] * rr * __half2float(w[i0 + j + D / 2]);
+    }
+  }
+  float oa[PL], ob[PL];
+#pragma unroll
+  for (int j = 0; j < PL; ++j) {
+    const float c = __ldg(cs_row + i0 + j), sv = __ldg(sn_row + i0 + j);
+    oa[j] = a[j] * c - b[j] * sv;
+    ob[j] = b[j] * c + a[j] * sv;
+  }
+  if (PL == 2) {
+    lo = pack_half2(__floats2half2_rn(oa[0], oa[PL - 1]));
+    hi = pack_half2(__floats2half2_rn(ob[0], ob[PL - 1]));
+  } else {
+    lo = (uint32_t)__half_as_ushort(__float2half_rn(oa[0]));
+    hi = (uint32_t)__half_as_ushort(__float2half_rn(ob[0]));
+  }
+}
+
+// Stores a head in the pair layout (see norm_rotate_head) at `dst` (global).
+template <int D>
+__device__ __forceinline__ void store_pairs(__half* dst, int lane, uint32_t lo, uint32_t hi) {
+  constexpr int PL = D / 64;
+  const int i0 = PL * lane;
+  if (PL == 2) {
+    *reinterpret_cast<uint32_t*>(dst + i0) = lo;
+    *reinterpret_cast<uint32_t*>(dst + i0 + D / 2) = hi;
+  } else {
+    dst[i0] = __ushort_as_half((unsigned short)lo);
+    dst[i0 + D / 2] = __ushort_as_half((unsigned short)hi);
+  }
+}
+
+// Q^T fragments from query heads held in shared memory [8][D] (heads at or
+// past `group` are zero), same layout as load_q_frags.
+template <int D>
+__device__ __forceinline__ void load_q_frags_smem(uint32_t (&qf)[D / 16][2], const __half* sq,
+                                                  int group, int lane) {
+  const int r = lane >> 2, c = lane & 3;
+  const bool live = r < group;
+  const uint32_t* qrow = reinterpret_cast<const uint32_t*>(sq + (live ? r : 0) * D);
+#pragma unroll
+  for (int ks = 0; ks < D / 16; ++ks) {
+    qf[ks][0] = live ? qrow[ks * 8 + c] : 0u;
+    qf[ks][1] = live ? qrow[ks * 8 + 4 + c] : 0u;
+  }
+}
 
 // Q^T fragments (B operand): column n = lane/4 is query head `head0 + n`;
 // columns at or past `group` are zero.
@@ -677,17 +765,19 @@ __device__ __forceinline__ void issue_tile_copy(uint32_t kdst, uint32_t bar, int
 
 // VLLM: the pools are in the vLLM layout (p.k_cache is the K pool; kmap is
 // unused); no fused append.
-template <int D, int BS, int W, int P, bool SPLIT, bool FUSE, bool VLLM = false>
+template <int D, int BS, int W, int P, bool SPLIT, bool FUSE, bool VLLM = false, bool QKV = false>
 __global__ void __launch_bounds__(W * 32)
 paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
   static_assert(!(FUSE && VLLM), "the fused append writes the blocked layout only");
+  static_assert(!(QKV && (FUSE || VLLM)), "the fused QKV step is its own variant");
   using Shape = DecodeShape<D, BS, W, P>;
   constexpr int KS = Shape::kKS;
   constexpr int TB = Shape::kTileBytes;
 
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_failed;
+  __shared__ __align__(16) __half s_q[QKV ? 8 * D : 2];  // QKV: the group's rotated queries
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t ring = smem_addr(smem);
@@ -745,6 +835,11 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     if (threadIdx.x == 0) atomicOr(&g_device_status, kDevBadContextLen);
     L = L < 0 ? 0 : cap;
   }
+  // QKV: a newest position without rotary angles is flagged; the sequence
+  // then attends with zero queries and appends nothing (its output is
+  // written but meaningless).
+  const bool qkv_bad = QKV && L > p.max_pos;
+  if (qkv_bad && threadIdx.x == 0) atomicOr(&g_device_status, kDevBadContextLen);
   int tok_begin = 0;
   int tok_end = L;
   if (SPLIT) {
@@ -779,16 +874,25 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   constexpr int HPL = D / 32;  // halves per lane of one row
   int fuse_li = -1;            // local tile index of the new row, in its owner warp
   int fuse_row = 0;
+  int fuse_phys = 0;           // QKV: its physical block
   uint32_t kn[HPL / 2], vn[HPL / 2];
-  if (FUSE && L > 0 && L - 1 >= tok_begin && L - 1 < tok_end && slot_new >= 0) {
+  if ((FUSE || QKV) && !qkv_bad && L > 0 && L - 1 >= tok_begin && L - 1 < tok_end &&
+      (QKV || slot_new >= 0)) {
     const int pos = L - 1;
     const int phys = __ldg(table + pos / BS);
-    const bool ok = phys >= 0 && phys < p.num_blocks && slot_new == phys * BS + pos % BS;
+    const bool ok = phys >= 0 && phys < p.num_blocks && (QKV || slot_new == phys * BS + pos % BS);
     if (!ok) {
       if (threadIdx.x == 0) atomicOr(&g_device_status, kDevBadSlot);
     } else {
       const int idx = pos / BS - blk_begin;  // tile within the chunk
-      if (warp == idx % WE) {
+      if (QKV) {
+        // the rows are computed after the first copies are issued (below)
+        if (warp == idx % WE) {
+          fuse_li = idx / WE;
+          fuse_row = pos % BS;
+          fuse_phys = phys;
+        }
+      } else if (warp == idx % WE) {
         fuse_li = idx / WE;
         fuse_row = pos % BS;
         const size_t src = ((size_t)s * p.num_kv_heads + g) * D + lane * HPL;
@@ -828,7 +932,48 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   }
 
   uint32_t qf[KS][2];
-  load_q_frags<D>(qf, p.q, (size_t)s * p.num_heads + (size_t)g * p.group, p.group, lane);
+  uint32_t qk_lo = 0, qk_hi = 0, qv_lo = 0, qv_hi = 0;  // QKV: the new key / value row
+  if (QKV) {
+    // With the first copies in flight: the group's queries (norm + rotary at
+    // position L-1) into shared memory, and in the owner warp the new key and
+    // value rows, written to the pools now and into the tile when it lands.
+    if (L > 0 && !qkv_bad) {
+      const int pos = L - 1;
+      const int H = p.num_heads, Hkv = p.num_kv_heads;
+      const __half* row = p.qkv + (size_t)s * (H + 2 * Hkv) * D;
+      const float* cs = p.cos_t + (size_t)pos * (D / 2);
+      const float* sn = p.sin_t + (size_t)pos * (D / 2);
+      for (int h = warp; h < p.group; h += W) {
+        uint32_t lo, hi;
+        norm_rotate_head<D>(row + (size_t)(g * p.group + h) * D, p.q_norm_w, cs, sn, p.eps, lane,
+                            lo, hi);
+        store_pairs<D>(s_q + h * D, lane, lo, hi);
+      }
+      if (fuse_li >= 0) {
+        norm_rotate_head<D>(row + (size_t)(H + g) * D, p.k_norm_w, cs, sn, p.eps, lane, qk_lo,
+                            qk_hi);
+        constexpr int PL = D / 64;
+        const __half* xv = row + (size_t)(H + Hkv + g) * D;
+        if (PL == 2) {
+          qv_lo = *reinterpret_cast<const uint32_t*>(xv + 2 * lane);
+          qv_hi = *reinterpret_cast<const uint32_t*>(xv + 2 * lane + D / 2);
+        } else {
+          qv_lo = __half_as_ushort(xv[lane]);
+          qv_hi = __half_as_ushort(xv[lane + D / 2]);
+        }
+        const size_t dst = (((size_t)fuse_phys * Hkv + g) * BS + fuse_row) * D;
+        store_pairs<D>(p.k_cache + dst, lane, qk_lo, qk_hi);
+        store_pairs<D>(p.v_cache + dst, lane, qv_lo, qv_hi);
+      }
+    } else {
+      for (int i = threadIdx.x; i < 8 * D / 2; i += W * 32)
+        reinterpret_cast<uint32_t*>(s_q)[i] = 0u;
+    }
+    __syncthreads();
+    load_q_frags_smem<D>(qf, s_q, p.group, lane);
+  } else {
+    load_q_frags<D>(qf, p.q, (size_t)s * p.num_heads + (size_t)g * p.group, p.group, lane);
+  }
 
   WarpState<D> st;
   st.reset();
@@ -846,6 +991,23 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     const int phys = __ldg(table + j);
     if (phys >= 0 && phys < p.num_blocks) {
       const uint32_t kb = k_stage(stage);
+      if (QKV && li == fuse_li) {
+        // the new row of this tile is the one computed above, not the copy
+        constexpr int PL = D / 64;
+        const int i0 = PL * lane;
+        if (PL == 2) {
+          asm volatile("st.shared.u32 [%0], %1;" ::"r"(kb + swz<BS>(fuse_row, i0)), "r"(qk_lo) : "memory");
+          asm volatile("st.shared.u32 [%0], %1;" ::"r"(kb + swz<BS>(fuse_row, i0 + D / 2)), "r"(qk_hi) : "memory");
+          asm volatile("st.shared.u32 [%0], %1;" ::"r"(kb + TB + swz<BS>(fuse_row, i0)), "r"(qv_lo) : "memory");
+          asm volatile("st.shared.u32 [%0], %1;" ::"r"(kb + TB + swz<BS>(fuse_row, i0 + D / 2)), "r"(qv_hi) : "memory");
+        } else {
+          asm volatile("st.shared.u16 [%0], %1;" ::"r"(kb + swz<BS>(fuse_row, i0)), "h"((unsigned short)qk_lo) : "memory");
+          asm volatile("st.shared.u16 [%0], %1;" ::"r"(kb + swz<BS>(fuse_row, i0 + D / 2)), "h"((unsigned short)qk_hi) : "memory");
+          asm volatile("st.shared.u16 [%0], %1;" ::"r"(kb + TB + swz<BS>(fuse_row, i0)), "h"((unsigned short)qv_lo) : "memory");
+          asm volatile("st.shared.u16 [%0], %1;" ::"r"(kb + TB + swz<BS>(fuse_row, i0 + D / 2)), "h"((unsigned short)qv_hi) : "memory");
+        }
+        __syncwarp();
+      }
       if (FUSE && li == fuse_li) {
         // the new row of this tile comes from the step's k/v, not the copy
 #pragma unroll

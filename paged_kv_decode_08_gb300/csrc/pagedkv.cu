@@ -213,13 +213,13 @@ struct Tuning {
                                : 1;
 };
 
-template <int D, int BS, bool SPLIT, bool FUSE, bool VLLM>
+template <int D, int BS, bool SPLIT, bool FUSE, bool VLLM, bool QKV = false>
 pkv_status launch_decode(const DecodeArgs& a, const DecodeParams& prm, cudaStream_t stream,
                          int grid) {
   constexpr int W = Tuning<D, BS>::W;
   constexpr int P = Tuning<D, BS>::P;
   using Shape = DecodeShape<D, BS, W, P>;
-  auto kernel = paged_decode_kernel<D, BS, W, P, SPLIT, FUSE, VLLM>;
+  auto kernel = paged_decode_kernel<D, BS, W, P, SPLIT, FUSE, VLLM, QKV>;
 
   static std::atomic<unsigned long long> attr_set{0};
   int dev = 0;
@@ -256,25 +256,26 @@ pkv_status launch_decode(const DecodeArgs& a, const DecodeParams& prm, cudaStrea
   return PKV_OK;
 }
 
-template <bool SPLIT, bool FUSE, bool VLLM>
+template <bool SPLIT, bool FUSE, bool VLLM, bool QKV = false>
 pkv_status dispatch_decode_f(const DecodeArgs& a, const DecodeParams& prm, cudaStream_t stream,
                              int grid) {
   if (a.head_dim == 128 && a.block_size == 16)
-    return launch_decode<128, 16, SPLIT, FUSE, VLLM>(a, prm, stream, grid);
+    return launch_decode<128, 16, SPLIT, FUSE, VLLM, QKV>(a, prm, stream, grid);
   if (a.head_dim == 128 && a.block_size == 32)
-    return launch_decode<128, 32, SPLIT, FUSE, VLLM>(a, prm, stream, grid);
+    return launch_decode<128, 32, SPLIT, FUSE, VLLM, QKV>(a, prm, stream, grid);
   if (a.head_dim == 64 && a.block_size == 16)
-    return launch_decode<64, 16, SPLIT, FUSE, VLLM>(a, prm, stream, grid);
+    return launch_decode<64, 16, SPLIT, FUSE, VLLM, QKV>(a, prm, stream, grid);
   if (a.head_dim == 64 && a.block_size == 32)
-    return launch_decode<64, 32, SPLIT, FUSE, VLLM>(a, prm, stream, grid);
+    return launch_decode<64, 32, SPLIT, FUSE, VLLM, QKV>(a, prm, stream, grid);
   return fail(PKV_ERR_UNSUPPORTED, "head_dim %d / block_size %d", a.head_dim, a.block_size);
 }
 
-// Kernels with the fused append (or the vLLM layout) only where a call asks
-// for it, so plain decode kernels carry none of that code.
+// Kernels with the fused append, the fused QKV step or the vLLM layout only
+// where a call asks for it, so plain decode kernels carry none of that code.
 template <bool SPLIT>
 pkv_status dispatch_decode(const DecodeArgs& a, const DecodeParams& prm, cudaStream_t stream,
                            int grid) {
+  if (prm.qkv) return dispatch_decode_f<SPLIT, false, false, true>(a, prm, stream, grid);
   if (a.vllm) {
     if (prm.new_slots) return fail(PKV_ERR_UNSUPPORTED, "no fused append on the vLLM layout");
     return dispatch_decode_f<SPLIT, false, true>(a, prm, stream, grid);
@@ -440,13 +441,21 @@ pkv_status dispatch_varlen(const DecodeArgs& a, const VarlenParams& vp, cudaStre
   return fail(PKV_ERR_UNSUPPORTED, "head_dim %d / block_size %d", a.head_dim, a.block_size);
 }
 
-// The fused append of pkv_append_decode (all null: none).
+// The fused append of pkv_append_decode (slots set), or the fused QKV step
+// of pkv_qkv_norm_rope_append_decode (qkv set); all null: neither.
 struct FuseArgs {
   const void* k_new = nullptr;
   const void* v_new = nullptr;
   const int32_t* slots = nullptr;
   void* k_cache = nullptr;
   void* v_cache = nullptr;
+  const void* qkv = nullptr;
+  const void* q_norm_w = nullptr;
+  const void* k_norm_w = nullptr;
+  const float* cos_t = nullptr;
+  const float* sin_t = nullptr;
+  int max_pos = 0;
+  float eps = 0.f;
 };
 
 void apply_fuse(DecodeParams& p, const FuseArgs* f) {
@@ -456,6 +465,13 @@ void apply_fuse(DecodeParams& p, const FuseArgs* f) {
   p.new_slots = f->slots;
   p.k_cache = static_cast<__half*>(f->k_cache);
   p.v_cache = static_cast<__half*>(f->v_cache);
+  p.qkv = static_cast<const __half*>(f->qkv);
+  p.q_norm_w = static_cast<const __half*>(f->q_norm_w);
+  p.k_norm_w = static_cast<const __half*>(f->k_norm_w);
+  p.cos_t = f->cos_t;
+  p.sin_t = f->sin_t;
+  p.max_pos = f->max_pos;
+  p.eps = f->eps;
 }
 
 pkv_status single_pass(const DecodeArgs& a, cudaStream_t stream, const FuseArgs* fuse = nullptr) {
@@ -636,6 +652,8 @@ pkv_status decode_impl(const DecodeArgs& a, int num_splits, void* scratch, size_
       return fail(PKV_ERR_SCRATCH_TOO_SMALL, "the balanced schedule needs %zu scratch bytes, got %zu",
                   need_b, scratch ? scratch_bytes : (size_t)0);
     if (!aligned(scratch, 16)) return fail(PKV_ERR_INVALID_ARG, "scratch must be 16-byte aligned");
+    if (fuse && fuse->qkv)
+      return fail(PKV_ERR_UNSUPPORTED, "no fused QKV step on the balanced schedule");
     if (fuse) {  // the balanced kernel does not fuse: append first, in stream order
       st = pkv_append(fuse->k_new, fuse->v_new, fuse->slots, num_seqs, fuse->k_cache,
                       fuse->v_cache, a.num_blocks, block_size, num_kv_heads, head_dim, cs);
@@ -962,6 +980,42 @@ pkv_status pkv_qkv_norm_rope_append(const void* qkv, const void* q_norm_w, const
                          : launch_pdl(qkv_norm_rope_kernel<64, 32>, grid, 128, 0, cs, qp);
   if (e != cudaSuccess) return cuda_fail(e, "qkv norm/rope/append launch");
   return PKV_OK;
+}
+
+pkv_status pkv_qkv_norm_rope_append_decode(
+    const void* qkv, const void* q_norm_w, const void* k_norm_w, const float* cos_table,
+    const float* sin_table, int32_t max_pos, float eps, void* k_cache, void* v_cache,
+    const int32_t* block_tables, const int32_t* context_lens, int32_t num_seqs,
+    int32_t max_blocks_per_seq, int32_t num_blocks, float scale, int32_t num_heads,
+    int32_t num_kv_heads, int32_t head_dim, int32_t block_size, void* out, int32_t num_splits,
+    void* scratch, size_t scratch_bytes, void* stream) {
+  // qkv stands in for q in the shared checks (4-byte alignment)
+  const DecodeArgs a{qkv, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                     max_blocks_per_seq, num_blocks, scale, num_heads, num_kv_heads,
+                     head_dim, block_size, out};
+  pkv_status st = validate_decode(a);
+  if (st != PKV_OK) return st;
+  if (!cos_table || !sin_table) return fail(PKV_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (max_pos <= 0) return fail(PKV_ERR_INVALID_ARG, "max_pos must be positive");
+  if (!std::isfinite(eps) || eps < 0.f) return fail(PKV_ERR_INVALID_ARG, "eps must be finite and >= 0");
+  if ((q_norm_w && !aligned(q_norm_w, 2)) || (k_norm_w && !aligned(k_norm_w, 2)) ||
+      !aligned(cos_table, 4) || !aligned(sin_table, 4))
+    return fail(PKV_ERR_INVALID_ARG, "misaligned pointer");
+  if ((long long)num_seqs * (num_heads + 2 * num_kv_heads) * head_dim >= (1ll << 40))
+    return fail(PKV_ERR_INVALID_ARG, "qkv too large");
+  if (num_splits == PKV_SPLITS_BALANCED)
+    return fail(PKV_ERR_UNSUPPORTED, "no fused QKV step on the balanced schedule");
+  FuseArgs f;
+  f.k_cache = k_cache;
+  f.v_cache = v_cache;
+  f.qkv = qkv;
+  f.q_norm_w = q_norm_w;
+  f.k_norm_w = k_norm_w;
+  f.cos_t = cos_table;
+  f.sin_t = sin_table;
+  f.max_pos = max_pos;
+  f.eps = eps;
+  return decode_impl(a, num_splits, scratch, scratch_bytes, static_cast<cudaStream_t>(stream), &f);
 }
 
 pkv_status pkv_selftest_wait_timeout(void* stream) {

@@ -89,6 +89,10 @@ def _load():
     lib.pkv_qkv_norm_rope_append.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32,
                                              i32, i32, i32, i32, i32, i32, i32, f32, vp]
     lib.pkv_qkv_norm_rope_append.restype = i32
+    lib.pkv_qkv_norm_rope_append_decode.argtypes = [vp, vp, vp, vp, vp, i32, f32, vp, vp, vp, vp,
+                                                    i32, i32, i32, f32, i32, i32, i32, i32, vp,
+                                                    i32, vp, sz, vp]
+    lib.pkv_qkv_norm_rope_append_decode.restype = i32
     lib.pkv_selftest_wait_timeout.argtypes = [vp]
     lib.pkv_selftest_wait_timeout.restype = i32
     lib.pkv_read_device_status.argtypes = [ctypes.POINTER(ctypes.c_int32), vp]
@@ -473,6 +477,47 @@ def pkv_qkv_norm_rope_append(qkv, q_norm_w, k_norm_w, cos_table, sin_table, k_ca
         pos_offsets.data_ptr(), block_tables.data_ptr(), B, total_q, block_tables.shape[1], NB,
         H, Hkv, D, bs, max_pos, float(eps), _stream_ptr(stream)), "pkv_qkv_norm_rope_append")
     return q_out
+
+
+def pkv_qkv_norm_rope_append_decode(qkv, q_norm_w, k_norm_w, cos_table, sin_table, k_cache,
+                                    v_cache, block_tables, context_lens, num_heads, scale,
+                                    eps=1e-6, num_splits=0, scratch=None, out=None, stream=None):
+    """One decode attention step from each sequence's fused projection row
+    ``qkv [B][(H + 2 Hkv) D]``: norm + rotary of its query and key heads at
+    position ``context_lens[s] - 1``, append of the key and value rows, and the
+    decode of :func:`pkv_decode_splitk` with the rotated queries; returns
+    ``out [B][H][D]``."""
+    import torch
+
+    _want(k_cache, "k_cache", torch.float16, 4)
+    NB, Hkv, bs, D = k_cache.shape
+    _want(v_cache, "v_cache", torch.float16, 4, k_cache.shape)
+    H = int(num_heads)
+    _want(block_tables, "block_tables", torch.int32, 2)
+    B, mbps = block_tables.shape
+    _want(qkv, "qkv", torch.float16, 2, (B, (H + 2 * Hkv) * D))
+    _want(context_lens, "context_lens", torch.int32, 1, (B,))
+    for name, w in (("q_norm_w", q_norm_w), ("k_norm_w", k_norm_w)):
+        if w is not None:
+            _want(w, name, torch.float16, 1, (D,))
+    _want(cos_table, "cos_table", torch.float32, 2)
+    max_pos = cos_table.shape[0]
+    _want(cos_table, "cos_table", torch.float32, 2, (max_pos, D // 2))
+    _want(sin_table, "sin_table", torch.float32, 2, (max_pos, D // 2))
+    if out is None:
+        out = torch.empty((B, H, D), dtype=torch.float16, device=qkv.device)
+    _want(out, "out", torch.float16, 3, (B, H, D))
+    if scratch is None:
+        scratch = alloc_scratch(out, k_cache, block_tables, num_splits)
+    _want(scratch, "scratch", torch.uint8, 1)
+    ptr = lambda t: None if t is None else t.data_ptr()  # noqa: E731
+    _check(lib.pkv_qkv_norm_rope_append_decode(
+        qkv.data_ptr(), ptr(q_norm_w), ptr(k_norm_w), cos_table.data_ptr(), sin_table.data_ptr(),
+        max_pos, float(eps), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
+        context_lens.data_ptr(), B, mbps, NB, float(scale), H, Hkv, D, bs, out.data_ptr(),
+        int(num_splits), scratch.data_ptr(), scratch.numel(), _stream_ptr(stream)),
+        "pkv_qkv_norm_rope_append_decode")
+    return out
 
 
 def pkv_selftest_wait_timeout(stream=None):

@@ -36,7 +36,8 @@ def test_header_declares_the_expected_calls():
               "pkv_read_device_status", "pkv_append_vllm_layout", "pkv_decode_vllm_layout",
               "pkv_varlen_attention_vllm_layout", "pkv_varlen_attention_splitk",
               "pkv_varlen_attention_splitk_vllm_layout", "pkv_varlen_pick_num_splits",
-              "pkv_qkv_norm_rope_append", "pkv_selftest_wait_timeout"]:
+              "pkv_qkv_norm_rope_append", "pkv_qkv_norm_rope_append_decode",
+              "pkv_selftest_wait_timeout"]:
         assert n in names
 
 
@@ -301,3 +302,38 @@ def test_qkv_norm_rope_rejects_bad_arguments(pk):
     assert call(cos=F16 + 2) == -1            # misaligned f32
     assert call(T=0) == 0                      # no rows: nothing launched
     assert call(B=0) == 0
+
+
+def test_qkv_norm_rope_append_decode_rejects_bad_arguments(pk):
+    """Every call here is rejected (or has no sequences) before any CUDA call."""
+    f = pk.lib.pkv_qkv_norm_rope_append_decode
+    names = ["qkv", "qw", "kw", "cos", "sin", "max_pos", "eps", "kc", "vc", "bt", "cl", "B",
+             "mbps", "nb", "scale", "H", "Hkv", "D", "bs", "out", "S", "scratch", "scratch_bytes"]
+    base = [F16, None, None, F16, F16, 100, 1e-6, F16, F16, F16, F16, 2, 3, 8, 0.125, 8, 2, 128,
+            16, F16, 0, None, 0]
+
+    def call(**over):
+        a = list(base)
+        for k, v in over.items():
+            a[names.index(k)] = v
+        return f(*a, None)
+
+    assert call(qkv=None) == -1
+    assert call(cos=None) == -1
+    assert call(sin=None) == -1
+    assert call(out=None) == -1
+    assert call(H=6, Hkv=4) == -1
+    assert call(H=32, Hkv=2) == -2             # group 16
+    assert call(D=96) == -2
+    assert call(bs=8) == -2
+    assert call(max_pos=0) == -1
+    assert call(eps=-1.0) == -1
+    assert call(eps=float("inf")) == -1
+    assert call(scale=float("nan")) == -1
+    assert call(qkv=F16 + 2) == -1            # half2 loads need 4-byte alignment
+    assert call(kc=F16 + 4) == -1             # tensor copies need 16-byte pools
+    assert call(qw=F16 + 1) == -1
+    assert call(cos=F16 + 2) == -1
+    assert call(S=-1) == -2                    # no balanced schedule
+    assert call(S=pk.PKV_MAX_SPLITS + 1) == -1
+    assert call(B=0) == 0                      # no sequences: nothing launched

@@ -447,43 +447,81 @@ struct WarpState {
   }
 };
 
-// One query or key head of a fused projection row, RMS-normed over its D
-// elements when `w` is given and turned by the rotary angles of one position
-// (rotate-half pairs (i, i + D/2); f32, rounded once to f16), in the pair
-// layout of qkv_norm_rope_kernel: lane holds elements PL*lane .. +PL and the
-// same + D/2, returned packed (PL = 2: one half2 word each; PL = 1: one half
-// in the low bits).  All lanes of the warp take part.
+// The pair layout of one head (or weight vector) of D halves: lane holds
+// elements PL*lane .. +PL and the same + D/2 (PL = D/64), so that each lane
+// has both halves of its rotate-half pairs.  `lo` / `hi` pack them: PL = 2,
+// one half2 word each; PL = 1, one half in the low bits.  Plain loads (the
+// source may be global or shared memory).
 template <int D>
-__device__ __forceinline__ void norm_rotate_head(const __half* x, const __half* w,
-                                                 const float* cs_row, const float* sn_row,
-                                                 float eps, int lane, uint32_t& lo, uint32_t& hi) {
+__device__ __forceinline__ void load_pairs(const __half* x, int lane, uint32_t& lo, uint32_t& hi) {
   constexpr int PL = D / 64;
   const int i0 = PL * lane;
-  float a[PL], b[PL];
-#pragma unroll
-  for (int j = 0; j < PL; ++j) {
-    a[j] = __half2float(x[i0 + j]);
-    b[j] = __half2float(x[i0 + j + D / 2]);
+  if (PL == 2) {
+    lo = *reinterpret_cast<const uint32_t*>(x + i0);
+    hi = *reinterpret_cast<const uint32_t*>(x + i0 + D / 2);
+  } else {
+    lo = *reinterpret_cast<const unsigned short*>(x + i0);
+    hi = *reinterpret_cast<const unsigned short*>(x + i0 + D / 2);
   }
-  if (w != nullptr) {
+}
+
+template <int D>
+__device__ __forceinline__ void unpack_pairs(uint32_t v, float (&f)[D / 64]) {
+  if (D / 64 == 2) {
+    const float2 t = __half22float2(*reinterpret_cast<const __half2*>(&v));
+    f[0] = t.x;
+    f[D / 64 - 1] = t.y;
+  } else {
+    f[0] = __half2float(__ushort_as_half((unsigned short)v));
+  }
+}
+
+// The rotary angles of one position for the lane's pairs.
+template <int D>
+__device__ __forceinline__ void load_angles(const float* cs_row, const float* sn_row, int lane,
+                                            float (&c)[D / 64], float (&sn)[D / 64]) {
+#pragma unroll
+  for (int j = 0; j < D / 64; ++j) {
+    c[j] = __ldg(cs_row + (D / 64) * lane + j);
+    sn[j] = __ldg(sn_row + (D / 64) * lane + j);
+  }
+}
+
+// One query or key head in the pair layout, RMS-normed over its D elements
+// when `has_w` (weights in the pair layout) and turned by the lane's rotary
+// angles (rotate-half pairs (i, i + D/2)); f32, rounded once to f16; the
+// result in the pair layout.  All lanes of the warp take part.
+template <int D>
+__device__ __forceinline__ void norm_rotate_pairs(uint32_t xlo, uint32_t xhi, bool has_w,
+                                                  uint32_t wlo, uint32_t whi,
+                                                  const float (&c)[D / 64],
+                                                  const float (&sn)[D / 64], float eps,
+                                                  uint32_t& lo, uint32_t& hi) {
+  constexpr int PL = D / 64;
+  float a[PL], b[PL];
+  unpack_pairs<D>(xlo, a);
+  unpack_pairs<D>(xhi, b);
+  if (has_w) {
     float ss = 0.f;
 #pragma unroll
     for (int j = 0; j < PL; ++j) ss += a[j] * a[j] + b[j] * b[j];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     const float rr = rsqrtf(ss / (float)D + eps);
+    float wa[PL], wb[PL];
+    unpack_pairs<D>(wlo, wa);
+    unpack_pairs<D>(whi, wb);
 #pragma unroll
     for (int j = 0; j < PL; ++j) {
-      a[j] = a[j] * rr * __half2float(w[i0 + j]);
-      b[j] = b[j] * rr * __half2float(w[i0 + j + D / 2]);
+      a[j] = a[j] * rr * wa[j];
+      b[j] = b[j] * rr * wb[j];
     }
   }
   float oa[PL], ob[PL];
 #pragma unroll
   for (int j = 0; j < PL; ++j) {
-    const float c = __ldg(cs_row + i0 + j), sv = __ldg(sn_row + i0 + j);
-    oa[j] = a[j] * c - b[j] * sv;
-    ob[j] = b[j] * c + a[j] * sv;
+    oa[j] = a[j] * c[j] - b[j] * sn[j];
+    ob[j] = b[j] * c[j] + a[j] * sn[j];
   }
   if (PL == 2) {
     lo = pack_half2(__floats2half2_rn(oa[0], oa[PL - 1]));
@@ -494,7 +532,7 @@ __device__ __forceinline__ void norm_rotate_head(const __half* x, const __half* 
   }
 }
 
-// Stores a head in the pair layout (see norm_rotate_head) at `dst` (global).
+// Stores a head in the pair layout (see load_pairs) at `dst` (global or shared).
 template <int D>
 __device__ __forceinline__ void store_pairs(__half* dst, int lane, uint32_t lo, uint32_t hi) {
   constexpr int PL = D / 64;
@@ -777,7 +815,8 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
 
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_failed;
-  __shared__ __align__(16) __half s_q[QKV ? 8 * D : 2];  // QKV: the group's rotated queries
+  __shared__ __align__(16) __half s_q[QKV ? 8 * D : 2];   // QKV: the group's rotated queries
+  __shared__ __align__(16) __half s_kv[QKV ? 2 * D : 2];  // QKV: the new key and value rows
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t ring = smem_addr(smem);
@@ -825,6 +864,26 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     }
   }
   const int slot_new = FUSE ? __ldg(p.new_slots + s) : -1;
+  // QKV: the loads that need no length go out with the rest: the warp's
+  // query heads (warp, warp + W) of the projection row, the norm weights, and
+  // in warp W-1 the KV head's key and value heads.
+  constexpr int PL = D / 64;
+  uint32_t xq[2][2] = {{0u, 0u}, {0u, 0u}}, wq[2] = {0u, 0u};
+  uint32_t xk[2] = {0u, 0u}, xv[2] = {0u, 0u}, wk[2] = {0u, 0u};
+  if (QKV) {
+    const int H = p.num_heads, Hkv = p.num_kv_heads;
+    const __half* row = p.qkv + (size_t)s * (H + 2 * Hkv) * D;
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+      if (warp + j * W < p.group)
+        load_pairs<D>(row + (size_t)(g * p.group + warp + j * W) * D, lane, xq[j][0], xq[j][1]);
+    if (p.q_norm_w && warp < p.group) load_pairs<D>(p.q_norm_w, lane, wq[0], wq[1]);
+    if (warp == W - 1) {
+      load_pairs<D>(row + (size_t)(H + g) * D, lane, xk[0], xk[1]);
+      load_pairs<D>(row + (size_t)(H + Hkv + g) * D, lane, xv[0], xv[1]);
+      if (p.k_norm_w) load_pairs<D>(p.k_norm_w, lane, wk[0], wk[1]);
+    }
+  }
 
   // After a lost copy has been flagged, later CTAs do no work (and write
   // nothing) until the host reads and clears the status word.  The decision
@@ -840,6 +899,10 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   // written but meaningless).
   const bool qkv_bad = QKV && L > p.max_pos;
   if (qkv_bad && threadIdx.x == 0) atomicOr(&g_device_status, kDevBadContextLen);
+  float ang_c[PL], ang_s[PL];  // QKV: the rotary angles of position L-1
+  if (QKV && !qkv_bad && L > 0 && (warp < p.group || warp == W - 1))
+    load_angles<D>(p.cos_t + (size_t)(L - 1) * (D / 2), p.sin_t + (size_t)(L - 1) * (D / 2), lane,
+                   ang_c, ang_s);
   int tok_begin = 0;
   int tok_end = L;
   if (SPLIT) {
@@ -874,7 +937,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   constexpr int HPL = D / 32;  // halves per lane of one row
   int fuse_li = -1;            // local tile index of the new row, in its owner warp
   int fuse_row = 0;
-  int fuse_phys = 0;           // QKV: its physical block
+  int kv_phys = -1;            // QKV: the new row's block when this CTA holds it
   uint32_t kn[HPL / 2], vn[HPL / 2];
   if ((FUSE || QKV) && !qkv_bad && L > 0 && L - 1 >= tok_begin && L - 1 < tok_end &&
       (QKV || slot_new >= 0)) {
@@ -886,12 +949,10 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     } else {
       const int idx = pos / BS - blk_begin;  // tile within the chunk
       if (QKV) {
-        // the rows are computed after the first copies are issued (below)
-        if (warp == idx % WE) {
-          fuse_li = idx / WE;
-          fuse_row = pos % BS;
-          fuse_phys = phys;
-        }
+        // the row is computed after the first copies are issued (below)
+        kv_phys = phys;
+        fuse_row = pos % BS;
+        if (warp == idx % WE) fuse_li = idx / WE;
       } else if (warp == idx % WE) {
         fuse_li = idx / WE;
         fuse_row = pos % BS;
@@ -935,35 +996,29 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   uint32_t qk_lo = 0, qk_hi = 0, qv_lo = 0, qv_hi = 0;  // QKV: the new key / value row
   if (QKV) {
     // With the first copies in flight: the group's queries (norm + rotary at
-    // position L-1) into shared memory, and in the owner warp the new key and
-    // value rows, written to the pools now and into the tile when it lands.
+    // position L-1) into shared memory; warp W-1 turns the new key row,
+    // writes key and value rows to the pools and leaves them in shared
+    // memory for the warp whose tile holds them.
     if (L > 0 && !qkv_bad) {
-      const int pos = L - 1;
-      const int H = p.num_heads, Hkv = p.num_kv_heads;
-      const __half* row = p.qkv + (size_t)s * (H + 2 * Hkv) * D;
-      const float* cs = p.cos_t + (size_t)pos * (D / 2);
-      const float* sn = p.sin_t + (size_t)pos * (D / 2);
-      for (int h = warp; h < p.group; h += W) {
-        uint32_t lo, hi;
-        norm_rotate_head<D>(row + (size_t)(g * p.group + h) * D, p.q_norm_w, cs, sn, p.eps, lane,
-                            lo, hi);
-        store_pairs<D>(s_q + h * D, lane, lo, hi);
-      }
-      if (fuse_li >= 0) {
-        norm_rotate_head<D>(row + (size_t)(H + g) * D, p.k_norm_w, cs, sn, p.eps, lane, qk_lo,
-                            qk_hi);
-        constexpr int PL = D / 64;
-        const __half* xv = row + (size_t)(H + Hkv + g) * D;
-        if (PL == 2) {
-          qv_lo = *reinterpret_cast<const uint32_t*>(xv + 2 * lane);
-          qv_hi = *reinterpret_cast<const uint32_t*>(xv + 2 * lane + D / 2);
-        } else {
-          qv_lo = __half_as_ushort(xv[lane]);
-          qv_hi = __half_as_ushort(xv[lane + D / 2]);
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int h = warp + j * W;
+        if (h < p.group) {
+          uint32_t lo, hi;
+          norm_rotate_pairs<D>(xq[j][0], xq[j][1], p.q_norm_w != nullptr, wq[0], wq[1], ang_c,
+                               ang_s, p.eps, lo, hi);
+          store_pairs<D>(s_q + h * D, lane, lo, hi);
         }
-        const size_t dst = (((size_t)fuse_phys * Hkv + g) * BS + fuse_row) * D;
-        store_pairs<D>(p.k_cache + dst, lane, qk_lo, qk_hi);
-        store_pairs<D>(p.v_cache + dst, lane, qv_lo, qv_hi);
+      }
+      if (warp == W - 1 && kv_phys >= 0) {
+        uint32_t lo, hi;
+        norm_rotate_pairs<D>(xk[0], xk[1], p.k_norm_w != nullptr, wk[0], wk[1], ang_c, ang_s,
+                             p.eps, lo, hi);
+        const size_t dst = (((size_t)kv_phys * p.num_kv_heads + g) * BS + fuse_row) * D;
+        store_pairs<D>(p.k_cache + dst, lane, lo, hi);
+        store_pairs<D>(p.v_cache + dst, lane, xv[0], xv[1]);
+        store_pairs<D>(s_kv, lane, lo, hi);
+        store_pairs<D>(s_kv + (QKV ? D : 0), lane, xv[0], xv[1]);
       }
     } else {
       for (int i = threadIdx.x; i < 8 * D / 2; i += W * 32)
@@ -971,6 +1026,10 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     }
     __syncthreads();
     load_q_frags_smem<D>(qf, s_q, p.group, lane);
+    if (fuse_li >= 0) {
+      load_pairs<D>(s_kv, lane, qk_lo, qk_hi);
+      load_pairs<D>(s_kv + (QKV ? D : 0), lane, qv_lo, qv_hi);
+    }
   } else {
     load_q_frags<D>(qf, p.q, (size_t)s * p.num_heads + (size_t)g * p.group, p.group, lane);
   }
@@ -993,7 +1052,6 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
       const uint32_t kb = k_stage(stage);
       if (QKV && li == fuse_li) {
         // the new row of this tile is the one computed above, not the copy
-        constexpr int PL = D / 64;
         const int i0 = PL * lane;
         if (PL == 2) {
           asm volatile("st.shared.u32 [%0], %1;" ::"r"(kb + swz<BS>(fuse_row, i0)), "r"(qk_lo) : "memory");

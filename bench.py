@@ -77,15 +77,36 @@ BASE_QKV_SEED = 20261210
 # Reported as null when the kernels have changed since.
 NCU_TRAFFIC = {
     # profiles/decode_llama8b.md: the fused append + single-pass decode launch,
-    # dram read 175.231 MB + write 3.333 MB
-    "llama8b": {"kernel_hash": "675ee69190d7ec06", "bytes_per_launch": 178563584, "num_splits": 1,
+    # dram read 175,222,784 B + write 3,152,640 B
+    "llama8b": {"kernel_hash": "01fa1b1775fdba94", "bytes_per_launch": 178375424, "num_splits": 1,
                 "fused": True, "layout": "blocked",
                 "kernel": "paged_decode_kernel<128,16,6,2,single,fused>"},
     # profiles/varlen_spec_long.md: the varlen split-K phase 1 (10 splits),
-    # dram read 1342.525 MB + write 3.425 MB
-    "spec_long": {"kernel_hash": "675ee69190d7ec06", "bytes_per_launch": 1345949952,
+    # dram read 1,342,484,224 B + write 3,473,920 B
+    "spec_long": {"kernel_hash": "01fa1b1775fdba94", "bytes_per_launch": 1345958144,
                   "num_splits": 10, "kernel": "paged_varlen_kernel<128,16,6,2,NT=2,blocked,split>"},
+    # profiles/qkv_prefill.md: one qkv_norm_rope_kernel launch, dram read
+    # 102,000,896 B + write 55,059,456 B (the rest of the writes stay in L2)
+    "qkv_prefill": {"kernel_hash": "01fa1b1775fdba94", "bytes_per_launch": 157060352,
+                    "kernel": "qkv_norm_rope_kernel<128,16>"},
+    # profiles/decode_llama8b.md (one-launch QKV step): the decode kernel with
+    # the QKV norm + rotary + append folded in, dram read 175,243,008 B +
+    # write 3,323,136 B
+    "step_qkv": {"kernel_hash": "01fa1b1775fdba94", "bytes_per_launch": 178566144,
+                 "num_splits": 1, "kernel": "paged_decode_kernel<128,16,6,2,single,qkv>"},
 }
+
+
+def ncu_traffic(workload, num_splits=None):
+    """DRAM bytes per launch of the workload's dominant kernel from the
+    committed ncu capture, or None once the kernels have changed since (or
+    the split count differs from the captured one)."""
+    tr = NCU_TRAFFIC.get(workload)
+    if not tr or tr.get("kernel_hash") != kernel_source_hash():
+        return None
+    if "num_splits" in tr and num_splits != tr["num_splits"]:
+        return None
+    return tr["bytes_per_launch"]
 
 
 def kernel_source_hash():
@@ -388,7 +409,8 @@ def run_qkv(args):
         "tokens_per_s": world * T / (ms * 1e-3),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_kind,
-                     "kernel": "qkv_norm_rope_kernel (bytes read + written)", "traffic": None},
+                     "kernel": "qkv_norm_rope_kernel (bytes read + written)",
+                     "traffic": ncu_traffic("qkv_prefill")},
         "clocks": clocks.summary(), "gpu_launches": rounds * n_sets,
         "device_status_flags": pk.pkv_read_device_status(), "e2e": None, "cpu_baseline": None,
     }
@@ -484,7 +506,7 @@ def run_step_qkv(args):
         return
     kv_bytes = w.kv_bytes
     peak, peak_kind = measured_peaks()
-    achieved = kv_bytes / (dec_ms * 1e-3) / 1e9
+    achieved = kv_bytes / (ms * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": job_throughput(kv_bytes, world, ms), "unit": UNIT,
         "n_gpus": world, "steps": rounds * n_sets, "warmup": args.warmup, "ms_per_step": ms,
@@ -498,8 +520,10 @@ def run_step_qkv(args):
         "decode_tokens_per_s": world * w.num_seqs / (ms * 1e-3),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_kind,
-                     "kernel": "the decode call alone (the fused step's attention part)",
-                     "traffic": None},
+                     "kernel": ("the step's single launch (QKV norm + rotary + append fused "
+                                "into the decode)" if S <= 1 else
+                                "the step (fused decode phase 1 + combine)"),
+                     "traffic": ncu_traffic("step_qkv", S)},
         "clocks": clocks.summary(), "gpu_launches": rounds * n_sets * (1 + (S > 1)),
         "device_status_flags": pk.pkv_read_device_status(), "e2e": None, "cpu_baseline": None,
     }

@@ -373,8 +373,10 @@ pkv_status pkv_varlen_attention_splitk_vllm_layout(
  * position is invalid (p < 0, p >= max_pos or beyond the table) is skipped
  * and sets PKV_DEV_BAD_CONTEXT_LEN; a table entry outside [0, num_blocks)
  * skips that row's key and value writes and sets PKV_DEV_BAD_BLOCK_ID.
- * head_dim in {64, 128}, block_size in {16, 32}; eps >= 0.  qkv, q_out and
- * the pools must be 4-byte aligned, the weights 2-byte, the tables 4-byte.
+ * head_dim in {64, 128}, block_size in {16, 32}; eps >= 0.  qkv, q_out, the
+ * pools, the weights and the rotary tables must be 16-byte aligned (the
+ * kernel moves 16-byte words), cu_seqlens_q, pos_offsets and block_tables
+ * 4-byte aligned.
  */
 pkv_status pkv_qkv_norm_rope_append(const void* qkv, const void* q_norm_w, const void* k_norm_w,
                                     const float* cos_table, const float* sin_table, void* q_out,

@@ -914,6 +914,33 @@ pkv_status pkv_varlen_attention_splitk_vllm_layout(
                      static_cast<cudaStream_t>(stream), true);
 }
 
+}  // extern "C"
+
+namespace pkv {
+namespace {
+
+// qkv_norm_rope_kernel<D, BS, NS> for the runtime head_dim, block_size and
+// slot count (NS0 .. 4).
+template <int NS0>
+cudaError_t launch_qkv(int head_dim, int block_size, int NS, dim3 grid, cudaStream_t cs,
+                       const QkvRopeParams& qp) {
+  if constexpr (NS0 <= 4) {
+    if (NS != NS0) return launch_qkv<NS0 + 1>(head_dim, block_size, NS, grid, cs, qp);
+    if (head_dim == 128)
+      return block_size == 16 ? launch_pdl(qkv_norm_rope_kernel<128, 16, NS0>, grid, 128, 0, cs, qp)
+                              : launch_pdl(qkv_norm_rope_kernel<128, 32, NS0>, grid, 128, 0, cs, qp);
+    return block_size == 16 ? launch_pdl(qkv_norm_rope_kernel<64, 16, NS0>, grid, 128, 0, cs, qp)
+                            : launch_pdl(qkv_norm_rope_kernel<64, 32, NS0>, grid, 128, 0, cs, qp);
+  } else {
+    return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" {
+
 pkv_status pkv_qkv_norm_rope_append(const void* qkv, const void* q_norm_w, const void* k_norm_w,
                                     const float* cos_table, const float* sin_table, void* q_out,
                                     void* k_cache, void* v_cache, const int32_t* cu_seqlens_q,
@@ -940,11 +967,13 @@ pkv_status pkv_qkv_norm_rope_append(const void* qkv, const void* q_norm_w, const
   if ((long long)num_blocks * block_size >= (1ll << 31) ||
       (long long)max_blocks_per_seq * block_size >= (1ll << 31))
     return fail(PKV_ERR_INVALID_ARG, "pool or table too large for 32-bit positions");
-  if (!aligned(qkv, 4) || !aligned(q_out, 4) || !aligned(k_cache, 4) || !aligned(v_cache, 4) ||
-      (q_norm_w && !aligned(q_norm_w, 2)) || (k_norm_w && !aligned(k_norm_w, 2)) ||
-      !aligned(cos_table, 4) || !aligned(sin_table, 4) || !aligned(cu_seqlens_q, 4) ||
-      !aligned(pos_offsets, 4) || !aligned(block_tables, 4))
-    return fail(PKV_ERR_INVALID_ARG, "misaligned pointer");
+  if (!aligned(qkv, 16) || !aligned(q_out, 16) || !aligned(k_cache, 16) ||
+      !aligned(v_cache, 16) || (q_norm_w && !aligned(q_norm_w, 16)) ||
+      (k_norm_w && !aligned(k_norm_w, 16)) || !aligned(cos_table, 16) ||
+      !aligned(sin_table, 16) || !aligned(cu_seqlens_q, 4) || !aligned(pos_offsets, 4) ||
+      !aligned(block_tables, 4))
+    return fail(PKV_ERR_INVALID_ARG,
+                "misaligned pointer (rows, weights, tables and pools: 16 bytes; indices: 4)");
   if (num_seqs == 0 || total_q == 0) return PKV_OK;
   QkvRopeParams qp{};
   qp.qkv = static_cast<const __half*>(qkv);
@@ -968,16 +997,22 @@ pkv_status pkv_qkv_norm_rope_append(const void* qkv, const void* q_norm_w, const
   qp.max_pos = max_pos;
   qp.eps = eps;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  const int groups = (num_heads + 2 * num_kv_heads + kQkvHeadsPerCta - 1) / kQkvHeadsPerCta;
+  // slots per warp: the fewest idle head slots per row, then the most heads per CTA
+  const int heads = num_heads + 2 * num_kv_heads;
+  int NS = 1, best = 1 << 30;
+  for (int ns = 1; ns <= 4; ++ns) {
+    const int per = qkv_heads_per_cta(head_dim, ns);
+    const int waste = (heads + per - 1) / per * per - heads;
+    if (waste <= best) {
+      best = waste;
+      NS = ns;
+    }
+  }
+  const int per_cta = qkv_heads_per_cta(head_dim, NS);
+  const int groups = (heads + per_cta - 1) / per_cta;
   if (groups > 65535) return fail(PKV_ERR_INVALID_ARG, "too many heads");
   const dim3 grid((unsigned)total_q, (unsigned)groups, 1);  // x: token, y: group of heads
-  cudaError_t e;
-  if (head_dim == 128)
-    e = block_size == 16 ? launch_pdl(qkv_norm_rope_kernel<128, 16>, grid, 128, 0, cs, qp)
-                         : launch_pdl(qkv_norm_rope_kernel<128, 32>, grid, 128, 0, cs, qp);
-  else
-    e = block_size == 16 ? launch_pdl(qkv_norm_rope_kernel<64, 16>, grid, 128, 0, cs, qp)
-                         : launch_pdl(qkv_norm_rope_kernel<64, 32>, grid, 128, 0, cs, qp);
+  cudaError_t e = launch_qkv<1>(head_dim, block_size, NS, grid, cs, qp);
   if (e != cudaSuccess) return cuda_fail(e, "qkv norm/rope/append launch");
   return PKV_OK;
 }

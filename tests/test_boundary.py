@@ -298,8 +298,13 @@ def test_qkv_norm_rope_rejects_bad_arguments(pk):
     assert call(max_pos=0) == -1
     assert call(eps=-1.0) == -1
     assert call(eps=float("nan")) == -1
-    assert call(qkv=F16 + 2) == -1            # 2-byte aligned only: half2 loads need 4
+    assert call(qkv=F16 + 2) == -1            # the kernel moves 16-byte words
+    assert call(qkv=F16 + 8) == -1
+    assert call(qo=F16 + 4) == -1
+    assert call(kc=F16 + 4) == -1
+    assert call(qw=F16 + 2) == -1
     assert call(cos=F16 + 2) == -1            # misaligned f32
+    assert call(sin=F16 + 8) == -1
     assert call(T=0) == 0                      # no rows: nothing launched
     assert call(B=0) == 0
 

@@ -71,6 +71,11 @@ def slots_of(c):
     (8, 8, 64, 32, [5, 17, 1], [0, 40, 300], False),             # prefill chunks, no norm
     (28, 4, 128, 32, [3, 3], [31, 1000], True),
     (16, 2, 64, 16, [9, 2], [7, 60], True),
+    # the kernel's slots per warp follow the head count: 48 heads of 64
+    # take 2, 64 heads of 128 and 128 heads of 64 take 4
+    (32, 8, 64, 16, [4, 3], [10, 100], True),
+    (32, 16, 128, 16, [2, 5], [33, 0], True),
+    (64, 32, 64, 32, [3], [47], True),
 ])
 def test_qkv_norm_rope_append_matches_oracle(pk, cuda_device, H, Hkv, D, bs, q_lens, prefix,
                                              norm):

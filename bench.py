@@ -820,21 +820,22 @@ def run_ours(args):
         raise RuntimeError(f"device status flags {flags:#x} after warm-up")
 
     def timed(g):
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(rounds):
+        """Total ms over `rounds` back-to-back replays, and the ms of each
+        replay (events between replays; the total spans first to last)."""
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(rounds + 1)]
+        ev[0].record(stream)
+        for r in range(rounds):
             g.replay()
-        b.record(stream)
+            ev[r + 1].record(stream)
         torch.cuda.synchronize()
-        return a.elapsed_time(b)
+        return ev[0].elapsed_time(ev[-1]), [ev[r].elapsed_time(ev[r + 1]) for r in range(rounds)]
 
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
-        total_ms = timed(g_step)
-        decode_total_ms = timed(g_decode)
+        total_ms, step_rounds = timed(g_step)
+        decode_total_ms, decode_rounds = timed(g_decode)
     if dist is not None:
         dist.barrier()
     total_ms = max_over_ranks(total_ms, dist, dev)
@@ -947,6 +948,11 @@ def run_ours(args):
         "decode_tokens_per_s": world * w.num_seqs / (ms_per_step * 1e-3),
         "us_per_step": ms_per_step * 1e3,
         "decode_us_per_call": dec_avg_ms * 1e3,
+        # per replay of the graph (n_sets steps), divided by n_sets
+        "us_per_step_median": 1e3 * statistics.median(step_rounds) / n_sets,
+        "us_per_step_min": 1e3 * min(step_rounds) / n_sets,
+        "decode_us_median": 1e3 * statistics.median(decode_rounds) / n_sets,
+        "decode_us_min": 1e3 * min(decode_rounds) / n_sets,
         "pct_of_8TBs": 100.0 * achieved / NOMINAL_HBM_GBS,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_kind,

@@ -794,8 +794,9 @@ __device__ __forceinline__ void merge_warps(const float* red, int stride, int h,
 }
 
 // Starts the TMA copies of the K and V tiles of (physical block, kv head)
-// into the stage at `kdst` (V follows K), completing on `bar`.  VLLM: K is
-// one contiguous bulk copy from `kpool`, V one 3-D tensor copy.
+// into the stage at `kdst` (V follows K), completing on `bar`: one tensor
+// box per tile (landing as [D/64][BS][64], swizzled).  VLLM: K is one
+// contiguous bulk copy from `kpool`, V one 3-D tensor copy.
 template <int D, int BS, bool VLLM = false>
 __device__ __forceinline__ void issue_tile_copy(uint32_t kdst, uint32_t bar, int tile,
                                                 const CUtensorMap* kmap, const CUtensorMap* vmap,
@@ -806,11 +807,8 @@ __device__ __forceinline__ void issue_tile_copy(uint32_t kdst, uint32_t bar, int
     bulk_load(kdst, kpool + (size_t)tile * (BS * D), TB, bar);
     tma_load_3d(kdst + TB, vmap, bar, 0, 0, tile);
   } else {
-#pragma unroll
-    for (int h2 = 0; h2 < D / 64; ++h2) {
-      tma_load_4d(kdst + h2 * BS * 128, kmap, bar, 0, h2, 0, tile);
-      tma_load_4d(kdst + TB + h2 * BS * 128, vmap, bar, 0, h2, 0, tile);
-    }
+    tma_load_4d(kdst, kmap, bar, 0, 0, 0, tile);
+    tma_load_4d(kdst + TB, vmap, bar, 0, 0, 0, tile);
   }
 }
 

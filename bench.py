@@ -77,22 +77,22 @@ BASE_QKV_SEED = 20261210
 # Reported as null when the kernels have changed since.
 NCU_TRAFFIC = {
     # profiles/decode_llama8b.md: the fused append + single-pass decode launch,
-    # dram read 175,222,784 B + write 3,152,640 B
-    "llama8b": {"kernel_hash": "01fa1b1775fdba94", "bytes_per_launch": 178375424, "num_splits": 1,
+    # dram read 175,230,976 B + write 3,221,760 B
+    "llama8b": {"kernel_hash": "fe533890695fa809", "bytes_per_launch": 178452736, "num_splits": 1,
                 "fused": True, "layout": "blocked",
                 "kernel": "paged_decode_kernel<128,16,6,2,single,fused>"},
     # profiles/varlen_spec_long.md: the varlen split-K phase 1 (10 splits),
-    # dram read 1,342,484,224 B + write 3,473,920 B
-    "spec_long": {"kernel_hash": "01fa1b1775fdba94", "bytes_per_launch": 1345958144,
+    # dram read 1,342,589,440 B + write 3,523,584 B
+    "spec_long": {"kernel_hash": "fe533890695fa809", "bytes_per_launch": 1346113024,
                   "num_splits": 10, "kernel": "paged_varlen_kernel<128,16,6,2,NT=2,blocked,split>"},
     # profiles/qkv_prefill.md: one qkv_norm_rope_kernel launch, dram read
-    # 102,000,896 B + write 55,059,456 B (the rest of the writes stay in L2)
-    "qkv_prefill": {"kernel_hash": "01fa1b1775fdba94", "bytes_per_launch": 157060352,
-                    "kernel": "qkv_norm_rope_kernel<128,16>"},
+    # 101,987,584 B + write 53,220,096 B (the rest of the writes stay in L2)
+    "qkv_prefill": {"kernel_hash": "fe533890695fa809", "bytes_per_launch": 155207680,
+                    "kernel": "qkv_norm_rope_kernel<128,16,3>"},
     # profiles/decode_llama8b.md (one-launch QKV step): the decode kernel with
-    # the QKV norm + rotary + append folded in, dram read 175,243,008 B +
-    # write 3,323,136 B
-    "step_qkv": {"kernel_hash": "01fa1b1775fdba94", "bytes_per_launch": 178566144,
+    # the QKV norm + rotary + append folded in, dram read 175,242,752 B +
+    # write 3,392,000 B
+    "step_qkv": {"kernel_hash": "fe533890695fa809", "bytes_per_launch": 178634752,
                  "num_splits": 1, "kernel": "paged_decode_kernel<128,16,6,2,single,qkv>"},
 }
 

@@ -4,8 +4,9 @@
 //   qkv_norm_rope_kernel          fused QKV split + RMS norm + rotary
 //                                 embedding + paged append
 //   paged_decode_kernel           decode: single pass, or split-K phase 1;
-//                                 optionally with the step's append fused in;
-//                                 blocked or vLLM-layout pools
+//                                 optionally with the step's append, or the
+//                                 step's QKV norm + rotary + append, fused
+//                                 in; blocked or vLLM-layout pools
 //   splitk_combine_kernel         log-sum-exp merge of split-K partials
 //   varlen_combine_kernel         the same for varlen split-K partials
 //   paged_varlen_kernel           several causal queries per sequence (one or
@@ -14,6 +15,8 @@
 //                                 vLLM-layout pools
 //   paged_decode_balanced_kernel  decode over equal tile ranges per CTA
 //   balanced_combine_kernel       merge of the balanced schedule's records
+//   wait_timeout_probe_kernel     failure-path diagnostic (a bounded wait on a
+//                                 barrier nothing arrives on)
 //
 // Decode design:
 //  * One CTA per (sequence, KV head[, split]).  It covers the whole GQA group
@@ -21,9 +24,9 @@
 //  * Each of the CTA's W warps owns a private ring of P shared-memory stages.
 //    A stage holds the K and V tiles of one physical block for this KV head
 //    (block_size x head_dim f16 each, contiguous in the pool).  Lane 0 of the
-//    warp fetches them with TMA copies (tensor copies with the 128-byte
-//    swizzle; a bulk copy for vLLM-layout K tiles) that complete on the
-//    stage's mbarrier.  Warp w takes the chunk's blocks w, w+WE, ...
+//    warp fetches them with TMA copies (one tensor copy per tile with the
+//    128-byte swizzle; a bulk copy for vLLM-layout K tiles) that complete on
+//    the stage's mbarrier.  Warp w takes the chunk's blocks w, w+WE, ...
 //    where WE <= W warps are active (fewer for short sequences under the
 //    fair-share depth, see DecodeParams::fair_depth).
 //  * Scores use tensor cores with tokens on M and the group on N:
@@ -146,8 +149,9 @@ append_vllm_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
 // fused QKV split + per-head RMS norm + rotary embedding + paged append
 // ---------------------------------------------------------------------------
 //
-// One CTA per (token, group of 24 heads) (grid x, y), four warps of six heads each,
-// over the token's row [q heads | k heads | v heads].  Token row r of sequence
+// One CTA of four warps per (token, group of heads) (grid x, y), over the
+// token's row [q heads | k heads | v heads]; the head layout is described at
+// qkv_norm_rope_kernel.  Token row r of sequence
 // s sits at position p = pos_offsets[s] + (r - cu_seqlens_q[s]), its rotary
 // position and its cache row.  Query and key heads are RMS-normalised when a
 // weight vector is given, then turned by the rotary angles of position p

@@ -171,3 +171,38 @@ def test_fused_step_flags_positions_without_angles_and_bad_blocks(pk, cuda_devic
                                   np.isnan(kc.astype(np.float32))))
     assert int(changed.any(axis=(1, 3)).sum()) == 2
     assert pk.pkv_read_device_status() == 0
+
+
+def test_fused_step_at_the_llama8b_size(pk, cuda_device):
+    """The step_qkv bench configuration: the Llama-3-8B decode workload's
+    pools and tables (32 sequences, contexts up to 2048), each sequence's
+    newest token given as its fused projection row; the heuristic split
+    count (what the bench times) and a forced split-K."""
+    w = W.make("llama8b")
+    H, Hkv = w.num_heads, w.num_kv_heads
+    lens = w.context_lens.astype(np.int32)
+    c = W.qkv_case(7300, H, Hkv, w.head_dim, w.block_size, [1] * w.num_seqs,
+                   (lens - 1).tolist())
+    kc, vc = W.host_pool(w)
+    q_ref, k_rows = Q.qkv_norm_rope_append(c.qkv, c.q_norm_w, c.k_norm_w, c.cos, c.sin, kc, vc,
+                                           c.cu_seqlens_q, lens - 1, w.block_tables, H, Hkv,
+                                           c.eps)
+    ref = oracle.decode_fast(q_ref.astype(np.float16), kc, vc, w.block_tables, lens, w.scale)
+    d = W.to_device(w, cuda_device)
+    for S in (0, 4):
+        kc_d, vc_d = d["k_cache"].clone(), d["v_cache"].clone()
+        out = pk.pkv_qkv_norm_rope_append_decode(
+            dev(c.qkv, cuda_device), dev(c.q_norm_w, cuda_device), dev(c.k_norm_w, cuda_device),
+            dev(c.cos, cuda_device), dev(c.sin, cuda_device), kc_d, vc_d, d["block_tables"],
+            d["context_lens"], H, w.scale, eps=c.eps, num_splits=S)
+        torch.cuda.synchronize()
+        assert_attention_close(out.float().cpu().numpy().astype(np.float64), ref,
+                               f"llama8b fused step S={S}")
+        got_k = kc_d.cpu().numpy()
+        got_v = vc_d.cpu().numpy()
+        for s in range(w.num_seqs):
+            p = int(lens[s]) - 1
+            blk, off = int(w.block_tables[s][p // w.block_size]), p % w.block_size
+            assert_within_one_ulp(got_k[blk, :, off], k_rows[s], f"k row of sequence {s}")
+            assert_bits_equal(got_v[blk, :, off], vc[blk, :, off], f"v row of sequence {s}")
+        assert pk.pkv_read_device_status() == 0

@@ -1,0 +1,60 @@
+"""bench.py's host-side helpers on CPU: the clock-sample summary, the
+comment-insensitive source hash that guards the committed ncu traffic, and
+the traffic lookup itself."""
+
+import os
+import shutil
+
+import bench
+
+
+def test_clock_summary_takes_the_median_and_the_active_reasons():
+    s = bench.ClockSampler(0)
+    s.lines = [
+        "0, 2070, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "0, 1980, 2070, 1390.5, 0x4, Not Active, Not Active, Not Active, Active",
+        "0, 2070, 2070, 950.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "garbled line",
+        "0, n/a, 2070, 0, 0x0, Not Active, Not Active, Not Active, Not Active",
+    ]
+    out = s.summary()
+    assert out["sm_mhz"] == 2070.0
+    assert out["sm_max_mhz"] == 2070.0
+    assert out["reasons"] == ["sw_power_cap"]
+    assert out["samples"] == 3
+
+
+def test_clock_summary_without_samples():
+    assert bench.ClockSampler(0).summary() == {"sm_mhz": None, "sm_max_mhz": None,
+                                               "reasons": [], "samples": 0}
+
+
+def test_source_hash_ignores_comments_but_not_code(tmp_path, monkeypatch):
+    src = os.path.join(bench.ROOT, "paged_kv_decode_08_gb300", "csrc")
+    dst = tmp_path / "paged_kv_decode_08_gb300" / "csrc"
+    shutil.copytree(src, dst)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h0 = bench.kernel_source_hash()
+    k = dst / "kernels.cuh"
+    text = k.read_text()
+    k.write_text("// a new comment line\n\n" + text.replace("\n", "  // trailing\n", 3))
+    assert bench.kernel_source_hash() == h0
+    k.write_text(text + "\nstatic const int pkv_extra_constant = 1;\n")
+    assert bench.kernel_source_hash() != h0
+
+
+def test_traffic_is_reported_only_for_the_captured_kernels(monkeypatch):
+    entry = bench.NCU_TRAFFIC["llama8b"]
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: entry["kernel_hash"])
+    assert bench.ncu_traffic("llama8b", entry["num_splits"]) == entry["bytes_per_launch"]
+    assert bench.ncu_traffic("llama8b", entry["num_splits"] + 1) is None
+    assert bench.ncu_traffic("no_such_workload", 1) is None
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "0" * 16)
+    assert bench.ncu_traffic("llama8b", entry["num_splits"]) is None
+
+
+def test_every_traffic_entry_is_a_plausible_capture():
+    for name, e in bench.NCU_TRAFFIC.items():
+        assert len(e["kernel_hash"]) == 16, name
+        assert e["bytes_per_launch"] > 0, name
+        assert e["kernel"], name

@@ -34,6 +34,34 @@ int main(void) {
   CHECK(strlen(pkv_last_error()) > 0);
   CHECK(pkv_append((void*)0x10000, (void*)0x10000, (const int32_t*)0x10000, 0, (void*)0x10000,
                    (void*)0x10000, 8, 16, 2, 64, NULL) == PKV_OK);
+  /* every other compute entry, called through its C prototype with a NULL
+   * input: rejected on the host, nothing launched */
+  CHECK(pkv_decode_splitk(NULL, NULL, NULL, NULL, NULL, 1, 1, 1, 0.125f, 4, 2, 64, 16, NULL, 0,
+                          NULL, 0, NULL) == PKV_ERR_INVALID_ARG);
+  CHECK(pkv_append_decode(NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, 1, 1, 1, 0.125f, 4, 2,
+                          64, 16, NULL, 0, NULL, 0, NULL) == PKV_ERR_INVALID_ARG);
+  CHECK(pkv_varlen_attention(NULL, NULL, NULL, NULL, NULL, NULL, 1, 1, 1, 1, 1, 0.125f, 4, 2, 64,
+                             16, NULL, NULL) == PKV_ERR_INVALID_ARG);
+  CHECK(pkv_varlen_attention_vllm_layout(NULL, NULL, NULL, NULL, NULL, NULL, 1, 1, 1, 1, 1, 0.125f,
+                                         4, 2, 64, 16, NULL, NULL) == PKV_ERR_INVALID_ARG);
+  CHECK(pkv_varlen_attention_splitk(NULL, NULL, NULL, NULL, NULL, NULL, 1, 1, 1, 1, 1, 0.125f, 4,
+                                    2, 64, 16, NULL, 0, NULL, 0, NULL) == PKV_ERR_INVALID_ARG);
+  CHECK(pkv_varlen_attention_splitk_vllm_layout(NULL, NULL, NULL, NULL, NULL, NULL, 1, 1, 1, 1, 1,
+                                                0.125f, 4, 2, 64, 16, NULL, 0, NULL, 0,
+                                                NULL) == PKV_ERR_INVALID_ARG);
+  CHECK(pkv_append_vllm_layout(NULL, NULL, NULL, 1, NULL, NULL, 8, 16, 2, 64, NULL) ==
+        PKV_ERR_INVALID_ARG);
+  CHECK(pkv_decode_vllm_layout(NULL, NULL, NULL, NULL, NULL, 1, 1, 1, 0.125f, 4, 2, 64, 16, NULL,
+                               0, NULL, 0, NULL) == PKV_ERR_INVALID_ARG);
+  CHECK(pkv_decode_splitk_noalloc(NULL, NULL, NULL, NULL, NULL, 1, 1, 1, 0.125f, 4, 2, 64, 16,
+                                  NULL, 0, NULL) == PKV_ERR_INVALID_ARG);
+  CHECK(pkv_qkv_norm_rope_append(NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL,
+                                 1, 1, 1, 8, 4, 2, 64, 16, 100, 1e-6f, NULL) ==
+        PKV_ERR_INVALID_ARG);
+  CHECK(pkv_qkv_norm_rope_append_decode(NULL, NULL, NULL, NULL, NULL, 100, 1e-6f, NULL, NULL, NULL,
+                                        NULL, 1, 1, 8, 0.125f, 4, 2, 64, 16, NULL, 0, NULL, 0,
+                                        NULL) == PKV_ERR_INVALID_ARG);
+  CHECK(pkv_read_device_status(NULL, NULL) == PKV_ERR_INVALID_ARG);
   printf("all ok\n");
   return 0;
 }

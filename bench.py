@@ -3,19 +3,28 @@
 One step = one pass of the whole hot path over one batch: the slot-mapped
 append of each sequence's newest token fused into the decode
 (``pkv_append_decode``; ``--separate`` runs ``pkv_append`` then
-``pkv_decode_splitk``), with the split count from the heuristic, on the
-Llama-3-8B-shaped workload (B=32, H=32, Hkv=8, D=128, bs=16, L~U[512,2048],
-16384-block pool).  ``--workload`` selects the other shapes, ``--layout vllm``
+``pkv_decode_splitk``), with the split count from the heuristic.
+
+The headline (no flags) is the largest configuration, the long-context
+split-K decode: B=4, H=32, Hkv=8, D=128, bs=16, contexts of 32K/64K/96K/128K
+tokens, 1.34 GB of K/V per call (phase 1 over 10 splits, then the combine).
+Its JSON line carries ``sub_records`` for the other configurations, each
+timed the same way in the same run: the Llama-3-8B-shaped step (B=32,
+L~U[512,2048]), the large ragged batch (B=256, lognormal lengths), the
+128-step append+decode loop and the tiny case.  ``--workload`` makes another
+shape the headline (``--no-sub`` skips the records), ``--layout vllm`` uses
 the vLLM cache layout.
 
 The metric is KV bytes read per second (each token's K and V once, f16),
-with decode tokens/s and microseconds per call alongside.  Four independent
-pool sets (4.3 GB together, far above the 129 MB L2) rotate between steps so
-no step is served from L2.
+with decode tokens/s and microseconds per call alongside.  Workloads near
+L2's size (the Llama-3-8B step reads 174 MB against a 129 MB L2) rotate four
+independent pool sets between steps; the others read far more than L2 holds
+per call.
 
 ``--impl reference`` times the CPU oracle on the host cores (each step one
 whole decode call of the same workload, its sequences spread over one worker
-process per core) and prints the same JSON line with ``"impl": "reference"``.
+process per sequence, at most one per core) and prints the same JSON line
+with ``"impl": "reference"``.
 
 Under ``torchrun`` (N>1) every rank runs its own replica on its own GPU (the
 path has no exchange step); time is the max over ranks and ``value`` counts
@@ -226,8 +235,9 @@ def cpu_oracle_sample(w, seqs, kc, vc):
 
 # The oracle timed on the host: a fresh interpreter that never touches CUDA
 # builds the workload once, then forks one worker per host core (forking is
-# safe there: no GPU context exists in that process); each step is one whole
-# decode call of the workload (its 32 sequences spread over the workers).
+# safe there: no GPU context exists in that process), at most one per
+# sequence; each step is one whole decode call of the workload, its
+# sequences spread over the workers.
 _ORACLE_STATE = {}
 
 
@@ -236,17 +246,18 @@ def _oracle_one_seq(s):
     return cpu_oracle_sample(w, [s], kc, vc)[0]
 
 
-def oracle_child_main(mode, steps, warmup, budget_s):
+def oracle_child_main(mode, name, steps, warmup, budget_s):
     import multiprocessing as mp
 
     from paged_kv_decode_08_gb300 import workloads as W
 
-    w = W.llama8b()
+    w = W.make(name)
     kc, vc = W.host_pool(w)
     _ORACLE_STATE.update(w=w, kc=kc, vc=vc)
-    procs = os.cpu_count() or 1
-    seqs = list(range(w.num_seqs))
-    res = {"procs": procs}
+    # longest sequences first, so the pool's last tasks are the short ones
+    seqs = sorted(range(w.num_seqs), key=lambda s: -int(w.context_lens[s]))
+    procs = max(1, min(os.cpu_count() or 1, w.num_seqs))
+    res = {"procs": procs, "num_seqs": w.num_seqs, "kv_mb": w.kv_bytes / 1e6}
     if mode == "baseline":  # one core: whole decode calls in this process
         tot_b, tot_t, calls = 0, 0.0, 0
         while tot_t < budget_s / 2:
@@ -269,31 +280,31 @@ def oracle_child_main(mode, steps, warmup, budget_s):
     print(json.dumps(res), flush=True)
 
 
-def run_oracle_child(mode, steps=0, warmup=1, budget_s=12.0):
+def run_oracle_child(mode, name, steps=0, warmup=1, budget_s=12.0):
     env = dict(os.environ)
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         env[k] = "1"
     res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--oracle-child", mode,
-                          "--steps", str(steps), "--warmup", str(max(warmup, 3)),
-                          "--oracle-budget", str(budget_s)],
+                          "--workload", name, "--steps", str(steps),
+                          "--warmup", str(max(warmup, 3)), "--oracle-budget", str(budget_s)],
                          capture_output=True, text=True, env=env, timeout=1200)
     if res.returncode != 0:
         return None
     return json.loads(res.stdout.strip().splitlines()[-1])
 
 
-def cpu_baseline_subprocess(budget_s=12.0):
-    """The oracle on all host cores and on one (about budget_s of CPU time)."""
-    d = run_oracle_child("baseline", budget_s=budget_s)
+def cpu_baseline_subprocess(name, budget_s=12.0):
+    """The oracle on the host cores (one worker per sequence, at most one per
+    core) and on one core, about budget_s of CPU time."""
+    d = run_oracle_child("baseline", name, budget_s=budget_s)
     if d is None:
         return None
     a, o = d["all_cores"], d["one_core"]
-    per_call = a["bytes"] / a["calls"] / 1e6
     return {"value": a["bytes"] / a["seconds"] / 1e9, "unit": UNIT, "cores": d["procs"],
             "kind": "oracle",
-            "sample": f"{a['calls']} full decode call(s) of the workload (32 sequences, "
-                      f"{per_call:.0f} MB of K/V each) in float64, sequences spread over "
-                      f"{d['procs']} worker processes, {a['seconds']:.1f} s",
+            "sample": f"{a['calls']} full decode call(s) of the workload ({d['num_seqs']} "
+                      f"sequences, {d['kv_mb']:.0f} MB of K/V each) in float64, sequences "
+                      f"spread over {d['procs']} worker processes, {a['seconds']:.1f} s",
             "one_core": {"value": o["bytes"] / o["seconds"] / 1e9, "unit": UNIT, "cores": 1,
                          "sample": f"{o['calls']} full decode call(s) on one host thread, "
                                    f"{o['seconds']:.1f} s"}}
@@ -301,25 +312,28 @@ def cpu_baseline_subprocess(budget_s=12.0):
 
 def run_reference(args):
     """The oracle on the host cores: each step one whole decode call of the
-    workload, its sequences spread over one worker process per core."""
+    workload, its sequences spread over one worker process per sequence (at
+    most one per core)."""
     world, rank, _ = dist_setup()
     if rank != 0:
         return
-    d = run_oracle_child("reference", steps=args.steps, warmup=args.warmup)
+    name = args.workload
+    d = run_oracle_child("reference", name, steps=args.steps, warmup=args.warmup)
     if d is None:
         print(json.dumps({"impl": "reference", "unavailable": "the oracle child process failed"}),
               flush=True)
         return
     a = d["all_cores"]
     value = a["bytes"] / a["seconds"] / 1e9
-    sample = (f"whole decode calls (32 sequences) per step, float64 numpy oracle, sequences "
-              f"spread over {d['procs']} worker processes")
+    sample = (f"whole decode calls ({d['num_seqs']} sequences, {d['kv_mb']:.0f} MB of K/V) per "
+              f"step, float64 numpy oracle, sequences spread over {d['procs']} worker processes")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": a["calls"], "warmup": args.warmup, "ms_per_step": a["seconds"] / a["calls"] * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD_DESC["llama8b"], "sample_per_step": "all 32 sequences"},
+        "config": {"workload": WORKLOAD_DESC[name],
+                   "sample_per_step": f"all {d['num_seqs']} sequences"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": d["procs"], "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -343,7 +357,7 @@ def run_qkv(args):
     torch.cuda.set_device(dev)
     H, Hkv, D, bs = 32, 8, 128, 16
     c = W.qkv_case(BASE_QKV_SEED, H, Hkv, D, bs, [2048] * 4, [0] * 4)
-    n_sets = args.sets
+    n_sets = args.sets or N_SETS
     g = torch.Generator(device=dev)
     sets = []
     for r in range(n_sets):
@@ -432,7 +446,7 @@ def run_step_qkv(args):
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
     w = W.make("llama8b")
-    n_sets = args.sets
+    n_sets = args.sets or N_SETS
     sets = build_sets(w, dev, n_sets)
     lens = w.context_lens.astype(np.int64)
     c = W.qkv_case(BASE_QKV_SEED + 1, w.num_heads, w.num_kv_heads, w.head_dim, w.block_size,
@@ -550,17 +564,23 @@ def build_sets(w, dev, n_sets, layout="blocked"):
 
 
 def run_loop(args):
+    world, rank, local = dist_setup()
+    line = measure_loop(args, local, world, rank)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+def measure_loop(args, local, world, rank):
     """The append+decode loop: every step appends one token per sequence
     (plus padding rows) and decodes over the grown contexts.  All 128 steps'
     inputs are uploaded first; the whole loop is one CUDA graph, replayed
     (re-appending the same rows to the same slots, so every replay does the
-    same work)."""
+    same work).  Returns the JSON line (rank 0) or None."""
     import torch
 
     from paged_kv_decode_08_gb300 import pagedkv as pk
     from paged_kv_decode_08_gb300 import workloads as W
 
-    world, rank, local = dist_setup()
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
     loop = W.AppendDecodeLoop()
@@ -625,8 +645,9 @@ def run_loop(args):
         step_ms = timed(g_loop)
         append_ms = timed(g_append)
         decode_ms = timed(g_decode)
+    flags = pk.pkv_read_device_status()
     if rank != 0:
-        return
+        return None
     kv_bytes = sum(loop.kv_bytes_per_step) / loop.steps
     peak, peak_kind = measured_peaks()
     achieved = kv_bytes / (decode_ms * 1e-3) / 1e9
@@ -646,9 +667,9 @@ def run_loop(args):
                      "frac": achieved / peak, "peak_source": peak_kind,
                      "kernel": "decode call", "traffic": None},
         "clocks": clocks.summary(), "gpu_launches": reps * loop.steps * (1 + (2 if S > 1 else 1)),
-        "device_status_flags": pk.pkv_read_device_status(), "e2e": None, "cpu_baseline": None,
+        "device_status_flags": flags, "e2e": None, "cpu_baseline": None,
     }
-    print(json.dumps(line), flush=True)
+    return line
 
 
 def run_varlen(args):
@@ -669,15 +690,14 @@ def run_varlen(args):
     torch.cuda.set_device(dev)
     v = W.spec_verify_long() if args.workload == "spec_long" else W.spec_verify()
     w = v.base
-    sets = build_sets(w, dev, args.sets)
+    n_sets = args.sets or N_SETS
+    sets = build_sets(w, dev, n_sets)
     q = torch.from_numpy(v.q).to(dev)
     cu = torch.from_numpy(v.cu_seqlens_q).to(dev)
     pos = torch.from_numpy(v.pos_offsets).to(dev)
     out = torch.empty_like(q)
-    n_sets = args.sets
-    S = pk.varlen_splits_for(q, sets[0]["k_cache"], sets[0]["block_tables"], w.num_kv_heads,
-                             v.max_q_len, args.splits)
-    n = pk.pkv_splitk_scratch_bytes(v.total_q, w.num_heads, w.head_dim, S) if S > 1 else 0
+    S, n = pk._varlen_plan(q, sets[0]["k_cache"], sets[0]["block_tables"], v.max_q_len,
+                           args.splits)
     scratch = torch.empty(max(n, 16), dtype=torch.uint8, device=dev)
 
     def call(i):
@@ -743,26 +763,20 @@ def run_varlen(args):
     print(json.dumps(line), flush=True)
 
 
-def run_ours(args):
+def measure_step(args, name, dev, dist, world, rank, n_sets, want_e2e, want_cpu):
+    """One decode step of workload `name` (the fused append + decode, or with
+    --separate / --layout vllm the append then the decode), timed as CUDA
+    graph replays over `n_sets` rotating pool sets, plus the decode call
+    alone; with `want_e2e` also end to end from host buffers.  Returns the
+    JSON line (rank 0) or None."""
     import torch
 
     from paged_kv_decode_08_gb300 import pagedkv as pk
     from paged_kv_decode_08_gb300 import workloads as W
 
-    world, rank, local = dist_setup()
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-
-        dist.init_process_group("nccl")
-    dev = torch.device(f"cuda:{local}")
-    torch.cuda.set_device(dev)
-
-    w = W.make(args.workload)
-    n_sets = args.sets
+    w = W.make(name)
     vllm = args.layout == "vllm"
-    if vllm:
-        args.separate = True  # no fused append on the vLLM layout
+    separate = args.separate or vllm  # no fused append on the vLLM layout
     sets = build_sets(w, dev, n_sets, args.layout)
     append_call = pk.pkv_append_vllm_layout if vllm else pk.pkv_append
     decode_call = pk.pkv_decode_vllm_layout if vllm else pk.pkv_decode_splitk
@@ -776,11 +790,11 @@ def run_ours(args):
     out = torch.empty_like(q)
     stream = torch.cuda.current_stream()
     kv_bytes = w.kv_bytes
-    launches_per_step = (1 if args.separate else 0) + (2 if S > 1 else 1)
+    launches_per_step = (1 if separate else 0) + (2 if S > 1 else 1)
 
     def step(i):
         st = sets[i % n_sets]
-        if args.separate:
+        if separate:
             append_call(k_new_d, v_new_d, slots_d, st["k_cache"], st["v_cache"])
             decode_call(q, st["k_cache"], st["v_cache"], bt, cl, w.scale,
                         num_splits=args.splits, scratch=scratch, out=out)
@@ -833,7 +847,7 @@ def run_ours(args):
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(local) as clocks:
+    with ClockSampler(dev.index) as clocks:
         total_ms, step_rounds = timed(g_step)
         decode_total_ms, decode_rounds = timed(g_decode)
     if dist is not None:
@@ -847,7 +861,7 @@ def run_ours(args):
     # pinned buffer, to the device in one copy, runs the step on views of
     # that device buffer, and copies the output back to pinned memory.
     e2e = None
-    if not args.no_e2e:
+    if want_e2e:
         import numpy as np
 
         parts = [("q", np.ascontiguousarray(w.q)), ("k", np.ascontiguousarray(k_new)),
@@ -855,16 +869,17 @@ def run_ours(args):
                  ("bt", np.ascontiguousarray(w.block_tables)),
                  ("cl", np.ascontiguousarray(w.context_lens))]
         offs, cur = {}, 0
-        for name, a in parts:
-            offs[name] = cur
+        for pname, a in parts:
+            offs[pname] = cur
             cur += (a.nbytes + 255) // 256 * 256
         h_buf = torch.empty(cur, dtype=torch.uint8).pin_memory()
-        for name, a in parts:
-            h_buf[offs[name]:offs[name] + a.nbytes] = torch.from_numpy(a.view(np.uint8).reshape(-1))
+        for pname, a in parts:
+            h_buf[offs[pname]:offs[pname] + a.nbytes] = torch.from_numpy(
+                a.view(np.uint8).reshape(-1))
         d_buf = torch.empty(cur, dtype=torch.uint8, device=dev)
 
-        def view(name, a, dtype):
-            return d_buf[offs[name]:offs[name] + a.nbytes].view(dtype).view(a.shape)
+        def view(pname, a, dtype):
+            return d_buf[offs[pname]:offs[pname] + a.nbytes].view(dtype).view(a.shape)
 
         d_q = view("q", w.q, torch.float16)
         d_k = view("k", k_new, torch.float16)
@@ -879,7 +894,7 @@ def run_ours(args):
         def e2e_step(i):
             st = sets[i % n_sets]
             d_buf.copy_(h_buf, non_blocking=True)
-            if args.separate:
+            if separate:
                 append_call(d_k, d_v, d_s, st["k_cache"], st["v_cache"], stream=stream)
                 decode_call(d_q, st["k_cache"], st["v_cache"], d_bt, d_cl, w.scale,
                             num_splits=args.splits, scratch=scratch, out=out, stream=stream)
@@ -908,46 +923,45 @@ def run_ours(args):
 
     flags = pk.pkv_read_device_status()
     if rank != 0:
-        if dist is not None:
-            dist.destroy_process_group()
-        return
+        return None
     ms_per_step = total_ms / steps
     value = job_throughput(kv_bytes, world, ms_per_step)
-    dec_avg_ms = decode_ms
     # The dominant kernel: the step's single fused launch when it is one
     # (pkv_append_decode, single pass), else the decode call (phase 1 +
     # combine when split) timed on its own.
-    one_launch = not args.separate and S == 1
-    kernel_ms = ms_per_step if one_launch else dec_avg_ms
+    one_launch = not separate and S == 1
+    kernel_ms = ms_per_step if one_launch else decode_ms
     achieved = kv_bytes / (kernel_ms * 1e-3) / 1e9
     peak, peak_kind = measured_peaks()
     traffic = None
-    tr = NCU_TRAFFIC.get(args.workload)
+    tr = NCU_TRAFFIC.get(name)
     if (tr and tr.get("kernel_hash") == kernel_source_hash() and S == tr.get("num_splits")
             and one_launch == tr.get("fused", False) and tr.get("layout", "blocked") == args.layout):
         traffic = tr["bytes_per_launch"]
-    cpu = None if args.no_cpu_baseline else cpu_baseline_subprocess()
+    cpu = cpu_baseline_subprocess(name) if want_cpu else None
+    l2_bytes = n_sets * 2 * sets[0]["k_cache"].numel() * 2
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
-        "config": {"workload": WORKLOAD_DESC[args.workload],
+        "config": {"workload": WORKLOAD_DESC[name],
                    "step": (f"pkv_append_vllm_layout ({w.num_seqs} tokens) + "
                             "pkv_decode_vllm_layout (vLLM cache layout)" if vllm else
                             f"pkv_append ({w.num_seqs} tokens) + pkv_decode_splitk"
-                            if args.separate else
+                            if separate else
                             f"pkv_append_decode (slot-mapped append of the {w.num_seqs} "
                             "newest tokens fused with the decode)")
                            + f", split count {'heuristic' if args.splits == 0 else 'forced'}",
                    "num_splits": S,
-                   "launch": f"CUDA graph of {n_sets} steps (one per pool set), replayed",
-                   "l2": f"{n_sets} rotating pool set(s) ({n_sets * 2 * sets[0]['k_cache'].numel() * 2 / 1e9:.1f} GB; "
-                         f"{kv_bytes / 1e6:.0f} MB of K/V read per step) vs 129 MB L2",
+                   "launch": f"CUDA graph of {n_sets} step(s) (one per pool set), replayed",
+                   "l2": (f"{n_sets} rotating pool set(s) ({l2_bytes / 1e9:.1f} GB; "
+                          f"{kv_bytes / 1e6:.0f} MB of K/V read per step) vs 129 MB L2"
+                          + ("" if n_sets > 1 else ": inputs larger than L2")),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "kv_bytes_per_step": kv_bytes,
         "decode_tokens_per_s": world * w.num_seqs / (ms_per_step * 1e-3),
         "us_per_step": ms_per_step * 1e3,
-        "decode_us_per_call": dec_avg_ms * 1e3,
+        "decode_us_per_call": decode_ms * 1e3,
         # per replay of the graph (n_sets steps), divided by n_sets
         "us_per_step_median": 1e3 * statistics.median(step_rounds) / n_sets,
         "us_per_step_min": 1e3 * min(step_rounds) / n_sets,
@@ -958,8 +972,8 @@ def run_ours(args):
                      "frac": achieved / peak, "peak_source": peak_kind,
                      "kernel": ("the step's single launch (fused append + single-pass decode), "
                                 "timed as a graph of back-to-back steps" if one_launch else
-                                "decode call (single-pass kernel, or phase 1 + combine when "
-                                "split), timed as a graph of back-to-back decode calls"),
+                                "decode call (single-pass kernel, or split-K phase 1 + combine "
+                                "when split), timed as a graph of back-to-back decode calls"),
                      "traffic": traffic,
                      "traffic_kernel": tr["kernel"] if traffic is not None else None},
         "clocks": clocks.summary(),
@@ -968,7 +982,64 @@ def run_ours(args):
         "e2e": e2e,
         "cpu_baseline": cpu,
     }
-    print(json.dumps(line), flush=True)
+    return line
+
+
+def sub_record(line, name):
+    """The per-config summary kept beside the headline: time per call and
+    step, bytes, roofline fraction and the clock record of that run."""
+    peak, _ = measured_peaks()
+    dec_us = line.get("decode_us_per_call", line["us_per_step"])
+    kv = line["kv_bytes_per_step"]
+    return {"workload": line["config"]["workload"], "name": name,
+            "num_splits": line["config"].get("num_splits"),
+            "us_per_call": dec_us, "us_per_step": line["us_per_step"], "kv_bytes": kv,
+            "kv_gbs": kv / (dec_us * 1e-6) / 1e9,
+            "frac": line["roofline"]["frac"], "frac_kernel": line["roofline"]["kernel"],
+            "frac_of_decode_call": kv / (dec_us * 1e-6) / 1e9 / peak,
+            "decode_tokens_per_s": line["decode_tokens_per_s"],
+            "traffic": line["roofline"].get("traffic"),
+            "gpu_launches": line["gpu_launches"], "steps": line["steps"],
+            "clocks": line["clocks"], "device_status_flags": line["device_status_flags"]}
+
+
+# Configurations timed beside the headline (name, rotating pool sets): the
+# Llama-3-8B step reads 174 MB, near L2's 129 MB, so its pools rotate; the
+# others read 0.8-1.3 GB per call, far above L2.
+SUB_CONFIGS = [("llama8b", N_SETS), ("ragged", 1), ("loop", None), ("tiny", N_SETS)]
+
+
+def run_ours(args):
+    import torch
+
+    world, rank, local = dist_setup()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+
+    name = args.workload
+    n_sets = args.sets if args.sets else (1 if name in ("long", "ragged") else N_SETS)
+    line = measure_step(args, name, dev, dist, world, rank, n_sets, want_e2e=not args.no_e2e,
+                        want_cpu=not args.no_cpu_baseline)
+    torch.cuda.empty_cache()
+    subs = []
+    if not args.no_sub and world == 1 and name == "long":
+        for sub, sets in SUB_CONFIGS:
+            if sub == "loop":
+                r = measure_loop(args, local, world, rank)
+            else:
+                r = measure_step(args, sub, dev, None, world, rank, sets, want_e2e=False,
+                                 want_cpu=False)
+            torch.cuda.empty_cache()
+            if r is not None:
+                subs.append(sub_record(r, sub))
+    if rank == 0:
+        line["sub_records"] = subs
+        print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
 
@@ -980,8 +1051,14 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--splits", type=int, default=0, help="0 = heuristic")
-    ap.add_argument("--sets", type=int, default=N_SETS, help="rotating pool sets")
-    ap.add_argument("--workload", choices=sorted(WORKLOAD_DESC), default="llama8b")
+    ap.add_argument("--sets", type=int, default=0,
+                    help="rotating pool sets (0 = 4 for workloads near L2's size, 1 for those "
+                         "far above it)")
+    ap.add_argument("--workload", choices=sorted(WORKLOAD_DESC), default="long",
+                    help="the headline workload (default: the long-context split-K decode, "
+                         "the largest configuration)")
+    ap.add_argument("--no-sub", action="store_true",
+                    help="skip the per-configuration records timed beside the headline")
     ap.add_argument("--separate", action="store_true",
                     help="step = pkv_append then pkv_decode_splitk (two calls) instead of "
                          "the fused pkv_append_decode")
@@ -995,7 +1072,8 @@ def main():
     ap.add_argument("--oracle-budget", type=float, default=12.0, help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.oracle_child:
-        oracle_child_main(args.oracle_child, args.steps, args.warmup, args.oracle_budget)
+        oracle_child_main(args.oracle_child, args.workload, args.steps, args.warmup,
+                          args.oracle_budget)
         return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

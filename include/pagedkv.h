@@ -15,9 +15,11 @@
  *
  * Conventions for every call
  *   - Pointers named "device" are CUDA device pointers (or managed memory).
- *     The caller owns every buffer.  The library allocates nothing per call;
- *     its only memory is one 32-bit device status word per GPU (see
- *     pkv_read_device_status).
+ *     The caller owns every buffer.  The library allocates nothing per call.
+ *     Its own device memory is static, declared in the library and held by
+ *     every GPU that loads it until the process exits: one 32-bit status
+ *     word (see pkv_read_device_status) and the PKV_NOALLOC_SCRATCH_BYTES
+ *     buffer of pkv_decode_splitk_noalloc.
  *   - f16 is IEEE binary16 (2 bytes).  All arrays are dense, row-major,
  *     with no padding between rows.
  *   - KV cache layout: k_cache and v_cache are each
@@ -131,8 +133,15 @@ pkv_status pkv_decode(const void* q, const void* k_cache, const void* v_cache,
  *
  *   num_splits    0 = pick with pkv_pick_num_splits for the current GPU; 1 =
  *                 run the single-pass kernel (no scratch needed);
- *                 2..PKV_MAX_SPLITS = forced fixed chunks of
- *                 ceil(max_blocks_per_seq / num_splits) blocks;
+ *                 2..PKV_MAX_SPLITS = that many splits (at most
+ *                 max_blocks_per_seq; pkv_decode_splitk_plan gives the count
+ *                 launched).  The chunks are cut on the GPU from the longest
+ *                 context in context_lens, Lmax: split k takes blocks
+ *                 [k c, (k+1) c) of every sequence, c = ceil(ceil(Lmax /
+ *                 block_size) / S) blocks (with num_splits = 0, at least
+ *                 256 tokens' worth), so tables sized beyond the contexts
+ *                 they hold still spread the work; splits past a sequence's
+ *                 end do no work;
  *                 PKV_SPLITS_BALANCED = the balanced schedule: the list of
  *                 all (sequence, kv head, block) tiles is cut into equal
  *                 contiguous ranges, one per resident CTA (at most
@@ -140,9 +149,10 @@ pkv_status pkv_decode(const void* q, const void* k_cache, const void* v_cache,
  *                 context_lens, so every CTA reads the same number of bytes
  *                 whatever the mix of lengths; (sequence, head) runs cut by a
  *                 range boundary are merged by a second kernel.
- *   scratch       device memory of at least
- *                 pkv_splitk_scratch_bytes(num_seqs, num_heads, head_dim, S)
- *                 bytes, 16-byte aligned, caller-owned; its contents need no
+ *   scratch       device memory of at least the bytes pkv_decode_splitk_plan
+ *                 returns for these sizes and num_splits
+ *                 (pkv_splitk_scratch_bytes of the split count launched),
+ *                 16-byte aligned, caller-owned; its contents need no
  *                 initialisation and are overwritten.  Calls that overlap on
  *                 the GPU must not share scratch.
  *   other arguments as pkv_decode.
@@ -300,13 +310,16 @@ pkv_status pkv_varlen_attention_vllm_layout(
  *                 split count that brings it nearest one wave, capped so a
  *                 split keeps >= 256 tokens of max_blocks_per_seq *
  *                 block_size, at most 64; else 1.  1 = no split (no scratch
- *                 needed); 2..PKV_MAX_SPLITS = chunks of
- *                 ceil(max_blocks_per_seq / num_splits) blocks.
- *   scratch       device memory of at least
- *                 pkv_splitk_scratch_bytes(total_q, num_heads, head_dim, S)
- *                 bytes (total_q in the num_seqs slot), 16-byte aligned,
- *                 caller-owned, no initialisation needed; calls that overlap
- *                 on the GPU must not share it.
+ *                 needed); 2..PKV_MAX_SPLITS = that many splits (at most
+ *                 max_blocks_per_seq).  As in pkv_decode_splitk the chunks
+ *                 are cut on the GPU: c = ceil(n / S) blocks, n the most
+ *                 blocks any chunk of queries reads (with num_splits = 0, at
+ *                 least 256 tokens' worth).
+ *   scratch       device memory of at least the bytes pkv_varlen_splitk_plan
+ *                 returns (pkv_splitk_scratch_bytes(total_q, num_heads,
+ *                 head_dim, S) for the split count launched), 16-byte
+ *                 aligned, caller-owned, no initialisation needed; calls that
+ *                 overlap on the GPU must not share it.
  *   other arguments, results and flags as pkv_varlen_attention.
  *
  * Returns PKV_ERR_SCRATCH_TOO_SMALL when S > 1 and the scratch is null or
@@ -456,14 +469,53 @@ size_t pkv_splitk_scratch_bytes(int32_t num_seqs, int32_t num_heads, int32_t hea
  * enough CTAs to fill the SMs; once the base grid saturates them, splitting
  * pays only for long contexts).  Here the base grid is num_seqs *
  * num_kv_heads (one CTA per sequence and KV head covers the whole group),
- * measured against num_sms.  max_context_len is the longest context the call
- * may see (pkv_decode_splitk passes max_blocks_per_seq * block_size).
- * Returns 1 (single pass), a split count in 2..64, or PKV_SPLITS_BALANCED;
- * 1 for invalid sizes.
+ * measured against num_sms x 2 resident CTAs.  max_context_len is the
+ * longest context the call may see (pkv_decode_splitk passes
+ * max_blocks_per_seq * block_size; the host never reads context_lens).
+ * Below one wave: the split count that brings the grid nearest one wave;
+ * at or above it: ceil(max_context_len / 2048); either capped at
+ * max_context_len / 256, the block count and 64.  Returns 1 (single pass)
+ * or a split count in 2..64 (never PKV_SPLITS_BALANCED); 1 for invalid
+ * sizes.
  */
 int32_t pkv_pick_num_splits(int32_t num_seqs, int32_t num_kv_heads,
                             int32_t max_context_len, int32_t block_size,
                             int32_t num_sms);
+
+/*
+ * pkv_decode_splitk_plan — what pkv_decode_splitk (and pkv_append_decode,
+ * pkv_decode_vllm_layout, pkv_qkv_norm_rope_append_decode) will launch for
+ * these sizes and num_splits, so a caller can size its scratch without
+ * repeating the library's rules (ferrum-kernels src/backend/cuda/paged.rs
+ * sizes its process-global split scratch from the split count it picks;
+ * here the caller sizes it).
+ *
+ *   *splits         1 (single pass), the split count launched
+ *                   (2..PKV_MAX_SPLITS; num_splits capped at
+ *                   max_blocks_per_seq), or PKV_SPLITS_BALANCED
+ *   *scratch_bytes  the scratch that call needs (0 for single pass)
+ *
+ * num_splits = 0 applies pkv_pick_num_splits for the current GPU (the one
+ * query this makes to CUDA, for the SM count); no other CUDA call.  Returns
+ * PKV_ERR_INVALID_ARG for null outputs, invalid sizes or num_splits outside
+ * -1..PKV_MAX_SPLITS.
+ */
+pkv_status pkv_decode_splitk_plan(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                                  int32_t head_dim, int32_t max_blocks_per_seq,
+                                  int32_t block_size, int32_t num_splits, int32_t* splits,
+                                  size_t* scratch_bytes);
+
+/*
+ * pkv_varlen_splitk_plan — the same for pkv_varlen_attention_splitk (and its
+ * vLLM-layout twin): *splits is 1 or the split count launched, and
+ * *scratch_bytes the scratch needed (0 when unsplit or when the call has no
+ * queries).  num_splits 0..PKV_MAX_SPLITS (0 = pkv_varlen_pick_num_splits on
+ * the current GPU).
+ */
+pkv_status pkv_varlen_splitk_plan(int32_t num_seqs, int32_t total_q, int32_t max_q_len,
+                                  int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                                  int32_t max_blocks_per_seq, int32_t block_size,
+                                  int32_t num_splits, int32_t* splits, size_t* scratch_bytes);
 
 /*
  * pkv_decode_splitk_noalloc — pkv_decode_splitk without caller scratch and
@@ -487,7 +539,7 @@ int32_t pkv_pick_num_splits(int32_t num_seqs, int32_t num_kv_heads,
  * Arguments and result are those of pkv_decode_splitk (num_splits 0 = the
  * heuristic, 1 = single pass).  Returns PKV_ERR_SCRATCH_TOO_SMALL, before any
  * launch, when the partials for the chosen split count need more than
- * PKV_NOALLOC_SCRATCH_BYTES (pkv_splitk_scratch_bytes gives the need); call
+ * PKV_NOALLOC_SCRATCH_BYTES (pkv_decode_splitk_plan gives the need); call
  * pkv_decode_splitk with caller-owned scratch, or fewer splits, instead.
  */
 #define PKV_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)

@@ -343,8 +343,15 @@ struct DecodeParams {
   int group;
   int max_blocks_per_seq;
   int num_blocks;
-  int num_splits;    // S (1 for single pass)
-  int chunk_blocks;  // blocks per split
+  int num_splits;  // S (1 for single pass)
+  // Split-K chunks are cut on the device from the longest context of the
+  // call: chunk = max(min_chunk_blocks, ceil(ceil(Lmax / BS) / S)) blocks,
+  // so tables sized for a larger maximum context than the call holds still
+  // spread the work over every split.  chunk_hint is the host's guess
+  // (ceil(max_blocks_per_seq / S)); when it is right the first table entry
+  // of a split is loaded before Lmax is known.
+  int min_chunk_blocks;
+  int chunk_hint;
   float scale_log2;  // scale * log2(e)
   // Fair-share depth (set when the whole grid is resident at once): a CTA
   // keeps copies in flight in proportion to its share of the longest chunk
@@ -860,23 +867,28 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   // Every independent global load of the prologue goes out together: the
   // status word, the length, the warp's first block-table entry (its first
   // tile is the chunk's block `warp` whatever the fair share decides; the
-  // entry is in bounds and only used if the tile exists), the lengths for
-  // the fair share and the fused slot.
+  // entry is in bounds and only used if the tile exists; split kernels load
+  // it under the host's chunk guess), every length (the longest context sets
+  // the split chunks and the fair share) and the fused slot.
   const int cap = p.max_blocks_per_seq * BS;
   const int32_t* table = p.block_tables + (size_t)s * p.max_blocks_per_seq;
   const unsigned int status = *reinterpret_cast<volatile unsigned int*>(&g_device_status);
   int L = __ldg(p.context_lens + s);
-  const int j0 = (SPLIT ? split * p.chunk_blocks : 0) + warp;
-  const int phys0 = (lane == 0 && j0 < p.max_blocks_per_seq) ? __ldg(table + j0) : -1;
-  int mx = 0;
-  if (p.fair_depth) {
+  const int j0_guess = (SPLIT ? split * p.chunk_hint : 0) + warp;
+  const int phys0_guess =
+      (lane == 0 && j0_guess < p.max_blocks_per_seq) ? __ldg(table + j0_guess) : -1;
+  __shared__ int s_max[W];
+  const bool need_max = SPLIT || p.fair_depth;
+  if (need_max) {
+    int mx = 0;
     for (int i = threadIdx.x; i < p.num_seqs; i += W * 32) {
       int Li = __ldg(p.context_lens + i);
       Li = Li < 0 ? 0 : (Li > cap ? cap : Li);
-      int ni = (Li + BS - 1) / BS;
-      if (SPLIT && ni > p.chunk_blocks) ni = p.chunk_blocks;
-      mx = max(mx, ni);
+      mx = max(mx, (Li + BS - 1) / BS);
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) s_max[warp] = mx;
   }
   const int slot_new = FUSE ? __ldg(p.new_slots + s) : -1;
   // QKV: the loads that need no length go out with the rest: the warp's
@@ -902,8 +914,15 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
 
   // After a lost copy has been flagged, later CTAs do no work (and write
   // nothing) until the host reads and clears the status word.  The decision
-  // is made for the whole CTA at once.
+  // is made for the whole CTA at once.  (The barrier also publishes s_max.)
   if (__syncthreads_or(status & kDevWaitTimeout)) return;
+  int nblk_max = 0;  // the call's longest context, in blocks
+  if (need_max) {
+#pragma unroll
+    for (int w = 0; w < W; ++w) nblk_max = max(nblk_max, s_max[w]);
+  }
+  const int chunk = SPLIT ? max(p.min_chunk_blocks, (nblk_max + p.num_splits - 1) / p.num_splits)
+                          : p.max_blocks_per_seq;
 
   if (L < 0 || L > cap) {
     if (threadIdx.x == 0) atomicOr(&g_device_status, kDevBadContextLen);
@@ -921,25 +940,34 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   int tok_begin = 0;
   int tok_end = L;
   if (SPLIT) {
-    tok_begin = split * p.chunk_blocks * BS;
-    if (tok_begin >= L) return;  // empty split: the combine never reads it
-    tok_end = min(L, tok_begin + p.chunk_blocks * BS);
+    if ((long long)split * chunk * BS >= L) {
+      // Empty split: max -inf and sum 0 for the group's heads, so the
+      // combine can read every split (it gives these weight 0).
+      for (int h = threadIdx.x; h < p.group; h += W * 32) {
+        const size_t slot =
+            ((size_t)s * p.num_heads + (size_t)g * p.group + h) * p.num_splits + split;
+        p.part_m[slot] = -CUDART_INF_F;
+        p.part_l[slot] = 0.f;
+      }
+      return;
+    }
+    tok_begin = split * chunk * BS;
+    tok_end = (int)min((long long)L, (long long)tok_begin + (long long)chunk * BS);
   }
   const int blk_begin = tok_begin / BS;
   const int n_tiles = (tok_end - tok_begin + BS - 1) / BS;
+  // the first tile's table entry: the prologue's guess when it was right
+  const int phys0 = (!SPLIT || split == 0 || chunk == p.chunk_hint)
+                        ? phys0_guess
+                        : ((lane == 0 && blk_begin + warp < p.max_blocks_per_seq)
+                               ? __ldg(table + blk_begin + warp)
+                               : -1);
 
   // Warps that take tiles: all W, or (fair share) W scaled by this chunk's
   // tiles over the longest chunk of the call.
   int WE = W;
   if (p.fair_depth) {
-    __shared__ int s_max[W];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if (lane == 0) s_max[warp] = mx;
-    __syncthreads();
-    mx = 0;
-#pragma unroll
-    for (int w = 0; w < W; ++w) mx = max(mx, s_max[w]);
+    const int mx = SPLIT ? min(nblk_max, chunk) : nblk_max;
     if (mx > 0) WE = max(1, min(W, (W * n_tiles + mx - 1) / mx));
   }
   const int my_tiles = (warp < WE && n_tiles > warp) ? (n_tiles - warp + WE - 1) / WE : 0;
@@ -1166,13 +1194,15 @@ struct VarlenParams {
   int num_seqs;
   int fair_depth;  // the grid is resident at once: scale in-flight depth
   const __half* k_pool;  // the K pool (vLLM layout: tiles are bulk-copied from it)
-  // split-K (SPLIT kernels): chunk_blocks blocks of context per split; f32
-  // partials per (query token, head, split)
+  // split-K (SPLIT kernels): f32 partials per (query token, head, split);
+  // each split takes chunk = max(min_chunk_blocks, ceil(n / S)) blocks of
+  // context, n the most blocks any chunk of queries reads in the call (cut
+  // on the device, as the decode kernel cuts its chunks)
   float* part_out;  // [total_q][H][S][D]
   float* part_m;    // [total_q][H][S]  base-2 running max
   float* part_l;    // [total_q][H][S]  running sum
   int num_splits;
-  int chunk_blocks;
+  int min_chunk_blocks;
   int max_blocks_per_seq;
   int num_blocks;
   float scale_log2;
@@ -1223,20 +1253,30 @@ paged_varlen_kernel(const __grid_constant__ CUtensorMap kmap,
   const int q_begin = __ldg(p.cu_seqlens_q + s);
   const int q_end = __ldg(p.cu_seqlens_q + s + 1);
   int pos0 = __ldg(p.pos_offsets + s);
-  // fair share (as in the decode kernel): the longest context any chunk of
-  // the call reads, in tiles
-  int mx = 0;
-  if (p.fair_depth) {
+  // the longest context any chunk of the call reads, in tiles (sets the
+  // split chunks and, as in the decode kernel, the fair share)
+  __shared__ int s_max[W];
+  const bool need_max = SPLIT || p.fair_depth;
+  if (need_max) {
+    int mx = 0;
     for (int i = threadIdx.x; i < p.num_seqs; i += W * 32) {
       int last = __ldg(p.pos_offsets + i) + __ldg(p.cu_seqlens_q + i + 1) -
                  __ldg(p.cu_seqlens_q + i);
       last = last < 0 ? 0 : (last > cap ? cap : last);
-      int ni = (last + BS - 1) / BS;
-      if (SPLIT && ni > p.chunk_blocks) ni = p.chunk_blocks;
-      mx = max(mx, ni);
+      mx = max(mx, (last + BS - 1) / BS);
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) s_max[warp] = mx;
   }
-  if (__syncthreads_or(status & kDevWaitTimeout)) return;
+  if (__syncthreads_or(status & kDevWaitTimeout)) return;  // also publishes s_max
+  int nblk_max = 0;
+  if (need_max) {
+#pragma unroll
+    for (int w = 0; w < W; ++w) nblk_max = max(nblk_max, s_max[w]);
+  }
+  const int chunk = SPLIT ? max(p.min_chunk_blocks, (nblk_max + p.num_splits - 1) / p.num_splits)
+                          : p.max_blocks_per_seq;
 
   // bad query ranges or positions are flagged and skipped / clamped
   if (q_begin < 0 || q_end < q_begin || q_end > p.total_q) {
@@ -1256,26 +1296,29 @@ paged_varlen_kernel(const __grid_constant__ CUtensorMap kmap,
   // positions this chunk of queries reads; with SPLIT, this CTA's slice of
   // them (a split starting at or past the end is never written nor read)
   const int chunk_end = min(cap, pos0 + t0 + nq);
+  const int ncols = nq * G;  // (query, head) columns of this chunk
   int tok_begin = 0;
   int tok_end = chunk_end;
   if (SPLIT) {
-    tok_begin = split * p.chunk_blocks * BS;
-    if (tok_begin >= chunk_end) return;
-    tok_end = min(chunk_end, tok_begin + p.chunk_blocks * BS);
+    if ((long long)split * chunk * BS >= chunk_end) {
+      // Empty split: max -inf and sum 0 for every column, so the combine can
+      // read every split (it gives these weight 0).
+      for (int n = threadIdx.x; n < ncols; n += W * 32) {
+        const size_t row = (size_t)(q_begin + t0 + n / G) * p.num_heads + (size_t)g * G + n % G;
+        p.part_m[row * p.num_splits + split] = -CUDART_INF_F;
+        p.part_l[row * p.num_splits + split] = 0.f;
+      }
+      return;
+    }
+    tok_begin = split * chunk * BS;
+    tok_end = (int)min((long long)chunk_end, (long long)tok_begin + (long long)chunk * BS);
   }
   const int blk_begin = tok_begin / BS;
   const int n_tiles = (tok_end - tok_begin + BS - 1) / BS;
   const int32_t* table = p.block_tables + (size_t)s * p.max_blocks_per_seq;
   int WE = W;  // warps that take tiles (fewer for short chunks under the fair share)
   if (p.fair_depth) {
-    __shared__ int s_max[W];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if (lane == 0) s_max[warp] = mx;
-    __syncthreads();
-    mx = 0;
-#pragma unroll
-    for (int w = 0; w < W; ++w) mx = max(mx, s_max[w]);
+    const int mx = SPLIT ? min(nblk_max, chunk) : nblk_max;
     if (mx > 0) WE = max(1, min(W, (W * n_tiles + mx - 1) / mx));
   }
   const int my_tiles = (warp < WE && n_tiles > warp) ? (n_tiles - warp + WE - 1) / WE : 0;
@@ -1301,7 +1344,6 @@ paged_varlen_kernel(const __grid_constant__ CUtensorMap kmap,
 
   // column n = (query t0 + n / G, head n % G) while n < nq * G; n-tile nt
   // holds columns 8 nt .. 8 nt + 7 (this lane's B fragment: column 8 nt + r)
-  const int ncols = nq * G;
   uint32_t qf[NT][KS][2];
   int lim[NT][2];
   WarpState<D> st[NT];
@@ -1869,31 +1911,29 @@ struct CombineParams {
   const float* part_out;
   const float* part_m;
   const float* part_l;
-  const int32_t* context_lens;
   __half* out;
   int num_heads;
   int head_dim;
   int num_splits;
-  int chunk_tokens;
-  int cap_tokens;  // max_blocks_per_seq * block_size
 };
 
 // The merge of one output row from its split partials, by a CTA of
 // kCombineThreads threads: thread k loads split k's max and sum (all splits
 // at once), the CTA reduces them, and thread d then sums the splits' partial
-// outputs with independent loads.  Only the first n_valid splits are read
-// (the others were never written).
+// outputs with independent loads.  Every split was written by phase 1; an
+// empty one holds max -inf and sum 0, gets weight 0, and its partial output
+// (never written) is not read.
 constexpr int kCombineThreads = 128;
 
 __device__ __forceinline__ void combine_row(const float* pm, const float* pl, const float* po,
-                                            int n_valid, int head_dim, __half* out_row,
+                                            int num_splits, int head_dim, __half* out_row,
                                             float* s_w, float* s_red) {
   constexpr int NT = kCombineThreads;
   static_assert(PKV_MAX_SPLITS <= NT, "one thread per split");
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int k = threadIdx.x;  // num_splits <= PKV_MAX_SPLITS = NT
-  const float mk = k < n_valid ? __ldg(pm + k) : -CUDART_INF_F;
-  const float lk = k < n_valid ? __ldg(pl + k) : 0.f;
+  const float mk = k < num_splits ? __ldg(pm + k) : -CUDART_INF_F;
+  const float lk = k < num_splits ? __ldg(pl + k) : 0.f;
   float M = mk;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
@@ -1910,23 +1950,28 @@ __device__ __forceinline__ void combine_row(const float* pm, const float* pl, co
   __syncthreads();
   den = s_red[0] + s_red[1] + s_red[2] + s_red[3];
 
+  // the last split with a weight (valid splits are a prefix of the chunks,
+  // but any zero-weight split is skipped, not read)
+  int n = num_splits;
+  while (n > 0 && s_w[n - 1] == 0.f) --n;
   for (int d = threadIdx.x; d < head_dim; d += NT) {
     float num = 0.f;
     int kk = 0;
-    for (; kk + 4 <= n_valid; kk += 4) {
-      const float a0 = __ldg(po + (size_t)kk * head_dim + d);
-      const float a1 = __ldg(po + (size_t)(kk + 1) * head_dim + d);
-      const float a2 = __ldg(po + (size_t)(kk + 2) * head_dim + d);
-      const float a3 = __ldg(po + (size_t)(kk + 3) * head_dim + d);
-      num += s_w[kk] * a0 + s_w[kk + 1] * a1 + s_w[kk + 2] * a2 + s_w[kk + 3] * a3;
+    for (; kk + 4 <= n; kk += 4) {
+      const float w0 = s_w[kk], w1 = s_w[kk + 1], w2 = s_w[kk + 2], w3 = s_w[kk + 3];
+      const float a0 = w0 != 0.f ? __ldg(po + (size_t)kk * head_dim + d) : 0.f;
+      const float a1 = w1 != 0.f ? __ldg(po + (size_t)(kk + 1) * head_dim + d) : 0.f;
+      const float a2 = w2 != 0.f ? __ldg(po + (size_t)(kk + 2) * head_dim + d) : 0.f;
+      const float a3 = w3 != 0.f ? __ldg(po + (size_t)(kk + 3) * head_dim + d) : 0.f;
+      num += w0 * a0 + w1 * a1 + w2 * a2 + w3 * a3;
     }
-    for (; kk < n_valid; ++kk) num += s_w[kk] * __ldg(po + (size_t)kk * head_dim + d);
+    for (; kk < n; ++kk)
+      if (s_w[kk] != 0.f) num += s_w[kk] * __ldg(po + (size_t)kk * head_dim + d);
     out_row[d] = __float2half_rn(den > 0.f ? num / den : 0.f);
   }
 }
 
-// Decode split-K: one CTA per (sequence, query head).  A split is valid when
-// its first token is before the context length.
+// Decode split-K: one CTA per (sequence, query head).
 __global__ void __launch_bounds__(kCombineThreads) splitk_combine_kernel(const CombineParams p) {
   __shared__ float s_w[PKV_MAX_SPLITS];
   __shared__ float s_red[kCombineThreads / 32];
@@ -1936,35 +1981,27 @@ __global__ void __launch_bounds__(kCombineThreads) splitk_combine_kernel(const C
   // partials were not written either); uniform for the CTA
   if (*reinterpret_cast<volatile unsigned int*>(&g_device_status) & kDevWaitTimeout) return;
   const int sh = blockIdx.x;
-  const int s = sh / p.num_heads;
-  int L = __ldg(p.context_lens + s);
-  L = L < 0 ? 0 : (L > p.cap_tokens ? p.cap_tokens : L);
-  const int n_valid = min(p.num_splits, (L + p.chunk_tokens - 1) / p.chunk_tokens);
   combine_row(p.part_m + (size_t)sh * p.num_splits, p.part_l + (size_t)sh * p.num_splits,
-              p.part_out + (size_t)sh * p.num_splits * p.head_dim, n_valid, p.head_dim,
+              p.part_out + (size_t)sh * p.num_splits * p.head_dim, p.num_splits, p.head_dim,
               p.out + (size_t)sh * p.head_dim, s_w, s_red);
 }
 
 // Varlen split-K: one CTA per (query token, head).  The token's sequence is
-// found by binary search in cu_seqlens_q; the query at position pos sees
-// positions 0..pos, so splits starting at or before pos are valid (the
-// phase-1 CTA of its chunk of queries wrote every one of them).  Positions
-// are clamped as phase 1 clamps them; rows phase 1 skipped (bad query
-// ranges, queries past the grid; both flagged there) are written as zeros.
+// found by binary search in cu_seqlens_q; phase 1 wrote every split of every
+// query it covered (max -inf and sum 0 where the split holds none of the
+// query's positions).  Rows phase 1 skipped (bad query ranges, queries past
+// the grid; both flagged there) are written as zeros.
 struct VarlenCombineParams {
   const float* part_out;
   const float* part_m;
   const float* part_l;
   const int32_t* cu_seqlens_q;
-  const int32_t* pos_offsets;
   __half* out;
   int num_seqs;
   int total_q;
   int num_heads;
   int head_dim;
   int num_splits;
-  int chunk_tokens;
-  int cap_tokens;
   int covered_q;  // queries per sequence the phase-1 grid covers
 };
 
@@ -1994,14 +2031,9 @@ varlen_combine_kernel(const VarlenCombineParams p) {
     for (int d = threadIdx.x; d < p.head_dim; d += kCombineThreads) out_row[d] = __float2half_rn(0.f);
     return;
   }
-  const int q_len = q_end - q_begin;
-  int pos0 = __ldg(p.pos_offsets + lo);
-  if (pos0 < 0 || pos0 + q_len > p.cap_tokens) pos0 = pos0 < 0 ? 0 : max(0, p.cap_tokens - q_len);
-  const int L = min(p.cap_tokens, pos0 + t + 1);
-  const int n_valid = min(p.num_splits, (L + p.chunk_tokens - 1) / p.chunk_tokens);
   combine_row(p.part_m + (size_t)rh * p.num_splits, p.part_l + (size_t)rh * p.num_splits,
-              p.part_out + (size_t)rh * p.num_splits * p.head_dim, n_valid, p.head_dim, out_row,
-              s_w, s_red);
+              p.part_out + (size_t)rh * p.num_splits * p.head_dim, p.num_splits, p.head_dim,
+              out_row, s_w, s_red);
 }
 
 // Diagnostic: one warp waits on an mbarrier that nothing arrives on.  The

@@ -121,8 +121,8 @@ int current_device_sms(int* sms) {
 // one whole tile, 64 x block_size x head_dim/64 x 1, landing as head_dim/64
 // runs of block_size 128-byte lines with the 128-byte swizzle (one request
 // per tile measured slightly faster than one per half).
-pkv_status make_cache_map(CUtensorMap* map, const void* base, int num_blocks, int num_kv_heads,
-                          int block_size, int head_dim) {
+pkv_status encode_cache_map(CUtensorMap* map, const void* base, int num_blocks, int num_kv_heads,
+                            int block_size, int head_dim) {
   auto encode = tensor_map_encoder();
   if (!encode) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   const cuuint64_t dims[4] = {64, (cuuint64_t)block_size, (cuuint64_t)(head_dim / 64),
@@ -143,8 +143,8 @@ pkv_status make_cache_map(CUtensorMap* map, const void* base, int num_blocks, in
 // lines, num_blocks*num_kv_heads tiles}: each V^T tile [head_dim][block_size]
 // read as 128-byte lines.  A box is one whole tile, landing with the 128-byte
 // swizzle.
-pkv_status make_vllm_v_map(CUtensorMap* map, const void* base, int num_blocks, int num_kv_heads,
-                           int block_size, int head_dim) {
+pkv_status encode_vllm_v_map(CUtensorMap* map, const void* base, int num_blocks,
+                             int num_kv_heads, int block_size, int head_dim) {
   auto encode = tensor_map_encoder();
   if (!encode) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   const int lines = head_dim * block_size / 64;
@@ -159,6 +159,62 @@ pkv_status make_vllm_v_map(CUtensorMap* map, const void* base, int num_blocks, i
                             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
   return PKV_OK;
+}
+
+// Encoded tensor maps are kept per (pool address, shape, kind): a decode
+// loop calls with the same pools every step, and a map depends on nothing
+// else, so an entry never goes stale (a pool freed and another allocated at
+// the same address with the same shape has the same map).  A small table,
+// replaced round robin, shared by all threads under a mutex.
+struct MapKey {
+  const void* base;
+  int num_blocks, num_kv_heads, block_size, head_dim, kind;
+  bool operator==(const MapKey& o) const {
+    return base == o.base && num_blocks == o.num_blocks && num_kv_heads == o.num_kv_heads &&
+           block_size == o.block_size && head_dim == o.head_dim && kind == o.kind;
+  }
+};
+constexpr int kMapCacheEntries = 32;
+struct MapCache {
+  std::mutex mu;
+  MapKey key[kMapCacheEntries] = {};
+  CUtensorMap map[kMapCacheEntries];
+  int used = 0, next = 0;
+};
+MapCache g_maps;
+
+// kind 0: a blocked-layout pool (K or V); kind 1: a vLLM-layout V pool.
+pkv_status cached_map(CUtensorMap* map, int kind, const void* base, int num_blocks,
+                      int num_kv_heads, int block_size, int head_dim) {
+  const MapKey k{base, num_blocks, num_kv_heads, block_size, head_dim, kind};
+  {
+    std::lock_guard<std::mutex> lock(g_maps.mu);
+    for (int i = 0; i < g_maps.used; ++i)
+      if (g_maps.key[i] == k) {
+        *map = g_maps.map[i];
+        return PKV_OK;
+      }
+  }
+  const pkv_status st = kind == 0
+                            ? encode_cache_map(map, base, num_blocks, num_kv_heads, block_size, head_dim)
+                            : encode_vllm_v_map(map, base, num_blocks, num_kv_heads, block_size, head_dim);
+  if (st != PKV_OK) return st;
+  std::lock_guard<std::mutex> lock(g_maps.mu);
+  const int i = g_maps.used < kMapCacheEntries ? g_maps.used++ : g_maps.next;
+  if (g_maps.used == kMapCacheEntries) g_maps.next = (i + 1) % kMapCacheEntries;
+  g_maps.key[i] = k;
+  g_maps.map[i] = *map;
+  return PKV_OK;
+}
+
+pkv_status make_cache_map(CUtensorMap* map, const void* base, int num_blocks, int num_kv_heads,
+                          int block_size, int head_dim) {
+  return cached_map(map, 0, base, num_blocks, num_kv_heads, block_size, head_dim);
+}
+
+pkv_status make_vllm_v_map(CUtensorMap* map, const void* base, int num_blocks, int num_kv_heads,
+                           int block_size, int head_dim) {
+  return cached_map(map, 1, base, num_blocks, num_kv_heads, block_size, head_dim);
 }
 
 struct DecodeArgs {
@@ -380,7 +436,8 @@ DecodeParams base_params(const DecodeArgs& a) {
   p.max_blocks_per_seq = a.max_blocks_per_seq;
   p.num_blocks = a.num_blocks;
   p.num_splits = 1;
-  p.chunk_blocks = a.max_blocks_per_seq;
+  p.min_chunk_blocks = 1;
+  p.chunk_hint = a.max_blocks_per_seq;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   return p;
 }
@@ -630,6 +687,43 @@ pkv_status pkv_decode(const void* q, const void* k_cache, const void* v_cache,
 namespace pkv {
 namespace {
 
+// The split count a decode call launches for `num_splits` (0 = the
+// heuristic for the current GPU): 1 (single pass), 2..PKV_MAX_SPLITS, or
+// PKV_SPLITS_BALANCED.  More splits than table blocks cannot all hold work,
+// so the count is capped at max_blocks_per_seq.
+pkv_status resolve_decode_splits(int num_seqs, int num_kv_heads, int max_blocks_per_seq,
+                                 int block_size, int num_splits, int* S_out) {
+  if (num_splits < PKV_SPLITS_BALANCED || num_splits > PKV_MAX_SPLITS)
+    return fail(PKV_ERR_INVALID_ARG, "num_splits %d outside -1..%d", num_splits, PKV_MAX_SPLITS);
+  int S = num_splits;
+  if (S == 0) {
+    int sms = 0;
+    if (current_device_sms(&sms) != 0) return fail(PKV_ERR_CUDA, "cannot query the SM count");
+    S = pkv_pick_num_splits(num_seqs, num_kv_heads, max_blocks_per_seq * block_size, block_size,
+                            sms);
+  }
+  if (S != PKV_SPLITS_BALANCED) S = S < 1 ? 1 : (S > max_blocks_per_seq ? max_blocks_per_seq : S);
+  *S_out = S;
+  return PKV_OK;
+}
+
+// The same for varlen split-K (0 = pkv_varlen_pick_num_splits).
+pkv_status resolve_varlen_splits(int num_seqs, int num_heads, int num_kv_heads, int max_q_len,
+                                 int max_blocks_per_seq, int block_size, int num_splits,
+                                 int* S_out) {
+  if (num_splits < 0 || num_splits > PKV_MAX_SPLITS)
+    return fail(PKV_ERR_INVALID_ARG, "num_splits %d outside 0..%d", num_splits, PKV_MAX_SPLITS);
+  int S = num_splits;
+  if (S == 0) {
+    int sms = 0;
+    if (current_device_sms(&sms) != 0) return fail(PKV_ERR_CUDA, "cannot query the SM count");
+    S = pkv_varlen_pick_num_splits(num_seqs, num_heads, num_kv_heads, max_q_len,
+                                   max_blocks_per_seq, block_size, sms);
+  }
+  *S_out = S < 1 ? 1 : (S > max_blocks_per_seq ? max_blocks_per_seq : S);
+  return PKV_OK;
+}
+
 // The body of pkv_decode_splitk and pkv_append_decode (arguments validated).
 pkv_status decode_impl(const DecodeArgs& a, int num_splits, void* scratch, size_t scratch_bytes,
                        cudaStream_t cs, const FuseArgs* fuse) {
@@ -641,12 +735,9 @@ pkv_status decode_impl(const DecodeArgs& a, int num_splits, void* scratch, size_
     return fail(PKV_ERR_INVALID_ARG, "num_splits %d outside -1..%d", num_splits, PKV_MAX_SPLITS);
   if (num_seqs == 0) return PKV_OK;
 
-  int S = num_splits;
-  if (S == 0) {
-    int sms = 0;
-    if (current_device_sms(&sms) != 0) return fail(PKV_ERR_CUDA, "cannot query the SM count");
-    S = pkv_pick_num_splits(num_seqs, num_kv_heads, max_blocks_per_seq * block_size, block_size, sms);
-  }
+  int S = 0;
+  st = resolve_decode_splits(num_seqs, num_kv_heads, max_blocks_per_seq, block_size, num_splits, &S);
+  if (st != PKV_OK) return st;
   if (S == PKV_SPLITS_BALANCED) {
     if (a.vllm) return fail(PKV_ERR_UNSUPPORTED, "no balanced schedule on the vLLM layout");
     const size_t need_b = balanced_scratch_bytes(head_dim);
@@ -663,8 +754,7 @@ pkv_status decode_impl(const DecodeArgs& a, int num_splits, void* scratch, size_
     }
     return dispatch_balanced(a, static_cast<float*>(scratch), cs);
   }
-  const int chunk_blocks = (max_blocks_per_seq + S - 1) / S;
-  const int S_eff = (max_blocks_per_seq + chunk_blocks - 1) / chunk_blocks;
+  const int S_eff = S;
   if (S_eff <= 1) return single_pass(a, cs, fuse);
 
   const size_t need = pkv_splitk_scratch_bytes(num_seqs, num_heads, head_dim, S_eff);
@@ -680,7 +770,10 @@ pkv_status decode_impl(const DecodeArgs& a, int num_splits, void* scratch, size_
   DecodeParams prm = base_params(a);
   apply_fuse(prm, fuse);
   prm.num_splits = S_eff;
-  prm.chunk_blocks = chunk_blocks;
+  // the heuristic keeps a split at >= kMinSplitTokens; forced counts cut the
+  // longest context into exactly S chunks
+  prm.min_chunk_blocks = num_splits == 0 ? (kMinSplitTokens + block_size - 1) / block_size : 1;
+  prm.chunk_hint = (max_blocks_per_seq + S_eff - 1) / S_eff;
   prm.part_out = reinterpret_cast<float*>(base);
   prm.part_m = reinterpret_cast<float*>(base + align256(rows * head_dim * sizeof(float)));
   prm.part_l = reinterpret_cast<float*>(base + align256(rows * head_dim * sizeof(float)) +
@@ -692,13 +785,10 @@ pkv_status decode_impl(const DecodeArgs& a, int num_splits, void* scratch, size_
   cp.part_out = prm.part_out;
   cp.part_m = prm.part_m;
   cp.part_l = prm.part_l;
-  cp.context_lens = a.context_lens;
   cp.out = static_cast<__half*>(a.out);
   cp.num_heads = num_heads;
   cp.head_dim = head_dim;
   cp.num_splits = S_eff;
-  cp.chunk_tokens = chunk_blocks * block_size;
-  cp.cap_tokens = max_blocks_per_seq * block_size;
   const cudaError_t e = launch_pdl(splitk_combine_kernel, num_seqs * num_heads, 128, 0, cs, cp);
   if (e != cudaSuccess) return cuda_fail(e, "split-K combine launch");
   return PKV_OK;
@@ -749,17 +839,12 @@ pkv_status varlen_impl(const void* q, const void* k_cache, const void* v_cache,
   vp.num_blocks = num_blocks;
   vp.scale_log2 = scale * 1.4426950408889634f;
   vp.num_splits = 1;
-  vp.chunk_blocks = max_blocks_per_seq;
+  vp.min_chunk_blocks = 1;
 
-  int S = num_splits;
-  if (S == 0) {
-    int sms = 0;
-    if (current_device_sms(&sms) != 0) return fail(PKV_ERR_CUDA, "cannot query the SM count");
-    S = pkv_varlen_pick_num_splits(num_seqs, num_heads, num_kv_heads, max_q_len,
-                                   max_blocks_per_seq, block_size, sms);
-  }
-  const int chunk_blocks = (max_blocks_per_seq + S - 1) / S;
-  const int S_eff = (max_blocks_per_seq + chunk_blocks - 1) / chunk_blocks;
+  int S_eff = 1;
+  st = resolve_varlen_splits(num_seqs, num_heads, num_kv_heads, max_q_len, max_blocks_per_seq,
+                             block_size, num_splits, &S_eff);
+  if (st != PKV_OK) return st;
   if (S_eff <= 1) return dispatch_varlen<false>(a, vp, cs, (int)grid, NT, vllm);
 
   const size_t need = pkv_splitk_scratch_bytes(total_q, num_heads, head_dim, S_eff);
@@ -774,7 +859,7 @@ pkv_status varlen_impl(const void* q, const void* k_cache, const void* v_cache,
   const size_t rows = (size_t)total_q * num_heads * S_eff;
   uint8_t* base = static_cast<uint8_t*>(scratch);
   vp.num_splits = S_eff;
-  vp.chunk_blocks = chunk_blocks;
+  vp.min_chunk_blocks = num_splits == 0 ? (kMinSplitTokens + block_size - 1) / block_size : 1;
   vp.part_out = reinterpret_cast<float*>(base);
   vp.part_m = reinterpret_cast<float*>(base + align256(rows * head_dim * sizeof(float)));
   vp.part_l = reinterpret_cast<float*>(base + align256(rows * head_dim * sizeof(float)) +
@@ -787,15 +872,12 @@ pkv_status varlen_impl(const void* q, const void* k_cache, const void* v_cache,
   cp.part_m = vp.part_m;
   cp.part_l = vp.part_l;
   cp.cu_seqlens_q = cu_seqlens_q;
-  cp.pos_offsets = pos_offsets;
   cp.out = static_cast<__half*>(out);
   cp.num_seqs = num_seqs;
   cp.total_q = total_q;
   cp.num_heads = num_heads;
   cp.head_dim = head_dim;
   cp.num_splits = S_eff;
-  cp.chunk_tokens = chunk_blocks * block_size;
-  cp.cap_tokens = max_blocks_per_seq * block_size;
   cp.covered_q = chunks * qc;
   const cudaError_t e = launch_pdl(varlen_combine_kernel, (int)grid2, kCombineThreads, 0, cs, cp);
   if (e != cudaSuccess) return cuda_fail(e, "varlen split-K combine launch");
@@ -914,6 +996,51 @@ pkv_status pkv_varlen_attention_splitk_vllm_layout(
                      total_q, max_q_len, max_blocks_per_seq, num_blocks, scale, num_heads,
                      num_kv_heads, head_dim, block_size, out, num_splits, scratch, scratch_bytes,
                      static_cast<cudaStream_t>(stream), true);
+}
+
+pkv_status pkv_decode_splitk_plan(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                                  int32_t head_dim, int32_t max_blocks_per_seq,
+                                  int32_t block_size, int32_t num_splits, int32_t* splits,
+                                  size_t* scratch_bytes) {
+  if (!splits || !scratch_bytes) return fail(PKV_ERR_INVALID_ARG, "splits and scratch_bytes must not be NULL");
+  if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0 ||
+      head_dim <= 0 || max_blocks_per_seq <= 0 || block_size <= 0)
+    return fail(PKV_ERR_INVALID_ARG, "invalid sizes");
+  if ((long long)max_blocks_per_seq * block_size >= (1ll << 31))
+    return fail(PKV_ERR_INVALID_ARG, "max_blocks_per_seq * block_size overflows");
+  int S = 1;
+  const pkv_status st = resolve_decode_splits(num_seqs, num_kv_heads, max_blocks_per_seq,
+                                              block_size, num_splits, &S);
+  if (st != PKV_OK) return st;
+  *splits = S;
+  *scratch_bytes = (S == 1 || num_seqs == 0) ? 0 : pkv_splitk_scratch_bytes(num_seqs, num_heads, head_dim, S);
+  return PKV_OK;
+}
+
+pkv_status pkv_varlen_splitk_plan(int32_t num_seqs, int32_t total_q, int32_t max_q_len,
+                                  int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                                  int32_t max_blocks_per_seq, int32_t block_size,
+                                  int32_t num_splits, int32_t* splits, size_t* scratch_bytes) {
+  if (!splits || !scratch_bytes) return fail(PKV_ERR_INVALID_ARG, "splits and scratch_bytes must not be NULL");
+  if (num_seqs < 0 || total_q < 0 || max_q_len < 0 || num_heads <= 0 || num_kv_heads <= 0 ||
+      num_heads % num_kv_heads != 0 || head_dim <= 0 || max_blocks_per_seq <= 0 || block_size <= 0)
+    return fail(PKV_ERR_INVALID_ARG, "invalid sizes");
+  if ((long long)max_blocks_per_seq * block_size >= (1ll << 31))
+    return fail(PKV_ERR_INVALID_ARG, "max_blocks_per_seq * block_size overflows");
+  if (num_seqs == 0 || total_q == 0 || max_q_len == 0) {
+    if (num_splits < 0 || num_splits > PKV_MAX_SPLITS)
+      return fail(PKV_ERR_INVALID_ARG, "num_splits %d outside 0..%d", num_splits, PKV_MAX_SPLITS);
+    *splits = 1;
+    *scratch_bytes = 0;
+    return PKV_OK;
+  }
+  int S = 1;
+  const pkv_status st = resolve_varlen_splits(num_seqs, num_heads, num_kv_heads, max_q_len,
+                                              max_blocks_per_seq, block_size, num_splits, &S);
+  if (st != PKV_OK) return st;
+  *splits = S;
+  *scratch_bytes = S == 1 ? 0 : pkv_splitk_scratch_bytes(total_q, num_heads, head_dim, S);
+  return PKV_OK;
 }
 
 }  // extern "C"
@@ -1133,18 +1260,11 @@ extern "C" pkv_status pkv_decode_splitk_noalloc(
   if (num_seqs == 0) return PKV_OK;
 
   // The split count pkv_decode_splitk will use, and the scratch it needs.
-  int S = num_splits;
-  if (S == 0) {
-    int sms = 0;
-    if (current_device_sms(&sms) != 0) return fail(PKV_ERR_CUDA, "cannot query the SM count");
-    S = pkv_pick_num_splits(num_seqs, num_kv_heads, max_blocks_per_seq * block_size, block_size, sms);
-  }
-  int S_eff = S;
-  if (S > 1) {
-    const int chunk_blocks = (max_blocks_per_seq + S - 1) / S;
-    S_eff = (max_blocks_per_seq + chunk_blocks - 1) / chunk_blocks;
-  }
-  const size_t need = pkv_splitk_scratch_bytes(num_seqs, num_heads, head_dim, S_eff);
+  int S_eff = 1;
+  size_t need = 0;
+  st = pkv_decode_splitk_plan(num_seqs, num_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                              block_size, num_splits, &S_eff, &need);
+  if (st != PKV_OK) return st;
   if (need > (size_t)PKV_NOALLOC_SCRATCH_BYTES)
     return fail(PKV_ERR_SCRATCH_TOO_SMALL,
                 "%d splits need %zu bytes of scratch but the built-in buffer holds %zu; use "
@@ -1156,6 +1276,6 @@ extern "C" pkv_status pkv_decode_splitk_noalloc(
   if (st != PKV_OK) return st;
   return pkv_decode_splitk(q, k_cache, v_cache, block_tables, context_lens, num_seqs,
                            max_blocks_per_seq, num_blocks, scale, num_heads, num_kv_heads,
-                           head_dim, block_size, out, S, scratch,
+                           head_dim, block_size, out, num_splits, scratch,
                            (size_t)PKV_NOALLOC_SCRATCH_BYTES, stream);
 }

@@ -82,6 +82,12 @@ def _load():
     lib.pkv_splitk_scratch_bytes.restype = sz
     lib.pkv_pick_num_splits.argtypes = [i32, i32, i32, i32, i32]
     lib.pkv_pick_num_splits.restype = i32
+    lib.pkv_decode_splitk_plan.argtypes = [i32, i32, i32, i32, i32, i32, i32,
+                                           ctypes.POINTER(i32), ctypes.POINTER(sz)]
+    lib.pkv_decode_splitk_plan.restype = i32
+    lib.pkv_varlen_splitk_plan.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, i32,
+                                           ctypes.POINTER(i32), ctypes.POINTER(sz)]
+    lib.pkv_varlen_splitk_plan.restype = i32
     lib.pkv_status_string.argtypes = [i32]
     lib.pkv_status_string.restype = ctypes.c_char_p
     lib.pkv_last_error.argtypes = []
@@ -201,27 +207,55 @@ def pkv_pick_num_splits(num_seqs, num_kv_heads, max_context_len, block_size, num
                                        num_sms))
 
 
-def splits_for(q, k_cache, block_tables, num_splits=0, device=None) -> int:
-    """The split count :func:`pkv_decode_splitk` will use for these tensors."""
+def pkv_decode_splitk_plan(num_seqs, num_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                           block_size, num_splits=0):
+    """``(splits, scratch_bytes)`` the decode calls launch for these sizes (the
+    library's own rule; ``num_splits`` 0 = the heuristic for the current GPU)."""
+    S = ctypes.c_int32(0)
+    n = ctypes.c_size_t(0)
+    _check(lib.pkv_decode_splitk_plan(num_seqs, num_heads, num_kv_heads, head_dim,
+                                      max_blocks_per_seq, block_size, int(num_splits),
+                                      ctypes.byref(S), ctypes.byref(n)), "pkv_decode_splitk_plan")
+    return int(S.value), int(n.value)
+
+
+def pkv_varlen_splitk_plan(num_seqs, total_q, max_q_len, num_heads, num_kv_heads, head_dim,
+                           max_blocks_per_seq, block_size, num_splits=0):
+    """``(splits, scratch_bytes)`` the varlen split-K calls launch."""
+    S = ctypes.c_int32(0)
+    n = ctypes.c_size_t(0)
+    _check(lib.pkv_varlen_splitk_plan(num_seqs, total_q, max_q_len, num_heads, num_kv_heads,
+                                      head_dim, max_blocks_per_seq, block_size, int(num_splits),
+                                      ctypes.byref(S), ctypes.byref(n)), "pkv_varlen_splitk_plan")
+    return int(S.value), int(n.value)
+
+
+def _pool_dims(k_cache):
+    """(num_kv_heads, block_size) of a blocked [NB][Hkv][bs][D] or vLLM-layout
+    [NB][Hkv][D/8][bs][8] K pool."""
+    return k_cache.shape[1], (k_cache.shape[3] if k_cache.dim() == 5 else k_cache.shape[2])
+
+
+def _decode_plan(q, k_cache, block_tables, num_splits, device=None):
     import torch
 
-    if num_splits:
-        return int(num_splits)
-    sms = torch.cuda.get_device_properties(device or q.device).multi_processor_count
-    bs = k_cache.shape[3] if k_cache.dim() == 5 else k_cache.shape[2]  # vLLM K: [..][bs][8]
-    return pkv_pick_num_splits(q.shape[0], k_cache.shape[1], block_tables.shape[1] * bs, bs, sms)
+    Hkv, bs = _pool_dims(k_cache)
+    with torch.cuda.device(device or q.device):
+        return pkv_decode_splitk_plan(q.shape[0], q.shape[1], Hkv, q.shape[2],
+                                      block_tables.shape[1], bs, num_splits)
+
+
+def splits_for(q, k_cache, block_tables, num_splits=0, device=None) -> int:
+    """The split count :func:`pkv_decode_splitk` launches for these tensors."""
+    return _decode_plan(q, k_cache, block_tables, num_splits, device)[0]
 
 
 def alloc_scratch(q, k_cache, block_tables, num_splits=0):
-    """A scratch tensor (uint8, on q's device) big enough for the split count
-    :func:`pkv_decode_splitk` will pick (or ``num_splits`` if given)."""
+    """A scratch tensor (uint8, on q's device) of the size the library's plan
+    gives for these tensors and ``num_splits`` (0 = the heuristic)."""
     import torch
 
-    S = splits_for(q, k_cache, block_tables, num_splits)
-    if S > 1:  # the kernel uses ceil(MBPS / ceil(MBPS / S)) <= S splits
-        mbps = block_tables.shape[1]
-        S = -(-mbps // -(-mbps // S))
-    n = pkv_splitk_scratch_bytes(q.shape[0], q.shape[1], q.shape[2], S)
+    n = _decode_plan(q, k_cache, block_tables, num_splits)[1]
     return torch.empty(max(n, 16), dtype=torch.uint8, device=q.device)
 
 
@@ -304,21 +338,19 @@ def pkv_varlen_pick_num_splits(num_seqs, num_heads, num_kv_heads, max_q_len,
                                               max_blocks_per_seq, block_size, num_sms))
 
 
-def varlen_splits_for(q, k_cache, block_tables, num_kv_heads, max_q_len, num_splits=0):
-    """The split count the varlen split-K call will use for these tensors."""
+def _varlen_plan(q, k_cache, block_tables, max_q_len, num_splits=0):
     import torch
 
-    mbps = block_tables.shape[1]
-    if num_splits:
-        S = int(num_splits)
-    else:
-        sms = torch.cuda.get_device_properties(q.device).multi_processor_count
-        bs = k_cache.shape[3] if k_cache.dim() == 5 else k_cache.shape[2]
-        S = pkv_varlen_pick_num_splits(block_tables.shape[0], q.shape[1], num_kv_heads,
-                                       max_q_len, mbps, bs, sms)
-    if S > 1:  # the kernel uses ceil(MBPS / ceil(MBPS / S)) <= S splits
-        S = -(-mbps // -(-mbps // S))
-    return S
+    Hkv, bs = _pool_dims(k_cache)
+    with torch.cuda.device(q.device):
+        return pkv_varlen_splitk_plan(block_tables.shape[0], q.shape[0], int(max_q_len),
+                                      q.shape[1], Hkv, q.shape[2], block_tables.shape[1], bs,
+                                      num_splits)
+
+
+def varlen_splits_for(q, k_cache, block_tables, max_q_len, num_splits=0):
+    """The split count the varlen split-K call launches for these tensors."""
+    return _varlen_plan(q, k_cache, block_tables, max_q_len, num_splits)[0]
 
 
 def _varlen(q, k_cache, v_cache, cu_seqlens_q, pos_offsets, block_tables, scale, max_q_len, out,
@@ -353,8 +385,7 @@ def _varlen(q, k_cache, v_cache, cu_seqlens_q, pos_offsets, block_tables, scale,
     else:
         num_splits, scratch = split
         if scratch is None:
-            S = varlen_splits_for(q, k_cache, block_tables, Hkv, int(max_q_len), num_splits)
-            n = pkv_splitk_scratch_bytes(total_q, H, D, S) if S > 1 else 0
+            n = _varlen_plan(q, k_cache, block_tables, max_q_len, num_splits)[1]
             scratch = torch.empty(max(n, 16), dtype=torch.uint8, device=q.device)
         _want(scratch, "scratch", torch.uint8, 1)
         args += [int(num_splits), scratch.data_ptr(), scratch.numel()]

@@ -258,6 +258,17 @@ def make(name: str) -> Workload:
             "ragged": ragged}[name]()
 
 
+def widen_tables(w: Workload, factor: int) -> Workload:
+    """The same workload with block tables ``factor`` times wider than its
+    longest context needs (as a server sizes them for the model's maximum
+    context); the extra entries point at the poison block."""
+    mbps = w.max_blocks_per_seq * factor
+    tables = np.full((w.num_seqs, mbps), w.poison_block, np.int32)
+    tables[:, :w.max_blocks_per_seq] = w.block_tables
+    return dataclasses.replace(w, name=f"{w.name}-x{factor}", max_blocks_per_seq=mbps,
+                               block_tables=tables)
+
+
 def small_random(seed: int, num_seqs: int, num_heads: int, num_kv_heads: int,
                  head_dim: int, block_size: int, lens, num_blocks: Optional[int] = None,
                  std: float = 1.0) -> Workload:

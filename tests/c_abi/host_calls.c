@@ -25,6 +25,23 @@ int main(void) {
   CHECK(pkv_splitk_scratch_bytes(4, 32, 128, 1) == 0);
   CHECK(pkv_splitk_scratch_bytes(4, 32, 128, 16) >= (size_t)4 * 32 * 16 * 130 * 4);
   CHECK(pkv_splitk_scratch_bytes(4, 32, 128, PKV_SPLITS_BALANCED) > 0);
+  /* split plans: what the decode calls launch and the scratch they need */
+  {
+    int32_t S = 0;
+    size_t need = 0;
+    CHECK(pkv_decode_splitk_plan(4, 32, 8, 128, 8192, 16, 16, &S, &need) == PKV_OK);
+    CHECK(S == 16 && need == pkv_splitk_scratch_bytes(4, 32, 128, 16));
+    CHECK(pkv_decode_splitk_plan(3, 8, 2, 64, 7, 16, 64, &S, &need) == PKV_OK);
+    CHECK(S == 7 && need == pkv_splitk_scratch_bytes(3, 8, 64, 7));
+    CHECK(pkv_decode_splitk_plan(4, 32, 8, 128, 8192, 16, 1, &S, &need) == PKV_OK);
+    CHECK(S == 1 && need == 0);
+    CHECK(pkv_decode_splitk_plan(4, 32, 8, 128, 8192, 16, 200, &S, &need) ==
+          PKV_ERR_INVALID_ARG);
+    CHECK(pkv_decode_splitk_plan(4, 32, 8, 128, 8192, 16, 4, NULL, &need) ==
+          PKV_ERR_INVALID_ARG);
+    CHECK(pkv_varlen_splitk_plan(4, 16, 4, 32, 8, 128, 8192, 16, 10, &S, &need) == PKV_OK);
+    CHECK(S == 10 && need == pkv_splitk_scratch_bytes(16, 32, 128, 10));
+  }
   /* status strings */
   CHECK(strcmp(pkv_status_string(PKV_OK), "ok") == 0);
   CHECK(strlen(pkv_status_string(PKV_ERR_SCRATCH_TOO_SMALL)) > 0);

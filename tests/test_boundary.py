@@ -37,7 +37,8 @@ def test_header_declares_the_expected_calls():
               "pkv_varlen_attention_vllm_layout", "pkv_varlen_attention_splitk",
               "pkv_varlen_attention_splitk_vllm_layout", "pkv_varlen_pick_num_splits",
               "pkv_qkv_norm_rope_append", "pkv_qkv_norm_rope_append_decode",
-              "pkv_selftest_wait_timeout"]:
+              "pkv_selftest_wait_timeout", "pkv_decode_splitk_plan", "pkv_varlen_splitk_plan",
+              "pkv_decode_splitk_noalloc"]:
         assert n in names
 
 
@@ -84,6 +85,53 @@ def test_scratch_bytes(pk):
 ])
 def test_pick_num_splits_table(pk, args, expect):
     assert pk.pkv_pick_num_splits(*args) == expect
+
+
+def test_decode_splitk_plan(pk):
+    """The plan the decode calls follow: forced counts capped at the table
+    width, single pass without scratch, the balanced schedule's records."""
+    assert pk.pkv_decode_splitk_plan(4, 32, 8, 128, 8192, 16, 16) == (
+        16, pk.pkv_splitk_scratch_bytes(4, 32, 128, 16))
+    assert pk.pkv_decode_splitk_plan(3, 8, 2, 64, 7, 16, 64) == (
+        7, pk.pkv_splitk_scratch_bytes(3, 8, 64, 7))
+    assert pk.pkv_decode_splitk_plan(4, 32, 8, 128, 8192, 16, 1) == (1, 0)
+    assert pk.pkv_decode_splitk_plan(0, 32, 8, 128, 8192, 16, 16) == (16, 0)
+    assert pk.pkv_decode_splitk_plan(4, 32, 8, 128, 8192, 16, -1) == (
+        -1, pk.pkv_splitk_scratch_bytes(4, 32, 128, -1))
+    for bad in (dict(num_splits=129), dict(num_splits=-2), dict(num_heads=30),
+                dict(max_blocks_per_seq=0)):
+        a = dict(num_seqs=4, num_heads=32, num_kv_heads=8, head_dim=128,
+                 max_blocks_per_seq=8192, block_size=16, num_splits=4)
+        a.update(bad)
+        with pytest.raises(pk.PagedKVError) as e:
+            pk.pkv_decode_splitk_plan(**a)
+        assert e.value.status == pk.PKV_ERR_INVALID_ARG
+    S, n = ctypes.c_int32(0), ctypes.c_size_t(0)
+    assert pk.lib.pkv_decode_splitk_plan(4, 32, 8, 128, 8192, 16, 4, None, ctypes.byref(n)) == -1
+    assert pk.lib.pkv_decode_splitk_plan(4, 32, 8, 128, 8192, 16, 4, ctypes.byref(S), None) == -1
+
+
+def test_decode_splitk_plan_heuristic_needs_a_device(pk):
+    """num_splits = 0 asks the current GPU for its SM count: without one the
+    call reports a CUDA error instead of guessing."""
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    with pytest.raises(pk.PagedKVError) as e:
+        pk.pkv_decode_splitk_plan(4, 32, 8, 128, 8192, 16, 0)
+    assert e.value.status == pk.PKV_ERR_CUDA
+
+
+def test_varlen_splitk_plan(pk):
+    assert pk.pkv_varlen_splitk_plan(4, 16, 4, 32, 8, 128, 8192, 16, 10) == (
+        10, pk.pkv_splitk_scratch_bytes(16, 32, 128, 10))
+    assert pk.pkv_varlen_splitk_plan(4, 16, 4, 32, 8, 128, 3, 16, 64) == (
+        3, pk.pkv_splitk_scratch_bytes(16, 32, 128, 3))
+    assert pk.pkv_varlen_splitk_plan(4, 16, 4, 32, 8, 128, 8192, 16, 1) == (1, 0)
+    assert pk.pkv_varlen_splitk_plan(4, 0, 0, 32, 8, 128, 8192, 16, 0) == (1, 0)
+    with pytest.raises(pk.PagedKVError):
+        pk.pkv_varlen_splitk_plan(4, 16, 4, 32, 8, 128, 8192, 16, -1)
 
 
 def test_pick_num_splits_never_leaves_a_split_empty_by_length(pk):

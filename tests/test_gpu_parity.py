@@ -6,6 +6,8 @@ blocks, rows past a sequence's length and table entries past its blocks all
 hold or point at NaN, so a stray read shows up as NaN.
 """
 
+import dataclasses
+
 import numpy as np
 import pytest
 
@@ -68,7 +70,7 @@ def decode_all(pk, w, d, splits):
 # append
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("name", ["tiny", "llama8b"])
+@pytest.mark.parametrize("name", ["tiny", "llama8b", "long", "ragged"])
 def test_append_is_bit_exact(pk, cuda_device, name):
     w, _ = workload(name)
     d = appended_device(pk, w, cuda_device)
@@ -117,6 +119,57 @@ def test_decode_matches_oracle(pk, cuda_device, name, splits):
     outs = decode_all(pk, w, d, splits)
     for label, got in outs.items():
         assert_attention_close(got, ref, f"{name}/{label}")
+    assert pk.pkv_read_device_status() == 0
+
+
+@pytest.mark.parametrize("name", ["llama8b", "long"])
+def test_overprovisioned_tables_split_the_real_contexts(pk, cuda_device, name):
+    """Tables four times wider than the longest context (a server sizes them
+    for the model's maximum context): the split chunks are cut from the real
+    longest context, so with S forced to 4 the last split of the longest
+    sequence holds work (its partial max is finite, not the -inf of an empty
+    split), and every split count matches the oracle."""
+    w0, ref = workload(name)
+    w = W.widen_tables(w0, 4)
+    d = appended_device(pk, w, cuda_device)
+    S = 4
+    S_run, need = pk.pkv_decode_splitk_plan(w.num_seqs, w.num_heads, w.num_kv_heads, w.head_dim,
+                                            w.max_blocks_per_seq, w.block_size, S)
+    assert S_run == S and need == pk.pkv_splitk_scratch_bytes(w.num_seqs, w.num_heads,
+                                                              w.head_dim, S)
+    scratch = torch.empty(need, dtype=torch.uint8, device=cuda_device)
+    out = pk.pkv_decode_splitk(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                               d["context_lens"], w.scale, num_splits=S, scratch=scratch)
+    torch.cuda.synchronize()
+    assert_attention_close(to_np(out), ref, f"{name} x4 tables, S=4")
+    # scratch layout: f32 part_out [B][H][S][D], then part_m [B][H][S] (256-byte aligned)
+    a256 = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    rows = w.num_seqs * w.num_heads * S
+    part_m = scratch[a256(rows * w.head_dim * 4):][:rows * 4].view(torch.float32)
+    part_m = part_m.view(w.num_seqs, w.num_heads, S).cpu().numpy()
+    longest = int(np.argmax(w.context_lens))
+    assert np.all(np.isfinite(part_m[longest, :, S - 1])), "last split of the longest sequence"
+    for label, got in decode_all(pk, w, d, [0, 16]).items():
+        assert_attention_close(got, ref, f"{name} x4 tables, {label}")
+    assert pk.pkv_read_device_status() == 0
+
+
+def test_overprovisioned_tables_varlen_splitk(pk, cuda_device):
+    """Long speculative verification with tables four times wider than the
+    contexts: the varlen split chunks are cut from the real longest context."""
+    v0 = W.spec_verify_long()
+    kc, vc = W.host_pool(v0.base)
+    ref = oracle.varlen_fast(v0.q, kc, vc, v0.cu_seqlens_q, v0.pos_offsets, v0.base.block_tables,
+                             v0.base.scale)
+    del kc, vc
+    v = dataclasses.replace(v0, base=W.widen_tables(v0.base, 4))
+    d = varlen_device(v, cuda_device)
+    for S_req in (0, 8):
+        got = pk.pkv_varlen_attention_splitk(d["q"], d["k_cache"], d["v_cache"], d["cu"],
+                                             d["pos"], d["block_tables"], v.base.scale,
+                                             max_q_len=v.max_q_len, num_splits=S_req)
+        torch.cuda.synchronize()
+        assert_attention_close(to_np(got), ref, f"x4 tables, varlen S={S_req}")
     assert pk.pkv_read_device_status() == 0
 
 
@@ -494,7 +547,7 @@ def test_varlen_splitk_long_context_speculative_verification(pk, cuda_device):
                              v.base.scale)
     del kc, vc
     d = varlen_device(v, cuda_device)
-    S = pk.varlen_splits_for(d["q"], d["k_cache"], d["block_tables"], v.base.num_kv_heads, 4)
+    S = pk.varlen_splits_for(d["q"], d["k_cache"], d["block_tables"], 4)
     assert S > 1
     outs = {}
     for label, S_req in (("heuristic", 0), ("S=16", 16)):

@@ -71,10 +71,6 @@ typedef int32_t pkv_status;
 
 /* Largest num_splits pkv_decode_splitk accepts. */
 #define PKV_MAX_SPLITS 128
-/* num_splits value selecting the balanced schedule of pkv_decode_splitk. */
-#define PKV_SPLITS_BALANCED (-1)
-/* Most CTAs the balanced schedule launches (sizes its scratch). */
-#define PKV_BALANCED_MAX_CTAS 768
 
 /*
  * pkv_append — slot-mapped KV write (kapsl-backends src/gguf_native.rs,
@@ -141,14 +137,7 @@ pkv_status pkv_decode(const void* q, const void* k_cache, const void* v_cache,
  *                 block_size) / S) blocks (with num_splits = 0, at least
  *                 256 tokens' worth), so tables sized beyond the contexts
  *                 they hold still spread the work; splits past a sequence's
- *                 end do no work;
- *                 PKV_SPLITS_BALANCED = the balanced schedule: the list of
- *                 all (sequence, kv head, block) tiles is cut into equal
- *                 contiguous ranges, one per resident CTA (at most
- *                 PKV_BALANCED_MAX_CTAS), planned on the GPU from
- *                 context_lens, so every CTA reads the same number of bytes
- *                 whatever the mix of lengths; (sequence, head) runs cut by a
- *                 range boundary are merged by a second kernel.
+ *                 end do no work.
  *   scratch       device memory of at least the bytes pkv_decode_splitk_plan
  *                 returns for these sizes and num_splits
  *                 (pkv_splitk_scratch_bytes of the split count launched),
@@ -189,8 +178,6 @@ pkv_status pkv_decode_splitk(const void* q, const void* k_cache, const void* v_c
  * that reads position context_lens[s] - 1 writes the row and uses it
  * directly.  A non-negative slot that is not that position's slot is not
  * written (PKV_DEV_BAD_SLOT is set) and the decode reads the cache as it is.
- * With num_splits = PKV_SPLITS_BALANCED the append runs as its own kernel
- * first.
  */
 pkv_status pkv_append_decode(const void* k_new, const void* v_new, const int32_t* slot_mapping,
                              void* k_cache, void* v_cache, const void* q,
@@ -272,7 +259,7 @@ pkv_status pkv_append_vllm_layout(const void* k, const void* v, const int32_t* s
  * decode of paged_decode_attention_v2 in ferrum-kernels
  * src/backend/cuda/paged.rs): the same attention, the same outputs within
  * rounding.  num_splits 0, 1 or 2..PKV_MAX_SPLITS as for pkv_decode_splitk
- * (same scratch); PKV_SPLITS_BALANCED returns PKV_ERR_UNSUPPORTED.
+ * (same scratch).
  */
 pkv_status pkv_decode_vllm_layout(const void* q, const void* k_cache, const void* v_cache,
                                   const int32_t* block_tables, const int32_t* context_lens,
@@ -421,8 +408,7 @@ pkv_status pkv_qkv_norm_rope_append(const void* qkv, const void* q_norm_w, const
  *                 appends nothing and attends with zero queries (its output
  *                 is written but meaningless)
  *   k_cache, v_cache  the pools (blocked layout), read and written in place
- *   other arguments as pkv_decode_splitk (num_splits = PKV_SPLITS_BALANCED
- *   returns PKV_ERR_UNSUPPORTED)
+ *   other arguments as pkv_decode_splitk
  *
  * The cache ends as pkv_qkv_norm_rope_append would leave it (the key and
  * value rows of position context_lens[s] - 1 written) and out holds the
@@ -452,11 +438,10 @@ pkv_status pkv_selftest_wait_timeout(void* stream);
 
 /*
  * pkv_splitk_scratch_bytes — bytes of scratch pkv_decode_splitk needs for S
- * splits: f32 partial outputs [num_seqs][num_heads][S][head_dim] followed by
- * f32 running max and running sum [num_seqs][num_heads][S] each (every part
- * 256-byte aligned).  For S = PKV_SPLITS_BALANCED: f32 records
- * [PKV_BALANCED_MAX_CTAS][2][8][2 + head_dim] (independent of num_seqs and
- * num_heads).  0 when S is 0 or 1 or for invalid sizes.
+ * splits: a 256-byte header (the chunk size phase 1 chose, read by the
+ * combine), f32 partial outputs [num_seqs][num_heads][S][head_dim], then f32
+ * running max and running sum [num_seqs][num_heads][S] each (every part
+ * 256-byte aligned).  0 when S is 0 or 1 or for invalid sizes.
  * (ferrum-kernels paged.rs keeps these three buffers process-global and grows
  * them on demand; here the caller owns them.)
  */
@@ -475,8 +460,7 @@ size_t pkv_splitk_scratch_bytes(int32_t num_seqs, int32_t num_heads, int32_t hea
  * Below one wave: the split count that brings the grid nearest one wave;
  * at or above it: ceil(max_context_len / 2048); either capped at
  * max_context_len / 256, the block count and 64.  Returns 1 (single pass)
- * or a split count in 2..64 (never PKV_SPLITS_BALANCED); 1 for invalid
- * sizes.
+ * or a split count in 2..64; 1 for invalid sizes.
  */
 int32_t pkv_pick_num_splits(int32_t num_seqs, int32_t num_kv_heads,
                             int32_t max_context_len, int32_t block_size,
@@ -490,15 +474,15 @@ int32_t pkv_pick_num_splits(int32_t num_seqs, int32_t num_kv_heads,
  * sizes its process-global split scratch from the split count it picks;
  * here the caller sizes it).
  *
- *   *splits         1 (single pass), the split count launched
+ *   *splits         1 (single pass) or the split count launched
  *                   (2..PKV_MAX_SPLITS; num_splits capped at
- *                   max_blocks_per_seq), or PKV_SPLITS_BALANCED
+ *                   max_blocks_per_seq)
  *   *scratch_bytes  the scratch that call needs (0 for single pass)
  *
  * num_splits = 0 applies pkv_pick_num_splits for the current GPU (the one
  * query this makes to CUDA, for the SM count); no other CUDA call.  Returns
  * PKV_ERR_INVALID_ARG for null outputs, invalid sizes or num_splits outside
- * -1..PKV_MAX_SPLITS.
+ * 0..PKV_MAX_SPLITS.
  */
 pkv_status pkv_decode_splitk_plan(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
                                   int32_t head_dim, int32_t max_blocks_per_seq,

@@ -7,14 +7,13 @@
 //                                 optionally with the step's append, or the
 //                                 step's QKV norm + rotary + append, fused
 //                                 in; blocked or vLLM-layout pools
-//   splitk_combine_kernel         log-sum-exp merge of split-K partials
+//   splitk_combine_kernel         log-sum-exp merge of split-K partials (a
+//                                 warp per output row)
 //   varlen_combine_kernel         the same for varlen split-K partials
 //   paged_varlen_kernel           several causal queries per sequence (one or
 //                                 two mma n-tiles of 8 query-head columns);
 //                                 single pass or split-K phase 1; blocked or
 //                                 vLLM-layout pools
-//   paged_decode_balanced_kernel  decode over equal tile ranges per CTA
-//   balanced_combine_kernel       merge of the balanced schedule's records
 //   wait_timeout_probe_kernel     failure-path diagnostic (a bounded wait on a
 //                                 barrier nothing arrives on)
 //
@@ -347,12 +346,13 @@ struct DecodeParams {
   // Split-K chunks are cut on the device from the longest context of the
   // call: chunk = max(min_chunk_blocks, ceil(ceil(Lmax / BS) / S)) blocks,
   // so tables sized for a larger maximum context than the call holds still
-  // spread the work over every split.  chunk_hint is the host's guess
-  // (ceil(max_blocks_per_seq / S)); when it is right the first table entry
-  // of a split is loaded before Lmax is known.
+  // spread the work over every split.
   int min_chunk_blocks;
+  // The host's guess of the chunk, ceil(max_blocks_per_seq / S): when it is
+  // right the first table entry of a chunk is loaded before Lmax is known.
   int chunk_hint;
-  float scale_log2;  // scale * log2(e)
+  int* split_header;  // split-K: where phase 1 leaves the chunk size for the combine
+  float scale_log2;   // scale * log2(e)
   // Fair-share depth (set when the whole grid is resident at once): a CTA
   // keeps copies in flight in proportion to its share of the longest chunk
   // in the call.  HBM serves outstanding requests about evenly, so every CTA
@@ -805,38 +805,59 @@ __device__ __forceinline__ void merge_warps(const float* red, int stride, int h,
 }
 
 // Starts the TMA copies of the K and V tiles of (physical block, kv head)
-// into the stage at `kdst` (V follows K), completing on `bar`: one tensor
-// box per tile (landing as [D/64][BS][64], swizzled).  VLLM: K is one
-// contiguous bulk copy from `kpool`, V one 3-D tensor copy.
-template <int D, int BS, bool VLLM = false>
-__device__ __forceinline__ void issue_tile_copy(uint32_t kdst, uint32_t bar, int tile,
+// into the stage at `kdst` (V follows K), completing on `bar`.  Blocked
+// pools: one tensor box of TR = 16 rows per tile, from row `row0` of the
+// block (landing as [D/64][16][64], swizzled).  VLLM: a whole block (TR =
+// block size); K is one contiguous bulk copy from `kpool`, V one 3-D tensor
+// copy.
+template <int D, int TR, bool VLLM = false>
+__device__ __forceinline__ void issue_tile_copy(uint32_t kdst, uint32_t bar, int tile, int row0,
                                                 const CUtensorMap* kmap, const CUtensorMap* vmap,
                                                 const __half* kpool = nullptr) {
-  constexpr int TB = BS * D * 2;
+  constexpr int TB = TR * D * 2;
   mbar_arrive_expect_tx(bar, 2 * TB);
   if (VLLM) {
-    bulk_load(kdst, kpool + (size_t)tile * (BS * D), TB, bar);
+    bulk_load(kdst, kpool + (size_t)tile * (TR * D), TB, bar);
     tma_load_3d(kdst + TB, vmap, bar, 0, 0, tile);
   } else {
-    tma_load_4d(kdst, kmap, bar, 0, 0, 0, tile);
-    tma_load_4d(kdst + TB, vmap, bar, 0, 0, 0, tile);
+    tma_load_4d(kdst, kmap, bar, 0, row0, 0, tile);
+    tma_load_4d(kdst + TB, vmap, bar, 0, row0, 0, tile);
   }
 }
 
+// Staging in 16-row sub-tiles for blocked pools (build flag; see the kernel).
+#ifndef PKV_SUBTILE
+#define PKV_SUBTILE 1
+#endif
+constexpr bool kSubtile = PKV_SUBTILE != 0;
+
 // VLLM: the pools are in the vLLM layout (p.k_cache is the K pool; kmap is
-// unused); no fused append.
+// unused); no fused append.  Single pass: one CTA per (sequence, KV head).
+// Split-K phase 1: one CTA per (sequence, KV head, chunk); a chunk past the
+// sequence's end exits at once, a (sequence, KV head) whose context fits one
+// chunk is finished here (f16 output, the combine skips it), and the others
+// leave f32 partials per chunk for the combine.
 template <int D, int BS, int W, int P, bool SPLIT, bool FUSE, bool VLLM = false, bool QKV = false>
 __global__ void __launch_bounds__(W * 32)
 paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
   static_assert(!(FUSE && VLLM), "the fused append writes the blocked layout only");
   static_assert(!(QKV && (FUSE || VLLM)), "the fused QKV step is its own variant");
-  using Shape = DecodeShape<D, BS, W, P>;
+  // Staging tiles hold TR rows of one (block, KV head).  A blocked pool is
+  // read in 16-row sub-tiles, SUB per block, so every block size keeps the
+  // same stage size and ring depth; the vLLM layout stages whole blocks.
+  // Tile indices below count these sub-tiles.
+  constexpr int TR = (VLLM || !kSubtile) ? BS : 16;
+  constexpr int SUB = BS / TR;
+  using Shape = DecodeShape<D, TR, W, P>;
   constexpr int KS = Shape::kKS;
   constexpr int TB = Shape::kTileBytes;
+  constexpr int PL = D / 64;
+  constexpr int HPL = D / 32;  // halves per lane of one row
 
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_failed;
+  __shared__ int s_max[W];
   __shared__ __align__(16) __half s_q[QKV ? 8 * D : 2];   // QKV: the group's rotated queries
   __shared__ __align__(16) __half s_kv[QKV ? 2 * D : 2];  // QKV: the new key and value rows
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -846,12 +867,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-
-  int item = blockIdx.x;
-  const int split = SPLIT ? item % p.num_splits : 0;
-  if (SPLIT) item /= p.num_splits;
-  const int g = item % p.num_kv_heads;
-  const int s = item / p.num_kv_heads;
+  const int Hkv = p.num_kv_heads;
 
   pdl_launch_dependents();
   // Barrier set-up touches no global memory: before the dependency wait.
@@ -864,41 +880,28 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   }
   pdl_wait();
 
-  // Every independent global load of the prologue goes out together: the
-  // status word, the length, the warp's first block-table entry (its first
-  // tile is the chunk's block `warp` whatever the fair share decides; the
-  // entry is in bounds and only used if the tile exists; split kernels load
-  // it under the host's chunk guess), every length (the longest context sets
-  // the split chunks and the fair share) and the fused slot.
   const int cap = p.max_blocks_per_seq * BS;
+  // The CTA's work: sequence s, KV head g and (split) chunk `piece`.  Every
+  // independent global load of the prologue goes out together: the status
+  // word, the length, the warp's first block-table entry (its first tile is
+  // the chunk's tile `warp` whatever the fair share decides; the entry is in
+  // bounds and only used if the tile exists; split kernels load it under
+  // the host's chunk guess), the fused slot, (QKV) the raw projection-row
+  // heads, and every length (the longest context sets the split chunks and
+  // the fair share).
+  int item = blockIdx.x;
+  const int piece = SPLIT ? item % p.num_splits : 0;
+  if (SPLIT) item /= p.num_splits;
+  const int g = item % Hkv;
+  const int s = item / Hkv;
   const int32_t* table = p.block_tables + (size_t)s * p.max_blocks_per_seq;
   const unsigned int status = *reinterpret_cast<volatile unsigned int*>(&g_device_status);
-  int L = __ldg(p.context_lens + s);
-  const int j0_guess = (SPLIT ? split * p.chunk_hint : 0) + warp;
-  const int phys0_guess =
-      (lane == 0 && j0_guess < p.max_blocks_per_seq) ? __ldg(table + j0_guess) : -1;
-  __shared__ int s_max[W];
-  const bool need_max = SPLIT || p.fair_depth;
-  if (need_max) {
-    int mx = 0;
-    for (int i = threadIdx.x; i < p.num_seqs; i += W * 32) {
-      int Li = __ldg(p.context_lens + i);
-      Li = Li < 0 ? 0 : (Li > cap ? cap : Li);
-      mx = max(mx, (Li + BS - 1) / BS);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if (lane == 0) s_max[warp] = mx;
-  }
-  const int slot_new = FUSE ? __ldg(p.new_slots + s) : -1;
-  // QKV: the loads that need no length go out with the rest: the warp's
-  // query heads (warp, warp + W) of the projection row, the norm weights, and
-  // in warp W-1 the KV head's key and value heads.
-  constexpr int PL = D / 64;
+  // QKV: the warp's query heads (warp, warp + W) of the projection row, the
+  // norm weights, and in warp W-1 the KV head's key and value heads.
   uint32_t xq[2][2] = {{0u, 0u}, {0u, 0u}}, wq[2] = {0u, 0u};
   uint32_t xk[2] = {0u, 0u}, xv[2] = {0u, 0u}, wk[2] = {0u, 0u};
   if (QKV) {
-    const int H = p.num_heads, Hkv = p.num_kv_heads;
+    const int H = p.num_heads;
     const __half* row = p.qkv + (size_t)s * (H + 2 * Hkv) * D;
 #pragma unroll
     for (int j = 0; j < 2; ++j)
@@ -910,6 +913,24 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
       load_pairs<D>(row + (size_t)(H + Hkv + g) * D, lane, xv[0], xv[1]);
       if (p.k_norm_w) load_pairs<D>(p.k_norm_w, lane, wk[0], wk[1]);
     }
+  }
+  int L = __ldg(p.context_lens + s);
+  const int j0_guess = (SPLIT ? piece * p.chunk_hint * SUB : 0) + warp;  // in tiles
+  const int phys0_guess =
+      (lane == 0 && j0_guess / SUB < p.max_blocks_per_seq) ? __ldg(table + j0_guess / SUB) : -1;
+  const int slot_new = FUSE ? __ldg(p.new_slots + s) : -1;
+  const bool need_max = SPLIT || p.fair_depth;
+  if (need_max) {
+    int mx = 0;
+    for (int i = threadIdx.x; i < p.num_seqs; i += W * 32) {
+      int Li = __ldg(p.context_lens + i);
+      if (SPLIT && blockIdx.x == 0 && (Li < 0 || Li > cap)) atomicOr(&g_device_status, kDevBadContextLen);
+      Li = Li < 0 ? 0 : (Li > cap ? cap : Li);
+      mx = max(mx, (Li + BS - 1) / BS);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) s_max[warp] = mx;
   }
 
   // After a lost copy has been flagged, later CTAs do no work (and write
@@ -924,9 +945,21 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   const int chunk = SPLIT ? max(p.min_chunk_blocks, (nblk_max + p.num_splits - 1) / p.num_splits)
                           : p.max_blocks_per_seq;
 
-  if (L < 0 || L > cap) {
-    if (threadIdx.x == 0) atomicOr(&g_device_status, kDevBadContextLen);
+  if (SPLIT && blockIdx.x == 0 && threadIdx.x == 0) *p.split_header = chunk;  // for the combine
+
+  if (L < 0 || L > cap) {  // (split kernels flag it once, in CTA 0's scan)
+    if (!SPLIT && threadIdx.x == 0) atomicOr(&g_device_status, kDevBadContextLen);
     L = L < 0 ? 0 : cap;
+  }
+  int tok_begin = 0;
+  int tok_end = L;
+  int n_pieces = 1;  // chunks of this sequence (1: this CTA writes the output)
+  if (SPLIT) {
+    const int nb = (L + BS - 1) / BS;
+    n_pieces = (nb + chunk - 1) / chunk;
+    if ((long long)piece * chunk >= nb) return;  // past the sequence's end
+    tok_begin = piece * chunk * BS;
+    tok_end = (int)min((long long)L, (long long)tok_begin + (long long)chunk * BS);
   }
   // QKV: a newest position without rotary angles is flagged; the sequence
   // then attends with zero queries and appends nothing (its output is
@@ -935,39 +968,22 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   if (qkv_bad && threadIdx.x == 0) atomicOr(&g_device_status, kDevBadContextLen);
   float ang_c[PL], ang_s[PL];  // QKV: the rotary angles of position L-1
   if (QKV && !qkv_bad && L > 0 && (warp < p.group || warp == W - 1))
-    load_angles<D>(p.cos_t + (size_t)(L - 1) * (D / 2), p.sin_t + (size_t)(L - 1) * (D / 2), lane,
-                   ang_c, ang_s);
-  int tok_begin = 0;
-  int tok_end = L;
-  if (SPLIT) {
-    if ((long long)split * chunk * BS >= L) {
-      // Empty split: max -inf and sum 0 for the group's heads, so the
-      // combine can read every split (it gives these weight 0).
-      for (int h = threadIdx.x; h < p.group; h += W * 32) {
-        const size_t slot =
-            ((size_t)s * p.num_heads + (size_t)g * p.group + h) * p.num_splits + split;
-        p.part_m[slot] = -CUDART_INF_F;
-        p.part_l[slot] = 0.f;
-      }
-      return;
-    }
-    tok_begin = split * chunk * BS;
-    tok_end = (int)min((long long)L, (long long)tok_begin + (long long)chunk * BS);
-  }
-  const int blk_begin = tok_begin / BS;
-  const int n_tiles = (tok_end - tok_begin + BS - 1) / BS;
+    load_angles<D>(p.cos_t + (size_t)(L - 1) * (D / 2), p.sin_t + (size_t)(L - 1) * (D / 2),
+                   lane, ang_c, ang_s);
+  const int sub_begin = tok_begin / TR;  // the chunk's first tile
+  const int n_tiles = (tok_end - tok_begin + TR - 1) / TR;
   // the first tile's table entry: the prologue's guess when it was right
-  const int phys0 = (!SPLIT || split == 0 || chunk == p.chunk_hint)
+  const int phys0 = (!SPLIT || piece == 0 || chunk == p.chunk_hint)
                         ? phys0_guess
-                        : ((lane == 0 && blk_begin + warp < p.max_blocks_per_seq)
-                               ? __ldg(table + blk_begin + warp)
+                        : ((lane == 0 && (sub_begin + warp) / SUB < p.max_blocks_per_seq)
+                               ? __ldg(table + (sub_begin + warp) / SUB)
                                : -1);
 
   // Warps that take tiles: all W, or (fair share) W scaled by this chunk's
   // tiles over the longest chunk of the call.
   int WE = W;
   if (p.fair_depth) {
-    const int mx = SPLIT ? min(nblk_max, chunk) : nblk_max;
+    const int mx = (SPLIT ? min(nblk_max, chunk) : nblk_max) * SUB;
     if (mx > 0) WE = max(1, min(W, (W * n_tiles + mx - 1) / mx));
   }
   const int my_tiles = (warp < WE && n_tiles > warp) ? (n_tiles - warp + WE - 1) / WE : 0;
@@ -977,30 +993,31 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   // row into that tile in shared memory once the tile's copy has landed (so
   // it never depends on the global write being visible to its TMA reads).
   // A slot other than that position's is neither written nor used: flagged.
-  constexpr int HPL = D / 32;  // halves per lane of one row
-  int fuse_li = -1;            // local tile index of the new row, in its owner warp
-  int fuse_row = 0;
-  int kv_phys = -1;            // QKV: the new row's block when this CTA holds it
+  int fuse_li = -1;  // local tile index of the new row, in its owner warp
+  int fuse_row = 0;  // its row in that tile
+  int kv_phys = -1;  // QKV: the new row's block when this CTA holds it
+  int kv_prow = 0;   // and its row in the block
   uint32_t kn[HPL / 2], vn[HPL / 2];
   if ((FUSE || QKV) && !qkv_bad && L > 0 && L - 1 >= tok_begin && L - 1 < tok_end &&
       (QKV || slot_new >= 0)) {
     const int pos = L - 1;
     const int phys = __ldg(table + pos / BS);
-    const bool ok = phys >= 0 && phys < p.num_blocks && (QKV || slot_new == phys * BS + pos % BS);
+    const bool ok =
+        phys >= 0 && phys < p.num_blocks && (QKV || slot_new == phys * BS + pos % BS);
     if (!ok) {
       if (threadIdx.x == 0) atomicOr(&g_device_status, kDevBadSlot);
     } else {
-      const int idx = pos / BS - blk_begin;  // tile within the chunk
+      const int idx = pos / TR - sub_begin;  // tile within the chunk
+      fuse_row = pos % TR;
       if (QKV) {
         // the row is computed after the first copies are issued (below)
         kv_phys = phys;
-        fuse_row = pos % BS;
+        kv_prow = pos % BS;
         if (warp == idx % WE) fuse_li = idx / WE;
       } else if (warp == idx % WE) {
         fuse_li = idx / WE;
-        fuse_row = pos % BS;
-        const size_t src = ((size_t)s * p.num_kv_heads + g) * D + lane * HPL;
-        const size_t dst = (((size_t)phys * p.num_kv_heads + g) * BS + fuse_row) * D + lane * HPL;
+        const size_t src = ((size_t)s * Hkv + g) * D + lane * HPL;
+        const size_t dst = (((size_t)phys * Hkv + g) * BS + pos % BS) * D + lane * HPL;
 #pragma unroll
         for (int x = 0; x < HPL / 2; ++x) {
           kn[x] = __ldg(reinterpret_cast<const uint32_t*>(p.k_new + src) + x);
@@ -1015,15 +1032,15 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   auto k_stage = [&](int stage) { return ring + (warp * P + stage) * Shape::kStageBytes; };
 
   // Lane 0: start the copies of this warp's local tile `li` into its stage
-  // (tile 0's block-table entry was loaded in the prologue).
+  // (tile 0's entry was loaded in the prologue).
   auto issue = [&](int li) {
     const int stage = li % P;
-    const int j = blk_begin + warp + li * WE;
-    const int phys = (li == 0) ? phys0 : __ldg(table + j);
+    const int j = sub_begin + warp + li * WE;
+    const int phys = (li == 0) ? phys0 : __ldg(table + j / SUB);
     const uint32_t bar = my_bars + 8 * stage;
     if (phys >= 0 && phys < p.num_blocks) {
-      issue_tile_copy<D, BS, VLLM>(k_stage(stage), bar, phys * p.num_kv_heads + g, &kmap, &vmap,
-                                   p.k_cache);
+      issue_tile_copy<D, TR, VLLM>(k_stage(stage), bar, phys * Hkv + g, (j % SUB) * TR, &kmap,
+                                   &vmap, p.k_cache);
     } else {
       atomicOr(&g_device_status, kDevBadBlockId);
       mbar_arrive(bar);
@@ -1038,8 +1055,8 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   uint32_t qf[KS][2];
   uint32_t qk_lo = 0, qk_hi = 0, qv_lo = 0, qv_hi = 0;  // QKV: the new key / value row
   if (QKV) {
-    // With the first copies in flight: the group's queries (norm + rotary at
-    // position L-1) into shared memory; warp W-1 turns the new key row,
+    // With the first copies in flight: the group's queries (norm + rotary
+    // at position L-1) into shared memory; warp W-1 turns the new key row,
     // writes key and value rows to the pools and leaves them in shared
     // memory for the warp whose tile holds them.
     if (L > 0 && !qkv_bad) {
@@ -1057,7 +1074,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
         uint32_t lo, hi;
         norm_rotate_pairs<D>(xk[0], xk[1], p.k_norm_w != nullptr, wk[0], wk[1], ang_c, ang_s,
                              p.eps, lo, hi);
-        const size_t dst = (((size_t)kv_phys * p.num_kv_heads + g) * BS + fuse_row) * D;
+        const size_t dst = (((size_t)kv_phys * Hkv + g) * BS + kv_prow) * D;
         store_pairs<D>(p.k_cache + dst, lane, lo, hi);
         store_pairs<D>(p.v_cache + dst, lane, xv[0], xv[1]);
         store_pairs<D>(s_kv, lane, lo, hi);
@@ -1089,23 +1106,23 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
       failed = true;
       break;
     }
-    const int j = blk_begin + warp + li * WE;
-    const int phys = __ldg(table + j);
+    const int j = sub_begin + warp + li * WE;
+    const int phys = __ldg(table + j / SUB);
     if (phys >= 0 && phys < p.num_blocks) {
       const uint32_t kb = k_stage(stage);
       if (QKV && li == fuse_li) {
         // the new row of this tile is the one computed above, not the copy
         const int i0 = PL * lane;
         if (PL == 2) {
-          asm volatile("st.shared.u32 [%0], %1;" ::"r"(kb + swz<BS>(fuse_row, i0)), "r"(qk_lo) : "memory");
-          asm volatile("st.shared.u32 [%0], %1;" ::"r"(kb + swz<BS>(fuse_row, i0 + D / 2)), "r"(qk_hi) : "memory");
-          asm volatile("st.shared.u32 [%0], %1;" ::"r"(kb + TB + swz<BS>(fuse_row, i0)), "r"(qv_lo) : "memory");
-          asm volatile("st.shared.u32 [%0], %1;" ::"r"(kb + TB + swz<BS>(fuse_row, i0 + D / 2)), "r"(qv_hi) : "memory");
+          asm volatile("st.shared.u32 [%0], %1;" ::"r"(kb + swz<TR>(fuse_row, i0)), "r"(qk_lo) : "memory");
+          asm volatile("st.shared.u32 [%0], %1;" ::"r"(kb + swz<TR>(fuse_row, i0 + D / 2)), "r"(qk_hi) : "memory");
+          asm volatile("st.shared.u32 [%0], %1;" ::"r"(kb + TB + swz<TR>(fuse_row, i0)), "r"(qv_lo) : "memory");
+          asm volatile("st.shared.u32 [%0], %1;" ::"r"(kb + TB + swz<TR>(fuse_row, i0 + D / 2)), "r"(qv_hi) : "memory");
         } else {
-          asm volatile("st.shared.u16 [%0], %1;" ::"r"(kb + swz<BS>(fuse_row, i0)), "h"((unsigned short)qk_lo) : "memory");
-          asm volatile("st.shared.u16 [%0], %1;" ::"r"(kb + swz<BS>(fuse_row, i0 + D / 2)), "h"((unsigned short)qk_hi) : "memory");
-          asm volatile("st.shared.u16 [%0], %1;" ::"r"(kb + TB + swz<BS>(fuse_row, i0)), "h"((unsigned short)qv_lo) : "memory");
-          asm volatile("st.shared.u16 [%0], %1;" ::"r"(kb + TB + swz<BS>(fuse_row, i0 + D / 2)), "h"((unsigned short)qv_hi) : "memory");
+          asm volatile("st.shared.u16 [%0], %1;" ::"r"(kb + swz<TR>(fuse_row, i0)), "h"((unsigned short)qk_lo) : "memory");
+          asm volatile("st.shared.u16 [%0], %1;" ::"r"(kb + swz<TR>(fuse_row, i0 + D / 2)), "h"((unsigned short)qk_hi) : "memory");
+          asm volatile("st.shared.u16 [%0], %1;" ::"r"(kb + TB + swz<TR>(fuse_row, i0)), "h"((unsigned short)qv_lo) : "memory");
+          asm volatile("st.shared.u16 [%0], %1;" ::"r"(kb + TB + swz<TR>(fuse_row, i0 + D / 2)), "h"((unsigned short)qv_hi) : "memory");
         }
         __syncwarp();
       }
@@ -1114,12 +1131,12 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
 #pragma unroll
         for (int x = 0; x < HPL / 2; ++x) {
           const int d = lane * HPL + 2 * x;
-          asm volatile("st.shared.u32 [%0], %1;" ::"r"(kb + swz<BS>(fuse_row, d)), "r"(kn[x]) : "memory");
-          asm volatile("st.shared.u32 [%0], %1;" ::"r"(kb + TB + swz<BS>(fuse_row, d)), "r"(vn[x]) : "memory");
+          asm volatile("st.shared.u32 [%0], %1;" ::"r"(kb + swz<TR>(fuse_row, d)), "r"(kn[x]) : "memory");
+          asm volatile("st.shared.u32 [%0], %1;" ::"r"(kb + TB + swz<TR>(fuse_row, d)), "r"(vn[x]) : "memory");
         }
         __syncwarp();
       }
-      consume_tile<D, BS, false, VLLM>(kb, kb + TB, j * BS, tok_end, qf, p.scale_log2, st, lane);
+      consume_tile<D, TR, false, VLLM>(kb, kb + TB, j * TR, tok_end, qf, p.scale_log2, st, lane);
     }
     __syncwarp();
     if (lane == 0 && li + P < my_tiles) {
@@ -1154,8 +1171,8 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     float M, num, den;
     merge_warps<W, D>(red, Shape::kRedFloats, h, d, M, num, den);
     const size_t qh = (size_t)s * p.num_heads + (size_t)g * G + h;
-    if (SPLIT) {
-      const size_t slot = qh * p.num_splits + split;
+    if (SPLIT && n_pieces > 1) {
+      const size_t slot = qh * p.num_splits + piece;
       p.part_out[slot * D + d] = num;
       if (d == 0) {
         p.part_m[slot] = M;
@@ -1212,7 +1229,10 @@ template <int D, int BS, int W, int P, int NT, bool VLLM, bool SPLIT>
 __global__ void __launch_bounds__(W * 32)
 paged_varlen_kernel(const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap, const VarlenParams p) {
-  using Shape = DecodeShape<D, BS, W, P>;
+  // staging tiles as in the decode kernel: 16-row sub-tiles of blocked pools
+  constexpr int TR = (VLLM || !kSubtile) ? BS : 16;
+  constexpr int SUB = BS / TR;
+  using Shape = DecodeShape<D, TR, W, P>;
   static_assert(W * NT * Shape::kRedFloats * 4 <= Shape::kRingBytes,
                 "the merge area reuses the ring");
   constexpr int KS = Shape::kKS;
@@ -1313,12 +1333,12 @@ paged_varlen_kernel(const __grid_constant__ CUtensorMap kmap,
     tok_begin = split * chunk * BS;
     tok_end = (int)min((long long)chunk_end, (long long)tok_begin + (long long)chunk * BS);
   }
-  const int blk_begin = tok_begin / BS;
-  const int n_tiles = (tok_end - tok_begin + BS - 1) / BS;
+  const int sub_begin = tok_begin / TR;  // the CTA's first tile
+  const int n_tiles = (tok_end - tok_begin + TR - 1) / TR;
   const int32_t* table = p.block_tables + (size_t)s * p.max_blocks_per_seq;
   int WE = W;  // warps that take tiles (fewer for short chunks under the fair share)
   if (p.fair_depth) {
-    const int mx = SPLIT ? min(nblk_max, chunk) : nblk_max;
+    const int mx = (SPLIT ? min(nblk_max, chunk) : nblk_max) * SUB;
     if (mx > 0) WE = max(1, min(W, (W * n_tiles + mx - 1) / mx));
   }
   const int my_tiles = (warp < WE && n_tiles > warp) ? (n_tiles - warp + WE - 1) / WE : 0;
@@ -1326,12 +1346,12 @@ paged_varlen_kernel(const __grid_constant__ CUtensorMap kmap,
   auto k_stage = [&](int stage) { return ring + (warp * P + stage) * Shape::kStageBytes; };
   auto issue = [&](int li) {
     const int stage = li % P;
-    const int j = blk_begin + warp + li * WE;
-    const int phys = __ldg(table + j);
+    const int j = sub_begin + warp + li * WE;
+    const int phys = __ldg(table + j / SUB);
     const uint32_t bar = my_bars + 8 * stage;
     if (phys >= 0 && phys < p.num_blocks) {
-      issue_tile_copy<D, BS, VLLM>(k_stage(stage), bar, phys * p.num_kv_heads + g, &kmap, &vmap,
-                                   p.k_pool);
+      issue_tile_copy<D, TR, VLLM>(k_stage(stage), bar, phys * p.num_kv_heads + g, (j % SUB) * TR,
+                                   &kmap, &vmap, p.k_pool);
     } else {
       atomicOr(&g_device_status, kDevBadBlockId);
       mbar_arrive(bar);
@@ -1373,11 +1393,11 @@ paged_varlen_kernel(const __grid_constant__ CUtensorMap kmap,
       failed = true;
       break;
     }
-    const int j = blk_begin + warp + li * WE;
-    const int phys = __ldg(table + j);
+    const int j = sub_begin + warp + li * WE;
+    const int phys = __ldg(table + j / SUB);
     if (phys >= 0 && phys < p.num_blocks) {
       const uint32_t kb = k_stage(stage);
-      consume_tiles<D, BS, NT, true, VLLM>(kb, kb + TB, j * BS, tok_end, qf, p.scale_log2, st,
+      consume_tiles<D, TR, NT, true, VLLM>(kb, kb + TB, j * TR, tok_end, qf, p.scale_log2, st,
                                            lane, lim);
     }
     __syncwarp();
@@ -1423,487 +1443,6 @@ paged_varlen_kernel(const __grid_constant__ CUtensorMap kmap,
 }
 
 // ---------------------------------------------------------------------------
-// balanced schedule
-// ---------------------------------------------------------------------------
-//
-// The work is the list of all (sequence s, logical block j) units in (s, j)
-// order, T = the total.  CTA c = m * Hkv + g of N = M * Hkv takes KV head g
-// of the contiguous unit range [m*T/M, (m+1)*T/M), so every CTA moves the
-// same number of K/V bytes whatever the mix of context lengths, and the Hkv
-// CTAs of a range read the Hkv tiles of each physical block (contiguous in
-// the pool) at about the same time.  Each CTA plans its range on the device
-// from context_lens (no host read).  A sequence wholly inside one range is
-// finished there (f16 output); a sequence cut by range boundaries leaves one
-// partial record (m, l, acc) per CTA piece, merged by
-// balanced_combine_kernel.  A CTA has at most two cut pieces (its first and
-// last), so records are [N][2][8 heads][2 + D] f32.
-
-struct BalancedParams {
-  const __half* q;
-  const int32_t* block_tables;
-  const int32_t* context_lens;
-  __half* out;
-  float* records;
-  int num_seqs;
-  int num_heads;
-  int num_kv_heads;
-  int group;
-  int max_blocks_per_seq;
-  int num_blocks;
-  int num_ctas;  // N
-  float scale_log2;
-};
-
-constexpr int kRecHeads = 8;
-
-template <int BS>
-__device__ __forceinline__ int clamped_len(const int32_t* lens, int s, int cap) {
-  int L = __ldg(lens + s);
-  return L < 0 ? 0 : (L > cap ? cap : L);
-}
-
-// Sum over the CTA (every thread passes its value; all get the total).
-template <int NT>
-__device__ __forceinline__ long long block_sum(long long v, long long* sm) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  if (lane == 0) sm[warp] = v;
-  __syncthreads();
-  long long t = 0;
-#pragma unroll
-  for (int w = 0; w < NT / 32; ++w) t += sm[w];
-  __syncthreads();
-  return t;
-}
-
-// Inclusive prefix sum over the CTA in thread order; *total gets the sum.
-template <int NT>
-__device__ __forceinline__ long long block_incl_scan(long long v, long long* sm, long long* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const long long y = __shfl_up_sync(0xffffffffu, v, o);
-    if (lane >= o) v += y;
-  }
-  if (lane == 31) sm[warp] = v;
-  __syncthreads();
-  long long before = 0, t = 0;
-#pragma unroll
-  for (int w = 0; w < NT / 32; ++w) {
-    const long long x = sm[w];
-    if (w < warp) before += x;
-    t += x;
-  }
-  __syncthreads();
-  *total = t;
-  return v + before;
-}
-
-// Position in the unit list: the sequence s holding a unit and where its
-// blocks start.  n is the block count of sequence s, start the units of
-// sequences < s.  (The KV head is the CTA's own.)
-struct SegCursor {
-  int s, n;
-  long long start;
-};
-
-template <int BS>
-__device__ __forceinline__ void cursor_next(SegCursor& cu, const int32_t* lens, int B, int cap) {
-  cu.start += cu.n;
-  do {
-    ++cu.s;
-    cu.n = cu.s < B ? (clamped_len<BS>(lens, cu.s, cap) + BS - 1) / BS : 1;
-  } while (cu.n == 0);
-}
-
-template <int BS>
-__device__ __forceinline__ void cursor_seek(SegCursor& cu, long long u, const int32_t* lens, int B,
-                                            int cap) {
-  while (u >= cu.start + cu.n) cursor_next<BS>(cu, lens, B, cap);
-}
-
-// Plans this CTA's range: T (units), [u_begin, u_end) and the sequence
-// holding u_begin.  Returns false (uniformly) when the range is empty.  With
-// at most NT sequences one block-wide scan gives everything; otherwise the
-// total comes first and a chunked scan then finds the sequence.
-template <int BS, int NT>
-__device__ __forceinline__ bool plan_range(const BalancedParams& p, int m, long long* T_out,
-                                           long long* ub, long long* ue, SegCursor* cu,
-                                           long long* sm_scan, int* sm_s, long long* sm_P) {
-  const int cap = p.max_blocks_per_seq * BS;
-  const int B = p.num_seqs;
-  const long long M = p.num_ctas / p.num_kv_heads;
-  const bool flag = blockIdx.x == 0;
-  if (threadIdx.x == 0) *sm_s = -1;  // ordered before its use by the scan's barriers
-  long long T, u_begin, u_end;
-  if (B <= NT) {
-    const int s = threadIdx.x;
-    const int L = s < B ? __ldg(p.context_lens + s) : 0;
-    if ((L < 0 || L > cap) && flag) atomicOr(&g_device_status, kDevBadContextLen);
-    const long long n = s < B ? (clamped_len<BS>(p.context_lens, s, cap) + BS - 1) / BS : 0;
-    long long total;
-    const long long incl = block_incl_scan<NT>(n, sm_scan, &total);
-    T = total;
-    *T_out = T;
-    if (T == 0) return false;
-    u_begin = T * m / M;
-    u_end = T * (m + 1) / M;
-    if (u_begin >= u_end) return false;
-    const long long first = incl - n;
-    if (n > 0 && first <= u_begin && u_begin < first + n) {
-      *sm_s = s;
-      *sm_P = first;
-    }
-    __syncthreads();
-  } else {
-    long long mine = 0;
-    for (int s = threadIdx.x; s < B; s += NT) {
-      const int L = __ldg(p.context_lens + s);
-      if ((L < 0 || L > cap) && flag) atomicOr(&g_device_status, kDevBadContextLen);
-      mine += (clamped_len<BS>(p.context_lens, s, cap) + BS - 1) / BS;
-    }
-    T = block_sum<NT>(mine, sm_scan);
-    *T_out = T;
-    if (T == 0) return false;
-    u_begin = T * m / M;
-    u_end = T * (m + 1) / M;
-    if (u_begin >= u_end) return false;
-    long long carry = 0;
-    for (int base = 0; base < B; base += NT) {
-      const int s = base + threadIdx.x;
-      const long long n = s < B ? (clamped_len<BS>(p.context_lens, s, cap) + BS - 1) / BS : 0;
-      long long chunk_total;
-      const long long incl = block_incl_scan<NT>(n, sm_scan, &chunk_total);
-      const long long first = carry + incl - n;  // blocks of sequences before s
-      if (n > 0 && first <= u_begin && u_begin < first + n) {
-        *sm_s = s;
-        *sm_P = first;
-      }
-      carry += chunk_total;
-      __syncthreads();
-      if (*sm_s >= 0) break;
-    }
-  }
-  *ub = u_begin;
-  *ue = u_end;
-  cu->s = *sm_s;
-  cu->start = *sm_P;
-  cu->n = (clamped_len<BS>(p.context_lens, cu->s, cap) + BS - 1) / BS;
-  return true;
-}
-
-// Bounded wait for a shared-memory counter to reach `want`.
-__device__ __forceinline__ bool smem_wait_eq(volatile int* x, int want, uint64_t limit_ns) {
-  if (*x == want) return true;
-  const uint64_t t0 = global_timer_ns();
-  while (*x != want) {
-    __nanosleep(64);
-    if (global_timer_ns() - t0 > limit_ns) return false;
-  }
-  return true;
-}
-
-template <int D, int BS, int W, int P>
-__global__ void __launch_bounds__(W * 32)
-paged_decode_balanced_kernel(const __grid_constant__ CUtensorMap kmap,
-                             const __grid_constant__ CUtensorMap vmap, const BalancedParams p) {
-  using Shape = DecodeShape<D, BS, W, P>;
-  constexpr int KS = Shape::kKS;
-  constexpr int TB = Shape::kTileBytes;
-  constexpr int NT = W * 32;
-
-  extern __shared__ uint8_t smem_raw[];
-  __shared__ int s_failed;
-  __shared__ int s_arrive;  // warps that deposited the current piece
-  __shared__ int s_done;    // pieces merged so far
-  __shared__ long long sm_scan[NT / 32];
-  __shared__ int sm_s;
-  __shared__ long long sm_P;
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t ring = smem_addr(smem);
-  const uint32_t bars = ring + Shape::kRingBytes;
-  const int G = p.group;
-  const int red_stride = 16 + G * D;
-  float* red = reinterpret_cast<float*>(smem + Shape::kRingBytes + Shape::kBarrierBytes);
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int c = blockIdx.x;
-  const int Hkv = p.num_kv_heads;
-  const int g = c % Hkv;  // this CTA's KV head
-  const int m = c / Hkv;  // and its unit range
-
-  pdl_launch_dependents();
-  pdl_wait();
-  if (__syncthreads_or(*reinterpret_cast<volatile unsigned int*>(&g_device_status) &
-                       kDevWaitTimeout))
-    return;
-
-  long long T, u_begin, u_end;
-  SegCursor cc;
-  if (!plan_range<BS, NT>(p, m, &T, &u_begin, &u_end, &cc, sm_scan, &sm_s, &sm_P)) return;
-
-  const int cap = p.max_blocks_per_seq * BS;
-  const int B = p.num_seqs;
-  const long long span = u_end - u_begin;
-  const int my_tiles = span > warp ? (int)((span - warp + W - 1) / W) : 0;
-
-  if (threadIdx.x == 0) {
-    s_failed = 0;
-    s_arrive = 0;
-    s_done = 0;
-  }
-  const uint32_t my_bars = bars + warp * P * 8;
-  if (lane == 0) {
-#pragma unroll
-    for (int i = 0; i < P; ++i) mbar_init(my_bars + 8 * i, 1);
-    fence_mbar_init();
-  }
-  __syncthreads();
-
-  auto k_stage = [&](int stage) { return ring + (warp * P + stage) * Shape::kStageBytes; };
-
-  // Producer (lane 0): the warp's k-th tile is u_begin + warp + k*W.
-  SegCursor pc = cc;
-  auto issue = [&](int k) {
-    const long long u = u_begin + warp + (long long)k * W;
-    cursor_seek<BS>(pc, u, p.context_lens, B, cap);
-    const int j = (int)(u - pc.start);
-    const int phys = __ldg(p.block_tables + (size_t)pc.s * p.max_blocks_per_seq + j);
-    const uint32_t bar = my_bars + 8 * (k % P);
-    if (phys >= 0 && phys < p.num_blocks) {
-      issue_tile_copy<D, BS>(k_stage(k % P), bar, phys * Hkv + g, &kmap, &vmap);
-    } else {
-      atomicOr(&g_device_status, kDevBadBlockId);
-      mbar_arrive(bar);
-    }
-  };
-  if (lane == 0) {
-    const int n0 = my_tiles < P ? my_tiles : P;
-    for (int k = 0; k < n0; ++k) issue(k);
-  }
-
-  // q of the current piece, and of the next one loaded a piece ahead
-  uint32_t qf[KS][2], qn[KS][2];
-  load_q_frags<D>(qf, p.q, (size_t)cc.s * p.num_heads + (size_t)g * G, G, lane);
-  SegCursor nc = cc;
-  bool has_next = cc.start + cc.n < u_end;
-  if (has_next) {
-    cursor_next<BS>(nc, p.context_lens, B, cap);
-    load_q_frags<D>(qn, p.q, (size_t)nc.s * p.num_heads + (size_t)g * G, G, lane);
-  }
-
-  bool failed = false;
-  int k_done = 0;  // tiles this warp has consumed
-  int piece = 0;
-  long long u = u_begin;
-  while (u < u_end) {
-    const long long seg_end = cc.start + cc.n;
-    const long long a = u, b = seg_end < u_end ? seg_end : u_end;
-    const int L = clamped_len<BS>(p.context_lens, cc.s, cap);
-
-    WarpState<D> st;
-    st.reset();
-    const int off = (int)((a - u_begin) % W);
-    for (long long t = a + ((warp - off + W) % W); t < b && !failed; t += W) {
-      const int k = (int)((t - u_begin - warp) / W);
-      if (!mbar_wait_bounded(my_bars + 8 * (k % P), (k / P) & 1, kWaitLimitNs)) {
-        failed = true;
-        break;
-      }
-      const int j = (int)(t - cc.start);
-      const int phys = __ldg(p.block_tables + (size_t)cc.s * p.max_blocks_per_seq + j);
-      if (phys >= 0 && phys < p.num_blocks) {
-        const uint32_t kb = k_stage(k % P);
-        consume_tile<D, BS>(kb, kb + TB, j * BS, L, qf, p.scale_log2, st, lane);
-      }
-      k_done = k + 1;
-      __syncwarp();
-      if (lane == 0 && k + P < my_tiles) {
-        fence_proxy_async_smem();
-        issue(k + P);
-      }
-    }
-    st.finish_sums();
-
-    // Deposit this warp's state for the piece; the last warp to arrive
-    // merges the W states and writes the piece's output or record while the
-    // others go on.  The buffer is free once the previous piece is merged.
-    if (!smem_wait_eq(&s_done, piece, kWaitLimitNs)) failed = true;
-    if (failed && lane == 0) atomicOr(&s_failed, 1);
-    __threadfence_block();
-    st.store(red + warp * red_stride, lane, G);
-    __threadfence_block();
-    __syncwarp();
-    int last = 0;
-    if (lane == 0) {
-      __threadfence_block();
-      last = atomicAdd(&s_arrive, 1) == W - 1;
-    }
-    last = __shfl_sync(0xffffffffu, last, 0);
-    if (last) {
-      __threadfence_block();
-      if (!*reinterpret_cast<volatile int*>(&s_failed)) {
-        const bool whole = (a == cc.start) && (b == seg_end);
-        const int slot = (a == u_begin) ? 0 : 1;
-        for (int idx = lane; idx < G * D; idx += 32) {
-          const int h = idx / D;
-          const int d = idx - h * D;
-          float M, num, den;
-          merge_warps<W, D>(red, red_stride, h, d, M, num, den);
-          if (whole) {
-            const size_t qh = (size_t)cc.s * p.num_heads + (size_t)g * G + h;
-            p.out[qh * D + d] = __float2half_rn(den > 0.f ? num / den : 0.f);
-          } else {
-            float* rec = p.records + (((size_t)c * 2 + slot) * kRecHeads + h) * (D + 2);
-            rec[2 + d] = num;
-            if (d == 0) {
-              rec[0] = M;
-              rec[1] = den;
-            }
-          }
-        }
-      }
-      __syncwarp();
-      if (lane == 0) {
-        s_arrive = 0;
-        __threadfence_block();
-        atomicAdd(&s_done, 1);
-      }
-    }
-
-    ++piece;
-    u = b;
-    if (u < u_end) {
-      cc = nc;
-#pragma unroll
-      for (int i = 0; i < KS; ++i) {
-        qf[i][0] = qn[i][0];
-        qf[i][1] = qn[i][1];
-      }
-      has_next = cc.start + cc.n < u_end;
-      if (has_next) {
-        cursor_next<BS>(nc, p.context_lens, B, cap);
-        load_q_frags<D>(qn, p.q, (size_t)nc.s * p.num_heads + (size_t)g * G, G, lane);
-      }
-    }
-  }
-
-  if (failed) {
-    if (lane == 0) atomicOr(&g_device_status, kDevWaitTimeout);
-    const int last_k = min(k_done + P, my_tiles);
-    for (int k = k_done; k < last_k; ++k)
-      (void)mbar_wait_bounded(my_bars + 8 * (k % P), (k / P) & 1, kWaitLimitNs);
-  }
-}
-
-// Merges the records of segments that CTA range boundaries cut, and writes
-// zeros for empty sequences.  One CTA per (sequence, query head), threads
-// over head_dim; each thread sums the records with batches of independent
-// loads.
-template <int D, int BS>
-__global__ void __launch_bounds__(128) balanced_combine_kernel(const BalancedParams p) {
-  constexpr int NT = 128;
-  __shared__ long long sm_scan[NT / 32];
-  __shared__ int s_rec[PKV_BALANCED_MAX_CTAS];   // record index, -1 = none
-  __shared__ float s_w[PKV_BALANCED_MAX_CTAS];   // 2^(m - M) per record
-  __shared__ float s_red[NT / 32];
-  pdl_launch_dependents();
-  pdl_wait();
-  const int s = blockIdx.x / p.num_heads;
-  const int hq = blockIdx.x % p.num_heads;  // query head
-  const int G = p.group;
-  const int g = hq / G, h = hq % G;
-  const int cap = p.max_blocks_per_seq * BS;
-  const int B = p.num_seqs, Hkv = p.num_kv_heads;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const size_t orow = ((size_t)s * p.num_heads + hq) * D;
-
-  long long all = 0, before = 0;
-  for (int s2 = threadIdx.x; s2 < B; s2 += NT) {
-    const long long n = (clamped_len<BS>(p.context_lens, s2, cap) + BS - 1) / BS;
-    all += n;
-    if (s2 < s) before += n;
-  }
-  const long long tiles = block_sum<NT>(all, sm_scan);
-  const long long Ps = block_sum<NT>(before, sm_scan);
-  const long long n = (clamped_len<BS>(p.context_lens, s, cap) + BS - 1) / BS;
-  if (n == 0) {
-    for (int d = threadIdx.x; d < D; d += NT) p.out[orow + d] = __float2half_rn(0.f);
-    return;
-  }
-  const long long T = tiles, Mp = p.num_ctas / Hkv;
-  const long long seg_start = Ps, seg_end = seg_start + n;
-  const long long m_lo = ((seg_start + 1) * Mp - 1) / T;  // range holding the first block
-  const long long m_hi = (seg_end * Mp - 1) / T;          // range holding the last block
-  if (m_lo == m_hi) return;  // finished by its CTA
-  const long long ub_lo = m_lo * T / Mp;
-  const int R = (int)(m_hi - m_lo + 1);
-
-  for (int r = threadIdx.x; r < R; r += NT) {
-    const long long mr = m_lo + r;
-    const bool has = mr * T / Mp < (mr + 1) * T / Mp;  // an empty range wrote nothing
-    const int slot = (mr == m_lo && seg_start > ub_lo) ? 1 : 0;
-    const int ri = has ? (int)((mr * Hkv + g) * 2 + slot) : -1;
-    s_rec[r] = ri;
-  }
-  __syncthreads();
-  float M = -CUDART_INF_F;
-  for (int r = threadIdx.x; r < R; r += NT) {
-    const int ri = s_rec[r];
-    if (ri >= 0) M = fmaxf(M, __ldg(p.records + ((size_t)ri * kRecHeads + h) * (D + 2)));
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  if (lane == 0) s_red[warp] = M;
-  __syncthreads();
-  M = fmaxf(fmaxf(s_red[0], s_red[1]), fmaxf(s_red[2], s_red[3]));
-  __syncthreads();
-  float den = 0.f;
-  for (int r = threadIdx.x; r < R; r += NT) {
-    const int ri = s_rec[r];
-    float f = 0.f;
-    if (ri >= 0) {
-      const float* rec = p.records + ((size_t)ri * kRecHeads + h) * (D + 2);
-      const float mr = __ldg(rec);
-      const float lr = __ldg(rec + 1);
-      if (mr != -CUDART_INF_F) {
-        f = exp2f(mr - M);
-        den += f * lr;
-      }
-    }
-    s_w[r] = f;
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-  if (lane == 0) s_red[warp] = den;
-  __syncthreads();
-  den = s_red[0] + s_red[1] + s_red[2] + s_red[3];
-
-  for (int d = threadIdx.x; d < D; d += NT) {
-    float num = 0.f;
-    int r = 0;
-    for (; r + 8 <= R; r += 8) {
-      float a[8];
-#pragma unroll
-      for (int x = 0; x < 8; ++x) {
-        const int ri = s_rec[r + x];
-        a[x] = ri >= 0 ? __ldg(p.records + ((size_t)ri * kRecHeads + h) * (D + 2) + 2 + d) : 0.f;
-      }
-#pragma unroll
-      for (int x = 0; x < 8; ++x) num += s_w[r + x] * a[x];
-    }
-    for (; r < R; ++r) {
-      const int ri = s_rec[r];
-      if (ri >= 0) num += s_w[r] * __ldg(p.records + ((size_t)ri * kRecHeads + h) * (D + 2) + 2 + d);
-    }
-    p.out[orow + d] = __float2half_rn(den > 0.f ? num / den : 0.f);
-  }
-}
-
-// ---------------------------------------------------------------------------
 // split-K combine
 // ---------------------------------------------------------------------------
 
@@ -1911,86 +1450,138 @@ struct CombineParams {
   const float* part_out;
   const float* part_m;
   const float* part_l;
+  const int32_t* context_lens;
+  const int* split_header;  // the chunk size (blocks) phase 1 used
   __half* out;
+  int num_rows;  // num_seqs * num_heads
   int num_heads;
-  int head_dim;
   int num_splits;
+  int block_size;
+  int cap_tokens;  // max_blocks_per_seq * block_size
 };
 
-// The merge of one output row from its split partials, by a CTA of
-// kCombineThreads threads: thread k loads split k's max and sum (all splits
-// at once), the CTA reduces them, and thread d then sums the splits' partial
-// outputs with independent loads.  Every split was written by phase 1; an
-// empty one holds max -inf and sum 0, gets weight 0, and its partial output
-// (never written) is not read.
-constexpr int kCombineThreads = 128;
+// Rows (output head vectors) merged per combine CTA: one warp each.
+constexpr int kCombineWarps = 4;
 
-__device__ __forceinline__ void combine_row(const float* pm, const float* pl, const float* po,
-                                            int num_splits, int head_dim, __half* out_row,
-                                            float* s_w, float* s_red) {
-  constexpr int NT = kCombineThreads;
-  static_assert(PKV_MAX_SPLITS <= NT, "one thread per split");
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int k = threadIdx.x;  // num_splits <= PKV_MAX_SPLITS = NT
-  const float mk = k < num_splits ? __ldg(pm + k) : -CUDART_INF_F;
-  const float lk = k < num_splits ? __ldg(pl + k) : 0.f;
-  float M = mk;
+// The log-sum-exp merge of one output row of D elements from its first n
+// split partials, by one warp: lanes read the splits' maxima and sums
+// (M = max m_k, w_k = 2^(m_k - M), den = sum w_k l_k), then each lane sums
+// its D/32 elements of the weighted partial outputs with vector loads.  A
+// split with weight 0 (max -inf: no position of the row in it) is not read.
+template <int D>
+__device__ __forceinline__ void merge_row_warp(const float* pm, const float* pl, const float* po,
+                                               int n, __half* out_row, float* s_w) {
+  constexpr int E = D / 32;  // elements per lane
+  const int lane = threadIdx.x & 31;
+  float M = -CUDART_INF_F;
+  for (int k = lane; k < n; k += 32) M = fmaxf(M, __ldg(pm + k));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  if (lane == 0) s_red[warp] = M;
-  __syncthreads();
-  M = fmaxf(fmaxf(s_red[0], s_red[1]), fmaxf(s_red[2], s_red[3]));
-  __syncthreads();
-  const float w = (mk == -CUDART_INF_F) ? 0.f : exp2f(mk - M);
-  if (k < PKV_MAX_SPLITS) s_w[k] = w;
-  float den = w * lk;
+  float den = 0.f;
+  for (int k = lane; k < n; k += 32) {
+    const float mk = __ldg(pm + k);
+    const float w = (mk == -CUDART_INF_F) ? 0.f : exp2f(mk - M);
+    s_w[k] = w;
+    den += w * __ldg(pl + k);
+  }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-  if (lane == 0) s_red[warp] = den;
-  __syncthreads();
-  den = s_red[0] + s_red[1] + s_red[2] + s_red[3];
-
-  // the last split with a weight (valid splits are a prefix of the chunks,
-  // but any zero-weight split is skipped, not read)
-  int n = num_splits;
-  while (n > 0 && s_w[n - 1] == 0.f) --n;
-  for (int d = threadIdx.x; d < head_dim; d += NT) {
-    float num = 0.f;
-    int kk = 0;
-    for (; kk + 4 <= n; kk += 4) {
-      const float w0 = s_w[kk], w1 = s_w[kk + 1], w2 = s_w[kk + 2], w3 = s_w[kk + 3];
-      const float a0 = w0 != 0.f ? __ldg(po + (size_t)kk * head_dim + d) : 0.f;
-      const float a1 = w1 != 0.f ? __ldg(po + (size_t)(kk + 1) * head_dim + d) : 0.f;
-      const float a2 = w2 != 0.f ? __ldg(po + (size_t)(kk + 2) * head_dim + d) : 0.f;
-      const float a3 = w3 != 0.f ? __ldg(po + (size_t)(kk + 3) * head_dim + d) : 0.f;
-      num += w0 * a0 + w1 * a1 + w2 * a2 + w3 * a3;
+  __syncwarp();
+  float acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  const float* base = po + lane * E;
+  auto load = [&](int k, float (&v)[E]) {
+    if constexpr (E == 4) {
+      const float4 x = __ldg(reinterpret_cast<const float4*>(base + (size_t)k * D));
+      v[0] = x.x;
+      v[1] = x.y;
+      v[2] = x.z;
+      v[3] = x.w;
+    } else {
+      const float2 x = __ldg(reinterpret_cast<const float2*>(base + (size_t)k * D));
+      v[0] = x.x;
+      v[1] = x.y;
     }
-    for (; kk < n; ++kk)
-      if (s_w[kk] != 0.f) num += s_w[kk] * __ldg(po + (size_t)kk * head_dim + d);
-    out_row[d] = __float2half_rn(den > 0.f ? num / den : 0.f);
+  };
+  int k = 0;
+  for (; k + 4 <= n; k += 4) {  // four splits' loads in flight at once
+    float v[4][E];
+    float w[4];
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      w[x] = s_w[k + x];
+      if (w[x] != 0.f) {
+        load(k + x, v[x]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e) v[x][e] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] += w[x] * v[x][e];
   }
+  for (; k < n; ++k) {
+    const float w = s_w[k];
+    if (w != 0.f) {
+      float v[E];
+      load(k, v);
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] += w * v[e];
+    }
+  }
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  __half2 h[E / 2];
+#pragma unroll
+  for (int e = 0; e < E / 2; ++e)
+    h[e] = __floats2half2_rn(den > 0.f ? acc[2 * e] * inv : 0.f,
+                             den > 0.f ? acc[2 * e + 1] * inv : 0.f);
+  if constexpr (E == 4)
+    *reinterpret_cast<uint2*>(out_row + lane * E) = make_uint2(pack_half2(h[0]), pack_half2(h[1]));
+  else
+    *reinterpret_cast<uint32_t*>(out_row + lane * E) = pack_half2(h[0]);
 }
 
-// Decode split-K: one CTA per (sequence, query head).
-__global__ void __launch_bounds__(kCombineThreads) splitk_combine_kernel(const CombineParams p) {
-  __shared__ float s_w[PKV_MAX_SPLITS];
-  __shared__ float s_red[kCombineThreads / 32];
+// Decode split-K: one warp per (sequence, query head) row.  The row's chunk
+// count n follows from its length and the chunk size phase 1 used: n = 1 was
+// finished by phase 1 (f16 output written), n = 0 (empty context) is zeros,
+// n > 1 merges the n partials phase 1 wrote.
+template <int D>
+__global__ void __launch_bounds__(kCombineWarps * 32) splitk_combine_kernel(const CombineParams p) {
+  __shared__ float s_w[kCombineWarps][PKV_MAX_SPLITS];
   pdl_launch_dependents();
   pdl_wait();
   // after a lost copy has been flagged, decode calls write nothing (the
   // partials were not written either); uniform for the CTA
   if (*reinterpret_cast<volatile unsigned int*>(&g_device_status) & kDevWaitTimeout) return;
-  const int sh = blockIdx.x;
-  combine_row(p.part_m + (size_t)sh * p.num_splits, p.part_l + (size_t)sh * p.num_splits,
-              p.part_out + (size_t)sh * p.num_splits * p.head_dim, p.num_splits, p.head_dim,
-              p.out + (size_t)sh * p.head_dim, s_w, s_red);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * kCombineWarps + warp;
+  if (row >= p.num_rows) return;
+  const int s = row / p.num_heads;
+  const int chunk = max(1, *reinterpret_cast<const volatile int*>(p.split_header));
+  int L = __ldg(p.context_lens + s);
+  L = L < 0 ? 0 : (L > p.cap_tokens ? p.cap_tokens : L);
+  const int nb = (L + p.block_size - 1) / p.block_size;
+  const int n = min(p.num_splits, (nb + chunk - 1) / chunk);
+  __half* out_row = p.out + (size_t)row * D;
+  if (n == 1) return;
+  if (n == 0) {
+    constexpr int E = D / 32;
+#pragma unroll
+    for (int e = 0; e < E; ++e) out_row[lane * E + e] = __float2half_rn(0.f);
+    return;
+  }
+  merge_row_warp<D>(p.part_m + (size_t)row * p.num_splits, p.part_l + (size_t)row * p.num_splits,
+                    p.part_out + (size_t)row * p.num_splits * D, n, out_row, s_w[warp]);
 }
 
-// Varlen split-K: one CTA per (query token, head).  The token's sequence is
-// found by binary search in cu_seqlens_q; phase 1 wrote every split of every
-// query it covered (max -inf and sum 0 where the split holds none of the
-// query's positions).  Rows phase 1 skipped (bad query ranges, queries past
-// the grid; both flagged there) are written as zeros.
+// Varlen split-K: one warp per (query token, head) row.  The token's
+// sequence is found by binary search in cu_seqlens_q; phase 1 wrote every
+// split of every query it covered (max -inf and sum 0 where the split holds
+// none of the query's positions).  Rows phase 1 skipped (bad query ranges,
+// queries past the grid; both flagged there) are written as zeros.
 struct VarlenCombineParams {
   const float* part_out;
   const float* part_m;
@@ -2000,19 +1591,20 @@ struct VarlenCombineParams {
   int num_seqs;
   int total_q;
   int num_heads;
-  int head_dim;
   int num_splits;
   int covered_q;  // queries per sequence the phase-1 grid covers
 };
 
-__global__ void __launch_bounds__(kCombineThreads)
+template <int D>
+__global__ void __launch_bounds__(kCombineWarps * 32)
 varlen_combine_kernel(const VarlenCombineParams p) {
-  __shared__ float s_w[PKV_MAX_SPLITS];
-  __shared__ float s_red[kCombineThreads / 32];
+  __shared__ float s_w[kCombineWarps][PKV_MAX_SPLITS];
   pdl_launch_dependents();
   pdl_wait();
   if (*reinterpret_cast<volatile unsigned int*>(&g_device_status) & kDevWaitTimeout) return;
-  const int rh = blockIdx.x;  // row * H + head
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rh = blockIdx.x * kCombineWarps + warp;  // row * H + head
+  if (rh >= p.total_q * p.num_heads) return;
   const int row = rh / p.num_heads;
   int lo = 0, hi = p.num_seqs - 1;  // last sequence whose first row is <= row
   while (lo < hi) {
@@ -2025,15 +1617,16 @@ varlen_combine_kernel(const VarlenCombineParams p) {
   const int q_begin = __ldg(p.cu_seqlens_q + lo);
   const int q_end = __ldg(p.cu_seqlens_q + lo + 1);
   const int t = row - q_begin;
-  __half* out_row = p.out + (size_t)rh * p.head_dim;
+  __half* out_row = p.out + (size_t)rh * D;
   if (q_begin < 0 || q_end < q_begin || q_end > p.total_q || t < 0 || t >= q_end - q_begin ||
       t >= p.covered_q) {
-    for (int d = threadIdx.x; d < p.head_dim; d += kCombineThreads) out_row[d] = __float2half_rn(0.f);
+    constexpr int E = D / 32;
+#pragma unroll
+    for (int e = 0; e < E; ++e) out_row[lane * E + e] = __float2half_rn(0.f);
     return;
   }
-  combine_row(p.part_m + (size_t)rh * p.num_splits, p.part_l + (size_t)rh * p.num_splits,
-              p.part_out + (size_t)rh * p.num_splits * p.head_dim, p.num_splits, p.head_dim,
-              out_row, s_w, s_red);
+  merge_row_warp<D>(p.part_m + (size_t)rh * p.num_splits, p.part_l + (size_t)rh * p.num_splits,
+                    p.part_out + (size_t)rh * p.num_splits * D, p.num_splits, out_row, s_w[warp]);
 }
 
 // Diagnostic: one warp waits on an mbarrier that nothing arrives on.  The

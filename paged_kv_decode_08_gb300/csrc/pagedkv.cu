@@ -118,9 +118,10 @@ int current_device_sms(int* sms) {
 // The pool as a 4-D tensor {64 elements, block_size rows, head_dim/64
 // halves, num_blocks*num_kv_heads tiles} (innermost first; the row stride,
 // head_dim * 2 bytes, is larger than the half stride, 128 bytes).  A box is
-// one whole tile, 64 x block_size x head_dim/64 x 1, landing as head_dim/64
-// runs of block_size 128-byte lines with the 128-byte swizzle (one request
-// per tile measured slightly faster than one per half).
+// 16 rows of one tile, 64 x 16 x head_dim/64 x 1 (the whole tile at block
+// size 16, either half at 32, chosen by the row coordinate), landing as
+// head_dim/64 runs of 16 128-byte lines with the 128-byte swizzle (one
+// request per 16 rows measured slightly faster than one per 64-element half).
 pkv_status encode_cache_map(CUtensorMap* map, const void* base, int num_blocks, int num_kv_heads,
                             int block_size, int head_dim) {
   auto encode = tensor_map_encoder();
@@ -129,7 +130,8 @@ pkv_status encode_cache_map(CUtensorMap* map, const void* base, int num_blocks, 
                               (cuuint64_t)num_blocks * (cuuint64_t)num_kv_heads};
   const cuuint64_t strides[3] = {(cuuint64_t)head_dim * 2, 128,
                                  (cuuint64_t)block_size * head_dim * 2};
-  const cuuint32_t box[4] = {64, (cuuint32_t)block_size, (cuuint32_t)(head_dim / 64), 1};
+  const cuuint32_t box[4] = {64, kSubtile ? 16u : (cuuint32_t)block_size,
+                             (cuuint32_t)(head_dim / 64), 1};
   const cuuint32_t estride[4] = {1, 1, 1, 1};
   const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void*>(base), dims,
                             strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -262,10 +264,12 @@ pkv_status validate_decode(const DecodeArgs& a) {
   return PKV_OK;
 }
 
-template <int D, int BS>
+// Warps and ring stages for staging tiles of TR rows (16 for blocked pools,
+// the block size for vLLM-layout pools).
+template <int D, int TR>
 struct Tuning {
   static constexpr int W = PKV_DECODE_WARPS;
-  static constexpr int kStage = 2 * BS * D * 2;
+  static constexpr int kStage = 2 * TR * D * 2;
   static constexpr int P = (PKV_DECODE_RING_KB * 1024) / (W * kStage) > 0
                                ? (PKV_DECODE_RING_KB * 1024) / (W * kStage)
                                : 1;
@@ -274,9 +278,10 @@ struct Tuning {
 template <int D, int BS, bool SPLIT, bool FUSE, bool VLLM, bool QKV = false>
 pkv_status launch_decode(const DecodeArgs& a, const DecodeParams& prm, cudaStream_t stream,
                          int grid) {
-  constexpr int W = Tuning<D, BS>::W;
-  constexpr int P = Tuning<D, BS>::P;
-  using Shape = DecodeShape<D, BS, W, P>;
+  constexpr int TR = (VLLM || !kSubtile) ? BS : 16;
+  constexpr int W = Tuning<D, TR>::W;
+  constexpr int P = Tuning<D, TR>::P;
+  using Shape = DecodeShape<D, TR, W, P>;
   auto kernel = paged_decode_kernel<D, BS, W, P, SPLIT, FUSE, VLLM, QKV>;
 
   static std::atomic<unsigned long long> attr_set{0};
@@ -342,87 +347,6 @@ pkv_status dispatch_decode(const DecodeArgs& a, const DecodeParams& prm, cudaStr
                        : dispatch_decode_f<SPLIT, false, false>(a, prm, stream, grid);
 }
 
-size_t balanced_scratch_bytes(int head_dim) {
-  return ((size_t)PKV_BALANCED_MAX_CTAS * 2 * kRecHeads * (head_dim + 2) * sizeof(float) + 255) &
-         ~size_t(255);
-}
-
-template <int D, int BS>
-pkv_status launch_balanced(const DecodeArgs& a, float* records, cudaStream_t stream) {
-  constexpr int W = Tuning<D, BS>::W;
-  constexpr int P = Tuning<D, BS>::P;
-  using Shape = DecodeShape<D, BS, W, P>;
-  auto kernel = paged_decode_balanced_kernel<D, BS, W, P>;
-  const int G = a.num_heads / a.num_kv_heads;
-  const int smem = Shape::kSmemBytes + W * (16 + G * D) * (int)sizeof(float);
-  const int smem_max = Shape::kSmemBytes + W * (16 + 8 * D) * (int)sizeof(float);
-
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  // per device: attribute set once; occupancy per group size
-  static std::atomic<int> occ_cache[64][9];
-  static std::atomic<unsigned long long> attr_set{0};
-  const unsigned long long bit = 1ull << (dev & 63);
-  if (!(attr_set.load(std::memory_order_relaxed) & bit)) {
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(balanced)");
-    attr_set.fetch_or(bit, std::memory_order_relaxed);
-  }
-  int occ = (dev >= 0 && dev < 64) ? occ_cache[dev][G].load(std::memory_order_relaxed) : 0;
-  if (occ <= 0) {
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, W * 32, smem);
-    if (e != cudaSuccess || occ <= 0) return cuda_fail(e, "occupancy of the balanced kernel");
-    if (dev >= 0 && dev < 64) occ_cache[dev][G].store(occ, std::memory_order_relaxed);
-  }
-  int sms = 0;
-  if (current_device_sms(&sms) != 0) return fail(PKV_ERR_CUDA, "cannot query the SM count");
-  // N = M * Hkv: each unit range is taken by one CTA per KV head
-  int N = sms * occ;
-  if (N > PKV_BALANCED_MAX_CTAS) N = PKV_BALANCED_MAX_CTAS;
-  N = (N / a.num_kv_heads) * a.num_kv_heads;
-  if (N < a.num_kv_heads) N = a.num_kv_heads;
-  if (N > PKV_BALANCED_MAX_CTAS)
-    return fail(PKV_ERR_UNSUPPORTED, "the balanced schedule supports at most %d kv heads",
-                PKV_BALANCED_MAX_CTAS);
-
-  CUtensorMap kmap, vmap;
-  pkv_status st = make_cache_map(&kmap, a.k_cache, a.num_blocks, a.num_kv_heads, BS, D);
-  if (st != PKV_OK) return st;
-  st = make_cache_map(&vmap, a.v_cache, a.num_blocks, a.num_kv_heads, BS, D);
-  if (st != PKV_OK) return st;
-
-  BalancedParams bp{};
-  bp.q = static_cast<const __half*>(a.q);
-  bp.block_tables = a.block_tables;
-  bp.context_lens = a.context_lens;
-  bp.out = static_cast<__half*>(a.out);
-  bp.records = records;
-  bp.num_seqs = a.num_seqs;
-  bp.num_heads = a.num_heads;
-  bp.num_kv_heads = a.num_kv_heads;
-  bp.group = G;
-  bp.max_blocks_per_seq = a.max_blocks_per_seq;
-  bp.num_blocks = a.num_blocks;
-  bp.num_ctas = N;
-  bp.scale_log2 = a.scale * 1.4426950408889634f;
-  e = launch_pdl(kernel, N, W * 32, smem, stream, kmap, vmap, bp);
-  if (e != cudaSuccess) return cuda_fail(e, "balanced decode launch");
-  const long long grid2 = (long long)a.num_seqs * a.num_heads;
-  if (grid2 >= (1ll << 31)) return fail(PKV_ERR_INVALID_ARG, "grid too large");
-  e = launch_pdl(balanced_combine_kernel<D, BS>, (int)grid2, 128, 0, stream, bp);
-  if (e != cudaSuccess) return cuda_fail(e, "balanced combine launch");
-  return PKV_OK;
-}
-
-pkv_status dispatch_balanced(const DecodeArgs& a, float* records, cudaStream_t stream) {
-  if (a.head_dim == 128 && a.block_size == 16) return launch_balanced<128, 16>(a, records, stream);
-  if (a.head_dim == 128 && a.block_size == 32) return launch_balanced<128, 32>(a, records, stream);
-  if (a.head_dim == 64 && a.block_size == 16) return launch_balanced<64, 16>(a, records, stream);
-  if (a.head_dim == 64 && a.block_size == 32) return launch_balanced<64, 32>(a, records, stream);
-  return fail(PKV_ERR_UNSUPPORTED, "head_dim %d / block_size %d", a.head_dim, a.block_size);
-}
-
 DecodeParams base_params(const DecodeArgs& a) {
   DecodeParams p{};
   p.q = static_cast<const __half*>(a.q);
@@ -445,9 +369,10 @@ DecodeParams base_params(const DecodeArgs& a) {
 template <int D, int BS, int NT, bool VLLM, bool SPLIT>
 pkv_status launch_varlen(const DecodeArgs& a, const VarlenParams& vp, cudaStream_t stream,
                          int grid) {
-  constexpr int W = Tuning<D, BS>::W;
-  constexpr int P = Tuning<D, BS>::P;
-  using Shape = DecodeShape<D, BS, W, P>;
+  constexpr int TR = (VLLM || !kSubtile) ? BS : 16;
+  constexpr int W = Tuning<D, TR>::W;
+  constexpr int P = Tuning<D, TR>::P;
+  using Shape = DecodeShape<D, TR, W, P>;
   auto kernel = paged_varlen_kernel<D, BS, W, P, NT, VLLM, SPLIT>;
   static std::atomic<unsigned long long> attr_set{0};
   int dev = 0;
@@ -583,6 +508,39 @@ pkv_status append_impl(const void* k, const void* v, const int32_t* slot_mapping
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Split-K scratch: a 256-byte header (the chunk size phase 1 used, for the
+// combine), then f32 part_out [rows][D], part_m [rows], part_l [rows] with
+// rows = (num_seqs or total_q) * num_heads * S, each 256-byte aligned.
+constexpr size_t kScratchHeaderBytes = 256;
+
+struct SplitScratch {
+  int* header;
+  float* part_out;
+  float* part_m;
+  float* part_l;
+};
+
+SplitScratch carve_scratch(void* scratch, size_t rows, int head_dim) {
+  uint8_t* b = static_cast<uint8_t*>(scratch);
+  SplitScratch sc;
+  sc.header = reinterpret_cast<int*>(b);
+  b += kScratchHeaderBytes;
+  sc.part_out = reinterpret_cast<float*>(b);
+  b += align256(rows * head_dim * sizeof(float));
+  sc.part_m = reinterpret_cast<float*>(b);
+  b += align256(rows * sizeof(float));
+  sc.part_l = reinterpret_cast<float*>(b);
+  return sc;
+}
+
+// The split-K combine for head_dim D (one warp per output row).
+template <typename Params>
+cudaError_t launch_combine(void (*k64)(Params), void (*k128)(Params), int head_dim,
+                           long long rows, cudaStream_t cs, const Params& cp) {
+  const long long grid = (rows + kCombineWarps - 1) / kCombineWarps;
+  return launch_pdl(head_dim == 128 ? k128 : k64, (int)grid, kCombineWarps * 32, 0, cs, cp);
+}
+
 }  // namespace
 }  // namespace pkv
 
@@ -605,10 +563,10 @@ const char* pkv_last_error(void) { return t_last_error; }
 
 size_t pkv_splitk_scratch_bytes(int32_t num_seqs, int32_t num_heads, int32_t head_dim,
                                 int32_t num_splits) {
-  if (num_splits == PKV_SPLITS_BALANCED) return head_dim > 0 ? balanced_scratch_bytes(head_dim) : 0;
   if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || num_splits <= 1) return 0;
   const size_t rows = (size_t)num_seqs * num_heads * num_splits;
-  return align256(rows * head_dim * sizeof(float)) + 2 * align256(rows * sizeof(float));
+  return kScratchHeaderBytes + align256(rows * head_dim * sizeof(float)) +
+         2 * align256(rows * sizeof(float));
 }
 
 int32_t pkv_pick_num_splits(int32_t num_seqs, int32_t num_kv_heads, int32_t max_context_len,
@@ -688,13 +646,13 @@ namespace pkv {
 namespace {
 
 // The split count a decode call launches for `num_splits` (0 = the
-// heuristic for the current GPU): 1 (single pass), 2..PKV_MAX_SPLITS, or
-// PKV_SPLITS_BALANCED.  More splits than table blocks cannot all hold work,
-// so the count is capped at max_blocks_per_seq.
+// heuristic for the current GPU): 1 (single pass) or 2..PKV_MAX_SPLITS.
+// More splits than table blocks cannot all hold work, so the count is capped
+// at max_blocks_per_seq.
 pkv_status resolve_decode_splits(int num_seqs, int num_kv_heads, int max_blocks_per_seq,
                                  int block_size, int num_splits, int* S_out) {
-  if (num_splits < PKV_SPLITS_BALANCED || num_splits > PKV_MAX_SPLITS)
-    return fail(PKV_ERR_INVALID_ARG, "num_splits %d outside -1..%d", num_splits, PKV_MAX_SPLITS);
+  if (num_splits < 0 || num_splits > PKV_MAX_SPLITS)
+    return fail(PKV_ERR_INVALID_ARG, "num_splits %d outside 0..%d", num_splits, PKV_MAX_SPLITS);
   int S = num_splits;
   if (S == 0) {
     int sms = 0;
@@ -702,8 +660,7 @@ pkv_status resolve_decode_splits(int num_seqs, int num_kv_heads, int max_blocks_
     S = pkv_pick_num_splits(num_seqs, num_kv_heads, max_blocks_per_seq * block_size, block_size,
                             sms);
   }
-  if (S != PKV_SPLITS_BALANCED) S = S < 1 ? 1 : (S > max_blocks_per_seq ? max_blocks_per_seq : S);
-  *S_out = S;
+  *S_out = S < 1 ? 1 : (S > max_blocks_per_seq ? max_blocks_per_seq : S);
   return PKV_OK;
 }
 
@@ -731,29 +688,13 @@ pkv_status decode_impl(const DecodeArgs& a, int num_splits, void* scratch, size_
   const int num_seqs = a.num_seqs, num_kv_heads = a.num_kv_heads, num_heads = a.num_heads;
   const int max_blocks_per_seq = a.max_blocks_per_seq, block_size = a.block_size;
   const int head_dim = a.head_dim;
-  if (num_splits < PKV_SPLITS_BALANCED || num_splits > PKV_MAX_SPLITS)
-    return fail(PKV_ERR_INVALID_ARG, "num_splits %d outside -1..%d", num_splits, PKV_MAX_SPLITS);
+  if (num_splits < 0 || num_splits > PKV_MAX_SPLITS)
+    return fail(PKV_ERR_INVALID_ARG, "num_splits %d outside 0..%d", num_splits, PKV_MAX_SPLITS);
   if (num_seqs == 0) return PKV_OK;
 
   int S = 0;
   st = resolve_decode_splits(num_seqs, num_kv_heads, max_blocks_per_seq, block_size, num_splits, &S);
   if (st != PKV_OK) return st;
-  if (S == PKV_SPLITS_BALANCED) {
-    if (a.vllm) return fail(PKV_ERR_UNSUPPORTED, "no balanced schedule on the vLLM layout");
-    const size_t need_b = balanced_scratch_bytes(head_dim);
-    if (!scratch || scratch_bytes < need_b)
-      return fail(PKV_ERR_SCRATCH_TOO_SMALL, "the balanced schedule needs %zu scratch bytes, got %zu",
-                  need_b, scratch ? scratch_bytes : (size_t)0);
-    if (!aligned(scratch, 16)) return fail(PKV_ERR_INVALID_ARG, "scratch must be 16-byte aligned");
-    if (fuse && fuse->qkv)
-      return fail(PKV_ERR_UNSUPPORTED, "no fused QKV step on the balanced schedule");
-    if (fuse) {  // the balanced kernel does not fuse: append first, in stream order
-      st = pkv_append(fuse->k_new, fuse->v_new, fuse->slots, num_seqs, fuse->k_cache,
-                      fuse->v_cache, a.num_blocks, block_size, num_kv_heads, head_dim, cs);
-      if (st != PKV_OK) return st;
-    }
-    return dispatch_balanced(a, static_cast<float*>(scratch), cs);
-  }
   const int S_eff = S;
   if (S_eff <= 1) return single_pass(a, cs, fuse);
 
@@ -766,7 +707,7 @@ pkv_status decode_impl(const DecodeArgs& a, int num_splits, void* scratch, size_
   if (grid1 >= (1ll << 31)) return fail(PKV_ERR_INVALID_ARG, "grid too large");
 
   const size_t rows = (size_t)num_seqs * num_heads * S_eff;
-  uint8_t* base = static_cast<uint8_t*>(scratch);
+  const SplitScratch sc = carve_scratch(scratch, rows, head_dim);
   DecodeParams prm = base_params(a);
   apply_fuse(prm, fuse);
   prm.num_splits = S_eff;
@@ -774,22 +715,27 @@ pkv_status decode_impl(const DecodeArgs& a, int num_splits, void* scratch, size_
   // longest context into exactly S chunks
   prm.min_chunk_blocks = num_splits == 0 ? (kMinSplitTokens + block_size - 1) / block_size : 1;
   prm.chunk_hint = (max_blocks_per_seq + S_eff - 1) / S_eff;
-  prm.part_out = reinterpret_cast<float*>(base);
-  prm.part_m = reinterpret_cast<float*>(base + align256(rows * head_dim * sizeof(float)));
-  prm.part_l = reinterpret_cast<float*>(base + align256(rows * head_dim * sizeof(float)) +
-                                        align256(rows * sizeof(float)));
+  prm.split_header = sc.header;
+  prm.part_out = sc.part_out;
+  prm.part_m = sc.part_m;
+  prm.part_l = sc.part_l;
   st = dispatch_decode<true>(a, prm, cs, (int)grid1);
   if (st != PKV_OK) return st;
 
   CombineParams cp{};
-  cp.part_out = prm.part_out;
-  cp.part_m = prm.part_m;
-  cp.part_l = prm.part_l;
+  cp.part_out = sc.part_out;
+  cp.part_m = sc.part_m;
+  cp.part_l = sc.part_l;
+  cp.context_lens = a.context_lens;
+  cp.split_header = sc.header;
   cp.out = static_cast<__half*>(a.out);
+  cp.num_rows = num_seqs * num_heads;
   cp.num_heads = num_heads;
-  cp.head_dim = head_dim;
   cp.num_splits = S_eff;
-  const cudaError_t e = launch_pdl(splitk_combine_kernel, num_seqs * num_heads, 128, 0, cs, cp);
+  cp.block_size = block_size;
+  cp.cap_tokens = max_blocks_per_seq * block_size;
+  const cudaError_t e = launch_combine(splitk_combine_kernel<64>, splitk_combine_kernel<128>,
+                                       head_dim, (long long)num_seqs * num_heads, cs, cp);
   if (e != cudaSuccess) return cuda_fail(e, "split-K combine launch");
   return PKV_OK;
 }
@@ -857,13 +803,12 @@ pkv_status varlen_impl(const void* q, const void* k_cache, const void* v_cache,
   if (grid1 >= (1ll << 31) || grid2 >= (1ll << 31))
     return fail(PKV_ERR_INVALID_ARG, "grid too large");
   const size_t rows = (size_t)total_q * num_heads * S_eff;
-  uint8_t* base = static_cast<uint8_t*>(scratch);
+  const SplitScratch sc = carve_scratch(scratch, rows, head_dim);
   vp.num_splits = S_eff;
   vp.min_chunk_blocks = num_splits == 0 ? (kMinSplitTokens + block_size - 1) / block_size : 1;
-  vp.part_out = reinterpret_cast<float*>(base);
-  vp.part_m = reinterpret_cast<float*>(base + align256(rows * head_dim * sizeof(float)));
-  vp.part_l = reinterpret_cast<float*>(base + align256(rows * head_dim * sizeof(float)) +
-                                      align256(rows * sizeof(float)));
+  vp.part_out = sc.part_out;
+  vp.part_m = sc.part_m;
+  vp.part_l = sc.part_l;
   st = dispatch_varlen<true>(a, vp, cs, (int)grid1, NT, vllm);
   if (st != PKV_OK) return st;
 
@@ -876,10 +821,10 @@ pkv_status varlen_impl(const void* q, const void* k_cache, const void* v_cache,
   cp.num_seqs = num_seqs;
   cp.total_q = total_q;
   cp.num_heads = num_heads;
-  cp.head_dim = head_dim;
   cp.num_splits = S_eff;
   cp.covered_q = chunks * qc;
-  const cudaError_t e = launch_pdl(varlen_combine_kernel, (int)grid2, kCombineThreads, 0, cs, cp);
+  const cudaError_t e = launch_combine(varlen_combine_kernel<64>, varlen_combine_kernel<128>,
+                                       head_dim, grid2, cs, cp);
   if (e != cudaSuccess) return cuda_fail(e, "varlen split-K combine launch");
   return PKV_OK;
 }
@@ -917,8 +862,6 @@ pkv_status pkv_decode_vllm_layout(const void* q, const void* k_cache, const void
   a.vllm = true;
   pkv_status st = validate_decode(a);
   if (st != PKV_OK) return st;
-  if (num_splits == PKV_SPLITS_BALANCED)
-    return fail(PKV_ERR_UNSUPPORTED, "no balanced schedule on the vLLM layout");
   return decode_impl(a, num_splits, scratch, scratch_bytes, static_cast<cudaStream_t>(stream),
                      nullptr);
 }
@@ -1167,8 +1110,6 @@ pkv_status pkv_qkv_norm_rope_append_decode(
     return fail(PKV_ERR_INVALID_ARG, "misaligned pointer");
   if ((long long)num_seqs * (num_heads + 2 * num_kv_heads) * head_dim >= (1ll << 40))
     return fail(PKV_ERR_INVALID_ARG, "qkv too large");
-  if (num_splits == PKV_SPLITS_BALANCED)
-    return fail(PKV_ERR_UNSUPPORTED, "no fused QKV step on the balanced schedule");
   FuseArgs f;
   f.k_cache = k_cache;
   f.v_cache = v_cache;
@@ -1255,8 +1196,8 @@ extern "C" pkv_status pkv_decode_splitk_noalloc(
                      head_dim, block_size, out};
   pkv_status st = validate_decode(a);
   if (st != PKV_OK) return st;
-  if (num_splits < PKV_SPLITS_BALANCED || num_splits > PKV_MAX_SPLITS)
-    return fail(PKV_ERR_INVALID_ARG, "num_splits %d outside -1..%d", num_splits, PKV_MAX_SPLITS);
+  if (num_splits < 0 || num_splits > PKV_MAX_SPLITS)
+    return fail(PKV_ERR_INVALID_ARG, "num_splits %d outside 0..%d", num_splits, PKV_MAX_SPLITS);
   if (num_seqs == 0) return PKV_OK;
 
   // The split count pkv_decode_splitk will use, and the scratch it needs.

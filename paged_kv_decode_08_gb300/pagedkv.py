@@ -30,8 +30,6 @@ PKV_DEV_BAD_CONTEXT_LEN = 0x4
 PKV_DEV_WAIT_TIMEOUT = 0x8
 
 PKV_MAX_SPLITS = 128
-PKV_SPLITS_BALANCED = -1
-PKV_BALANCED_MAX_CTAS = 768
 PKV_NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
 
 

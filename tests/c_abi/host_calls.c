@@ -24,7 +24,6 @@ int main(void) {
   /* scratch sizes */
   CHECK(pkv_splitk_scratch_bytes(4, 32, 128, 1) == 0);
   CHECK(pkv_splitk_scratch_bytes(4, 32, 128, 16) >= (size_t)4 * 32 * 16 * 130 * 4);
-  CHECK(pkv_splitk_scratch_bytes(4, 32, 128, PKV_SPLITS_BALANCED) > 0);
   /* split plans: what the decode calls launch and the scratch they need */
   {
     int32_t S = 0;

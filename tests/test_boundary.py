@@ -55,21 +55,14 @@ def test_status_strings(pk):
     assert pk.status_string(-3).startswith("split-K scratch")
 
 
-def test_balanced_scratch_bytes(pk):
-    for D in (64, 128):
-        n = pk.pkv_splitk_scratch_bytes(4, 32, D, -1)
-        assert n >= pk.PKV_BALANCED_MAX_CTAS * 2 * 8 * (D + 2) * 4
-        assert n == pk.pkv_splitk_scratch_bytes(256, 28, D, -1)  # independent of B and H
-    assert pk.pkv_splitk_scratch_bytes(4, 32, 128, -1) <= pk.PKV_NOALLOC_SCRATCH_BYTES
-
-
 def test_scratch_bytes(pk):
     assert pk.pkv_splitk_scratch_bytes(4, 32, 128, 1) == 0
     assert pk.pkv_splitk_scratch_bytes(0, 32, 128, 4) == 0
     n = pk.pkv_splitk_scratch_bytes(4, 32, 128, 64)
     rows = 4 * 32 * 64
     a = lambda x: (x + 255) // 256 * 256  # noqa: E731
-    assert n == a(rows * 128 * 4) + 2 * a(rows * 4)
+    # a 256-byte header, then f32 partial outputs, maxima and sums
+    assert n == 256 + a(rows * 128 * 4) + 2 * a(rows * 4)
 
 
 @pytest.mark.parametrize("args,expect", [
@@ -89,16 +82,14 @@ def test_pick_num_splits_table(pk, args, expect):
 
 def test_decode_splitk_plan(pk):
     """The plan the decode calls follow: forced counts capped at the table
-    width, single pass without scratch, the balanced schedule's records."""
+    width, single pass without scratch."""
     assert pk.pkv_decode_splitk_plan(4, 32, 8, 128, 8192, 16, 16) == (
         16, pk.pkv_splitk_scratch_bytes(4, 32, 128, 16))
     assert pk.pkv_decode_splitk_plan(3, 8, 2, 64, 7, 16, 64) == (
         7, pk.pkv_splitk_scratch_bytes(3, 8, 64, 7))
     assert pk.pkv_decode_splitk_plan(4, 32, 8, 128, 8192, 16, 1) == (1, 0)
     assert pk.pkv_decode_splitk_plan(0, 32, 8, 128, 8192, 16, 16) == (16, 0)
-    assert pk.pkv_decode_splitk_plan(4, 32, 8, 128, 8192, 16, -1) == (
-        -1, pk.pkv_splitk_scratch_bytes(4, 32, 128, -1))
-    for bad in (dict(num_splits=129), dict(num_splits=-2), dict(num_heads=30),
+    for bad in (dict(num_splits=129), dict(num_splits=-1), dict(num_heads=30),
                 dict(max_blocks_per_seq=0)):
         a = dict(num_seqs=4, num_heads=32, num_kv_heads=8, head_dim=128,
                  max_blocks_per_seq=8192, block_size=16, num_splits=4)
@@ -190,7 +181,7 @@ def test_splitk_rejects_bad_splits_and_small_scratch(pk):
             a["H"], a["Hkv"], a["D"], a["bs"], a["out"]]
     assert f(*args, -2, F16, 1 << 30, None) == -1
     assert f(*args, 129, F16, 1 << 30, None) == -1
-    assert f(*args, -1, F16, pk.pkv_splitk_scratch_bytes(4, 32, 128, -1) - 1, None) == -3
+    assert f(*args, -1, F16, 1 << 30, None) == -1
     assert f(*args, 16, None, 0, None) == -3
     need = pk.pkv_splitk_scratch_bytes(4, 32, 128, 16)
     assert f(*args, 16, F16, need - 1, None) == -3
@@ -251,7 +242,7 @@ def test_varlen_rejects_bad_arguments(pk):
 def test_vllm_layout_calls_reject_bad_arguments(pk):
     f = pk.lib.pkv_decode_vllm_layout
     ok = [F16, F16, F16, F16, F16, 2, 3, 8, 0.125, 4, 2, 64, 16, F16]
-    assert f(*ok, -1, F16, 1 << 30, None) == -2   # no balanced schedule on this layout
+    assert f(*ok, -1, F16, 1 << 30, None) == -1   # no negative split counts
     assert f(*ok, -2, F16, 1 << 30, None) == -1
     assert f(*ok, 4, None, 0, None) == -3
     bad = list(ok)
@@ -387,6 +378,6 @@ def test_qkv_norm_rope_append_decode_rejects_bad_arguments(pk):
     assert call(kc=F16 + 4) == -1             # tensor copies need 16-byte pools
     assert call(qw=F16 + 1) == -1
     assert call(cos=F16 + 2) == -1
-    assert call(S=-1) == -2                    # no balanced schedule
+    assert call(S=-1) == -1                    # no negative split counts
     assert call(S=pk.PKV_MAX_SPLITS + 1) == -1
     assert call(B=0) == 0                      # no sequences: nothing launched

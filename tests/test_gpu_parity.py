@@ -108,10 +108,10 @@ def test_append_skips_padding_and_flags_bad_slots(pk, cuda_device):
 # ---------------------------------------------------------------------------
 
 @pytest.mark.parametrize("name,splits", [
-    ("tiny", [0, 2, 3, -1]),
-    ("llama8b", [0, 2, 4, 16, -1]),
-    ("long", [0, 4, 16, 64, -1]),
-    ("ragged", [0, 3, 8, -1]),
+    ("tiny", [0, 2, 3]),
+    ("llama8b", [0, 2, 4, 16]),
+    ("long", [0, 4, 16, 64]),
+    ("ragged", [0, 3, 8, 32]),
 ])
 def test_decode_matches_oracle(pk, cuda_device, name, splits):
     w, ref = workload(name)
@@ -142,10 +142,11 @@ def test_overprovisioned_tables_split_the_real_contexts(pk, cuda_device, name):
                                d["context_lens"], w.scale, num_splits=S, scratch=scratch)
     torch.cuda.synchronize()
     assert_attention_close(to_np(out), ref, f"{name} x4 tables, S=4")
-    # scratch layout: f32 part_out [B][H][S][D], then part_m [B][H][S] (256-byte aligned)
+    # scratch layout: a 256-byte header, f32 part_out [B][H][S][D], then
+    # part_m [B][H][S] (each 256-byte aligned)
     a256 = lambda x: (x + 255) // 256 * 256  # noqa: E731
     rows = w.num_seqs * w.num_heads * S
-    part_m = scratch[a256(rows * w.head_dim * 4):][:rows * 4].view(torch.float32)
+    part_m = scratch[256 + a256(rows * w.head_dim * 4):][:rows * 4].view(torch.float32)
     part_m = part_m.view(w.num_seqs, w.num_heads, S).cpu().numpy()
     longest = int(np.argmax(w.context_lens))
     assert np.all(np.isfinite(part_m[longest, :, S - 1])), "last split of the longest sequence"
@@ -190,7 +191,7 @@ def test_context_len_one_is_exact(pk, cuda_device):
     w = W.small_random(41, num_seqs=6, num_heads=14, num_kv_heads=2, head_dim=128,
                        block_size=32, lens=[1, 1, 33, 1, 64, 1])
     d = appended_device(pk, w, cuda_device)
-    for S in (1, 2, -1):
+    for S in (1, 2, 3):
         out = pk.pkv_decode_splitk(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
                                    d["context_lens"], w.scale, num_splits=S).cpu().numpy()
         for s in range(w.num_seqs):
@@ -210,7 +211,7 @@ def test_ragged_small_shapes(pk, cuda_device, D, bs, G):
     kc, vc = W.host_pool(w)
     ref = oracle.decode(w.q, kc, vc, w.block_tables, w.context_lens, w.scale)
     d = appended_device(pk, w, cuda_device)
-    for label, got in decode_all(pk, w, d, [0, 2, 5, 128, -1]).items():
+    for label, got in decode_all(pk, w, d, [0, 2, 5, 128]).items():
         assert_attention_close(got, ref, f"D{D} bs{bs} G{G} {label}")
 
 
@@ -223,7 +224,7 @@ def test_empty_context_gives_zeros(pk, cuda_device):
     lens[1] = 0
     d["context_lens"] = torch.from_numpy(lens).to(cuda_device)
     ref = oracle.decode(w.q, kc, vc, w.block_tables, lens, w.scale)
-    for label, got in decode_all(pk, w, d, [2, -1]).items():
+    for label, got in decode_all(pk, w, d, [2, 3]).items():
         assert np.all(got[1] == 0.0), label
         assert_attention_close(got, ref, label)
 
@@ -253,7 +254,7 @@ def test_bad_block_id_is_skipped_and_flagged(pk, cuda_device):
     tables = w.block_tables.copy()
     tables[0, 1] = w.num_blocks + 5  # out of range: tokens 16..31 of sequence 0 are skipped
     d["block_tables"] = torch.from_numpy(tables).to(cuda_device)
-    for S in (1, 3, -1):
+    for S in (1, 3, 2):
         out = to_np(pk.pkv_decode_splitk(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
                                          d["context_lens"], w.scale, num_splits=S))
         assert pk.pkv_read_device_status() & pk.PKV_DEV_BAD_BLOCK_ID
@@ -323,6 +324,41 @@ def test_append_decode_loop(pk, cuda_device):
     assert pk.pkv_read_device_status() == 0
 
 
+def test_splitk_on_many_short_and_empty_sequences(pk, cuda_device):
+    """Hundreds of sequences of 0-70 tokens: most fit one chunk (phase 1
+    writes their output), a few span several, and empty ones must come out as
+    zeros from the combine."""
+    rng = np.random.default_rng(77)
+    lens = [int(x) for x in rng.integers(0, 70, size=300)]
+    lens[:5] = [0, 1, 0, 70, 2]
+    w = W.small_random(1077, num_seqs=len(lens), num_heads=8, num_kv_heads=2, head_dim=64,
+                       block_size=16, lens=[max(L, 1) for L in lens])
+    kc, vc = W.host_pool(w)
+    real = np.array(lens, np.int32)
+    ref = oracle.decode(w.q, kc, vc, w.block_tables, real, w.scale)
+    d = W.to_device(w, cuda_device)
+    d["context_lens"] = torch.from_numpy(real).to(cuda_device)
+    for S in (0, 2, 5):
+        out = torch.full_like(d["q"], float("nan"))
+        got = to_np(pk.pkv_decode_splitk(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                                         d["context_lens"], w.scale, num_splits=S, out=out))
+        assert_attention_close(got, ref, f"many short, S={S}")
+        assert np.all(got[real == 0] == 0.0)
+    assert pk.pkv_read_device_status() == 0
+
+
+def test_splitk_with_every_length_zero(pk, cuda_device):
+    w = W.small_random(1088, num_seqs=3, num_heads=4, num_kv_heads=2, head_dim=128,
+                       block_size=32, lens=[5, 6, 7])
+    d = W.to_device(w, cuda_device)
+    d["context_lens"] = torch.zeros(3, dtype=torch.int32, device=cuda_device)
+    for S in (1, 2):
+        out = torch.full_like(d["q"], float("nan"))
+        pk.pkv_decode_splitk(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                             d["context_lens"], w.scale, num_splits=S, out=out)
+        assert torch.count_nonzero(out).item() == 0
+
+
 # ---------------------------------------------------------------------------
 # graphs and streams
 # ---------------------------------------------------------------------------
@@ -356,44 +392,13 @@ def test_append_and_decode_replay_from_a_cuda_graph(pk, cuda_device):
     assert_attention_close(to_np(out), ref, "graph replay")
 
 
-def test_balanced_schedule_on_many_short_and_empty_sequences(pk, cuda_device):
-    """Hundreds of sequences of 0-70 tokens: most CTAs hold many whole
-    segments and some hold cut ones; empty sequences must come out as zeros."""
-    rng = np.random.default_rng(77)
-    lens = [int(x) for x in rng.integers(0, 70, size=300)]
-    lens[:5] = [0, 1, 0, 70, 2]
-    w = W.small_random(1077, num_seqs=len(lens), num_heads=8, num_kv_heads=2, head_dim=64,
-                       block_size=16, lens=[max(L, 1) for L in lens])
-    kc, vc = W.host_pool(w)
-    real = np.array(lens, np.int32)
-    ref = oracle.decode(w.q, kc, vc, w.block_tables, real, w.scale)
-    d = W.to_device(w, cuda_device)
-    d["context_lens"] = torch.from_numpy(real).to(cuda_device)
-    out = to_np(pk.pkv_decode_splitk(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
-                                     d["context_lens"], w.scale, num_splits=-1))
-    assert_attention_close(out, ref, "balanced, many short")
-    assert np.all(out[real == 0] == 0.0)
-    assert pk.pkv_read_device_status() == 0
-
-
-def test_balanced_schedule_with_every_length_zero(pk, cuda_device):
-    w = W.small_random(1088, num_seqs=3, num_heads=4, num_kv_heads=2, head_dim=128,
-                       block_size=32, lens=[5, 6, 7])
-    d = W.to_device(w, cuda_device)
-    d["context_lens"] = torch.zeros(3, dtype=torch.int32, device=cuda_device)
-    out = torch.full_like(d["q"], float("nan"))
-    pk.pkv_decode_splitk(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
-                         d["context_lens"], w.scale, num_splits=-1, out=out)
-    assert torch.count_nonzero(out).item() == 0
-
-
 # ---------------------------------------------------------------------------
 # fused append + decode
 # ---------------------------------------------------------------------------
 
 @pytest.mark.parametrize("name,splits", [
-    ("tiny", [0, 2, -1]),
-    ("llama8b", [0, 1, 3, -1]),
+    ("tiny", [0, 2]),
+    ("llama8b", [0, 1, 3]),
     ("ragged", [0, 8]),
     ("long", [0, 1]),
 ])

@@ -11,8 +11,8 @@ The test calls it through the C ABI, one call after another on the same
 stream, and checks every output element against the float64 oracle (the
 attention tolerance of the other parity tests) and against
 ``pkv_decode_splitk`` with caller-owned scratch.  The calls cover forced
-split counts, the heuristic (0), the balanced schedule (-1) and a forced
-count above the table width (launched as max_blocks_per_seq splits); each
+split counts, the heuristic (0) and a forced count above the table width
+(launched as max_blocks_per_seq splits); each
 call has a different shape or split count from the one before, so partials
 left in the shared buffer by an earlier call would show if they were read.
 
@@ -56,7 +56,7 @@ def test_noalloc_matches_the_oracle_on_calls_in_a_row(cuda_device):
     a = _case(901, 32, 8, 128, 16, [4096, 1, 777, 2048, 3000, 16, 4095, 1500])
     b = _case(902, 28, 4, 64, 32, [100, 2000, 33, 1, 640])
     c = _case(903, 8, 2, 64, 16, [100, 37, 5])  # 7 table blocks: S = 64 runs as 7 splits
-    calls = [(a, 16), (b, 3), (a, 0), (b, -1), (c, 64), (a, 16)]
+    calls = [(a, 16), (b, 3), (a, 0), (b, 0), (c, 64), (b, 7), (a, 16)]
     for (w, ref), S in calls:
         S_run, need = pk.pkv_decode_splitk_plan(w.num_seqs, w.num_heads, w.num_kv_heads,
                                                 w.head_dim, w.max_blocks_per_seq, w.block_size,

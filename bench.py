@@ -1000,13 +1000,33 @@ def sub_record(line, name):
             "decode_tokens_per_s": line["decode_tokens_per_s"],
             "traffic": line["roofline"].get("traffic"),
             "gpu_launches": line["gpu_launches"], "steps": line["steps"],
+            "e2e": line.get("e2e"),
             "clocks": line["clocks"], "device_status_flags": line["device_status_flags"]}
+
+
+def c_driver_record(steps=200, warmup=20):
+    """The plain-C end-to-end driver (tests/c_abi/e2e_step.c) on the
+    Llama-3-8B-shaped step: host buffers, one packed copy in, the step, the
+    output copied back; reports the library's host time per call apart from
+    Python.  None when it cannot be built or run."""
+    from paged_kv_decode_08_gb300 import build
+
+    try:
+        exe = build.build_c_e2e()
+        r = subprocess.run([exe, str(steps), str(warmup)], capture_output=True, text=True,
+                           timeout=600)
+    except (RuntimeError, OSError, subprocess.TimeoutExpired) as e:
+        return {"unavailable": str(e).splitlines()[0][:200]}
+    if r.returncode != 0:
+        return {"unavailable": (r.stderr or r.stdout).strip()[:200]}
+    return json.loads(r.stdout.strip().splitlines()[-1])
 
 
 # Configurations timed beside the headline (name, rotating pool sets): the
 # Llama-3-8B step reads 174 MB, near L2's 129 MB, so its pools rotate; the
 # others read 0.8-1.3 GB per call, far above L2.
-SUB_CONFIGS = [("llama8b", N_SETS), ("ragged", 1), ("loop", None), ("tiny", N_SETS)]
+SUB_CONFIGS = [("llama8b", N_SETS, True), ("ragged", 1, False), ("loop", None, False),
+               ("tiny", N_SETS, False)]
 
 
 def run_ours(args):
@@ -1028,20 +1048,70 @@ def run_ours(args):
     torch.cuda.empty_cache()
     subs = []
     if not args.no_sub and world == 1 and name == "long":
-        for sub, sets in SUB_CONFIGS:
+        for sub, sets, e2e in SUB_CONFIGS:
             if sub == "loop":
                 r = measure_loop(args, local, world, rank)
             else:
-                r = measure_step(args, sub, dev, None, world, rank, sets, want_e2e=False,
-                                 want_cpu=False)
+                r = measure_step(args, sub, dev, None, world, rank, sets,
+                                 want_e2e=e2e and not args.no_e2e, want_cpu=False)
             torch.cuda.empty_cache()
             if r is not None:
                 subs.append(sub_record(r, sub))
     if rank == 0:
         line["sub_records"] = subs
+        if not args.no_sub and world == 1 and name == "long":
+            line["c_e2e_llama8b"] = c_driver_record()
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def run_profile(args):
+    """A few plain calls of the step (no graph, no timing) for profiler
+    captures: the workload over a compact pool (the blocks it reads,
+    re-permuted; see workloads.compact_pool) so that a capture saves and
+    restores little device memory.  `loop` runs its first steps (append of
+    142 rows, then the decode)."""
+    import torch
+
+    from paged_kv_decode_08_gb300 import pagedkv as pk
+    from paged_kv_decode_08_gb300 import workloads as W
+
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    n = args.ncu_calls
+    if args.workload == "loop":
+        loop = W.AppendDecodeLoop()
+        d0 = W.to_device(loop.initial_workload(), dev)
+        kc, vc = d0["k_cache"], d0["v_cache"]
+        for t in range(n):
+            st = loop.step(t)
+            x = {k: torch.from_numpy(getattr(st, k)).to(dev) for k in
+                 ("k_new", "v_new", "slot_mapping", "q", "block_tables", "context_lens")}
+            pk.pkv_append(x["k_new"], x["v_new"], x["slot_mapping"], kc, vc)
+            pk.pkv_decode_splitk(x["q"], kc, vc, x["block_tables"], x["context_lens"], loop.scale,
+                                 num_splits=args.splits)
+    else:
+        w = W.compact_pool(W.make(args.workload))
+        d = W.to_device(w, dev, upto_last=True)
+        k_new, v_new, slots = (torch.from_numpy(a).to(dev) for a in w.last_token_append())
+        scratch = pk.alloc_scratch(d["q"], d["k_cache"], d["block_tables"], args.splits)
+        out = torch.empty_like(d["q"])
+        for _ in range(n):
+            if args.separate:
+                pk.pkv_append(k_new, v_new, slots, d["k_cache"], d["v_cache"])
+                pk.pkv_decode_splitk(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                                     d["context_lens"], w.scale, num_splits=args.splits,
+                                     scratch=scratch, out=out)
+            else:
+                pk.pkv_append_decode(k_new, v_new, slots, d["k_cache"], d["v_cache"], d["q"],
+                                     d["block_tables"], d["context_lens"], w.scale,
+                                     num_splits=args.splits, scratch=scratch, out=out)
+    torch.cuda.synchronize()
+    flags = pk.pkv_read_device_status()
+    print(json.dumps({"profile_calls": n, "workload": args.workload, "status_flags": flags}))
+    if flags:
+        raise SystemExit(f"device status flags {flags:#x}")
 
 
 def main():
@@ -1067,6 +1137,9 @@ def main():
                          "with V [NB][Hkv][D][bs] (append and decode as two calls)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ncu-calls", type=int, default=0,
+                    help="profiling mode: run this many plain calls of the step on a compact "
+                         "pool, untimed, and exit")
     ap.add_argument("--oracle-child", choices=["baseline", "reference"], default=None,
                     help=argparse.SUPPRESS)
     ap.add_argument("--oracle-budget", type=float, default=12.0, help=argparse.SUPPRESS)
@@ -1074,6 +1147,9 @@ def main():
     if args.oracle_child:
         oracle_child_main(args.oracle_child, args.workload, args.steps, args.warmup,
                           args.oracle_budget)
+        return
+    if args.ncu_calls:
+        run_profile(args)
         return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -54,6 +54,34 @@ def build_library(force=False, verbose=False, extra=()):
     return LIB
 
 
+C_E2E_SRC = os.path.join(ROOT, "tests", "c_abi", "e2e_step.c")
+C_E2E_EXE = os.path.join(HERE, "_build", "e2e_step")
+
+
+def build_c_e2e(force=False):
+    """Compiles the plain-C end-to-end driver (tests/c_abi/e2e_step.c)
+    against libpagedkv.so and the CUDA runtime; returns the executable."""
+    lib = build_library()
+    if (not force and os.path.exists(C_E2E_EXE)
+            and os.path.getmtime(C_E2E_EXE) >= max(os.path.getmtime(C_E2E_SRC),
+                                                    os.path.getmtime(lib))):
+        return C_E2E_EXE
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        raise RuntimeError("no C compiler")
+    cuda_home = os.path.dirname(os.path.dirname(os.path.realpath(nvcc_path())))
+    os.makedirs(os.path.dirname(C_E2E_EXE), exist_ok=True)
+    cmd = [cc, "-std=c11", "-O2", "-Wall", "-Wextra", "-Werror", "-D_POSIX_C_SOURCE=199309L",
+           "-I", os.path.join(ROOT, "include"), "-I", os.path.join(cuda_home, "include"),
+           C_E2E_SRC, "-o", C_E2E_EXE, "-L", HERE, "-lpagedkv",
+           "-L", os.path.join(cuda_home, "lib64"), "-lcudart",
+           "-Wl,-rpath," + HERE, "-Wl,-rpath," + os.path.join(cuda_home, "lib64")]
+    res = subprocess.run(cmd, capture_output=True, text=True)
+    if res.returncode != 0:
+        raise RuntimeError(f"C driver build failed ({res.returncode}):\n{res.stderr}")
+    return C_E2E_EXE
+
+
 if __name__ == "__main__":
     extra = [a for a in sys.argv[1:] if a.startswith("-D")]
     if "--ptxas-v" in sys.argv:

@@ -1165,21 +1165,27 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   __syncthreads();
 
   const int G = p.group;
-  for (int idx = threadIdx.x; idx < G * D; idx += W * 32) {
-    const int h = idx / D;
-    const int d = idx - h * D;
-    float M, num, den;
-    merge_warps<W, D>(red, Shape::kRedFloats, h, d, M, num, den);
-    const size_t qh = (size_t)s * p.num_heads + (size_t)g * G + h;
-    if (SPLIT && n_pieces > 1) {
-      const size_t slot = qh * p.num_splits + piece;
+  const size_t qh0 = (size_t)s * p.num_heads + (size_t)g * G;
+  if (SPLIT && n_pieces > 1) {  // this chunk's partials, for the combine
+    for (int idx = threadIdx.x; idx < G * D; idx += W * 32) {
+      const int h = idx / D;
+      const int d = idx - h * D;
+      float M, num, den;
+      merge_warps<W, D>(red, Shape::kRedFloats, h, d, M, num, den);
+      const size_t slot = (qh0 + h) * p.num_splits + piece;
       p.part_out[slot * D + d] = num;
       if (d == 0) {
         p.part_m[slot] = M;
         p.part_l[slot] = den;
       }
-    } else {
-      p.out[qh * D + d] = __float2half_rn(den > 0.f ? num / den : 0.f);
+    }
+  } else {  // the whole context: the f16 output
+    for (int idx = threadIdx.x; idx < G * D; idx += W * 32) {
+      const int h = idx / D;
+      const int d = idx - h * D;
+      float M, num, den;
+      merge_warps<W, D>(red, Shape::kRedFloats, h, d, M, num, den);
+      p.out[(qh0 + h) * D + d] = __float2half_rn(den > 0.f ? num / den : 0.f);
     }
   }
 }
@@ -1462,27 +1468,54 @@ struct CombineParams {
 
 // Rows (output head vectors) merged per combine CTA: one warp each.
 constexpr int kCombineWarps = 4;
+// Split maxima and sums a lane holds (k = lane + 32 i); with
+// PKV_MAX_SPLITS = 128 every split of a row is loaded in one round.
+constexpr int kCombineSlots = (PKV_MAX_SPLITS + 31) / 32;
+// Partial outputs a lane loads per round (each D/32 floats).
+constexpr int kCombineBatch = 16;
+
+// Lane `lane` loads the maxima and sums of splits lane, lane + 32, ... below
+// num_splits (independent loads, issued together).
+__device__ __forceinline__ void load_split_stats(const float* pm, const float* pl, int num_splits,
+                                                 int lane, float (&mk)[kCombineSlots],
+                                                 float (&lk)[kCombineSlots]) {
+#pragma unroll
+  for (int i = 0; i < kCombineSlots; ++i) {
+    const int k = lane + 32 * i;
+    mk[i] = k < num_splits ? __ldg(pm + k) : -CUDART_INF_F;
+    lk[i] = k < num_splits ? __ldg(pl + k) : 0.f;
+  }
+}
 
 // The log-sum-exp merge of one output row of D elements from its first n
-// split partials, by one warp: lanes read the splits' maxima and sums
-// (M = max m_k, w_k = 2^(m_k - M), den = sum w_k l_k), then each lane sums
-// its D/32 elements of the weighted partial outputs with vector loads.  A
-// split with weight 0 (max -inf: no position of the row in it) is not read.
+// split partials, by one warp, given the split maxima and sums the lanes
+// loaded (load_split_stats): M = max m_k, w_k = 2^(m_k - M) (0 for a split
+// with max -inf, which holds no position of the row), den = sum w_k l_k;
+// then each lane sums its D/32 elements of the weighted partial outputs with
+// up to kCombineBatch independent vector loads in flight.  Splits at or past
+// n are never read; a zero-weight split's partial is read but not used (it
+// may never have been written).
 template <int D>
-__device__ __forceinline__ void merge_row_warp(const float* pm, const float* pl, const float* po,
+__device__ __forceinline__ void merge_row_warp(const float (&mk)[kCombineSlots],
+                                               const float (&lk)[kCombineSlots], const float* po,
                                                int n, __half* out_row, float* s_w) {
   constexpr int E = D / 32;  // elements per lane
   const int lane = threadIdx.x & 31;
   float M = -CUDART_INF_F;
-  for (int k = lane; k < n; k += 32) M = fmaxf(M, __ldg(pm + k));
+#pragma unroll
+  for (int i = 0; i < kCombineSlots; ++i)
+    if (lane + 32 * i < n) M = fmaxf(M, mk[i]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   float den = 0.f;
-  for (int k = lane; k < n; k += 32) {
-    const float mk = __ldg(pm + k);
-    const float w = (mk == -CUDART_INF_F) ? 0.f : exp2f(mk - M);
-    s_w[k] = w;
-    den += w * __ldg(pl + k);
+#pragma unroll
+  for (int i = 0; i < kCombineSlots; ++i) {
+    const int k = lane + 32 * i;
+    if (k < n) {
+      const float w = (mk[i] == -CUDART_INF_F) ? 0.f : exp2f(mk[i] - M);
+      s_w[k] = w;
+      if (w != 0.f) den += w * lk[i];
+    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
@@ -1491,45 +1524,33 @@ __device__ __forceinline__ void merge_row_warp(const float* pm, const float* pl,
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
   const float* base = po + lane * E;
-  auto load = [&](int k, float (&v)[E]) {
-    if constexpr (E == 4) {
-      const float4 x = __ldg(reinterpret_cast<const float4*>(base + (size_t)k * D));
-      v[0] = x.x;
-      v[1] = x.y;
-      v[2] = x.z;
-      v[3] = x.w;
-    } else {
-      const float2 x = __ldg(reinterpret_cast<const float2*>(base + (size_t)k * D));
-      v[0] = x.x;
-      v[1] = x.y;
-    }
-  };
-  int k = 0;
-  for (; k + 4 <= n; k += 4) {  // four splits' loads in flight at once
-    float v[4][E];
-    float w[4];
+  for (int kk = 0; kk < n; kk += kCombineBatch) {
+    const int m = min(kCombineBatch, n - kk);
+    float v[kCombineBatch][E];
 #pragma unroll
-    for (int x = 0; x < 4; ++x) {
-      w[x] = s_w[k + x];
-      if (w[x] != 0.f) {
-        load(k + x, v[x]);
-      } else {
-#pragma unroll
-        for (int e = 0; e < E; ++e) v[x][e] = 0.f;
+    for (int x = 0; x < kCombineBatch; ++x) {
+      if (x < m) {  // in bounds: loaded whatever the weight
+        const float* src = base + (size_t)(kk + x) * D;
+        if constexpr (E == 4) {
+          const float4 t = __ldg(reinterpret_cast<const float4*>(src));
+          v[x][0] = t.x;
+          v[x][1] = t.y;
+          v[x][2] = t.z;
+          v[x][3] = t.w;
+        } else {
+          const float2 t = __ldg(reinterpret_cast<const float2*>(src));
+          v[x][0] = t.x;
+          v[x][1] = t.y;
+        }
       }
     }
 #pragma unroll
-    for (int x = 0; x < 4; ++x)
+    for (int x = 0; x < kCombineBatch; ++x) {
+      const float w = x < m ? s_w[kk + x] : 0.f;
+      if (w != 0.f) {  // (a varlen split with no position of the row wrote no partial)
 #pragma unroll
-      for (int e = 0; e < E; ++e) acc[e] += w[x] * v[x][e];
-  }
-  for (; k < n; ++k) {
-    const float w = s_w[k];
-    if (w != 0.f) {
-      float v[E];
-      load(k, v);
-#pragma unroll
-      for (int e = 0; e < E; ++e) acc[e] += w * v[e];
+        for (int e = 0; e < E; ++e) acc[e] += w * v[x][e];
+      }
     }
   }
   const float inv = den > 0.f ? 1.f / den : 0.f;
@@ -1547,7 +1568,9 @@ __device__ __forceinline__ void merge_row_warp(const float* pm, const float* pl,
 // Decode split-K: one warp per (sequence, query head) row.  The row's chunk
 // count n follows from its length and the chunk size phase 1 used: n = 1 was
 // finished by phase 1 (f16 output written), n = 0 (empty context) is zeros,
-// n > 1 merges the n partials phase 1 wrote.
+// n > 1 merges the n partials phase 1 wrote.  The chunk size, the length and
+// every split's maximum and sum are loaded in one round (the maxima and sums
+// past n are read but never used), the partials in the next.
 template <int D>
 __global__ void __launch_bounds__(kCombineWarps * 32) splitk_combine_kernel(const CombineParams p) {
   __shared__ float s_w[kCombineWarps][PKV_MAX_SPLITS];
@@ -1560,8 +1583,12 @@ __global__ void __launch_bounds__(kCombineWarps * 32) splitk_combine_kernel(cons
   const int row = blockIdx.x * kCombineWarps + warp;
   if (row >= p.num_rows) return;
   const int s = row / p.num_heads;
-  const int chunk = max(1, *reinterpret_cast<const volatile int*>(p.split_header));
+  const int chunk_raw = *reinterpret_cast<const volatile int*>(p.split_header);
   int L = __ldg(p.context_lens + s);
+  float mk[kCombineSlots], lk[kCombineSlots];
+  load_split_stats(p.part_m + (size_t)row * p.num_splits, p.part_l + (size_t)row * p.num_splits,
+                   p.num_splits, lane, mk, lk);
+  const int chunk = max(1, chunk_raw);
   L = L < 0 ? 0 : (L > p.cap_tokens ? p.cap_tokens : L);
   const int nb = (L + p.block_size - 1) / p.block_size;
   const int n = min(p.num_splits, (nb + chunk - 1) / chunk);
@@ -1573,8 +1600,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) splitk_combine_kernel(cons
     for (int e = 0; e < E; ++e) out_row[lane * E + e] = __float2half_rn(0.f);
     return;
   }
-  merge_row_warp<D>(p.part_m + (size_t)row * p.num_splits, p.part_l + (size_t)row * p.num_splits,
-                    p.part_out + (size_t)row * p.num_splits * D, n, out_row, s_w[warp]);
+  merge_row_warp<D>(mk, lk, p.part_out + (size_t)row * p.num_splits * D, n, out_row, s_w[warp]);
 }
 
 // Varlen split-K: one warp per (query token, head) row.  The token's
@@ -1606,6 +1632,9 @@ varlen_combine_kernel(const VarlenCombineParams p) {
   const int rh = blockIdx.x * kCombineWarps + warp;  // row * H + head
   if (rh >= p.total_q * p.num_heads) return;
   const int row = rh / p.num_heads;
+  float mk[kCombineSlots], lk[kCombineSlots];  // in flight during the search
+  load_split_stats(p.part_m + (size_t)rh * p.num_splits, p.part_l + (size_t)rh * p.num_splits,
+                   p.num_splits, lane, mk, lk);
   int lo = 0, hi = p.num_seqs - 1;  // last sequence whose first row is <= row
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -1625,8 +1654,8 @@ varlen_combine_kernel(const VarlenCombineParams p) {
     for (int e = 0; e < E; ++e) out_row[lane * E + e] = __float2half_rn(0.f);
     return;
   }
-  merge_row_warp<D>(p.part_m + (size_t)rh * p.num_splits, p.part_l + (size_t)rh * p.num_splits,
-                    p.part_out + (size_t)rh * p.num_splits * D, p.num_splits, out_row, s_w[warp]);
+  merge_row_warp<D>(mk, lk, p.part_out + (size_t)rh * p.num_splits * D, p.num_splits, out_row,
+                    s_w[warp]);
 }
 
 // Diagnostic: one warp waits on an mbarrier that nothing arrives on.  The

@@ -258,6 +258,24 @@ def make(name: str) -> Workload:
             "ragged": ragged}[name]()
 
 
+def compact_pool(w: Workload, seed: int = BASE_SEED + 99, slack: int = 64) -> Workload:
+    """The same workload over a smaller pool: the blocks its sequences use
+    (and the poison block) renumbered by a seeded random permutation of
+    ``used + slack`` ids, so the reads stay scattered but the pool holds only
+    what the call reads (for profiling captures that save and restore device
+    memory).  Values, lengths and the logical tables are unchanged."""
+    ids, _, _ = compact_blocks(w)
+    used = np.unique(ids)
+    nb = len(used) + slack
+    perm = _rng(seed).permutation(nb).astype(np.int32)
+    remap = np.full(w.num_blocks, -1, np.int64)
+    remap[used] = perm[:len(used)]
+    tables = remap[w.block_tables].astype(np.int32)
+    assert (tables >= 0).all()
+    return dataclasses.replace(w, name=f"{w.name}-compact", num_blocks=nb, block_tables=tables,
+                               poison_block=int(remap[w.poison_block]))
+
+
 def widen_tables(w: Workload, factor: int) -> Workload:
     """The same workload with block tables ``factor`` times wider than its
     longest context needs (as a server sizes them for the model's maximum

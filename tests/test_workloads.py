@@ -3,6 +3,7 @@
 import numpy as np
 import pytest
 
+import oracle
 from paged_kv_decode_08_gb300 import workloads as W
 
 
@@ -113,3 +114,18 @@ def test_loop_allocator_reports_exhaustion_and_overflow():
         W.AppendDecodeLoop(steps=1, num_blocks=50, max_blocks_per_seq=2, **kw)
     ok = W.AppendDecodeLoop(steps=1, num_blocks=7, max_blocks_per_seq=4, **kw)  # 2 + 2 + 2 + poison
     assert ok.end_lens.tolist() == [33, 33]
+
+
+def test_compact_pool_keeps_the_attention():
+    """The compact pool renumbers the used blocks (and the poison block) and
+    changes nothing the oracle computes."""
+    w = W.small_random(5, num_seqs=5, num_heads=4, num_kv_heads=2, head_dim=64, block_size=16,
+                       lens=[40, 1, 77, 16, 130], num_blocks=500)
+    c = W.compact_pool(w)
+    assert c.num_blocks < w.num_blocks
+    assert len(np.unique(c.block_tables)) == len(np.unique(w.block_tables))
+    kc, vc = W.host_pool(w)
+    kc2, vc2 = W.host_pool(c)
+    a = oracle.decode(w.q, kc, vc, w.block_tables, w.context_lens, w.scale)
+    b = oracle.decode(c.q, kc2, vc2, c.block_tables, c.context_lens, c.scale)
+    assert np.array_equal(a, b)

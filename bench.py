@@ -920,6 +920,40 @@ def measure_step(args, name, dev, dist, world, rank, n_sets, want_e2e, want_cpu)
                "ms_per_step": e2e_ms / args.steps,
                "how": "direct Python calls each step: one pinned H2D copy of the packed step "
                       "inputs, the step, one D2H copy of the output"}
+        if not separate:
+            # the same steps with the kernels reading the pinned inputs and
+            # writing the pinned output in place (no copies; pools on the GPU)
+            h_view = {pname: h_buf[offs[pname]:offs[pname] + a.nbytes] for pname, a in parts}
+            h_out2 = torch.empty(tuple(q.shape), dtype=torch.float16).pin_memory()
+
+            def zc_step(i):
+                st = sets[i % n_sets]
+                rc = pk.lib.pkv_append_decode(
+                    h_view["k"].data_ptr(), h_view["v"].data_ptr(), h_view["slots"].data_ptr(),
+                    st["k_cache"].data_ptr(), st["v_cache"].data_ptr(), h_view["q"].data_ptr(),
+                    h_view["bt"].data_ptr(), h_view["cl"].data_ptr(), w.num_seqs,
+                    w.max_blocks_per_seq, w.num_blocks, float(w.scale), w.num_heads,
+                    w.num_kv_heads, w.head_dim, w.block_size, h_out2.data_ptr(),
+                    int(args.splits), scratch.data_ptr(), scratch.numel(), stream.cuda_stream)
+                if rc != pk.PKV_OK:
+                    raise RuntimeError(pk.last_error())
+
+            for i in range(args.warmup):
+                zc_step(i)
+            torch.cuda.synchronize()
+            a.record(stream)
+            for i in range(args.steps):
+                zc_step(i)
+            b.record(stream)
+            torch.cuda.synchronize()
+            zc_ms = max_over_ranks(a.elapsed_time(b), dist, dev)
+            e2e["zero_copy"] = {
+                "value": job_throughput(kv_bytes, world, zc_ms / args.steps), "unit": UNIT,
+                "ms_per_step": zc_ms / args.steps, "host_bytes_read_per_step": h2d,
+                "host_bytes_written_per_step": d2h,
+                "how": "the same steps through the C ABI with the packed inputs and the output "
+                       "in page-locked host memory, read and written by the kernels in place "
+                       "(no copies)"}
 
     flags = pk.pkv_read_device_status()
     if rank != 0:

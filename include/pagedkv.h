@@ -15,6 +15,13 @@
  *
  * Conventions for every call
  *   - Pointers named "device" are CUDA device pointers (or managed memory).
+ *     Every one of them except the K/V pools (which the kernels read with
+ *     TMA tensor copies and must be device memory) may instead point at
+ *     page-locked host memory (cudaMallocHost, cudaHostAlloc, or memory
+ *     registered with cudaHostRegister): the kernels then read and write it
+ *     in place over the host link, so a decode step needs no separate copy
+ *     of its small inputs (q, new rows, slots, tables, lengths) or of its
+ *     output.
  *     The caller owns every buffer.  The library allocates nothing per call.
  *     Its own device memory is static, declared in the library and held by
  *     every GPU that loads it until the process exits: one 32-bit status

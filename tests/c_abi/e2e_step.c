@@ -11,7 +11,11 @@
  * call (the library's own cost: validation, tensor maps, the launch), the
  * device time per step (CUDA events around the copy-step-copy chain of back-
  * to-back steps), and the wall time per step with a stream synchronisation
- * after each step.  Exits non-zero on any error.
+ * after each step.  Then the same steps without the two copies: the kernels
+ * read the inputs from, and write the output to, the pinned host buffers
+ * directly over the host link (zero-copy; the pools stay in device memory),
+ * and the outputs of both forms are compared bit for bit.  Exits non-zero
+ * on any error.
  *
  * usage: e2e_step [steps] [warmup]
  */
@@ -167,6 +171,34 @@ int main(int argc, char** argv) {
   }
   float ev_ms = 0.f;
   CK(cudaEventElapsedTime(&ev_ms, ev0, ev1));
+
+  /* zero-copy: the same steps on the host buffers themselves (page-locked
+   * host memory is addressable from the device with the same pointer) */
+  uint16_t* h_out_zc = NULL;
+  CK(cudaMallocHost((void**)&h_out_zc, q_bytes));
+  for (int phase = 0; phase < 2; ++phase) {
+    const int n = phase == 0 ? warmup : steps;
+    if (phase == 1) CK(cudaEventRecord(ev0, st));
+    for (int i = 0; i < n; ++i) {
+      const pkv_status rc = pkv_append_decode(
+          h_in + off_k, h_in + off_v, (const int32_t*)(h_in + off_slot), k_cache, v_cache,
+          h_in + off_q, (const int32_t*)(h_in + off_tab), (const int32_t*)(h_in + off_len), B,
+          MBPS, NB, 0.08838834764831845f, H, HKV, D, BS, h_out_zc, 0, scratch, scratch_bytes, st);
+      if (rc != PKV_OK) {
+        fprintf(stderr, "pkv_append_decode (zero-copy): %s: %s\n", pkv_status_string(rc),
+                pkv_last_error());
+        return 1;
+      }
+    }
+    if (phase == 1) CK(cudaEventRecord(ev1, st));
+    CK(cudaStreamSynchronize(st));
+  }
+  float zc_ms = 0.f;
+  CK(cudaEventElapsedTime(&zc_ms, ev0, ev1));
+  if (memcmp(h_out, h_out_zc, q_bytes) != 0) {
+    fprintf(stderr, "zero-copy output differs from the copied one\n");
+    return 1;
+  }
   int32_t flags = -1;
   if (pkv_read_device_status(&flags, st) != PKV_OK || flags != 0) {
     fprintf(stderr, "device status flags %d\n", (int)flags);
@@ -182,12 +214,14 @@ int main(int argc, char** argv) {
   qsort(wall_us, (size_t)steps, sizeof(double), cmp_double);
   const double kv = (double)total_tokens * 2 * HKV * D * 2;
   const double step_us = 1e3 * ev_ms / steps;
+  const double zc_us = 1e3 * zc_ms / steps;
   printf("{\"workload\": \"B=32 H=32 Hkv=8 D=128 bs=16 L~U[512,2048], 16384-block pool\", "
          "\"splits\": %d, \"steps\": %d, \"host_us_per_call_median\": %.2f, "
          "\"host_us_per_call_min\": %.2f, \"e2e_us_per_step\": %.2f, \"e2e_gbs\": %.1f, "
          "\"wall_us_per_step_median\": %.2f, \"h2d_bytes_per_step\": %zu, "
-         "\"d2h_bytes_per_step\": %zu}\n",
+         "\"d2h_bytes_per_step\": %zu, \"zero_copy_us_per_step\": %.2f, "
+         "\"zero_copy_gbs\": %.1f}\n",
          (int)splits, steps, host_us[steps / 2], host_us[0], step_us, kv / (step_us * 1e3),
-         wall_us[steps / 2], packed, q_bytes);
+         wall_us[steps / 2], packed, q_bytes, zc_us, kv / (zc_us * 1e3));
   return 0;
 }

@@ -359,6 +359,40 @@ def test_splitk_with_every_length_zero(pk, cuda_device):
         assert torch.count_nonzero(out).item() == 0
 
 
+def test_host_resident_inputs_and_output(pk, cuda_device):
+    """q, the new rows, slots, tables, lengths and out in page-locked host
+    memory, passed straight to the C ABI (the kernels read and write them
+    over the host link; the pools stay on the device): the same result, bit
+    for bit, as with every buffer on the device."""
+    w, ref = workload("llama8b")
+    k_new, v_new, slots = w.last_token_append()
+    host = {name: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+            for name, a in (("q", w.q), ("k", k_new), ("v", v_new), ("slots", slots),
+                            ("bt", w.block_tables), ("cl", w.context_lens))}
+    for S in (1, 4):
+        d = W.to_device(w, cuda_device, upto_last=True)
+        dev = {name: t.to(cuda_device) for name, t in host.items()}
+        scratch = pk.alloc_scratch(dev["q"], d["k_cache"], dev["bt"], S)
+        out_dev = pk.pkv_append_decode(dev["k"], dev["v"], dev["slots"], d["k_cache"],
+                                       d["v_cache"], dev["q"], dev["bt"], dev["cl"], w.scale,
+                                       num_splits=S, scratch=scratch)
+        d2 = W.to_device(w, cuda_device, upto_last=True)
+        out_host = torch.full(tuple(w.q.shape), float("nan"), dtype=torch.float16).pin_memory()
+        status = pk.lib.pkv_append_decode(
+            host["k"].data_ptr(), host["v"].data_ptr(), host["slots"].data_ptr(),
+            d2["k_cache"].data_ptr(), d2["v_cache"].data_ptr(), host["q"].data_ptr(),
+            host["bt"].data_ptr(), host["cl"].data_ptr(), w.num_seqs, w.max_blocks_per_seq,
+            w.num_blocks, float(w.scale), w.num_heads, w.num_kv_heads, w.head_dim, w.block_size,
+            out_host.data_ptr(), S, scratch.data_ptr(), scratch.numel(),
+            torch.cuda.current_stream().cuda_stream)
+        assert status == pk.PKV_OK, pk.last_error()
+        torch.cuda.synchronize()
+        assert_bits_equal(out_host.numpy(), out_dev.cpu().numpy(), f"host-resident, S={S}")
+        assert_attention_close(out_host.float().numpy().astype(np.float64), ref, f"S={S}")
+        assert torch.equal(d2["k_cache"].view(torch.int16), d["k_cache"].view(torch.int16))
+    assert pk.pkv_read_device_status() == 0
+
+
 # ---------------------------------------------------------------------------
 # graphs and streams
 # ---------------------------------------------------------------------------

@@ -122,7 +122,7 @@ def kernel_source_hash():
     """Hash of the CUDA sources with comments and blank lines left out (a
     comment edit does not change a kernel; any code edit does)."""
     h = hashlib.sha256()
-    for f in ("kernels.cuh", "ptx.cuh", "pagedkv.cu"):
+    for f in ("kernels.cuh", "ptx.cuh", "varlen_tc.cuh", "pagedkv.cu"):
         with open(os.path.join(ROOT, "paged_kv_decode_08_gb300", "csrc", f)) as fh:
             for line in fh:
                 code = line.split("//", 1)[0].strip()
@@ -673,13 +673,20 @@ def measure_loop(args, local, world, rank):
 
 
 def run_varlen(args):
+    line = measure_varlen(args, args.workload, args.varlen_tc)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+def measure_varlen(args, workload, tensor_path):
     """Speculative verification: 4 query tokens per sequence, causal, over
     the paged context (pkv_varlen_attention_splitk; the split count is the
-    library's heuristic unless --splits forces one).  Algorithmic bytes count
-    each sequence's context once; a CTA covers max(1, 8 NT / G) queries (NT =
-    2 n-tiles once a sequence has more than 8 query-head pairs), so the
-    kernel reads a context ceil(q_len / that) times: once for 4 queries at
-    G = 4."""
+    library's heuristic unless --splits forces one), on the mma.sync kernel
+    or (tensor_path) the tcgen05 one.  Algorithmic bytes count each
+    sequence's context once; a CTA covers max(1, 8 NT / G) queries (NT = 2
+    n-tiles once a sequence has more than 8 query-head pairs), so the kernel
+    reads a context ceil(q_len / that) times: once for 4 queries at G = 4.
+    Returns rank 0's line (None on the other ranks)."""
     import torch
 
     from paged_kv_decode_08_gb300 import pagedkv as pk
@@ -688,7 +695,17 @@ def run_varlen(args):
     world, rank, local = dist_setup()
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
-    v = W.spec_verify_long() if args.workload == "spec_long" else W.spec_verify()
+    prev_path = pk.pkv_set_varlen_tensor_path(1 if tensor_path else 0)
+    try:
+        return _measure_varlen(args, workload, tensor_path, pk, W, world, rank, local, dev)
+    finally:
+        pk.pkv_set_varlen_tensor_path(prev_path)
+
+
+def _measure_varlen(args, workload, tensor_path, pk, W, world, rank, local, dev):
+    import torch
+
+    v = W.spec_verify_long() if workload == "spec_long" else W.spec_verify()
     w = v.base
     n_sets = args.sets or N_SETS
     sets = build_sets(w, dev, n_sets)
@@ -730,14 +747,15 @@ def run_varlen(args):
         torch.cuda.synchronize()
     ms = a.elapsed_time(b) / (rounds * n_sets)
     if rank != 0:
-        return
+        return None
     kv_bytes = w.kv_bytes
     G = w.group
     nt = 2 if v.max_q_len * G > 8 else 1
     reads = -(-int(v.max_q_len) // max(1, 8 * nt // G))
     peak, peak_kind = measured_peaks()
     achieved = kv_bytes / (ms * 1e-3) / 1e9
-    tr = NCU_TRAFFIC.get(args.workload)
+    tc = tensor_path and v.max_q_len * G > 8 and w.head_dim == 128
+    tr = NCU_TRAFFIC.get(workload + ("_tc" if tc else ""))
     traffic = (tr["bytes_per_launch"] if tr and tr.get("kernel_hash") == kernel_source_hash()
                and S == tr.get("num_splits") else None)
     line = {
@@ -745,22 +763,23 @@ def run_varlen(args):
         "n_gpus": world, "steps": rounds * n_sets, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD_DESC[args.workload], "launch": "CUDA graph, replayed",
+        "config": {"workload": WORKLOAD_DESC[workload], "launch": "CUDA graph, replayed",
                    "num_splits": S, "context_reads_per_call": reads,
+                   "kernel_path": "tcgen05" if tc else "mma.sync",
                    "l2": f"{n_sets} rotating pool sets; {reads * kv_bytes / 1e6:.0f} MB read per call"},
         "kv_bytes_per_step": kv_bytes, "us_per_step": ms * 1e3,
         "query_tokens_per_s": world * v.total_q / (ms * 1e-3),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_kind,
-                     "kernel": ("paged_varlen_kernel" + (" split-K phase 1 + varlen_combine_kernel"
-                                                         if S > 1 else "")
+                     "kernel": (("paged_varlen_tc_kernel" if tc else "paged_varlen_kernel")
+                                + (" split-K phase 1 + varlen_combine_kernel" if S > 1 else "")
                                 + " (algorithmic bytes: each context once)"),
                      "bytes_read_frac": reads * achieved / peak, "traffic": traffic,
                      "traffic_kernel": tr["kernel"] if traffic is not None else None},
         "clocks": clocks.summary(), "gpu_launches": rounds * n_sets * (2 if S > 1 else 1),
         "device_status_flags": pk.pkv_read_device_status(), "e2e": None, "cpu_baseline": None,
     }
-    print(json.dumps(line), flush=True)
+    return line
 
 
 def measure_step(args, name, dev, dist, world, rank, n_sets, want_e2e, want_cpu):
@@ -1031,7 +1050,9 @@ def sub_record(line, name):
             "kv_gbs": kv / (dec_us * 1e-6) / 1e9,
             "frac": line["roofline"]["frac"], "frac_kernel": line["roofline"]["kernel"],
             "frac_of_decode_call": kv / (dec_us * 1e-6) / 1e9 / peak,
-            "decode_tokens_per_s": line["decode_tokens_per_s"],
+            "decode_tokens_per_s": line.get("decode_tokens_per_s"),
+            "query_tokens_per_s": line.get("query_tokens_per_s"),
+            "kernel_path": line["config"].get("kernel_path"),
             "traffic": line["roofline"].get("traffic"),
             "gpu_launches": line["gpu_launches"], "steps": line["steps"],
             "e2e": line.get("e2e"),
@@ -1060,7 +1081,7 @@ def c_driver_record(steps=200, warmup=20):
 # Llama-3-8B step reads 174 MB, near L2's 129 MB, so its pools rotate; the
 # others read 0.8-1.3 GB per call, far above L2.
 SUB_CONFIGS = [("llama8b", N_SETS, True), ("ragged", 1, False), ("loop", None, False),
-               ("tiny", N_SETS, False)]
+               ("tiny", N_SETS, False), ("spec", N_SETS, False), ("spec_tc", N_SETS, False)]
 
 
 def run_ours(args):
@@ -1085,6 +1106,8 @@ def run_ours(args):
         for sub, sets, e2e in SUB_CONFIGS:
             if sub == "loop":
                 r = measure_loop(args, local, world, rank)
+            elif sub in ("spec", "spec_tc"):
+                r = measure_varlen(args, "spec", sub == "spec_tc")
             else:
                 r = measure_step(args, sub, dev, None, world, rank, sets,
                                  want_e2e=e2e and not args.no_e2e, want_cpu=False)
@@ -1114,7 +1137,20 @@ def run_profile(args):
     dev = torch.device("cuda:0")
     torch.cuda.set_device(dev)
     n = args.ncu_calls
-    if args.workload == "loop":
+    if args.workload in ("spec", "spec_long"):
+        import dataclasses
+
+        v = W.spec_verify_long() if args.workload == "spec_long" else W.spec_verify()
+        v = dataclasses.replace(v, base=W.compact_pool(v.base))
+        d = W.to_device(v.base, dev)
+        q = torch.from_numpy(v.q).to(dev)
+        cu = torch.from_numpy(v.cu_seqlens_q).to(dev)
+        pos = torch.from_numpy(v.pos_offsets).to(dev)
+        for _ in range(n):
+            pk.pkv_varlen_attention_splitk(q, d["k_cache"], d["v_cache"], cu, pos,
+                                           d["block_tables"], v.base.scale,
+                                           max_q_len=v.max_q_len, num_splits=args.splits)
+    elif args.workload == "loop":
         loop = W.AppendDecodeLoop()
         d0 = W.to_device(loop.initial_workload(), dev)
         kc, vc = d0["k_cache"], d0["v_cache"]
@@ -1169,6 +1205,9 @@ def main():
     ap.add_argument("--layout", choices=["blocked", "vllm"], default="blocked",
                     help="cache layout: [NB][Hkv][bs][D], or vLLM's K [NB][Hkv][D/8][bs][8] "
                          "with V [NB][Hkv][D][bs] (append and decode as two calls)")
+    ap.add_argument("--varlen-tc", action="store_true",
+                    help="spec / spec_long: run the tcgen05 varlen kernel "
+                         "(pkv_set_varlen_tensor_path(1)) instead of the mma.sync one")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ncu-calls", type=int, default=0,

@@ -337,6 +337,23 @@ int32_t pkv_varlen_pick_num_splits(int32_t num_seqs, int32_t num_heads, int32_t 
                                    int32_t block_size, int32_t num_sms);
 
 /*
+ * pkv_set_varlen_tensor_path — which kernel pkv_varlen_attention and
+ * pkv_varlen_attention_splitk run (blocked pools, head_dim 128) when a CTA
+ * covers more than 8 (query, head) columns (group x queries per sequence
+ * above 8, e.g. 4 draft tokens at group 4): 0 (the initial setting) the
+ * mma.sync kernel; 1 the kernel that computes both products on the
+ * 5th-generation tensor cores (tcgen05.mma, scores and output accumulated
+ * in tensor memory, 128-token spans).  Both compute the same attention
+ * (within the stated tolerance; they round differently) from the same
+ * arguments, split-K partials included.  Other calls, the vLLM layout,
+ * head_dim 64 and smaller column counts are unaffected.  Process-wide;
+ * calls already enqueued keep the kernel they were launched with.
+ * Returns the previous setting, or -1 (nothing changed) for a value other
+ * than 0 or 1.
+ */
+int32_t pkv_set_varlen_tensor_path(int32_t on);
+
+/*
  * pkv_varlen_attention_splitk_vllm_layout — pkv_varlen_attention_splitk over
  * vLLM-layout pools.
  */

@@ -15,7 +15,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libpagedkv.so")
 SOURCES = [os.path.join(HERE, "csrc", "pagedkv.cu")]
-DEPS = SOURCES + [os.path.join(HERE, "csrc", f) for f in ("kernels.cuh", "ptx.cuh")] + [
+DEPS = SOURCES + [os.path.join(HERE, "csrc", f) for f in ("kernels.cuh", "ptx.cuh",
+                                                              "varlen_tc.cuh")] + [
     os.path.join(ROOT, "include", "pagedkv.h")]
 
 

@@ -19,6 +19,7 @@
 
 #include "kernels.cuh"
 #include "pagedkv.h"
+#include "varlen_tc.cuh"
 
 // Warps per decode CTA and the shared-memory ring they split (KB); the
 // defaults (6 warps, 96 KB: two resident CTAs per SM) won a sweep of warps x
@@ -31,6 +32,12 @@
 #endif
 #ifndef PKV_CTAS_PER_SM
 #define PKV_CTAS_PER_SM 2
+#endif
+// The initial setting of pkv_set_varlen_tensor_path: varlen attention with
+// more than 8 (query, head) columns per CTA on the tcgen05 kernel (blocked
+// pools, head_dim 128) when 1, on the mma.sync kernel when 0.
+#ifndef PKV_VARLEN_TC
+#define PKV_VARLEN_TC 0
 #endif
 
 
@@ -123,15 +130,15 @@ int current_device_sms(int* sms) {
 // head_dim/64 runs of 16 128-byte lines with the 128-byte swizzle (one
 // request per 16 rows measured slightly faster than one per 64-element half).
 pkv_status encode_cache_map(CUtensorMap* map, const void* base, int num_blocks, int num_kv_heads,
-                            int block_size, int head_dim) {
+                            int block_size, int head_dim, bool half_box = false) {
   auto encode = tensor_map_encoder();
   if (!encode) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   const cuuint64_t dims[4] = {64, (cuuint64_t)block_size, (cuuint64_t)(head_dim / 64),
                               (cuuint64_t)num_blocks * (cuuint64_t)num_kv_heads};
   const cuuint64_t strides[3] = {(cuuint64_t)head_dim * 2, 128,
                                  (cuuint64_t)block_size * head_dim * 2};
-  const cuuint32_t box[4] = {64, kSubtile ? 16u : (cuuint32_t)block_size,
-                             (cuuint32_t)(head_dim / 64), 1};
+  const cuuint32_t box[4] = {64, (kSubtile || half_box) ? 16u : (cuuint32_t)block_size,
+                             half_box ? 1u : (cuuint32_t)(head_dim / 64), 1};
   const cuuint32_t estride[4] = {1, 1, 1, 1};
   const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void*>(base), dims,
                             strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -185,7 +192,9 @@ struct MapCache {
 };
 MapCache g_maps;
 
-// kind 0: a blocked-layout pool (K or V); kind 1: a vLLM-layout V pool.
+// kind 0: a blocked-layout pool (K or V), 16 rows x head_dim per box;
+// kind 1: a vLLM-layout V pool; kind 2: a blocked-layout pool, 16 rows x one
+// 64-element half per box.
 pkv_status cached_map(CUtensorMap* map, int kind, const void* base, int num_blocks,
                       int num_kv_heads, int block_size, int head_dim) {
   const MapKey k{base, num_blocks, num_kv_heads, block_size, head_dim, kind};
@@ -197,9 +206,10 @@ pkv_status cached_map(CUtensorMap* map, int kind, const void* base, int num_bloc
         return PKV_OK;
       }
   }
-  const pkv_status st = kind == 0
-                            ? encode_cache_map(map, base, num_blocks, num_kv_heads, block_size, head_dim)
-                            : encode_vllm_v_map(map, base, num_blocks, num_kv_heads, block_size, head_dim);
+  const pkv_status st =
+      kind == 1 ? encode_vllm_v_map(map, base, num_blocks, num_kv_heads, block_size, head_dim)
+                : encode_cache_map(map, base, num_blocks, num_kv_heads, block_size, head_dim,
+                                   kind == 2);
   if (st != PKV_OK) return st;
   std::lock_guard<std::mutex> lock(g_maps.mu);
   const int i = g_maps.used < kMapCacheEntries ? g_maps.used++ : g_maps.next;
@@ -217,6 +227,11 @@ pkv_status make_cache_map(CUtensorMap* map, const void* base, int num_blocks, in
 pkv_status make_vllm_v_map(CUtensorMap* map, const void* base, int num_blocks, int num_kv_heads,
                            int block_size, int head_dim) {
   return cached_map(map, 1, base, num_blocks, num_kv_heads, block_size, head_dim);
+}
+
+pkv_status make_half_box_map(CUtensorMap* map, const void* base, int num_blocks, int num_kv_heads,
+                             int block_size, int head_dim) {
+  return cached_map(map, 2, base, num_blocks, num_kv_heads, block_size, head_dim);
 }
 
 struct DecodeArgs {
@@ -406,9 +421,39 @@ pkv_status launch_varlen(const DecodeArgs& a, const VarlenParams& vp, cudaStream
   return PKV_OK;
 }
 
+template <int BS, bool SPLIT>
+pkv_status launch_varlen_tc(const DecodeArgs& a, const VarlenParams& vp, cudaStream_t stream,
+                            int grid) {
+  using Sh = TcVarlenShape<128>;
+  auto kernel = paged_varlen_tc_kernel<128, BS, SPLIT>;
+  static std::atomic<unsigned long long> attr_set{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (!(attr_set.load(std::memory_order_relaxed) & bit)) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::kSmemBytes);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(varlen tc)");
+    attr_set.fetch_or(bit, std::memory_order_relaxed);
+  }
+  CUtensorMap kmap, vmap;
+  pkv_status st = make_half_box_map(&kmap, a.k_cache, a.num_blocks, a.num_kv_heads, BS, 128);
+  if (st != PKV_OK) return st;
+  st = make_half_box_map(&vmap, a.v_cache, a.num_blocks, a.num_kv_heads, BS, 128);
+  if (st != PKV_OK) return st;
+  e = launch_pdl(kernel, grid, Sh::kThreads, Sh::kSmemBytes, stream, kmap, vmap, vp);
+  if (e != cudaSuccess) return cuda_fail(e, "varlen attention (tcgen05) launch");
+  return PKV_OK;
+}
+
+std::atomic<int> g_varlen_tc{PKV_VARLEN_TC};
+
 template <bool SPLIT>
 pkv_status dispatch_varlen(const DecodeArgs& a, const VarlenParams& vp, cudaStream_t cs, int grid,
                            int NT, bool vllm) {
+  if (g_varlen_tc.load(std::memory_order_relaxed) && !vllm && NT == 2 && a.head_dim == 128)
+    return a.block_size == 16 ? launch_varlen_tc<16, SPLIT>(a, vp, cs, grid)
+                              : launch_varlen_tc<32, SPLIT>(a, vp, cs, grid);
 #define PKV_VARLEN_CASE(D_, BS_)                                                              \
   if (a.head_dim == D_ && a.block_size == BS_) {                                              \
     if (NT == 2)                                                                              \
@@ -589,6 +634,11 @@ int32_t pkv_pick_num_splits(int32_t num_seqs, int32_t num_kv_heads, int32_t max_
   if (s > kMaxAutoSplits) s = kMaxAutoSplits;
   if (s < 1) s = 1;
   return (int32_t)s;
+}
+
+int32_t pkv_set_varlen_tensor_path(int32_t on) {
+  if (on != 0 && on != 1) return -1;
+  return pkv::g_varlen_tc.exchange(on);
 }
 
 int32_t pkv_varlen_pick_num_splits(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,

@@ -66,6 +66,8 @@ def _load():
     lib.pkv_varlen_attention_splitk.restype = i32
     lib.pkv_varlen_attention_splitk_vllm_layout.argtypes = split_args
     lib.pkv_varlen_attention_splitk_vllm_layout.restype = i32
+    lib.pkv_set_varlen_tensor_path.argtypes = [i32]
+    lib.pkv_set_varlen_tensor_path.restype = i32
     lib.pkv_decode_splitk_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, f32, i32, i32,
                                               i32, i32, vp, i32, vp]
     lib.pkv_decode_splitk_noalloc.restype = i32
@@ -328,6 +330,16 @@ def pkv_varlen_attention_splitk_vllm_layout(q, k_cache, v_cache, cu_seqlens_q, p
     """:func:`pkv_varlen_attention_splitk` over vLLM-layout pools."""
     return _varlen(q, k_cache, v_cache, cu_seqlens_q, pos_offsets, block_tables, scale,
                    max_q_len, out, stream, vllm=True, split=(num_splits, scratch))
+
+
+def pkv_set_varlen_tensor_path(on) -> int:
+    """Run varlen attention with more than 8 (query, head) columns per CTA
+    on the tcgen05 kernel (``on`` = 1) or the mma.sync kernel (0, the
+    initial setting); returns the previous setting."""
+    prev = int(lib.pkv_set_varlen_tensor_path(int(on)))
+    if prev < 0:
+        raise ValueError(f"pkv_set_varlen_tensor_path: {on!r} is not 0 or 1")
+    return prev
 
 
 def pkv_varlen_pick_num_splits(num_seqs, num_heads, num_kv_heads, max_q_len,

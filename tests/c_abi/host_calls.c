@@ -21,6 +21,12 @@ int main(void) {
   CHECK(pkv_pick_num_splits(4, 8, 131072, 16, 152) > 1);
   CHECK(pkv_pick_num_splits(0, 8, 2048, 16, 152) == 1);
   CHECK(pkv_varlen_pick_num_splits(4, 32, 8, 4, 8192, 16, 152) == 10);
+  /* the varlen kernel switch: initially the mma.sync kernel; bad values
+     change nothing */
+  CHECK(pkv_set_varlen_tensor_path(1) == 0);
+  CHECK(pkv_set_varlen_tensor_path(2) == -1);
+  CHECK(pkv_set_varlen_tensor_path(0) == 1);
+  CHECK(pkv_set_varlen_tensor_path(-1) == -1);
   /* scratch sizes */
   CHECK(pkv_splitk_scratch_bytes(4, 32, 128, 1) == 0);
   CHECK(pkv_splitk_scratch_bytes(4, 32, 128, 16) >= (size_t)4 * 32 * 16 * 130 * 4);

@@ -38,7 +38,7 @@ def test_header_declares_the_expected_calls():
               "pkv_varlen_attention_splitk_vllm_layout", "pkv_varlen_pick_num_splits",
               "pkv_qkv_norm_rope_append", "pkv_qkv_norm_rope_append_decode",
               "pkv_selftest_wait_timeout", "pkv_decode_splitk_plan", "pkv_varlen_splitk_plan",
-              "pkv_decode_splitk_noalloc"]:
+              "pkv_decode_splitk_noalloc", "pkv_set_varlen_tensor_path"]:
         assert n in names
 
 

@@ -28,6 +28,17 @@ def pk(cuda_device):
     return pagedkv
 
 
+@pytest.fixture(params=[0, 1], ids=["mma_sync", "tcgen05"])
+def varlen_path(request, pk):
+    """The kernel varlen attention runs for chunks of more than 8 (query,
+    head) columns at head_dim 128 (pkv_set_varlen_tensor_path): the
+    mma.sync kernel or the tcgen05 one; other shapes run the same kernel
+    under both."""
+    prev = pk.pkv_set_varlen_tensor_path(request.param)
+    yield request.param
+    pk.pkv_set_varlen_tensor_path(prev)
+
+
 _CACHE = {}
 
 
@@ -155,7 +166,7 @@ def test_overprovisioned_tables_split_the_real_contexts(pk, cuda_device, name):
     assert pk.pkv_read_device_status() == 0
 
 
-def test_overprovisioned_tables_varlen_splitk(pk, cuda_device):
+def test_overprovisioned_tables_varlen_splitk(pk, cuda_device, varlen_path):
     """Long speculative verification with tables four times wider than the
     contexts: the varlen split chunks are cut from the real longest context."""
     v0 = W.spec_verify_long()
@@ -502,7 +513,7 @@ def varlen_device(v, dev):
     (8, 4, 128, 32, [4, 1, 3], [64, 200, 1]),            # G=2, NT=1: 4 queries per CTA
     (32, 8, 128, 16, [40, 3], [100, 0]),                 # G=4, NT=2: a 40-token prefill chunk
 ])
-def test_varlen_matches_oracle(pk, cuda_device, H, Hkv, D, bs, q_lens, prefix):
+def test_varlen_matches_oracle(pk, cuda_device, varlen_path, H, Hkv, D, bs, q_lens, prefix):
     v = W.varlen_random(3000 + H + D + bs, H, Hkv, D, bs, q_lens, prefix)
     kc, vc = W.host_pool(v.base)
     ref = oracle.varlen(v.q, kc, vc, v.cu_seqlens_q, v.pos_offsets, v.base.block_tables,
@@ -515,7 +526,7 @@ def test_varlen_matches_oracle(pk, cuda_device, H, Hkv, D, bs, q_lens, prefix):
     assert pk.pkv_read_device_status() == 0
 
 
-def test_varlen_speculative_verification(pk, cuda_device):
+def test_varlen_speculative_verification(pk, cuda_device, varlen_path):
     """Four draft tokens per sequence on the Llama-3-8B attention shape."""
     v = W.spec_verify()
     kc, vc = W.host_pool(v.base)
@@ -540,6 +551,56 @@ def test_varlen_single_queries_match_decode(pk, cuda_device):
     assert_attention_close(to_np(a), to_np(b), "varlen q_len=1 vs decode")
 
 
+def test_varlen_bad_block_id_is_skipped_and_flagged(pk, cuda_device, varlen_path):
+    """A table entry outside the pool: its 16 positions are left out (never
+    read) and flagged; the other sequence is untouched.  Group 4 with 4 and 3
+    queries: more than 8 columns per CTA at head_dim 128."""
+    v = W.varlen_random(3300, 8, 2, 128, 16, [4, 3], [300, 20])
+    kc, vc = W.host_pool(v.base)
+    ref = oracle.varlen(v.q, kc, vc, v.cu_seqlens_q, v.pos_offsets, v.base.block_tables,
+                        v.base.scale)
+    d = varlen_device(v, cuda_device)
+    tables = v.base.block_tables.copy()
+    tables[0, 5] = v.base.num_blocks + 7  # positions 80..95 of sequence 0
+    d["block_tables"] = torch.from_numpy(tables).to(cuda_device)
+    for S in (1, 3):
+        out = to_np(pk.pkv_varlen_attention_splitk(d["q"], d["k_cache"], d["v_cache"], d["cu"],
+                                                   d["pos"], d["block_tables"], v.base.scale,
+                                                   max_q_len=4, num_splits=S))
+        assert pk.pkv_read_device_status() & pk.PKV_DEV_BAD_BLOCK_ID
+        assert np.all(np.isfinite(out))
+        assert_attention_close(out[4:], ref[4:], f"S={S} untouched sequence")
+        K = v.base.seq_k[0].astype(np.float64)
+        V = v.base.seq_v[0].astype(np.float64)
+        for t in range(4):
+            keep = [j for j in range(300 + t + 1) if not 80 <= j < 96]
+            for h in range(8):
+                z = v.base.scale * K[keep, h // 4] @ v.q[t, h].astype(np.float64)
+                p = np.exp(z - z.max())
+                p /= p.sum()
+                assert_attention_close(out[t, h], p @ V[keep, h // 4], f"S={S} query {t} head {h}")
+
+
+def test_varlen_kernels_agree(pk, cuda_device):
+    """The mma.sync and tcgen05 kernels on speculative verification: both
+    within the oracle tolerance of each other (they round P and the sums
+    differently, so not bit for bit)."""
+    v = W.spec_verify()
+    d = varlen_device(v, cuda_device)
+    outs = []
+    prev = pk.pkv_set_varlen_tensor_path(0)
+    try:
+        for path in (0, 1):
+            pk.pkv_set_varlen_tensor_path(path)
+            outs.append(to_np(pk.pkv_varlen_attention(d["q"], d["k_cache"], d["v_cache"], d["cu"],
+                                                      d["pos"], d["block_tables"], v.base.scale,
+                                                      max_q_len=4)))
+    finally:
+        pk.pkv_set_varlen_tensor_path(prev)
+    assert_attention_close(outs[1], outs[0].astype(np.float64), "tcgen05 vs mma.sync")
+    assert pk.pkv_read_device_status() == 0
+
+
 def test_varlen_flags_bad_query_ranges(pk, cuda_device):
     v = W.varlen_random(3200, 4, 2, 64, 16, [2, 2], [5, 5])
     d = varlen_device(v, cuda_device)
@@ -561,7 +622,8 @@ def test_varlen_flags_bad_query_ranges(pk, cuda_device):
     (8, 4, 128, 32, [4, 1, 3], [64, 200, 1]),
     (32, 8, 128, 16, [40, 3], [100, 0]),  # early queries see none of the later splits
 ])
-def test_varlen_splitk_matches_oracle(pk, cuda_device, H, Hkv, D, bs, q_lens, prefix):
+def test_varlen_splitk_matches_oracle(pk, cuda_device, varlen_path, H, Hkv, D, bs, q_lens,
+                                      prefix):
     v = W.varlen_random(5000 + H + D + bs, H, Hkv, D, bs, q_lens, prefix)
     kc, vc = W.host_pool(v.base)
     ref = oracle.varlen(v.q, kc, vc, v.cu_seqlens_q, v.pos_offsets, v.base.block_tables,
@@ -576,10 +638,11 @@ def test_varlen_splitk_matches_oracle(pk, cuda_device, H, Hkv, D, bs, q_lens, pr
     assert pk.pkv_read_device_status() == 0
 
 
-def test_varlen_splitk_long_context_speculative_verification(pk, cuda_device):
+def test_varlen_splitk_long_context_speculative_verification(pk, cuda_device, varlen_path):
     """Four draft tokens after 32K..128K-token prefixes: the heuristic splits
     each context (the unsplit grid is 32 CTAs), and the result matches the
-    oracle; the vLLM-layout call equals the blocked one bit for bit."""
+    oracle, for the blocked layout (either kernel) and the vLLM layout (the
+    mma.sync kernel) alike."""
     v = W.spec_verify_long()
     kc, vc = W.host_pool(v.base)
     ref = oracle.varlen_fast(v.q, kc, vc, v.cu_seqlens_q, v.pos_offsets, v.base.block_tables,
@@ -601,7 +664,7 @@ def test_varlen_splitk_long_context_speculative_verification(pk, cuda_device):
                                                        d["cu"], d["pos"], d["block_tables"],
                                                        v.base.scale, max_q_len=4, num_splits=0)
     torch.cuda.synchronize()
-    assert_bits_equal(got_v.cpu().numpy(), outs["heuristic"].cpu().numpy(), "vLLM vs blocked")
+    assert_attention_close(to_np(got_v), ref, "long spec verify, vLLM layout")
     assert pk.pkv_read_device_status() == 0
 
 
@@ -616,7 +679,7 @@ def test_varlen_splitk_rejects_small_scratch(pk, cuda_device):
     assert e.value.status == pk.PKV_ERR_SCRATCH_TOO_SMALL
 
 
-def test_varlen_splitk_replays_from_a_cuda_graph(pk, cuda_device):
+def test_varlen_splitk_replays_from_a_cuda_graph(pk, cuda_device, varlen_path):
     """Phase 1 and the combine, captured once and replayed, reproduce the
     eager result bit for bit (no host reads; the split count and scratch
     are fixed at capture)."""

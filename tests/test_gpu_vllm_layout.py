@@ -264,9 +264,10 @@ def test_vllm_varlen_matches_oracle(pk, cuda_device, H, Hkv, D, bs, q_lens, pref
     assert pk.pkv_read_device_status() == 0
 
 
-def test_vllm_varlen_speculative_verification_equals_blocked(pk, cuda_device):
+def test_vllm_and_blocked_speculative_verification_match_the_oracle(pk, cuda_device):
     """Four draft tokens per sequence on the Llama-3-8B shape: the vLLM-layout
-    call matches the oracle and the blocked call bit for bit."""
+    call (mma.sync kernel) and the blocked call (tcgen05 kernel at head_dim
+    128) both match the oracle."""
     v = W.spec_verify()
     kc, vc = W.host_pool_vllm(v.base)
     ref = oracle.varlen_vllm_layout(v.q, kc, vc, v.cu_seqlens_q, v.pos_offsets,
@@ -282,5 +283,5 @@ def test_vllm_varlen_speculative_verification_equals_blocked(pk, cuda_device):
                                       d["block_tables"], v.base.scale, max_q_len=4)
     torch.cuda.synchronize()
     assert_attention_close(to_np(got), ref, "vLLM spec verify")
-    assert_bits_equal(got.cpu().numpy(), blocked.cpu().numpy(), "vLLM vs blocked varlen")
+    assert_attention_close(to_np(blocked), ref, "blocked spec verify")
     assert pk.pkv_read_device_status() == 0

@@ -85,23 +85,47 @@ BASE_QKV_SEED = 20261210
 # ncu capture summarised in profiles/ (kernel source hash at capture time).
 # Reported as null when the kernels have changed since.
 NCU_TRAFFIC = {
+    # profiles/split_k.md: the long-context decode call, split-K phase 1
+    # (10 splits, dram read 1,342,369,000 B + write 3,687,680 B) + the combine
+    # (read 450,000 B)
+    "long": {"kernel_hash": "804b82c86616ebca", "bytes_per_launch": 1346506680, "num_splits": 10,
+             "fused": False, "layout": "blocked",
+             "kernel": "paged_decode_kernel<128,16,6,2,split> + splitk_combine_kernel<128>"},
+    # profiles/split_k.md: the ragged decode call, phase 1 (8 splits, read
+    # 810,120,448 B + write 6,809,856 B) + the combine (read 3,282,432 B)
+    "ragged": {"kernel_hash": "804b82c86616ebca", "bytes_per_launch": 820212736, "num_splits": 8,
+               "fused": False, "layout": "blocked",
+               "kernel": "paged_decode_kernel<128,32,6,2,split> + splitk_combine_kernel<128>"},
     # profiles/decode_llama8b.md: the fused append + single-pass decode launch,
-    # dram read 175,230,976 B + write 3,221,760 B
-    "llama8b": {"kernel_hash": "fe533890695fa809", "bytes_per_launch": 178452736, "num_splits": 1,
+    # dram read 175,223,808 B + write 3,479,296 B
+    "llama8b": {"kernel_hash": "804b82c86616ebca", "bytes_per_launch": 178703104, "num_splits": 1,
                 "fused": True, "layout": "blocked",
                 "kernel": "paged_decode_kernel<128,16,6,2,single,fused>"},
-    # profiles/varlen_spec_long.md: the varlen split-K phase 1 (10 splits),
-    # dram read 1,342,589,440 B + write 3,523,584 B
-    "spec_long": {"kernel_hash": "fe533890695fa809", "bytes_per_launch": 1346113024,
-                  "num_splits": 10, "kernel": "paged_varlen_kernel<128,16,6,2,NT=2,blocked,split>"},
+    # profiles/varlen_spec.md: one paged_varlen_kernel launch (mma.sync),
+    # read 174,706,176 B + write 3,722,240 B
+    "spec": {"kernel_hash": "804b82c86616ebca", "bytes_per_launch": 178428416, "num_splits": 1,
+             "kernel": "paged_varlen_kernel<128,16,6,2,NT=2,blocked,single>"},
+    # profiles/varlen_spec.md: one paged_varlen_tc_kernel launch (tcgen05),
+    # read 174,747,904 B + write 3,599,872 B
+    "spec_tc": {"kernel_hash": "804b82c86616ebca", "bytes_per_launch": 178347776, "num_splits": 1,
+                "kernel": "paged_varlen_tc_kernel<128,16,single>"},
+    # profiles/varlen_spec_long.md: the varlen split-K phase 1 (10 splits,
+    # read 1,342,483,000 B + write 3,526,912 B) + the combine (read 2,674,000 B)
+    "spec_long": {"kernel_hash": "804b82c86616ebca", "bytes_per_launch": 1348683912,
+                  "num_splits": 10,
+                  "kernel": "paged_varlen_kernel<128,16,6,2,NT=2,blocked,split> + "
+                            "varlen_combine_kernel<128>"},
+    "spec_long_tc": {"kernel_hash": "804b82c86616ebca", "bytes_per_launch": 1348444960,
+                     "num_splits": 10,
+                     "kernel": "paged_varlen_tc_kernel<128,16,split> + varlen_combine_kernel<128>"},
     # profiles/qkv_prefill.md: one qkv_norm_rope_kernel launch, dram read
-    # 101,987,584 B + write 53,220,096 B (the rest of the writes stay in L2)
-    "qkv_prefill": {"kernel_hash": "fe533890695fa809", "bytes_per_launch": 155207680,
+    # 101,985,792 B + write 53,701,888 B (the rest of the writes stay in L2)
+    "qkv_prefill": {"kernel_hash": "804b82c86616ebca", "bytes_per_launch": 155687680,
                     "kernel": "qkv_norm_rope_kernel<128,16,3>"},
     # profiles/decode_llama8b.md (one-launch QKV step): the decode kernel with
-    # the QKV norm + rotary + append folded in, dram read 175,242,752 B +
-    # write 3,392,000 B
-    "step_qkv": {"kernel_hash": "fe533890695fa809", "bytes_per_launch": 178634752,
+    # the QKV norm + rotary + append folded in, dram read 175,240,192 B +
+    # write 3,737,088 B
+    "step_qkv": {"kernel_hash": "804b82c86616ebca", "bytes_per_launch": 178977280,
                  "num_splits": 1, "kernel": "paged_decode_kernel<128,16,6,2,single,qkv>"},
 }
 
@@ -1137,6 +1161,7 @@ def run_profile(args):
     dev = torch.device("cuda:0")
     torch.cuda.set_device(dev)
     n = args.ncu_calls
+    pk.pkv_set_varlen_tensor_path(1 if args.varlen_tc else 0)
     if args.workload in ("spec", "spec_long"):
         import dataclasses
 

@@ -34,6 +34,7 @@ the bytes all ranks processed.
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import os
@@ -165,22 +166,28 @@ def measured_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi samples every 200 ms while the timed region runs."""
+    """nvidia-smi samples (every `interval_ms`) while the timed region runs.
+    begin() / end() mark the timed window inside a longer sampled stretch
+    (a soak of untimed replays before it), so that the record holds both the
+    samples under steady load and those that fell inside the window."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index):
+    def __init__(self, gpu_index, interval_ms=200):
         self.gpu_index = gpu_index
+        self.interval_ms = interval_ms
         self.proc = None
         self.lines = []
+        self.window = None
+        self.soak_steps = 0
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.interval_ms)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -192,9 +199,28 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
+    def begin(self):
+        self.window = [datetime.datetime.now(), None]
+
+    def end(self):
+        if self.window:
+            self.window[1] = datetime.datetime.now()
+
+    def soak(self, fn, seconds):
+        """Run fn() (untimed work) for about `seconds`, to have the GPU at
+        steady load when the timed window begins."""
+        import torch
+
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < seconds:
+            for _ in range(8):
+                fn()
+                self.soak_steps += 1
+            torch.cuda.synchronize()
+
     def __exit__(self, *exc):
         if self.proc is not None:
-            time.sleep(0.25)
+            time.sleep(max(0.05, 1.25 * self.interval_ms / 1e3))
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
@@ -202,24 +228,37 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
-        sm, smax, reasons = [], [], set()
+        sm, smax, reasons, in_window = [], [], set(), 0
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in self.lines:
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
+                mhz, mx = float(parts[2]), float(parts[3])
             except ValueError:
                 continue
-            for name, val in zip(names, parts[5:9]):
+            sm.append(mhz)
+            smax.append(mx)
+            for name, val in zip(names, parts[6:10]):
                 if val.lower() == "active":
                     reasons.add(name)
+            if self.window and self.window[1]:
+                try:
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
+                except ValueError:
+                    continue
+                if self.window[0] <= ts <= self.window[1]:
+                    in_window += 1
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        out = {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+               "reasons": sorted(reasons), "samples": len(sm),
+               "interval_ms": self.interval_ms}
+        if self.window:
+            out["samples_in_timed_window"] = in_window
+            out["soak_steps_before_window"] = self.soak_steps
+        return out
 
 
 def dist_setup():
@@ -890,9 +929,15 @@ def measure_step(args, name, dev, dist, world, rank, n_sets, want_e2e, want_cpu)
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(dev.index) as clocks:
+    # clocks: sampled every 20 ms through an untimed soak of the same graph
+    # (about 0.3 s, so the samples show the clocks under steady load) and the
+    # timed window right after it
+    with ClockSampler(dev.index, interval_ms=20) as clocks:
+        clocks.soak(g_step.replay, 0.3)
+        clocks.begin()
         total_ms, step_rounds = timed(g_step)
         decode_total_ms, decode_rounds = timed(g_decode)
+        clocks.end()
     if dist is not None:
         dist.barrier()
     total_ms = max_over_ranks(total_ms, dist, dev)

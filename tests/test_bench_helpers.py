@@ -9,19 +9,26 @@ import bench
 
 
 def test_clock_summary_takes_the_median_and_the_active_reasons():
-    s = bench.ClockSampler(0)
+    import datetime
+
+    s = bench.ClockSampler(0, interval_ms=20)
     s.lines = [
-        "0, 2070, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Not Active",
-        "0, 1980, 2070, 1390.5, 0x4, Not Active, Not Active, Not Active, Active",
-        "0, 2070, 2070, 950.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "2026/12/02 10:00:00.000, 0, 2070, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "2026/12/02 10:00:00.020, 0, 1980, 2070, 1390.5, 0x4, Not Active, Not Active, Not Active, Active",
+        "2026/12/02 10:00:00.040, 0, 2070, 2070, 950.0, 0x0, Not Active, Not Active, Not Active, Not Active",
         "garbled line",
-        "0, n/a, 2070, 0, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "2026/12/02 10:00:00.060, 0, n/a, 2070, 0, 0x0, Not Active, Not Active, Not Active, Not Active",
     ]
+    s.window = [datetime.datetime(2026, 12, 2, 10, 0, 0, 10000),
+                datetime.datetime(2026, 12, 2, 10, 0, 0, 50000)]
+    s.soak_steps = 16
     out = s.summary()
     assert out["sm_mhz"] == 2070.0
     assert out["sm_max_mhz"] == 2070.0
     assert out["reasons"] == ["sw_power_cap"]
     assert out["samples"] == 3
+    assert out["samples_in_timed_window"] == 2  # the samples at .020 and .040
+    assert out["soak_steps_before_window"] == 16
 
 
 def test_clock_summary_without_samples():

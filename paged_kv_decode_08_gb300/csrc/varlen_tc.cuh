@@ -14,8 +14,10 @@
 // (eight 16-row sub-tiles per tensor, one TMA box per 64-element half,
 // landing as [2 halves][128 rows][64] with the 128-byte swizzle: the K-major
 // and MN-major shared-memory layouts of the two MMAs) into a ring of three
-// 32 KB slots taken in the order K0, V0, K1, V1, ...; a K slot is released
-// when S has read it, a V slot when PV has.  Warp 5 (one lane) issues each
+// 32 KB slots taken in the order K0, K1, V0, K2, V1, ... (a span's V goes out
+// after the next span's K, so that it is in flight while the span's scores
+// and softmax run rather than held in a slot); a K slot is released when S
+// has read it, a V slot when PV has.  Warp 5 (one lane) issues each
 // product as soon as its inputs are ready (S is double-buffered in tensor
 // memory, so the next span's scores are computed during this span's
 // softmax).  Warps 0-3 run the online softmax: lane l of warp w owns token
@@ -104,8 +106,8 @@ paged_varlen_tc_kernel(const __grid_constant__ CUtensorMap kmap,
   auto s_free = [&](int i) { return bars + 8 * (8 + i); };
   auto p_ready = [&](int i) { return bars + 8 * (10 + i); };
   auto pv_done = [&](int i) { return bars + 8 * (12 + i); };
-  // Ring loads are numbered 2i (K of span i) and 2i + 1 (V of span i); load
-  // n goes to slot n % 3, its (n / 3)-th use of that slot.
+  // Ring loads in issue order: K0, then K(i+1), V(i) for each span i, V of
+  // the last span last; load n goes to slot n % 3, its (n / 3)-th use.
   auto slot_of = [](int n) { return n % Sh::kSlots; };
   auto use_of = [](int n) { return (uint32_t)(n / Sh::kSlots); };
 
@@ -201,6 +203,9 @@ paged_varlen_tc_kernel(const __grid_constant__ CUtensorMap kmap,
   const int n_spans = (n_tiles + Sh::kSubs - 1) / Sh::kSubs;  // >= 1
   const int32_t* table = p.block_tables + (size_t)s * p.max_blocks_per_seq;
 
+  auto kload = [&](int j) { return j == 0 ? 0 : 2 * j - 1; };                  // K(j)'s load
+  auto vload = [&](int i) { return i == n_spans - 1 ? 2 * n_spans - 1 : 2 * i + 2; };  // V(i)'s
+
   // ---- set-up: tensor memory, the queries as the B operand of S
   if (warp == 0) tmem_alloc(smem_addr(&s_tmem), Sh::kTmemCols);
   if (warp < 4) {
@@ -252,15 +257,22 @@ paged_varlen_tc_kernel(const __grid_constant__ CUtensorMap kmap,
         }
       };
       int issued = 0;
-      int phys[Sh::kSubs], nxt[Sh::kSubs];
+      // the entries of the span being loaded, the next span's (looked up a
+      // span ahead), and the validated entries of the last two spans' K
+      // loads (their V loads follow one K later)
+      int phys[Sh::kSubs], nxt[Sh::kSubs], ph0[Sh::kSubs], ph1[Sh::kSubs];
       lookup(0, nxt);
       for (int n = 0; n < 2 * n_spans; ++n) {
-        const int i = n >> 1;
-        const bool is_v = n & 1;
+        const bool last = n == 2 * n_spans - 1;
+        const bool is_v = last || (n > 0 && !(n & 1));
+        const int i = last ? n_spans - 1 : (is_v ? n / 2 - 1 : (n + 1) / 2);
         if (!is_v) {
 #pragma unroll
           for (int u = 0; u < Sh::kSubs; ++u) phys[u] = nxt[u];
           if (i + 1 < n_spans) lookup(i + 1, nxt);  // in flight during the waits below
+        } else {
+#pragma unroll
+          for (int u = 0; u < Sh::kSubs; ++u) phys[u] = (i & 1) ? ph1[u] : ph0[u];
         }
         // the slot's previous load (n - 3) must have been released
         const int slot = slot_of(n);
@@ -280,6 +292,10 @@ paged_varlen_tc_kernel(const __grid_constant__ CUtensorMap kmap,
               atomicOr(&g_device_status, kDevBadBlockId);
               phys[u] = -1;
             }
+            if (i & 1)
+              ph1[u] = phys[u];
+            else
+              ph0[u] = phys[u];
           }
         }
         int n_ok = 0;
@@ -313,17 +329,18 @@ paged_varlen_tc_kernel(const __grid_constant__ CUtensorMap kmap,
       // K(j) and S buffer j % 2 read by the softmax warps (span j - 2).
       // A barrier's phase is tested by its parity alone, so a test must not
       // run while the slot's previous load can still be in flight (it would
-      // see the completion before that one): K(j)'s slot held V(j - 2),
-      // which has landed once PV(j - 2) has been issued; V(i)'s slot held
-      // K(i - 1), landed once S(i - 1) has been.
+      // see the completion before that one): K(j)'s slot held V(j - 3) (K0
+      // for j = 2), which has landed once PV(j - 3) has been issued; V(i)'s
+      // slot held K(i) (V(i - 2) for the last span), landed before S(i) (or
+      // PV(i - 2)) was issued.
       int next_s = 0, next_pv = 0;
       uint64_t t_last = global_timer_ns();
       int idle = 0;
       while (next_pv < n_spans) {
         bool progressed = false;
         const int i = next_pv;
-        const int vs = slot_of(2 * i + 1);
-        if (mbar_test(p_ready(i & 1), (i >> 1) & 1) && mbar_test(full(vs), use_of(2 * i + 1) & 1)) {
+        const int vs = slot_of(vload(i));
+        if (mbar_test(p_ready(i & 1), (i >> 1) & 1) && mbar_test(full(vs), use_of(vload(i)) & 1)) {
           tc_fence_after();
           const uint32_t vb = ring + vs * Sh::kSlotBytes;
           const uint32_t pb = pbuf + (i & 1) * Sh::kPBytes;
@@ -342,8 +359,8 @@ paged_varlen_tc_kernel(const __grid_constant__ CUtensorMap kmap,
           progressed = true;
         }
         const int j = next_s;
-        const int ks_slot = slot_of(2 * j);
-        if (j < n_spans && j <= next_pv + 1 && mbar_test(full(ks_slot), use_of(2 * j) & 1) &&
+        const int ks_slot = slot_of(kload(j));
+        if (j < n_spans && j <= next_pv + 2 && mbar_test(full(ks_slot), use_of(kload(j)) & 1) &&
             (j < 2 || mbar_test(s_free(j & 1), ((j - 2) >> 1) & 1))) {
           tc_fence_after();
           const uint32_t kb = ring + ks_slot * Sh::kSlotBytes;
@@ -521,9 +538,10 @@ paged_varlen_tc_kernel(const __grid_constant__ CUtensorMap kmap,
         if (!simple && !valid) {
           // a V row that does not count: zero it once it has landed (the
           // pool, or what a slot held before, may be NaN there)
-          // (V(i)'s slot held K(i - 1), landed: S(i - 1) has run)
-          if (wait(full(slot_of(2 * i + 1)), use_of(2 * i + 1) & 1)) {
-            const uint32_t vb = ring + slot_of(2 * i + 1) * Sh::kSlotBytes + row * 128;
+          // (V(i)'s slot held K(i), landed: S(i) has run; or, for the last
+          // span, V(i - 2), landed: PV(i - 2) completed, waited for above)
+          if (wait(full(slot_of(vload(i))), use_of(vload(i)) & 1)) {
+            const uint32_t vb = ring + slot_of(vload(i)) * Sh::kSlotBytes + row * 128;
 #pragma unroll
             for (int h = 0; h < Sh::kHalves; ++h)
 #pragma unroll

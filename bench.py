@@ -83,52 +83,59 @@ N_SETS = 4  # default number of rotating pool sets (--sets)
 BASE_QKV_SEED = 20261210
 
 # DRAM bytes (read + write) of one decode launch on this workload, from the
-# ncu capture summarised in profiles/ (kernel source hash at capture time).
-# Reported as null when the kernels have changed since.
+# ncu capture summarised in profiles/ (the hash of the kernel's sources at
+# capture time: BASE_SOURCES, or TC_SOURCES for "sources": "tc").  Reported
+# as null when those sources have changed since.
 NCU_TRAFFIC = {
     # profiles/split_k.md: the long-context decode call, split-K phase 1
     # (10 splits, dram read 1,342,369,000 B + write 3,687,680 B) + the combine
     # (read 450,000 B)
-    "long": {"kernel_hash": "804b82c86616ebca", "bytes_per_launch": 1346506680, "num_splits": 10,
+    "long": {"kernel_hash": "b9835bf21d7ab40f", "bytes_per_launch": 1346506680, "num_splits": 10,
              "fused": False, "layout": "blocked",
              "kernel": "paged_decode_kernel<128,16,6,2,split> + splitk_combine_kernel<128>"},
     # profiles/split_k.md: the ragged decode call, phase 1 (8 splits, read
     # 810,120,448 B + write 6,809,856 B) + the combine (read 3,282,432 B)
-    "ragged": {"kernel_hash": "804b82c86616ebca", "bytes_per_launch": 820212736, "num_splits": 8,
+    "ragged": {"kernel_hash": "b9835bf21d7ab40f", "bytes_per_launch": 820212736, "num_splits": 8,
                "fused": False, "layout": "blocked",
                "kernel": "paged_decode_kernel<128,32,6,2,split> + splitk_combine_kernel<128>"},
     # profiles/decode_llama8b.md: the fused append + single-pass decode launch,
     # dram read 175,223,808 B + write 3,479,296 B
-    "llama8b": {"kernel_hash": "804b82c86616ebca", "bytes_per_launch": 178703104, "num_splits": 1,
+    "llama8b": {"kernel_hash": "b9835bf21d7ab40f", "bytes_per_launch": 178703104, "num_splits": 1,
                 "fused": True, "layout": "blocked",
                 "kernel": "paged_decode_kernel<128,16,6,2,single,fused>"},
     # profiles/varlen_spec.md: one paged_varlen_kernel launch (mma.sync),
     # read 174,706,176 B + write 3,722,240 B
-    "spec": {"kernel_hash": "804b82c86616ebca", "bytes_per_launch": 178428416, "num_splits": 1,
+    "spec": {"kernel_hash": "b9835bf21d7ab40f", "bytes_per_launch": 178428416, "num_splits": 1,
              "kernel": "paged_varlen_kernel<128,16,6,2,NT=2,blocked,single>"},
     # profiles/varlen_spec.md: one paged_varlen_tc_kernel launch (tcgen05),
     # read 174,747,904 B + write 3,599,872 B
-    "spec_tc": {"kernel_hash": "804b82c86616ebca", "bytes_per_launch": 178347776, "num_splits": 1,
+    "spec_tc": {"kernel_hash": "1a9d7de64e1d2231", "sources": "tc", "bytes_per_launch": 178347776, "num_splits": 1,
                 "kernel": "paged_varlen_tc_kernel<128,16,single>"},
     # profiles/varlen_spec_long.md: the varlen split-K phase 1 (10 splits,
     # read 1,342,483,000 B + write 3,526,912 B) + the combine (read 2,674,000 B)
-    "spec_long": {"kernel_hash": "804b82c86616ebca", "bytes_per_launch": 1348683912,
+    "spec_long": {"kernel_hash": "b9835bf21d7ab40f", "bytes_per_launch": 1348683912,
                   "num_splits": 10,
                   "kernel": "paged_varlen_kernel<128,16,6,2,NT=2,blocked,split> + "
                             "varlen_combine_kernel<128>"},
-    "spec_long_tc": {"kernel_hash": "804b82c86616ebca", "bytes_per_launch": 1348444960,
+    "spec_long_tc": {"kernel_hash": "1a9d7de64e1d2231", "sources": "tc", "bytes_per_launch": 1348444960,
                      "num_splits": 10,
                      "kernel": "paged_varlen_tc_kernel<128,16,split> + varlen_combine_kernel<128>"},
     # profiles/qkv_prefill.md: one qkv_norm_rope_kernel launch, dram read
     # 101,985,792 B + write 53,701,888 B (the rest of the writes stay in L2)
-    "qkv_prefill": {"kernel_hash": "804b82c86616ebca", "bytes_per_launch": 155687680,
+    "qkv_prefill": {"kernel_hash": "b9835bf21d7ab40f", "bytes_per_launch": 155687680,
                     "kernel": "qkv_norm_rope_kernel<128,16,3>"},
     # profiles/decode_llama8b.md (one-launch QKV step): the decode kernel with
     # the QKV norm + rotary + append folded in, dram read 175,240,192 B +
     # write 3,737,088 B
-    "step_qkv": {"kernel_hash": "804b82c86616ebca", "bytes_per_launch": 178977280,
+    "step_qkv": {"kernel_hash": "b9835bf21d7ab40f", "bytes_per_launch": 178977280,
                  "num_splits": 1, "kernel": "paged_decode_kernel<128,16,6,2,single,qkv>"},
 }
+
+
+def traffic_current(tr):
+    """Whether a traffic entry's kernel sources still hash as captured."""
+    files = TC_SOURCES if tr.get("sources") == "tc" else BASE_SOURCES
+    return tr.get("kernel_hash") == kernel_source_hash(files)
 
 
 def ncu_traffic(workload, num_splits=None):
@@ -136,18 +143,24 @@ def ncu_traffic(workload, num_splits=None):
     committed ncu capture, or None once the kernels have changed since (or
     the split count differs from the captured one)."""
     tr = NCU_TRAFFIC.get(workload)
-    if not tr or tr.get("kernel_hash") != kernel_source_hash():
+    if not tr or not traffic_current(tr):
         return None
     if "num_splits" in tr and num_splits != tr["num_splits"]:
         return None
     return tr["bytes_per_launch"]
 
 
-def kernel_source_hash():
-    """Hash of the CUDA sources with comments and blank lines left out (a
-    comment edit does not change a kernel; any code edit does)."""
+# The CUDA sources a kernel is built from: every kernel but the tcgen05 varlen
+# one (which adds varlen_tc.cuh) comes from these three.
+BASE_SOURCES = ("kernels.cuh", "ptx.cuh", "pagedkv.cu")
+TC_SOURCES = BASE_SOURCES + ("varlen_tc.cuh",)
+
+
+def kernel_source_hash(files=BASE_SOURCES):
+    """Hash of the given CUDA sources with comments and blank lines left out
+    (a comment edit does not change a kernel; any code edit does)."""
     h = hashlib.sha256()
-    for f in ("kernels.cuh", "ptx.cuh", "varlen_tc.cuh", "pagedkv.cu"):
+    for f in files:
         with open(os.path.join(ROOT, "paged_kv_decode_08_gb300", "csrc", f)) as fh:
             for line in fh:
                 code = line.split("//", 1)[0].strip()
@@ -819,7 +832,7 @@ def _measure_varlen(args, workload, tensor_path, pk, W, world, rank, local, dev)
     achieved = kv_bytes / (ms * 1e-3) / 1e9
     tc = tensor_path and v.max_q_len * G > 8 and w.head_dim == 128
     tr = NCU_TRAFFIC.get(workload + ("_tc" if tc else ""))
-    traffic = (tr["bytes_per_launch"] if tr and tr.get("kernel_hash") == kernel_source_hash()
+    traffic = (tr["bytes_per_launch"] if tr and traffic_current(tr)
                and S == tr.get("num_splits") else None)
     line = {
         "metric": METRIC, "value": job_throughput(kv_bytes, world, ms), "unit": UNIT,
@@ -1057,7 +1070,7 @@ def measure_step(args, name, dev, dist, world, rank, n_sets, want_e2e, want_cpu)
     peak, peak_kind = measured_peaks()
     traffic = None
     tr = NCU_TRAFFIC.get(name)
-    if (tr and tr.get("kernel_hash") == kernel_source_hash() and S == tr.get("num_splits")
+    if (tr and traffic_current(tr) and S == tr.get("num_splits")
             and one_launch == tr.get("fused", False) and tr.get("layout", "blocked") == args.layout):
         traffic = tr["bytes_per_launch"]
     cpu = cpu_baseline_subprocess(name) if want_cpu else None

@@ -52,11 +52,11 @@ def test_source_hash_ignores_comments_but_not_code(tmp_path, monkeypatch):
 
 def test_traffic_is_reported_only_for_the_captured_kernels(monkeypatch):
     entry = bench.NCU_TRAFFIC["llama8b"]
-    monkeypatch.setattr(bench, "kernel_source_hash", lambda: entry["kernel_hash"])
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda files=None: entry["kernel_hash"])
     assert bench.ncu_traffic("llama8b", entry["num_splits"]) == entry["bytes_per_launch"]
     assert bench.ncu_traffic("llama8b", entry["num_splits"] + 1) is None
     assert bench.ncu_traffic("no_such_workload", 1) is None
-    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "0" * 16)
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda files=None: "0" * 16)
     assert bench.ncu_traffic("llama8b", entry["num_splits"]) is None
 
 
@@ -65,3 +65,17 @@ def test_every_traffic_entry_is_a_plausible_capture():
         assert len(e["kernel_hash"]) == 16, name
         assert e["bytes_per_launch"] > 0, name
         assert e["kernel"], name
+
+
+def test_a_tcgen05_source_edit_leaves_the_other_kernels_traffic(tmp_path, monkeypatch):
+    """Only the tcgen05 varlen kernel is built from varlen_tc.cuh: editing it
+    changes that kernel's hash and no other."""
+    src = os.path.join(bench.ROOT, "paged_kv_decode_08_gb300", "csrc")
+    dst = tmp_path / "paged_kv_decode_08_gb300" / "csrc"
+    shutil.copytree(src, dst)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    base, tc = bench.kernel_source_hash(), bench.kernel_source_hash(bench.TC_SOURCES)
+    f = dst / "varlen_tc.cuh"
+    f.write_text(f.read_text() + "\nstatic const int pkv_extra_constant = 2;\n")
+    assert bench.kernel_source_hash() == base
+    assert bench.kernel_source_hash(bench.TC_SOURCES) != tc

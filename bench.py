@@ -108,17 +108,19 @@ NCU_TRAFFIC = {
     "spec": {"kernel_hash": "b9835bf21d7ab40f", "bytes_per_launch": 178428416, "num_splits": 1,
              "kernel": "paged_varlen_kernel<128,16,6,2,NT=2,blocked,single>"},
     # profiles/varlen_spec.md: one paged_varlen_tc_kernel launch (tcgen05),
-    # read 174,747,904 B + write 3,599,872 B
-    "spec_tc": {"kernel_hash": "1a9d7de64e1d2231", "sources": "tc", "bytes_per_launch": 178347776, "num_splits": 1,
-                "kernel": "paged_varlen_tc_kernel<128,16,single>"},
+    # read 174,750,720 B + write 3,690,496 B
+    "spec_tc": {"kernel_hash": "668072eb485127d9", "sources": "tc", "bytes_per_launch": 178441216,
+                "num_splits": 1, "kernel": "paged_varlen_tc_kernel<128,16,single>"},
     # profiles/varlen_spec_long.md: the varlen split-K phase 1 (10 splits,
     # read 1,342,483,000 B + write 3,526,912 B) + the combine (read 2,674,000 B)
     "spec_long": {"kernel_hash": "b9835bf21d7ab40f", "bytes_per_launch": 1348683912,
                   "num_splits": 10,
                   "kernel": "paged_varlen_kernel<128,16,6,2,NT=2,blocked,split> + "
                             "varlen_combine_kernel<128>"},
-    "spec_long_tc": {"kernel_hash": "1a9d7de64e1d2231", "sources": "tc", "bytes_per_launch": 1348444960,
-                     "num_splits": 10,
+    # profiles/varlen_spec_long.md: tcgen05 phase 1 (read 1,342,567,000 B +
+    # write 3,853,056 B) + the combine (read 2,675,000 B)
+    "spec_long_tc": {"kernel_hash": "668072eb485127d9", "sources": "tc",
+                     "bytes_per_launch": 1349095056, "num_splits": 10,
                      "kernel": "paged_varlen_tc_kernel<128,16,split> + varlen_combine_kernel<128>"},
     # profiles/qkv_prefill.md: one qkv_norm_rope_kernel launch, dram read
     # 101,985,792 B + write 53,701,888 B (the rest of the writes stay in L2)

@@ -1131,6 +1131,7 @@ def sub_record(line, name):
     return {"workload": line["config"]["workload"], "name": name,
             "num_splits": line["config"].get("num_splits"),
             "us_per_call": dec_us, "us_per_step": line["us_per_step"], "kv_bytes": kv,
+            "append_us_per_step": line.get("append_us_per_step"),
             "kv_gbs": kv / (dec_us * 1e-6) / 1e9,
             "frac": line["roofline"]["frac"], "frac_kernel": line["roofline"]["kernel"],
             "frac_of_decode_call": kv / (dec_us * 1e-6) / 1e9 / peak,

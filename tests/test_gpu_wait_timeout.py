@@ -1,7 +1,7 @@
 """The failure path on the GPU, without a fault: a wait that nothing will
 satisfy gives up after its 100 ms limit, flags PKV_DEV_WAIT_TIMEOUT and
 returns; while the flag is set every decode and varlen call (combine kernels
-included) writes nothing; reading the status clears it and the next calls
+and the tcgen05 varlen kernel included) writes nothing; reading the status clears it and the next calls
 are correct again (the context stayed usable)."""
 
 import time
@@ -48,12 +48,20 @@ def test_wait_timeout_is_flagged_and_nothing_is_written_until_cleared(pk, cuda_d
                       w.scale, out=outs[0])
         pk.pkv_decode_splitk(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
                              d["context_lens"], w.scale, num_splits=3, out=outs[1])
-        vouts = [torch.full_like(vq, sentinel) for _ in range(2)]
-        pk.pkv_varlen_attention(vq, dv["k_cache"], dv["v_cache"], cu, pos, dv["block_tables"],
-                                v.base.scale, max_q_len=3, out=vouts[0])
-        pk.pkv_varlen_attention_splitk(vq, dv["k_cache"], dv["v_cache"], cu, pos,
-                                       dv["block_tables"], v.base.scale, max_q_len=3,
-                                       num_splits=4, out=vouts[1])
+        # varlen on both kernels (12 columns per CTA: the tcgen05 one when selected)
+        vouts = [torch.full_like(vq, sentinel) for _ in range(4)]
+        prev = pk.pkv_set_varlen_tensor_path(0)
+        try:
+            for path in (0, 1):
+                pk.pkv_set_varlen_tensor_path(path)
+                pk.pkv_varlen_attention(vq, dv["k_cache"], dv["v_cache"], cu, pos,
+                                        dv["block_tables"], v.base.scale, max_q_len=3,
+                                        out=vouts[2 * path])
+                pk.pkv_varlen_attention_splitk(vq, dv["k_cache"], dv["v_cache"], cu, pos,
+                                               dv["block_tables"], v.base.scale, max_q_len=3,
+                                               num_splits=4, out=vouts[2 * path + 1])
+        finally:
+            pk.pkv_set_varlen_tensor_path(prev)
         torch.cuda.synchronize()
         for i, o in enumerate(outs + vouts):
             assert bool((o == sentinel).all()), f"call {i} wrote while the timeout flag was set"

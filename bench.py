@@ -64,6 +64,8 @@ WORKLOAD_DESC = {
              "8-block pool"),
     "spec": ("speculative-decode verification: B=32, H=32, Hkv=8, D=128, bs=16, 4 draft tokens "
              "per sequence over a prefix ~U[508,2044] (pkv_varlen_attention_splitk, causal)"),
+    "prefill": ("chunked prefill: B=4, H=32, Hkv=8, D=128, bs=16, 512 new tokens per sequence "
+                "after a 2048-token prefix, causal (pkv_varlen_attention_splitk; tensor-bound)"),
     "spec_long": ("speculative-decode verification over long contexts: B=4, H=32, Hkv=8, D=128, "
                   "bs=16, 4 draft tokens per sequence after prefixes {32768,65536,98304,131072}-4, "
                   "24576-block pool (pkv_varlen_attention_splitk, causal)"),
@@ -156,6 +158,7 @@ def ncu_traffic(workload, num_splits=None):
 # one (which adds varlen_tc.cuh) comes from these three.
 BASE_SOURCES = ("kernels.cuh", "ptx.cuh", "pagedkv.cu")
 TC_SOURCES = BASE_SOURCES + ("varlen_tc.cuh",)
+PREFILL_SOURCES = BASE_SOURCES + ("varlen_tc.cuh", "prefill_tc.cuh")
 
 
 def kernel_source_hash(files=BASE_SOURCES):
@@ -178,6 +181,18 @@ def measured_peaks():
             d = json.load(fh)
         return float(d["hbm_gbs"]), "measured"
     return 6800.0, "fallback"
+
+
+def measured_tensor_peak():
+    """Dense bf16 tensor TFLOP/s measured on this machine (a burst of cuBLAS
+    GEMMs); f16 runs at the same dense rate on these tensor cores."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            d = json.load(fh)
+        if "bf16_tflops" in d:
+            return float(d["bf16_tflops"]), "measured (bf16 burst; f16 dense rate is the same)"
+    return 1900.0, "fallback"
 
 
 class ClockSampler:
@@ -781,9 +796,11 @@ def measure_varlen(args, workload, tensor_path):
 
 
 def _measure_varlen(args, workload, tensor_path, pk, W, world, rank, local, dev):
+    import numpy as np
     import torch
 
-    v = W.spec_verify_long() if workload == "spec_long" else W.spec_verify()
+    v = {"spec_long": W.spec_verify_long, "prefill": W.prefill_chunk}.get(
+        workload, W.spec_verify)()
     w = v.base
     n_sets = args.sets or N_SETS
     sets = build_sets(w, dev, n_sets)
@@ -828,12 +845,14 @@ def _measure_varlen(args, workload, tensor_path, pk, W, world, rank, local, dev)
         return None
     kv_bytes = w.kv_bytes
     G = w.group
+    prefill = S == 1 and v.max_q_len * G >= 128 and w.head_dim == 128
     nt = 2 if v.max_q_len * G > 8 else 1
-    reads = -(-int(v.max_q_len) // max(1, 8 * nt // G))
+    per_cta = max(1, 128 // G) if prefill else max(1, 8 * nt // G)
+    reads = -(-int(v.max_q_len) // per_cta)
     peak, peak_kind = measured_peaks()
     achieved = kv_bytes / (ms * 1e-3) / 1e9
-    tc = tensor_path and v.max_q_len * G > 8 and w.head_dim == 128
-    tr = NCU_TRAFFIC.get(workload + ("_tc" if tc else ""))
+    tc = prefill or (tensor_path and v.max_q_len * G > 8 and w.head_dim == 128)
+    tr = NCU_TRAFFIC.get(workload + ("_tc" if tc and not prefill else ""))
     traffic = (tr["bytes_per_launch"] if tr and traffic_current(tr)
                and S == tr.get("num_splits") else None)
     line = {
@@ -843,7 +862,8 @@ def _measure_varlen(args, workload, tensor_path, pk, W, world, rank, local, dev)
         "data": "synthetic",
         "config": {"workload": WORKLOAD_DESC[workload], "launch": "CUDA graph, replayed",
                    "num_splits": S, "context_reads_per_call": reads,
-                   "kernel_path": "tcgen05" if tc else "mma.sync",
+                   "kernel_path": ("tcgen05 prefill" if prefill else
+                                   "tcgen05" if tc else "mma.sync"),
                    "l2": f"{n_sets} rotating pool sets; {reads * kv_bytes / 1e6:.0f} MB read per call"},
         "kv_bytes_per_step": kv_bytes, "us_per_step": ms * 1e3,
         "query_tokens_per_s": world * v.total_q / (ms * 1e-3),
@@ -857,6 +877,22 @@ def _measure_varlen(args, workload, tensor_path, pk, W, world, rank, local, dev)
         "clocks": clocks.summary(), "gpu_launches": rounds * n_sets * (2 if S > 1 else 1),
         "device_status_flags": pk.pkv_read_device_status(), "e2e": None, "cpu_baseline": None,
     }
+    if prefill:
+        # tensor-bound: causal attention flops (4 D per query, head and
+        # position it sees) over the measured dense f16/bf16 peak
+        lens = v.pos_offsets.astype(np.int64)
+        qls = np.diff(v.cu_seqlens_q).astype(np.int64)
+        pairs = int(sum(ql * (p0 + 1) + ql * (ql - 1) // 2 for p0, ql in zip(lens, qls)))
+        flops = 4.0 * w.head_dim * w.num_heads * pairs
+        tpeak, tkind = measured_tensor_peak()
+        tflops = flops / (ms * 1e-3) / 1e12
+        line["flops_per_step"] = flops
+        line["roofline"] = {
+            "bound": "tensor", "achieved": tflops, "peak": tpeak, "unit": "TFLOP/s",
+            "frac": tflops / tpeak, "peak_source": tkind,
+            "kernel": "paged_prefill_tc_kernel (algorithmic flops: the causal triangle, "
+                      "4 * head_dim per (query, head, position))",
+            "kv_gbs_contexts_once": achieved, "traffic": None}
     return line
 
 
@@ -1223,10 +1259,11 @@ def run_profile(args):
     torch.cuda.set_device(dev)
     n = args.ncu_calls
     pk.pkv_set_varlen_tensor_path(1 if args.varlen_tc else 0)
-    if args.workload in ("spec", "spec_long"):
+    if args.workload in ("spec", "spec_long", "prefill"):
         import dataclasses
 
-        v = W.spec_verify_long() if args.workload == "spec_long" else W.spec_verify()
+        v = {"spec_long": W.spec_verify_long, "prefill": W.prefill_chunk}.get(
+            args.workload, W.spec_verify)()
         v = dataclasses.replace(v, base=W.compact_pool(v.base))
         d = W.to_device(v.base, dev)
         q = torch.from_numpy(v.q).to(dev)
@@ -1321,7 +1358,7 @@ def main():
     if args.impl == "ours" and args.workload == "qkv_prefill":
         run_qkv(args)
         return
-    if args.impl == "ours" and args.workload in ("spec", "spec_long"):
+    if args.impl == "ours" and args.workload in ("spec", "spec_long", "prefill"):
         run_varlen(args)
         return
     if args.impl == "reference":

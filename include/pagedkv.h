@@ -218,9 +218,15 @@ pkv_status pkv_append_decode(const void* k_new, const void* v_new, const int32_t
  *   out           device f16 [total_q][num_heads][head_dim]
  *   other arguments as pkv_decode.
  *
- * One CTA covers max(1, 8 / group) queries of one sequence and KV head, so
- * each reads the context once per chunk of queries: meant for short query
- * runs (a few tokens per sequence), not long prompts.
+ * Two kernels serve it.  For short query runs (a few tokens per sequence)
+ * one CTA covers max(1, 8 / group) queries of one sequence and KV head and
+ * reads the context once per chunk of queries.  When max_q_len x group >=
+ * 128 at head_dim 128 on blocked pools (chunked prefill), the call runs the
+ * prefill kernel instead: one CTA per 128 / group queries of a sequence and
+ * KV head, both products on the 5th-generation tensor cores (tcgen05.mma,
+ * 128 (query, head) rows x 128-token spans, scores and output in tensor
+ * memory), one CTA per SM.  The two compute the same attention within the
+ * stated tolerance; arguments, flags and errors are the same.
  */
 pkv_status pkv_varlen_attention(const void* q, const void* k_cache, const void* v_cache,
                                 const int32_t* cu_seqlens_q, const int32_t* pos_offsets,

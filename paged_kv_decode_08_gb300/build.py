@@ -16,7 +16,7 @@ ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libpagedkv.so")
 SOURCES = [os.path.join(HERE, "csrc", "pagedkv.cu")]
 DEPS = SOURCES + [os.path.join(HERE, "csrc", f) for f in ("kernels.cuh", "ptx.cuh",
-                                                              "varlen_tc.cuh")] + [
+                                                              "varlen_tc.cuh", "prefill_tc.cuh")] + [
     os.path.join(ROOT, "include", "pagedkv.h")]
 
 

@@ -19,6 +19,7 @@
 
 #include "kernels.cuh"
 #include "pagedkv.h"
+#include "prefill_tc.cuh"
 #include "varlen_tc.cuh"
 
 // Warps per decode CTA and the shared-memory ring they split (KB); the
@@ -38,6 +39,11 @@
 // pools, head_dim 128) when 1, on the mma.sync kernel when 0.
 #ifndef PKV_VARLEN_TC
 #define PKV_VARLEN_TC 0
+#endif
+// Varlen attention (blocked pools, head_dim 128, no split) on the tcgen05
+// prefill kernel once a sequence brings at least 128 (query, head) rows.
+#ifndef PKV_PREFILL_TC
+#define PKV_PREFILL_TC 1
 #endif
 
 
@@ -448,6 +454,31 @@ pkv_status launch_varlen_tc(const DecodeArgs& a, const VarlenParams& vp, cudaStr
 
 std::atomic<int> g_varlen_tc{PKV_VARLEN_TC};
 
+template <int BS>
+pkv_status launch_prefill_tc(const DecodeArgs& a, const VarlenParams& vp, cudaStream_t stream,
+                             int grid) {
+  using Sh = TcPrefillShape;
+  auto kernel = paged_prefill_tc_kernel<BS>;
+  static std::atomic<unsigned long long> attr_set{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (!(attr_set.load(std::memory_order_relaxed) & bit)) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::kSmemBytes);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(prefill tc)");
+    attr_set.fetch_or(bit, std::memory_order_relaxed);
+  }
+  CUtensorMap kmap, vmap;
+  pkv_status st = make_half_box_map(&kmap, a.k_cache, a.num_blocks, a.num_kv_heads, BS, 128);
+  if (st != PKV_OK) return st;
+  st = make_half_box_map(&vmap, a.v_cache, a.num_blocks, a.num_kv_heads, BS, 128);
+  if (st != PKV_OK) return st;
+  e = launch_pdl(kernel, grid, Sh::kThreads, Sh::kSmemBytes, stream, kmap, vmap, vp);
+  if (e != cudaSuccess) return cuda_fail(e, "varlen attention (tcgen05 prefill) launch");
+  return PKV_OK;
+}
+
 template <bool SPLIT>
 pkv_status dispatch_varlen(const DecodeArgs& a, const VarlenParams& vp, cudaStream_t cs, int grid,
                            int NT, bool vllm) {
@@ -841,6 +872,16 @@ pkv_status varlen_impl(const void* q, const void* k_cache, const void* v_cache,
   st = resolve_varlen_splits(num_seqs, num_heads, num_kv_heads, max_q_len, max_blocks_per_seq,
                              block_size, num_splits, &S_eff);
   if (st != PKV_OK) return st;
+  if (S_eff <= 1 && PKV_PREFILL_TC && !vllm && head_dim == 128 &&
+      (long long)max_q_len * G >= TcPrefillShape::kRows) {
+    // tiles of 128 / G queries: 128 (query, head) rows per CTA
+    vp.qc = TcPrefillShape::kRows / G;
+    vp.num_chunks = (max_q_len + vp.qc - 1) / vp.qc;
+    const long long pgrid = (long long)num_seqs * num_kv_heads * vp.num_chunks;
+    if (pgrid >= (1ll << 31)) return fail(PKV_ERR_INVALID_ARG, "grid too large");
+    return block_size == 16 ? launch_prefill_tc<16>(a, vp, cs, (int)pgrid)
+                            : launch_prefill_tc<32>(a, vp, cs, (int)pgrid);
+  }
   if (S_eff <= 1) return dispatch_varlen<false>(a, vp, cs, (int)grid, NT, vllm);
 
   const size_t need = pkv_splitk_scratch_bytes(total_q, num_heads, head_dim, S_eff);

@@ -10,14 +10,15 @@
 //   S  [128 tok x 16]  = K_span [128 x 128] . Q^T              (M = 128, tensor memory)
 //   O^T[128 d x 16]   += V_span^T [128 x 128] . P^T [128 x 16]  (M = 128, tensor memory)
 //
-// Warp roles (192 threads).  Warp 4 (one lane) copies each span's K and V
-// (eight 16-row sub-tiles per tensor, one TMA box per 64-element half,
-// landing as [2 halves][128 rows][64] with the 128-byte swizzle: the K-major
-// and MN-major shared-memory layouts of the two MMAs) into a ring of three
-// 32 KB slots taken in the order K0, K1, V0, K2, V1, ... (a span's V goes out
-// after the next span's K, so that it is in flight while the span's scores
-// and softmax run rather than held in a slot); a K slot is released when S
-// has read it, a V slot when PV has.  Warp 5 (one lane) issues each
+// Warp roles.  Warps 5 .. copy each span's K and V (eight 16-row sub-tiles
+// per tensor, one TMA box per 64-element half, each warp issuing its share
+// of the 16 boxes, one per lane, landing as [2 halves][128 rows][64] with
+// the 128-byte swizzle: the K-major and MN-major shared-memory layouts of
+// the two MMAs) into a ring of three 32 KB slots taken in the order K0, K1,
+// V0, K2, V1, ... (a span's V goes out after the next span's K, so that it
+// is in flight while the span's scores and softmax run rather than held in
+// a slot); a K slot is released when S has read it, a V slot when PV has.
+// Warp 4 (one lane) issues each
 // product as soon as its inputs are ready (S is double-buffered in tensor
 // memory, so the next span's scores are computed during this span's
 // softmax).  Warps 0-3 run the online softmax: lane l of warp w owns token
@@ -37,6 +38,13 @@
 #pragma once
 
 #include "kernels.cuh"
+
+// Warps that issue the copies (each takes 16 / n of a load's boxes): a warp
+// issues TMA boxes at a bounded rate, so the copies of one CTA go faster
+// when several warps share them.
+#ifndef PKV_TC_COPY_WARPS
+#define PKV_TC_COPY_WARPS 2
+#endif
 
 // Sleep (ns) between polls of the copy and MMA threads; 0 spins.
 #ifndef PKV_TC_POLL_NS
@@ -64,7 +72,13 @@ struct TcVarlenShape {
   static constexpr int kNumBars = 14;
   static constexpr int kSmemBytes = 1024 + kBarOff + kNumBars * 8;
   static constexpr int kTmemCols = 64;  // S[2] (16 columns each), O (16)
-  static constexpr int kThreads = 192;  // softmax warps 0-3, copy warp 4, MMA warp 5
+  static constexpr int kMmaWarp = 4;     // softmax warps 0-3, MMA warp 4, copy warps 5 ..
+  static constexpr int kCopyWarps = PKV_TC_COPY_WARPS;
+  static constexpr int kBoxesPerWarp = 2 * kSubs / kCopyWarps;
+  static_assert(kHalves == 2 && kBoxesPerWarp % 2 == 0 && kBoxesPerWarp * kCopyWarps == 2 * kSubs,
+                "each copy warp takes whole sub-tiles");
+  static constexpr int kWarps = kMmaWarp + 1 + kCopyWarps;
+  static constexpr int kThreads = kWarps * 32;
   static constexpr uint32_t kIdescS = mma_idesc_f16(128, 16, false, false);
   static constexpr uint32_t kIdescPV = mma_idesc_f16(128, 16, true, false);
 };
@@ -91,7 +105,7 @@ paged_varlen_tc_kernel(const __grid_constant__ CUtensorMap kmap,
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_abort;
   __shared__ uint32_t s_tmem;
-  __shared__ int s_max[6];
+  __shared__ int s_max[Sh::kWarps];
   __shared__ float s_red[2][4][16];             // column maxima per warp (double-buffered)
   __shared__ float s_sum[4][16];                // final column sums per warp
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -125,10 +139,10 @@ paged_varlen_tc_kernel(const __grid_constant__ CUtensorMap kmap,
 
   pdl_launch_dependents();
   if (threadIdx.x == 0) s_abort = 0;
-  if (warp == 4 && lane == 0) {
+  if (warp == Sh::kMmaWarp && lane == 0) {
 #pragma unroll
     for (int i = 0; i < 3; ++i) {
-      mbar_init(full(i), 1);
+      mbar_init(full(i), Sh::kCopyWarps);  // one arrival (with its bytes) per copy warp
       mbar_init(empty(i), 1);
     }
 #pragma unroll
@@ -164,7 +178,7 @@ paged_varlen_tc_kernel(const __grid_constant__ CUtensorMap kmap,
   int nblk_max = 0;
   if (SPLIT) {
 #pragma unroll
-    for (int w = 0; w < 6; ++w) nblk_max = max(nblk_max, s_max[w]);
+    for (int w = 0; w < Sh::kWarps; ++w) nblk_max = max(nblk_max, s_max[w]);
   }
   const int chunk = SPLIT ? max(p.min_chunk_blocks, (nblk_max + p.num_splits - 1) / p.num_splits)
                           : p.max_blocks_per_seq;
@@ -245,83 +259,80 @@ paged_varlen_tc_kernel(const __grid_constant__ CUtensorMap kmap,
     return true;
   };
 
-  if (warp == 4) {
-    // ================= copies (warp 4, lane 0) =================
-    if (lane == 0) {
-      // the block-table entries of span i's sub-tiles (-1: no data)
-      auto lookup = [&](int i, int (&phys)[Sh::kSubs]) {
-#pragma unroll
-        for (int u = 0; u < Sh::kSubs; ++u) {
-          const int t = i * Sh::kSubs + u;
-          phys[u] = t < n_tiles ? __ldg(table + (sub_begin + t) / SUB) : -1;
-        }
-      };
-      int issued = 0;
-      // the entries of the span being loaded, the next span's (looked up a
-      // span ahead), and the validated entries of the last two spans' K
-      // loads (their V loads follow one K later)
-      int phys[Sh::kSubs], nxt[Sh::kSubs], ph0[Sh::kSubs], ph1[Sh::kSubs];
-      lookup(0, nxt);
-      for (int n = 0; n < 2 * n_spans; ++n) {
-        const bool last = n == 2 * n_spans - 1;
-        const bool is_v = last || (n > 0 && !(n & 1));
-        const int i = last ? n_spans - 1 : (is_v ? n / 2 - 1 : (n + 1) / 2);
-        if (!is_v) {
-#pragma unroll
-          for (int u = 0; u < Sh::kSubs; ++u) phys[u] = nxt[u];
-          if (i + 1 < n_spans) lookup(i + 1, nxt);  // in flight during the waits below
-        } else {
-#pragma unroll
-          for (int u = 0; u < Sh::kSubs; ++u) phys[u] = (i & 1) ? ph1[u] : ph0[u];
-        }
-        // the slot's previous load (n - 3) must have been released
-        const int slot = slot_of(n);
-        const uint32_t use = use_of(n);
+  if (warp > Sh::kMmaWarp) {
+    // ================= copies (warps 5 ..) =================
+    // A load is 16 boxes (8 sub-tiles x 2 halves).  Copy warp c issues boxes
+    // c B .. c B + B - 1 (B = 16 / copy warps), one per lane (box 2u + h:
+    // sub-tile u, half h).  Every copy warp walks the whole load sequence:
+    // its lane 0 waits for the slot itself and arrives on the slot's full
+    // barrier with the bytes of its own boxes before any of them is issued.
+    const int box = (warp - Sh::kMmaWarp - 1) * Sh::kBoxesPerWarp + lane;
+    const int u = box >> 1, hh = box & 1;
+    const bool boxer = lane < Sh::kBoxesPerWarp;
+    // this lane's table entry for span i (-1: no data)
+    auto lookup = [&](int i) {
+      const int t = i * Sh::kSubs + u;
+      return (boxer && t < n_tiles) ? __ldg(table + (sub_begin + t) / SUB) : -1;
+    };
+    int issued = 0;
+    // the entry of the span being loaded, the next span's (a span ahead), and
+    // the validated entries of the last two spans' K loads (their V loads
+    // follow one K later)
+    int nxt = lookup(0), e0 = -1, e1 = -1;
+    for (int n = 0; n < 2 * n_spans; ++n) {
+      const bool last = n == 2 * n_spans - 1;
+      const bool is_v = last || (n > 0 && !(n & 1));
+      const int i = last ? n_spans - 1 : (is_v ? n / 2 - 1 : (n + 1) / 2);
+      int e;
+      if (!is_v) {
+        e = nxt;
+        if (i + 1 < n_spans) nxt = lookup(i + 1);  // in flight during the wait below
+      } else {
+        e = (i & 1) ? e1 : e0;
+      }
+      // the slot's previous load (n - 3) must have been released
+      const int slot = slot_of(n);
+      const uint32_t use = use_of(n);
+      bool go = true;
+      if (lane == 0) {
         if (use >= 1 && !(PKV_TC_POLL_NS ? mbar_wait_backoff(empty(slot), (use - 1) & 1,
                                                            kWaitLimitNs, PKV_TC_POLL_NS)
                                         : mbar_wait_bounded(empty(slot), (use - 1) & 1,
                                                             kWaitLimitNs))) {
           abort_now();
-          break;
+          go = false;
         }
-        if (aborted()) break;
-        if (!is_v) {
-#pragma unroll
-          for (int u = 0; u < Sh::kSubs; ++u) {
-            if (phys[u] >= p.num_blocks || (phys[u] < 0 && i * Sh::kSubs + u < n_tiles)) {
-              atomicOr(&g_device_status, kDevBadBlockId);
-              phys[u] = -1;
-            }
-            if (i & 1)
-              ph1[u] = phys[u];
-            else
-              ph0[u] = phys[u];
-          }
-        }
-        int n_ok = 0;
-#pragma unroll
-        for (int u = 0; u < Sh::kSubs; ++u) n_ok += phys[u] >= 0;
-        const uint32_t dst = ring + slot * Sh::kSlotBytes;
-        mbar_arrive_expect_tx(full(slot), (uint32_t)(n_ok * Sh::kHalves * 2048));
-#pragma unroll
-        for (int u = 0; u < Sh::kSubs; ++u) {
-          if (phys[u] < 0) continue;
-          const int t = sub_begin + i * Sh::kSubs + u;
-          const int tile = phys[u] * p.num_kv_heads + g;
-          const int row0 = (t % SUB) * 16;
-#pragma unroll
-          for (int h = 0; h < Sh::kHalves; ++h)
-            tma_load_4d(dst + h * Sh::kHalfBytes + u * 2048, is_v ? &vmap : &kmap, full(slot), 0,
-                        row0, h, tile);
-        }
-        issued = n + 1;
+        go = go && !aborted();
       }
-      // every started copy lands before the CTA can exit (bounded)
+      if (!__shfl_sync(0xffffffffu, go, 0)) break;
+      if (!is_v) {
+        const int t = i * Sh::kSubs + u;
+        if (boxer && (e >= p.num_blocks || (e < 0 && t < n_tiles))) {
+          if (hh == 0) atomicOr(&g_device_status, kDevBadBlockId);
+          e = -1;
+        }
+        if (i & 1)
+          e1 = e;
+        else
+          e0 = e;
+      }
+      const uint32_t ok = __ballot_sync(0xffffffffu, boxer && e >= 0);
+      const uint32_t dst = ring + slot * Sh::kSlotBytes;
+      if (lane == 0) mbar_arrive_expect_tx(full(slot), (uint32_t)(__popc(ok) * 2048));
+      __syncwarp();
+      if (boxer && e >= 0) {
+        const int t = sub_begin + i * Sh::kSubs + u;
+        tma_load_4d(dst + hh * Sh::kHalfBytes + u * 2048, is_v ? &vmap : &kmap, full(slot), 0,
+                    (t % SUB) * 16, hh, e * p.num_kv_heads + g);
+      }
+      issued = n + 1;
+    }
+    // every started copy lands before the CTA can exit (bounded)
+    if (lane == 0)
       for (int n = max(0, issued - Sh::kSlots); n < issued; ++n)
         (void)mbar_wait_bounded(full(slot_of(n)), use_of(n) & 1, kWaitLimitNs);
-    }
-  } else if (warp == 5) {
-    // ================= MMAs (warp 5, lane 0) =================
+  } else if (warp == Sh::kMmaWarp) {
+    // ================= MMAs (warp 4, lane 0) =================
     if (lane == 0) {
       uint32_t last_bar = 0, last_phase = 0;  // the last commit (drained before exit)
       // Issue whichever product is ready.  PV products go in span order (the

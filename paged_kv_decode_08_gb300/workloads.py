@@ -542,6 +542,12 @@ def spec_verify_long() -> VarlenWorkload:
     return varlen_random(BASE_SEED + 6, 32, 8, 128, 16, [4] * 4, prefix, num_blocks=24576)
 
 
+def prefill_chunk() -> VarlenWorkload:
+    """Chunked prefill on the Llama-3-8B attention shape: B=4 sequences, 512
+    new tokens each after a 2048-token prefix (H=32, Hkv=8, D=128, bs=16)."""
+    return varlen_random(BASE_SEED + 7, 32, 8, 128, 16, [512] * 4, [2048] * 4)
+
+
 def spec_verify() -> VarlenWorkload:
     """Speculative-decode verification on the Llama-3-8B attention shape:
     B=32, H=32, Hkv=8, D=128, bs=16, 4 draft tokens per sequence over a

@@ -601,6 +601,76 @@ def test_varlen_kernels_agree(pk, cuda_device):
     assert pk.pkv_read_device_status() == 0
 
 
+# chunked prefill: at least 128 (query, head) rows per sequence at head_dim
+# 128 run the tcgen05 prefill kernel (tiles of 128 / G queries)
+@pytest.mark.parametrize("H,Hkv,bs,q_lens,prefix", [
+    (32, 8, 16, [256, 100, 1, 0, 37], [300, 0, 513, 7, 2000]),   # G=4: 32-query tiles
+    (8, 8, 32, [130, 129, 3], [0, 64, 1000]),                      # G=1: 128-query tiles
+    (28, 4, 16, [40, 19], [100, 5]),                               # G=7: 18 queries, 2 idle rows
+    (16, 2, 16, [33, 16], [50, 0]),                                # G=8: 16-query tiles
+    (4, 2, 32, [70, 64, 1], [17, 0, 300]),                         # G=2: 64-query tiles
+])
+def test_prefill_matches_oracle(pk, cuda_device, H, Hkv, bs, q_lens, prefix):
+    v = W.varlen_random(3400 + H + bs + len(q_lens), H, Hkv, 128, bs, q_lens, prefix)
+    kc, vc = W.host_pool(v.base)
+    ref = oracle.varlen(v.q, kc, vc, v.cu_seqlens_q, v.pos_offsets, v.base.block_tables,
+                        v.base.scale)
+    d = varlen_device(v, cuda_device)
+    for label, call in (("single", lambda: pk.pkv_varlen_attention(
+            d["q"], d["k_cache"], d["v_cache"], d["cu"], d["pos"], d["block_tables"],
+            v.base.scale, max_q_len=v.max_q_len)),
+                        ("splitk heuristic", lambda: pk.pkv_varlen_attention_splitk(
+            d["q"], d["k_cache"], d["v_cache"], d["cu"], d["pos"], d["block_tables"],
+            v.base.scale, max_q_len=v.max_q_len, num_splits=0))):
+        out = call()
+        torch.cuda.synchronize()
+        assert_attention_close(to_np(out), ref, f"prefill {label} H{H} Hkv{Hkv} bs{bs}")
+    assert pk.pkv_read_device_status() == 0
+
+
+@pytest.mark.parametrize("scale_mul", [-1.0, 0.0])
+def test_prefill_nonpositive_scale(pk, cuda_device, scale_mul):
+    """A negative or zero scale (the maximum of the scaled scores is then not
+    the raw maximum scaled): softmax(scale q.k) as defined."""
+    v = W.varlen_random(3450, 32, 8, 128, 16, [200, 64], [400, 0])
+    kc, vc = W.host_pool(v.base)
+    scale = scale_mul * v.base.scale
+    ref = oracle.varlen(v.q, kc, vc, v.cu_seqlens_q, v.pos_offsets, v.base.block_tables, scale)
+    d = varlen_device(v, cuda_device)
+    out = pk.pkv_varlen_attention(d["q"], d["k_cache"], d["v_cache"], d["cu"], d["pos"],
+                                  d["block_tables"], scale, max_q_len=v.max_q_len)
+    torch.cuda.synchronize()
+    assert_attention_close(to_np(out), ref, f"prefill scale x{scale_mul}")
+    assert pk.pkv_read_device_status() == 0
+
+
+def test_prefill_bad_block_id_is_skipped_and_flagged(pk, cuda_device):
+    """A table entry outside the pool inside a prefill tile's context: its 16
+    positions are left out and flagged, the other sequence is untouched."""
+    v = W.varlen_random(3500, 8, 2, 128, 16, [64, 40], [200, 30])
+    kc, vc = W.host_pool(v.base)
+    ref = oracle.varlen(v.q, kc, vc, v.cu_seqlens_q, v.pos_offsets, v.base.block_tables,
+                        v.base.scale)
+    d = varlen_device(v, cuda_device)
+    tables = v.base.block_tables.copy()
+    tables[0, 5] = v.base.num_blocks + 3  # positions 80..95 of sequence 0
+    d["block_tables"] = torch.from_numpy(tables).to(cuda_device)
+    out = to_np(pk.pkv_varlen_attention(d["q"], d["k_cache"], d["v_cache"], d["cu"], d["pos"],
+                                        d["block_tables"], v.base.scale, max_q_len=64))
+    assert pk.pkv_read_device_status() & pk.PKV_DEV_BAD_BLOCK_ID
+    assert np.all(np.isfinite(out))
+    assert_attention_close(out[64:], ref[64:], "untouched sequence")
+    K = v.base.seq_k[0].astype(np.float64)
+    V = v.base.seq_v[0].astype(np.float64)
+    for t in (0, 17, 63):
+        keep = [j for j in range(200 + t + 1) if not 80 <= j < 96]
+        for h in range(8):
+            z = v.base.scale * K[keep, h // 4] @ v.q[t, h].astype(np.float64)
+            p = np.exp(z - z.max())
+            p /= p.sum()
+            assert_attention_close(out[t, h], p @ V[keep, h // 4], f"query {t} head {h}")
+
+
 def test_varlen_flags_bad_query_ranges(pk, cuda_device):
     v = W.varlen_random(3200, 4, 2, 64, 16, [2, 2], [5, 5])
     d = varlen_device(v, cuda_device)

@@ -874,8 +874,8 @@ pkv_status varlen_impl(const void* q, const void* k_cache, const void* v_cache,
   if (st != PKV_OK) return st;
   if (S_eff <= 1 && PKV_PREFILL_TC && !vllm && head_dim == 128 &&
       (long long)max_q_len * G >= TcPrefillShape::kRows) {
-    // tiles of 128 / G queries: 128 (query, head) rows per CTA
-    vp.qc = TcPrefillShape::kRows / G;
+    // pairs of tiles of 128 / G queries: 2 x 128 (query, head) rows per CTA
+    vp.qc = TcPrefillShape::kTiles * (TcPrefillShape::kRows / G);
     vp.num_chunks = (max_q_len + vp.qc - 1) / vp.qc;
     const long long pgrid = (long long)num_seqs * num_kv_heads * vp.num_chunks;
     if (pgrid >= (1ll << 31)) return fail(PKV_ERR_INVALID_ARG, "grid too large");

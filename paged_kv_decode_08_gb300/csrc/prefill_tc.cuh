@@ -3,30 +3,35 @@
 // sequence brings at least 128 (query, head) rows), with both products on
 // the 5th-generation tensor cores, head_dim 128.
 //
-// One CTA per (sequence, KV head, tile of Q_T = 128 / G queries); its 128
-// rows r = (query r / G, head r % G) (rows past the tile's queries hold zero
-// queries) are the M of both MMAs per span of 128 context tokens:
+// One CTA per (sequence, KV head, pair of query tiles).  A tile holds
+// Q_T = 128 / G queries: its 128 rows r = (query r / G, head r % G) (rows
+// past the tile's queries hold zero queries) are the M of both products of
+// every span of 128 context tokens:
 //
-//   S[128 rows x 128 tok] = Q [128 x 128 d] . K_span^T       (K-major A and B)
-//   O[128 rows x 128 d]  += P [128 x 128 tok] . V_span        (K-major A, MN-major B)
+//   S_X[128 rows x 128 tok] = Q_X [128 x 128 d] . K_span^T     (K-major A and B)
+//   O_X[128 rows x 128 d]  += P_X [128 x 128 tok] . V_span     (K-major A, MN-major B)
 //
-// both accumulated in tensor memory (S double-buffered, 2 x 128 columns; O
-// 128 columns).  Warps 9 .. copy K and V as the tcgen05 varlen kernel does
-// (16-row sub-tiles, one TMA box per 64-element half, a ring of three 32 KB
-// slots in the order K0, K1, V0, K2, V1, ...), each warp issuing its share
-// of a load's 16 boxes, one per lane.  Warp 8 (one lane) issues each
-// product once its inputs are ready.  Warps 0-7 run the
-// online softmax with two threads per row (tensor-memory lane r = row r;
-// warps w and w + 4 share a lane quarter and take one half of the span's
-// tokens each): a thread loads its half of the row of S, the two halves
-// exchange their maxima through shared memory, and each keeps the row's
-// reference maximum, which moves only when a score exceeds it by 2^8 (then
-// its half of the row of O is rescaled in tensor memory), writes its half of
-// the row of P (f16) to shared memory as the K-major A operand of the second
-// product, and adds the exponentials to its share of the row's sum.  Positions
-// past a query's causal limit get P = 0; V rows of positions that count for
-// no row (past the tile's last query, or in a sub-tile whose table entry is
-// out of range) are zeroed before PV, since 0 x NaN would poison it.
+// for tiles X = A, B.  The two tiles share each K/V span, so a span's bytes
+// feed twice the products of one tile, and the tiles take turns on the
+// tensor cores: while one tile's softmax runs, the other's products do.
+// Tensor memory holds S and O of each tile (4 x 128 columns); shared memory
+// the ring, Q and P of each tile (225 KB).
+//
+// Warp roles (416 threads).  Warps 9-12 copy K and V into a ring of three
+// 32 KB slots in the order K0, K1, V0, K2, V1, ... (16-row sub-tiles, one TMA
+// box per 64-element half, each warp issuing its share of a load's 16 boxes,
+// one per lane: a warp issues boxes at a bounded rate).  Warp 8 (one lane)
+// issues each product once its inputs are ready.  Warps 0-3 run the online
+// softmax of tile A and warps 4-7 that of tile B, one thread per row
+// (tensor-memory lane r), over the span in two chunks of 64 tokens: the
+// thread loads a chunk of its row of S, keeps the row's reference maximum,
+// which moves only when a score exceeds it by 2^8 (then the row of O, and
+// the first chunk's P when the second chunk moves it, are rescaled), writes
+// the chunk of its row of P (f16) to shared memory as the K-major A operand
+// of the second product, and adds the exponentials to the row's sum.  Positions past a query's causal limit get
+// P = 0; V rows of positions that count for no row (past the pair's last
+// query, or in a sub-tile whose table entry is out of range) are zeroed
+// before PV, since 0 x NaN would poison it.
 //
 // Every wait is bounded; a wait that runs out sets PKV_DEV_WAIT_TIMEOUT and
 // the CTA stops, lets its copies and MMAs drain (bounded as well), writes
@@ -35,23 +40,16 @@
 
 #include "varlen_tc.cuh"
 
-// Warps that issue the copies (each takes 16 / n of a load's boxes): a warp
-// issues TMA boxes at a bounded rate, so the copies of one CTA go faster
-// when several warps share them.
+// Warps that issue the copies (each takes 16 / n of a load's boxes).
 #ifndef PKV_PREFILL_COPY_WARPS
 #define PKV_PREFILL_COPY_WARPS 4
-#endif
-
-// Sleep (ns) between idle polls of the MMA thread (0: spin); it shares a
-// warp scheduler with two softmax warps.
-#ifndef PKV_PREFILL_MMA_POLL_NS
-#define PKV_PREFILL_MMA_POLL_NS 0
 #endif
 
 namespace pkv {
 
 struct TcPrefillShape {
   static constexpr int D = 128;
+  static constexpr int kTiles = 2;                    // query tiles per CTA
   static constexpr int kRows = 128;                   // (query, head) rows per tile: M
   static constexpr int kSpan = 128;                   // context tokens per span: N of S
   static constexpr int kSubs = kSpan / 16;            // 16-row sub-tiles per span
@@ -59,24 +57,24 @@ struct TcPrefillShape {
   static constexpr int kSlotBytes = 2 * kHalfBytes;   // K (or V) of a span: 32 KB
   static constexpr int kSlots = 3;
   static constexpr int kRingBytes = kSlots * kSlotBytes;  // 96 KB
-  static constexpr int kQBytes = 2 * kRows * 128;         // Q [d halves][128 rows][64]: 32 KB
-  static constexpr int kPBytes = 2 * kRows * 128;         // P [token halves][128 rows][64]
+  static constexpr int kQBytes = 2 * kRows * 128;         // Q_X [d halves][128 rows][64]: 32 KB
+  static constexpr int kPBytes = 2 * kRows * 128;  // P_X [token halves][128 rows][64]: 32 KB
   static constexpr int kQOff = kRingBytes;
-  static constexpr int kPOff = kQOff + kQBytes;           // two P buffers
-  static constexpr int kBarOff = kPOff + 2 * kPBytes;
-  // full[3], empty[3], s_ready[2], s_free[2], p_ready[2], pv_done[2]
-  static constexpr int kNumBars = 14;
-  static constexpr int kSmemBytes = 1024 + kBarOff + kNumBars * 8;  // ~193 KB: one CTA per SM
-  static constexpr int kTmemCols = 512;  // S[2] (128 columns each), O (128)
-  static constexpr int kSoftWarps = 8;   // two per tensor-memory lane quarter
-  static constexpr int kMmaWarp = 8;
-  static constexpr int kCopyWarps = PKV_PREFILL_COPY_WARPS;  // warps 9 ..
+  static constexpr int kPOff = kQOff + kTiles * kQBytes;  // P [tile]
+  static constexpr int kBarOff = kPOff + kTiles * kPBytes;
+  // full[3], empty[3], then per tile s_ready, s_free, p_ready, pv_done
+  static constexpr int kNumBars = 6 + kTiles * 4;
+  static constexpr int kSmemBytes = 1024 + kBarOff + kNumBars * 8;  // ~225 KB: one CTA per SM
+  static constexpr int kTmemCols = 512;  // S [tile] (128 columns each), O [tile] (128)
+  static constexpr int kSoftWarps = 4 * kTiles;  // one thread per row of each tile
+  static constexpr int kMmaWarp = kSoftWarps;
+  static constexpr int kCopyWarps = PKV_PREFILL_COPY_WARPS;  // warps kMmaWarp + 1 ..
   static constexpr int kBoxesPerWarp = 2 * kSubs / kCopyWarps;
-  static_assert(kBoxesPerWarp % 2 == 0 && kBoxesPerWarp * kCopyWarps == 2 * kSubs,
-                "each copy warp takes whole sub-tiles");
+  static_assert(kBoxesPerWarp >= 1 && kBoxesPerWarp * kCopyWarps == 2 * kSubs,
+                "the copy warps share a load's boxes evenly");
   static constexpr int kThreads = (kMmaWarp + 1 + kCopyWarps) * 32;
-  static constexpr uint32_t kIdescS = mma_idesc_f16(128, 128, false, false);
-  static constexpr uint32_t kIdescPV = mma_idesc_f16(128, 128, false, true);
+  static constexpr uint32_t kIdescS = mma_idesc_f16(kRows, kSpan, false, false);
+  static constexpr uint32_t kIdescPV = mma_idesc_f16(kRows, D, false, true);
 };
 
 template <int BS>
@@ -96,10 +94,11 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
   const uint32_t bars = ring + Sh::kBarOff;
   auto full = [&](int i) { return bars + 8 * i; };
   auto empty = [&](int i) { return bars + 8 * (3 + i); };
-  auto s_ready = [&](int i) { return bars + 8 * (6 + i); };
-  auto s_free = [&](int i) { return bars + 8 * (8 + i); };
-  auto p_ready = [&](int i) { return bars + 8 * (10 + i); };
-  auto pv_done = [&](int i) { return bars + 8 * (12 + i); };
+  // per tile X: one phase per span
+  auto s_ready = [&](int X) { return bars + 8 * (6 + 4 * X); };
+  auto s_free = [&](int X) { return bars + 8 * (7 + 4 * X); };
+  auto p_ready = [&](int X) { return bars + 8 * (8 + 4 * X); };
+  auto pv_done = [&](int X) { return bars + 8 * (9 + 4 * X); };
   // Ring loads in issue order: K0, then K(i+1), V(i) for each span i, V of
   // the last span last; load n goes to slot n % 3, its (n / 3)-th use.
   auto slot_of = [](int n) { return n % Sh::kSlots; };
@@ -108,14 +107,15 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // the tile index is the slowest and runs backwards: the tiles with the
+  // the pair index is the slowest and runs backwards: the pairs with the
   // most positions (the latest queries) start first, the short ones last
-  const int per_tile = gridDim.x / p.num_chunks;  // sequences x KV heads
-  const int qt = p.num_chunks - 1 - (int)blockIdx.x / per_tile;
-  const int item = (int)blockIdx.x % per_tile;
+  const int per_pair = gridDim.x / p.num_chunks;  // sequences x KV heads
+  const int qt = p.num_chunks - 1 - (int)blockIdx.x / per_pair;
+  const int item = (int)blockIdx.x % per_pair;
   const int g = item % p.num_kv_heads;
   const int s = item / p.num_kv_heads;
   const int G = p.group;
+  const int QT = p.qc / Sh::kTiles;  // queries per tile (128 / G)
 
   pdl_launch_dependents();
   if (threadIdx.x == 0) s_abort = 0;
@@ -126,17 +126,17 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
       mbar_init(empty(i), 1);
     }
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(s_ready(i), 1);
-      mbar_init(s_free(i), Sh::kSoftWarps);
-      mbar_init(p_ready(i), Sh::kSoftWarps);
-      mbar_init(pv_done(i), 1);
+    for (int X = 0; X < Sh::kTiles; ++X) {
+      mbar_init(s_ready(X), 1);
+      mbar_init(s_free(X), 4);
+      mbar_init(p_ready(X), 4);
+      mbar_init(pv_done(X), 1);
     }
     fence_mbar_init();
   }
   pdl_wait();
 
-  // ---- the tile of queries and the positions it reads (as paged_varlen_kernel)
+  // ---- the queries of the pair and the positions they read (as paged_varlen_kernel)
   const unsigned int status = *reinterpret_cast<volatile unsigned int*>(&g_device_status);
   const int cap = p.max_blocks_per_seq * BS;
   const int q_begin = __ldg(p.cu_seqlens_q + s);
@@ -157,35 +157,39 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
     if (threadIdx.x == 0) atomicOr(&g_device_status, kDevBadContextLen);
     pos0 = pos0 < 0 ? 0 : max(0, cap - q_len);
   }
-  const int tok_end = min(cap, pos0 + t0 + nq);  // >= 1: the last query's limit
-  const int nrows = nq * G;                       // <= 128
+  const int tok_end = min(cap, pos0 + t0 + nq);  // >= 1: the pair's last query's limit
   const int n_tiles = (tok_end + 15) / 16;
   const int n_spans = (n_tiles + Sh::kSubs - 1) / Sh::kSubs;  // >= 1
+  // tile B holds queries only when the pair has more than Q_T of them
+  const int ntile = nq > QT ? 2 : 1;
   const int32_t* table = p.block_tables + (size_t)s * p.max_blocks_per_seq;
   auto kload = [&](int j) { return j == 0 ? 0 : 2 * j - 1; };                        // K(j)'s load
   auto vload = [&](int i) { return i == n_spans - 1 ? 2 * n_spans - 1 : 2 * i + 2; };  // V(i)'s
 
   // ---- set-up: tensor memory, the queries as the A operand of S
   if (warp == 0) tmem_alloc(smem_addr(&s_tmem), Sh::kTmemCols);
-  if (warp < 4) {
-    // row r = threadIdx.x (warps 0-3): query t0 + r / G, head g G + r % G (zeros past nrows),
-    // 16 chunks of 16 bytes into [d halves][128 rows][64] with the swizzle
-    const int r = threadIdx.x;
+  if (warp < Sh::kSoftWarps) {
+    // thread = (tile X, row r): query t0 + X Q_T + r / G, head g G + r % G
+    // (zeros past the tile's rows), 16 chunks of 16 bytes into
+    // [d halves][128 rows][64] with the swizzle
+    const int X = threadIdx.x / Sh::kRows, r = threadIdx.x % Sh::kRows;
+    const int nrows = max(0, min(QT, nq - X * QT)) * G;
     const bool live = r < nrows;
-    const size_t row = (size_t)(q_begin + t0 + (live ? r / G : 0)) * p.num_heads + (size_t)g * G +
-                       (live ? r % G : 0);
+    const size_t row = (size_t)(q_begin + t0 + X * QT + (live ? r / G : 0)) * p.num_heads +
+                       (size_t)g * G + (live ? r % G : 0);
     const uint4* src = reinterpret_cast<const uint4*>(p.q + row * Sh::D);
+    const uint32_t qx = qbuf + X * Sh::kQBytes;
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
       const uint4 v = live ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
-      const uint32_t dst = qbuf + (c / 8) * (Sh::kRows * 128) + sw128_off(r, (c % 8) * 8);
+      const uint32_t dst = qx + (c / 8) * (Sh::kRows * 128) + sw128_off(r, (c % 8) * 8);
       asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v.x), "r"(v.y),
                    "r"(v.z), "r"(v.w)
                    : "memory");
     }
     fence_proxy_async_smem();
   }
-  // whether any table entry the tile reads is out of range (the copies skip
+  // whether any table entry the pair reads is out of range (the copies skip
   // such sub-tiles; the softmax then masks them span by span)
   bool bad_entry = false;
   for (int t = threadIdx.x; t * SUB < n_tiles; t += Sh::kThreads) {
@@ -196,8 +200,8 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
   const bool any_bad = __syncthreads_or(bad_entry);
   tc_fence_after();
   const uint32_t tbase = s_tmem;
-  const uint32_t tS = tbase;         // S buffers: columns 0..127 and 128..255
-  const uint32_t tO = tbase + 256;   // O: columns 256..383
+  auto tS = [&](int X) { return tbase + (uint32_t)(X * 128); };
+  auto tO = [&](int X) { return tbase + 256u + (uint32_t)(X * 128); };
 
   auto abort_now = [&]() {
     atomicOr(&g_device_status, kDevWaitTimeout);
@@ -285,66 +289,87 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
     // ================= MMAs (warp 8, lane 0) =================
     if (lane == 0) {
       uint32_t last_bar = 0, last_phase = 0;  // the last commit (drained before exit)
-      // Issue whichever product is ready.  PV products go in span order (the
-      // softmax warps rescale O between them) and need P and V; S(j) needs
-      // K(j) and S buffer j % 2 read by the softmax warps (span j - 2).
+      // Issue whichever product is ready.  S products go in order S_A(j),
+      // S_B(j), S_A(j+1), ...; PV products in order PV_A(i), PV_B(i), ...
+      // (the softmax warps rescale O between them).  S_X(j) needs K(j) and
+      // S_X(j - 1) read by the softmax warps of tile X; PV_X(i) needs P_X(i)
+      // and V(i).
       // A barrier's phase is tested by its parity alone, so a test must not
-      // run while the slot's previous load can still be in flight: K(j)'s
-      // slot held V(j - 3) (K0 for j = 2), landed once PV(j - 3) was issued;
-      // V(i)'s slot held K(i) (V(i - 2) for the last span), landed before S(i)
-      // (or PV(i - 2)) was issued.
-      int next_s = 0, next_pv = 0;
+      // run while the phase two back can still be pending: K(j)'s slot held
+      // V(j - 3) (K0 for j = 2), landed once PV(j - 3) was issued (the gate
+      // j <= next_pv + 2) or, for K0, before S(0); V(i)'s slot held K(i)
+      // (V(i - 2) for the last span), landed before S(i) (or PV(i - 2)) was
+      // issued, and V(i) is tested only once P_A(i) is ready (after S(i));
+      // s_free, p_ready: the span before was waited on before the product
+      // that followed it.
+      int next_s = 0, sx = 0, next_pv = 0, px = 0;
       uint64_t t_last = global_timer_ns();
       int idle = 0;
       while (next_pv < n_spans) {
         bool progressed = false;
-        const int i = next_pv;
-        const int vs = slot_of(vload(i));
-        if (mbar_test(p_ready(i & 1), (i >> 1) & 1) && mbar_test(full(vs), use_of(vload(i)) & 1)) {
-          tc_fence_after();
-          const uint32_t vb = ring + vs * Sh::kSlotBytes;
-          const uint32_t pb = pbuf + (i & 1) * Sh::kPBytes;
+        {
+          const int i = next_pv, X = px;
+          const int vs = slot_of(vload(i));
+          if (mbar_test(p_ready(X), i & 1) &&
+              (X > 0 || mbar_test(full(vs), use_of(vload(i)) & 1))) {
+            tc_fence_after();
+            const uint32_t vb = ring + vs * Sh::kSlotBytes;
+            const uint32_t pb = pbuf + X * Sh::kPBytes;
 #pragma unroll
-          for (int ks = 0; ks < Sh::kSpan / 16; ++ks) {
-            // P: K-major over the span's tokens; V: MN-major (d contiguous),
-            // its two d halves kHalfBytes apart, 8-token groups 1 KB apart
-            const uint64_t a = smem_desc_sw128(pb + (ks / 4) * (Sh::kRows * 128) + (ks % 4) * 32,
-                                               16, 1024);
-            const uint64_t b = smem_desc_sw128(vb + ks * 2048, Sh::kHalfBytes, 1024);
-            tc_mma_f16(tO, a, b, Sh::kIdescPV, (i > 0 || ks > 0) ? 1u : 0u);
+            for (int ks = 0; ks < Sh::kSpan / 16; ++ks) {
+              // P: K-major over the span's tokens; V: MN-major (d contiguous),
+              // its two d halves kHalfBytes apart, 8-token groups 1 KB apart
+              const uint64_t a =
+                  smem_desc_sw128(pb + (ks / 4) * (Sh::kRows * 128) + (ks % 4) * 32, 16, 1024);
+              const uint64_t b = smem_desc_sw128(vb + ks * 2048, Sh::kHalfBytes, 1024);
+              tc_mma_f16(tO(X), a, b, Sh::kIdescPV, (i > 0 || ks > 0) ? 1u : 0u);
+            }
+            tc_commit(pv_done(X));
+            last_bar = pv_done(X);
+            last_phase = i & 1;
+            if (X + 1 == ntile) {
+              tc_commit(empty(vs));
+              ++next_pv;
+              px = 0;
+            } else {
+              ++px;
+            }
+            progressed = true;
           }
-          tc_commit(empty(vs));
-          tc_commit(pv_done(i & 1));
-          last_bar = pv_done(i & 1);
-          last_phase = (i >> 1) & 1;
-          ++next_pv;
-          progressed = true;
         }
-        const int j = next_s;
-        const int ks_slot = slot_of(kload(j));
-        if (j < n_spans && j <= next_pv + 2 && mbar_test(full(ks_slot), use_of(kload(j)) & 1) &&
-            (j < 2 || mbar_test(s_free(j & 1), ((j - 2) >> 1) & 1))) {
-          tc_fence_after();
-          const uint32_t kb = ring + ks_slot * Sh::kSlotBytes;
+        {
+          const int j = next_s, X = sx;
+          const int ks_slot = slot_of(kload(j));
+          if (j < n_spans && j <= next_pv + 2 &&
+              (X > 0 || mbar_test(full(ks_slot), use_of(kload(j)) & 1)) &&
+              (j < 1 || mbar_test(s_free(X), (j - 1) & 1))) {
+            tc_fence_after();
+            const uint32_t kb = ring + ks_slot * Sh::kSlotBytes;
+            const uint32_t qx = qbuf + X * Sh::kQBytes;
 #pragma unroll
-          for (int ks = 0; ks < Sh::D / 16; ++ks) {
-            const int h = ks / 4, w4 = ks % 4;
-            const uint64_t a = smem_desc_sw128(qbuf + h * (Sh::kRows * 128) + w4 * 32, 16, 1024);
-            const uint64_t b = smem_desc_sw128(kb + h * Sh::kHalfBytes + w4 * 32, 16, 1024);
-            tc_mma_f16(tS + (j & 1) * 128, a, b, Sh::kIdescS, ks > 0);
+            for (int ks = 0; ks < Sh::D / 16; ++ks) {
+              const int h = ks / 4, w4 = ks % 4;
+              const uint64_t a = smem_desc_sw128(qx + h * (Sh::kRows * 128) + w4 * 32, 16, 1024);
+              const uint64_t b = smem_desc_sw128(kb + h * Sh::kHalfBytes + w4 * 32, 16, 1024);
+              tc_mma_f16(tS(X), a, b, Sh::kIdescS, ks > 0);
+            }
+            tc_commit(s_ready(X));
+            last_bar = s_ready(X);
+            last_phase = j & 1;
+            if (X + 1 == ntile) {
+              tc_commit(empty(ks_slot));
+              ++next_s;
+              sx = 0;
+            } else {
+              ++sx;
+            }
+            progressed = true;
           }
-          tc_commit(empty(ks_slot));
-          tc_commit(s_ready(j & 1));
-          last_bar = s_ready(j & 1);
-          last_phase = (j >> 1) & 1;
-          ++next_s;
-          progressed = true;
         }
         if (progressed) {
           idle = 0;
         } else {
           if (aborted()) break;
-          if (PKV_PREFILL_MMA_POLL_NS > 0) __nanosleep(PKV_PREFILL_MMA_POLL_NS);
           // the clock is read once every 64 idle polls (it is slow to read)
           if ((++idle & 63) == 0) {
             const uint64_t t = global_timer_ns();
@@ -360,34 +385,29 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
       // every issued product completes before tensor memory is freed
       if (last_bar) (void)mbar_wait_bounded(last_bar, last_phase, kWaitLimitNs);
     }
-  } else {
-    // ============ softmax warps 0..7: two threads per row ============
-    // Warps w and w + 4 share tensor-memory lanes 32 (w % 4) .. + 31 (rows);
-    // `hf` = w / 4 picks the half of the span's tokens a thread handles (and
-    // the half of O's columns it rescales and writes).  A row's two halves
-    // exchange their maxima through shared memory once per span, and their
-    // sums at the end.  The warps never leave the span loop early: on an
-    // abort they skip the work but still pass every barrier among them.
-    __shared__ float s_mx[2][2][Sh::kRows];  // [span parity][half][row]
-    __shared__ float s_l[2][Sh::kRows];      // final sums [half][row]
-    const int hf = warp >> 2;
-    const int r = 32 * (warp & 3) + lane;    // this thread's row (tensor-memory lane)
+  } else if (warp < Sh::kSoftWarps && (warp >> 2) < ntile) {
+    // ============ softmax warps: tile X = warp / 4, one thread per row ============
+    // Every wait is bounded; on an abort a warp skips the work but still
+    // walks its spans (no barrier among the softmax warps depends on it).
+    const int X = warp >> 2;
+    const int r = 32 * (warp & 3) + lane;  // this thread's row (tensor-memory lane)
+    const int nrows = max(0, min(QT, nq - X * QT)) * G;
     const bool live = r < nrows;
-    const int lim = live ? pos0 + t0 + r / G + 1 : 0;  // positions below it count
-    // positions below this count for every row (the first query's limit)
-    const int all_see = min(tok_end, pos0 + t0 + 1);
+    const int qx0 = t0 + X * QT;  // the tile's first query
+    const int lim = live ? pos0 + qx0 + r / G + 1 : 0;  // positions below it count
+    // positions below this count for every row of the tile (its first query's limit)
+    const int all_see = min(tok_end, pos0 + qx0 + 1);
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-    constexpr int kSoftThreads = Sh::kSoftWarps * 32;
     // Lazy rescaling: the row's reference maximum moves only when a score
     // exceeds it by more than 2^kLazy, so P stays <= 2^kLazy (exact in f16,
-    // and the running sum and O scale together, cancelling in O / l).  Both
-    // threads of a row take the same decisions from the same maxima.
+    // and the running sum and O scale together, cancelling in O / l).
     constexpr float kLazy = 8.f;
+    constexpr uint32_t kAllOk = (1u << Sh::kSubs) - 1;
     const float sl2 = p.scale_log2;
     float m_run = -CUDART_INF_F, l_run = 0.f;
     // which sub-tiles of span i hold data (bit u; the copy warps skip, and
     // flag, a sub-tile whose table entry is out of range), read a span ahead
-    // when the tile reads any such entry (else every sub-tile holds data;
+    // when the pair reads any such entry (else every sub-tile holds data;
     // those past the last position are masked by the causal limit)
     auto span_ok = [&](int i) {
       uint32_t bits = 0;
@@ -399,162 +419,202 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
       }
       return bits;
     };
-    uint32_t ok_next = any_bad ? span_ok(0) : 0xFFu;
+    uint32_t ok_next = any_bad ? span_ok(0) : kAllOk;
     bool dead = false;
+    // O is rescaled (rows of this warp that moved their reference) once
+    // PV_X(i-1) completed (waited before the first chunk's P is written)
+    auto rescale_o = [&](float alpha) {
+      tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < Sh::D / 16; ++c) {
+        uint32_t o[16];
+        const uint32_t ta = tO(X) + c * 16 + lane_base;
+        tmem_ld16(ta, o);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+        tmem_st16(ta, o);
+      }
+    };
     for (int i = 0; i < n_spans; ++i) {
-      const int b = i & 1;
       const uint32_t okb = ok_next;
       if (any_bad && i + 1 < n_spans) ok_next = span_ok(i + 1);
       dead = dead || aborted();
-      if (!dead && !wait(s_ready(b), (i >> 1) & 1)) dead = true;
+      if (!dead && !wait(s_ready(X), i & 1)) dead = true;
       dead = __any_sync(0xffffffffu, dead);  // warp-uniform before the .sync.aligned loads
-      uint32_t ra[64];                       // this row's scores, tokens 64 hf .. 64 hf + 63
-      if (!dead) {
-        tc_fence_after();
-        tmem_ld64(tS + b * 128 + hf * 64 + lane_base, ra);
-        tc_fence_before();
-      } else {
-#pragma unroll
-        for (int j = 0; j < 64; ++j) ra[j] = 0u;
-      }
-      __syncwarp();
-      if (!dead && lane == 0) mbar_arrive(s_free(b));
       const int span0 = i * Sh::kSpan;
-      const int tok0 = span0 + hf * 64;  // this thread's first position
-      // every position of the span counts for every row: no masks
-      const bool simple = okb == 0xFFu && span0 + Sh::kSpan <= all_see;
-      // this half's maximum in the log2 domain; the exponents below are
-      // fma(ra, mul, -mu).  With no masks and a positive scale the scores
-      // stay raw (scaling by a positive factor keeps their order, so the
-      // scaled maximum is the raw one scaled); else they are scaled (and
-      // masked) in place.
+      // every position of the span counts for every row of the tile: no masks
+      const bool simple = okb == kAllOk && span0 + Sh::kSpan <= all_see;
+      // The scores are taken in two chunks of 64 tokens.  Each chunk's
+      // maximum (log2 domain) may move the row's reference; P of a chunk is
+      // written against the reference at that time, so when the second
+      // chunk moves it the first chunk's P is rescaled in shared memory.
+      // With no masks and a positive scale the scores stay raw (scaling by a
+      // positive factor keeps their order, so the scaled maximum is the raw
+      // one scaled) and each exponent is fma(s, scale log2 e, -mu); else
+      // they are scaled (and masked) in place.  Four independent
+      // three-input max chains; four independent partial sums.
       const bool raw = simple && sl2 > 0.f;
       const float mul = raw ? sl2 : 1.f;
-      float mx = -CUDART_INF_F;
-      if (raw) {
-#pragma unroll
-        for (int j = 0; j < 64; ++j) mx = fmaxf(mx, __uint_as_float(ra[j]));
-        mx *= sl2;
-      } else if (simple) {
-#pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          const float x = __uint_as_float(ra[j]) * sl2;
-          ra[j] = __float_as_uint(x);
-          mx = fmaxf(mx, x);
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          const bool ok = ((okb >> ((hf * 64 + j) >> 4)) & 1u) && tok0 + j < lim;
-          const float x = ok ? __uint_as_float(ra[j]) * sl2 : -CUDART_INF_F;
-          ra[j] = __float_as_uint(x);
-          mx = fmaxf(mx, x);
-        }
-      }
-      // the row's maximum: this half's and the other's
-      s_mx[b][hf][r] = mx;
-      named_barrier(1, kSoftThreads);
-      mx = fmaxf(mx, s_mx[b][hf ^ 1][r]);
-      const bool grow =
-          mx > m_run + kLazy || (m_run == -CUDART_INF_F && mx != -CUDART_INF_F);
-      float alpha = 1.f;
-      if (grow) {
-        alpha = m_run == -CUDART_INF_F ? 0.f : ex2_approx(m_run - mx);
-        m_run = mx;
-        l_run *= alpha;
-      }
-      const float mu = m_run == -CUDART_INF_F ? 0.f : m_run;
-      // P buffer b was read by PV(i-2); O changes only after PV(i-1)
-      if (!dead && i >= 2 && !wait(pv_done(b), ((i - 2) >> 1) & 1)) dead = true;
-      if (__any_sync(0xffffffffu, grow && i >= 1)) {
-        // some row of this warp moved its maximum: rescale this warp's half
-        // of those rows of O (alpha = 1 for the others) once PV(i-1) completed
-        if (!dead && !wait(pv_done((i - 1) & 1), ((i - 1) >> 1) & 1)) dead = true;
-        dead = __any_sync(0xffffffffu, dead);
+      const uint32_t pb = pbuf + X * Sh::kPBytes;
+#pragma unroll 1
+      for (int ch = 0; ch < 2; ++ch) {
+        uint32_t ra[64];  // this row's scores, tokens 64 ch .. 64 ch + 63 of the span
+        dead = __any_sync(0xffffffffu, dead);  // warp-uniform before the .sync.aligned loads
         if (!dead) {
           tc_fence_after();
-#pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            uint32_t o[16];
-            const uint32_t ta = tO + hf * 64 + c * 16 + lane_base;
-            tmem_ld16(ta, o);
+          tmem_ld64(tS(X) + ch * 64 + lane_base, ra);
+          tc_fence_before();
+        } else {
 #pragma unroll
-            for (int k = 0; k < 16; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-            tmem_st16(ta, o);
+          for (int j = 0; j < 64; ++j) ra[j] = 0u;
+        }
+        if (ch == 1) {
+          // S_X(i) is read: the next span's scores may go in
+          __syncwarp();
+          if (!dead && lane == 0) mbar_arrive(s_free(X));
+        }
+        const int tok0 = span0 + ch * 64;
+        float m4[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
+        if (raw) {
+#pragma unroll
+          for (int j = 0; j < 64; j += 2)
+            m4[(j >> 1) & 3] = fmax3(m4[(j >> 1) & 3], __uint_as_float(ra[j]),
+                                     __uint_as_float(ra[j + 1]));
+        } else if (simple) {
+#pragma unroll
+          for (int j = 0; j < 64; j += 2) {
+            const float x0 = __uint_as_float(ra[j]) * sl2, x1 = __uint_as_float(ra[j + 1]) * sl2;
+            ra[j] = __float_as_uint(x0);
+            ra[j + 1] = __float_as_uint(x1);
+            m4[(j >> 1) & 3] = fmax3(m4[(j >> 1) & 3], x0, x1);
           }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 64; j += 2) {
+            float x[2];
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              const bool ok = ((okb >> ((ch * 64 + j + k) >> 4)) & 1u) && tok0 + j + k < lim;
+              x[k] = ok ? __uint_as_float(ra[j + k]) * sl2 : -CUDART_INF_F;
+              ra[j + k] = __float_as_uint(x[k]);
+            }
+            m4[(j >> 1) & 3] = fmax3(m4[(j >> 1) & 3], x[0], x[1]);
+          }
+        }
+        float mx = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
+        if (raw) mx *= sl2;
+        const bool grow =
+            mx > m_run + kLazy || (m_run == -CUDART_INF_F && mx != -CUDART_INF_F);
+        float alpha = 1.f;
+        if (grow) {
+          alpha = m_run == -CUDART_INF_F ? 0.f : ex2_approx(m_run - mx);
+          m_run = mx;
+          l_run *= alpha;
+        }
+        const float mu = m_run == -CUDART_INF_F ? 0.f : m_run;
+        // P_X and O_X were last read by PV_X(i-1)
+        if (ch == 0 && !dead && i >= 1 && !wait(pv_done(X), (i - 1) & 1)) dead = true;
+        if (__any_sync(0xffffffffu, grow)) {
+          dead = __any_sync(0xffffffffu, dead);
+          if (!dead && i >= 1) rescale_o(alpha);  // O holds products from span 1 on
+          if (!dead && ch == 1 && grow) {
+            // the first chunk's P was written against the old reference
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const uint32_t a = pb + sw128_off(r, c * 8);
+              uint32_t w[4];
+              asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                           : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                           : "r"(a)
+                           : "memory");
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+                const __half2 h2 = __floats2half2_rn(f.x * alpha, f.y * alpha);
+                w[e] = *reinterpret_cast<const uint32_t*>(&h2);
+              }
+              asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(w[0]),
+                           "r"(w[1]), "r"(w[2]), "r"(w[3])
+                           : "memory");
+            }
+          }
+        }
+        if (!dead) {
+          // this chunk of the row of P (f16), [token half ch][128 rows][64],
+          // K-major with the swizzle; the running sum adds the same exponentials
+          const uint32_t pc = pb + ch * (Sh::kRows * 128);
+          float l4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int j = c * 8 + 2 * e;
+              const float p0 = ex2_approx(fmaf(__uint_as_float(ra[j]), mul, -mu));
+              const float p1 = ex2_approx(fmaf(__uint_as_float(ra[j + 1]), mul, -mu));
+              l4[e] += p0 + p1;
+              const __half2 h2 = __floats2half2_rn(p0, p1);
+              w[e] = *reinterpret_cast<const uint32_t*>(&h2);
+            }
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(pc + sw128_off(r, c * 8)),
+                         "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
+                         : "memory");
+          }
+          l_run += (l4[0] + l4[1]) + (l4[2] + l4[3]);
         }
       }
-      if (!dead) {
-        // this half of the row of P (f16), [token half][128 rows][64 tokens],
-        // K-major with the swizzle; the running sum adds the same exponentials
-        const uint32_t pb = pbuf + b * Sh::kPBytes + hf * (Sh::kRows * 128);
+      // V row r of the span (tile A's threads): zero it when its position
+      // counts for no row of the pair (past the pair's last query, or in a
+      // sub-tile with no data) once it has landed.  PV_B(i) is issued after
+      // PV_A(i), so after this.  V(i)'s slot held K(i) (V(i - 2) for the last
+      // span), landed before S(i) (or PV(i - 2), completed: PV_A(i-1) was
+      // waited above).  Tile A's simple spans hold no such position.
+      const int tok = span0 + r;
+      if (!dead && X == 0 && !simple && (!((okb >> (r >> 4)) & 1u) || tok >= tok_end)) {
+        if (wait(full(slot_of(vload(i))), use_of(vload(i)) & 1)) {
+          const uint32_t vb = ring + slot_of(vload(i)) * Sh::kSlotBytes + r * 128;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint32_t w[4];
+          for (int h = 0; h < 2; ++h)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int j = c * 8 + 2 * e;
-            const float p0 = ex2_approx(fmaf(__uint_as_float(ra[j]), mul, -mu));
-            const float p1 = ex2_approx(fmaf(__uint_as_float(ra[j + 1]), mul, -mu));
-            l_run += p0 + p1;
-            const __half2 h2 = __floats2half2_rn(p0, p1);
-            w[e] = *reinterpret_cast<const uint32_t*>(&h2);
-          }
-          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(pb + sw128_off(r, c * 8)),
-                       "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
-                       : "memory");
-        }
-        // V row r of the span (threads of half 0): zero it when its position
-        // counts for no row (past the tile's last query, or in a sub-tile with
-        // no data) once it has landed; V(i)'s slot held K(i) (V(i - 2) for the
-        // last span), landed before S(i) (or PV(i - 2), completed above)
-        const int tok = span0 + r;
-        if (hf == 0 && !simple && (!((okb >> (r >> 4)) & 1u) || tok >= tok_end)) {
-          if (wait(full(slot_of(vload(i))), use_of(vload(i)) & 1)) {
-            const uint32_t vb = ring + slot_of(vload(i)) * Sh::kSlotBytes + r * 128;
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-#pragma unroll
-              for (int c = 0; c < 8; ++c)
-                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(
-                                 vb + h * Sh::kHalfBytes + c * 16),
-                             "r"(0)
-                             : "memory");
-          }
+            for (int c = 0; c < 8; ++c)
+              asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(
+                               vb + h * Sh::kHalfBytes + c * 16),
+                           "r"(0)
+                           : "memory");
         }
       }
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (!dead && lane == 0) mbar_arrive(p_ready(b));
+      if (!dead && lane == 0) mbar_arrive(p_ready(X));
     }
-    // ---- the result: this half of the row of O over the row's sum
+    // ---- the result: the row of O over the row's sum
     const int last = n_spans - 1;
-    if (!dead && !wait(pv_done(last & 1), (last >> 1) & 1)) dead = true;
+    if (!dead && !wait(pv_done(X), last & 1)) dead = true;
     dead = __any_sync(0xffffffffu, dead);
-    s_l[hf][r] = l_run;
-    named_barrier(1, kSoftThreads);  // every softmax warp has seen the end (or the abort)
     const bool write = !dead && !aborted();
     if (__any_sync(0xffffffffu, write)) {
       tc_fence_after();
-      const float den = s_l[0][r] + s_l[1][r];
-      const float inv = den > 0.f ? 1.f / den : 0.f;
-      const size_t orow = (size_t)(q_begin + t0 + (live ? r / G : 0)) * p.num_heads +
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      const size_t orow = (size_t)(q_begin + qx0 + (live ? r / G : 0)) * p.num_heads +
                           (size_t)g * G + (live ? r % G : 0);
-      uint4* dst = reinterpret_cast<uint4*>(p.out + orow * Sh::D + hf * 64);
-      uint32_t o[64];
-      tmem_ld64(tO + hf * 64 + lane_base, o);
-      if (write && live) {
+      uint4* dst = reinterpret_cast<uint4*>(p.out + orow * Sh::D);
+#pragma unroll 1
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t o[64];
+        tmem_ld64(tO(X) + hf * 64 + lane_base, o);
+        if (write && live) {
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint32_t w[4];
+          for (int c = 0; c < 8; ++c) {
+            uint32_t w[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const __half2 h2 = __floats2half2_rn(__uint_as_float(o[c * 8 + 2 * e]) * inv,
-                                                 __uint_as_float(o[c * 8 + 2 * e + 1]) * inv);
-            w[e] = *reinterpret_cast<const uint32_t*>(&h2);
+            for (int e = 0; e < 4; ++e) {
+              const __half2 h2 = __floats2half2_rn(__uint_as_float(o[c * 8 + 2 * e]) * inv,
+                                                   __uint_as_float(o[c * 8 + 2 * e + 1]) * inv);
+              w[e] = *reinterpret_cast<const uint32_t*>(&h2);
+            }
+            dst[hf * 8 + c] = make_uint4(w[0], w[1], w[2], w[3]);
           }
-          dst[c] = make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
     }

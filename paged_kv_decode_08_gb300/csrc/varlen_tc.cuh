@@ -89,6 +89,13 @@ __device__ __forceinline__ uint32_t sw128_off(int row, int e) {
   return (uint32_t)(row * 128 + ((((e >> 3) ^ (row & 7))) << 4) + (e & 7) * 2);
 }
 
+// max(a, b, c) in one instruction (the three-input form of max.f32).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float y;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
+  return y;
+}
+
 // 2^x by the hardware approximation (x <= 8 here; -inf gives 0).
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;

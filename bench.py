@@ -86,59 +86,65 @@ BASE_QKV_SEED = 20261210
 
 # DRAM bytes (read + write) of one decode launch on this workload, from the
 # ncu capture summarised in profiles/ (the hash of the kernel's sources at
-# capture time: BASE_SOURCES, or TC_SOURCES for "sources": "tc").  Reported
-# as null when those sources have changed since.
+# capture time: BASE_SOURCES, TC_SOURCES for "sources": "tc", PREFILL_SOURCES
+# for "sources": "prefill").  Reported as null when those sources have
+# changed since.
 NCU_TRAFFIC = {
     # profiles/split_k.md: the long-context decode call, split-K phase 1
-    # (10 splits, dram read 1,342,369,000 B + write 3,687,680 B) + the combine
-    # (read 450,000 B)
-    "long": {"kernel_hash": "b9835bf21d7ab40f", "bytes_per_launch": 1346506680, "num_splits": 10,
+    # (10 splits, dram read 1,342,344,704 B + write 3,127,552 B) + the combine
+    # (read 449,536 B)
+    "long": {"kernel_hash": "a7a592997aa82f34", "bytes_per_launch": 1345921792, "num_splits": 10,
              "fused": False, "layout": "blocked",
              "kernel": "paged_decode_kernel<128,16,6,2,split> + splitk_combine_kernel<128>"},
     # profiles/split_k.md: the ragged decode call, phase 1 (8 splits, read
-    # 810,120,448 B + write 6,809,856 B) + the combine (read 3,282,432 B)
-    "ragged": {"kernel_hash": "b9835bf21d7ab40f", "bytes_per_launch": 820212736, "num_splits": 8,
+    # 810,103,552 B + write 6,965,760 B) + the combine (read 3,282,432 B +
+    # write 2,048 B)
+    "ragged": {"kernel_hash": "a7a592997aa82f34", "bytes_per_launch": 820353792, "num_splits": 8,
                "fused": False, "layout": "blocked",
                "kernel": "paged_decode_kernel<128,32,6,2,split> + splitk_combine_kernel<128>"},
     # profiles/decode_llama8b.md: the fused append + single-pass decode launch,
-    # dram read 175,223,808 B + write 3,479,296 B
-    "llama8b": {"kernel_hash": "b9835bf21d7ab40f", "bytes_per_launch": 178703104, "num_splits": 1,
+    # dram read 175,224,320 B + write 3,510,528 B
+    "llama8b": {"kernel_hash": "a7a592997aa82f34", "bytes_per_launch": 178734848, "num_splits": 1,
                 "fused": True, "layout": "blocked",
                 "kernel": "paged_decode_kernel<128,16,6,2,single,fused>"},
     # profiles/varlen_spec.md: one paged_varlen_kernel launch (mma.sync),
-    # read 174,706,176 B + write 3,722,240 B
-    "spec": {"kernel_hash": "b9835bf21d7ab40f", "bytes_per_launch": 178428416, "num_splits": 1,
+    # read 174,704,896 B + write 2,997,760 B
+    "spec": {"kernel_hash": "a7a592997aa82f34", "bytes_per_launch": 177702656, "num_splits": 1,
              "kernel": "paged_varlen_kernel<128,16,6,2,NT=2,blocked,single>"},
     # profiles/varlen_spec.md: one paged_varlen_tc_kernel launch (tcgen05),
-    # read 174,750,720 B + write 3,690,496 B
-    "spec_tc": {"kernel_hash": "668072eb485127d9", "sources": "tc", "bytes_per_launch": 178441216,
+    # read 174,740,224 B + write 2,975,744 B
+    "spec_tc": {"kernel_hash": "2f0b295c5122c251", "sources": "tc", "bytes_per_launch": 177715968,
                 "num_splits": 1, "kernel": "paged_varlen_tc_kernel<128,16,single>"},
     # profiles/varlen_spec_long.md: the varlen split-K phase 1 (10 splits,
-    # read 1,342,483,000 B + write 3,526,912 B) + the combine (read 2,674,000 B)
-    "spec_long": {"kernel_hash": "b9835bf21d7ab40f", "bytes_per_launch": 1348683912,
+    # read 1,342,545,408 B + write 3,588,352 B) + the combine (read 2,673,920 B)
+    "spec_long": {"kernel_hash": "a7a592997aa82f34", "bytes_per_launch": 1348807680,
                   "num_splits": 10,
                   "kernel": "paged_varlen_kernel<128,16,6,2,NT=2,blocked,split> + "
                             "varlen_combine_kernel<128>"},
-    # profiles/varlen_spec_long.md: tcgen05 phase 1 (read 1,342,567,000 B +
-    # write 3,853,056 B) + the combine (read 2,675,000 B)
-    "spec_long_tc": {"kernel_hash": "668072eb485127d9", "sources": "tc",
-                     "bytes_per_launch": 1349095056, "num_splits": 10,
+    # profiles/varlen_spec_long.md: tcgen05 phase 1 (read 1,342,633,216 B +
+    # write 3,641,344 B) + the combine (read 2,675,456 B)
+    "spec_long_tc": {"kernel_hash": "2f0b295c5122c251", "sources": "tc",
+                     "bytes_per_launch": 1348950016, "num_splits": 10,
                      "kernel": "paged_varlen_tc_kernel<128,16,split> + varlen_combine_kernel<128>"},
+    # profiles/prefill.md: one paged_prefill_tc_kernel launch, dram read
+    # 61,776,640 B + write 2,307,072 B
+    "prefill": {"kernel_hash": "8c9b1fe2e374c9aa", "sources": "prefill", "bytes_per_launch": 64083712,
+                "num_splits": 1, "kernel": "paged_prefill_tc_kernel<16>"},
     # profiles/qkv_prefill.md: one qkv_norm_rope_kernel launch, dram read
-    # 101,985,792 B + write 53,701,888 B (the rest of the writes stay in L2)
-    "qkv_prefill": {"kernel_hash": "b9835bf21d7ab40f", "bytes_per_launch": 155687680,
+    # 102,018,816 B + write 53,312,000 B (the rest of the writes stay in L2)
+    "qkv_prefill": {"kernel_hash": "a7a592997aa82f34", "bytes_per_launch": 155330816,
                     "kernel": "qkv_norm_rope_kernel<128,16,3>"},
     # profiles/decode_llama8b.md (one-launch QKV step): the decode kernel with
-    # the QKV norm + rotary + append folded in, dram read 175,240,192 B +
-    # write 3,737,088 B
-    "step_qkv": {"kernel_hash": "b9835bf21d7ab40f", "bytes_per_launch": 178977280,
+    # the QKV norm + rotary + append folded in, dram read 175,249,152 B +
+    # write 3,072,000 B
+    "step_qkv": {"kernel_hash": "a7a592997aa82f34", "bytes_per_launch": 178321152,
                  "num_splits": 1, "kernel": "paged_decode_kernel<128,16,6,2,single,qkv>"},
 }
 
 
 def traffic_current(tr):
     """Whether a traffic entry's kernel sources still hash as captured."""
-    files = TC_SOURCES if tr.get("sources") == "tc" else BASE_SOURCES
+    files = {"tc": TC_SOURCES, "prefill": PREFILL_SOURCES}.get(tr.get("sources"), BASE_SOURCES)
     return tr.get("kernel_hash") == kernel_source_hash(files)
 
 
@@ -154,8 +160,9 @@ def ncu_traffic(workload, num_splits=None):
     return tr["bytes_per_launch"]
 
 
-# The CUDA sources a kernel is built from: every kernel but the tcgen05 varlen
-# one (which adds varlen_tc.cuh) comes from these three.
+# The CUDA sources a kernel is built from: every kernel but the tcgen05 ones
+# (the varlen kernel adds varlen_tc.cuh, the prefill kernel prefill_tc.cuh as
+# well) comes from these three.
 BASE_SOURCES = ("kernels.cuh", "ptx.cuh", "pagedkv.cu")
 TC_SOURCES = BASE_SOURCES + ("varlen_tc.cuh",)
 PREFILL_SOURCES = BASE_SOURCES + ("varlen_tc.cuh", "prefill_tc.cuh")
@@ -847,7 +854,7 @@ def _measure_varlen(args, workload, tensor_path, pk, W, world, rank, local, dev)
     G = w.group
     prefill = S == 1 and v.max_q_len * G >= 128 and w.head_dim == 128
     nt = 2 if v.max_q_len * G > 8 else 1
-    per_cta = max(1, 128 // G) if prefill else max(1, 8 * nt // G)
+    per_cta = 2 * (128 // G) if prefill else max(1, 8 * nt // G)  # prefill: two 128-row tiles
     reads = -(-int(v.max_q_len) // per_cta)
     peak, peak_kind = measured_peaks()
     achieved = kv_bytes / (ms * 1e-3) / 1e9
@@ -892,7 +899,7 @@ def _measure_varlen(args, workload, tensor_path, pk, W, world, rank, local, dev)
             "frac": tflops / tpeak, "peak_source": tkind,
             "kernel": "paged_prefill_tc_kernel (algorithmic flops: the causal triangle, "
                       "4 * head_dim per (query, head, position))",
-            "kv_gbs_contexts_once": achieved, "traffic": None}
+            "kv_gbs_contexts_once": achieved, "traffic": traffic}
     return line
 
 
@@ -1170,7 +1177,10 @@ def sub_record(line, name):
             "append_us_per_step": line.get("append_us_per_step"),
             "kv_gbs": kv / (dec_us * 1e-6) / 1e9,
             "frac": line["roofline"]["frac"], "frac_kernel": line["roofline"]["kernel"],
-            "frac_of_decode_call": kv / (dec_us * 1e-6) / 1e9 / peak,
+            "bound": line["roofline"]["bound"], "achieved": line["roofline"]["achieved"],
+            "achieved_unit": line["roofline"]["unit"],
+            "frac_of_decode_call": (kv / (dec_us * 1e-6) / 1e9 / peak
+                                    if line["roofline"]["bound"] == "hbm" else None),
             "decode_tokens_per_s": line.get("decode_tokens_per_s"),
             "query_tokens_per_s": line.get("query_tokens_per_s"),
             "kernel_path": line["config"].get("kernel_path"),
@@ -1202,7 +1212,8 @@ def c_driver_record(steps=200, warmup=20):
 # Llama-3-8B step reads 174 MB, near L2's 129 MB, so its pools rotate; the
 # others read 0.8-1.3 GB per call, far above L2.
 SUB_CONFIGS = [("llama8b", N_SETS, True), ("ragged", 1, False), ("loop", None, False),
-               ("tiny", N_SETS, False), ("spec", N_SETS, False), ("spec_tc", N_SETS, False)]
+               ("tiny", N_SETS, False), ("spec", N_SETS, False), ("spec_tc", N_SETS, False),
+               ("prefill", N_SETS, False)]
 
 
 def run_ours(args):
@@ -1229,6 +1240,8 @@ def run_ours(args):
                 r = measure_loop(args, local, world, rank)
             elif sub in ("spec", "spec_tc"):
                 r = measure_varlen(args, "spec", sub == "spec_tc")
+            elif sub == "prefill":
+                r = measure_varlen(args, "prefill", False)
             else:
                 r = measure_step(args, sub, dev, None, world, rank, sets,
                                  want_e2e=e2e and not args.no_e2e, want_cpu=False)

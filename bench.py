@@ -66,6 +66,9 @@ WORKLOAD_DESC = {
              "per sequence over a prefix ~U[508,2044] (pkv_varlen_attention_splitk, causal)"),
     "prefill": ("chunked prefill: B=4, H=32, Hkv=8, D=128, bs=16, 512 new tokens per sequence "
                 "after a 2048-token prefix, causal (pkv_varlen_attention_splitk; tensor-bound)"),
+    "prefill_one": ("chunked prefill of one sequence: B=1, H=32, Hkv=8, D=128, bs=16, 512 new "
+                    "tokens after a 2048-token prefix, causal (pkv_varlen_attention_splitk; "
+                    "tensor-bound)"),
     "spec_long": ("speculative-decode verification over long contexts: B=4, H=32, Hkv=8, D=128, "
                   "bs=16, 4 draft tokens per sequence after prefixes {32768,65536,98304,131072}-4, "
                   "24576-block pool (pkv_varlen_attention_splitk, causal)"),
@@ -806,8 +809,8 @@ def _measure_varlen(args, workload, tensor_path, pk, W, world, rank, local, dev)
     import numpy as np
     import torch
 
-    v = {"spec_long": W.spec_verify_long, "prefill": W.prefill_chunk}.get(
-        workload, W.spec_verify)()
+    v = {"spec_long": W.spec_verify_long, "prefill": W.prefill_chunk,
+         "prefill_one": W.prefill_one}.get(workload, W.spec_verify)()
     w = v.base
     n_sets = args.sets or N_SETS
     sets = build_sets(w, dev, n_sets)
@@ -852,7 +855,7 @@ def _measure_varlen(args, workload, tensor_path, pk, W, world, rank, local, dev)
         return None
     kv_bytes = w.kv_bytes
     G = w.group
-    prefill = S == 1 and v.max_q_len * G >= 128 and w.head_dim == 128
+    prefill = v.max_q_len * G >= 128 and w.head_dim == 128  # the prefill kernel, any S
     nt = 2 if v.max_q_len * G > 8 else 1
     per_cta = 2 * (128 // G) if prefill else max(1, 8 * nt // G)  # prefill: two 128-row tiles
     reads = -(-int(v.max_q_len) // per_cta)
@@ -897,8 +900,10 @@ def _measure_varlen(args, workload, tensor_path, pk, W, world, rank, local, dev)
         line["roofline"] = {
             "bound": "tensor", "achieved": tflops, "peak": tpeak, "unit": "TFLOP/s",
             "frac": tflops / tpeak, "peak_source": tkind,
-            "kernel": "paged_prefill_tc_kernel (algorithmic flops: the causal triangle, "
-                      "4 * head_dim per (query, head, position))",
+            "kernel": ("paged_prefill_tc_kernel" + (" split-K phase 1 + varlen_combine_kernel"
+                                                     if S > 1 else "")
+                       + " (algorithmic flops: the causal triangle, 4 * head_dim per "
+                         "(query, head, position))"),
             "kv_gbs_contexts_once": achieved, "traffic": traffic}
     return line
 
@@ -1272,11 +1277,11 @@ def run_profile(args):
     torch.cuda.set_device(dev)
     n = args.ncu_calls
     pk.pkv_set_varlen_tensor_path(1 if args.varlen_tc else 0)
-    if args.workload in ("spec", "spec_long", "prefill"):
+    if args.workload in ("spec", "spec_long", "prefill", "prefill_one"):
         import dataclasses
 
-        v = {"spec_long": W.spec_verify_long, "prefill": W.prefill_chunk}.get(
-            args.workload, W.spec_verify)()
+        v = {"spec_long": W.spec_verify_long, "prefill": W.prefill_chunk,
+             "prefill_one": W.prefill_one}.get(args.workload, W.spec_verify)()
         v = dataclasses.replace(v, base=W.compact_pool(v.base))
         d = W.to_device(v.base, dev)
         q = torch.from_numpy(v.q).to(dev)
@@ -1371,7 +1376,7 @@ def main():
     if args.impl == "ours" and args.workload == "qkv_prefill":
         run_qkv(args)
         return
-    if args.impl == "ours" and args.workload in ("spec", "spec_long", "prefill"):
+    if args.impl == "ours" and args.workload in ("spec", "spec_long", "prefill", "prefill_one"):
         run_varlen(args)
         return
     if args.impl == "reference":

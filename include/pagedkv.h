@@ -222,10 +222,10 @@ pkv_status pkv_append_decode(const void* k_new, const void* v_new, const int32_t
  * one CTA covers max(1, 8 / group) queries of one sequence and KV head and
  * reads the context once per chunk of queries.  When max_q_len x group >=
  * 128 at head_dim 128 on blocked pools (chunked prefill), the call runs the
- * prefill kernel instead: one CTA per 128 / group queries of a sequence and
- * KV head, both products on the 5th-generation tensor cores (tcgen05.mma,
- * 128 (query, head) rows x 128-token spans, scores and output in tensor
- * memory), one CTA per SM.  The two compute the same attention within the
+ * prefill kernel instead: one CTA per pair of tiles of 128 / group queries
+ * of a sequence and KV head, both products on the 5th-generation tensor
+ * cores (tcgen05.mma, 128 (query, head) rows per tile x 128-token spans,
+ * scores and output in tensor memory), one CTA per SM.  The two compute the same attention within the
  * stated tolerance; arguments, flags and errors are the same.
  */
 pkv_status pkv_varlen_attention(const void* q, const void* k_cache, const void* v_cache,
@@ -309,12 +309,18 @@ pkv_status pkv_varlen_attention_vllm_layout(
  *                 query chunks) is under one wave of resident CTAs, the
  *                 split count that brings it nearest one wave, capped so a
  *                 split keeps >= 256 tokens of max_blocks_per_seq *
- *                 block_size, at most 64; else 1.  1 = no split (no scratch
- *                 needed); 2..PKV_MAX_SPLITS = that many splits (at most
+ *                 block_size, at most 64; else 1.  Chunked-prefill sizes
+ *                 (max_q_len x group >= 128 at head_dim 128, either layout)
+ *                 count instead the prefill kernel's pairs of 128 / group
+ *                 query tiles against one CTA per SM, each split keeping
+ *                 >= 512 tokens.  1 = no split (no scratch needed);
+ *                 2..PKV_MAX_SPLITS = that many splits (at most
  *                 max_blocks_per_seq).  As in pkv_decode_splitk the chunks
  *                 are cut on the GPU: c = ceil(n / S) blocks, n the most
  *                 blocks any chunk of queries reads (with num_splits = 0, at
- *                 least 256 tokens' worth).
+ *                 least 256 tokens' worth, 512 for chunked prefill).  On
+ *                 blocked pools a chunked-prefill call runs the prefill
+ *                 kernel for every split (see pkv_varlen_attention).
  *   scratch       device memory of at least the bytes pkv_varlen_splitk_plan
  *                 returns (pkv_splitk_scratch_bytes(total_q, num_heads,
  *                 head_dim, S) for the split count launched), 16-byte
@@ -336,7 +342,9 @@ pkv_status pkv_varlen_attention_splitk(
 /*
  * pkv_varlen_pick_num_splits — the split count pkv_varlen_attention_splitk
  * uses for num_splits = 0 (host arithmetic only; num_sms is the GPU's SM
- * count).  Returns 1 for invalid arguments.
+ * count) at sizes other than chunked prefill at head_dim 128, whose rule
+ * (pkv_varlen_attention_splitk) pkv_varlen_splitk_plan applies.  Returns 1
+ * for invalid arguments.
  */
 int32_t pkv_varlen_pick_num_splits(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
                                    int32_t max_q_len, int32_t max_blocks_per_seq,
@@ -523,8 +531,9 @@ pkv_status pkv_decode_splitk_plan(int32_t num_seqs, int32_t num_heads, int32_t n
  * pkv_varlen_splitk_plan — the same for pkv_varlen_attention_splitk (and its
  * vLLM-layout twin): *splits is 1 or the split count launched, and
  * *scratch_bytes the scratch needed (0 when unsplit or when the call has no
- * queries).  num_splits 0..PKV_MAX_SPLITS (0 = pkv_varlen_pick_num_splits on
- * the current GPU).
+ * queries).  num_splits 0..PKV_MAX_SPLITS (0 = the pick of
+ * pkv_varlen_attention_splitk on the current GPU: pkv_varlen_pick_num_splits,
+ * or the chunked-prefill rule for those sizes).
  */
 pkv_status pkv_varlen_splitk_plan(int32_t num_seqs, int32_t total_q, int32_t max_q_len,
                                   int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,

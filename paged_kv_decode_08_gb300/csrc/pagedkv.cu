@@ -59,6 +59,9 @@ constexpr int kSaturatedChunkTokens = 2048;
 // Below this a split's fixed costs outweigh its work.
 constexpr int kMinSplitTokens = 256;
 constexpr int kMaxAutoSplits = 64;
+// The heuristic's smallest split of a chunked-prefill call (four 128-token
+// spans: below that a split's fixed cost outweighs what it spreads).
+constexpr int kMinPrefillSplitTokens = 512;
 
 thread_local char t_last_error[512] = "";
 
@@ -454,11 +457,11 @@ pkv_status launch_varlen_tc(const DecodeArgs& a, const VarlenParams& vp, cudaStr
 
 std::atomic<int> g_varlen_tc{PKV_VARLEN_TC};
 
-template <int BS>
+template <int BS, bool SPLIT>
 pkv_status launch_prefill_tc(const DecodeArgs& a, const VarlenParams& vp, cudaStream_t stream,
                              int grid) {
   using Sh = TcPrefillShape;
-  auto kernel = paged_prefill_tc_kernel<BS>;
+  auto kernel = paged_prefill_tc_kernel<BS, SPLIT>;
   static std::atomic<unsigned long long> attr_set{0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -745,18 +748,45 @@ pkv_status resolve_decode_splits(int num_seqs, int num_kv_heads, int max_blocks_
   return PKV_OK;
 }
 
-// The same for varlen split-K (0 = pkv_varlen_pick_num_splits).
+// Whether a varlen call of these sizes is chunked prefill (the tcgen05
+// prefill kernel on blocked pools; the split count below for either layout,
+// so that the plan does not depend on the layout).
+bool prefill_shaped(int num_heads, int num_kv_heads, int max_q_len, int head_dim) {
+  return PKV_PREFILL_TC && head_dim == TcPrefillShape::D && num_kv_heads > 0 &&
+         (long long)max_q_len * (num_heads / num_kv_heads) >= TcPrefillShape::kRows;
+}
+
+// Split count of a chunked-prefill call: below one wave of one CTA per SM,
+// the count that brings the grid of tile pairs nearest one wave, each split
+// keeping at least kMinPrefillSplitTokens of the table's capacity.
+int prefill_pick_num_splits(int num_seqs, int num_heads, int num_kv_heads, int max_q_len,
+                            int max_blocks_per_seq, int block_size, int num_sms) {
+  const int G = num_heads / num_kv_heads;
+  const int qc = TcPrefillShape::kTiles * (TcPrefillShape::kRows / G);
+  const long long pairs = (long long)num_seqs * num_kv_heads * ((max_q_len + qc - 1) / qc);
+  long long s = pairs >= num_sms ? 1 : (2LL * num_sms + pairs) / (2 * pairs);
+  const long long cap_tokens = (long long)max_blocks_per_seq * block_size;
+  if (s > cap_tokens / kMinPrefillSplitTokens) s = cap_tokens / kMinPrefillSplitTokens;
+  if (s > kMaxAutoSplits) s = kMaxAutoSplits;
+  return s < 1 ? 1 : (int)s;
+}
+
+// The same for varlen split-K (0 = pkv_varlen_pick_num_splits, or the
+// prefill rule above for chunked-prefill sizes).
 pkv_status resolve_varlen_splits(int num_seqs, int num_heads, int num_kv_heads, int max_q_len,
-                                 int max_blocks_per_seq, int block_size, int num_splits,
-                                 int* S_out) {
+                                 int max_blocks_per_seq, int block_size, int head_dim,
+                                 int num_splits, int* S_out) {
   if (num_splits < 0 || num_splits > PKV_MAX_SPLITS)
     return fail(PKV_ERR_INVALID_ARG, "num_splits %d outside 0..%d", num_splits, PKV_MAX_SPLITS);
   int S = num_splits;
   if (S == 0) {
     int sms = 0;
     if (current_device_sms(&sms) != 0) return fail(PKV_ERR_CUDA, "cannot query the SM count");
-    S = pkv_varlen_pick_num_splits(num_seqs, num_heads, num_kv_heads, max_q_len,
-                                   max_blocks_per_seq, block_size, sms);
+    S = prefill_shaped(num_heads, num_kv_heads, max_q_len, head_dim)
+            ? prefill_pick_num_splits(num_seqs, num_heads, num_kv_heads, max_q_len,
+                                      max_blocks_per_seq, block_size, sms)
+            : pkv_varlen_pick_num_splits(num_seqs, num_heads, num_kv_heads, max_q_len,
+                                         max_blocks_per_seq, block_size, sms);
   }
   *S_out = S < 1 ? 1 : (S > max_blocks_per_seq ? max_blocks_per_seq : S);
   return PKV_OK;
@@ -870,37 +900,48 @@ pkv_status varlen_impl(const void* q, const void* k_cache, const void* v_cache,
 
   int S_eff = 1;
   st = resolve_varlen_splits(num_seqs, num_heads, num_kv_heads, max_q_len, max_blocks_per_seq,
-                             block_size, num_splits, &S_eff);
+                             block_size, head_dim, num_splits, &S_eff);
   if (st != PKV_OK) return st;
-  if (S_eff <= 1 && PKV_PREFILL_TC && !vllm && head_dim == 128 &&
-      (long long)max_q_len * G >= TcPrefillShape::kRows) {
-    // pairs of tiles of 128 / G queries: 2 x 128 (query, head) rows per CTA
+  // chunked prefill on blocked pools: pairs of tiles of 128 / G queries,
+  // 2 x 128 (query, head) rows per CTA, on the tcgen05 prefill kernel
+  const bool prefill = !vllm && prefill_shaped(num_heads, num_kv_heads, max_q_len, head_dim);
+  long long base_grid = grid;
+  if (prefill) {
     vp.qc = TcPrefillShape::kTiles * (TcPrefillShape::kRows / G);
     vp.num_chunks = (max_q_len + vp.qc - 1) / vp.qc;
-    const long long pgrid = (long long)num_seqs * num_kv_heads * vp.num_chunks;
-    if (pgrid >= (1ll << 31)) return fail(PKV_ERR_INVALID_ARG, "grid too large");
-    return block_size == 16 ? launch_prefill_tc<16>(a, vp, cs, (int)pgrid)
-                            : launch_prefill_tc<32>(a, vp, cs, (int)pgrid);
+    base_grid = (long long)num_seqs * num_kv_heads * vp.num_chunks;
   }
-  if (S_eff <= 1) return dispatch_varlen<false>(a, vp, cs, (int)grid, NT, vllm);
+  auto launch_prefill = [&](bool split, long long g) {
+    if (split)
+      return block_size == 16 ? launch_prefill_tc<16, true>(a, vp, cs, (int)g)
+                              : launch_prefill_tc<32, true>(a, vp, cs, (int)g);
+    return block_size == 16 ? launch_prefill_tc<16, false>(a, vp, cs, (int)g)
+                            : launch_prefill_tc<32, false>(a, vp, cs, (int)g);
+  };
+  if (S_eff <= 1) {
+    if (base_grid >= (1ll << 31)) return fail(PKV_ERR_INVALID_ARG, "grid too large");
+    return prefill ? launch_prefill(false, base_grid)
+                   : dispatch_varlen<false>(a, vp, cs, (int)grid, NT, vllm);
+  }
 
   const size_t need = pkv_splitk_scratch_bytes(total_q, num_heads, head_dim, S_eff);
   if (!scratch || scratch_bytes < need)
     return fail(PKV_ERR_SCRATCH_TOO_SMALL, "varlen split-K with %d splits needs %zu scratch bytes, got %zu",
                 S_eff, need, scratch ? scratch_bytes : (size_t)0);
   if (!aligned(scratch, 16)) return fail(PKV_ERR_INVALID_ARG, "scratch must be 16-byte aligned");
-  const long long grid1 = grid * S_eff;
+  const long long grid1 = base_grid * S_eff;
   const long long grid2 = (long long)total_q * num_heads;
   if (grid1 >= (1ll << 31) || grid2 >= (1ll << 31))
     return fail(PKV_ERR_INVALID_ARG, "grid too large");
   const size_t rows = (size_t)total_q * num_heads * S_eff;
   const SplitScratch sc = carve_scratch(scratch, rows, head_dim);
   vp.num_splits = S_eff;
-  vp.min_chunk_blocks = num_splits == 0 ? (kMinSplitTokens + block_size - 1) / block_size : 1;
+  const int min_tokens = prefill ? kMinPrefillSplitTokens : kMinSplitTokens;
+  vp.min_chunk_blocks = num_splits == 0 ? (min_tokens + block_size - 1) / block_size : 1;
   vp.part_out = sc.part_out;
   vp.part_m = sc.part_m;
   vp.part_l = sc.part_l;
-  st = dispatch_varlen<true>(a, vp, cs, (int)grid1, NT, vllm);
+  st = prefill ? launch_prefill(true, grid1) : dispatch_varlen<true>(a, vp, cs, (int)grid1, NT, vllm);
   if (st != PKV_OK) return st;
 
   VarlenCombineParams cp{};
@@ -913,7 +954,7 @@ pkv_status varlen_impl(const void* q, const void* k_cache, const void* v_cache,
   cp.total_q = total_q;
   cp.num_heads = num_heads;
   cp.num_splits = S_eff;
-  cp.covered_q = chunks * qc;
+  cp.covered_q = vp.num_chunks * vp.qc;
   const cudaError_t e = launch_combine(varlen_combine_kernel<64>, varlen_combine_kernel<128>,
                                        head_dim, grid2, cs, cp);
   if (e != cudaSuccess) return cuda_fail(e, "varlen split-K combine launch");
@@ -1070,7 +1111,8 @@ pkv_status pkv_varlen_splitk_plan(int32_t num_seqs, int32_t total_q, int32_t max
   }
   int S = 1;
   const pkv_status st = resolve_varlen_splits(num_seqs, num_heads, num_kv_heads, max_q_len,
-                                              max_blocks_per_seq, block_size, num_splits, &S);
+                                              max_blocks_per_seq, block_size, head_dim,
+                                              num_splits, &S);
   if (st != PKV_OK) return st;
   *splits = S;
   *scratch_bytes = S == 1 ? 0 : pkv_splitk_scratch_bytes(total_q, num_heads, head_dim, S);

@@ -77,7 +77,7 @@ struct TcPrefillShape {
   static constexpr uint32_t kIdescPV = mma_idesc_f16(kRows, D, false, true);
 };
 
-template <int BS>
+template <int BS, bool SPLIT>
 __global__ void __launch_bounds__(TcPrefillShape::kThreads, 1)
 paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, const VarlenParams p) {
@@ -86,6 +86,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_abort;
   __shared__ uint32_t s_tmem;
+  __shared__ int s_max[Sh::kThreads / 32];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t ring = smem_addr(smem);
@@ -108,10 +109,14 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
   const int lane = threadIdx.x & 31;
 
   // the pair index is the slowest and runs backwards: the pairs with the
-  // most positions (the latest queries) start first, the short ones last
-  const int per_pair = gridDim.x / p.num_chunks;  // sequences x KV heads
-  const int qt = p.num_chunks - 1 - (int)blockIdx.x / per_pair;
-  const int item = (int)blockIdx.x % per_pair;
+  // most positions (the latest queries) start first, the short ones last;
+  // the split (split-K) is the fastest
+  const int nsplit = SPLIT ? p.num_splits : 1;
+  const int per_pair = gridDim.x / (p.num_chunks * nsplit);  // sequences x KV heads
+  const int split = SPLIT ? (int)blockIdx.x % nsplit : 0;
+  const int idx = (int)blockIdx.x / nsplit;
+  const int qt = p.num_chunks - 1 - idx / per_pair;
+  const int item = idx % per_pair;
   const int g = item % p.num_kv_heads;
   const int s = item / p.num_kv_heads;
   const int G = p.group;
@@ -142,7 +147,27 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
   const int q_begin = __ldg(p.cu_seqlens_q + s);
   const int q_end = __ldg(p.cu_seqlens_q + s + 1);
   int pos0 = __ldg(p.pos_offsets + s);
+  if (SPLIT) {
+    // the longest context of the call, in blocks: the split chunks are cut
+    // from it (as the varlen split kernels cut theirs)
+    int mx = 0;
+    for (int i = threadIdx.x; i < p.num_seqs; i += Sh::kThreads) {
+      int last = __ldg(p.pos_offsets + i) + __ldg(p.cu_seqlens_q + i + 1) -
+                 __ldg(p.cu_seqlens_q + i);
+      last = last < 0 ? 0 : (last > cap ? cap : last);
+      mx = max(mx, (last + BS - 1) / BS);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) s_max[warp] = mx;
+  }
   if (__syncthreads_or(status & kDevWaitTimeout)) return;
+  int nblk_max = 0;
+  if (SPLIT) {
+#pragma unroll
+    for (int w = 0; w < Sh::kThreads / 32; ++w) nblk_max = max(nblk_max, s_max[w]);
+  }
+  const int chunk = SPLIT ? max(p.min_chunk_blocks, (nblk_max + nsplit - 1) / nsplit) : 0;
   if (q_begin < 0 || q_end < q_begin || q_end > p.total_q) {
     if (threadIdx.x == 0) atomicOr(&g_device_status, kDevBadContextLen);
     return;
@@ -157,8 +182,26 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
     if (threadIdx.x == 0) atomicOr(&g_device_status, kDevBadContextLen);
     pos0 = pos0 < 0 ? 0 : max(0, cap - q_len);
   }
-  const int tok_end = min(cap, pos0 + t0 + nq);  // >= 1: the pair's last query's limit
-  const int n_tiles = (tok_end + 15) / 16;
+  // >= 1: the pair's last query's limit
+  const int chunk_end = min(cap, pos0 + t0 + nq);
+  // this CTA's positions: [tok_begin, tok_end) (all of them in one pass)
+  int tok_begin = 0, tok_end = chunk_end;
+  if (SPLIT) {
+    if ((long long)split * chunk * BS >= chunk_end) {
+      // the split holds none of the pair's positions: maximum -inf and sum 0
+      // for its rows (the combine gives them weight 0)
+      for (int n = threadIdx.x; n < nq * G; n += Sh::kThreads) {
+        const size_t row = (size_t)(q_begin + t0 + n / G) * p.num_heads + (size_t)g * G + n % G;
+        p.part_m[row * nsplit + split] = -CUDART_INF_F;
+        p.part_l[row * nsplit + split] = 0.f;
+      }
+      return;
+    }
+    tok_begin = split * chunk * BS;
+    tok_end = (int)min((long long)chunk_end, (long long)tok_begin + (long long)chunk * BS);
+  }
+  const int sub_begin = tok_begin / 16;  // 16-row sub-tile of the first position
+  const int n_tiles = (tok_end - tok_begin + 15) / 16;
   const int n_spans = (n_tiles + Sh::kSubs - 1) / Sh::kSubs;  // >= 1
   // tile B holds queries only when the pair has more than Q_T of them
   const int ntile = nq > QT ? 2 : 1;
@@ -192,7 +235,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
   // whether any table entry the pair reads is out of range (the copies skip
   // such sub-tiles; the softmax then masks them span by span)
   bool bad_entry = false;
-  for (int t = threadIdx.x; t * SUB < n_tiles; t += Sh::kThreads) {
+  for (int t = sub_begin / SUB + threadIdx.x; t * SUB < sub_begin + n_tiles; t += Sh::kThreads) {
     const int e = __ldg(table + t);
     bad_entry = bad_entry || e < 0 || e >= p.num_blocks;
   }
@@ -229,7 +272,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
     // this lane's table entry for span i (-1: no data)
     auto lookup = [&](int i) {
       const int t = i * Sh::kSubs + u;
-      return (boxer && t < n_tiles) ? __ldg(table + t / SUB) : -1;
+      return (boxer && t < n_tiles) ? __ldg(table + (sub_begin + t) / SUB) : -1;
     };
     int issued = 0;
     // the entry of the span being loaded, the next span's (a span ahead), and
@@ -275,7 +318,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
       if (lane == 0) mbar_arrive_expect_tx(full(slot), (uint32_t)(__popc(ok) * 2048));
       __syncwarp();
       if (boxer && e >= 0) {
-        const int t = i * Sh::kSubs + u;
+        const int t = sub_begin + i * Sh::kSubs + u;
         tma_load_4d(dst + hh * Sh::kHalfBytes + u * 2048, is_v ? &vmap : &kmap, full(slot), 0,
                     (t % SUB) * 16, hh, e * p.num_kv_heads + g);
       }
@@ -394,7 +437,10 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
     const int nrows = max(0, min(QT, nq - X * QT)) * G;
     const bool live = r < nrows;
     const int qx0 = t0 + X * QT;  // the tile's first query
-    const int lim = live ? pos0 + qx0 + r / G + 1 : 0;  // positions below it count
+    // positions below it count: the row's causal limit, clipped to this
+    // CTA's range (a split's last span may run past it into the next split,
+    // whose positions were not loaded)
+    const int lim = live ? min(pos0 + qx0 + r / G + 1, tok_end) : 0;
     // positions below this count for every row of the tile (its first query's limit)
     const int all_see = min(tok_end, pos0 + qx0 + 1);
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
@@ -414,7 +460,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
 #pragma unroll
       for (int u = 0; u < Sh::kSubs; ++u) {
         const int t = i * Sh::kSubs + u;
-        const int e = t < n_tiles ? __ldg(table + t / SUB) : -1;
+        const int e = t < n_tiles ? __ldg(table + (sub_begin + t) / SUB) : -1;
         if (e >= 0 && e < p.num_blocks) bits |= 1u << u;
       }
       return bits;
@@ -441,7 +487,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
       dead = dead || aborted();
       if (!dead && !wait(s_ready(X), i & 1)) dead = true;
       dead = __any_sync(0xffffffffu, dead);  // warp-uniform before the .sync.aligned loads
-      const int span0 = i * Sh::kSpan;
+      const int span0 = tok_begin + i * Sh::kSpan;  // the span's first position
       // every position of the span counts for every row of the tile: no masks
       const bool simple = okb == kAllOk && span0 + Sh::kSpan <= all_see;
       // The scores are taken in two chunks of 64 tokens.  Each chunk's
@@ -598,12 +644,23 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
       const size_t orow = (size_t)(q_begin + qx0 + (live ? r / G : 0)) * p.num_heads +
                           (size_t)g * G + (live ? r % G : 0);
-      uint4* dst = reinterpret_cast<uint4*>(p.out + orow * Sh::D);
+      // split-K: the unnormalised row of O, the reference maximum and the
+      // sum, for the combine; else the row of O over its sum (f16)
+      const size_t slot = orow * nsplit + split;
 #pragma unroll 1
       for (int hf = 0; hf < 2; ++hf) {
         uint32_t o[64];
+        __syncwarp();  // converged for the .sync.aligned load
         tmem_ld64(tO(X) + hf * 64 + lane_base, o);
-        if (write && live) {
+        if (!(write && live)) {
+        } else if (SPLIT) {
+          float4* po = reinterpret_cast<float4*>(p.part_out + slot * Sh::D) + hf * 16;
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            po[c] = make_float4(__uint_as_float(o[4 * c]), __uint_as_float(o[4 * c + 1]),
+                                __uint_as_float(o[4 * c + 2]), __uint_as_float(o[4 * c + 3]));
+        } else {
+          uint4* dst = reinterpret_cast<uint4*>(p.out + orow * Sh::D) + hf * 8;
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             uint32_t w[4];
@@ -613,9 +670,13 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                                                    __uint_as_float(o[c * 8 + 2 * e + 1]) * inv);
               w[e] = *reinterpret_cast<const uint32_t*>(&h2);
             }
-            dst[hf * 8 + c] = make_uint4(w[0], w[1], w[2], w[3]);
+            dst[c] = make_uint4(w[0], w[1], w[2], w[3]);
           }
         }
+      }
+      if (SPLIT && write && live) {
+        p.part_m[slot] = m_run;
+        p.part_l[slot] = l_run;
       }
     }
   }

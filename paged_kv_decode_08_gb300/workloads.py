@@ -548,6 +548,13 @@ def prefill_chunk() -> VarlenWorkload:
     return varlen_random(BASE_SEED + 7, 32, 8, 128, 16, [512] * 4, [2048] * 4)
 
 
+def prefill_one() -> VarlenWorkload:
+    """Chunked prefill of one sequence (the common serving case): 512 new
+    tokens after a 2048-token prefix on the Llama-3-8B attention shape; its
+    pairs of query tiles fill under half of the GPU without split-K."""
+    return varlen_random(BASE_SEED + 8, 32, 8, 128, 16, [512], [2048])
+
+
 def spec_verify() -> VarlenWorkload:
     """Speculative-decode verification on the Llama-3-8B attention shape:
     B=32, H=32, Hkv=8, D=128, bs=16, 4 draft tokens per sequence over a

@@ -616,15 +616,18 @@ def test_prefill_matches_oracle(pk, cuda_device, H, Hkv, bs, q_lens, prefix):
     ref = oracle.varlen(v.q, kc, vc, v.cu_seqlens_q, v.pos_offsets, v.base.block_tables,
                         v.base.scale)
     d = varlen_device(v, cuda_device)
-    for label, call in (("single", lambda: pk.pkv_varlen_attention(
-            d["q"], d["k_cache"], d["v_cache"], d["cu"], d["pos"], d["block_tables"],
-            v.base.scale, max_q_len=v.max_q_len)),
-                        ("splitk heuristic", lambda: pk.pkv_varlen_attention_splitk(
-            d["q"], d["k_cache"], d["v_cache"], d["cu"], d["pos"], d["block_tables"],
-            v.base.scale, max_q_len=v.max_q_len, num_splits=0))):
-        out = call()
+    out = pk.pkv_varlen_attention(d["q"], d["k_cache"], d["v_cache"], d["cu"], d["pos"],
+                                  d["block_tables"], v.base.scale, max_q_len=v.max_q_len)
+    torch.cuda.synchronize()
+    assert_attention_close(to_np(out), ref, f"prefill single H{H} Hkv{Hkv} bs{bs}")
+    # split-K on the prefill kernel: the heuristic and forced counts (many
+    # splits empty for the short contexts, one split for some pairs)
+    for S in (0, 2, 5):
+        out = pk.pkv_varlen_attention_splitk(d["q"], d["k_cache"], d["v_cache"], d["cu"], d["pos"],
+                                             d["block_tables"], v.base.scale,
+                                             max_q_len=v.max_q_len, num_splits=S)
         torch.cuda.synchronize()
-        assert_attention_close(to_np(out), ref, f"prefill {label} H{H} Hkv{Hkv} bs{bs}")
+        assert_attention_close(to_np(out), ref, f"prefill splitk S={S} H{H} Hkv{Hkv} bs{bs}")
     assert pk.pkv_read_device_status() == 0
 
 
@@ -655,20 +658,23 @@ def test_prefill_bad_block_id_is_skipped_and_flagged(pk, cuda_device):
     tables = v.base.block_tables.copy()
     tables[0, 5] = v.base.num_blocks + 3  # positions 80..95 of sequence 0
     d["block_tables"] = torch.from_numpy(tables).to(cuda_device)
-    out = to_np(pk.pkv_varlen_attention(d["q"], d["k_cache"], d["v_cache"], d["cu"], d["pos"],
-                                        d["block_tables"], v.base.scale, max_q_len=64))
-    assert pk.pkv_read_device_status() & pk.PKV_DEV_BAD_BLOCK_ID
-    assert np.all(np.isfinite(out))
-    assert_attention_close(out[64:], ref[64:], "untouched sequence")
     K = v.base.seq_k[0].astype(np.float64)
     V = v.base.seq_v[0].astype(np.float64)
-    for t in (0, 17, 63):
-        keep = [j for j in range(200 + t + 1) if not 80 <= j < 96]
-        for h in range(8):
-            z = v.base.scale * K[keep, h // 4] @ v.q[t, h].astype(np.float64)
-            p = np.exp(z - z.max())
-            p /= p.sum()
-            assert_attention_close(out[t, h], p @ V[keep, h // 4], f"query {t} head {h}")
+    for S in (1, 3):  # one pass, and split-K (the entry falls in the first split)
+        out = to_np(pk.pkv_varlen_attention_splitk(d["q"], d["k_cache"], d["v_cache"], d["cu"],
+                                                   d["pos"], d["block_tables"], v.base.scale,
+                                                   max_q_len=64, num_splits=S))
+        assert pk.pkv_read_device_status() & pk.PKV_DEV_BAD_BLOCK_ID
+        assert np.all(np.isfinite(out))
+        assert_attention_close(out[64:], ref[64:], f"untouched sequence, S={S}")
+        for t in (0, 17, 63):
+            keep = [j for j in range(200 + t + 1) if not 80 <= j < 96]
+            for h in range(8):
+                z = v.base.scale * K[keep, h // 4] @ v.q[t, h].astype(np.float64)
+                p = np.exp(z - z.max())
+                p /= p.sum()
+                assert_attention_close(out[t, h], p @ V[keep, h // 4],
+                                       f"query {t} head {h}, S={S}")
 
 
 def test_varlen_flags_bad_query_ranges(pk, cuda_device):

@@ -87,60 +87,59 @@ WORKLOAD_DESC = {
 N_SETS = 4  # default number of rotating pool sets (--sets)
 BASE_QKV_SEED = 20261210
 
-# DRAM bytes (read + write) of one decode launch on this workload, from the
-# ncu capture summarised in profiles/ (the hash of the kernel's sources at
+# DRAM bytes (read + write) of one decode launch on this workload, from a
+# DRAM-only ncu pass over the workload's kernels (the hash of the kernel's sources at
 # capture time: BASE_SOURCES, TC_SOURCES for "sources": "tc", PREFILL_SOURCES
 # for "sources": "prefill").  Reported as null when those sources have
 # changed since.
 NCU_TRAFFIC = {
-    # profiles/split_k.md: the long-context decode call, split-K phase 1
-    # (10 splits, dram read 1,342,344,704 B + write 3,127,552 B) + the combine
-    # (read 449,536 B)
-    "long": {"kernel_hash": "a7a592997aa82f34", "bytes_per_launch": 1345921792, "num_splits": 10,
+    # the long-context decode call, split-K phase 1
+    # (10 splits, dram read 1,342,345,728 B + write 3,075,584 B) + the combine
+    # (read 449,280 B)
+    "long": {"kernel_hash": "4141458843a655c8", "bytes_per_launch": 1345870592, "num_splits": 10,
              "fused": False, "layout": "blocked",
              "kernel": "paged_decode_kernel<128,16,6,2,split> + splitk_combine_kernel<128>"},
-    # profiles/split_k.md: the ragged decode call, phase 1 (8 splits, read
-    # 810,103,552 B + write 6,965,760 B) + the combine (read 3,282,432 B +
-    # write 2,048 B)
-    "ragged": {"kernel_hash": "a7a592997aa82f34", "bytes_per_launch": 820353792, "num_splits": 8,
+    # the ragged decode call, phase 1 (8 splits, read
+    # 810,166,016 B + write 6,290,176 B) + the combine (read 3,282,944 B)
+    "ragged": {"kernel_hash": "4141458843a655c8", "bytes_per_launch": 819739136, "num_splits": 8,
                "fused": False, "layout": "blocked",
                "kernel": "paged_decode_kernel<128,32,6,2,split> + splitk_combine_kernel<128>"},
-    # profiles/decode_llama8b.md: the fused append + single-pass decode launch,
-    # dram read 175,224,320 B + write 3,510,528 B
-    "llama8b": {"kernel_hash": "a7a592997aa82f34", "bytes_per_launch": 178734848, "num_splits": 1,
+    # the fused append + single-pass decode launch,
+    # dram read 175,223,808 B + write 3,140,608 B
+    "llama8b": {"kernel_hash": "4141458843a655c8", "bytes_per_launch": 178364416, "num_splits": 1,
                 "fused": True, "layout": "blocked",
                 "kernel": "paged_decode_kernel<128,16,6,2,single,fused>"},
-    # profiles/varlen_spec.md: one paged_varlen_kernel launch (mma.sync),
-    # read 174,704,896 B + write 2,997,760 B
-    "spec": {"kernel_hash": "a7a592997aa82f34", "bytes_per_launch": 177702656, "num_splits": 1,
+    # one paged_varlen_kernel launch (mma.sync),
+    # read 174,704,640 B + write 3,002,112 B
+    "spec": {"kernel_hash": "4141458843a655c8", "bytes_per_launch": 177706752, "num_splits": 1,
              "kernel": "paged_varlen_kernel<128,16,6,2,NT=2,blocked,single>"},
-    # profiles/varlen_spec.md: one paged_varlen_tc_kernel launch (tcgen05),
-    # read 174,740,224 B + write 2,975,744 B
-    "spec_tc": {"kernel_hash": "2f0b295c5122c251", "sources": "tc", "bytes_per_launch": 177715968,
+    # one paged_varlen_tc_kernel launch (tcgen05),
+    # read 174,740,992 B + write 2,960,640 B
+    "spec_tc": {"kernel_hash": "8a6b497ef88a907b", "sources": "tc", "bytes_per_launch": 177701632,
                 "num_splits": 1, "kernel": "paged_varlen_tc_kernel<128,16,single>"},
-    # profiles/varlen_spec_long.md: the varlen split-K phase 1 (10 splits,
-    # read 1,342,545,408 B + write 3,588,352 B) + the combine (read 2,673,920 B)
-    "spec_long": {"kernel_hash": "a7a592997aa82f34", "bytes_per_launch": 1348807680,
+    # the varlen split-K phase 1 (10 splits,
+    # read 1,342,488,576 B + write 3,243,008 B) + the combine (read 2,674,176 B)
+    "spec_long": {"kernel_hash": "4141458843a655c8", "bytes_per_launch": 1348405760,
                   "num_splits": 10,
                   "kernel": "paged_varlen_kernel<128,16,6,2,NT=2,blocked,split> + "
                             "varlen_combine_kernel<128>"},
-    # profiles/varlen_spec_long.md: tcgen05 phase 1 (read 1,342,633,216 B +
-    # write 3,641,344 B) + the combine (read 2,675,456 B)
-    "spec_long_tc": {"kernel_hash": "2f0b295c5122c251", "sources": "tc",
-                     "bytes_per_launch": 1348950016, "num_splits": 10,
+    # tcgen05 phase 1 (read 1,342,530,816 B +
+    # write 3,159,040 B) + the combine (read 2,674,688 B)
+    "spec_long_tc": {"kernel_hash": "8a6b497ef88a907b", "sources": "tc",
+                     "bytes_per_launch": 1348364544, "num_splits": 10,
                      "kernel": "paged_varlen_tc_kernel<128,16,split> + varlen_combine_kernel<128>"},
-    # profiles/prefill.md: one paged_prefill_tc_kernel launch, dram read
-    # 61,776,640 B + write 2,307,072 B
-    "prefill": {"kernel_hash": "8c9b1fe2e374c9aa", "sources": "prefill", "bytes_per_launch": 64083712,
+    # one paged_prefill_tc_kernel launch, dram read
+    # 61,618,944 B + write 2,190,336 B
+    "prefill": {"kernel_hash": "ca23019c848f6234", "sources": "prefill", "bytes_per_launch": 63809280,
                 "num_splits": 1, "kernel": "paged_prefill_tc_kernel<16>"},
-    # profiles/qkv_prefill.md: one qkv_norm_rope_kernel launch, dram read
-    # 102,018,816 B + write 53,312,000 B (the rest of the writes stay in L2)
-    "qkv_prefill": {"kernel_hash": "a7a592997aa82f34", "bytes_per_launch": 155330816,
+    # one qkv_norm_rope_kernel launch, dram read
+    # 102,025,216 B + write 52,952,064 B (the rest of the writes stay in L2)
+    "qkv_prefill": {"kernel_hash": "4141458843a655c8", "bytes_per_launch": 154977280,
                     "kernel": "qkv_norm_rope_kernel<128,16,3>"},
-    # profiles/decode_llama8b.md (one-launch QKV step): the decode kernel with
-    # the QKV norm + rotary + append folded in, dram read 175,249,152 B +
-    # write 3,072,000 B
-    "step_qkv": {"kernel_hash": "a7a592997aa82f34", "bytes_per_launch": 178321152,
+    # one-launch QKV step: the decode kernel with
+    # the QKV norm + rotary + append folded in, dram read 175,252,736 B +
+    # write 3,195,392 B
+    "step_qkv": {"kernel_hash": "4141458843a655c8", "bytes_per_launch": 178448128,
                  "num_splits": 1, "kernel": "paged_decode_kernel<128,16,6,2,single,qkv>"},
 }
 

@@ -356,17 +356,17 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
           if (mbar_test(p_ready(X), i & 1) &&
               (X > 0 || mbar_test(full(vs), use_of(vload(i)) & 1))) {
             tc_fence_after();
-            const uint32_t vb = ring + vs * Sh::kSlotBytes;
-            const uint32_t pb = pbuf + X * Sh::kPBytes;
+            // P: K-major over the span's tokens; V: MN-major (d contiguous),
+            // its two d halves kHalfBytes apart, 8-token groups 1 KB apart.
+            // A descriptor's address field is the byte address / 16, so a
+            // step within the operand adds its offset / 16.
+            const uint64_t a0 = smem_desc_sw128(pbuf + X * Sh::kPBytes, 16, 1024);
+            const uint64_t b0 = smem_desc_sw128(ring + vs * Sh::kSlotBytes, Sh::kHalfBytes, 1024);
 #pragma unroll
-            for (int ks = 0; ks < Sh::kSpan / 16; ++ks) {
-              // P: K-major over the span's tokens; V: MN-major (d contiguous),
-              // its two d halves kHalfBytes apart, 8-token groups 1 KB apart
-              const uint64_t a =
-                  smem_desc_sw128(pb + (ks / 4) * (Sh::kRows * 128) + (ks % 4) * 32, 16, 1024);
-              const uint64_t b = smem_desc_sw128(vb + ks * 2048, Sh::kHalfBytes, 1024);
-              tc_mma_f16(tO(X), a, b, Sh::kIdescPV, (i > 0 || ks > 0) ? 1u : 0u);
-            }
+            for (int ks = 0; ks < Sh::kSpan / 16; ++ks)
+              tc_mma_f16(tO(X), a0 + (uint64_t)(((ks / 4) * (Sh::kRows * 128) + (ks % 4) * 32) >> 4),
+                         b0 + (uint64_t)((ks * 2048) >> 4), Sh::kIdescPV,
+                         (i > 0 || ks > 0) ? 1u : 0u);
             tc_commit(pv_done(X));
             last_bar = pv_done(X);
             last_phase = i & 1;
@@ -387,14 +387,13 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
               (X > 0 || mbar_test(full(ks_slot), use_of(kload(j)) & 1)) &&
               (j < 1 || mbar_test(s_free(X), (j - 1) & 1))) {
             tc_fence_after();
-            const uint32_t kb = ring + ks_slot * Sh::kSlotBytes;
-            const uint32_t qx = qbuf + X * Sh::kQBytes;
+            const uint64_t a0 = smem_desc_sw128(qbuf + X * Sh::kQBytes, 16, 1024);
+            const uint64_t b0 = smem_desc_sw128(ring + ks_slot * Sh::kSlotBytes, 16, 1024);
 #pragma unroll
             for (int ks = 0; ks < Sh::D / 16; ++ks) {
               const int h = ks / 4, w4 = ks % 4;
-              const uint64_t a = smem_desc_sw128(qx + h * (Sh::kRows * 128) + w4 * 32, 16, 1024);
-              const uint64_t b = smem_desc_sw128(kb + h * Sh::kHalfBytes + w4 * 32, 16, 1024);
-              tc_mma_f16(tS(X), a, b, Sh::kIdescS, ks > 0);
+              tc_mma_f16(tS(X), a0 + (uint64_t)((h * (Sh::kRows * 128) + w4 * 32) >> 4),
+                         b0 + (uint64_t)((h * Sh::kHalfBytes + w4 * 32) >> 4), Sh::kIdescS, ks > 0);
             }
             tc_commit(s_ready(X));
             last_bar = s_ready(X);

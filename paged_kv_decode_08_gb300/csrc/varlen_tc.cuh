@@ -360,15 +360,16 @@ paged_varlen_tc_kernel(const __grid_constant__ CUtensorMap kmap,
         const int vs = slot_of(vload(i));
         if (mbar_test(p_ready(i & 1), (i >> 1) & 1) && mbar_test(full(vs), use_of(vload(i)) & 1)) {
           tc_fence_after();
-          const uint32_t vb = ring + vs * Sh::kSlotBytes;
-          const uint32_t pb = pbuf + (i & 1) * Sh::kPBytes;
+          // V^T is MN-major: its two d halves kHalfBytes apart, 8-token
+          // groups 1 KB apart.  A descriptor's address field is the byte
+          // address / 16, so a step within the operand adds its offset / 16.
+          const uint64_t a0 = smem_desc_sw128(ring + vs * Sh::kSlotBytes, Sh::kHalfBytes, 1024);
+          const uint64_t b0 = smem_desc_sw128(pbuf + (i & 1) * Sh::kPBytes, 16, 1024);
 #pragma unroll
-          for (int ks = 0; ks < Sh::kSpan / 16; ++ks) {
-            // V^T is MN-major: its two d halves kHalfBytes apart, 8-token groups 1 KB apart
-            const uint64_t a = smem_desc_sw128(vb + ks * 2048, Sh::kHalfBytes, 1024);
-            const uint64_t b = smem_desc_sw128(pb + (ks / 4) * 2048 + (ks % 4) * 32, 16, 1024);
-            tc_mma_f16(tO, a, b, Sh::kIdescPV, (i > 0 || ks > 0) ? 1u : 0u);
-          }
+          for (int ks = 0; ks < Sh::kSpan / 16; ++ks)
+            tc_mma_f16(tO, a0 + (uint64_t)((ks * 2048) >> 4),
+                       b0 + (uint64_t)(((ks / 4) * 2048 + (ks % 4) * 32) >> 4), Sh::kIdescPV,
+                       (i > 0 || ks > 0) ? 1u : 0u);
           tc_commit(empty(vs));
           tc_commit(pv_done(i & 1));
           last_bar = pv_done(i & 1);
@@ -381,13 +382,13 @@ paged_varlen_tc_kernel(const __grid_constant__ CUtensorMap kmap,
         if (j < n_spans && j <= next_pv + 2 && mbar_test(full(ks_slot), use_of(kload(j)) & 1) &&
             (j < 2 || mbar_test(s_free(j & 1), ((j - 2) >> 1) & 1))) {
           tc_fence_after();
-          const uint32_t kb = ring + ks_slot * Sh::kSlotBytes;
+          const uint64_t a0 = smem_desc_sw128(ring + ks_slot * Sh::kSlotBytes, 16, 1024);
+          const uint64_t b0 = smem_desc_sw128(qbuf, 16, 1024);
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
             const int h = ks / 4, w4 = ks % 4;
-            const uint64_t a = smem_desc_sw128(kb + h * Sh::kHalfBytes + w4 * 32, 16, 1024);
-            const uint64_t b = smem_desc_sw128(qbuf + h * (16 * 128) + w4 * 32, 16, 1024);
-            tc_mma_f16(tS + (j & 1) * 16, a, b, Sh::kIdescS, ks > 0);
+            tc_mma_f16(tS + (j & 1) * 16, a0 + (uint64_t)((h * Sh::kHalfBytes + w4 * 32) >> 4),
+                       b0 + (uint64_t)((h * (16 * 128) + w4 * 32) >> 4), Sh::kIdescS, ks > 0);
           }
           tc_commit(empty(ks_slot));
           tc_commit(s_ready(j & 1));

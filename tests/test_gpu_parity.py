@@ -631,6 +631,37 @@ def test_prefill_matches_oracle(pk, cuda_device, H, Hkv, bs, q_lens, prefix):
     assert pk.pkv_read_device_status() == 0
 
 
+def _prefill_rule(num_seqs, H, Hkv, max_q_len, mbps, bs, sms):
+    """The chunked-prefill split rule written out: pairs of 128 / G-query
+    tiles against one CTA per SM, nearest one wave when fewer, >= 512 tokens
+    of table capacity per split, at most 64, at most max_blocks_per_seq."""
+    G = H // Hkv
+    qc = 2 * (128 // G)
+    pairs = num_seqs * Hkv * -(-max_q_len // qc)
+    s = 1 if pairs >= sms else (2 * sms + pairs) // (2 * pairs)
+    s = min(s, mbps * bs // 512, 64)
+    return max(1, min(s, mbps))
+
+
+@pytest.mark.parametrize("num_seqs,total_q,max_q_len,H,Hkv,mbps,bs", [
+    (1, 512, 512, 32, 8, 160, 16),     # one sequence: 64 pairs
+    (4, 2048, 512, 32, 8, 160, 16),    # four: 256 pairs, a full wave
+    (1, 128, 128, 8, 8, 64, 16),       # G = 1 (one 128-query tile per pair): capped by capacity
+    (1, 64, 64, 32, 8, 1000, 16),      # 8 pairs, long tables
+    (3, 300, 100, 28, 4, 40, 32),      # G = 7
+])
+def test_prefill_split_plan_follows_the_rule(pk, cuda_device, num_seqs, total_q, max_q_len, H,
+                                             Hkv, mbps, bs):
+    sms = torch.cuda.get_device_properties(cuda_device).multi_processor_count
+    S, n = pk.pkv_varlen_splitk_plan(num_seqs, total_q, max_q_len, H, Hkv, 128, mbps, bs, 0)
+    assert S == _prefill_rule(num_seqs, H, Hkv, max_q_len, mbps, bs, sms)
+    assert n == (0 if S == 1 else pk.pkv_splitk_scratch_bytes(total_q, H, 128, S))
+    # head_dim 64 is not chunked prefill: the varlen rule
+    S64, _ = pk.pkv_varlen_splitk_plan(num_seqs, total_q, max_q_len, H, Hkv, 64, mbps, bs, 0)
+    assert S64 == max(1, min(pk.pkv_varlen_pick_num_splits(num_seqs, H, Hkv, max_q_len, mbps,
+                                                           bs, sms), mbps))
+
+
 @pytest.mark.parametrize("scale_mul", [-1.0, 0.0])
 def test_prefill_nonpositive_scale(pk, cuda_device, scale_mul):
     """A negative or zero scale (the maximum of the scaled scores is then not

@@ -125,6 +125,20 @@ def test_varlen_splitk_plan(pk):
         pk.pkv_varlen_splitk_plan(4, 16, 4, 32, 8, 128, 8192, 16, -1)
 
 
+def test_varlen_splitk_plan_prefill_sizes_forced(pk):
+    """Chunked-prefill sizes (4 x 512 queries, group 4, head_dim 128) with a
+    forced split count: that count (at most max_blocks_per_seq) and its
+    scratch, with no device query; the pick for num_splits = 0 needs the GPU."""
+    assert pk.pkv_varlen_splitk_plan(4, 2048, 512, 32, 8, 128, 160, 16, 3) == (
+        3, pk.pkv_splitk_scratch_bytes(2048, 32, 128, 3))
+    assert pk.pkv_varlen_splitk_plan(4, 2048, 512, 32, 8, 128, 2, 16, 5) == (
+        2, pk.pkv_splitk_scratch_bytes(2048, 32, 128, 2))
+    assert pk.pkv_varlen_splitk_plan(4, 2048, 512, 32, 8, 128, 160, 16, 1) == (1, 0)
+    with pytest.raises(pk.PagedKVError) as e:
+        pk.pkv_varlen_splitk_plan(4, 2048, 512, 32, 8, 128, 160, 16, 0)
+    assert e.value.status == pk.PKV_ERR_CUDA
+
+
 def test_pick_num_splits_never_leaves_a_split_empty_by_length(pk):
     for L in (256, 300, 512, 777, 4096, 65536):
         for base in (1, 4, 32, 300, 2000):
